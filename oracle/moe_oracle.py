@@ -1,0 +1,285 @@
+"""Plain fp64 CPU oracle of one routed MoE layer forward (test infrastructure).
+
+Each function follows one step of the method as the source pages state it;
+page references name the article and its section:
+
+  [V4-EP]    "DeepSeek-V4 Expert Parallelism and computation/communication
+             overlap", sections 2.1 (per-expert logits), 3.2 (routing:
+             max-subtracted softmax, partial top-8 then exact softmax over
+             those 8, hard top-k), 3.3 (packing by expert id), 5.2 (expert
+             weights laid out contiguously by expert id).
+  [SYNC-TAX] "Deepseek-MoE sync tax", sections 2.1 (top-k gating, per-
+             destination packed buffers), 2.3 (weighted sum of the k expert
+             outputs per token), 3.1 (per-token FP8 payload quantisation).
+  [V3V4-PAR] "DeepSeek V3/V4 parallel strategy", EP and Waved-EP sections
+             (dispatch, expert L1 + Act + L2, combine).
+
+Readings taken where the pages leave a step open are listed with each
+function (expert FFN form, selection order, FP8 scale form, rounding points).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .numerics import round_to_bf16, round_to_f32, e4m3_round_satfinite
+
+ROUTER_RENORM = 0
+ROUTER_PREK_SOFTMAX = 1
+E4M3_MAX_F32 = np.float32(448.0)
+
+
+# ----------------------------------------------------------------------------
+# inputs
+# ----------------------------------------------------------------------------
+def _np64(t) -> np.ndarray:
+    """fp64 numpy copy of a torch tensor or array (bf16/fp32 values are exact)."""
+    if hasattr(t, "detach"):
+        t = t.detach()
+        if t.dtype.is_floating_point:
+            t = t.to(dtype=__import__("torch").float64)
+        return t.cpu().numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def inputs_to_numpy(inp: dict) -> dict:
+    """x, Wg, bias as fp64 arrays; W1/W2 stay as given and are fetched one
+    expert at a time by ``_expert`` (the largest layer's weights are 15 GB)."""
+    return {"x": _np64(inp["x"]), "Wg": _np64(inp["Wg"]), "bias": _np64(inp["bias"]),
+            "W1": inp["W1"], "W2": inp["W2"]}
+
+
+def _expert(W, e: int) -> np.ndarray:
+    return _np64(W[e])
+
+
+# ----------------------------------------------------------------------------
+# gate [V4-EP 2.1]: each expert's logit is the token's dot product with that
+# expert's gate column, plus the expert's bias.
+# ----------------------------------------------------------------------------
+def gate_logits(x: np.ndarray, Wg: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
+    L = np.asarray(x, np.float64) @ np.asarray(Wg, np.float64)
+    if bias is not None:
+        L = L + np.asarray(bias, np.float64)[None, :]
+    return L
+
+
+# ----------------------------------------------------------------------------
+# router [V4-EP 3.2]
+# ----------------------------------------------------------------------------
+def _softmax_max_subtracted(L: np.ndarray) -> np.ndarray:
+    """Softmax along the last axis after subtracting the row maximum
+    ("logits - logits.max()" to avoid overflow)."""
+    z = L - L.max(axis=-1, keepdims=True)
+    ez = np.exp(z)
+    return ez / ez.sum(axis=-1, keepdims=True)
+
+
+def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8):
+    """Top-k expert selection and gate weights.
+
+    Order: logits descending, equal logits by expert id ascending (the lower
+    id wins). The partial top-``pre_k`` is found first; the k chosen experts
+    are its first k entries, and slot j of a token holds its j-th choice.
+
+    * ROUTER_RENORM (hard top-k): p = softmax(L - max L) over all E experts;
+      the k chosen probabilities are divided by their sum.
+    * ROUTER_PREK_SOFTMAX: the exact softmax is taken over the pre_k largest
+      logits only; the k chosen entries of that softmax are the weights, not
+      renormalised (their sum is at most 1).
+
+    Returns (topk_idx int32 [T, k], topk_w fp64 [T, k]).
+    """
+    L = np.asarray(L, np.float64)
+    T, E = L.shape
+    pre_k = min(pre_k, E)
+    if not (1 <= k <= pre_k):
+        raise ValueError("need 1 <= k <= min(pre_k, E)")
+    # stable sort of -L: descending logits, ties keep ascending expert id
+    order = np.argsort(-L, axis=1, kind="stable")
+    S = order[:, :pre_k]                              # partial top-pre_k
+    sel = S[:, :k]
+    rows = np.arange(T)[:, None]
+    if router == ROUTER_RENORM:
+        p = _softmax_max_subtracted(L)
+        ps = p[rows, sel]
+        w = ps / ps.sum(axis=1, keepdims=True)
+    elif router == ROUTER_PREK_SOFTMAX:
+        q = _softmax_max_subtracted(L[rows, S])
+        w = q[:, :k]
+    else:
+        raise ValueError(f"unknown router mode {router}")
+    return sel.astype(np.int32), w
+
+
+# ----------------------------------------------------------------------------
+# dispatch [V4-EP 3.3; SYNC-TAX 2.1]: pack the (token, expert) pairs
+# contiguously by expert id with a stable counting sort.
+# ----------------------------------------------------------------------------
+def dispatch(topk_idx: np.ndarray, E: int):
+    """Returns counts [E], offsets [E+1], pos [R], src [R] (all int64).
+
+    Flat entry i = t*k + j (token t's j-th choice, expert e) goes to row
+    pos[i] = offsets[e] + (number of earlier flat entries with expert e);
+    src[pos[i]] = t.
+    """
+    idx = np.asarray(topk_idx)
+    T, k = idx.shape
+    flat = idx.reshape(-1).astype(np.int64)
+    R = flat.size
+    if R and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert index out of range")
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:                      # histogram
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):                  # exclusive scan
+        offsets[e + 1] = offsets[e] + counts[e]
+    fill = offsets[:-1].copy()
+    pos = np.empty(R, dtype=np.int64)
+    for i in range(R):                  # stable placement, flat order
+        e = flat[i]
+        pos[i] = fill[e]
+        fill[e] += 1
+    src = np.empty(R, dtype=np.int64)
+    src[pos] = np.arange(R) // k
+    return counts, offsets, pos, src
+
+
+# ----------------------------------------------------------------------------
+# FP8 payload [SYNC-TAX 3.1]: per-token scale so the token's largest magnitude
+# maps to the E4M3 maximum; symmetric (absmax) form, fp32 scale.
+# ----------------------------------------------------------------------------
+def quantize_payload_fp8(x_rows: np.ndarray):
+    """Per row t: a = max |x_t| (fp32), s = fp32(a / 448) with an fp32 IEEE
+    division (s = 1 for an all-zero row), q = E4M3(fp32(x / s)) with an fp32
+    IEEE division, rounded to nearest even and saturated to +-448.
+
+    Returns (q as fp64 E4M3 values [T, d], s as fp64 holding fp32 values [T])."""
+    x32 = np.asarray(x_rows, np.float64).astype(np.float32)
+    a = np.abs(x32).max(axis=1)
+    s = (a / E4M3_MAX_F32).astype(np.float32)
+    s = np.where(a == 0, np.float32(1.0), s).astype(np.float32)
+    ratio = (x32 / s[:, None]).astype(np.float32)     # fp32 division, RN
+    q = e4m3_round_satfinite(ratio.astype(np.float64))
+    return q, s.astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# expert FFN [V3V4-PAR Waved-EP: "L1 + Act + L2"; V4-EP 2.3: W1 by columns,
+# W2 by rows]: reading = one up projection, SiLU, one down projection, no
+# biases and no gating branch.
+# ----------------------------------------------------------------------------
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z / (1 + e^-z)."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def expert_ffn_rows(x_rows: np.ndarray, W1e: np.ndarray, W2e: np.ndarray,
+                    h_storage: str = "bf16"):
+    """y = round_storage(SiLU(x W1_e)) W2_e for the rows routed to expert e.
+
+    ``h_storage`` mirrors the dtype the hidden activation is stored in
+    between the two projections ("bf16", "f32", or "exact" for none)."""
+    z = np.asarray(x_rows, np.float64) @ np.asarray(W1e, np.float64)
+    h = silu(z)
+    if h_storage == "bf16":
+        h = round_to_bf16(h)
+    elif h_storage == "f32":
+        h = round_to_f32(h)
+    return h @ np.asarray(W2e, np.float64), h
+
+
+# ----------------------------------------------------------------------------
+# combine [SYNC-TAX 2.3]: weighted sum of a token's k expert outputs.
+# ----------------------------------------------------------------------------
+def combine(Y: np.ndarray, pos: np.ndarray, topk_w: np.ndarray) -> np.ndarray:
+    """out[t] = sum over j = 0..k-1 of w[t, j] * Y[pos[t*k + j]]."""
+    w = np.asarray(topk_w, np.float64)
+    T, k = w.shape
+    Y = np.asarray(Y, np.float64)
+    out = np.zeros((T, Y.shape[1]), dtype=np.float64)
+    for j in range(k):
+        out += w[:, j:j + 1] * Y[np.asarray(pos).reshape(T, k)[:, j]]
+    return out
+
+
+# ----------------------------------------------------------------------------
+# whole layer
+# ----------------------------------------------------------------------------
+def _storage(cfg) -> str:
+    return "bf16" if cfg.dtype == "bf16" else "f32"
+
+
+def _round_out(cfg, v):
+    return round_to_bf16(v) if cfg.dtype == "bf16" else round_to_f32(v)
+
+
+def forward(cfg, inp: dict, keep_h: bool = True) -> dict:
+    """Every intermediate of the layer for a (small) config.
+
+    ``inp`` is the dict from ``workloads.make_inputs`` (or inputs_to_numpy of
+    it). Returns a dict with L, topk_idx, topk_w, counts, offsets, pos, src,
+    x_hat (the rows the experts see: x, or the dequantised FP8 payload),
+    q / scale (FP8 only), H (optional), Y, out (fp64) and out_rounded (the
+    output dtype's rounding of out)."""
+    a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
+    x = a["x"]
+    L = gate_logits(x, a["Wg"], a["bias"])
+    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k)
+    counts, offsets, pos, src = dispatch(idx, cfg.E)
+    res = {"L": L, "topk_idx": idx, "topk_w": w, "counts": counts,
+           "offsets": offsets, "pos": pos, "src": src}
+    if cfg.payload_fp8:
+        q_tok, s_tok = quantize_payload_fp8(x)
+        res["q"] = q_tok[src]
+        res["scale"] = s_tok[src]
+        x_hat_tok = q_tok * s_tok[:, None]
+    else:
+        x_hat_tok = x
+    R = idx.size
+    Y = np.zeros((R, cfg.d), dtype=np.float64)
+    H = np.zeros((R, cfg.f), dtype=np.float64) if keep_h else None
+    for e in range(cfg.E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue                    # an expert with no tokens does no work
+        rows = x_hat_tok[src[lo:hi]]
+        y, h = expert_ffn_rows(rows, _expert(a["W1"], e), _expert(a["W2"], e),
+                               _storage(cfg))
+        Y[lo:hi] = y
+        if keep_h:
+            H[lo:hi] = h
+    out = combine(Y, pos, w)
+    res.update({"Y": Y, "out": out, "out_rounded": _round_out(cfg, out)})
+    if keep_h:
+        res["H"] = H
+    return res
+
+
+def forward_tokens(cfg, inp: dict, tokens) -> dict:
+    """Route, FFN and combine for a subset of tokens only (a token's output
+    does not depend on other tokens). Used for sampled checks on the large
+    layers. Returns L, topk_idx, topk_w, out, out_rounded for ``tokens``."""
+    a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
+    tokens = np.asarray(tokens, dtype=np.int64)
+    x = a["x"][tokens]
+    L = gate_logits(x, a["Wg"], a["bias"])
+    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k)
+    if cfg.payload_fp8:
+        q, s = quantize_payload_fp8(x)
+        x_hat = q * s[:, None]
+    else:
+        x_hat = x
+    n, k = idx.shape
+    y_slot = np.zeros((n, k, cfg.d), dtype=np.float64)
+    for e in np.unique(idx):
+        tt, jj = np.nonzero(idx == e)
+        y, _ = expert_ffn_rows(x_hat[tt], _expert(a["W1"], int(e)),
+                               _expert(a["W2"], int(e)), _storage(cfg))
+        y_slot[tt, jj] = y
+    out = np.zeros((n, cfg.d), dtype=np.float64)
+    for j in range(k):
+        out += w[:, j:j + 1] * y_slot[:, j]
+    return {"tokens": tokens, "L": L, "topk_idx": idx, "topk_w": w,
+            "out": out, "out_rounded": _round_out(cfg, out)}
