@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Throughput of one routed MoE layer forward on GB300 (routed tokens/s).
+
+A step is one moe_forward (route -> dispatch -> grouped expert FFN ->
+combine) over one batch of synthetic tokens already resident in HBM. The
+default workload is the balanced 8-expert layer (T=1024, d=4096, E=8, top-2,
+f=11008, bf16). Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Per-kernel times come from CUDA events recorded by moe_forward_with_events
+on the launching stream inside the timed steps. The per-step working set
+(expert weights, 1.44 GB for the default layer) is larger than the 129 MB L2,
+so no L2 flush is needed between steps; --flush-l2 adds one anyway.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "routed tokens/s per MoE layer fwd at 1 GB300"
+UNIT = "tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["route", "dispatch", "fp8_to_bf16", "gemm_w1_silu", "gemm_w2", "combine"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--config", default=None)
+    p.add_argument("--flush-l2", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=256)
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {k: d[k] for k in PEAKS_FALLBACK}, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ---------------------------------------------------------------- algorithmic work
+def stage_work(cfg, counts):
+    """Algorithmic bytes and flops per launch of each stage: only what the
+    method must move (weights of experts that received rows, each operand
+    read once, each result written once)."""
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    R = T * k
+    b = 4 if cfg.dtype == "f32" else 2
+    pb = 1 if cfg.payload_fp8 else b
+    active = sum(1 for c in counts if c > 0)
+    w = {}
+    w["route"] = (T * d * b + d * E * b + E * 4 + R * 8, 2.0 * T * d * E)
+    w["dispatch"] = (T * d * b + R * d * pb + R * 12 + (R * 4 if cfg.payload_fp8 else 0), 0.0)
+    w["fp8_to_bf16"] = ((R * d + R * d * 2) if cfg.payload_fp8 else 0, 0.0)
+    a_bytes = R * d * (2 if cfg.payload_fp8 else b)
+    w["gemm_w1_silu"] = (active * d * f * b + a_bytes + R * f * b, 2.0 * R * d * f)
+    w["gemm_w2"] = (active * f * d * b + R * f * b + R * d * 4, 2.0 * R * f * d)
+    w["combine"] = (R * d * 4 + R * 8 + T * d * b, 2.0 * R * d)
+    return w
+
+
+def source_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        ent = d.get(workload, {}).get(os.path.basename(kernel_file))
+        if ent and ent.get("source_sha") == source_sha(kernel_file):
+            return ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def cpu_oracle_run(cfg, host, tokens):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward_tokens(cfg, host, tokens)
+    return time.perf_counter() - t0
+
+
+def host_inputs(inp):
+    """CPU copies of the inputs (outside any timed region)."""
+    return {k: v.detach().cpu() for k, v in inp.items()}
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, cfg):
+    import numpy as np
+    from workloads import make_inputs
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = make_inputs(cfg, device="cpu")
+    host = host_inputs(inp)
+    S = min(cfg.T, 64)
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        cpu_oracle_run(cfg, host, np.sort(rng.choice(cfg.T, S, replace=False)))
+    t = 0.0
+    for _ in range(args.steps):
+        t += cpu_oracle_run(cfg, host, np.sort(rng.choice(cfg.T, S, replace=False)))
+    per_step = t / args.steps
+    value = S / per_step
+    sample = (f"{S} random tokens of the {cfg.T}-token batch per step (all {cfg.E} experts' "
+              f"weights upcast to fp64 as the oracle does), numpy fp64")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(cfg, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg, args):
+    return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "f": cfg.f,
+            "router": "prek_softmax" if cfg.router else "renorm", "pre_k": cfg.pre_k,
+            "payload": "fp8_e4m3" if cfg.payload_fp8 else cfg.dtype, "seed": cfg.seed,
+            "parallelism": f"replicas x{args.gpus}",
+            "l2": ("flushed between steps" if args.flush_l2 else
+                   "not flushed: per-step working set (expert weights) exceeds the 129 MB L2")}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, cfg):
+    import numpy as np
+    import torch
+    import mixture_experts_routed_gb300 as moe
+    from mixture_experts_routed_gb300.stats import load_stats
+    from workloads import make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    inp = make_inputs(cfg, device=dev)
+    ws = moe.alloc_workspace(cfg, device=dev)
+    out = torch.empty((cfg.T, cfg.d), dtype=cfg.torch_dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = None
+    if args.flush_l2:
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def step(events=None):
+        if flush is not None:
+            flush.fill_(1)
+        moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
+                    out=out, events=events, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if moe.get_device_error(ws) != moe.MOE_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: K steps, events at every kernel boundary
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_NUM_EVENTS)]
+           for _ in range(K)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if moe.get_device_error(ws) != moe.MOE_OK:
+        raise RuntimeError("device error in the timed steps")
+    ms_per_step = total_ms / K
+    value = cfg.T * world / (ms_per_step / 1e3)
+
+    # per-kernel averages (event i -> i+1 brackets one stage)
+    stage_ms = {}
+    for si, name in enumerate(STAGES):
+        stage_ms[name] = sum(evs[i][si].elapsed_time(evs[i][si + 1]) for i in range(K)) / K
+
+    views = moe.forward_views(cfg, ws)
+    counts = views["counts"].cpu().tolist()
+    work = stage_work(cfg, counts)
+    peaks, peak_src = load_peaks()
+    kernels = {}
+    for name in STAGES:
+        by, fl = work[name]
+        t = stage_ms[name] / 1e3
+        if by == 0 and fl == 0:
+            continue
+        gbs = by / t / 1e9 if t > 0 else 0.0
+        tfl = fl / t / 1e12 if t > 0 else 0.0
+        kernels[name] = {"us": stage_ms[name] * 1e3, "bytes": by, "flops": fl, "GB_s": gbs,
+                         "TFLOP_s": tfl, "hbm_frac": gbs / peaks["hbm_gbs"],
+                         "tensor_frac": (tfl / peaks["bf16_tflops"]) if name.startswith("gemm")
+                         else None}
+    dom = max(kernels, key=lambda n: kernels[n]["us"])
+    kd = kernels[dom]
+    by, fl = work[dom]
+    is_tensor = dom.startswith("gemm") and cfg.dtype == "bf16" and \
+        fl / (peaks["bf16_tflops"] * 1e12) > by / (peaks["hbm_gbs"] * 1e9)
+    kfile = os.path.join(ROOT, "mixture_experts_routed_gb300", "csrc",
+                         "gemm_tc.cu" if dom.startswith("gemm") else
+                         {"route": "route.cu", "dispatch": "dispatch.cu",
+                          "combine": "combine.cu", "fp8_to_bf16": "dispatch.cu"}[dom])
+    traffic = ncu_traffic(kfile, f"{cfg.name}:{dom}")
+    if is_tensor:
+        roof = {"bound": "tensor", "achieved": kd["TFLOP_s"], "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": kd["TFLOP_s"] / peaks["bf16_tflops"],
+                "traffic": traffic}
+    else:
+        roof = {"bound": "hbm", "achieved": kd["GB_s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": kd["GB_s"] / peaks["hbm_gbs"], "traffic": traffic}
+    roof["kernel"] = dom
+    roof["algorithmic_bytes"] = by
+    roof["algorithmic_flops"] = fl
+    roof["peak_source"] = peak_src
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp["x"].cpu().pin_memory()
+        out_host = torch.empty((cfg.T, cfg.d), dtype=cfg.torch_dtype).pin_memory()
+        x_dev = torch.empty_like(inp["x"])
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.forward(cfg, x_dev, inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
+                        out=out, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = a.elapsed_time(b)
+        if dist:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": cfg.T * world / (e_ms / K / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+               "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    if dist:
+        dist.barrier()
+    if rank != 0:
+        dist.destroy_process_group()
+        return 0
+
+    # ---- CPU oracle on a bounded sample (rank 0 only, N = 1 only)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        host = host_inputs(inp)
+        S = min(cfg.T, args.cpu_sample_tokens)
+        toks = np.arange(S)
+        t = cpu_oracle_run(cfg, host, toks)
+        cpu = {"value": S / t, "unit": UNIT, "cores": cores(), "kind": "oracle",
+               "sample": f"first {S} tokens of the {cfg.T}-token batch, whole layer (gate, "
+                         f"router, FFN of every chosen expert incl. its fp64 weight upcast, "
+                         f"combine) in numpy fp64; {t:.1f} s"}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": workload_config(cfg, args), "roofline": roof, "cpu_baseline": cpu,
+            "e2e": e2e, "gpu_launches": moe.kernel_count(cfg) * K, "clocks": clk,
+            "kernels": kernels, "grouped_gemm_tflops":
+                (work["gemm_w1_silu"][1] + work["gemm_w2"][1]) /
+                ((stage_ms["gemm_w1_silu"] + stage_ms["gemm_w2"]) / 1e3) / 1e12,
+            "load": load_stats(counts), "peaks": peaks}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    from workloads import get_config, BENCH_CONFIG
+    cfg = get_config(args.config or BENCH_CONFIG)
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

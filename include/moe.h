@@ -1,0 +1,214 @@
+/*
+ * moe.h - C ABI of a routed mixture-of-experts (MoE) layer forward on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer, as the source pages describe it:
+ *   gate      L = x W_g + b, one logit per expert
+ *             (DeepSeek-V4 EP article, section 2.1)
+ *   router    max-subtracted softmax, partial top-8, exact top-k; the lower
+ *             expert id wins a tie (same article, section 3.2)
+ *   dispatch  per-expert histogram, exclusive scan and a stable permutation
+ *             that packs the routed rows contiguously by expert id - the
+ *             single-GPU form of the expert-parallel all-to-all layout
+ *             (same article, section 3.3; Deepseek-MoE sync-tax article,
+ *             section 2.1), optionally as a per-token FP8 E4M3 payload
+ *             (sync-tax article, section 3.1)
+ *   FFN       per expert e: H = SiLU(X_e W1_e), Y = H W2_e ("L1 + Act + L2",
+ *             DeepSeek V3/V4 parallel-strategy article, Waved-EP section)
+ *   combine   out_t = sum_{j=0..k-1} w_tj * Y[pos(t, j)], in that order
+ *             (sync-tax article, section 2.3)
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers named as device pointers must point to device (or managed)
+ *    memory of the current CUDA device. Host pointers are never accepted.
+ *  - All tensors are dense, row-major, with no padding between rows.
+ *  - Device pointers to activations, weights, payloads, H, Y and outputs must
+ *    be 16-byte aligned; the workspace must be 256-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Every call is asynchronous on that stream: it only enqueues
+ *    kernels, never allocates, frees or synchronises (except
+ *    moe_get_device_error, which synchronises by design). The caller owns
+ *    every buffer, including the workspace.
+ *  - Calls return MOE_OK (0) or a negative moe_status. Argument errors are
+ *    found on the host before anything is enqueued. Errors found by a kernel
+ *    (an expert index or row position out of range, a device wait that ran
+ *    past its bound) are recorded in the workspace's error word; the kernel
+ *    skips the offending access instead of faulting. Read them with
+ *    moe_get_device_error.
+ *  - T = 0 is valid and produces empty outputs (counts/offsets are zeroed).
+ */
+#ifndef MOE_GB300_MOE_H_
+#define MOE_GB300_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,         /* null pointer, misaligned pointer, bad shape */
+  MOE_ERR_UNSUPPORTED = -2,         /* valid but unsupported combination */
+  MOE_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes below the size query's answer */
+  MOE_ERR_LAUNCH = -4,              /* a CUDA runtime/driver call failed */
+  MOE_ERR_BAD_INDEX = -5,           /* device: expert id or row position out of range */
+  MOE_ERR_TIMEOUT = -6              /* device: a bounded wait gave up */
+} moe_status;
+
+/* ---- configuration ----------------------------------------------------- */
+enum { MOE_DTYPE_F32 = 0, MOE_DTYPE_BF16 = 1 };
+
+enum {
+  /* softmax over all E logits, keep the k largest, divide them by their sum */
+  MOE_ROUTER_RENORM = 0,
+  /* exact softmax over the pre_k largest logits only; keep its first k
+   * entries without renormalising (the partial top-8 router of the
+   * DeepSeek-V4 EP article, section 3.2) */
+  MOE_ROUTER_PREK_SOFTMAX = 1
+};
+
+typedef struct moe_config {
+  int32_t T;           /* tokens, >= 0 */
+  int32_t d;           /* hidden size, multiple of 64 */
+  int32_t E;           /* experts, 1..256 */
+  int32_t k;           /* experts per token, 1..min(E, pre_k, 8) */
+  int32_t f;           /* expert FFN inner size, multiple of 64 */
+  int32_t dtype;       /* MOE_DTYPE_F32 or MOE_DTYPE_BF16: x, W_g, W1, W2, H, out */
+  int32_t router;      /* MOE_ROUTER_* */
+  int32_t pre_k;       /* partial top-k width, k..min(8, E) (8 on the pages) */
+  int32_t payload_fp8; /* 1: dispatch rows as FP8 E4M3 + fp32 scale (bf16 only) */
+} moe_config_t;
+
+/* Validate a configuration. Returns MOE_OK or MOE_ERR_INVALID_ARG /
+ * MOE_ERR_UNSUPPORTED without touching the device. */
+MOE_API int moe_check_config(const moe_config_t* cfg);
+
+/* ---- workspace ----------------------------------------------------------
+ * moe_scratch_size: bytes of workspace that moe_dispatch, moe_expert_ffn and
+ *   moe_combine need (an error word, dispatch per-block tables and, with the
+ *   FP8 payload, a bf16 staging copy of the rows for the tensor cores).
+ * moe_workspace_size: bytes moe_forward needs: the scratch above followed by
+ *   every intermediate of the layer (routing, permutation, payload, H, Y).
+ *   A forward workspace therefore also serves the stage calls.
+ * Both return 0 for an invalid configuration. The caller allocates the
+ * workspace (256-byte aligned); zero it once before first use, or call
+ * moe_clear_device_error, so the error word starts clear. */
+MOE_API size_t moe_scratch_size(const moe_config_t* cfg);
+MOE_API size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* ---- stage 1: gate + router ---------------------------------------------
+ * x [T, d] (dtype), W_g [d, E] (dtype), bias [E] fp32 or NULL (= zeros).
+ * Outputs: topk_idx [T, k] int32, topk_w [T, k] fp32, slot j = j-th choice
+ * (logit descending, lower id first on ties); logits [T, E] fp32 or NULL:
+ * the gate logits including the bias, as the router saw them.
+ * Logits are accumulated in fp32 from exact products, in K-chunks combined
+ * with compensated summation. */
+MOE_API int moe_route(const moe_config_t* cfg, const void* x, const void* W_g,
+              const float* bias, int32_t* topk_idx, float* topk_w,
+              float* logits, void* stream);
+
+/* ---- stage 2: dispatch ---------------------------------------------------
+ * Inputs: x [T, d] (dtype), topk_idx [T, k] int32.
+ * Outputs (R = T*k):
+ *   counts  [E]    int32  rows routed to each expert
+ *   offsets [E+1]  int32  exclusive prefix sum of counts; offsets[E] = R
+ *   pos     [R]    int32  flat entry i = t*k + j goes to row pos[i]; within an
+ *                         expert, rows follow increasing i (stable)
+ *   src     [R]    int32  src[pos[i]] = i / k (token of each packed row)
+ *   x_perm  [R, d]        packed rows: x[src[r]] in dtype, or with
+ *                         cfg->payload_fp8 the FP8 E4M3 bytes (uint8) of
+ *                         x / scale, rounded to nearest even, saturating
+ *   x_scale [R]    fp32   FP8 only (else may be NULL): scale = fp32(absmax of
+ *                         the token's row / 448), 1 for an all-zero row
+ * Entries of topk_idx outside [0, E) are skipped (pos = -1) and flag
+ * MOE_ERR_BAD_INDEX in the error word. ws: >= moe_scratch_size bytes. */
+MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                 int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                 void* x_perm, float* x_scale, void* ws, size_t ws_bytes,
+                 void* stream);
+
+/* ---- stage 3: grouped expert FFN -----------------------------------------
+ * For every expert e with rows [offsets[e], offsets[e+1]) of x_perm:
+ *   h[r] = SiLU(s_r * x_perm[r] . W1[e])   (s_r = x_scale[r] with FP8, else 1)
+ *   y_perm[r] = h[r] . W2[e]
+ * x_perm [R, d] (dtype, or uint8 E4M3 with the FP8 payload), x_scale [R]
+ * fp32 (FP8 only), offsets [E+1] int32 (non-decreasing, offsets[E] <= R;
+ * rows past offsets[E] are not touched), W1 [E, d, f] and W2 [E, f, d]
+ * (dtype, expert-major), h [R, f] (dtype) output, y_perm [R, d] fp32 output.
+ * bf16 uses the tcgen05 tensor cores (fp32 accumulate in TMEM); fp32 uses
+ * fp32 FMA. Experts with no rows read none of their weights.
+ * ws: >= moe_scratch_size bytes. */
+MOE_API int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
+                   const float* x_scale, const int32_t* offsets, const void* W1,
+                   const void* W2, void* h, float* y_perm, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* ---- stage 4: combine ------------------------------------------------------
+ * out[t] = sum_{j=0..k-1} topk_w[t, j] * y_perm[pos[t*k + j]], accumulated in
+ * fp32 in increasing j, then stored in dtype. No atomics: the result is
+ * bitwise reproducible. y_perm [R, d] fp32, pos [R] int32, topk_w [T, k]
+ * fp32, out [T, d] (dtype). A pos outside [0, R) contributes nothing and
+ * flags MOE_ERR_BAD_INDEX. ws: >= moe_scratch_size bytes. */
+MOE_API int moe_combine(const moe_config_t* cfg, const float* y_perm, const int32_t* pos,
+                const float* topk_w, void* out, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* ---- whole layer -----------------------------------------------------------
+ * moe_route -> moe_dispatch -> moe_expert_ffn -> moe_combine on one stream,
+ * with every intermediate in the workspace (>= moe_workspace_size bytes).
+ * No host synchronisation, so the call can be captured into a CUDA graph. */
+MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g,
+                const float* bias, const void* W1, const void* W2, void* out,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward that also records CUDA events (cudaEvent_t, passed as void*)
+ * at the kernel boundaries, for per-kernel timing on the launching stream:
+ *   events[0] before the route kernel      events[1] after route
+ *   events[2] after dispatch (3 kernels)   events[3] after the FP8 row
+ *   conversion (= events[2] without FP8)   events[4] after the W1 GEMM
+ *   events[5] after the W2 GEMM            events[6] after combine
+ * n_events must be MOE_NUM_EVENTS; any entry may be NULL (not recorded). */
+#define MOE_NUM_EVENTS 7
+MOE_API int moe_forward_with_events(const moe_config_t* cfg, const void* x,
+                            const void* W_g, const float* bias, const void* W1,
+                            const void* W2, void* out, void* ws, size_t ws_bytes,
+                            void* const* events, int n_events, void* stream);
+
+/* Pointers into a forward workspace, so a caller can inspect the
+ * intermediates of the last moe_forward (routing, permutation, H, Y).
+ * Any output pointer may be NULL. Returns MOE_ERR_INVALID_ARG for a bad
+ * configuration. No device access. */
+typedef struct moe_forward_views {
+  int32_t* topk_idx; float* topk_w;
+  int32_t* counts; int32_t* offsets; int32_t* pos; int32_t* src;
+  void* x_perm; float* x_scale; void* h; float* y_perm;
+} moe_forward_views_t;
+MOE_API int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* views);
+
+/* ---- errors --------------------------------------------------------------
+ * moe_get_device_error synchronises `stream`, reads the workspace error
+ * word, clears it, and returns MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_TIMEOUT
+ * (or MOE_ERR_LAUNCH if the stream itself reports an error).
+ * moe_clear_device_error enqueues a clear of the error word on `stream`. */
+MOE_API int moe_get_device_error(void* ws, void* stream);
+MOE_API int moe_clear_device_error(void* ws, void* stream);
+MOE_API const char* moe_strerror(int status);
+
+/* Number of kernels one moe_forward call launches for cfg (0 if invalid). */
+MOE_API int moe_forward_kernel_count(const moe_config_t* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H_ */

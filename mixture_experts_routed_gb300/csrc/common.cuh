@@ -1,0 +1,68 @@
+// common.cuh - internal declarations shared by the kernel translation units
+// and the C-ABI layer (moe_abi.cu). Nothing here is exported.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// Bits of the device error word (the first 4 bytes of the workspace).
+constexpr uint32_t kErrBadIndex = 1u;
+constexpr uint32_t kErrTimeout = 2u;
+
+// Bound on any device-side wait (mbarrier): 2 s of wall time.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Dispatch works on chunks of this many tokens (one CTA per chunk).
+constexpr int kDispatchTokensPerChunk = 8;
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- route.cu
+// Gate GEMM + softmax + top-k, fused. `dtype` 0 = fp32, 1 = bf16.
+cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* bias, int T,
+                         int d, int E, int k, int pre_k, int router, int32_t* topk_idx,
+                         float* topk_w, float* logits, cudaStream_t s);
+
+// ---------------------------------------------------------------- dispatch.cu
+// Zero counts[E] and offsets[E+1] (empty batch).
+cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cudaStream_t s);
+// Per-chunk histograms -> hist[e * nchunk + c].
+cudaError_t launch_dispatch_count(const int32_t* topk_idx, int T, int k, int E, int nchunk,
+                                  int32_t* hist, uint32_t* err, cudaStream_t s);
+// Per-expert exclusive scan over chunks -> base[e * nchunk + c], counts[e].
+cudaError_t launch_dispatch_scan(const int32_t* hist, int nchunk, int E, int32_t* base,
+                                 int32_t* counts, cudaStream_t s);
+// Stable ranks -> pos, src, offsets; row copy (or FP8 quantisation) -> x_perm.
+cudaError_t launch_dispatch_scatter(int dtype, int fp8, const void* x, const int32_t* topk_idx,
+                                    int T, int d, int k, int E, int nchunk,
+                                    const int32_t* counts, const int32_t* base,
+                                    int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
+                                    float* x_scale, uint32_t* err, cudaStream_t s);
+// E4M3 payload bytes -> bf16 (exact), for the tensor-core A operand.
+cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s);
+
+// ---------------------------------------------------------------- combine.cu
+cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const float* w, int T,
+                           int d, int k, int R, void* out, uint32_t* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- gemm_tc.cu
+// Grouped GEMM over expert segments on tcgen05: out[r] = epi(A[r] . W[e]).
+// A [R, K] bf16, W [E, K, N] bf16, offsets [E+1]. epi 0: (row scale) -> SiLU
+// -> bf16 out; epi 1: fp32 out.
+cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, int K, int N,
+                           const int32_t* offsets, const float* row_scale, void* out,
+                           uint32_t* err, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- gemm_simt.cu
+// The same grouped GEMM in fp32 FMA for fp32 layers.
+cudaError_t launch_gemm_simt(int epi, const float* A, int R, const float* W, int E, int K, int N,
+                             const int32_t* offsets, float* out, uint32_t* err, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,322 @@
+// dispatch.cu - pack the routed rows contiguously by expert id (DeepSeek-V4
+// EP article, section 3.3: "one send chunk per expert"; Deepseek-MoE
+// sync-tax article, section 2.1: per-destination packed buffers). On one GPU
+// the all-to-all layout is a stable counting sort of the flat entries
+// i = t*k + j by expert id, done in three kernels with no atomics on data:
+//
+//  count    one CTA per chunk of kDispatchTokensPerChunk tokens: shared-memory
+//           histogram of the chunk's expert ids -> hist[e][chunk]
+//  scan     one CTA per expert: exclusive scan of hist[e][.] over chunks ->
+//           base[e][chunk] (rows of expert e that earlier chunks own) and
+//           counts[e]
+//  scatter  one CTA per chunk: offsets = exclusive scan of counts (each CTA
+//           recomputes it from E <= 256 values); the stable rank of an entry
+//           inside its chunk comes from warp match_any + popc of the lanes
+//           below it plus the counts of earlier warps; then each warp copies
+//           one token row, read once with 16-byte loads and written to its k
+//           destinations (or quantised to an FP8 E4M3 payload with a
+//           per-token absmax scale, sync-tax article section 3.1).
+//
+// Expert ids outside [0, E) are skipped and flag kErrBadIndex.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTPC = kDispatchTokensPerChunk;
+
+__global__ void dispatch_empty_kernel(int E, int32_t* counts, int32_t* offsets) {
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    if (e < E) counts[e] = 0;
+    offsets[e] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(128) dispatch_count_kernel(const int32_t* __restrict__ idx,
+                                                             int T, int k, int E, int nchunk,
+                                                             int32_t* __restrict__ hist,
+                                                             uint32_t* __restrict__ err) {
+  __shared__ int h[kMaxExperts];
+  const int c = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const long long i0 = static_cast<long long>(c) * kTPC * k;
+  const long long R = static_cast<long long>(T) * k;
+  const int n = static_cast<int>(min(static_cast<long long>(kTPC * k), R - i0));
+  for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    const int e = __ldg(idx + i0 + q);
+    if (e >= 0 && e < E)
+      atomicAdd(&h[e], 1);
+    else
+      atomicOr(err, kErrBadIndex);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[static_cast<size_t>(e) * nchunk + c] = h[e];
+}
+
+// Block-wide exclusive scan of one int per thread (256 threads).
+__device__ __forceinline__ int block_exclusive_scan_256(int v, int* total) {
+  __shared__ int warp_sums[8];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  int wbase = 0, all = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < w) wbase += warp_sums[i];
+    all += warp_sums[i];
+  }
+  __syncthreads();
+  *total = all;
+  return wbase + incl - v;
+}
+
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t* __restrict__ hist,
+                                                            int nchunk, int E,
+                                                            int32_t* __restrict__ base,
+                                                            int32_t* __restrict__ counts) {
+  const int e = blockIdx.x;
+  const int32_t* h = hist + static_cast<size_t>(e) * nchunk;
+  int32_t* b = base + static_cast<size_t>(e) * nchunk;
+  // each thread owns a contiguous run of chunks
+  const int per = (nchunk + 255) / 256;
+  const int c0 = threadIdx.x * per;
+  const int c1 = min(c0 + per, nchunk);
+  int sum = 0;
+  for (int c = c0; c < c1; ++c) sum += __ldg(h + c);
+  int total;
+  int run = block_exclusive_scan_256(sum, &total);
+  for (int c = c0; c < c1; ++c) {
+    b[c] = run;
+    run += __ldg(h + c);
+  }
+  if (threadIdx.x == 0) counts[e] = total;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t u) {
+  return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+
+// 8 floats -> 8 E4M3 bytes (round to nearest even, saturating), element 0 in
+// the lowest byte.
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], float s) {
+  uint32_t w[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t acc = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const float a = __fdiv_rn(v[h * 4 + p * 2], s);
+      const float b = __fdiv_rn(v[h * 4 + p * 2 + 1], s);
+      const __nv_fp8x2_storage_t q =
+          __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+      acc |= static_cast<uint32_t>(q) << (16 * p);
+    }
+    w[h] = acc;
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+// dtype 0: fp32 rows, 1: bf16 rows. FP8 only with bf16.
+template <int DT, bool FP8>
+__global__ void __launch_bounds__(256) dispatch_scatter_kernel(
+    const void* __restrict__ xv, const int32_t* __restrict__ idx, int T, int d, int k, int E,
+    int nchunk, const int32_t* __restrict__ counts, const int32_t* __restrict__ base,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ src,
+    void* __restrict__ x_perm, float* __restrict__ x_scale, uint32_t* __restrict__ err) {
+  __shared__ int off_s[kMaxExperts + 1];
+  __shared__ int cnt_w[2][kMaxExperts];  // per-warp expert counts (<= 64 entries, 2 warps)
+  __shared__ int pos_s[kTPC * kMaxTopK];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int c = blockIdx.x;
+
+  // offsets = exclusive scan of counts
+  {
+    const int v = (tid < E) ? __ldg(counts + tid) : 0;
+    int total;
+    const int ex = block_exclusive_scan_256(v, &total);
+    if (tid < E) off_s[tid] = ex;
+    if (tid == 0) off_s[E] = total;
+    if (c == 0) {
+      if (tid < E) offsets[tid] = ex;
+      if (tid == 0) offsets[E] = total;
+    }
+  }
+  for (int q = tid; q < 2 * kMaxExperts; q += 256) (&cnt_w[0][0])[q] = 0;
+  __syncthreads();
+
+  // stable ranks of this chunk's entries (at most 64: warps 0 and 1)
+  const long long R = static_cast<long long>(T) * k;
+  const long long i0 = static_cast<long long>(c) * kTPC * k;
+  const int n = static_cast<int>(min(static_cast<long long>(kTPC * k), R - i0));
+  int e = -2;
+  unsigned mask = 0;
+  if (w < 2) {
+    const int q = w * 32 + lane;
+    if (q < n) {
+      e = __ldg(idx + i0 + q);
+      if (e < 0 || e >= E) e = -1;
+    }
+    mask = __match_any_sync(0xffffffffu, e);
+    const int leader = __ffs(mask) - 1;
+    if (lane == leader && e >= 0) cnt_w[w][e] = __popc(mask);
+  }
+  __syncthreads();
+  if (w < 2) {
+    const int q = w * 32 + lane;
+    if (q < n) {
+      int p = -1;
+      if (e >= 0) {
+        const int before = (w == 1) ? cnt_w[0][e] : 0;
+        const int rank = before + __popc(mask & ((1u << lane) - 1u));
+        p = off_s[e] + __ldg(base + static_cast<size_t>(e) * nchunk + c) + rank;
+        src[p] = static_cast<int32_t>((i0 + q) / k);
+      }
+      pos[i0 + q] = p;
+      pos_s[q] = p;
+    }
+  }
+  __syncthreads();
+
+  // row copy: warp w moves token t0 + w
+  const int t = c * kTPC + w;
+  if (t >= T) return;
+  int p[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) p[j] = (j < k) ? pos_s[w * k + j] : -1;
+
+  if constexpr (!FP8) {
+    constexpr int ES = DT == 0 ? 4 : 2;
+    const int nvec = d * ES / 16;
+    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const char*>(xv) +
+                                                     static_cast<size_t>(t) * d * ES);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm);
+    const size_t row_vecs = static_cast<size_t>(nvec);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(xr + v);
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = val;
+    }
+  } else {
+    // pass 1: absmax of the token's row (bf16 values are exact in fp32)
+    const int nvec = d / 8;
+    const uint4* xr =
+        reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xv) +
+                                       static_cast<size_t>(t) * d);
+    float amax = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(xr + v);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&val);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(h[i])));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    // pass 2: q = E4M3(x / s); the k copies share the scale
+    uint2* dst = reinterpret_cast<uint2*>(x_perm);
+    const size_t row_vecs = static_cast<size_t>(nvec);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(xr + v);
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&val);
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = bf16_to_f32(h[i]);
+      const uint2 q = quant8(f, s);
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = q;
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (p[j] >= 0) x_scale[p[j]] = s;
+    }
+  }
+}
+
+__global__ void fp8_to_bf16_kernel(const uint8_t* __restrict__ q, size_t n16,
+                                   __nv_bfloat16* __restrict__ out) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(q) + i);
+    const uint8_t* b = reinterpret_cast<const uint8_t*>(&raw);
+    uint32_t o[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const __nv_fp8x2_storage_t pair =
+          static_cast<__nv_fp8x2_storage_t>(b[2 * p] | (static_cast<uint16_t>(b[2 * p + 1]) << 8));
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+      const __half2 h2 = *reinterpret_cast<const __half2*>(&hr);
+      const float2 f2 = __half22float2(h2);
+      const __nv_bfloat162 bb = __floats2bfloat162_rn(f2.x, f2.y);  // exact: E4M3 fits in bf16
+      o[p] = *reinterpret_cast<const uint32_t*>(&bb);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out) + 2 * i;
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cudaStream_t s) {
+  dispatch_empty_kernel<<<1, 256, 0, s>>>(E, counts, offsets);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_count(const int32_t* topk_idx, int T, int k, int E, int nchunk,
+                                  int32_t* hist, uint32_t* err, cudaStream_t s) {
+  dispatch_count_kernel<<<nchunk, 128, 0, s>>>(topk_idx, T, k, E, nchunk, hist, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scan(const int32_t* hist, int nchunk, int E, int32_t* base,
+                                 int32_t* counts, cudaStream_t s) {
+  dispatch_scan_kernel<<<E, 256, 0, s>>>(hist, nchunk, E, base, counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_scatter(int dtype, int fp8, const void* x, const int32_t* topk_idx,
+                                    int T, int d, int k, int E, int nchunk,
+                                    const int32_t* counts, const int32_t* base,
+                                    int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
+                                    float* x_scale, uint32_t* err, cudaStream_t s) {
+  const dim3 grid(nchunk), block(256);
+  if (dtype == 0)
+    dispatch_scatter_kernel<0, false><<<grid, block, 0, s>>>(x, topk_idx, T, d, k, E, nchunk,
+                                                             counts, base, offsets, pos, src,
+                                                             x_perm, x_scale, err);
+  else if (!fp8)
+    dispatch_scatter_kernel<1, false><<<grid, block, 0, s>>>(x, topk_idx, T, d, k, E, nchunk,
+                                                             counts, base, offsets, pos, src,
+                                                             x_perm, x_scale, err);
+  else
+    dispatch_scatter_kernel<1, true><<<grid, block, 0, s>>>(x, topk_idx, T, d, k, E, nchunk,
+                                                            counts, base, offsets, pos, src,
+                                                            x_perm, x_scale, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s) {
+  const size_t n16 = n / 16;
+  if (n16 == 0) return cudaSuccess;
+  int blocks = static_cast<int>(min(n16 / 256 + 1, static_cast<size_t>(152 * 8)));
+  fp8_to_bf16_kernel<<<blocks, 256, 0, s>>>(q, n16, static_cast<__nv_bfloat16*>(out_bf16));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,355 @@
+// moe_abi.cu - the exported C ABI (include/moe.h): host-side validation,
+// workspace layout, and the launch sequence of each stage. No entry point
+// allocates, frees or synchronises (except moe_get_device_error).
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "moe.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_cfg(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d <= 0 || c->f <= 0 || c->E < 1 || c->k < 1) return MOE_ERR_INVALID_ARG;
+  if (c->d % 64 != 0 || c->f % 64 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->router != MOE_ROUTER_RENORM && c->router != MOE_ROUTER_PREK_SOFTMAX)
+    return MOE_ERR_INVALID_ARG;
+  if (c->payload_fp8 != 0 && c->payload_fp8 != 1) return MOE_ERR_INVALID_ARG;
+  const int max_pre = c->E < kMaxTopK ? c->E : kMaxTopK;
+  if (c->pre_k < 1 || c->pre_k > max_pre) return MOE_ERR_INVALID_ARG;
+  if (c->k > c->pre_k) return MOE_ERR_INVALID_ARG;
+  if (c->payload_fp8 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (c->d > 65536 || c->f > 65536) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c->T) * c->k > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
+
+struct Layout {
+  size_t err, hist, base, stage, scratch_end;
+  size_t topk_idx, topk_w, counts, offsets, pos, src, x_perm, x_scale, h, y, total;
+  int nchunk;
+};
+
+Layout layout_of(const moe_config_t& c) {
+  Layout L;
+  const size_t R = static_cast<size_t>(c.T) * c.k;
+  const size_t es = elem_size(c.dtype);
+  L.nchunk = ceil_div(c.T, kDispatchTokensPerChunk);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    return at;
+  };
+  L.err = take(kAlign);
+  L.hist = take(static_cast<size_t>(c.E) * L.nchunk * 4);
+  L.base = take(static_cast<size_t>(c.E) * L.nchunk * 4);
+  L.stage = take(c.payload_fp8 ? R * c.d * 2 : 0);
+  L.scratch_end = o;
+  L.topk_idx = take(R * 4);
+  L.topk_w = take(R * 4);
+  L.counts = take(static_cast<size_t>(c.E) * 4);
+  L.offsets = take(static_cast<size_t>(c.E + 1) * 4);
+  L.pos = take(R * 4);
+  L.src = take(R * 4);
+  L.x_perm = take(R * c.d * (c.payload_fp8 ? 1 : es));
+  L.x_scale = take(c.payload_fp8 ? R * 4 : 0);
+  L.h = take(R * c.f * es);
+  L.y = take(R * c.d * 4);
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+void record(void* const* ev, int i, cudaStream_t s) {
+  if (ev != nullptr && ev[i] != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+}
+
+// ---------------------------------------------------------------- stages
+int run_route(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
+              int32_t* idx, float* w, float* logits, cudaStream_t s) {
+  return status_of(launch_route(c.dtype, x, Wg, bias, c.T, c.d, c.E, c.k, c.pre_k, c.router,
+                                idx, w, logits, s));
+}
+
+int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x,
+                 const int32_t* idx, int32_t* counts, int32_t* offsets, int32_t* pos,
+                 int32_t* src, void* x_perm, float* x_scale, cudaStream_t s) {
+  if (c.T == 0) return status_of(launch_dispatch_empty(c.E, counts, offsets, s));
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  int32_t* hist = at<int32_t>(ws, L.hist);
+  int32_t* base = at<int32_t>(ws, L.base);
+  cudaError_t e = launch_dispatch_count(idx, c.T, c.k, c.E, L.nchunk, hist, err, s);
+  if (e == cudaSuccess) e = launch_dispatch_scan(hist, L.nchunk, c.E, base, counts, s);
+  if (e == cudaSuccess)
+    e = launch_dispatch_scatter(c.dtype, c.payload_fp8, x, idx, c.T, c.d, c.k, c.E, L.nchunk,
+                                counts, base, offsets, pos, src, x_perm, x_scale, err, s);
+  return status_of(e);
+}
+
+// FP8 payload -> bf16 staging rows (the GEMM prologue).
+int run_ffn_prologue(const moe_config_t& c, const Layout& L, void* ws, const void* x_perm,
+                     cudaStream_t s) {
+  if (!c.payload_fp8 || c.T == 0) return MOE_OK;
+  const size_t n = static_cast<size_t>(c.T) * c.k * c.d;
+  return status_of(
+      launch_fp8_to_bf16(static_cast<const uint8_t*>(x_perm), n, at<void>(ws, L.stage), s));
+}
+
+int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const void* x_perm,
+             const float* x_scale, const int32_t* offsets, const void* W1, const void* W2,
+             void* h, float* y, cudaStream_t s) {
+  const int R = c.T * c.k;
+  if (R == 0) return MOE_OK;
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  if (c.dtype == MOE_DTYPE_F32) {
+    if (which == 1)
+      return status_of(launch_gemm_simt(0, static_cast<const float*>(x_perm), R,
+                                        static_cast<const float*>(W1), c.E, c.d, c.f, offsets,
+                                        static_cast<float*>(h), err, s));
+    return status_of(launch_gemm_simt(1, static_cast<const float*>(h), R,
+                                      static_cast<const float*>(W2), c.E, c.f, c.d, offsets, y,
+                                      err, s));
+  }
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_LAUNCH;
+  if (which == 1) {
+    const void* A = c.payload_fp8 ? at<void>(ws, L.stage) : x_perm;
+    return status_of(launch_gemm_tc(0, A, R, W1, c.E, c.d, c.f, offsets,
+                                    c.payload_fp8 ? x_scale : nullptr, h, err, sms, s));
+  }
+  return status_of(launch_gemm_tc(1, h, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, sms, s));
+}
+
+int run_combine(const moe_config_t& c, const Layout& L, void* ws, const float* y,
+                const int32_t* pos, const float* w, void* out, cudaStream_t s) {
+  return status_of(launch_combine(c.dtype, y, pos, w, c.T, c.d, c.k, c.T * c.k, out,
+                                  at<uint32_t>(ws, L.err), s));
+}
+
+bool ok_ptr(const void* p) { return p != nullptr && aligned(p, 16); }
+
+int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const float* bias,
+                 const void* W1, const void* W2, void* out, void* ws, size_t ws_bytes,
+                 void* const* events, void* stream) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config_t& c = *cfg;
+  if (!ok_ptr(x) || Wg == nullptr || !ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(out) ||
+      ws == nullptr || !aligned(ws, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(c);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = as_stream(stream);
+  int32_t* idx = at<int32_t>(ws, L.topk_idx);
+  float* w = at<float>(ws, L.topk_w);
+  int32_t* counts = at<int32_t>(ws, L.counts);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* pos = at<int32_t>(ws, L.pos);
+  int32_t* src = at<int32_t>(ws, L.src);
+  void* x_perm = at<void>(ws, L.x_perm);
+  float* x_scale = c.payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
+  void* h = at<void>(ws, L.h);
+  float* y = at<float>(ws, L.y);
+
+  record(events, 0, s);
+  if ((st = run_route(c, x, Wg, bias, idx, w, nullptr, s)) != MOE_OK) return st;
+  record(events, 1, s);
+  if ((st = run_dispatch(c, L, ws, x, idx, counts, offsets, pos, src, x_perm, x_scale, s)) !=
+      MOE_OK)
+    return st;
+  record(events, 2, s);
+  if ((st = run_ffn_prologue(c, L, ws, x_perm, s)) != MOE_OK) return st;
+  record(events, 3, s);
+  if ((st = run_gemm(c, L, ws, 1, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
+    return st;
+  record(events, 4, s);
+  if ((st = run_gemm(c, L, ws, 2, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
+    return st;
+  record(events, 5, s);
+  if ((st = run_combine(c, L, ws, y, pos, w, out, s)) != MOE_OK) return st;
+  record(events, 6, s);
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_check_config(const moe_config_t* cfg) { return check_cfg(cfg); }
+
+size_t moe_scratch_size(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return layout_of(*cfg).scratch_end;
+}
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return layout_of(*cfg).total;
+}
+
+int moe_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+              int32_t* topk_idx, float* topk_w, float* logits, void* stream) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(x) || W_g == nullptr || topk_idx == nullptr || topk_w == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  return run_route(*cfg, x, W_g, bias, topk_idx, topk_w, logits, as_stream(stream));
+}
+
+int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                 int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
+                 float* x_scale, void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (counts == nullptr || offsets == nullptr || ws == nullptr || !aligned(ws, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!ok_ptr(x) || topk_idx == nullptr || pos == nullptr || src == nullptr ||
+                     !ok_ptr(x_perm) || (cfg->payload_fp8 && x_scale == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  if (ws_bytes < L.scratch_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return run_dispatch(*cfg, L, ws, x, topk_idx, counts, offsets, pos, src, x_perm, x_scale,
+                      as_stream(stream));
+}
+
+int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const float* x_scale,
+                   const int32_t* offsets, const void* W1, const void* W2, void* h,
+                   float* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (ws == nullptr || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 &&
+      (!ok_ptr(x_perm) || offsets == nullptr || !ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(h) ||
+       !ok_ptr(y_perm) || (cfg->payload_fp8 && x_scale == nullptr)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  if (ws_bytes < L.scratch_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = as_stream(stream);
+  if ((st = run_ffn_prologue(*cfg, L, ws, x_perm, s)) != MOE_OK) return st;
+  if ((st = run_gemm(*cfg, L, ws, 1, x_perm, x_scale, offsets, W1, W2, h, y_perm, s)) != MOE_OK)
+    return st;
+  return run_gemm(*cfg, L, ws, 2, x_perm, x_scale, offsets, W1, W2, h, y_perm, s);
+}
+
+int moe_combine(const moe_config_t* cfg, const float* y_perm, const int32_t* pos,
+                const float* topk_w, void* out, void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (ws == nullptr || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!ok_ptr(y_perm) || pos == nullptr || topk_w == nullptr || !ok_ptr(out)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  if (ws_bytes < L.scratch_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return run_combine(*cfg, L, ws, y_perm, pos, topk_w, out, as_stream(stream));
+}
+
+int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                const void* W1, const void* W2, void* out, void* ws, size_t ws_bytes,
+                void* stream) {
+  return forward_impl(cfg, x, W_g, bias, W1, W2, out, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_forward_with_events(const moe_config_t* cfg, const void* x, const void* W_g,
+                            const float* bias, const void* W1, const void* W2, void* out,
+                            void* ws, size_t ws_bytes, void* const* events, int n_events,
+                            void* stream) {
+  if (events != nullptr && n_events != MOE_NUM_EVENTS) return MOE_ERR_INVALID_ARG;
+  return forward_impl(cfg, x, W_g, bias, W1, W2, out, ws, ws_bytes, events, stream);
+}
+
+int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* v) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (ws == nullptr || v == nullptr) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  v->topk_idx = at<int32_t>(ws, L.topk_idx);
+  v->topk_w = at<float>(ws, L.topk_w);
+  v->counts = at<int32_t>(ws, L.counts);
+  v->offsets = at<int32_t>(ws, L.offsets);
+  v->pos = at<int32_t>(ws, L.pos);
+  v->src = at<int32_t>(ws, L.src);
+  v->x_perm = at<void>(ws, L.x_perm);
+  v->x_scale = cfg->payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
+  v->h = at<void>(ws, L.h);
+  v->y_perm = at<float>(ws, L.y);
+  return MOE_OK;
+}
+
+int moe_get_device_error(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_LAUNCH;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
+  if (cudaMemsetAsync(ws, 0, sizeof(v), s) != cudaSuccess) return MOE_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_LAUNCH;
+  if (v & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kErrBadIndex) return MOE_ERR_BAD_INDEX;
+  return MOE_OK;
+}
+
+int moe_clear_device_error(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, sizeof(uint32_t), as_stream(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_LAUNCH;
+}
+
+const char* moe_strerror(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_LAUNCH: return "CUDA launch or runtime error";
+    case MOE_ERR_BAD_INDEX: return "expert index or row position out of range (device)";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int moe_forward_kernel_count(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  if (cfg->T == 0) return 1;
+  return 1 + 3 + (cfg->payload_fp8 ? 1 : 0) + 2 + 1;
+}
+
+}  // extern "C"

@@ -34,10 +34,10 @@ E4M3_MAX_F32 = np.float32(448.0)
 def _np64(t) -> np.ndarray:
     """fp64 numpy copy of a torch tensor or array (bf16/fp32 values are exact)."""
     if hasattr(t, "detach"):
-        t = t.detach()
+        t = t.detach().cpu()            # the conversion itself runs on the host
         if t.dtype.is_floating_point:
             t = t.to(dtype=__import__("torch").float64)
-        return t.cpu().numpy()
+        return t.numpy()
     return np.asarray(t, dtype=np.float64)
 
 

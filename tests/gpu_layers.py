@@ -1,0 +1,112 @@
+"""Layer shapes and cached inputs/oracle results for the GPU parity tests.
+
+Inputs are drawn on the GPU by ``workloads.make_inputs`` (seeded) and copied
+to the host for the oracle; the oracle never sees anything the CUDA path
+produced."""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+from workloads import CONFIGS, CONFIG_ORDER, MoEConfig, ROUTER_PREK_SOFTMAX
+
+# Small shapes that exercise ragged tails, partial tiles and degenerate cases.
+SMALL = {
+    "ragged_T129_d256_E8_k2_f320": MoEConfig("ragged_T129_d256_E8_k2_f320", T=129, d=256, E=8,
+                                             k=2, f=320, dtype="bf16", seed=11),
+    "one_token_T1_d128_E4_k2_f128": MoEConfig("one_token_T1_d128_E4_k2_f128", T=1, d=128, E=4,
+                                              k=2, f=128, dtype="bf16", pre_k=4, seed=12),
+    "T7_d192_E16_k3_f192": MoEConfig("T7_d192_E16_k3_f192", T=7, d=192, E=16, k=3, f=192,
+                                     dtype="bf16", seed=13),
+    "single_expert_T70_d128_E1_k1_f192": MoEConfig("single_expert_T70_d128_E1_k1_f192", T=70,
+                                                   d=128, E=1, k=1, f=192, dtype="bf16",
+                                                   pre_k=1, seed=14),
+    "k_eq_E_T33_d128_E4_k4_f128": MoEConfig("k_eq_E_T33_d128_E4_k4_f128", T=33, d=128, E=4,
+                                            k=4, f=128, dtype="bf16", pre_k=4, seed=15),
+    "wide_E40_T100_d256_k3_f256": MoEConfig("wide_E40_T100_d256_k3_f256", T=100, d=256, E=40,
+                                            k=3, f=256, dtype="bf16", bias="normal",
+                                            bias_var=2.0, seed=16),
+    "fp8_T64_d256_E4_k2_f256": MoEConfig("fp8_T64_d256_E4_k2_f256", T=64, d=256, E=4, k=2,
+                                         f=256, dtype="bf16", pre_k=4, payload_fp8=True,
+                                         outlier_rate=0.01, seed=17),
+    "prek_T200_d256_E64_k2_f128": MoEConfig("prek_T200_d256_E64_k2_f128", T=200, d=256, E=64,
+                                            k=2, f=128, dtype="bf16",
+                                            router=ROUTER_PREK_SOFTMAX, bias="normal",
+                                            bias_var=0.5, seed=18),
+    "f32_T50_d64_E5_k2_f128": MoEConfig("f32_T50_d64_E5_k2_f128", T=50, d=64, E=5, k=2,
+                                        f=128, dtype="f32", pre_k=5, seed=19),
+    "multi_mtile_T300_d512_E2_k1_f768": MoEConfig("multi_mtile_T300_d512_E2_k1_f768", T=300,
+                                                  d=512, E=2, k=1, f=768, dtype="bf16",
+                                                  pre_k=2, seed=20),
+    "skew_T256_d128_E64_k8_f128_zipf": MoEConfig("skew_T256_d128_E64_k8_f128_zipf", T=256,
+                                                 d=128, E=64, k=8, f=128, dtype="bf16",
+                                                 bias="zipf", zipf_s=3.0, seed=21),
+}
+ALL = dict(SMALL)
+ALL.update(CONFIGS)
+SMALL_NAMES = list(SMALL)
+FULL_NAMES = CONFIG_ORDER
+# configs whose whole-layer oracle is cheap enough to run on every token
+ORACLE_FULL_OK = set(SMALL_NAMES) | {CONFIG_ORDER[0], CONFIG_ORDER[1]}
+
+
+@functools.lru_cache(maxsize=2)
+def layer(name: str):
+    """(cfg, gpu inputs, host fp64 inputs) for a named shape."""
+    cfg = ALL[name]
+    inp = make(cfg)
+    host = oracle.inputs_to_numpy({k: v for k, v in inp.items()})
+    return cfg, inp, host
+
+
+def make(cfg):
+    from workloads import make_inputs
+    return make_inputs(cfg, device="cuda")
+
+
+@functools.lru_cache(maxsize=2)
+def oracle_route(name: str):
+    cfg, inp, host = layer(name)
+    L = oracle.gate_logits(host["x"], host["Wg"], host["bias"])
+    idx, w = oracle.route(L, cfg.k, cfg.router, cfg.pre_k)
+    return L, idx, w
+
+
+@functools.lru_cache(maxsize=2)
+def oracle_dispatch(name: str):
+    cfg, _, _ = layer(name)
+    _, idx, _ = oracle_route(name)
+    return oracle.dispatch(idx, cfg.E)
+
+
+def sample_rows(offsets: np.ndarray, max_experts: int = 6, per_expert: int = 6, seed: int = 0):
+    """Rows to check per expert: first, last (the ragged tail of the last
+    m-tile) and a few random ones, from a spread of non-empty experts."""
+    rng = np.random.default_rng(seed)
+    E = len(offsets) - 1
+    nonempty = [e for e in range(E) if offsets[e + 1] > offsets[e]]
+    if len(nonempty) > max_experts:
+        pick = [nonempty[0], nonempty[-1]]
+        counts = np.diff(offsets)
+        pick.append(int(np.argmax(counts)))
+        rest = [e for e in nonempty if e not in pick]
+        pick += list(rng.choice(rest, size=max_experts - len(pick), replace=False))
+        nonempty = sorted(set(int(e) for e in pick))
+    rows = {}
+    for e in nonempty:
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        r = {lo, hi - 1}
+        if hi - lo > 2:
+            r |= set(int(v) for v in rng.integers(lo, hi, size=min(per_expert, hi - lo)))
+        rows[e] = sorted(r)
+    return rows
+
+
+@functools.lru_cache(maxsize=1)
+def oracle_payload(name: str):
+    """Per-token FP8 payload of the oracle: (q values, scales)."""
+    _, _, host = layer(name)
+    return oracle.quantize_payload_fp8(host["x"])

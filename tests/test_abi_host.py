@@ -1,0 +1,177 @@
+"""The C-ABI library builds, loads and exports exactly what include/moe.h
+declares; host-side validation returns the documented status codes. No test
+here reaches a CUDA call (they all fail validation first), so the file runs
+without a GPU."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from mixture_experts_routed_gb300 import build as B
+from mixture_experts_routed_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load()
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_stage_calls():
+    names = header_functions()
+    for n in ("moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert names == set(L.PROTOTYPES), names ^ set(L.PROTOTYPES)
+    for n in names:
+        assert getattr(lib, n) is not None
+
+
+def test_only_abi_symbols_are_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", L.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    funcs = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert header_functions() <= funcs
+    stray = {f for f in funcs if not f.startswith("moe_") and not f.startswith("_")}
+    assert not stray, stray
+
+
+def cfg(**kw):
+    base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0)
+    base.update(kw)
+    return L.MoeConfig(*[base[n] for n, _ in L.MoeConfig._fields_])
+
+
+@pytest.mark.parametrize("kw,status", [
+    ({}, L.MOE_OK),
+    (dict(T=0), L.MOE_OK),
+    (dict(dtype=0), L.MOE_OK),
+    (dict(payload_fp8=1), L.MOE_OK),
+    (dict(E=256, k=8), L.MOE_OK),
+    (dict(E=1, k=1, pre_k=1), L.MOE_OK),
+    (dict(router=1, E=64), L.MOE_OK),
+    (dict(T=-1), L.MOE_ERR_INVALID_ARG),
+    (dict(d=100), L.MOE_ERR_INVALID_ARG),
+    (dict(f=96), L.MOE_ERR_INVALID_ARG),
+    (dict(E=0), L.MOE_ERR_INVALID_ARG),
+    (dict(E=257), L.MOE_ERR_INVALID_ARG),
+    (dict(k=0), L.MOE_ERR_INVALID_ARG),
+    (dict(k=9, pre_k=8), L.MOE_ERR_INVALID_ARG),
+    (dict(k=3, pre_k=2), L.MOE_ERR_INVALID_ARG),
+    (dict(E=4, k=2, pre_k=8), L.MOE_ERR_INVALID_ARG),
+    (dict(dtype=2), L.MOE_ERR_INVALID_ARG),
+    (dict(router=2), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=2), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=1, dtype=0), L.MOE_ERR_UNSUPPORTED),
+    (dict(T=1 << 30, k=8), L.MOE_ERR_UNSUPPORTED),
+])
+def test_check_config(lib, kw, status):
+    c = cfg(**kw)
+    assert lib.moe_check_config(ctypes.byref(c)) == status
+    if status != L.MOE_OK:
+        assert lib.moe_workspace_size(ctypes.byref(c)) == 0
+        assert lib.moe_scratch_size(ctypes.byref(c)) == 0
+        assert lib.moe_forward_kernel_count(ctypes.byref(c)) == 0
+
+
+def test_null_config(lib):
+    assert lib.moe_check_config(None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_size(None) == 0
+
+
+def test_workspace_sizes(lib):
+    c = cfg(T=1024, d=4096, E=8, k=2, f=11008)
+    ws = lib.moe_workspace_size(ctypes.byref(c))
+    sc = lib.moe_scratch_size(ctypes.byref(c))
+    R = 1024 * 2
+    need = R * 4096 * 2 + R * 11008 * 2 + R * 4096 * 4   # x_perm + H + Y
+    assert sc > 0 and ws >= sc + need
+    assert ws < sc + need + (1 << 20)
+    assert ws % 256 == 0 and sc % 256 == 0
+    c8 = cfg(T=1024, d=4096, E=8, k=2, f=11008, payload_fp8=1)
+    # the FP8 layer stages a bf16 copy of the payload in scratch
+    assert lib.moe_scratch_size(ctypes.byref(c8)) >= sc + R * 4096 * 2
+    assert lib.moe_forward_kernel_count(ctypes.byref(c)) == 7
+    assert lib.moe_forward_kernel_count(ctypes.byref(c8)) == 8
+
+
+FAKE = ctypes.c_void_p(0x100000)       # never dereferenced: validation fails first
+FAKE_ODD = ctypes.c_void_p(0x100008)   # 8-byte aligned only
+
+
+def test_forward_argument_errors(lib):
+    c = cfg()
+    n = lib.moe_workspace_size(ctypes.byref(c))
+    f = lib.moe_forward
+    assert f(None, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), None, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE_ODD, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE_ODD, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, n - 1, None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    bad = cfg(d=96)
+    assert f(ctypes.byref(bad), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_forward_with_events_wrong_count(lib):
+    c = cfg()
+    n = lib.moe_workspace_size(ctypes.byref(c))
+    ev = (ctypes.c_void_p * 3)()
+    assert lib.moe_forward_with_events(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                                       FAKE, n, ev, 3, None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_stage_argument_errors(lib):
+    c = cfg()
+    sc = lib.moe_scratch_size(ctypes.byref(c))
+    assert lib.moe_route(ctypes.byref(c), None, FAKE, None, FAKE, FAKE, None, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                            FAKE, sc - 1, None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_dispatch(ctypes.byref(c), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                            FAKE, sc, None) == L.MOE_ERR_INVALID_ARG
+    c8 = cfg(payload_fp8=1)
+    sc8 = lib.moe_scratch_size(ctypes.byref(c8))
+    assert lib.moe_dispatch(ctypes.byref(c8), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                            FAKE, sc8, None) == L.MOE_ERR_INVALID_ARG   # no x_scale
+    assert lib.moe_expert_ffn(ctypes.byref(c), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE_ODD,
+                              FAKE, sc, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, None, sc, None) == L.MOE_ERR_INVALID_ARG
+    # an empty batch needs no device work for routing
+    c0 = cfg(T=0)
+    assert lib.moe_route(ctypes.byref(c0), None, None, None, None, None, None, None) == L.MOE_OK
+
+
+def test_strerror(lib):
+    for code in range(-6, 1):
+        s = lib.moe_strerror(code).decode()
+        assert s and s != "unknown status"
+    assert lib.moe_strerror(-99).decode() == "unknown status"
+    assert lib.moe_get_device_error(None, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_clear_device_error(None, None) == L.MOE_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    mod = importlib.import_module("mixture_experts_routed_gb300._lib")
+    saved = mod._lib
+    try:
+        mod._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            mod.load(str(tmp_path / "missing.so"))
+    finally:
+        mod._lib = saved
