@@ -164,6 +164,10 @@ def forward(c, x, Wg, bias, W1, W2, *, ws, out=None, events=None, stream=None):
         st = lib.moe_forward(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(W1), _p(W2),
                              _p(out), _p(ws), nbytes, _s(stream))
     else:
+        strm = stream if stream is not None else torch.cuda.current_stream()
+        for e in events:
+            if e is not None and not e.cuda_event:
+                e.record(strm)          # torch creates its CUDA event lazily
         arr = (ctypes.c_void_p * L.MOE_NUM_EVENTS)(
             *[None if e is None else e.cuda_event for e in events])
         st = lib.moe_forward_with_events(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(W1),
