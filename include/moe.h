@@ -137,6 +137,29 @@ MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* 
                  void* x_perm, float* x_scale, void* ws, size_t ws_bytes,
                  void* stream);
 
+/* ---- dispatch without a workspace ---------------------------------------
+ * The source pages have no counterpart to this entry point; it exists for
+ * callers that cannot allocate device memory when they dispatch (a locked,
+ * pre-sized memory pool; a plugin that is only handed its input and output
+ * buffers; code that must not call cudaMalloc because it can synchronise
+ * the device). It does what moe_dispatch does, with the same arguments
+ * except the workspace: its scratch tables live in a fixed array compiled
+ * into the library (4 MiB + 256 bytes, held on every GPU that loads the
+ * library until the process exits), and it allocates nothing.
+ * Limit: E * ceil(T / 8) <= 524288 (T = 16384 tokens over 256 experts
+ * fits); larger requests return MOE_ERR_WORKSPACE_TOO_SMALL before anything
+ * is enqueued. Out-of-range expert ids are skipped exactly as in
+ * moe_dispatch (pos = -1); there is no error word to read back.
+ * Every call shares the array and it keeps the last call's contents (each
+ * call rewrites the tables and clears its error word first). Calls whose
+ * kernels overlap on the GPU race on the array: order them on one stream.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture. */
+MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
+                         const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                         int32_t* pos, int32_t* src, void* x_perm, float* x_scale,
+                         void* stream);
+
 /* ---- stage 3: grouped expert FFN -----------------------------------------
  * For every expert e with rows [offsets[e], offsets[e+1]) of x_perm:
  *   h[r] = SiLU(s_r * x_perm[r] . W1[e])   (s_r = x_scale[r] with FP8, else 1)

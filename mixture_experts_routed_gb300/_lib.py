@@ -57,6 +57,7 @@ PROTOTYPES = {
     "moe_clear_device_error": (_I, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [_I]),
     "moe_forward_kernel_count": (_I, [_CFG]),
+    "moe_dispatch_noalloc": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
