@@ -1,7 +1,7 @@
 // combine.cu - weighted sum of each token's k expert outputs back in token
 // order (Deepseek-MoE sync-tax article, section 2.3):
 //   out[t] = sum_{j=0..k-1} w[t, j] * Y[pos[t*k + j]]
-// One warp per token; each lane owns 4-float columns, issues the k row loads
+// 128 threads per token; each owns 4-float columns, issues the k row loads
 // together and accumulates in fp32 in increasing j with no atomics, so the
 // result is bitwise reproducible. A pos outside [0, R) adds nothing and flags
 // kErrBadIndex.
@@ -13,20 +13,22 @@
 namespace moe {
 namespace {
 
-template <int DT>  // 0: fp32 out, 1: bf16 out
+// 128 threads per token, two tokens per CTA; each thread owns float4
+// columns c, c+128, ... and keeps U = 16/KMAX of them (16 rows) in flight.
+template <int DT, int KMAX>  // DT 0: fp32 out, 1: bf16 out; k <= KMAX
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
                                                       const int32_t* __restrict__ pos,
                                                       const float* __restrict__ w, int T, int d,
                                                       int k, int R, void* __restrict__ out,
                                                       uint32_t* __restrict__ err) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int tl = threadIdx.x & 127;
+  const int t = blockIdx.x * 2 + (threadIdx.x >> 7);
   if (t >= T) return;
-  int p[kMaxTopK];
-  float wt[kMaxTopK];
+  int p[KMAX];
+  float wt[KMAX];
   bool bad = false;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
+  for (int j = 0; j < KMAX; ++j) {
     p[j] = -1;
     wt[j] = 0.f;
     if (j < k) {
@@ -39,34 +41,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
       }
     }
   }
-  if (bad && lane == 0) atomicOr(err, kErrBadIndex);
+  if (bad && tl == 0) atomicOr(err, kErrBadIndex);
 
   const int nv = d / 4;
   const float4* yv = reinterpret_cast<const float4*>(y);
-  for (int c = lane; c < nv; c += 32) {
-    float4 rows[kMaxTopK];
+  constexpr int U = 16 / KMAX;
+  for (int c0 = tl; c0 < nv; c0 += 128 * U) {
+    float4 rows[U][KMAX];
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j)
-      if (p[j] >= 0) rows[j] = __ldg(yv + static_cast<size_t>(p[j]) * nv + c);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 128;
 #pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (p[j] >= 0) {
-        acc.x = fmaf(wt[j], rows[j].x, acc.x);
-        acc.y = fmaf(wt[j], rows[j].y, acc.y);
-        acc.z = fmaf(wt[j], rows[j].z, acc.z);
-        acc.w = fmaf(wt[j], rows[j].w, acc.w);
-      }
+      for (int j = 0; j < KMAX; ++j)
+        if (p[j] >= 0 && c < nv) rows[u][j] = __ldg(yv + static_cast<size_t>(p[j]) * nv + c);
     }
-    if constexpr (DT == 0) {
-      reinterpret_cast<float4*>(out)[static_cast<size_t>(t) * nv + c] = acc;
-    } else {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-      uint2 u;
-      u.x = *reinterpret_cast<const uint32_t*>(&lo);
-      u.y = *reinterpret_cast<const uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(out)[static_cast<size_t>(t) * nv + c] = u;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 128;
+      if (c >= nv) break;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (p[j] >= 0) {
+          acc.x = fmaf(wt[j], rows[u][j].x, acc.x);
+          acc.y = fmaf(wt[j], rows[u][j].y, acc.y);
+          acc.z = fmaf(wt[j], rows[u][j].z, acc.z);
+          acc.w = fmaf(wt[j], rows[u][j].w, acc.w);
+        }
+      }
+      if constexpr (DT == 0) {
+        reinterpret_cast<float4*>(out)[static_cast<size_t>(t) * nv + c] = acc;
+      } else {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 uu;
+        uu.x = *reinterpret_cast<const uint32_t*>(&lo);
+        uu.y = *reinterpret_cast<const uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(out)[static_cast<size_t>(t) * nv + c] = uu;
+      }
     }
   }
 }
@@ -76,11 +88,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const float* w, int T,
                            int d, int k, int R, void* out, uint32_t* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const dim3 grid(ceil_div(T, 8)), block(256);
-  if (dtype == 0)
-    combine_kernel<0><<<grid, block, 0, s>>>(y, pos, w, T, d, k, R, out, err);
-  else
-    combine_kernel<1><<<grid, block, 0, s>>>(y, pos, w, T, d, k, R, out, err);
+  const dim3 grid(ceil_div(T, 2)), block(256);
+#define MOE_COMBINE(DT, KM) combine_kernel<DT, KM><<<grid, block, 0, s>>>(y, pos, w, T, d, k, R, out, err)
+  if (dtype == 0) {
+    if (k <= 2) MOE_COMBINE(0, 2); else if (k <= 4) MOE_COMBINE(0, 4); else MOE_COMBINE(0, 8);
+  } else {
+    if (k <= 2) MOE_COMBINE(1, 2); else if (k <= 4) MOE_COMBINE(1, 4); else MOE_COMBINE(1, 8);
+  }
+#undef MOE_COMBINE
   return cudaGetLastError();
 }
 

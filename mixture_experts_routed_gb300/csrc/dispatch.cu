@@ -189,27 +189,49 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
   }
   __syncthreads();
 
-  // row copy: warp w moves token t0 + w
+  if constexpr (!FP8) {
+    // row copy: the whole CTA strides the chunk's rows (16-byte vectors),
+    // four loads in flight per thread; each row is read once and written to
+    // its k destinations
+    constexpr int ES = DT == 0 ? 4 : 2;
+    const int nvec = d * ES / 16;
+    const int t0 = c * kTPC;
+    const int ntok = min(kTPC, T - t0);
+    const int items = ntok * nvec;
+    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const char*>(xv) +
+                                                     static_cast<size_t>(t0) * d * ES);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm);
+    const size_t row_vecs = static_cast<size_t>(nvec);
+    constexpr int U = 4;
+    for (int base = tid; base < items; base += 256 * U) {
+      uint4 val[U];
+      int it[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        it[u] = base + u * 256;
+        if (it[u] < items) val[u] = __ldg(xr + it[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (it[u] >= items) continue;
+        const int q = it[u] / nvec, v = it[u] - q * nvec;
+        for (int j = 0; j < k; ++j) {
+          const int pj = pos_s[q * k + j];
+          if (pj >= 0) dst[static_cast<size_t>(pj) * row_vecs + v] = val[u];
+        }
+      }
+    }
+    return;
+  }
+
+  // FP8 payload: warp w quantises token t0 + w
   const int t = c * kTPC + w;
   if (t >= T) return;
   int p[kMaxTopK];
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) p[j] = (j < k) ? pos_s[w * k + j] : -1;
 
-  if constexpr (!FP8) {
-    constexpr int ES = DT == 0 ? 4 : 2;
-    const int nvec = d * ES / 16;
-    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const char*>(xv) +
-                                                     static_cast<size_t>(t) * d * ES);
-    uint4* dst = reinterpret_cast<uint4*>(x_perm);
-    const size_t row_vecs = static_cast<size_t>(nvec);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(xr + v);
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = val;
-    }
-  } else {
+  if constexpr (FP8) {
     // pass 1: absmax of the token's row (bf16 values are exact in fp32)
     const int nvec = d / 8;
     const uint4* xr =

@@ -9,15 +9,16 @@
 // The logits never go to HBM unless the caller asks for them.
 //
 // Two gate GEMM shapes:
-//  * E <= 32 ("narrow"): one warp per token; each lane accumulates a strided
-//    slice of the hidden dimension for all E experts, then a butterfly
-//    reduction (bitwise identical on every lane) gives the E logits.
+//  * E <= 32 ("narrow"): 4 warps per token split the hidden dimension; each
+//    thread accumulates its slice for all E experts, a butterfly reduces
+//    inside each warp and the 4 warp partials are added in warp order.
 //  * E > 32 ("wide"): a CTA computes a 32-token x E tile from shared-memory
 //    staged x and W_g; each thread owns 4 tokens x E/32 experts, accumulates
 //    32-long K chunks and folds them into the total with compensated
 //    (Kahan) summation, which keeps |L - L_fp64| ~1e-7 at d = 7168.
 #include <cfloat>
 #include <cstdint>
+#include <cstddef>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -99,52 +100,95 @@ __device__ __forceinline__ void warp_select_and_weigh(const float (&v)[NJ], cons
 }
 
 // ---------------------------------------------------------------- narrow
-// One warp per token, NE >= E accumulators per lane. Lane l covers hidden
-// indices [8c, 8c+8) (bf16) or [4c, 4c+4) (fp32) for c = l, l+32, ...
-template <typename Tin, int NE>
-__global__ void __launch_bounds__(256) route_narrow_kernel(
+// E <= 32. A CTA of 4 warps handles TPB tokens; its 128 threads stride the
+// hidden dimension in 16-byte vectors of x (thread i takes vectors i, i+128,
+// ...), so each thread sums a d/128 slice for every expert and token. W_g
+// rows are read as 16-byte vectors when a row is a whole number of them
+// (VW), else element by element. Partial sums: butterfly inside each warp
+// (identical bits on every lane), then the 4 warp partials are added in warp
+// order, so the result does not depend on scheduling.
+template <typename Tin, int NE, int TPB, bool VW>
+__global__ void __launch_bounds__(128) route_narrow_kernel(
     const Tin* __restrict__ x, const Tin* __restrict__ Wg, const float* __restrict__ bias, int T,
     int d, int E, int k, int pre_k, int router, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, float* __restrict__ logits) {
   constexpr int VEC = 16 / sizeof(Tin);  // elements per 16-byte load
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (t >= T) return;
+  __shared__ float part[4][TPB][NE];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * TPB;
 
-  float acc[NE];
+  float acc[TPB][NE];
 #pragma unroll
-  for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+  for (int q = 0; q < TPB; ++q)
+#pragma unroll
+    for (int e = 0; e < NE; ++e) acc[q][e] = 0.f;
 
-  const Tin* xr = x + static_cast<size_t>(t) * d;
   const int nvec = d / VEC;
-  for (int c = lane; c < nvec; c += 32) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(xr) + c);
-    const Tin* xv = reinterpret_cast<const Tin*>(&raw);
+  for (int c = threadIdx.x; c < nvec; c += 128) {
+    uint4 raw[TPB];
+#pragma unroll
+    for (int q = 0; q < TPB; ++q)
+      raw[q] = (t0 + q < T) ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t0 + q) * d) + c)
+                            : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
-      const float xi = to_f32(xv[i]);
       const Tin* wrow = Wg + static_cast<size_t>(c * VEC + i) * E;
+      float wv[NE];
+      if constexpr (VW) {
+        constexpr int PER = 16 / sizeof(Tin);
 #pragma unroll
-      for (int e = 0; e < NE; ++e)
-        if (e < E) acc[e] = fmaf(xi, to_f32(__ldg(wrow + e)), acc[e]);
+        for (int v = 0; v < NE / PER; ++v) {
+          if (v * PER < E) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(wrow) + v);
+            const Tin* ue = reinterpret_cast<const Tin*>(&u);
+#pragma unroll
+            for (int j = 0; j < PER; ++j) wv[v * PER + j] = to_f32(ue[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < PER; ++j) wv[v * PER + j] = 0.f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) wv[e] = (e < E) ? to_f32(__ldg(wrow + e)) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < TPB; ++q) {
+        const float xi = to_f32(reinterpret_cast<const Tin*>(&raw[q])[i]);
+#pragma unroll
+        for (int e = 0; e < NE; ++e) acc[q][e] = fmaf(xi, wv[e], acc[q][e]);
+      }
     }
   }
-  // butterfly: every lane ends with the same bits (a + b == b + a)
 #pragma unroll
-  for (int e = 0; e < NE; ++e) {
+  for (int q = 0; q < TPB; ++q)
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-  }
-  // lane e holds expert e's logit
-  float mine = -INFINITY;
+    for (int e = 0; e < NE; ++e) {
 #pragma unroll
-  for (int e = 0; e < NE; ++e)
-    if (e == lane && e < E) mine = acc[e] + (bias ? __ldg(bias + e) : 0.f);
-  if (logits && lane < E) logits[static_cast<size_t>(t) * E + lane] = mine;
+      for (int off = 16; off > 0; off >>= 1)
+        acc[q][e] += __shfl_xor_sync(0xffffffffu, acc[q][e], off);
+    }
+#pragma unroll
+  for (int q = 0; q < TPB; ++q)
+#pragma unroll
+    for (int e = 0; e < NE; ++e)
+      if (e == lane) part[w][q][e] = acc[q][e];
+  __syncthreads();
 
-  float v[1] = {mine};
-  int id[1] = {lane < E ? lane : 0x7fffffff};
-  warp_select_and_weigh<1>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+  // warp q selects for token t0 + q; lane e owns expert e
+  for (int q = w; q < TPB; q += 4) {
+    const int t = t0 + q;
+    if (t >= T) break;
+    float mine = -INFINITY;
+    if (lane < E) {
+      mine = ((part[0][q][lane] + part[1][q][lane]) + part[2][q][lane]) + part[3][q][lane];
+      mine += bias ? __ldg(bias + lane) : 0.f;
+      if (logits) logits[static_cast<size_t>(t) * E + lane] = mine;
+    }
+    float v[1] = {mine};
+    int id[1] = {lane < E ? lane : 0x7fffffff};
+    warp_select_and_weigh<1>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+  }
 }
 
 // ---------------------------------------------------------------- wide
@@ -260,16 +304,28 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
                            float* logits, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   if (E <= 32) {
-    const dim3 grid(ceil_div(T, 8)), block(256);
-#define MOE_NARROW(NE)                                                                        \
-  route_narrow_kernel<Tin, NE><<<grid, block, 0, s>>>(x, Wg, bias, T, d, E, k, pre_k, router, \
-                                                      topk_idx, topk_w, logits)
-    if (E <= 8)
-      MOE_NARROW(8);
-    else if (E <= 16)
-      MOE_NARROW(16);
-    else
-      MOE_NARROW(32);
+    const bool vw = (reinterpret_cast<uintptr_t>(Wg) % 16 == 0) &&
+                    ((E * static_cast<int>(sizeof(Tin))) % 16 == 0);
+    const int tpb = (T >= 4096) ? 2 : 1;
+    const dim3 block(128);
+#define MOE_NARROW(NE, TPB, VW)                                                          \
+  route_narrow_kernel<Tin, NE, TPB, VW><<<dim3(ceil_div(T, TPB)), block, 0, s>>>(      \
+      x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits)
+#define MOE_NARROW_E(TPB, VW) \
+  do {                        \
+    if (E <= 8)               \
+      MOE_NARROW(8, TPB, VW); \
+    else if (E <= 16)         \
+      MOE_NARROW(16, TPB, VW);\
+    else                      \
+      MOE_NARROW(32, TPB, VW);\
+  } while (0)
+    if (tpb == 1) {
+      if (vw) MOE_NARROW_E(1, true); else MOE_NARROW_E(1, false);
+    } else {
+      if (vw) MOE_NARROW_E(2, true); else MOE_NARROW_E(2, false);
+    }
+#undef MOE_NARROW_E
 #undef MOE_NARROW
   } else {
     const dim3 grid(ceil_div(T, kWideTokens)), block(256);
