@@ -324,6 +324,309 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA pair
+// The same grouped GEMM on the 2-SM tensor-core path (tcgen05 cta_group::2).
+// A cluster of two CTAs computes a 256-row x 256-feature pair tile with one
+// M256 N256 K16 MMA per k-step, issued by the even CTA: each CTA stages its
+// own 128 token rows (A) and its own 128-feature half of the weight tile (B),
+// so per SM the shared-memory traffic (TMA fills plus tensor-core operand
+// reads) is 2/3 of the single-CTA kernel's, which is what limits that one.
+// Each CTA's tensor memory holds the accumulator rows of its own 128 tokens.
+// Synchronisation across the pair:
+//   full[s]   (even CTA) the TMA bytes of both CTAs: each CTA loads into its
+//             own shared memory and counts the bytes on the even CTA's
+//             barrier (the cta_group::2 form of the tensor copy);
+//   empty[s]  both CTAs, from one multicast tcgen05.commit;
+//   tfull     both CTAs, multicast commit after a tile's last MMA;
+//   tempty    (even CTA) 4 local + 4 remote epilogue-warp arrives.
+namespace pairk {
+constexpr int BM = 256, BN = 256, BK = 64, STAGES = 6;
+constexpr int A_BYTES = 128 * BK * 2;       // 16 KB: this CTA's 128 rows
+constexpr int BOX_BYTES = BK * 64 * 2;      // 8 KB: [64 k][64 n]
+constexpr int B_BYTES = 2 * BOX_BYTES;      // 16 KB: this CTA's 128 features
+constexpr int B_SLOT = B_BYTES;
+constexpr int STAGE_BYTES = A_BYTES + B_SLOT;
+constexpr int ACC_COLS = BN;                // 128 lanes x 256 fp32 columns
+constexpr int NUM_ACC = 2;
+constexpr int TMEM_COLS = ACC_COLS * NUM_ACC;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+constexpr int OFF_A = 0;
+constexpr int OFF_B = STAGES * A_BYTES;
+constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;  // full, empty, tfull, tempty, drain
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_SEG = OFF_MISC + 16;
+constexpr int OFF_TSTART = OFF_SEG + (kMaxExperts + 1) * 4;
+constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;
+
+struct PTile {
+  int e, row0, rows_end, n0;  // pair rows [row0, min(row0 + 256, rows_end)), features n0..
+};
+
+__device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* seg, int E,
+                                        int n_tiles) {
+  int lo = 0, hi = E;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tstart[mid] <= tile)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  PTile t;
+  t.e = lo;
+  const int local = tile - tstart[lo];
+  const int mt = (seg[lo + 1] - seg[lo] + BM - 1) / BM;
+  const int nt = local / mt, m = local - nt * mt;
+  t.row0 = seg[lo] + m * BM;
+  t.rows_end = seg[lo + 1];
+  t.n0 = nt * BN;
+  return t;
+}
+}  // namespace pairk
+
+template <int EPI>
+__global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem + pairk::OFF_A;
+  uint8_t* sB = smem + pairk::OFF_B;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pairk::OFF_BAR);
+  uint64_t* empty = full + pairk::STAGES;
+  uint64_t* tfull = empty + pairk::STAGES;
+  uint64_t* tempty = tfull + pairk::NUM_ACC;
+  uint64_t* drain = tempty + pairk::NUM_ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pairk::OFF_MISC);
+  int* s_total = reinterpret_cast<int*>(smem + pairk::OFF_MISC + 4);
+  int* seg = reinterpret_cast<int*>(smem + pairk::OFF_SEG);
+  int* tstart = reinterpret_cast<int*>(smem + pairk::OFF_TSTART);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int E = p.E;
+
+  if (warp == 0) {
+    for (int e = lane; e <= E; e += 32) seg[e] = __ldg(p.offsets + e);
+    __syncwarp();
+    bool ok = true;
+    int running = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      int tiles = 0;
+      bool bad = false;
+      if (e < E) {
+        const int lo = seg[e], hi = seg[e + 1];
+        bad = lo < 0 || hi < lo || hi > p.R;
+        tiles = bad ? 0 : ((hi - lo + pairk::BM - 1) / pairk::BM) * p.n_tiles;
+      }
+      if (__any_sync(0xffffffffu, bad)) ok = false;
+      int incl = tiles;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (e < E) tstart[e] = running + incl - tiles;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      tstart[E] = running;
+      *s_total = ok ? running : 0;
+      if (!ok && blockIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+      for (int i = 0; i < pairk::STAGES; ++i) {
+        mbar_init(&full[i], 1);
+        mbar_init(&empty[i], 1);
+      }
+      for (int i = 0; i < pairk::NUM_ACC; ++i) {
+        mbar_init(&tfull[i], 1);
+        mbar_init(&tempty[i], 8);  // 4 epilogue warps in each CTA of the pair
+      }
+      mbar_init(drain, 1);
+      fence_mbar_init();
+    }
+  } else if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, pairk::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anyone signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = *s_total;
+  const int KB = p.K / pairk::BK;
+  bool timed_out = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      // both CTAs' bytes of a stage are counted on the even CTA's full[s]
+      const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
+      for (int tile = pair; tile < total && !timed_out; tile += npairs) {
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
+        const int my_row = min(t.row0 + static_cast<int>(rank) * 128, p.R - 1);
+        const int my_n0 = t.n0 + static_cast<int>(rank) * 128;
+        const int nbox = my_n0 < p.N ? min(2, (p.N - my_n0) / 64) : 0;
+        const int n1 = t.n0 + 128;
+        const int nbox_pair = min(2, (p.N - t.n0) / 64) + (n1 < p.N ? min(2, (p.N - n1) / 64) : 0);
+        const uint32_t bytes = static_cast<uint32_t>(2 * pairk::A_BYTES + nbox_pair * pairk::BOX_BYTES);
+        const int brow = t.e * p.K;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
+          const uint32_t bar = leader_full + static_cast<uint32_t>(s * 8);
+          tma_load_2d_pair(sA + s * pairk::A_BYTES, &tmA, bar, kb * pairk::BK, my_row);
+          for (int c = 0; c < nbox; ++c)
+            tma_load_2d_pair(sB + s * pairk::B_SLOT + c * pairk::BOX_BYTES, &tmB, bar,
+                             my_n0 + c * 64, brow + kb * pairk::BK);
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          if (++s == pairk::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // drain (even CTA: its full[s] also counts the odd CTA's bytes)
+      if (rank == 0)
+        for (int i = 0; i < pairk::STAGES; ++i)
+          if ((armed >> i) & 1u)
+            if (!mbar_wait_spin(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // -------------------------------------------------------- MMA issuer (even CTA)
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool issued = false;
+      for (int tile = pair; tile < total && !timed_out; tile += npairs) {
+        if (!mbar_wait_spin(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * pairk::ACC_COLS);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * pairk::A_BYTES);
+          const uint32_t b_base = smem_u32(sB + s * pairk::B_SLOT);
+#pragma unroll
+          for (int kk = 0; kk < pairk::BK / 16; ++kk)
+            tc_mma_f16_pair(d_tmem, make_sdesc_sw128(a_base + kk * 32, 16, 1024),
+                            make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024), pairk::IDESC,
+                            (kb | kk) != 0 ? 1u : 0u);
+          issued = true;
+          tc_commit_pair_mc(&empty[s], 0x3);
+          if (++s == pairk::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (timed_out) break;
+        tc_commit_pair_mc(&tfull[acc], 0x3);
+        if (++acc == pairk::NUM_ACC) {
+          acc = 0;
+          aph ^= 1u;
+        }
+      }
+      if (timed_out && issued) {
+        tc_commit_pair_mc(drain, 0x1);
+        mbar_wait_spin(drain, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = pair; tile < total; tile += npairs) {
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
+      const bool ok = mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+      const int my_row0 = t.row0 + static_cast<int>(rank) * 128;
+      const int r = q * 32 + lane;
+      const bool valid = my_row0 + r < min(t.row0 + pairk::BM, t.rows_end);
+      const size_t grow = static_cast<size_t>(my_row0) + r;
+      float scale = 1.f;
+      if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * pairk::ACC_COLS) +
+                             (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < pairk::BN / 32; ++c) {
+        const int col = t.n0 + c * 32;
+        if (col >= p.N) break;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tbase + c * 32, v);
+        tmem_ld_wait();
+        if (!valid) continue;
+        if constexpr (EPI == 0) {
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = silu(__uint_as_float(v[2 * i]) * scale);
+            const float b = silu(__uint_as_float(v[2 * i + 1]) * scale);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                grow * p.N + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                packed[4 * i + 3]);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + grow * p.N + col);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_remote(leader_tempty + static_cast<uint32_t>(acc * 8));
+      }
+      if (++acc == pairk::NUM_ACC) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+  }
+
+  if (timed_out) atomicOr(p.err, kErrTimeout);
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal or read it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, pairk::TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -368,6 +671,40 @@ cudaError_t set_smem_attr() {
   return st;
 }
 
+template <int EPI>
+cudaError_t set_pair_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t st = cudaSuccess;
+  std::call_once(once, [] {
+    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              pairk::SMEM_BYTES);
+  });
+  return st;
+}
+
+constexpr bool kUsePairKernel = true;
+
+// Clusters of two that can be resident at once for the pair kernel (cached
+// per device and epilogue).
+int resident_pairs(int epi, const cudaLaunchConfig_t& lc_in, int num_sms) {
+  static int cache[64][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cache[dev][epi] > 0) return cache[dev][epi];
+  cudaLaunchConfig_t lc = lc_in;
+  lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
+  int n = 0;
+  const cudaError_t e =
+      epi == 0 ? cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<0>, &lc)
+               : cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<1>, &lc);
+  if (e != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  cache[dev][epi] = n;
+  return n;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, int K, int N,
@@ -395,6 +732,32 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
       static_cast<long long>(ceil_div(R, BM) + E) * static_cast<long long>(prm.n_tiles);
   const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
   cudaError_t st;
+  if (kUsePairKernel && num_sms >= 2) {
+    // pair tiles of 256 rows x 256 features, one cluster of two CTAs per SM pair
+    prm.n_tiles = ceil_div(N, pairk::BN);
+    const long long max_pt =
+        static_cast<long long>(ceil_div(R, pairk::BM) + E) * static_cast<long long>(prm.n_tiles);
+    cudaLaunchConfig_t lc = {};
+    lc.blockDim = dim3(pairk::NUM_THREADS);
+    lc.dynamicSmemBytes = pairk::SMEM_BYTES;
+    lc.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    // a persistent grid must fit at once: as many pairs as can be resident
+    // together (a pair needs two free SMs of one GPC), not num_sms / 2
+    if ((st = epi == 0 ? set_pair_smem_attr<0>() : set_pair_smem_attr<1>()) != cudaSuccess)
+      return st;
+    const int resident = resident_pairs(epi, lc, num_sms);
+    const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
+    lc.gridDim = dim3(2 * pairs);
+    if (epi == 0) return cudaLaunchKernelEx(&lc, gemm_pair_kernel<0>, mA, mB, prm);
+    return cudaLaunchKernelEx(&lc, gemm_pair_kernel<1>, mA, mB, prm);
+  }
   if (epi == 0) {
     if ((st = set_smem_attr<0>()) != cudaSuccess) return st;
     gemm_tc_kernel<0><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mA, mB, prm);
