@@ -1,35 +1,37 @@
 // gemm_tc.cu - grouped expert GEMM on the sm_103a tensor cores (tcgen05 +
-// TMEM), fed by TMA, over the variable-length expert segments the dispatch
-// produced. One kernel serves both projections of the expert FFN ("L1 + Act
-// + L2", DeepSeek V3/V4 parallel-strategy article, Waved-EP section):
+// TMEM, 2-SM pair mode), fed by TMA, over the variable-length expert segments
+// the dispatch produced. One kernel serves both projections of the expert
+// FFN ("L1 + Act + L2", DeepSeek V3/V4 parallel-strategy article, Waved-EP
+// section):
 //   W1 pass: H[r] = SiLU(s_r * A[r] . W1[e])  -> bf16   (epi 0)
 //   W2 pass: Y[r] = H[r] . W2[e]              -> fp32   (epi 1)
 // for the rows r of each expert's segment [offsets[e], offsets[e+1]).
 //
-// Shape of the work: the segment's rows are M (tokens), the weight columns
-// are N, K is the contraction. A CTA tile is 128 rows x 256 columns with a
-// 128 x 256 fp32 accumulator in tensor memory (256 of the 512 TMEM columns);
-// two accumulators let the epilogue of one tile overlap the main loop of the
-// next. Tiles are enumerated per expert with the m-tiles of one (expert,
-// n-tile) adjacent, so CTAs running side by side read the same weight tile
-// and HBM sees each weight byte about once; an expert with no rows has no
-// tiles and its weights are never read (the pages' contiguous per-expert
-// weight layout, DeepSeek-V4 EP article section 5.2, keeps every weight
-// tile one strided box).
+// Work split. A cluster of two CTAs (one per SM of an SM pair) computes a
+// pair tile of 256 token rows x 256 output features with one
+// tcgen05.mma.cta_group::2 M256 N256 K16 per k-step, issued by the even CTA.
+// Each CTA stages only its own 128 token rows (A, K-major) and its own
+// 128-feature half of the weight tile (B, the row-major weight read
+// MN-major), and each CTA's tensor memory receives the accumulator rows of
+// its own tokens. Per SM this is 2/3 of the shared-memory traffic of a
+// one-CTA M128 N256 tile (TMA fills plus tensor-core operand reads), which is
+// what bounds the one-CTA form. An expert's rows are covered by full
+// 256-row tiles plus, for the remainder, one swapped tile (weights as the
+// MMA's M side, the remaining tokens as its N, any multiple of 16), so a
+// short tail costs a fraction of a full tile. Tiles run expert by expert,
+// weight tile by weight tile, with the token tiles of one weight tile
+// adjacent, so pairs running side by side share the weight tile through
+// L2; an expert with no rows has no tiles and its weights are never read
+// (the contiguous per-expert weight layout of the DeepSeek-V4 EP article,
+// section 5.2, makes every weight tile one strided TMA box).
 //
-// Operands in shared memory (128-byte swizzle, TMA-written):
-//   A  [128 rows][64 k] bf16, K-major: one 16 KB box per stage.
-//   B  [64 k][256 n] bf16, N-major ("MN-major", the row-major weight as
-//      stored): four 8 KB boxes of [64 k][64 n], 8 KB apart.
-// A 4-stage mbarrier ring connects the roles of the 6 warps:
-//   warp 0     TMA producer (one thread)
-//   warp 1     TMEM allocator + MMA issuer (one thread): 4 x
-//              tcgen05.mma.cta_group::1.kind::f16 (M128 N256 K16) per stage,
-//              tcgen05.commit frees the stage / publishes the accumulator
-//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, scale / SiLU,
-//              masked row stores (rows past the segment are not written)
-// Every wait is bounded; a timeout sets kErrTimeout and the kernel drains
-// its copies and MMAs, frees TMEM and exits.
+// Shared memory per CTA: a 6-stage ring of 32 KB (16 KB token rows, 16 KB
+// weight half, 128-byte swizzle). Warp roles: warp 0 TMA producer (one
+// thread, both CTAs); warp 1 TMEM allocation (both CTAs) and MMA issue (even
+// CTA); warps 2-5 epilogue (tcgen05.ld 32 columns at a time, FP8 row scale
+// and SiLU or fp32 store, rows past the segment masked). Every wait is
+// bounded; a timeout sets kErrTimeout and the kernel drains its copies and
+// MMAs, frees TMEM and exits.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -46,26 +48,6 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
-constexpr int B_BOX_BYTES = BK * 64 * 2;    // 8 KB: [64 k][64 n]
-constexpr int B_BYTES = BK * BN * 2;        // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int TMEM_COLS = 2 * BN;           // two fp32 accumulators
-constexpr int NUM_THREADS = 192;
-constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
-
-// shared memory map (offsets from a 1024-aligned base)
-constexpr int OFF_A = 0;
-constexpr int OFF_B = STAGES * A_BYTES;
-constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], drain
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_SEG = OFF_MISC + 16;
-constexpr int OFF_TSTART = OFF_SEG + (kMaxExperts + 1) * 4;
-constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
-
 struct TcParams {
   const int32_t* offsets;
   const float* row_scale;
@@ -74,264 +56,9 @@ struct TcParams {
   int E, K, N, R, n_tiles;
 };
 
-struct Tile {
-  int e, row0, nrows, n0;
-};
-
-__device__ __forceinline__ Tile decode_tile(int tile, const int* tstart, const int* seg, int E,
-                                            int n_tiles) {
-  // largest e with tstart[e] <= tile; tstart[E] = total > tile
-  int lo = 0, hi = E;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (tstart[mid] <= tile)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  Tile t;
-  t.e = lo;
-  const int local = tile - tstart[lo];
-  const int mt = (seg[lo + 1] - seg[lo] + BM - 1) / BM;
-  const int nt = local / mt, m = local - nt * mt;
-  t.row0 = seg[lo] + m * BM;
-  t.nrows = min(BM, seg[lo + 1] - t.row0);
-  t.n0 = nt * BN;
-  return t;
-}
-
 __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
 
-template <int EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const TcParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem + OFF_A;
-  uint8_t* sB = smem + OFF_B;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  int* s_total = reinterpret_cast<int*>(smem + OFF_MISC + 4);
-  int* seg = reinterpret_cast<int*>(smem + OFF_SEG);
-  int* tstart = reinterpret_cast<int*>(smem + OFF_TSTART);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int E = p.E;
-
-  // ---- set-up: segment table, tile prefix, barriers, TMEM
-  if (warp == 0) {
-    for (int e = lane; e <= E; e += 32) seg[e] = __ldg(p.offsets + e);
-    __syncwarp();
-    bool ok = true;
-    int running = 0;
-    for (int b = 0; b < E; b += 32) {
-      const int e = b + lane;
-      int tiles = 0;
-      bool bad = false;
-      if (e < E) {
-        const int lo = seg[e], hi = seg[e + 1];
-        bad = lo < 0 || hi < lo || hi > p.R;
-        tiles = bad ? 0 : ((hi - lo + BM - 1) / BM) * p.n_tiles;
-      }
-      if (__any_sync(0xffffffffu, bad)) ok = false;
-      int incl = tiles;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      if (e < E) tstart[e] = running + incl - tiles;
-      running += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) {
-      tstart[E] = running;
-      *s_total = ok ? running : 0;
-      if (!ok && blockIdx.x == 0) atomicOr(p.err, kErrBadIndex);
-      for (int i = 0; i < STAGES; ++i) {
-        mbar_init(&full[i], 1);
-        mbar_init(&empty[i], 1);
-      }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&tfull[i], 1);
-        mbar_init(&tempty[i], 4);  // one arrive per epilogue warp
-      }
-      mbar_init(drain, 1);
-      fence_mbar_init();
-    }
-  } else if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total = *s_total;
-  const int KB = p.K / BK;
-  bool timed_out = false;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
-      int s = 0;
-      uint32_t ph = 0;
-      uint32_t armed = 0, armed_ph = 0;  // bit per stage
-      for (int tile = blockIdx.x; tile < total && !timed_out; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, tstart, seg, E, p.n_tiles);
-        const int nbox = min(4, (p.N - t.n0) / 64);
-        const int brow = t.e * p.K;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
-            timed_out = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[s], A_BYTES + nbox * B_BOX_BYTES);
-          tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * BK, t.row0);
-          for (int c = 0; c < nbox; ++c)
-            tma_load_2d(sB + s * B_BYTES + c * B_BOX_BYTES, &tmB, &full[s], t.n0 + c * 64,
-                        brow + kb * BK);
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-      }
-      // drain: every armed stage's bytes must have landed before exit
-      for (int i = 0; i < STAGES; ++i)
-        if ((armed >> i) & 1u)
-          if (!mbar_wait(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int s = 0, acc = 0;
-      uint32_t ph = 0, aph = 0;
-      bool issued = false;
-      for (int tile = blockIdx.x; tile < total && !timed_out; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
-          timed_out = true;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(&full[s], ph, kWaitLimitNs)) {
-            timed_out = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * A_BYTES);
-          const uint32_t b_base = smem_u32(sB + s * B_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t adesc = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t bdesc = make_sdesc_sw128(b_base + kk * 2048, B_BOX_BYTES, 1024);
-            tc_mma_f16(d_tmem, adesc, bdesc, IDESC, (kb | kk) != 0 ? 1u : 0u);
-          }
-          issued = true;
-          tc_commit(&empty[s]);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        if (timed_out) break;
-        tc_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
-      }
-      // drain after a timeout: all issued MMAs complete before TMEM is
-      // released (on the normal path the epilogue has already seen every
-      // accumulator complete)
-      if (timed_out && issued) {
-        tc_commit(drain);
-        mbar_wait(drain, 0, kWaitLimitNs);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    int acc = 0;
-    uint32_t aph = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, tstart, seg, E, p.n_tiles);
-      const bool ok = mbar_wait(&tfull[acc], aph, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) {
-        timed_out = true;
-        break;
-      }
-      tc_fence_after();
-      const int r = q * 32 + lane;
-      const bool valid = r < t.nrows;
-      const size_t grow = static_cast<size_t>(t.row0) + r;
-      float scale = 1.f;
-      if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
-      const uint32_t tbase =
-          tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col = t.n0 + c * 32;
-        if (col >= p.N) break;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tbase + c * 32, v);
-        tmem_ld_wait();
-        if (!valid) continue;
-        if constexpr (EPI == 0) {
-          uint32_t packed[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = silu(__uint_as_float(v[2 * i]) * scale);
-            const float b = silu(__uint_as_float(v[2 * i + 1]) * scale);
-            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                grow * p.N + col);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                packed[4 * i + 3]);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + grow * p.N + col);
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
-    }
-  }
-
-  if (timed_out) atomicOr(p.err, kErrTimeout);
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
-}
-
-// ---------------------------------------------------------------- CTA pair
-// The same grouped GEMM on the 2-SM tensor-core path (tcgen05 cta_group::2).
-// A cluster of two CTAs computes a 256-row x 256-feature pair tile with one
-// M256 N256 K16 MMA per k-step, issued by the even CTA: each CTA stages its
-// own 128 token rows (A) and its own 128-feature half of the weight tile (B),
-// so per SM the shared-memory traffic (TMA fills plus tensor-core operand
-// reads) is 2/3 of the single-CTA kernel's, which is what limits that one.
-// Each CTA's tensor memory holds the accumulator rows of its own 128 tokens.
+// ---------------------------------------------------------------- pair kernel
 // Synchronisation across the pair:
 //   full[s]   (even CTA) the TMA bytes of both CTAs: each CTA loads into its
 //             own shared memory and counts the bytes on the even CTA's
@@ -362,9 +89,13 @@ constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;
 
 struct PTile {
-  int e, row0, rows_end, n0;  // pair rows [row0, min(row0 + 256, rows_end)), features n0..
+  int e, row0, ntok, n0;  // token rows [row0, row0 + ntok), features n0..n0+255
+  bool swap;              // tail tile: weights are the MMA's M side, tokens its N
 };
 
+// An expert's rows are covered by full 256-row pair tiles and, for the
+// remainder (1..255 rows), one swapped tile whose MMA N is the remainder
+// rounded up to 16, so a short tail costs a fraction of a full tile.
 __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* seg, int E,
                                         int n_tiles) {
   int lo = 0, hi = E;
@@ -378,10 +109,13 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
   PTile t;
   t.e = lo;
   const int local = tile - tstart[lo];
-  const int mt = (seg[lo + 1] - seg[lo] + BM - 1) / BM;
+  const int rows = seg[lo + 1] - seg[lo];
+  const int full = rows / BM, rem = rows - full * BM;
+  const int mt = full + (rem > 0 ? 1 : 0);
   const int nt = local / mt, m = local - nt * mt;
   t.row0 = seg[lo] + m * BM;
-  t.rows_end = seg[lo + 1];
+  t.swap = m == full;
+  t.ntok = t.swap ? rem : BM;
   t.n0 = nt * BN;
   return t;
 }
@@ -473,7 +207,9 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
       const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
       for (int tile = pair; tile < total && !timed_out; tile += npairs) {
         const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
-        const int my_row = min(t.row0 + static_cast<int>(rank) * 128, p.R - 1);
+        // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
+        const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
+        const int my_row = min(t.row0 + static_cast<int>(rank) * half_rows, p.R - 1);
         const int my_n0 = t.n0 + static_cast<int>(rank) * 128;
         const int nbox = my_n0 < p.N ? min(2, (p.N - my_n0) / 64) : 0;
         const int n1 = t.n0 + 128;
@@ -518,6 +254,10 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * pairk::ACC_COLS);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
+        // swapped tile: A = weights (MN-major, the B slot), B = tokens (K-major, the A slot)
+        const uint32_t idesc =
+            t.swap ? make_idesc_bf16_f32(pairk::BM, (t.ntok + 15) & ~15, true, false) : pairk::IDESC;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
             timed_out = true;
@@ -527,10 +267,12 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
           const uint32_t a_base = smem_u32(sA + s * pairk::A_BYTES);
           const uint32_t b_base = smem_u32(sB + s * pairk::B_SLOT);
 #pragma unroll
-          for (int kk = 0; kk < pairk::BK / 16; ++kk)
-            tc_mma_f16_pair(d_tmem, make_sdesc_sw128(a_base + kk * 32, 16, 1024),
-                            make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024), pairk::IDESC,
+          for (int kk = 0; kk < pairk::BK / 16; ++kk) {
+            const uint64_t tok = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t wt = make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024);
+            tc_mma_f16_pair(d_tmem, t.swap ? wt : tok, t.swap ? tok : wt, idesc,
                             (kb | kk) != 0 ? 1u : 0u);
+          }
           issued = true;
           tc_commit_pair_mc(&empty[s], 0x3);
           if (++s == pairk::STAGES) {
@@ -564,43 +306,77 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int my_row0 = t.row0 + static_cast<int>(rank) * 128;
-      const int r = q * 32 + lane;
-      const bool valid = my_row0 + r < min(t.row0 + pairk::BM, t.rows_end);
-      const size_t grow = static_cast<size_t>(my_row0) + r;
-      float scale = 1.f;
-      if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
       const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * pairk::ACC_COLS) +
                              (static_cast<uint32_t>(q * 32) << 16);
+      if (!t.swap) {
+        // lane = token row of this CTA, columns = the tile's 256 features
+        const int r = static_cast<int>(rank) * 128 + q * 32 + lane;
+        const bool valid = r < t.ntok && t.row0 + r < p.R;
+        const size_t grow = static_cast<size_t>(t.row0) + r;
+        float scale = 1.f;
+        if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
 #pragma unroll 1
-      for (int c = 0; c < pairk::BN / 32; ++c) {
-        const int col = t.n0 + c * 32;
-        if (col >= p.N) break;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tbase + c * 32, v);
-        tmem_ld_wait();
-        if (!valid) continue;
-        if constexpr (EPI == 0) {
-          uint32_t packed[16];
+        for (int c = 0; c < pairk::BN / 32; ++c) {
+          const int col = t.n0 + c * 32;
+          if (col >= p.N) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (!valid) continue;
+          if constexpr (EPI == 0) {
+            uint32_t packed[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float a = silu(__uint_as_float(v[2 * i]) * scale);
-            const float b = silu(__uint_as_float(v[2 * i + 1]) * scale);
-            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-            packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int i = 0; i < 16; ++i) {
+              const float a = silu(__uint_as_float(v[2 * i]) * scale);
+              const float b = silu(__uint_as_float(v[2 * i + 1]) * scale);
+              const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+              packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                  grow * p.N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                  packed[4 * i + 3]);
+          } else {
+            float4* dst =
+                reinterpret_cast<float4*>(static_cast<float*>(p.out) + grow * p.N + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
           }
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                grow * p.N + col);
+        }
+      } else {
+        // lane = output feature of this CTA's half, columns = the tail's tokens
+        const int f = t.n0 + static_cast<int>(rank) * 128 + q * 32 + lane;
+        const bool f_ok = f < p.N;
+#pragma unroll 1
+        for (int c = 0; c * 32 < t.ntok; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_wait();
+          const int tok0 = c * 32;
+          const int nt = min(32, t.ntok - tok0);
+          float my_scale = 1.f;
+          if (EPI == 0 && p.row_scale != nullptr && lane < nt)
+            my_scale = __ldg(p.row_scale + t.row0 + tok0 + lane);
+          const size_t base = (static_cast<size_t>(t.row0) + tok0) * p.N + f;
+          if constexpr (EPI == 0) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                packed[4 * i + 3]);
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + grow * p.N + col);
+            for (int j = 0; j < 32; ++j) {
+              const float sj = __shfl_sync(0xffffffffu, my_scale, j);
+              if (j < nt && f_ok)
+                out[static_cast<size_t>(j) * p.N] =
+                    __float2bfloat16_rn(silu(__uint_as_float(v[j]) * sj));
+            }
+          } else {
+            float* out = static_cast<float*>(p.out) + base;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            for (int j = 0; j < 32; ++j)
+              if (j < nt && f_ok) out[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+          }
         }
       }
       tc_fence_before();
@@ -661,17 +437,6 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
 }
 
 template <int EPI>
-cudaError_t set_smem_attr() {
-  static std::once_flag once;
-  static cudaError_t st = cudaSuccess;
-  std::call_once(once, [] {
-    st = cudaFuncSetAttribute(gemm_tc_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              SMEM_BYTES);
-  });
-  return st;
-}
-
-template <int EPI>
 cudaError_t set_pair_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
@@ -681,8 +446,6 @@ cudaError_t set_pair_smem_attr() {
   });
   return st;
 }
-
-constexpr bool kUsePairKernel = true;
 
 // Clusters of two that can be resident at once for the pair kernel (cached
 // per device and epilogue).
@@ -711,12 +474,15 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
                            const int32_t* offsets, const float* row_scale, void* out,
                            uint32_t* err, int num_sms, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
+  if (num_sms < 2) return cudaErrorInvalidValue;
   CUtensorMap mA, mB;
   std::memset(&mA, 0, sizeof(mA));
   std::memset(&mB, 0, sizeof(mB));
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, BM))
+  // A: token rows, [128 rows][64 k] boxes; B: weights as [E*K rows, N], [64 k][64 n] boxes
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128))
     return cudaErrorInvalidValue;
-  if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64, BK))
+  if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64,
+                   pairk::BK))
     return cudaErrorInvalidValue;
   TcParams prm;
   prm.offsets = offsets;
@@ -727,12 +493,8 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
   prm.K = K;
   prm.N = N;
   prm.R = R;
-  prm.n_tiles = ceil_div(N, BN);
-  const long long max_tiles =
-      static_cast<long long>(ceil_div(R, BM) + E) * static_cast<long long>(prm.n_tiles);
-  const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
   cudaError_t st;
-  if (kUsePairKernel && num_sms >= 2) {
+  {
     // pair tiles of 256 rows x 256 features, one cluster of two CTAs per SM pair
     prm.n_tiles = ceil_div(N, pairk::BN);
     const long long max_pt =
@@ -758,14 +520,6 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
     if (epi == 0) return cudaLaunchKernelEx(&lc, gemm_pair_kernel<0>, mA, mB, prm);
     return cudaLaunchKernelEx(&lc, gemm_pair_kernel<1>, mA, mB, prm);
   }
-  if (epi == 0) {
-    if ((st = set_smem_attr<0>()) != cudaSuccess) return st;
-    gemm_tc_kernel<0><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mA, mB, prm);
-  } else {
-    if ((st = set_smem_attr<1>()) != cudaSuccess) return st;
-    gemm_tc_kernel<1><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(mA, mB, prm);
-  }
-  return cudaGetLastError();
 }
 
 }  // namespace moe
