@@ -12,10 +12,11 @@
 //  * E <= 32 ("narrow"): 4 warps per token split the hidden dimension; each
 //    thread accumulates its slice for all E experts, a butterfly reduces
 //    inside each warp and the 4 warp partials are added in warp order.
-//  * E > 32 ("wide"): a CTA computes a 32-token x E tile from shared-memory
-//    staged x and W_g; each thread owns 4 tokens x E/32 experts, accumulates
-//    32-long K chunks and folds them into the total with compensated
-//    (Kahan) summation, which keeps |L - L_fp64| ~1e-7 at d = 7168.
+//  * E > 32, or many tokens ("tiled"): a CTA computes a token x expert tile
+//    from shared-memory staged x and W_g with a register micro-tile per
+//    thread, accumulates 32-long K chunks and folds them into the totals with
+//    compensated (Kahan) summation, which keeps |L - L_fp64| ~1e-7 at
+//    d = 7168.
 #include <cfloat>
 #include <cstdint>
 #include <cstddef>
@@ -191,111 +192,240 @@ __global__ void __launch_bounds__(128) route_narrow_kernel(
   }
 }
 
-// ---------------------------------------------------------------- wide
-// CTA = 256 threads, 32 tokens x (32 * EPT) experts. Thread (ty, tx):
-// tokens 4*ty .. 4*ty+3, experts tx + 32*j (j < EPT).
-constexpr int kWideTokens = 32;
-constexpr int kWideBK = 32;
+// ---------------------------------------------------------------- tiled
+// A CTA of 256 threads computes a tile of NTT*TM tokens x NTE*TE experts
+// (NTT*NTE = 256 threads). Thread (ty, tx) owns tokens ty*TM .. ty*TM+TM-1
+// and experts g*(NTE*V) + tx*V + v (g < TE/V, v < V, V = min(TE, 4)), so
+// each k step is one vector load of x (broadcast in the warp) plus TE/V
+// vector loads of W_g (consecutive lanes read consecutive addresses). x and
+// W_g stream through shared memory (fp32) in 32-long K chunks, the next
+// chunk's global loads (16-byte vectors) issued before this chunk's math;
+// each chunk's sums are folded into the totals with Kahan summation.
+constexpr int kTileBK = 32;
 
-template <typename Tin, int EPT>
-__global__ void __launch_bounds__(256) route_wide_kernel(
+template <typename Tin, int TM, int TE, int NTT, int KG, bool VW>
+__global__ void __launch_bounds__(256) route_tiled_kernel(
     const Tin* __restrict__ x, const Tin* __restrict__ Wg, const float* __restrict__ bias, int T,
     int d, int E, int k, int pre_k, int router, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, float* __restrict__ logits) {
-  constexpr int EP = 32 * EPT;  // padded expert count
-  __shared__ __align__(16) float xs[kWideBK][kWideTokens];
-  __shared__ __align__(16) float ws[kWideBK * EP > kWideTokens * EP ? kWideBK * EP : kWideTokens * EP];
+  constexpr int NG = 256 / KG;     // threads per K group
+  constexpr int NTE = NG / NTT;
+  constexpr int BT = NTT * TM;     // tokens per tile
+  constexpr int EP = NTE * TE;     // experts per tile (>= E, padded)
+  constexpr int V = TE < 4 ? TE : 4;
+  constexpr int G = TE / V;
+  constexpr int EVEC = 16 / sizeof(Tin);               // elements per 16-byte load
+  constexpr int NXV = BT * kTileBK / EVEC;              // x vectors per chunk
+  constexpr int XLD = (NXV + NG - 1) / NG;               // ... per thread
+  constexpr int WLD = (kTileBK * EP + NG * EVEC - 1) / (NG * EVEC);
+  static_assert((BT * kTileBK) % EVEC == 0 && EP % EVEC == 0, "tile must split into vectors");
+  extern __shared__ __align__(16) float tsm[];
+  const int kg = threadIdx.x / NG;          // this thread's K group
+  const int tid = threadIdx.x % NG;         // index inside the group
+  float* xs = tsm + kg * kTileBK * (BT + EP);   // [kTileBK][BT] of this group
+  float* ws = xs + kTileBK * BT;                // [kTileBK][EP] of this group
+  float* Ls = tsm;                              // [BT][EP] after the K loop (aliases)
 
-  const int tid = threadIdx.x;
-  const int tx = tid & 31;
-  const int ty = tid >> 5;
-  const int t0 = blockIdx.x * kWideTokens;
+  const int tx = tid % NTE, ty = tid / NTE;
+  const int t0 = blockIdx.x * BT;
 
-  float tot[4][EPT], comp[4][EPT];
+  float tot[TM][TE], comp[TM][TE];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) tot[i][j] = comp[i][j] = 0.f;
+    for (int j = 0; j < TE; ++j) tot[i][j] = comp[i][j] = 0.f;
 
-  for (int k0 = 0; k0 < d; k0 += kWideBK) {
-    // x tile [32 tokens][32 k] -> xs[k][token]; 4 elements per thread
-    {
-      const int r = tid >> 3;           // token within tile
-      const int c = (tid & 7) * 4;      // k within chunk
+  uint4 xr[XLD], wr[WLD];
+  auto load_chunk = [&](int k0) {
+#pragma unroll
+    for (int u = 0; u < XLD; ++u) {
+      const int q = tid + u * NG;                 // vector index in the tile
+      const int r = q / (kTileBK / EVEC), cv = q % (kTileBK / EVEC);
       const int t = t0 + r;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        xs[c + i][r] = (t < T) ? to_f32(x[static_cast<size_t>(t) * d + k0 + c + i]) : 0.f;
+      xr[u] = (q < NXV && t < T)
+                  ? __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(t) * d + k0) + cv)
+                  : make_uint4(0, 0, 0, 0);
     }
-    // W_g tile [32 k][EP experts]
-    for (int idx = tid; idx < kWideBK * EP; idx += 256) {
-      const int r = idx / EP, e = idx % EP;
-      ws[idx] = (e < E) ? to_f32(Wg[static_cast<size_t>(k0 + r) * E + e]) : 0.f;
-    }
-    __syncthreads();
-    float acc[4][EPT];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int u = 0; u < WLD; ++u) {
+      const int q = tid + u * NG;
+      const int r = q / (EP / EVEC), cv = q % (EP / EVEC);
+      const int e0 = cv * EVEC;
+      if (VW && r < kTileBK && e0 + EVEC <= E) {   // rows 16-byte aligned (checked by the launcher)
+        wr[u] = __ldg(reinterpret_cast<const uint4*>(Wg + static_cast<size_t>(k0 + r) * E + e0));
+      } else if (r < kTileBK && e0 < E) {          // element loads
+        Tin tmp[EVEC];
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) acc[i][j] = 0.f;
-#pragma unroll 8
-    for (int kk = 0; kk < kWideBK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
-      float b[EPT];
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) b[j] = ws[kk * EP + tx + 32 * j];
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        acc[0][j] = fmaf(a.x, b[j], acc[0][j]);
-        acc[1][j] = fmaf(a.y, b[j], acc[1][j]);
-        acc[2][j] = fmaf(a.z, b[j], acc[2][j]);
-        acc[3][j] = fmaf(a.w, b[j], acc[3][j]);
+        for (int i = 0; i < EVEC; ++i)
+          tmp[i] = (e0 + i < E) ? Wg[static_cast<size_t>(k0 + r) * E + e0 + i] : Tin(0.f);
+        wr[u] = *reinterpret_cast<const uint4*>(tmp);
+      } else {
+        wr[u] = make_uint4(0, 0, 0, 0);
       }
     }
-    // compensated fold of the chunk sums into the totals
+  };
+  auto store_chunk = [&]() {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int u = 0; u < XLD; ++u) {
+      const int q = tid + u * NG;
+      if (q >= NXV) continue;
+      const int r = q / (kTileBK / EVEC), c0 = (q % (kTileBK / EVEC)) * EVEC;
+      const Tin* v = reinterpret_cast<const Tin*>(&xr[u]);
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        const float y = acc[i][j] - comp[i][j];
-        const float s = tot[i][j] + y;
-        comp[i][j] = (s - tot[i][j]) - y;
-        tot[i][j] = s;
+      for (int i = 0; i < EVEC; ++i) xs[(c0 + i) * BT + r] = to_f32(v[i]);
+    }
+#pragma unroll
+    for (int u = 0; u < WLD; ++u) {
+      const int q = tid + u * NG;
+      const int r = q / (EP / EVEC), e0 = (q % (EP / EVEC)) * EVEC;
+      if (r < kTileBK) {
+        const Tin* v = reinterpret_cast<const Tin*>(&wr[u]);
+#pragma unroll
+        for (int i = 0; i < EVEC; ++i) ws[r * EP + e0 + i] = to_f32(v[i]);
       }
-    __syncthreads();
-  }
+    }
+  };
 
-  // logits tile -> shared (reusing ws as [32 tokens][EP])
-  float* Ls = ws;
+  // group kg takes chunks kg, kg + KG, ... (all groups run the same number of
+  // iterations so that the CTA barriers line up; a group past the end idles)
+  const int nchunk = d / kTileBK;
+  const int iters = (nchunk + KG - 1) / KG;
+  if (kg < nchunk) load_chunk(kg * kTileBK);
+  for (int it = 0; it < iters; ++it) {
+    const int c = it * KG + kg;
+    const int k0 = c * kTileBK;
+    __syncthreads();          // previous chunk's math is done with xs / ws
+    if (c < nchunk) store_chunk();
+    __syncthreads();
+    if (c >= nchunk) continue;
+    if (c + KG < nchunk) load_chunk(k0 + KG * kTileBK);
+    float acc[TM][TE];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = tx + 32 * j;
-      const int r = ty * 4 + i;
-      float val = -INFINITY;
-      if (e < E) val = tot[i][j] + (bias ? __ldg(bias + e) : 0.f);
-      Ls[r * EP + e] = val;
-      if (logits && e < E && t0 + r < T) logits[static_cast<size_t>(t0 + r) * E + e] = val;
+      for (int j = 0; j < TE; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < kTileBK; ++kk) {
+      float a[TM], b[TE];
+      const float* xp = xs + kk * BT + ty * TM;
+      if constexpr (TM == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(xp);
+        a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+      } else if constexpr (TM == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(xp);
+        a[0] = v.x; a[1] = v.y;
+      } else {
+#pragma unroll
+        for (int i = 0; i < TM; ++i) a[i] = xp[i];
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float* wp = ws + kk * EP + g * (NTE * V) + tx * V;
+        if constexpr (V == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(wp);
+          b[g * 4 + 0] = v.x; b[g * 4 + 1] = v.y; b[g * 4 + 2] = v.z; b[g * 4 + 3] = v.w;
+        } else if constexpr (V == 2) {
+          const float2 v = *reinterpret_cast<const float2*>(wp);
+          b[g * 2 + 0] = v.x; b[g * 2 + 1] = v.y;
+        } else {
+          b[g] = wp[0];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TE; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int j = 0; j < TE; ++j) {
+        const float y = acc[i][j] - comp[i][j];
+        const float s2 = tot[i][j] + y;
+        comp[i][j] = (s2 - tot[i][j]) - y;
+        tot[i][j] = s2;
+      }
+  }
   __syncthreads();
 
-  // 8 warps x 4 tokens: select and weigh
+  // K-group totals -> shared [KG][BT][EP], added in group order, then the
+  // logits tile [BT][EP]
+  float* part = tsm;
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TE; ++j) {
+      const int e = (j / V) * (NTE * V) + tx * V + (j % V);
+      const int r = ty * TM + i;
+      part[(kg * BT + r) * EP + e] = tot[i][j];
+    }
+  __syncthreads();
+  for (int q = threadIdx.x; q < BT * EP; q += 256) {
+    const int r = q / EP, e = q % EP;
+    float sum = part[q];
+#pragma unroll
+    for (int g = 1; g < KG; ++g) sum += part[g * BT * EP + q];
+    float val = -INFINITY;
+    if (e < E) val = sum + (bias ? __ldg(bias + e) : 0.f);
+    if (logits && e < E && t0 + r < T) logits[static_cast<size_t>(t0 + r) * E + e] = val;
+    part[q] = val;   // each q is read and rewritten by the same thread
+  }
+  __syncthreads();
+
+  // 8 warps select and weigh BT/8 tokens each; lane holds experts lane + 32*j
+  constexpr int NJ = (EP + 31) / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll 1
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty * 4 + i;
+  for (int r = warp; r < BT; r += 8) {
     const int t = t0 + r;
     if (t >= T) break;
-    float v[EPT];
-    int id[EPT];
+    float v[NJ];
+    int id[NJ];
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = tx + 32 * j;
-      v[j] = Ls[r * EP + e];
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < EP) ? Ls[r * EP + e] : -INFINITY;
       id[j] = (e < E) ? e : 0x7fffffff;
     }
-    warp_select_and_weigh<EPT>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+    warp_select_and_weigh<NJ>(v, id, k, pre_k, router, t, topk_idx, topk_w);
   }
+}
+
+template <typename Tin, int TM, int TE, int NTT, int KG, bool VW>
+cudaError_t launch_tiled_v(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
+                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           float* logits, cudaStream_t s) {
+  constexpr int NTE = 256 / KG / NTT;
+  constexpr int BT = NTT * TM, EP = NTE * TE;
+  constexpr size_t smem_k = static_cast<size_t>(KG) * kTileBK * (BT + EP) * sizeof(float);
+  constexpr size_t smem_l = static_cast<size_t>(KG) * BT * EP * sizeof(float);
+  constexpr size_t smem = smem_k > smem_l ? smem_k : smem_l;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(route_tiled_kernel<Tin, TM, TE, NTT, KG, VW>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  route_tiled_kernel<Tin, TM, TE, NTT, KG, VW><<<ceil_div(T, BT), 256, smem, s>>>(
+      x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits);
+  return cudaGetLastError();
+}
+
+// W_g rows are read as 16-byte vectors only when every row starts 16-byte
+// aligned (aligned base and E * sizeof(Tin) a multiple of 16).
+template <typename Tin, int TM, int TE, int NTT, int KG = 1>
+cudaError_t launch_tiled(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
+                         int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                         float* logits, cudaStream_t s) {
+  const bool vw = (reinterpret_cast<uintptr_t>(Wg) % 16 == 0) &&
+                  ((static_cast<size_t>(E) * sizeof(Tin)) % 16 == 0);
+  if (vw)
+    return launch_tiled_v<Tin, TM, TE, NTT, KG, true>(x, Wg, bias, T, d, E, k, pre_k, router,
+                                                      topk_idx, topk_w, logits, s);
+  return launch_tiled_v<Tin, TM, TE, NTT, KG, false>(x, Wg, bias, T, d, E, k, pre_k, router,
+                                                     topk_idx, topk_w, logits, s);
 }
 
 template <typename Tin>
@@ -303,6 +433,14 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
                            int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
                            float* logits, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  if (E <= 32 && T >= 4096) {
+    // 64 tokens per CTA, K split over 4 groups of 64 threads
+    if (E <= 16)
+      return launch_tiled<Tin, 4, 4, 16, 4>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx,
+                                            topk_w, logits, s);   // 64 tokens x 16 experts
+    return launch_tiled<Tin, 4, 4, 16, 2>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx,
+                                          topk_w, logits, s);     // 64 tokens x 32 experts
+  }
   if (E <= 32) {
     const bool vw = (reinterpret_cast<uintptr_t>(Wg) % 16 == 0) &&
                     ((E * static_cast<int>(sizeof(Tin))) % 16 == 0);
@@ -327,18 +465,15 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
     }
 #undef MOE_NARROW_E
 #undef MOE_NARROW
+  } else if (E <= 64) {
+    return launch_tiled<Tin, 4, 2, 8>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w,
+                                      logits, s);   // 32 tokens x 64 experts
+  } else if (E <= 128) {
+    return launch_tiled<Tin, 4, 4, 8>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w,
+                                      logits, s);   // 32 tokens x 128 experts
   } else {
-    const dim3 grid(ceil_div(T, kWideTokens)), block(256);
-#define MOE_WIDE(EPT)                                                                        \
-  route_wide_kernel<Tin, EPT><<<grid, block, 0, s>>>(x, Wg, bias, T, d, E, k, pre_k, router, \
-                                                     topk_idx, topk_w, logits)
-    if (E <= 64)
-      MOE_WIDE(2);
-    else if (E <= 128)
-      MOE_WIDE(4);
-    else
-      MOE_WIDE(8);
-#undef MOE_WIDE
+    return launch_tiled<Tin, 4, 8, 8>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w,
+                                      logits, s);   // 32 tokens x 256 experts
   }
   return cudaGetLastError();
 }
