@@ -25,10 +25,18 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---------------------------------------------------------------- route.cu
-// Gate GEMM + softmax + top-k, fused. `dtype` 0 = fp32, 1 = bf16.
+// Gate GEMM + softmax + top-k, fused. `dtype` 0 = fp32, 1 = bf16. `err`
+// (nullable) receives kErrTimeout from the tensor-core gate.
 cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* bias, int T,
                          int d, int E, int k, int pre_k, int router, int32_t* topk_idx,
-                         float* topk_w, float* logits, cudaStream_t s);
+                         float* topk_w, float* logits, uint32_t* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- gate_tc.cu
+// Tensor-core gate (bf16, E a multiple of 64 up to 256, 16-byte aligned x, W_g).
+bool gate_tc_supported(int dtype, int E, const void* Wg, const void* x);
+cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int T, int d, int E,
+                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           float* logits, uint32_t* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- dispatch.cu
 // Zero counts[E] and offsets[E+1] (empty batch).

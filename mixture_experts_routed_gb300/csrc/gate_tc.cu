@@ -1,0 +1,315 @@
+// gate_tc.cu - gate projection and router on the tensor cores, for bf16
+// layers with E a multiple of 64 (DeepSeek-V4 EP article, sections 2.1 and
+// 3.2): L = x W_g + b, then the same warp top-k and weights as route.cu.
+//
+// The gate is a GEMM of T x d by d x E (60 GFLOP for 16384 tokens, d = 7168,
+// E = 256), too much for fp32 FMA, but fp32 accumulation inside tcgen05 over
+// K = 7168 drifts up to 4e-5 from fp64 (measured on GB300), past the 1e-5
+// logit / 1e-6 weight bounds. So the MMA accumulator restarts every 128 K
+// (two 64-wide k-blocks) and the CUDA cores add each 128-long partial into
+// fp32 totals: measured error then 1.7e-6 max, 1.8e-7 RMS at K = 7168.
+//
+// CTA = 128 tokens x E experts (tcgen05.mma.cta_group::1 M128 N=E K16), one
+// CTA per 128 tokens:
+//   warp 0     TMA producer: x [128 tokens][64 k] (K-major) and W_g
+//              [64 k][E] as E/64 boxes of 64 experts (MN-major), 128-byte
+//              swizzle, 4-stage ring
+//   warp 1     TMEM allocation + MMA issue; commits a chunk to one of two
+//              E-column accumulators
+//   warps 2-9  epilogue: warp (half, q) adds TMEM lanes 32q..32q+31, columns
+//              of its half, into register totals after every chunk
+// then all warps meet, write logits (+ bias) to shared memory over the ring,
+// and select / weigh tokens with the warp top-k. Every wait is bounded.
+#include <cfloat>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace moe {
+
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = 128, BK = 64, STAGES = 4, CHUNK_KB = 2;
+constexpr int X_BYTES = BM * BK * 2;     // 16 KB
+constexpr int BOX_BYTES = BK * 64 * 2;   // 8 KB: [64 k][64 experts]
+constexpr int MAX_E = 256;
+constexpr int STAGE_BYTES = X_BYTES + (MAX_E / 64) * BOX_BYTES;  // 48 KB
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], drain
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+// The logits tile is [BM][E + 1] (padded: row-strided writes hit distinct banks).
+static_assert(BM * (MAX_E + 1) * 4 <= OFF_BAR, "logits tile must fit over the stage ring");
+
+// The epilogue keeps E/2 totals per thread (a compile-time bound, HALF).
+template <int HALF>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                   const float* __restrict__ bias, int T, int d, int E, int k, int pre_k,
+                   int router, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                   float* __restrict__ logits, uint32_t* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  float* Ls = reinterpret_cast<float*>(smem);  // [BM][E + 1] after the main loop
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * BM;
+  const int nwbox = E / 64;
+  const uint32_t stage_bytes = static_cast<uint32_t>(X_BYTES + nwbox * BOX_BYTES);
+  const int KB = d / BK;
+  const int nchunk = (KB + CHUNK_KB - 1) / CHUNK_KB;
+  // TMEM: two accumulators of E columns, allocation rounded up to a power of 2
+  const uint32_t tmem_cols = E <= 64 ? 128u : (E <= 128 ? 256u : 512u);
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], NUM_EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  } else if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  bool timed_out = false;
+
+  float tot[HALF];
+#pragma unroll
+  for (int j = 0; j < HALF; ++j) tot[j] = 0.f;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmX);
+      prefetch_tmap(&tmW);
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        uint8_t* st = smem + s * STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        tma_load_2d(st, &tmX, &full[s], kb * BK, t0);
+        for (int c = 0; c < nwbox; ++c)
+          tma_load_2d(st + X_BYTES + c * BOX_BYTES, &tmW, &full[s], c * 64, kb * BK);
+        armed |= 1u << s;
+        armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      for (int i = 0; i < STAGES; ++i)
+        if ((armed >> i) & 1u)
+          if (!mbar_wait(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_bf16_f32(BM, E, /*A MN*/ false, /*B MN*/ true);
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool issued = false;
+      for (int c = 0; c < nchunk && !timed_out; ++c) {
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * E);
+        const int kb_end = min(KB, (c + 1) * CHUNK_KB);
+        for (int kb = c * CHUNK_KB; kb < kb_end; ++kb) {
+          if (!mbar_wait(&full[s], ph, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t b_base = a_base + X_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_f16(d_tmem, make_sdesc_sw128(a_base + kk * 32, 16, 1024),
+                       make_sdesc_sw128(b_base + kk * 2048, BOX_BYTES, 1024), idesc,
+                       (kb != c * CHUNK_KB || kk != 0) ? 1u : 0u);
+          issued = true;
+          tc_commit(&empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (timed_out) break;
+        tc_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (timed_out && issued) {  // MMAs in flight finish before TMEM is freed
+        tc_commit(drain);
+        mbar_wait(drain, 0, kWaitLimitNs);
+      }
+    }
+  } else {
+    // epilogue: columns [half * E/2, half * E/2 + E/2) of lanes 32q..32q+31
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int ncol = E / 2;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int c = 0; c < nchunk; ++c) {
+      const bool ok = mbar_wait(&tfull[acc], aph, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok)) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * E + half * ncol) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll
+      for (int cc = 0; cc < HALF / 32; ++cc) {
+        if (cc * 32 < ncol) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + cc * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tot[cc * 32 + j] += __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  if (timed_out && err != nullptr) atomicOr(err, kErrTimeout);
+  __syncthreads();  // the ring is idle: reuse it for the logits tile
+  if (warp >= 2) {
+    const int q = warp & 3, half = (warp - 2) >> 2, ncol = E / 2;
+    const int r = q * 32 + lane;
+#pragma unroll
+    for (int j = 0; j < HALF; ++j) {
+      if (j < ncol) {
+        const int e = half * ncol + j;
+        const float val = tot[j] + (bias ? __ldg(bias + e) : 0.f);
+        Ls[r * (E + 1) + e] = val;
+        if (logits && t0 + r < T) logits[static_cast<size_t>(t0 + r) * E + e] = val;
+      }
+    }
+  }
+  __syncthreads();
+  // every warp selects and weighs tokens warp, warp + 10, ...
+  constexpr int NJ = MAX_E / 32;
+  for (int r = warp; r < BM; r += NUM_THREADS / 32) {
+    const int t = t0 + r;
+    if (t >= T) break;
+    float v[NJ];
+    int id[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = e < E ? Ls[r * (E + 1) + e] : -INFINITY;
+      id[j] = e < E ? e : 0x7fffffff;
+    }
+    topk::warp_select_and_weigh<NJ>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+std::once_flag g_enc_once;
+
+bool map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+            uint32_t box_rows) {
+  std::call_once(g_enc_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HALF>
+cudaError_t launch_half(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int T,
+                        int d, int E, int k, int pre_k, int router, int32_t* idx, float* w,
+                        float* logits, uint32_t* err, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t st = cudaSuccess;
+  std::call_once(once, [] {
+    st = cudaFuncSetAttribute(gate_tc_kernel<HALF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SMEM_BYTES);
+  });
+  if (st != cudaSuccess) return st;
+  gate_tc_kernel<HALF><<<ceil_div(T, BM), NUM_THREADS, SMEM_BYTES, s>>>(
+      mx, mw, bias, T, d, E, k, pre_k, router, idx, w, logits, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gate_tc_supported(int dtype, int E, const void* Wg, const void* x) {
+  return dtype == 1 && E >= 64 && E <= MAX_E && E % 64 == 0 &&
+         reinterpret_cast<uintptr_t>(Wg) % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
+}
+
+cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int T, int d, int E,
+                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           float* logits, uint32_t* err, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  CUtensorMap mx, mw;
+  std::memset(&mx, 0, sizeof(mx));
+  std::memset(&mw, 0, sizeof(mw));
+  if (!map_2d(&mx, x, static_cast<uint64_t>(T), static_cast<uint64_t>(d), 64, BM))
+    return cudaErrorInvalidValue;
+  if (!map_2d(&mw, Wg, static_cast<uint64_t>(d), static_cast<uint64_t>(E), 64, BK))
+    return cudaErrorInvalidValue;
+  if (E <= 64)
+    return launch_half<32>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+                           err, s);
+  return launch_half<128>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+                          err, s);
+}
+
+}  // namespace moe

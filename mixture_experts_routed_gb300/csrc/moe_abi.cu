@@ -99,9 +99,9 @@ void record(void* const* ev, int i, cudaStream_t s) {
 
 // ---------------------------------------------------------------- stages
 int run_route(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
-              int32_t* idx, float* w, float* logits, cudaStream_t s) {
+              int32_t* idx, float* w, float* logits, uint32_t* err, cudaStream_t s) {
   return status_of(launch_route(c.dtype, x, Wg, bias, c.T, c.d, c.E, c.k, c.pre_k, c.router,
-                                idx, w, logits, s));
+                                idx, w, logits, err, s));
 }
 
 int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x,
@@ -185,7 +185,8 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
   float* y = at<float>(ws, L.y);
 
   record(events, 0, s);
-  if ((st = run_route(c, x, Wg, bias, idx, w, nullptr, s)) != MOE_OK) return st;
+  if ((st = run_route(c, x, Wg, bias, idx, w, nullptr, at<uint32_t>(ws, L.err), s)) != MOE_OK)
+    return st;
   record(events, 1, s);
   if ((st = run_dispatch(c, L, ws, x, idx, counts, offsets, pos, src, x_perm, x_scale, s)) !=
       MOE_OK)
@@ -230,7 +231,7 @@ int moe_route(const moe_config_t* cfg, const void* x, const void* W_g, const flo
   if (cfg->T == 0) return MOE_OK;
   if (!ok_ptr(x) || W_g == nullptr || topk_idx == nullptr || topk_w == nullptr)
     return MOE_ERR_INVALID_ARG;
-  return run_route(*cfg, x, W_g, bias, topk_idx, topk_w, logits, as_stream(stream));
+  return run_route(*cfg, x, W_g, bias, topk_idx, topk_w, logits, nullptr, as_stream(stream));
 }
 
 int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,

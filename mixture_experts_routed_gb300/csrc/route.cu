@@ -23,82 +23,15 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kRouterRenorm = 0;
+using topk::warp_select_and_weigh;
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
-
-// Ranking rule: a beats b if a has the larger logit, or equal logits and the
-// lower expert id.
-__device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// Each lane holds NJ (logit, expert id) pairs; padding uses -inf and an id
-// >= E. Selects the top pre_k (or k, for renorm) by repeated warp argmax and
-// writes slots j < k of token t.
-template <int NJ>
-__device__ __forceinline__ void warp_select_and_weigh(const float (&v)[NJ], const int (&id)[NJ],
-                                                      int k, int pre_k, int router, int t,
-                                                      int32_t* __restrict__ topk_idx,
-                                                      float* __restrict__ topk_w) {
-  const int lane = threadIdx.x & 31;
-  bool taken[NJ];
-#pragma unroll
-  for (int j = 0; j < NJ; ++j) taken[j] = false;
-  float sel_v[kMaxTopK];
-  int sel_i[kMaxTopK];
-  const int rounds = (router == kRouterRenorm) ? k : pre_k;
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    sel_v[s] = -FLT_MAX;
-    sel_i[s] = 0x7fffffff;
-    if (s < rounds) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if (!taken[j] && beats(v[j], id[j], bv, bi)) {
-          bv = v[j];
-          bi = id[j];
-        }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (beats(ov, oi, bv, bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      sel_v[s] = bv;
-      sel_i[s] = bi;
-#pragma unroll
-      for (int j = 0; j < NJ; ++j)
-        if (id[j] == bi) taken[j] = true;
-    }
-  }
-  // weights: max-subtracted exponentials of the chosen logits
-  const float m = sel_v[0];
-  float den = 0.f;
-  float ex[kMaxTopK];
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    ex[s] = (s < rounds) ? expf(sel_v[s] - m) : 0.f;
-    den += ex[s];
-  }
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    if (s < k && lane == s) {
-      topk_idx[static_cast<size_t>(t) * k + s] = sel_i[s];
-      topk_w[static_cast<size_t>(t) * k + s] = ex[s] / den;
-    }
-  }
-}
 
 // ---------------------------------------------------------------- narrow
 // E <= 32. A CTA of 4 warps handles TPB tokens; its 128 threads stride the
@@ -482,7 +415,10 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* bias, int T,
                          int d, int E, int k, int pre_k, int router, int32_t* topk_idx,
-                         float* topk_w, float* logits, cudaStream_t s) {
+                         float* topk_w, float* logits, uint32_t* err, cudaStream_t s) {
+  if (T > 0 && gate_tc_supported(dtype, E, Wg, x))
+    return launch_gate_tc(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits, err,
+                          s);
   if (dtype == 0)
     return launch_route_t<float>(static_cast<const float*>(x), static_cast<const float*>(Wg),
                                  bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits, s);

@@ -44,6 +44,16 @@ SMALL = {
     "skew_T256_d128_E64_k8_f128_zipf": MoEConfig("skew_T256_d128_E64_k8_f128_zipf", T=256,
                                                  d=128, E=64, k=8, f=128, dtype="bf16",
                                                  bias="zipf", zipf_s=3.0, seed=21),
+    # tensor-core gate: E = 192 (half-width column offset 96), a 1-block last
+    # K chunk (d = 320), 3 token tiles with a 44-token tail
+    "gate_E192_T300_d320_k4_f128": MoEConfig("gate_E192_T300_d320_k4_f128", T=300, d=320,
+                                             E=192, k=4, f=128, dtype="bf16", bias="normal",
+                                             bias_var=1.0, seed=22),
+    "gate_E256_T130_d192_k8_f128": MoEConfig("gate_E256_T130_d192_k8_f128", T=130, d=192,
+                                             E=256, k=8, f=128, dtype="bf16", seed=23),
+    "gate_E128_T1_d1024_k2_f128_prek": MoEConfig("gate_E128_T1_d1024_k2_f128_prek", T=1,
+                                                 d=1024, E=128, k=2, f=128, dtype="bf16",
+                                                 router=ROUTER_PREK_SOFTMAX, seed=24),
 }
 ALL = dict(SMALL)
 ALL.update(CONFIGS)
