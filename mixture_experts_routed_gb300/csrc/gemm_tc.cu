@@ -26,13 +26,17 @@
 // section 5.2, makes every weight tile one strided TMA box).
 //
 // Shared memory per CTA: a 6-stage ring of 32 KB (16 KB token rows, 16 KB
-// weight half, 128-byte swizzle). Warp roles: warp 0 TMA producer (one
-// thread, both CTAs); warp 1 TMEM allocation (both CTAs) and MMA issue (even
-// CTA); warps 2-5 epilogue (tcgen05.ld 32 columns at a time, FP8 row scale
-// and SiLU or fp32 store, rows past the segment masked). Every wait is
-// bounded; a timeout sets kErrTimeout and the kernel drains its copies and
-// MMAs, frees TMEM and exits.
+// weight half, 128-byte swizzle) for 256-feature tiles, or 4 stages of 48 KB
+// for 512-feature tiles (two MMAs per k-step sharing the token operand, used
+// for long-K SiLU passes with many tiles). Warp roles: warp 0 TMA producer
+// (one thread, both CTAs); warp 1 TMEM allocation (both CTAs) and MMA issue
+// (even CTA); warps 2.. epilogue, 8 for the SiLU pass (two per TMEM lane
+// quadrant, each half the columns) and 4 for the fp32 pass (tcgen05.ld 32
+// columns at a time, FP8 row scale and SiLU or fp32 store, rows past the
+// segment masked). Every wait is bounded; a timeout sets kErrTimeout and the
+// kernel drains its copies and MMAs, frees TMEM and exits.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -56,7 +60,10 @@ struct TcParams {
   int E, K, N, R, n_tiles;
 };
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+// z * sigmoid(z) with the approximate divide: the result is rounded to bf16,
+// far coarser than the few-ulp error of __expf / __fdividef. For z < -87 the
+// denominator passes 2^126 and the quotient flushes to 0 (|silu| < 1e-36).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // ---------------------------------------------------------------- pair kernel
 // Synchronisation across the pair:
@@ -65,31 +72,51 @@ __device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); 
 //             barrier (the cta_group::2 form of the tensor copy);
 //   empty[s]  both CTAs, from one multicast tcgen05.commit;
 //   tfull     both CTAs, multicast commit after a tile's last MMA;
-//   tempty    (even CTA) 4 local + 4 remote epilogue-warp arrives.
+//   tempty    (even CTA) one arrive per epilogue warp of either CTA.
 namespace pairk {
-constexpr int BM = 256, BN = 256, BK = 64, STAGES = 6;
+constexpr int BM = 256, BK = 64;
 constexpr int A_BYTES = 128 * BK * 2;       // 16 KB: this CTA's 128 rows
 constexpr int BOX_BYTES = BK * 64 * 2;      // 8 KB: [64 k][64 n]
-constexpr int B_BYTES = 2 * BOX_BYTES;      // 16 KB: this CTA's 128 features
-constexpr int B_SLOT = B_BYTES;
-constexpr int STAGE_BYTES = A_BYTES + B_SLOT;
-constexpr int ACC_COLS = BN;                // 128 lanes x 256 fp32 columns
-constexpr int NUM_ACC = 2;
-constexpr int TMEM_COLS = ACC_COLS * NUM_ACC;
-constexpr int NUM_THREADS = 192;
-constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
-constexpr int OFF_A = 0;
-constexpr int OFF_B = STAGES * A_BYTES;
-constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;  // full, empty, tfull, tempty, drain
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_SEG = OFF_MISC + 16;
-constexpr int OFF_TSTART = OFF_SEG + (kMaxExperts + 1) * 4;
-constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;
+constexpr int HALF_B_BYTES = 2 * BOX_BYTES; // 16 KB: this CTA's 128 features of one MMA
+constexpr int TMEM_COLS = 512;
+// Epilogue warps: 8 for the SiLU pass (two per TMEM lane quadrant, each half
+// the columns: the exp/divide work is issue-bound at one warp per SM
+// sub-partition), 4 for the fp32 pass (plain stores; more warps only add
+// store bursts against the operand loads, measured slower on GB300).
+template <int EPI>
+constexpr int num_epi_warps() { return EPI == 0 ? 8 : 4; }
+template <int EPI>
+constexpr int num_threads() { return 64 + 32 * num_epi_warps<EPI>(); }
+constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*B MN-major*/ true);
+
+// NB = 1: 256-feature pair tiles, two TMEM accumulators (the epilogue of one
+// tile overlaps the next tile's main loop), 6 stages of 32 KB.
+// NB = 2: 512-feature pair tiles, two M256 N256 MMAs per k-step sharing the
+// token operand, one accumulator filling TMEM, 4 stages of 48 KB: a third
+// fewer operand bytes per flop through L2 and shared memory, the epilogue
+// exposed once per tile.
+template <int NB>
+struct Shape {
+  static constexpr int BN = 256 * NB;
+  static constexpr int STAGES = NB == 1 ? 6 : 4;
+  static constexpr int B_BYTES = NB * HALF_B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NUM_ACC = 2 / NB;
+  static constexpr int ACC_COLS = TMEM_COLS / NUM_ACC;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;  // full, empty, tfull, tempty, drain
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_SEG = OFF_MISC + 16;
+  static constexpr int OFF_TSTART = OFF_SEG + (kMaxExperts + 1) * 4;
+  static constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
 
 struct PTile {
-  int e, row0, ntok, n0;  // token rows [row0, row0 + ntok), features n0..n0+255
+  int e, row0, ntok, n0;  // token rows [row0, row0 + ntok), features from n0
   bool swap;              // tail tile: weights are the MMA's M side, tokens its N
 };
 
@@ -97,7 +124,7 @@ struct PTile {
 // remainder (1..255 rows), one swapped tile whose MMA N is the remainder
 // rounded up to 16, so a short tail costs a fraction of a full tile.
 __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* seg, int E,
-                                        int n_tiles) {
+                                        int n_tiles, int bn) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -116,29 +143,32 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
   t.row0 = seg[lo] + m * BM;
   t.swap = m == full;
   t.ntok = t.swap ? rem : BM;
-  t.n0 = nt * BN;
+  t.n0 = nt * bn;
   return t;
 }
 }  // namespace pairk
 
-template <int EPI>
-__global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
+template <int EPI, int NB>
+__global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  using S = pairk::Shape<NB>;
+  constexpr int NEW = pairk::num_epi_warps<EPI>();
+  constexpr int NH = NEW / 4;  // warps per TMEM lane quadrant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem + pairk::OFF_A;
-  uint8_t* sB = smem + pairk::OFF_B;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + pairk::OFF_BAR);
-  uint64_t* empty = full + pairk::STAGES;
-  uint64_t* tfull = empty + pairk::STAGES;
-  uint64_t* tempty = tfull + pairk::NUM_ACC;
-  uint64_t* drain = tempty + pairk::NUM_ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + pairk::OFF_MISC);
-  int* s_total = reinterpret_cast<int*>(smem + pairk::OFF_MISC + 4);
-  int* seg = reinterpret_cast<int*>(smem + pairk::OFF_SEG);
-  int* tstart = reinterpret_cast<int*>(smem + pairk::OFF_TSTART);
+  uint8_t* sA = smem + S::OFF_A;
+  uint8_t* sB = smem + S::OFF_B;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
+  uint64_t* empty = full + S::STAGES;
+  uint64_t* tfull = empty + S::STAGES;
+  uint64_t* tempty = tfull + S::NUM_ACC;
+  uint64_t* drain = tempty + S::NUM_ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::OFF_MISC);
+  int* s_total = reinterpret_cast<int*>(smem + S::OFF_MISC + 4);
+  int* seg = reinterpret_cast<int*>(smem + S::OFF_SEG);
+  int* tstart = reinterpret_cast<int*>(smem + S::OFF_TSTART);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -173,13 +203,13 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
       tstart[E] = running;
       *s_total = ok ? running : 0;
       if (!ok && blockIdx.x == 0) atomicOr(p.err, kErrBadIndex);
-      for (int i = 0; i < pairk::STAGES; ++i) {
+      for (int i = 0; i < S::STAGES; ++i) {
         mbar_init(&full[i], 1);
         mbar_init(&empty[i], 1);
       }
-      for (int i = 0; i < pairk::NUM_ACC; ++i) {
+      for (int i = 0; i < S::NUM_ACC; ++i) {
         mbar_init(&tfull[i], 1);
-        mbar_init(&tempty[i], 8);  // 4 epilogue warps in each CTA of the pair
+        mbar_init(&tempty[i], 2 * NEW);  // epilogue warps of both CTAs
       }
       mbar_init(drain, 1);
       fence_mbar_init();
@@ -206,15 +236,23 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
       // both CTAs' bytes of a stage are counted on the even CTA's full[s]
       const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
       for (int tile = pair; tile < total && !timed_out; tile += npairs) {
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
         // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
         const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
         const int my_row = min(t.row0 + static_cast<int>(rank) * half_rows, p.R - 1);
-        const int my_n0 = t.n0 + static_cast<int>(rank) * 128;
-        const int nbox = my_n0 < p.N ? min(2, (p.N - my_n0) / 64) : 0;
-        const int n1 = t.n0 + 128;
-        const int nbox_pair = min(2, (p.N - t.n0) / 64) + (n1 < p.N ? min(2, (p.N - n1) / 64) : 0);
-        const uint32_t bytes = static_cast<uint32_t>(2 * pairk::A_BYTES + nbox_pair * pairk::BOX_BYTES);
+        // MMA j covers features n0 + 256 j + [0, 256); this CTA holds the
+        // 128 at n0 + 256 j + 128 rank (whole 64-wide boxes only: N % 64 == 0)
+        int nbox[NB];
+        uint32_t bytes = 2 * pairk::A_BYTES;
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+          const int my_n0 = t.n0 + j * 256 + static_cast<int>(rank) * 128;
+          nbox[j] = my_n0 < p.N ? min(2, (p.N - my_n0) / 64) : 0;
+          const int m0 = t.n0 + j * 256, m1 = m0 + 128;
+          const int pair_boxes = (m0 < p.N ? min(2, (p.N - m0) / 64) : 0) +
+                                 (m1 < p.N ? min(2, (p.N - m1) / 64) : 0);
+          bytes += static_cast<uint32_t>(pair_boxes * pairk::BOX_BYTES);
+        }
         const int brow = t.e * p.K;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
@@ -224,12 +262,15 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
           const uint32_t bar = leader_full + static_cast<uint32_t>(s * 8);
           tma_load_2d_pair(sA + s * pairk::A_BYTES, &tmA, bar, kb * pairk::BK, my_row);
-          for (int c = 0; c < nbox; ++c)
-            tma_load_2d_pair(sB + s * pairk::B_SLOT + c * pairk::BOX_BYTES, &tmB, bar,
-                             my_n0 + c * 64, brow + kb * pairk::BK);
+#pragma unroll
+          for (int j = 0; j < NB; ++j)
+            for (int c = 0; c < nbox[j]; ++c)
+              tma_load_2d_pair(sB + s * S::B_BYTES + j * pairk::HALF_B_BYTES + c * pairk::BOX_BYTES,
+                               &tmB, bar, t.n0 + j * 256 + static_cast<int>(rank) * 128 + c * 64,
+                               brow + kb * pairk::BK);
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == pairk::STAGES) {
+          if (++s == S::STAGES) {
             s = 0;
             ph ^= 1u;
           }
@@ -237,7 +278,7 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
       }
       // drain (even CTA: its full[s] also counts the odd CTA's bytes)
       if (rank == 0)
-        for (int i = 0; i < pairk::STAGES; ++i)
+        for (int i = 0; i < S::STAGES; ++i)
           if ((armed >> i) & 1u)
             if (!mbar_wait_spin(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
     }
@@ -253,8 +294,10 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * pairk::ACC_COLS);
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
+        // MMAs with any feature below N (the rest of a last tile is skipped)
+        const int nmma = min(NB, (p.N - t.n0 + 255) / 256);
         // swapped tile: A = weights (MN-major, the B slot), B = tokens (K-major, the A slot)
         const uint32_t idesc =
             t.swap ? make_idesc_bf16_f32(pairk::BM, (t.ntok + 15) & ~15, true, false) : pairk::IDESC;
@@ -265,24 +308,29 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + s * pairk::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + s * pairk::B_SLOT);
+          const uint32_t b_base = smem_u32(sB + s * S::B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < pairk::BK / 16; ++kk) {
             const uint64_t tok = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
-            const uint64_t wt = make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024);
-            tc_mma_f16_pair(d_tmem, t.swap ? wt : tok, t.swap ? tok : wt, idesc,
-                            (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              if (j >= nmma) break;
+              const uint64_t wt = make_sdesc_sw128(b_base + j * pairk::HALF_B_BYTES + kk * 2048,
+                                                   pairk::BOX_BYTES, 1024);
+              tc_mma_f16_pair(d_tmem + j * 256, t.swap ? wt : tok, t.swap ? tok : wt, idesc,
+                              (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           issued = true;
           tc_commit_pair_mc(&empty[s], 0x3);
-          if (++s == pairk::STAGES) {
+          if (++s == S::STAGES) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (timed_out) break;
         tc_commit_pair_mc(&tfull[acc], 0x3);
-        if (++acc == pairk::NUM_ACC) {
+        if (++acc == S::NUM_ACC) {
           acc = 0;
           aph ^= 1u;
         }
@@ -294,29 +342,33 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
+    // warp w reads TMEM lanes 32 (w % 4) .. +31; with 8 warps, warps 2-5
+    // take the first half of the accumulator columns, warps 6-9 the second
     const int q = warp & 3;
+    const int hh = (warp - 2) >> 2;
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = pair; tile < total; tile += npairs) {
-      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles);
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
       const bool ok = mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) {
         timed_out = true;
         break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * pairk::ACC_COLS) +
+      const uint32_t tbase = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS) +
                              (static_cast<uint32_t>(q * 32) << 16);
       if (!t.swap) {
-        // lane = token row of this CTA, columns = the tile's 256 features
+        // lane = token row of this CTA, columns = the tile's features (MMA j
+        // at TMEM columns 256 j)
         const int r = static_cast<int>(rank) * 128 + q * 32 + lane;
         const bool valid = r < t.ntok && t.row0 + r < p.R;
         const size_t grow = static_cast<size_t>(t.row0) + r;
         float scale = 1.f;
         if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
 #pragma unroll 1
-        for (int c = 0; c < pairk::BN / 32; ++c) {
+        for (int c = hh * (S::BN / 32 / NH); c < (hh + 1) * (S::BN / 32 / NH); ++c) {
           const int col = t.n0 + c * 32;
           if (col >= p.N) break;
           uint32_t v[32];
@@ -348,13 +400,17 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
           }
         }
       } else {
-        // lane = output feature of this CTA's half, columns = the tail's tokens
-        const int f = t.n0 + static_cast<int>(rank) * 128 + q * 32 + lane;
-        const bool f_ok = f < p.N;
+        // lane = output feature (MMA j's M row 128 rank + 32 q + lane),
+        // columns = the tail's tokens; the (MMA, 32-token chunk) pieces are
+        // dealt round-robin to the warps of a lane quadrant
+        const int nch = (t.ntok + 31) / 32;
 #pragma unroll 1
-        for (int c = 0; c * 32 < t.ntok; ++c) {
+        for (int i = hh; i < NB * nch; i += NH) {
+          const int j = i / nch, c = i - j * nch;
+          const int f = t.n0 + j * 256 + static_cast<int>(rank) * 128 + q * 32 + lane;
+          const bool f_ok = f < p.N;
           uint32_t v[32];
-          tmem_ld_32x32b_x32(tbase + c * 32, v);
+          tmem_ld_32x32b_x32(tbase + j * 256 + c * 32, v);
           tmem_ld_wait();
           const int tok0 = c * 32;
           const int nt = min(32, t.ntok - tok0);
@@ -365,17 +421,17 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
           if constexpr (EPI == 0) {
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float sj = __shfl_sync(0xffffffffu, my_scale, j);
-              if (j < nt && f_ok)
-                out[static_cast<size_t>(j) * p.N] =
-                    __float2bfloat16_rn(silu(__uint_as_float(v[j]) * sj));
+            for (int jj = 0; jj < 32; ++jj) {
+              const float sj = __shfl_sync(0xffffffffu, my_scale, jj);
+              if (jj < nt && f_ok)
+                out[static_cast<size_t>(jj) * p.N] =
+                    __float2bfloat16_rn(silu(__uint_as_float(v[jj]) * sj));
             }
           } else {
             float* out = static_cast<float*>(p.out) + base;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nt && f_ok) out[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+            for (int jj = 0; jj < 32; ++jj)
+              if (jj < nt && f_ok) out[static_cast<size_t>(jj) * p.N] = __uint_as_float(v[jj]);
           }
         }
       }
@@ -387,7 +443,7 @@ __global__ void __launch_bounds__(pairk::NUM_THREADS, 1)
         else
           mbar_arrive_remote(leader_tempty + static_cast<uint32_t>(acc * 8));
       }
-      if (++acc == pairk::NUM_ACC) {
+      if (++acc == S::NUM_ACC) {
         acc = 0;
         aph ^= 1u;
       }
@@ -436,36 +492,73 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI>
+template <int EPI, int NB>
 cudaError_t set_pair_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              pairk::SMEM_BYTES);
+    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              pairk::Shape<NB>::SMEM_BYTES);
   });
   return st;
 }
 
-// Clusters of two that can be resident at once for the pair kernel (cached
-// per device and epilogue).
-int resident_pairs(int epi, const cudaLaunchConfig_t& lc_in, int num_sms) {
-  static int cache[64][2] = {};
+// Clusters of two that can be resident at once (cached per device and kernel).
+template <int EPI, int NB>
+int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
+  static int cache[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
-  if (cache[dev][epi] > 0) return cache[dev][epi];
+  if (cache[dev] > 0) return cache[dev];
   cudaLaunchConfig_t lc = lc_in;
   lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
   int n = 0;
-  const cudaError_t e =
-      epi == 0 ? cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<0>, &lc)
-               : cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<1>, &lc);
-  if (e != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB>, &lc) != cudaSuccess ||
+      n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
   }
-  cache[dev][epi] = n;
+  cache[dev] = n;
   return n;
+}
+
+template <int EPI, int NB>
+cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, TcParams prm, int num_sms,
+                        cudaStream_t s) {
+  using S = pairk::Shape<NB>;
+  prm.n_tiles = ceil_div(prm.N, S::BN);
+  const long long max_pt = static_cast<long long>(ceil_div(prm.R, pairk::BM) + prm.E) *
+                           static_cast<long long>(prm.n_tiles);
+  cudaLaunchConfig_t lc = {};
+  lc.blockDim = dim3(pairk::num_threads<EPI>());
+  lc.dynamicSmemBytes = S::SMEM_BYTES;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t st = set_pair_smem_attr<EPI, NB>();
+  if (st != cudaSuccess) return st;
+  // a persistent grid must fit at once: as many pairs as can be resident
+  // together (a pair needs two free SMs of one GPC), not num_sms / 2
+  const int resident = resident_pairs<EPI, NB>(lc, num_sms);
+  const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
+  lc.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB>, mA, mB, prm);
+}
+
+// 512-feature tiles (one accumulator, epilogue exposed) pay off only for the
+// SiLU pass with a long main loop and many tiles per pair (measured on
+// GB300: the 16384-token d = 7168 E = 256 layer's W1 pass 8 % faster; every
+// shorter or fp32-output pass slower).
+int pick_nb(int epi, int R, int E, int K, int N, int num_sms) {
+  if (epi != 0 || K < 4096 || N < 512) return 1;
+  const long long tiles = static_cast<long long>(ceil_div(R, pairk::BM) + E) * ceil_div(N, 512);
+  return tiles >= 8LL * (num_sms / 2) ? 2 : 1;
 }
 
 }  // namespace
@@ -493,33 +586,18 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
   prm.K = K;
   prm.N = N;
   prm.R = R;
-  cudaError_t st;
-  {
-    // pair tiles of 256 rows x 256 features, one cluster of two CTAs per SM pair
-    prm.n_tiles = ceil_div(N, pairk::BN);
-    const long long max_pt =
-        static_cast<long long>(ceil_div(R, pairk::BM) + E) * static_cast<long long>(prm.n_tiles);
-    cudaLaunchConfig_t lc = {};
-    lc.blockDim = dim3(pairk::NUM_THREADS);
-    lc.dynamicSmemBytes = pairk::SMEM_BYTES;
-    lc.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    // a persistent grid must fit at once: as many pairs as can be resident
-    // together (a pair needs two free SMs of one GPC), not num_sms / 2
-    if ((st = epi == 0 ? set_pair_smem_attr<0>() : set_pair_smem_attr<1>()) != cudaSuccess)
-      return st;
-    const int resident = resident_pairs(epi, lc, num_sms);
-    const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
-    lc.gridDim = dim3(2 * pairs);
-    if (epi == 0) return cudaLaunchKernelEx(&lc, gemm_pair_kernel<0>, mA, mB, prm);
-    return cudaLaunchKernelEx(&lc, gemm_pair_kernel<1>, mA, mB, prm);
+  prm.n_tiles = 0;
+  int nb = pick_nb(epi, R, E, K, N, num_sms);
+  // MOE_GEMM_TILE_FEATURES=256|512 overrides the choice (read on every call)
+  if (const char* f = std::getenv("MOE_GEMM_TILE_FEATURES")) {
+    if (std::strcmp(f, "256") == 0) nb = 1;
+    if (std::strcmp(f, "512") == 0) nb = 2;
   }
+  if (epi == 0)
+    return nb == 2 ? launch_pair<0, 2>(mA, mB, prm, num_sms, s)
+                   : launch_pair<0, 1>(mA, mB, prm, num_sms, s);
+  return nb == 2 ? launch_pair<1, 2>(mA, mB, prm, num_sms, s)
+                 : launch_pair<1, 1>(mA, mB, prm, num_sms, s);
 }
 
 }  // namespace moe

@@ -54,6 +54,16 @@ SMALL = {
     "gate_E128_T1_d1024_k2_f128_prek": MoEConfig("gate_E128_T1_d1024_k2_f128_prek", T=1,
                                                  d=1024, E=128, k=2, f=128, dtype="bf16",
                                                  router=ROUTER_PREK_SOFTMAX, seed=24),
+    # 512-feature GEMM tiles (K >= 1024, N >= 512): 300 rows per expert = a full
+    # 256-row tile + a swapped 44-row tail; f = 1600 leaves a last feature
+    # block of 64 (one box, one of the two MMAs)
+    "wide_tile_T300_d1024_E2_k2_f1600": MoEConfig("wide_tile_T300_d1024_E2_k2_f1600", T=300,
+                                                  d=1024, E=2, k=2, f=1600, dtype="bf16",
+                                                  pre_k=2, seed=25),
+    "wide_tile_fp8_T520_d1024_E4_k1_f1024": MoEConfig("wide_tile_fp8_T520_d1024_E4_k1_f1024",
+                                                      T=520, d=1024, E=4, k=1, f=1024,
+                                                      dtype="bf16", pre_k=4, payload_fp8=True,
+                                                      seed=26),
 }
 ALL = dict(SMALL)
 ALL.update(CONFIGS)

@@ -124,3 +124,20 @@ def test_ffn_skips_empty_experts_and_flags_bad_offsets(cuda_ok):
     moe.expert_ffn(cfg, x_perm, x_scale, torch.from_numpy(bad).cuda(), inp["W1"], inp["W2"],
                    ws=ws, y_perm=y2)
     assert moe.get_device_error(ws) == moe.MOE_ERR_BAD_INDEX
+
+
+# both pair-tile widths on shapes whose default is the other one: 512-feature
+# tiles (two MMAs per k-step, one accumulator) on small layers with swapped
+# tails and ragged last feature blocks, 256-feature tiles on the one full
+# layer that defaults to 512
+WIDTH_CASES = [(n, w) for n in ("wide_tile_T300_d1024_E2_k2_f1600",
+                                "wide_tile_fp8_T520_d1024_E4_k1_f1024",
+                                "ragged_T129_d256_E8_k2_f320",
+                                "gate_E192_T300_d320_k4_f128") for w in ("512", "256")]
+WIDTH_CASES.append((FULL_NAMES[4], "256"))
+
+
+@pytest.mark.parametrize("name,width", WIDTH_CASES)
+def test_expert_ffn_tile_width(cuda_ok, monkeypatch, name, width):
+    monkeypatch.setenv("MOE_GEMM_TILE_FEATURES", width)
+    test_expert_ffn_parity(cuda_ok, name)
