@@ -84,9 +84,9 @@ constexpr int TMEM_COLS = 512;
 // sub-partition), 4 for the fp32 pass (plain stores; more warps only add
 // store bursts against the operand loads, measured slower on GB300).
 template <int EPI>
-constexpr int num_epi_warps() { return EPI == 0 ? 8 : 4; }
+__host__ __device__ constexpr int num_epi_warps() { return EPI == 0 ? 8 : 4; }
 template <int EPI>
-constexpr int num_threads() { return 64 + 32 * num_epi_warps<EPI>(); }
+__host__ __device__ constexpr int num_threads() { return 64 + 32 * num_epi_warps<EPI>(); }
 constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*B MN-major*/ true);
 
 // NB = 1: 256-feature pair tiles, two TMEM accumulators (the epilogue of one
