@@ -12,6 +12,11 @@ namespace moe {
 constexpr uint32_t kErrBadIndex = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 
+// Tile counters of the two expert GEMMs: 32-bit words of the workspace's
+// first 256-byte block (after the error word), zeroed before each layer.
+constexpr size_t kGemmCounterOffset = 64;
+constexpr int kNumGemmCounters = 2;
+
 // Bound on any device-side wait (mbarrier): 2 s of wall time.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
@@ -41,9 +46,11 @@ cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int
 // ---------------------------------------------------------------- dispatch.cu
 // Zero counts[E] and offsets[E+1] (empty batch).
 cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cudaStream_t s);
-// Per-chunk histograms -> hist[e * nchunk + c].
+// Per-chunk histograms -> hist[e * nchunk + c]; also zeroes `nzero` words
+// at `zero` (the GEMM tile counters) when non-null.
 cudaError_t launch_dispatch_count(const int32_t* topk_idx, int T, int k, int E, int nchunk,
-                                  int32_t* hist, uint32_t* err, cudaStream_t s);
+                                  int32_t* hist, uint32_t* err, uint32_t* zero, int nzero,
+                                  cudaStream_t s);
 // Per-expert exclusive scan over chunks -> base[e * nchunk + c], counts[e].
 cudaError_t launch_dispatch_scan(const int32_t* hist, int nchunk, int E, int32_t* base,
                                  int32_t* counts, cudaStream_t s);
@@ -63,10 +70,10 @@ cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const 
 // ---------------------------------------------------------------- gemm_tc.cu
 // Grouped GEMM over expert segments on tcgen05: out[r] = epi(A[r] . W[e]).
 // A [R, K] bf16, W [E, K, N] bf16, offsets [E+1]. epi 0: (row scale) -> SiLU
-// -> bf16 out; epi 1: fp32 out.
+// -> bf16 out; epi 1: fp32 out. `tile_ctr` must be zero at launch.
 cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, int K, int N,
                            const int32_t* offsets, const float* row_scale, void* out,
-                           uint32_t* err, int num_sms, cudaStream_t s);
+                           uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm_simt.cu
 // The same grouped GEMM in fp32 FMA for fp32 layers.

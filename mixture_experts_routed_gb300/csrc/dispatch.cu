@@ -39,9 +39,12 @@ __global__ void dispatch_empty_kernel(int E, int32_t* counts, int32_t* offsets) 
 __global__ void __launch_bounds__(128) dispatch_count_kernel(const int32_t* __restrict__ idx,
                                                              int T, int k, int E, int nchunk,
                                                              int32_t* __restrict__ hist,
-                                                             uint32_t* __restrict__ err) {
+                                                             uint32_t* __restrict__ err,
+                                                             uint32_t* __restrict__ zero,
+                                                             int nzero) {
   __shared__ int h[kMaxExperts];
   const int c = blockIdx.x;
+  if (zero != nullptr && c == 0 && static_cast<int>(threadIdx.x) < nzero) zero[threadIdx.x] = 0u;
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
   const long long i0 = static_cast<long long>(c) * kTPC * k;
@@ -301,8 +304,10 @@ cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cuda
 }
 
 cudaError_t launch_dispatch_count(const int32_t* topk_idx, int T, int k, int E, int nchunk,
-                                  int32_t* hist, uint32_t* err, cudaStream_t s) {
-  dispatch_count_kernel<<<nchunk, 128, 0, s>>>(topk_idx, T, k, E, nchunk, hist, err);
+                                  int32_t* hist, uint32_t* err, uint32_t* zero, int nzero,
+                                  cudaStream_t s) {
+  dispatch_count_kernel<<<nchunk, 128, 0, s>>>(topk_idx, T, k, E, nchunk, hist, err, zero,
+                                               nzero);
   return cudaGetLastError();
 }
 

@@ -99,7 +99,8 @@ extern "C" MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void*
   int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(base) + kNoAllocHeader);
   int32_t* tbase = hist + kNoAllocTableEntries;
   if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_LAUNCH;
-  cudaError_t e = launch_dispatch_count(topk_idx, cfg->T, cfg->k, cfg->E, nchunk, hist, err, s);
+  cudaError_t e = launch_dispatch_count(topk_idx, cfg->T, cfg->k, cfg->E, nchunk, hist, err,
+                                        nullptr, 0, s);
   if (e == cudaSuccess) e = launch_dispatch_scan(hist, nchunk, cfg->E, tbase, counts, s);
   if (e == cudaSuccess)
     e = launch_dispatch_scatter(cfg->dtype, cfg->payload_fp8, x, topk_idx, cfg->T, cfg->d,

@@ -57,6 +57,7 @@ struct TcParams {
   const float* row_scale;
   void* out;
   uint32_t* err;
+  uint32_t* tile_ctr;  // next tile to hand out; zero before the launch
   int E, K, N, R, n_tiles;
 };
 
@@ -72,7 +73,16 @@ __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __ex
 //             barrier (the cta_group::2 form of the tensor copy);
 //   empty[s]  both CTAs, from one multicast tcgen05.commit;
 //   tfull     both CTAs, multicast commit after a tile's last MMA;
-//   tempty    (even CTA) one arrive per epilogue warp of either CTA.
+//   tempty    (even CTA) one arrive per epilogue warp of either CTA;
+//   tq_full   both CTAs: the even CTA's producer claims the next tile with a
+//             global atomic and posts its index to a slot of both CTAs' tile
+//             queues (local store + st.shared::cluster, then arrive);
+//   tq_empty  (even CTA) every reader of a queue slot: the even CTA's MMA
+//             thread and epilogue warps, the odd CTA's producer and
+//             epilogue warps.
+// Tiles are claimed in index order as pairs become free (dynamic
+// scheduling): a fixed round-robin split left some pairs with every full
+// tile and others with every short tail.
 namespace pairk {
 constexpr int BM = 256, BK = 64;
 constexpr int A_BYTES = 128 * BK * 2;       // 16 KB: this CTA's 128 rows
@@ -106,9 +116,12 @@ struct Shape {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = STAGES * A_BYTES;
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;  // full, empty, tfull, tempty, drain
+  static constexpr int TQ = 8;  // tile queue slots
+  // full, empty, tfull, tempty, drain, tq_full, tq_empty
+  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * TQ;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int OFF_SEG = OFF_MISC + 16;
+  static constexpr int OFF_TQ = OFF_MISC + 16;
+  static constexpr int OFF_SEG = OFF_TQ + TQ * 4;
   static constexpr int OFF_TSTART = OFF_SEG + (kMaxExperts + 1) * 4;
   static constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;
@@ -165,6 +178,9 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
   uint64_t* tfull = empty + S::STAGES;
   uint64_t* tempty = tfull + S::NUM_ACC;
   uint64_t* drain = tempty + S::NUM_ACC;
+  uint64_t* tq_full = drain + 1;
+  uint64_t* tq_empty = tq_full + S::TQ;
+  int* tq = reinterpret_cast<int*>(smem + S::OFF_TQ);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::OFF_MISC);
   int* s_total = reinterpret_cast<int*>(smem + S::OFF_MISC + 4);
   int* seg = reinterpret_cast<int*>(smem + S::OFF_SEG);
@@ -172,7 +188,6 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int E = p.E;
 
   if (warp == 0) {
@@ -212,6 +227,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         mbar_init(&tempty[i], 2 * NEW);  // epilogue warps of both CTAs
       }
       mbar_init(drain, 1);
+      for (int i = 0; i < S::TQ; ++i) {
+        mbar_init(&tq_full[i], 1);
+        mbar_init(&tq_empty[i], 2 + 2 * NEW);
+      }
       fence_mbar_init();
     }
   } else if (warp == 1) {
@@ -226,6 +245,34 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
   const int KB = p.K / pairk::BK;
   bool timed_out = false;
 
+  // Tile queue. Readers take slots in order; `next_tile` waits for the slot
+  // (cluster-scope acquire: the odd CTA's copy is written remotely), reads
+  // the index and releases the slot on the even CTA's tq_empty.
+  int q_slot = 0;
+  uint32_t q_ph = 0;
+  const uint32_t leader_tq_empty = mapa_shared(smem_u32(tq_empty), 0);
+  auto next_tile = [&](bool whole_warp) -> int {
+    const bool ok = mbar_wait_cluster(&tq_full[q_slot], q_ph, kWaitLimitNs);
+    const bool all_ok = whole_warp ? __all_sync(0xffffffffu, ok) : ok;
+    int t = total;  // a timeout reads as the end of the work
+    if (all_ok) {
+      t = tq[q_slot];
+      if (!whole_warp || lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&tq_empty[q_slot]);
+        else
+          mbar_arrive_remote(leader_tq_empty + static_cast<uint32_t>(q_slot * 8));
+      }
+    } else {
+      timed_out = true;
+    }
+    if (++q_slot == S::TQ) {
+      q_slot = 0;
+      q_ph ^= 1u;
+    }
+    return t;
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
@@ -235,7 +282,33 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       uint32_t ph = 0, armed = 0, armed_ph = 0;
       // both CTAs' bytes of a stage are counted on the even CTA's full[s]
       const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
-      for (int tile = pair; tile < total && !timed_out; tile += npairs) {
+      // even CTA: claim tiles (one claim ahead) and post them; odd CTA: read
+      // them from its queue copy
+      const uint32_t peer_tq = mapa_shared(smem_u32(tq), 1);
+      const uint32_t peer_tq_full = mapa_shared(smem_u32(tq_full), 1);
+      // unsigned: any counter value maps to a valid tile or to the end
+      uint32_t claimed = rank == 0 ? atomicAdd(p.tile_ctr, 1u) : 0u;
+      for (;;) {
+        int tile;
+        if (rank == 0) {
+          tile = claimed < static_cast<uint32_t>(total) ? static_cast<int>(claimed) : total;
+          if (!mbar_wait_cluster(&tq_empty[q_slot], q_ph ^ 1u, kWaitLimitNs)) {
+            timed_out = true;
+            tile = total;
+          }
+          tq[q_slot] = tile;
+          st_shared_cluster_s32(peer_tq + static_cast<uint32_t>(q_slot * 4), tile);
+          mbar_arrive(&tq_full[q_slot]);
+          mbar_arrive_remote(peer_tq_full + static_cast<uint32_t>(q_slot * 8));
+          if (++q_slot == S::TQ) {
+            q_slot = 0;
+            q_ph ^= 1u;
+          }
+          if (tile < total) claimed = atomicAdd(p.tile_ctr, 1u);
+        } else {
+          tile = next_tile(false);
+        }
+        if (tile >= total || timed_out) break;
         const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
         // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
         const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
@@ -288,7 +361,9 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       bool issued = false;
-      for (int tile = pair; tile < total && !timed_out; tile += npairs) {
+      for (;;) {
+        const int tile = next_tile(false);
+        if (tile >= total || timed_out) break;
         if (!mbar_wait_spin(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
           timed_out = true;
           break;
@@ -349,7 +424,9 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = pair; tile < total; tile += npairs) {
+    for (;;) {
+      const int tile = next_tile(true);
+      if (tile >= total || timed_out) break;
       const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
       const bool ok = mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -565,7 +642,7 @@ int pick_nb(int epi, int R, int E, int K, int N, int num_sms) {
 
 cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, int K, int N,
                            const int32_t* offsets, const float* row_scale, void* out,
-                           uint32_t* err, int num_sms, cudaStream_t s) {
+                           uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   if (num_sms < 2) return cudaErrorInvalidValue;
   CUtensorMap mA, mB;
@@ -582,6 +659,7 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
   prm.row_scale = row_scale;
   prm.out = out;
   prm.err = err;
+  prm.tile_ctr = tile_ctr;
   prm.E = E;
   prm.K = K;
   prm.N = N;

@@ -93,6 +93,8 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+uint32_t* gemm_counters(void* ws) { return at<uint32_t>(ws, kGemmCounterOffset); }
+
 void record(void* const* ev, int i, cudaStream_t s) {
   if (ev != nullptr && ev[i] != nullptr) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
 }
@@ -111,7 +113,9 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* hist = at<int32_t>(ws, L.hist);
   int32_t* base = at<int32_t>(ws, L.base);
-  cudaError_t e = launch_dispatch_count(idx, c.T, c.k, c.E, L.nchunk, hist, err, s);
+  // the count kernel also zeroes the GEMM tile counters for the layer
+  cudaError_t e = launch_dispatch_count(idx, c.T, c.k, c.E, L.nchunk, hist, err,
+                                        gemm_counters(ws), kNumGemmCounters, s);
   if (e == cudaSuccess) e = launch_dispatch_scan(hist, L.nchunk, c.E, base, counts, s);
   if (e == cudaSuccess)
     e = launch_dispatch_scatter(c.dtype, c.payload_fp8, x, idx, c.T, c.d, c.k, c.E, L.nchunk,
@@ -145,12 +149,14 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
   }
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_LAUNCH;
+  uint32_t* ctr = gemm_counters(ws) + (which - 1);
   if (which == 1) {
     const void* A = c.payload_fp8 ? at<void>(ws, L.stage) : x_perm;
     return status_of(launch_gemm_tc(0, A, R, W1, c.E, c.d, c.f, offsets,
-                                    c.payload_fp8 ? x_scale : nullptr, h, err, sms, s));
+                                    c.payload_fp8 ? x_scale : nullptr, h, err, ctr, sms, s));
   }
-  return status_of(launch_gemm_tc(1, h, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, sms, s));
+  return status_of(
+      launch_gemm_tc(1, h, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, ctr, sms, s));
 }
 
 int run_combine(const moe_config_t& c, const Layout& L, void* ws, const float* y,
@@ -263,6 +269,9 @@ int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const float* x_s
   const Layout L = layout_of(*cfg);
   if (ws_bytes < L.scratch_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = as_stream(stream);
+  if (cfg->T > 0 && cudaMemsetAsync(gemm_counters(ws), 0, kNumGemmCounters * sizeof(uint32_t),
+                                    s) != cudaSuccess)
+    return MOE_ERR_LAUNCH;
   if ((st = run_ffn_prologue(*cfg, L, ws, x_perm, s)) != MOE_OK) return st;
   if ((st = run_gemm(*cfg, L, ws, 1, x_perm, x_scale, offsets, W1, W2, h, y_perm, s)) != MOE_OK)
     return st;
