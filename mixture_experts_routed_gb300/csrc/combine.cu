@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ w, int T, int d,
                                                       int k, int R, void* __restrict__ out,
                                                       uint32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_trigger();
   const int tl = threadIdx.x & 127;
   const int t = blockIdx.x * 2 + (threadIdx.x >> 7);
   if (t >= T) return;
@@ -89,14 +91,17 @@ cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const 
                            int d, int k, int R, void* out, uint32_t* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const dim3 grid(ceil_div(T, 2)), block(256);
-#define MOE_COMBINE(DT, KM) combine_kernel<DT, KM><<<grid, block, 0, s>>>(y, pos, w, T, d, k, R, out, err)
+#define MOE_COMBINE(DT, KM) \
+  return launch_pdl(combine_kernel<DT, KM>, grid, block, 0, s, y, pos, w, T, d, k, R, out, err)
   if (dtype == 0) {
-    if (k <= 2) MOE_COMBINE(0, 2); else if (k <= 4) MOE_COMBINE(0, 4); else MOE_COMBINE(0, 8);
-  } else {
-    if (k <= 2) MOE_COMBINE(1, 2); else if (k <= 4) MOE_COMBINE(1, 4); else MOE_COMBINE(1, 8);
+    if (k <= 2) MOE_COMBINE(0, 2);
+    if (k <= 4) MOE_COMBINE(0, 4);
+    MOE_COMBINE(0, 8);
   }
+  if (k <= 2) MOE_COMBINE(1, 2);
+  if (k <= 4) MOE_COMBINE(1, 4);
+  MOE_COMBINE(1, 8);
 #undef MOE_COMBINE
-  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -4,9 +4,40 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace moe {
+
+// ---------------------------------------------------------------- launch
+// Programmatic dependent launch: every kernel of the layer is launched with
+// programmatic stream serialisation, so its CTAs may be scheduled while the
+// previous kernel in the stream is still draining. Each kernel calls
+// pdl_wait() before its first global-memory access (read or write); it
+// returns once the previous grid has completed and its writes are visible,
+// which by induction orders it after every earlier kernel of the stream.
+// pdl_trigger() lets the next kernel be scheduled (it takes effect once
+// every CTA of this grid has issued it or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, std::forward<Args>(args)...);
+}
 
 // Bits of the device error word (the first 4 bytes of the workspace).
 constexpr uint32_t kErrBadIndex = 1u;

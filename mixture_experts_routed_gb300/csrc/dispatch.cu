@@ -30,6 +30,8 @@ namespace {
 constexpr int kTPC = kDispatchTokensPerChunk;
 
 __global__ void dispatch_empty_kernel(int E, int32_t* counts, int32_t* offsets) {
+  pdl_wait();
+  pdl_trigger();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     if (e < E) counts[e] = 0;
     offsets[e] = 0;
@@ -43,6 +45,8 @@ __global__ void __launch_bounds__(128) dispatch_count_kernel(const int32_t* __re
                                                              uint32_t* __restrict__ zero,
                                                              int nzero) {
   __shared__ int h[kMaxExperts];
+  pdl_wait();
+  pdl_trigger();
   const int c = blockIdx.x;
   if (zero != nullptr && c == 0 && static_cast<int>(threadIdx.x) < nzero) zero[threadIdx.x] = 0u;
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
@@ -89,6 +93,8 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t* __res
                                                             int nchunk, int E,
                                                             int32_t* __restrict__ base,
                                                             int32_t* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   const int e = blockIdx.x;
   const int32_t* h = hist + static_cast<size_t>(e) * nchunk;
   int32_t* b = base + static_cast<size_t>(e) * nchunk;
@@ -141,6 +147,8 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
   __shared__ int off_s[kMaxExperts + 1];
   __shared__ int cnt_w[2][kMaxExperts];  // per-warp expert counts (<= 64 entries, 2 warps)
   __shared__ int pos_s[kTPC * kMaxTopK];
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int c = blockIdx.x;
 
@@ -275,6 +283,8 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
 
 __global__ void fp8_to_bf16_kernel(const uint8_t* __restrict__ q, size_t n16,
                                    __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint4 raw = __ldg(reinterpret_cast<const uint4*>(q) + i);
@@ -299,22 +309,20 @@ __global__ void fp8_to_bf16_kernel(const uint8_t* __restrict__ q, size_t n16,
 }  // namespace
 
 cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cudaStream_t s) {
-  dispatch_empty_kernel<<<1, 256, 0, s>>>(E, counts, offsets);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_empty_kernel, dim3(1), dim3(256), 0, s, E, counts, offsets);
 }
 
 cudaError_t launch_dispatch_count(const int32_t* topk_idx, int T, int k, int E, int nchunk,
                                   int32_t* hist, uint32_t* err, uint32_t* zero, int nzero,
                                   cudaStream_t s) {
-  dispatch_count_kernel<<<nchunk, 128, 0, s>>>(topk_idx, T, k, E, nchunk, hist, err, zero,
-                                               nzero);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_count_kernel, dim3(nchunk), dim3(128), 0, s, topk_idx, T, k, E,
+                    nchunk, hist, err, zero, nzero);
 }
 
 cudaError_t launch_dispatch_scan(const int32_t* hist, int nchunk, int E, int32_t* base,
                                  int32_t* counts, cudaStream_t s) {
-  dispatch_scan_kernel<<<E, 256, 0, s>>>(hist, nchunk, E, base, counts);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_scan_kernel, dim3(E), dim3(256), 0, s, hist, nchunk, E, base,
+                    counts);
 }
 
 cudaError_t launch_dispatch_scatter(int dtype, int fp8, const void* x, const int32_t* topk_idx,
@@ -323,27 +331,18 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, const void* x, const int
                                     int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
                                     float* x_scale, uint32_t* err, cudaStream_t s) {
   const dim3 grid(nchunk), block(256);
-  if (dtype == 0)
-    dispatch_scatter_kernel<0, false><<<grid, block, 0, s>>>(x, topk_idx, T, d, k, E, nchunk,
-                                                             counts, base, offsets, pos, src,
-                                                             x_perm, x_scale, err);
-  else if (!fp8)
-    dispatch_scatter_kernel<1, false><<<grid, block, 0, s>>>(x, topk_idx, T, d, k, E, nchunk,
-                                                             counts, base, offsets, pos, src,
-                                                             x_perm, x_scale, err);
-  else
-    dispatch_scatter_kernel<1, true><<<grid, block, 0, s>>>(x, topk_idx, T, d, k, E, nchunk,
-                                                            counts, base, offsets, pos, src,
-                                                            x_perm, x_scale, err);
-  return cudaGetLastError();
+  auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false>
+                : (!fp8 ? dispatch_scatter_kernel<1, false> : dispatch_scatter_kernel<1, true>);
+  return launch_pdl(kernel, grid, block, 0, s, x, topk_idx, T, d, k, E, nchunk, counts, base,
+                    offsets, pos, src, x_perm, x_scale, err);
 }
 
 cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s) {
   const size_t n16 = n / 16;
   if (n16 == 0) return cudaSuccess;
   int blocks = static_cast<int>(min(n16 / 256 + 1, static_cast<size_t>(152 * 8)));
-  fp8_to_bf16_kernel<<<blocks, 256, 0, s>>>(q, n16, static_cast<__nv_bfloat16*>(out_bf16));
-  return cudaGetLastError();
+  return launch_pdl(fp8_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, q, n16,
+                    static_cast<__nv_bfloat16*>(out_bf16));
 }
 
 }  // namespace moe

@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   tc_fence_after();
+  // barriers and tensor memory are set up: from here on global memory
+  pdl_wait();
+  pdl_trigger();
   const uint32_t tmem_base = *tmem_slot;
   bool timed_out = false;
 
@@ -282,9 +285,8 @@ cudaError_t launch_half(const CUtensorMap& mx, const CUtensorMap& mw, const floa
                               SMEM_BYTES);
   });
   if (st != cudaSuccess) return st;
-  gate_tc_kernel<HALF><<<ceil_div(T, BM), NUM_THREADS, SMEM_BYTES, s>>>(
-      mx, mw, bias, T, d, E, k, pre_k, router, idx, w, logits, err);
-  return cudaGetLastError();
+  return launch_pdl(gate_tc_kernel<HALF>, dim3(ceil_div(T, BM)), dim3(NUM_THREADS), SMEM_BYTES, s,
+                    mx, mw, bias, T, d, E, k, pre_k, router, idx, w, logits, err);
 }
 
 }  // namespace

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN];
   __shared__ int s_e, s_row0, s_row1;
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x;
   if (tid == 0) {
     // m-tile index -> (expert, rows)
@@ -106,11 +108,8 @@ cudaError_t launch_gemm_simt(int epi, const float* A, int R, const float* W, int
                              const int32_t* offsets, float* out, uint32_t* err, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   const dim3 grid(ceil_div(R, BM) + E, ceil_div(N, BN)), block(256);
-  if (epi == 0)
-    gemm_simt_kernel<0><<<grid, block, 0, s>>>(A, R, W, E, K, N, offsets, out, err);
-  else
-    gemm_simt_kernel<1><<<grid, block, 0, s>>>(A, R, W, E, K, N, offsets, out, err);
-  return cudaGetLastError();
+  return launch_pdl(epi == 0 ? gemm_simt_kernel<0> : gemm_simt_kernel<1>, grid, block, 0, s, A,
+                    R, W, E, K, N, offsets, out, err);
 }
 
 }  // namespace moe

@@ -189,6 +189,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int E = p.E;
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     for (int e = lane; e <= E; e += 32) seg[e] = __ldg(p.offsets + e);
@@ -611,13 +613,15 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, TcParams p
   lc.blockDim = dim3(pairk::num_threads<EPI>());
   lc.dynamicSmemBytes = S::SMEM_BYTES;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   cudaError_t st = set_pair_smem_attr<EPI, NB>();
   if (st != cudaSuccess) return st;
   // a persistent grid must fit at once: as many pairs as can be resident
