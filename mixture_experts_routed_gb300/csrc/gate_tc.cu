@@ -13,9 +13,9 @@
 // CTA per 128 tokens:
 //   warp 0     TMA producer: x [128 tokens][64 k] (K-major) and W_g
 //              [64 k][E] as E/64 boxes of 64 experts (MN-major), 128-byte
-//              swizzle, 4-stage ring
-//   warp 1     TMEM allocation + MMA issue; commits a chunk to one of two
-//              E-column accumulators
+//              swizzle, a 192 KB ring of 4 (E = 256) to 8 (E = 64) stages
+//   warp 1     TMEM allocation + MMA issue; commits a chunk to one of
+//              min(8, 512 / E) E-column accumulators
 //   warps 2-9  epilogue: warp (half, q) adds TMEM lanes 32q..32q+31, columns
 //              of its half, into register totals after every chunk
 // then all warps meet, write logits (+ bias) to shared memory over the ring,
@@ -39,22 +39,27 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128, BK = 64, STAGES = 4, CHUNK_KB = 2;
+constexpr int BM = 128, BK = 64, CHUNK_KB = 2;
 constexpr int X_BYTES = BM * BK * 2;     // 16 KB
 constexpr int BOX_BYTES = BK * 64 * 2;   // 8 KB: [64 k][64 experts]
 constexpr int MAX_E = 256;
-constexpr int STAGE_BYTES = X_BYTES + (MAX_E / 64) * BOX_BYTES;  // 48 KB
+// The stage ring is 192 KB: 4 stages of 48 KB at E = 256, up to 8 stages
+// of 24 KB at E = 64 (a stage is x [128][64] plus E/64 weight boxes).
+constexpr int RING_BYTES = 4 * (X_BYTES + (MAX_E / 64) * BOX_BYTES);
+constexpr int MAX_STAGES = 8;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
-constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1;  // full, empty, tfull[2], tempty[2], drain
+constexpr int OFF_BAR = RING_BYTES;
+constexpr int MAX_ACC = 8;                    // TMEM accumulators (512 / E of them)
+constexpr int NUM_BARS = 2 * MAX_STAGES + 2 * MAX_ACC + 1;  // full, empty, tfull, tempty, drain
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 // The logits tile is [BM][E + 1] (padded: row-strided writes hit distinct banks).
 static_assert(BM * (MAX_E + 1) * 4 <= OFF_BAR, "logits tile must fit over the stage ring");
 
-// The epilogue keeps E/2 totals per thread (a compile-time bound, HALF).
-template <int HALF>
+// EMAX (64, 128 or 256) bounds E: the epilogue keeps EMAX/2 totals per
+// thread and the selection scans EMAX/32 logits per lane.
+template <int EMAX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const float* __restrict__ bias, int T, int d, int E, int k, int pre_k,
@@ -64,10 +69,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* tfull = empty + MAX_STAGES;
+  uint64_t* tempty = tfull + MAX_ACC;
+  uint64_t* drain = tempty + MAX_ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   float* Ls = reinterpret_cast<float*>(smem);  // [BM][E + 1] after the main loop
 
@@ -75,17 +80,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int t0 = blockIdx.x * BM;
   const int nwbox = E / 64;
   const uint32_t stage_bytes = static_cast<uint32_t>(X_BYTES + nwbox * BOX_BYTES);
+  const int nst = min(MAX_STAGES, RING_BYTES / static_cast<int>(stage_bytes));
   const int KB = d / BK;
   const int nchunk = (KB + CHUNK_KB - 1) / CHUNK_KB;
-  // TMEM: two accumulators of E columns, allocation rounded up to a power of 2
-  const uint32_t tmem_cols = E <= 64 ? 128u : (E <= 128 ? 256u : 512u);
+  // TMEM: 512 columns (one CTA per SM) as 512 / E accumulators of E columns,
+  // so the MMA runs up to that many 128-K chunks ahead of the epilogue
+  constexpr int HALF = EMAX / 2;
+  const uint32_t tmem_cols = 512u;
+  const int nacc = min(MAX_ACC, 512 / E);
 
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < MAX_STAGES; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < MAX_ACC; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], NUM_EPI_WARPS);
     }
@@ -118,19 +127,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           timed_out = true;
           break;
         }
-        uint8_t* st = smem + s * STAGE_BYTES;
+        uint8_t* st = smem + s * stage_bytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
         tma_load_2d(st, &tmX, &full[s], kb * BK, t0);
         for (int c = 0; c < nwbox; ++c)
           tma_load_2d(st + X_BYTES + c * BOX_BYTES, &tmW, &full[s], c * 64, kb * BK);
         armed |= 1u << s;
         armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-        if (++s == STAGES) {
+        if (++s == nst) {
           s = 0;
           ph ^= 1u;
         }
       }
-      for (int i = 0; i < STAGES; ++i)
+      for (int i = 0; i < nst; ++i)
         if ((armed >> i) & 1u)
           if (!mbar_wait(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
     }
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + s * STAGE_BYTES);
+          const uint32_t a_base = smem_u32(smem + s * stage_bytes);
           const uint32_t b_base = a_base + X_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
@@ -163,15 +172,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        (kb != c * CHUNK_KB || kk != 0) ? 1u : 0u);
           issued = true;
           tc_commit(&empty[s]);
-          if (++s == STAGES) {
+          if (++s == nst) {
             s = 0;
             ph ^= 1u;
           }
         }
         if (timed_out) break;
         tc_commit(&tfull[acc]);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
+        if (++acc == nacc) {
+          acc = 0;
+          aph ^= 1u;
+        }
       }
       if (timed_out && issued) {  // MMAs in flight finish before TMEM is freed
         tc_commit(drain);
@@ -207,8 +218,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
-      acc ^= 1;
-      if (acc == 0) aph ^= 1u;
+      if (++acc == nacc) {
+        acc = 0;
+        aph ^= 1u;
+      }
     }
   }
 
@@ -229,7 +242,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   __syncthreads();
   // every warp selects and weighs tokens warp, warp + 10, ...
-  constexpr int NJ = MAX_E / 32;
+  constexpr int NJ = EMAX / 32;
   for (int r = warp; r < BM; r += NUM_THREADS / 32) {
     const int t = t0 + r;
     if (t >= T) break;
@@ -274,18 +287,18 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HALF>
-cudaError_t launch_half(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int T,
+template <int EMAX>
+cudaError_t launch_emax(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int T,
                         int d, int E, int k, int pre_k, int router, int32_t* idx, float* w,
                         float* logits, uint32_t* err, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(gate_tc_kernel<HALF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    st = cudaFuncSetAttribute(gate_tc_kernel<EMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               SMEM_BYTES);
   });
   if (st != cudaSuccess) return st;
-  return launch_pdl(gate_tc_kernel<HALF>, dim3(ceil_div(T, BM)), dim3(NUM_THREADS), SMEM_BYTES, s,
+  return launch_pdl(gate_tc_kernel<EMAX>, dim3(ceil_div(T, BM)), dim3(NUM_THREADS), SMEM_BYTES, s,
                     mx, mw, bias, T, d, E, k, pre_k, router, idx, w, logits, err);
 }
 
@@ -308,9 +321,12 @@ cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int
   if (!map_2d(&mw, Wg, static_cast<uint64_t>(d), static_cast<uint64_t>(E), 64, BK))
     return cudaErrorInvalidValue;
   if (E <= 64)
-    return launch_half<32>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+    return launch_emax<64>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
                            err, s);
-  return launch_half<128>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+  if (E <= 128)
+    return launch_emax<128>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+                            err, s);
+  return launch_emax<256>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
                           err, s);
 }
 
