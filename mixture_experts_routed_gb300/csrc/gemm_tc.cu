@@ -59,6 +59,7 @@ struct TcParams {
   uint32_t* err;
   uint32_t* tile_ctr;  // next tile to hand out; zero before the launch
   int E, K, N, R, n_tiles;
+  int n_tiles_m;       // feature blocks of a merged tile (ceil(N / 224))
 };
 
 // z * sigmoid(z) with the approximate divide: the result is rounded to bf16,
@@ -99,6 +100,19 @@ template <int EPI>
 __host__ __device__ constexpr int num_threads() { return 64 + 32 * num_epi_warps<EPI>(); }
 constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*B MN-major*/ true);
 
+// Merged tiles (256-feature shape only). An expert whose rows end in a short
+// remainder (1..TAIL_MAX rows after at least one full 256-row tile) covers
+// its last full tile and the remainder together: 224 features per tile, the
+// odd CTA's weight half shifted to start at n0 + 112 so that the pair MMA
+// M256 N224 sees 224 contiguous features, plus one swapped MMA M256 (the
+// same staged weights, features n0 .. n0 + 239 with 16 seen twice) x
+// N = remainder padded to 16, accumulating at TMEM column 224. The whole tile
+// still fits one 256-column accumulator, and the remainder costs neither a
+// second read of the weight tile nor a tile of its own.
+constexpr int MT_W = 224, MT_HALF = 112, TAIL_MAX = 32;
+constexpr int TAIL_SLOT = (TAIL_MAX / 2) * BK * 2;  // 2 KB: this CTA's half of the remainder
+constexpr uint32_t IDESC_MT = make_idesc_bf16_f32(BM, MT_W, false, true);
+
 // NB = 1: 256-feature pair tiles, two TMEM accumulators (the epilogue of one
 // tile overlaps the next tile's main loop), 6 stages of 32 KB.
 // NB = 2: 512-feature pair tiles, two M256 N256 MMAs per k-step sharing the
@@ -108,13 +122,16 @@ constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*
 template <int NB>
 struct Shape {
   static constexpr int BN = 256 * NB;
+  static constexpr bool MERGE = NB == 1;  // merged remainder tiles
   static constexpr int STAGES = NB == 1 ? 6 : 4;
   static constexpr int B_BYTES = NB * HALF_B_BYTES;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int T_BYTES = MERGE ? TAIL_SLOT : 0;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + T_BYTES;
   static constexpr int NUM_ACC = 2 / NB;
   static constexpr int ACC_COLS = TMEM_COLS / NUM_ACC;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = STAGES * A_BYTES;
+  static constexpr int OFF_T = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
   static constexpr int TQ = 8;  // tile queue slots
   // full, empty, tfull, tempty, drain, tq_full, tq_empty
@@ -131,13 +148,30 @@ struct Shape {
 struct PTile {
   int e, row0, ntok, n0;  // token rows [row0, row0 + ntok), features from n0
   bool swap;              // tail tile: weights are the MMA's M side, tokens its N
+  int width;              // features (bn, or MT_W for a merged tile)
+  int tail;               // merged tile: remainder rows at row0 + BM (else 0)
 };
+
+__device__ __forceinline__ bool merges(int rows, bool merge) {
+  const int full = rows / BM, rem = rows - full * BM;
+  return merge && full > 0 && rem > 0 && rem <= TAIL_MAX;
+}
+
+// Tiles of one expert with `rows` rows.
+__device__ __forceinline__ int expert_tiles(int rows, int n_tiles, int n_tiles_m, bool merge) {
+  const int full = rows / BM, rem = rows - full * BM;
+  if (merges(rows, merge)) return (full - 1) * n_tiles + n_tiles_m;
+  return (full + (rem > 0 ? 1 : 0)) * n_tiles;
+}
 
 // An expert's rows are covered by full 256-row pair tiles and, for the
 // remainder (1..255 rows), one swapped tile whose MMA N is the remainder
-// rounded up to 16, so a short tail costs a fraction of a full tile.
+// rounded up to 16, so a short tail costs a fraction of a full tile; or, for
+// a remainder of at most TAIL_MAX rows, merged tiles (see MT_W) in place of
+// the last full tile and the swapped one. Token tiles of one weight tile are
+// adjacent in the order.
 __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* seg, int E,
-                                        int n_tiles, int bn) {
+                                        int n_tiles, int bn, int n_tiles_m, bool merge) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -151,6 +185,26 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
   const int local = tile - tstart[lo];
   const int rows = seg[lo + 1] - seg[lo];
   const int full = rows / BM, rem = rows - full * BM;
+  t.width = bn;
+  t.tail = 0;
+  if (merges(rows, merge)) {
+    const int plain = (full - 1) * n_tiles;
+    if (local >= plain) {
+      t.row0 = seg[lo] + (full - 1) * BM;
+      t.swap = false;
+      t.ntok = BM;
+      t.n0 = (local - plain) * MT_W;
+      t.width = MT_W;
+      t.tail = rem;
+      return t;
+    }
+    const int nt = local / (full - 1), m = local - nt * (full - 1);
+    t.row0 = seg[lo] + m * BM;
+    t.swap = false;
+    t.ntok = BM;
+    t.n0 = nt * bn;
+    return t;
+  }
   const int mt = full + (rem > 0 ? 1 : 0);
   const int nt = local / mt, m = local - nt * mt;
   t.row0 = seg[lo] + m * BM;
@@ -164,6 +218,7 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
 template <int EPI, int NB>
 __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmA8,
                      const __grid_constant__ CUtensorMap tmB, const TcParams p) {
   using S = pairk::Shape<NB>;
   constexpr int NEW = pairk::num_epi_warps<EPI>();
@@ -173,6 +228,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem + S::OFF_A;
   uint8_t* sB = smem + S::OFF_B;
+  uint8_t* sT = smem + S::OFF_T;  // merged tiles' remainder rows (S::MERGE)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
   uint64_t* empty = full + S::STAGES;
   uint64_t* tfull = empty + S::STAGES;
@@ -204,7 +260,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       if (e < E) {
         const int lo = seg[e], hi = seg[e + 1];
         bad = lo < 0 || hi < lo || hi > p.R;
-        tiles = bad ? 0 : ((hi - lo + pairk::BM - 1) / pairk::BM) * p.n_tiles;
+        tiles = bad ? 0 : pairk::expert_tiles(hi - lo, p.n_tiles, p.n_tiles_m, S::MERGE);
       }
       if (__any_sync(0xffffffffu, bad)) ok = false;
       int incl = tiles;
@@ -279,6 +335,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       prefetch_tmap(&tmA);
+      prefetch_tmap(&tmA8);
       prefetch_tmap(&tmB);
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
@@ -311,23 +368,29 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           tile = next_tile(false);
         }
         if (tile >= total || timed_out) break;
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
         // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
         const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
         const int my_row = min(t.row0 + static_cast<int>(rank) * half_rows, p.R - 1);
         // MMA j covers features n0 + 256 j + [0, 256); this CTA holds the
-        // 128 at n0 + 256 j + 128 rank (whole 64-wide boxes only: N % 64 == 0)
+        // 128 at n0 + 256 j + half_w rank (half_w = 128, or 112 in a merged
+        // tile); a box is issued when it starts below N (one that runs past
+        // N is zero-filled, its bytes still counted)
+        const int half_w = t.tail > 0 ? pairk::MT_HALF : 128;
+        auto boxes = [&](int n) { return n < p.N ? min(2, (p.N - n + 63) / 64) : 0; };
         int nbox[NB];
         uint32_t bytes = 2 * pairk::A_BYTES;
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
-          const int my_n0 = t.n0 + j * 256 + static_cast<int>(rank) * 128;
-          nbox[j] = my_n0 < p.N ? min(2, (p.N - my_n0) / 64) : 0;
-          const int m0 = t.n0 + j * 256, m1 = m0 + 128;
-          const int pair_boxes = (m0 < p.N ? min(2, (p.N - m0) / 64) : 0) +
-                                 (m1 < p.N ? min(2, (p.N - m1) / 64) : 0);
-          bytes += static_cast<uint32_t>(pair_boxes * pairk::BOX_BYTES);
+          nbox[j] = boxes(t.n0 + j * 256 + static_cast<int>(rank) * half_w);
+          bytes += static_cast<uint32_t>((boxes(t.n0 + j * 256) + boxes(t.n0 + j * 256 + half_w)) *
+                                         pairk::BOX_BYTES);
         }
+        // merged tile: this CTA's half of the remainder rows (8 or 16) in
+        // 8-row boxes
+        const int tail_half = ((t.tail + 15) & ~15) / 2;
+        const int tail_row = t.row0 + pairk::BM + static_cast<int>(rank) * tail_half;
+        bytes += static_cast<uint32_t>(2 * tail_half * pairk::BK * 2);
         const int brow = t.e * p.K;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
@@ -341,8 +404,13 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           for (int j = 0; j < NB; ++j)
             for (int c = 0; c < nbox[j]; ++c)
               tma_load_2d_pair(sB + s * S::B_BYTES + j * pairk::HALF_B_BYTES + c * pairk::BOX_BYTES,
-                               &tmB, bar, t.n0 + j * 256 + static_cast<int>(rank) * 128 + c * 64,
+                               &tmB, bar, t.n0 + j * 256 + static_cast<int>(rank) * half_w + c * 64,
                                brow + kb * pairk::BK);
+          if constexpr (S::MERGE) {
+            for (int r = 0; r < tail_half; r += 8)
+              tma_load_2d_pair(sT + s * S::T_BYTES + r * pairk::BK * 2, &tmA8, bar,
+                               kb * pairk::BK, min(tail_row + r, p.R - 1));
+          }
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
           if (++s == S::STAGES) {
@@ -372,37 +440,74 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
         // MMAs with any feature below N (the rest of a last tile is skipped)
         const int nmma = min(NB, (p.N - t.n0 + 255) / 256);
         // swapped tile: A = weights (MN-major, the B slot), B = tokens (K-major, the A slot)
         const uint32_t idesc =
             t.swap ? make_idesc_bf16_f32(pairk::BM, (t.ntok + 15) & ~15, true, false) : pairk::IDESC;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
-            timed_out = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * pairk::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + s * S::B_BYTES);
+        bool merged = false;
+        if constexpr (S::MERGE) merged = t.tail > 0;
+        if (merged) {
+          // merged tile: per k-block the four M256 N224 MMAs, then the
+          // remainder's four swapped MMAs into columns 224.. (its own loop:
+          // the extra MMA inside the plain loop slowed every tile's issue)
+          const uint32_t idesc_tail =
+              make_idesc_bf16_f32(pairk::BM, (t.tail + 15) & ~15, true, false);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
+              timed_out = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + s * pairk::A_BYTES);
+            const uint32_t b_base = smem_u32(sB + s * S::B_BYTES);
+            const uint32_t t_base = smem_u32(sT + s * S::T_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < pairk::BK / 16; ++kk) {
-            const uint64_t tok = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+            for (int kk = 0; kk < pairk::BK / 16; ++kk)
+              tc_mma_f16_pair(d_tmem, make_sdesc_sw128(a_base + kk * 32, 16, 1024),
+                              make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024),
+                              pairk::IDESC_MT, (kb | kk) != 0 ? 1u : 0u);
 #pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              if (j >= nmma) break;
-              const uint64_t wt = make_sdesc_sw128(b_base + j * pairk::HALF_B_BYTES + kk * 2048,
-                                                   pairk::BOX_BYTES, 1024);
-              tc_mma_f16_pair(d_tmem + j * 256, t.swap ? wt : tok, t.swap ? tok : wt, idesc,
+            for (int kk = 0; kk < pairk::BK / 16; ++kk)
+              tc_mma_f16_pair(d_tmem + pairk::MT_W,
+                              make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024),
+                              make_sdesc_sw128(t_base + kk * 32, 16, 1024), idesc_tail,
                               (kb | kk) != 0 ? 1u : 0u);
+            issued = true;
+            tc_commit_pair_mc(&empty[s], 0x3);
+            if (++s == S::STAGES) {
+              s = 0;
+              ph ^= 1u;
             }
           }
-          issued = true;
-          tc_commit_pair_mc(&empty[s], 0x3);
-          if (++s == S::STAGES) {
-            s = 0;
-            ph ^= 1u;
+        } else {
+          for (int kb = 0; kb < KB; ++kb) {
+            if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
+              timed_out = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + s * pairk::A_BYTES);
+            const uint32_t b_base = smem_u32(sB + s * S::B_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < pairk::BK / 16; ++kk) {
+              const uint64_t tok = make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+#pragma unroll
+              for (int j = 0; j < NB; ++j) {
+                if (j >= nmma) break;
+                const uint64_t wt = make_sdesc_sw128(b_base + j * pairk::HALF_B_BYTES + kk * 2048,
+                                                     pairk::BOX_BYTES, 1024);
+                tc_mma_f16_pair(d_tmem + j * 256, t.swap ? wt : tok, t.swap ? tok : wt, idesc,
+                                (kb | kk) != 0 ? 1u : 0u);
+              }
+            }
+            issued = true;
+            tc_commit_pair_mc(&empty[s], 0x3);
+            if (++s == S::STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
         }
         if (timed_out) break;
@@ -429,7 +534,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     for (;;) {
       const int tile = next_tile(true);
       if (tile >= total || timed_out) break;
-      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN);
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
       const bool ok = mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) {
         timed_out = true;
@@ -446,8 +551,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         const size_t grow = static_cast<size_t>(t.row0) + r;
         float scale = 1.f;
         if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
+        const int nch = t.width / 32, per = (nch + NH - 1) / NH;
+        const int c_end = min(nch, (hh + 1) * per);
 #pragma unroll 1
-        for (int c = hh * (S::BN / 32 / NH); c < (hh + 1) * (S::BN / 32 / NH); ++c) {
+        for (int c = hh * per; c < c_end; ++c) {
           const int col = t.n0 + c * 32;
           if (col >= p.N) break;
           uint32_t v[32];
@@ -476,6 +583,39 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
             for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+        if constexpr (S::MERGE) {
+          if (t.tail > 0 && hh == NH - 1) {
+            // merged tile's remainder: lane = feature (this CTA's M row of
+            // the swapped MMA: n0 + 112 rank + 32 q + lane, the first 112 of
+            // each CTA distinct), columns = the remainder's tokens
+            const int l = q * 32 + lane;
+            const int f = t.n0 + static_cast<int>(rank) * pairk::MT_HALF + l;
+            const bool f_ok = l < pairk::MT_HALF && f < p.N;
+            uint32_t v[32];
+            tmem_ld_32x32b_x32(tbase + pairk::MT_W, v);
+            tmem_ld_wait();
+            const int trow = t.row0 + pairk::BM;
+            float my_scale = 1.f;
+            if (EPI == 0 && p.row_scale != nullptr && lane < t.tail)
+              my_scale = __ldg(p.row_scale + trow + lane);
+            const size_t base = static_cast<size_t>(trow) * p.N + f;
+            if constexpr (EPI == 0) {
+              __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const float sj = __shfl_sync(0xffffffffu, my_scale, jj);
+                if (jj < t.tail && f_ok)
+                  out[static_cast<size_t>(jj) * p.N] =
+                      __float2bfloat16_rn(silu(__uint_as_float(v[jj]) * sj));
+              }
+            } else {
+              float* out = static_cast<float*>(p.out) + base;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                if (jj < t.tail && f_ok) out[static_cast<size_t>(jj) * p.N] = __uint_as_float(v[jj]);
+            }
           }
         }
       } else {
@@ -603,12 +743,15 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
 }
 
 template <int EPI, int NB>
-cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, TcParams prm, int num_sms,
+cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUtensorMap& mB,
+                        TcParams prm, int num_sms,
                         cudaStream_t s) {
   using S = pairk::Shape<NB>;
   prm.n_tiles = ceil_div(prm.N, S::BN);
-  const long long max_pt = static_cast<long long>(ceil_div(prm.R, pairk::BM) + prm.E) *
-                           static_cast<long long>(prm.n_tiles);
+  prm.n_tiles_m = ceil_div(prm.N, pairk::MT_W);
+  const long long max_pt =
+      static_cast<long long>(ceil_div(prm.R, pairk::BM) + prm.E) *
+      static_cast<long long>(prm.n_tiles > prm.n_tiles_m ? prm.n_tiles : prm.n_tiles_m);
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(pairk::num_threads<EPI>());
   lc.dynamicSmemBytes = S::SMEM_BYTES;
@@ -629,7 +772,7 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mB, TcParams p
   const int resident = resident_pairs<EPI, NB>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB>, mA, mB, prm);
+  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB>, mA, mA8, mB, prm);
 }
 
 // 512-feature tiles (one accumulator, epilogue exposed) pay off only for the
@@ -649,11 +792,15 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
                            uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   if (num_sms < 2) return cudaErrorInvalidValue;
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mA8, mB;
   std::memset(&mA, 0, sizeof(mA));
+  std::memset(&mA8, 0, sizeof(mA8));
   std::memset(&mB, 0, sizeof(mB));
   // A: token rows, [128 rows][64 k] boxes; B: weights as [E*K rows, N], [64 k][64 n] boxes
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128))
+  // A: token rows in [128 rows][64 k] boxes, and [8 rows][64 k] boxes for
+  // merged tiles' remainders
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128) ||
+      !make_map_2d(&mA8, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 8))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64,
                    pairk::BK))
@@ -676,10 +823,10 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
     if (std::strcmp(f, "512") == 0) nb = 2;
   }
   if (epi == 0)
-    return nb == 2 ? launch_pair<0, 2>(mA, mB, prm, num_sms, s)
-                   : launch_pair<0, 1>(mA, mB, prm, num_sms, s);
-  return nb == 2 ? launch_pair<1, 2>(mA, mB, prm, num_sms, s)
-                 : launch_pair<1, 1>(mA, mB, prm, num_sms, s);
+    return nb == 2 ? launch_pair<0, 2>(mA, mA8, mB, prm, num_sms, s)
+                   : launch_pair<0, 1>(mA, mA8, mB, prm, num_sms, s);
+  return nb == 2 ? launch_pair<1, 2>(mA, mA8, mB, prm, num_sms, s)
+                 : launch_pair<1, 1>(mA, mA8, mB, prm, num_sms, s);
 }
 
 }  // namespace moe

@@ -64,6 +64,20 @@ SMALL = {
                                                       T=520, d=1024, E=4, k=1, f=1024,
                                                       dtype="bf16", pre_k=4, payload_fp8=True,
                                                       seed=26),
+    # merged remainder tiles (one full 256-row tile + 1..32 rows): 270 rows
+    # per expert (remainder 14) with partial last 224-feature blocks; 544
+    # rows (remainder 32, FP8 row scales, a plain full tile before the
+    # merged one); 257 rows (remainder 1)
+    "merged_tail_T270_d256_E2_k2_f320": MoEConfig("merged_tail_T270_d256_E2_k2_f320", T=270,
+                                                  d=256, E=2, k=2, f=320, dtype="bf16",
+                                                  pre_k=2, seed=27),
+    "merged_tail_fp8_T544_d512_E1_k1_f576": MoEConfig("merged_tail_fp8_T544_d512_E1_k1_f576",
+                                                      T=544, d=512, E=1, k=1, f=576,
+                                                      dtype="bf16", pre_k=1, payload_fp8=True,
+                                                      outlier_rate=0.01, seed=28),
+    "merged_tail_T257_d128_E1_k1_f256": MoEConfig("merged_tail_T257_d128_E1_k1_f256", T=257,
+                                                  d=128, E=1, k=1, f=256, dtype="bf16",
+                                                  pre_k=1, seed=29),
 }
 ALL = dict(SMALL)
 ALL.update(CONFIGS)
