@@ -68,7 +68,7 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* 
                          float* topk_w, float* logits, uint32_t* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- gate_tc.cu
-// Tensor-core gate (bf16, E a multiple of 64 up to 256, 16-byte aligned x, W_g).
+// Tensor-core gate (bf16, E a multiple of 8 up to 256, 16-byte aligned x, W_g).
 bool gate_tc_supported(int dtype, int E, const void* Wg, const void* x);
 cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int T, int d, int E,
                            int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,

@@ -1,6 +1,8 @@
 // gate_tc.cu - gate projection and router on the tensor cores, for bf16
-// layers with E a multiple of 64 (DeepSeek-V4 EP article, sections 2.1 and
-// 3.2): L = x W_g + b, then the same warp top-k and weights as route.cu.
+// layers with E a multiple of 8 up to 256 (DeepSeek-V4 EP article, sections
+// 2.1 and 3.2): L = x W_g + b, then the same warp top-k and weights as
+// route.cu. The weight tile is Ep = E rounded up to 64 experts wide; TMA
+// zero-fills the columns past E and the padded logits are never read.
 //
 // The gate is a GEMM of T x d by d x E (60 GFLOP for 16384 tokens, d = 7168,
 // E = 256), too much for fp32 FMA, but fp32 accumulation inside tcgen05 over
@@ -9,7 +11,7 @@
 // (two 64-wide k-blocks) and the CUDA cores add each 128-long partial into
 // fp32 totals: measured error then 1.7e-6 max, 1.8e-7 RMS at K = 7168.
 //
-// CTA = 128 tokens x E experts (tcgen05.mma.cta_group::1 M128 N=E K16), one
+// CTA = 128 tokens x Ep experts (tcgen05.mma.cta_group::1 M128 N=Ep K16), one
 // CTA per 128 tokens:
 //   warp 0     TMA producer: x [128 tokens][64 k] (K-major) and W_g
 //              [64 k][E] as E/64 boxes of 64 experts (MN-major), 128-byte
@@ -78,7 +80,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * BM;
-  const int nwbox = E / 64;
+  // the weight tile is Ep = E rounded up to 64 experts wide: TMA zero-fills
+  // the boxes past E, and the padded columns are never read back
+  const int Ep = (E + 63) & ~63;
+  const int nwbox = Ep / 64;
   const uint32_t stage_bytes = static_cast<uint32_t>(X_BYTES + nwbox * BOX_BYTES);
   const int nst = min(MAX_STAGES, RING_BYTES / static_cast<int>(stage_bytes));
   const int KB = d / BK;
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // so the MMA runs up to that many 128-K chunks ahead of the epilogue
   constexpr int HALF = EMAX / 2;
   const uint32_t tmem_cols = 512u;
-  const int nacc = min(MAX_ACC, 512 / E);
+  const int nacc = min(MAX_ACC, 512 / Ep);
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < MAX_STAGES; ++i) {
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = make_idesc_bf16_f32(BM, E, /*A MN*/ false, /*B MN*/ true);
+      const uint32_t idesc = make_idesc_bf16_f32(BM, Ep, /*A MN*/ false, /*B MN*/ true);
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       bool issued = false;
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * E);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Ep);
         const int kb_end = min(KB, (c + 1) * CHUNK_KB);
         for (int kb = c * CHUNK_KB; kb < kb_end; ++kb) {
           if (!mbar_wait(&full[s], ph, kWaitLimitNs)) {
@@ -190,10 +195,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else {
-    // epilogue: columns [half * E/2, half * E/2 + E/2) of lanes 32q..32q+31
+    // epilogue: columns [half * Ep/2, half * Ep/2 + Ep/2) of lanes 32q..32q+31
     const int q = warp & 3;
     const int half = (warp - 2) >> 2;
-    const int ncol = E / 2;
+    const int ncol = Ep / 2;
     int acc = 0;
     uint32_t aph = 0;
     for (int c = 0; c < nchunk; ++c) {
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * E + half * ncol) +
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * Ep + half * ncol) +
                           (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
       for (int cc = 0; cc < HALF / 32; ++cc) {
@@ -228,11 +233,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (timed_out && err != nullptr) atomicOr(err, kErrTimeout);
   __syncthreads();  // the ring is idle: reuse it for the logits tile
   if (warp >= 2) {
-    const int q = warp & 3, half = (warp - 2) >> 2, ncol = E / 2;
+    const int q = warp & 3, half = (warp - 2) >> 2, ncol = Ep / 2;
     const int r = q * 32 + lane;
 #pragma unroll
     for (int j = 0; j < HALF; ++j) {
-      if (j < ncol) {
+      if (j < ncol && half * ncol + j < E) {
         const int e = half * ncol + j;
         const float val = tot[j] + (bias ? __ldg(bias + e) : 0.f);
         Ls[r * (E + 1) + e] = val;
@@ -305,7 +310,8 @@ cudaError_t launch_emax(const CUtensorMap& mx, const CUtensorMap& mw, const floa
 }  // namespace
 
 bool gate_tc_supported(int dtype, int E, const void* Wg, const void* x) {
-  return dtype == 1 && E >= 64 && E <= MAX_E && E % 64 == 0 &&
+  // E % 8 == 0: a W_g row is a whole number of 16-byte units (TMA stride)
+  return dtype == 1 && E >= 8 && E <= MAX_E && E % 8 == 0 &&
          reinterpret_cast<uintptr_t>(Wg) % 16 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0;
 }
 

@@ -422,7 +422,10 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
 cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* bias, int T,
                          int d, int E, int k, int pre_k, int router, int32_t* topk_idx,
                          float* topk_w, float* logits, uint32_t* err, cudaStream_t s) {
-  if (T > 0 && gate_tc_supported(dtype, E, Wg, x))
+  // tensor-core gate: always for E a multiple of 64; for narrower gates only
+  // with enough 128-token CTAs to fill the GPU (the SIMT kernels win on small
+  // batches, e.g. T = 1024)
+  if (T > 0 && gate_tc_supported(dtype, E, Wg, x) && (E % 64 == 0 || T >= 4096))
     return launch_gate_tc(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits, err,
                           s);
   if (dtype == 0)

@@ -78,6 +78,14 @@ SMALL = {
     "merged_tail_T257_d128_E1_k1_f256": MoEConfig("merged_tail_T257_d128_E1_k1_f256", T=257,
                                                   d=128, E=1, k=1, f=256, dtype="bf16",
                                                   pre_k=1, seed=29),
+    # tensor-core gate for E < 64 (T >= 4096): E = 16 with a 4-token last
+    # tile; E = 40 (weight boxes past E zero-filled) with a bias and a
+    # one-block last K chunk
+    "gate_E16_T4100_d256_k2_f128": MoEConfig("gate_E16_T4100_d256_k2_f128", T=4100, d=256,
+                                             E=16, k=2, f=128, dtype="bf16", seed=30),
+    "gate_E40_T4096_d320_k3_f128": MoEConfig("gate_E40_T4096_d320_k3_f128", T=4096, d=320,
+                                             E=40, k=3, f=128, dtype="bf16", bias="normal",
+                                             bias_var=1.0, seed=31),
 }
 ALL = dict(SMALL)
 ALL.update(CONFIGS)
