@@ -21,7 +21,7 @@
 //   warps 2-9  epilogue: warp (half, q) adds TMEM lanes 32q..32q+31, columns
 //              of its half, into register totals after every chunk
 // then all warps meet, write logits (+ bias) to shared memory over the ring,
-// and select / weigh tokens with the warp top-k. Every wait is bounded.
+// and one thread per token selects and weighs it. Every wait is bounded.
 #include <cfloat>
 #include <cstdint>
 #include <cstring>
@@ -60,7 +60,7 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(BM * (MAX_E + 1) * 4 <= OFF_BAR, "logits tile must fit over the stage ring");
 
 // EMAX (64, 128 or 256) bounds E: the epilogue keeps EMAX/2 totals per
-// thread and the selection scans EMAX/32 logits per lane.
+// thread.
 template <int EMAX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -246,20 +246,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
-  // every warp selects and weighs tokens warp, warp + 10, ...
-  constexpr int NJ = EMAX / 32;
-  for (int r = warp; r < BM; r += NUM_THREADS / 32) {
-    const int t = t0 + r;
-    if (t >= T) break;
-    float v[NJ];
-    int id[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = e < E ? Ls[r * (E + 1) + e] : -INFINITY;
-      id[j] = e < E ? e : 0x7fffffff;
-    }
-    topk::warp_select_and_weigh<NJ>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+  // selection and weights: one thread per token (row r = thread r), reading
+  // the logits row from shared memory (stride E + 1: conflict-free)
+  if (threadIdx.x < BM) {
+    const int r = threadIdx.x;
+    if (t0 + r < T)
+      topk::thread_select_and_weigh(Ls + r * (E + 1), E, k, pre_k, router, t0 + r, topk_idx,
+                                    topk_w);
   }
   __syncthreads();
   if (warp == 1) {
