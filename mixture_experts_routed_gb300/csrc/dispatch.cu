@@ -117,8 +117,8 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t u) {
   return __uint_as_float(static_cast<uint32_t>(u) << 16);
 }
 
-// 8 floats -> 8 E4M3 bytes (round to nearest even, saturating), element 0 in
-// the lowest byte.
+// 8 floats -> 8 E4M3 bytes of x / s (round to nearest even, saturating),
+// element 0 in the lowest byte.
 __device__ __forceinline__ uint2 quant8(const float (&v)[8], float s) {
   uint32_t w[2];
 #pragma unroll
@@ -248,12 +248,21 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
     const uint4* xr =
         reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xv) +
                                        static_cast<size_t>(t) * d);
+    // four 16-byte loads in flight per lane (one at a time is latency-bound)
+    constexpr int UQ = 4;
     float amax = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(xr + v);
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(&val);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * UQ) {
+      uint4 val[UQ];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(h[i])));
+      for (int u = 0; u < UQ; ++u)
+        if (v0 + 32 * u < nvec) val[u] = __ldg(xr + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < UQ; ++u) {
+        if (v0 + 32 * u >= nvec) break;
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&val[u]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(h[i])));
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -262,16 +271,24 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
     // pass 2: q = E4M3(x / s); the k copies share the scale
     uint2* dst = reinterpret_cast<uint2*>(x_perm);
     const size_t row_vecs = static_cast<size_t>(nvec);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(xr + v);
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(&val);
-      float f[8];
+    for (int v0 = lane; v0 < nvec; v0 += 32 * UQ) {
+      uint4 val[UQ];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = bf16_to_f32(h[i]);
-      const uint2 q = quant8(f, s);
+      for (int u = 0; u < UQ; ++u)
+        if (v0 + 32 * u < nvec) val[u] = __ldg(xr + v0 + 32 * u);
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = q;
+      for (int u = 0; u < UQ; ++u) {
+        const int v = v0 + 32 * u;
+        if (v >= nvec) break;
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(&val[u]);
+        float f[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = bf16_to_f32(h[i]);
+        const uint2 q = quant8(f, s);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j)
+          if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = q;
+      }
     }
     if (lane == 0) {
 #pragma unroll
