@@ -12,7 +12,8 @@ page references name the article and its section:
              destination packed buffers), 2.3 (weighted sum of the k expert
              outputs per token), 3.1 (per-token FP8 payload quantisation).
   [V3V4-PAR] "DeepSeek V3/V4 parallel strategy", EP and Waved-EP sections
-             (dispatch, expert L1 + Act + L2, combine).
+             (dispatch, expert L1 + Act + L2, combine; the V3 limit of a
+             token's 8 experts to the 4 nodes that are best on average).
 
 Readings taken where the pages leave a step open are listed with each
 function (expert FFN form, selection order, FP8 scale form, rounding points).
@@ -25,6 +26,7 @@ from .numerics import round_to_bf16, round_to_f32, e4m3_round_satfinite
 
 ROUTER_RENORM = 0
 ROUTER_PREK_SOFTMAX = 1
+ROUTER_GROUP_LIMITED = 2
 E4M3_MAX_F32 = np.float32(448.0)
 
 
@@ -74,7 +76,8 @@ def _softmax_max_subtracted(L: np.ndarray) -> np.ndarray:
     return ez / ez.sum(axis=-1, keepdims=True)
 
 
-def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8):
+def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8,
+          n_group: int = 1, topk_group: int = 1):
     """Top-k expert selection and gate weights.
 
     Order: logits descending, equal logits by expert id ascending (the lower
@@ -86,11 +89,20 @@ def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8):
     * ROUTER_PREK_SOFTMAX: the exact softmax is taken over the pre_k largest
       logits only; the k chosen entries of that softmax are the weights, not
       renormalised (their sum is at most 1).
+    * ROUTER_GROUP_LIMITED (node-limited, [V3V4-PAR] EP section): the E
+      experts form n_group equal groups of consecutive ids (a node's
+      experts). A group's score is the average softmax probability of its
+      experts; the topk_group best groups are kept (equal scores: the lower
+      group id first). The k chosen experts are the top-k logits among the
+      kept groups' experts, weighted as in ROUTER_RENORM (their full-softmax
+      probabilities divided by their sum). pre_k plays no part.
 
     Returns (topk_idx int32 [T, k], topk_w fp64 [T, k]).
     """
     L = np.asarray(L, np.float64)
     T, E = L.shape
+    if router == ROUTER_GROUP_LIMITED:
+        return _route_group_limited(L, k, n_group, topk_group)
     pre_k = min(pre_k, E)
     if not (1 <= k <= pre_k):
         raise ValueError("need 1 <= k <= min(pre_k, E)")
@@ -109,6 +121,29 @@ def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8):
     else:
         raise ValueError(f"unknown router mode {router}")
     return sel.astype(np.int32), w
+
+
+def _route_group_limited(L: np.ndarray, k: int, n_group: int, topk_group: int):
+    """Node-limited top-k [V3V4-PAR EP section]: keep the topk_group groups
+    with the best average probability, then the k best experts inside them."""
+    T, E = L.shape
+    if n_group < 1 or E % n_group:
+        raise ValueError("n_group must divide E")
+    gs = E // n_group
+    if not (1 <= topk_group <= n_group and 1 <= k <= topk_group * gs):
+        raise ValueError("need 1 <= topk_group <= n_group and 1 <= k <= topk_group * E/n_group")
+    p = _softmax_max_subtracted(L)
+    score = p.reshape(T, n_group, gs).mean(axis=2)          # average affinity per group
+    kept = np.argsort(-score, axis=1, kind="stable")[:, :topk_group]
+    allowed = np.zeros((T, E), dtype=bool)
+    for t in range(T):
+        for g in kept[t]:
+            allowed[t, g * gs:(g + 1) * gs] = True
+    # experts outside the kept groups sort after every allowed one
+    Lk = np.where(allowed, L, -np.inf)
+    sel = np.argsort(-Lk, axis=1, kind="stable")[:, :k]
+    ps = p[np.arange(T)[:, None], sel]
+    return sel.astype(np.int32), ps / ps.sum(axis=1, keepdims=True)
 
 
 # ----------------------------------------------------------------------------
@@ -207,6 +242,10 @@ def combine(Y: np.ndarray, pos: np.ndarray, topk_w: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # whole layer
 # ----------------------------------------------------------------------------
+def _groups(cfg):
+    return getattr(cfg, "n_group", 1), getattr(cfg, "topk_group", 1)
+
+
 def _storage(cfg) -> str:
     return "bf16" if cfg.dtype == "bf16" else "f32"
 
@@ -226,7 +265,7 @@ def forward(cfg, inp: dict, keep_h: bool = True) -> dict:
     a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
     x = a["x"]
     L = gate_logits(x, a["Wg"], a["bias"])
-    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k)
+    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k, *_groups(cfg))
     counts, offsets, pos, src = dispatch(idx, cfg.E)
     res = {"L": L, "topk_idx": idx, "topk_w": w, "counts": counts,
            "offsets": offsets, "pos": pos, "src": src}
@@ -265,7 +304,7 @@ def forward_tokens(cfg, inp: dict, tokens) -> dict:
     tokens = np.asarray(tokens, dtype=np.int64)
     x = a["x"][tokens]
     L = gate_logits(x, a["Wg"], a["bias"])
-    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k)
+    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k, *_groups(cfg))
     if cfg.payload_fp8:
         q, s = quantize_payload_fp8(x)
         x_hat = q * s[:, None]

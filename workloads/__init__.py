@@ -30,12 +30,13 @@ from dataclasses import dataclass, replace
 
 import torch
 
-__all__ = ["MoEConfig", "CONFIGS", "BENCH_CONFIG", "get_config", "make_inputs",
-           "ROUTER_RENORM", "ROUTER_PREK_SOFTMAX"]
+__all__ = ["MoEConfig", "CONFIGS", "VARIANTS", "BENCH_CONFIG", "get_config", "make_inputs",
+           "ROUTER_RENORM", "ROUTER_PREK_SOFTMAX", "ROUTER_GROUP_LIMITED"]
 
 # Router modes (mirrors the values in include/moe.h).
 ROUTER_RENORM = 0        # softmax over all E, keep top-k, divide by their sum
 ROUTER_PREK_SOFTMAX = 1  # softmax over the pre_k largest logits, keep top-k as is
+ROUTER_GROUP_LIMITED = 2  # top-k inside the topk_group best of n_group expert groups
 
 
 @dataclass(frozen=True)
@@ -49,6 +50,8 @@ class MoEConfig:
     dtype: str        # "f32" or "bf16": activations and weights
     router: int = ROUTER_RENORM
     pre_k: int = 8
+    n_group: int = 1          # expert groups (group-limited router only)
+    topk_group: int = 1       # groups kept per token (group-limited router only)
     payload_fp8: bool = False
     bias: str = "zero"        # "zero" | "normal" (variance bias_var) | "zipf" (exponent zipf_s)
     bias_var: float = 0.0
@@ -92,6 +95,18 @@ CONFIGS = {
         f=2048, dtype="bf16", bias="zipf", zipf_s=1.1, seed=4),
 }
 CONFIG_ORDER = list(CONFIGS)
+
+# Variants of the five shapes for the router and payload options the pages
+# describe besides the default path. Node-limited routing: the fine-grained
+# layer (256 experts, top-8) with its experts in 8 groups of 32 ("nodes") and
+# each token's 8 experts taken from its 4 best groups (DeepSeek V3/V4
+# parallel-strategy article, EP section).
+VARIANTS = {
+    "skewed_T16384_d7168_E256_k8_f2048_zipf_group8top4": MoEConfig(
+        "skewed_T16384_d7168_E256_k8_f2048_zipf_group8top4", T=16384, d=7168, E=256, k=8,
+        f=2048, dtype="bf16", router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=4,
+        bias="zipf", zipf_s=1.1, seed=4),
+}
 # The layer the headline throughput is quoted on (balanced, 8 experts).
 BENCH_CONFIG = CONFIG_ORDER[1]
 
@@ -99,6 +114,8 @@ BENCH_CONFIG = CONFIG_ORDER[1]
 def get_config(name: str) -> MoEConfig:
     if name in CONFIGS:
         return CONFIGS[name]
+    if name in VARIANTS:
+        return VARIANTS[name]
     # also accept a 1-based position ("1".."5") or a unique prefix
     if name.isdigit() and 1 <= int(name) <= len(CONFIG_ORDER):
         return CONFIGS[CONFIG_ORDER[int(name) - 1]]
