@@ -74,7 +74,15 @@ enum {
   /* exact softmax over the pre_k largest logits only; keep its first k
    * entries without renormalising (the partial top-8 router of the
    * DeepSeek-V4 EP article, section 3.2) */
-  MOE_ROUTER_PREK_SOFTMAX = 1
+  MOE_ROUTER_PREK_SOFTMAX = 1,
+  /* node-limited top-k (DeepSeek V3/V4 parallel-strategy article, EP
+   * section: a token's experts come from its best nodes only). The E experts
+   * form n_group equal groups of consecutive ids; a group's score is the
+   * mean softmax probability of its experts; the topk_group best groups are
+   * kept (equal scores: lower group id first); the k largest logits among
+   * the kept groups' experts are chosen (lower id first on ties) and
+   * weighted as in MOE_ROUTER_RENORM. pre_k is validated but not used. */
+  MOE_ROUTER_GROUP_LIMITED = 2
 };
 
 typedef struct moe_config {
@@ -87,6 +95,10 @@ typedef struct moe_config {
   int32_t router;      /* MOE_ROUTER_* */
   int32_t pre_k;       /* partial top-k width, k..min(8, E) (8 on the pages) */
   int32_t payload_fp8; /* 1: dispatch rows as FP8 E4M3 + fp32 scale (bf16 only) */
+  int32_t n_group;     /* MOE_ROUTER_GROUP_LIMITED: expert groups, 1..32, dividing E;
+                        * ignored by the other routers */
+  int32_t topk_group;  /* MOE_ROUTER_GROUP_LIMITED: groups kept per token,
+                        * 1..n_group, with k <= topk_group * E / n_group */
 } moe_config_t;
 
 /* Validate a configuration. Returns MOE_OK or MOE_ERR_INVALID_ARG /

@@ -19,12 +19,14 @@ MOE_DTYPE_F32 = 0
 MOE_DTYPE_BF16 = 1
 MOE_ROUTER_RENORM = 0
 MOE_ROUTER_PREK_SOFTMAX = 1
+MOE_ROUTER_GROUP_LIMITED = 2
 MOE_NUM_EVENTS = 7
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("T", "d", "E", "k", "f", "dtype", "router", "pre_k", "payload_fp8")]
+                ("T", "d", "E", "k", "f", "dtype", "router", "pre_k", "payload_fp8",
+                 "n_group", "topk_group")]
 
 
 class MoeForwardViews(ctypes.Structure):

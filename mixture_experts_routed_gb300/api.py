@@ -28,18 +28,20 @@ class MoEError(RuntimeError):
 
 
 def make_config(T, d, E, k, f, dtype="bf16", router=L.MOE_ROUTER_RENORM, pre_k=8,
-                payload_fp8=False) -> L.MoeConfig:
+                payload_fp8=False, n_group=1, topk_group=1) -> L.MoeConfig:
     dt = {"f32": L.MOE_DTYPE_F32, "fp32": L.MOE_DTYPE_F32, "bf16": L.MOE_DTYPE_BF16,
           torch.float32: L.MOE_DTYPE_F32, torch.bfloat16: L.MOE_DTYPE_BF16}[dtype]
     return L.MoeConfig(int(T), int(d), int(E), int(k), int(f), dt, int(router), int(pre_k),
-                       int(bool(payload_fp8)))
+                       int(bool(payload_fp8)), int(n_group), int(topk_group))
 
 
 def config_from(c) -> L.MoeConfig:
-    """From any object with T, d, E, k, f, dtype, router, pre_k, payload_fp8."""
+    """From any object with T, d, E, k, f, dtype, router, pre_k, payload_fp8
+    (and, optionally, n_group and topk_group)."""
     if isinstance(c, L.MoeConfig):
         return c
-    return make_config(c.T, c.d, c.E, c.k, c.f, c.dtype, c.router, c.pre_k, c.payload_fp8)
+    return make_config(c.T, c.d, c.E, c.k, c.f, c.dtype, c.router, c.pre_k, c.payload_fp8,
+                       getattr(c, "n_group", 1), getattr(c, "topk_group", 1))
 
 
 def _cfg(c):

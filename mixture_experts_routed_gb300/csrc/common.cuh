@@ -57,6 +57,18 @@ constexpr int kDispatchTokensPerChunk = 8;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 
+// Router parameters, as in moe_config_t. mode: 0 renormalised top-k, 1
+// softmax over the pre_k largest logits, 2 group-limited top-k (the k best
+// experts inside the topk_group best of n_group groups of consecutive ids).
+struct RouterSpec {
+  int k;
+  int pre_k;
+  int mode;
+  int n_group;
+  int topk_group;
+};
+constexpr int kMaxGroups = 32;
+
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -64,14 +76,14 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Gate GEMM + softmax + top-k, fused. `dtype` 0 = fp32, 1 = bf16. `err`
 // (nullable) receives kErrTimeout from the tensor-core gate.
 cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* bias, int T,
-                         int d, int E, int k, int pre_k, int router, int32_t* topk_idx,
+                         int d, int E, RouterSpec rs, int32_t* topk_idx,
                          float* topk_w, float* logits, uint32_t* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- gate_tc.cu
 // Tensor-core gate (bf16, E a multiple of 8 up to 256, 16-byte aligned x, W_g).
 bool gate_tc_supported(int dtype, int E, const void* Wg, const void* x);
 cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int T, int d, int E,
-                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           RouterSpec rs, int32_t* topk_idx, float* topk_w,
                            float* logits, uint32_t* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- dispatch.cu

@@ -64,8 +64,8 @@ static_assert(BM * (MAX_E + 1) * 4 <= OFF_BAR, "logits tile must fit over the st
 template <int EMAX>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                   const float* __restrict__ bias, int T, int d, int E, int k, int pre_k,
-                   int router, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                   const float* __restrict__ bias, int T, int d, int E, RouterSpec rs,
+                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
                    float* __restrict__ logits, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x < BM) {
     const int r = threadIdx.x;
     if (t0 + r < T)
-      topk::thread_select_and_weigh(Ls + r * (E + 1), E, k, pre_k, router, t0 + r, topk_idx,
+      topk::thread_select_and_weigh(Ls + r * (E + 1), E, rs, t0 + r, topk_idx,
                                     topk_w);
   }
   __syncthreads();
@@ -287,7 +287,7 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
 
 template <int EMAX>
 cudaError_t launch_emax(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int T,
-                        int d, int E, int k, int pre_k, int router, int32_t* idx, float* w,
+                        int d, int E, RouterSpec rs, int32_t* idx, float* w,
                         float* logits, uint32_t* err, cudaStream_t s) {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
@@ -297,7 +297,7 @@ cudaError_t launch_emax(const CUtensorMap& mx, const CUtensorMap& mw, const floa
   });
   if (st != cudaSuccess) return st;
   return launch_pdl(gate_tc_kernel<EMAX>, dim3(ceil_div(T, BM)), dim3(NUM_THREADS), SMEM_BYTES, s,
-                    mx, mw, bias, T, d, E, k, pre_k, router, idx, w, logits, err);
+                    mx, mw, bias, T, d, E, rs, idx, w, logits, err);
 }
 
 }  // namespace
@@ -309,7 +309,7 @@ bool gate_tc_supported(int dtype, int E, const void* Wg, const void* x) {
 }
 
 cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int T, int d, int E,
-                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           RouterSpec rs, int32_t* topk_idx, float* topk_w,
                            float* logits, uint32_t* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   CUtensorMap mx, mw;
@@ -320,12 +320,12 @@ cudaError_t launch_gate_tc(const void* x, const void* Wg, const float* bias, int
   if (!map_2d(&mw, Wg, static_cast<uint64_t>(d), static_cast<uint64_t>(E), 64, BK))
     return cudaErrorInvalidValue;
   if (E <= 64)
-    return launch_emax<64>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+    return launch_emax<64>(mx, mw, bias, T, d, E, rs, topk_idx, topk_w, logits,
                            err, s);
   if (E <= 128)
-    return launch_emax<128>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+    return launch_emax<128>(mx, mw, bias, T, d, E, rs, topk_idx, topk_w, logits,
                             err, s);
-  return launch_emax<256>(mx, mw, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits,
+  return launch_emax<256>(mx, mw, bias, T, d, E, rs, topk_idx, topk_w, logits,
                           err, s);
 }
 

@@ -23,8 +23,15 @@ int check_cfg(const moe_config_t* c) {
   if (c->d % 64 != 0 || c->f % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->router != MOE_ROUTER_RENORM && c->router != MOE_ROUTER_PREK_SOFTMAX)
+  if (c->router != MOE_ROUTER_RENORM && c->router != MOE_ROUTER_PREK_SOFTMAX &&
+      c->router != MOE_ROUTER_GROUP_LIMITED)
     return MOE_ERR_INVALID_ARG;
+  if (c->router == MOE_ROUTER_GROUP_LIMITED) {
+    if (c->n_group < 1 || c->n_group > kMaxGroups || c->E % c->n_group != 0)
+      return MOE_ERR_INVALID_ARG;
+    if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
+    if (c->k > c->topk_group * (c->E / c->n_group)) return MOE_ERR_INVALID_ARG;
+  }
   if (c->payload_fp8 != 0 && c->payload_fp8 != 1) return MOE_ERR_INVALID_ARG;
   const int max_pre = c->E < kMaxTopK ? c->E : kMaxTopK;
   if (c->pre_k < 1 || c->pre_k > max_pre) return MOE_ERR_INVALID_ARG;
@@ -102,8 +109,8 @@ void record(void* const* ev, int i, cudaStream_t s) {
 // ---------------------------------------------------------------- stages
 int run_route(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
               int32_t* idx, float* w, float* logits, uint32_t* err, cudaStream_t s) {
-  return status_of(launch_route(c.dtype, x, Wg, bias, c.T, c.d, c.E, c.k, c.pre_k, c.router,
-                                idx, w, logits, err, s));
+  const RouterSpec rs{c.k, c.pre_k, c.router, c.n_group, c.topk_group};
+  return status_of(launch_route(c.dtype, x, Wg, bias, c.T, c.d, c.E, rs, idx, w, logits, err, s));
 }
 
 int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x,

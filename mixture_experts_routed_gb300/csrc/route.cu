@@ -6,6 +6,9 @@
 //                  (= the full max-subtracted softmax of the chosen experts
 //                  divided by their sum)
 //   pre_k softmax: w_j = exp(L_j - L_max) / sum_{i<pre_k} exp(L_i - L_max)
+//   group-limited: as renorm, over the experts of the topk_group groups with
+//                  the best mean probability (DeepSeek V3/V4 parallel-
+//                  strategy article, EP section: the node limit)
 // The logits never go to HBM unless the caller asks for them.
 //
 // Two gate GEMM shapes:
@@ -44,7 +47,7 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162flo
 template <typename Tin, int NE, int TPB, bool VW>
 __global__ void __launch_bounds__(128) route_narrow_kernel(
     const Tin* __restrict__ x, const Tin* __restrict__ Wg, const float* __restrict__ bias, int T,
-    int d, int E, int k, int pre_k, int router, int32_t* __restrict__ topk_idx,
+    int d, int E, RouterSpec rs, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, float* __restrict__ logits) {
   constexpr int VEC = 16 / sizeof(Tin);  // elements per 16-byte load
   __shared__ float part[4][TPB][NE];
@@ -126,7 +129,8 @@ __global__ void __launch_bounds__(128) route_narrow_kernel(
     }
     float v[1] = {mine};
     int id[1] = {lane < E ? lane : 0x7fffffff};
-    warp_select_and_weigh<1>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+    if (rs.mode == topk::kRouterGroup) topk::warp_group_limit<1>(v, id, E, rs);
+    warp_select_and_weigh<1>(v, id, rs, t, topk_idx, topk_w);
   }
 }
 
@@ -144,7 +148,7 @@ constexpr int kTileBK = 32;
 template <typename Tin, int TM, int TE, int NTT, int KG, bool VW>
 __global__ void __launch_bounds__(256) route_tiled_kernel(
     const Tin* __restrict__ x, const Tin* __restrict__ Wg, const float* __restrict__ bias, int T,
-    int d, int E, int k, int pre_k, int router, int32_t* __restrict__ topk_idx,
+    int d, int E, RouterSpec rs, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, float* __restrict__ logits) {
   constexpr int NG = 256 / KG;     // threads per K group
   constexpr int NTE = NG / NTT;
@@ -327,13 +331,14 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(
       v[j] = (e < EP) ? Ls[r * EP + e] : -INFINITY;
       id[j] = (e < E) ? e : 0x7fffffff;
     }
-    warp_select_and_weigh<NJ>(v, id, k, pre_k, router, t, topk_idx, topk_w);
+    if (rs.mode == topk::kRouterGroup) topk::warp_group_limit<NJ>(v, id, E, rs);
+    warp_select_and_weigh<NJ>(v, id, rs, t, topk_idx, topk_w);
   }
 }
 
 template <typename Tin, int TM, int TE, int NTT, int KG, bool VW>
 cudaError_t launch_tiled_v(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
-                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           RouterSpec rs, int32_t* topk_idx, float* topk_w,
                            float* logits, cudaStream_t s) {
   constexpr int NTE = 256 / KG / NTT;
   constexpr int BT = NTT * TM, EP = NTE * TE;
@@ -349,35 +354,35 @@ cudaError_t launch_tiled_v(const Tin* x, const Tin* Wg, const float* bias, int T
     attr_set = true;
   }
   return launch_pdl(route_tiled_kernel<Tin, TM, TE, NTT, KG, VW>, dim3(ceil_div(T, BT)), dim3(256),
-                    smem, s, x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits);
+                    smem, s, x, Wg, bias, T, d, E, rs, topk_idx, topk_w, logits);
 }
 
 // W_g rows are read as 16-byte vectors only when every row starts 16-byte
 // aligned (aligned base and E * sizeof(Tin) a multiple of 16).
 template <typename Tin, int TM, int TE, int NTT, int KG = 1>
 cudaError_t launch_tiled(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
-                         int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                         RouterSpec rs, int32_t* topk_idx, float* topk_w,
                          float* logits, cudaStream_t s) {
   const bool vw = (reinterpret_cast<uintptr_t>(Wg) % 16 == 0) &&
                   ((static_cast<size_t>(E) * sizeof(Tin)) % 16 == 0);
   if (vw)
-    return launch_tiled_v<Tin, TM, TE, NTT, KG, true>(x, Wg, bias, T, d, E, k, pre_k, router,
+    return launch_tiled_v<Tin, TM, TE, NTT, KG, true>(x, Wg, bias, T, d, E, rs,
                                                       topk_idx, topk_w, logits, s);
-  return launch_tiled_v<Tin, TM, TE, NTT, KG, false>(x, Wg, bias, T, d, E, k, pre_k, router,
+  return launch_tiled_v<Tin, TM, TE, NTT, KG, false>(x, Wg, bias, T, d, E, rs,
                                                      topk_idx, topk_w, logits, s);
 }
 
 template <typename Tin>
 cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
-                           int k, int pre_k, int router, int32_t* topk_idx, float* topk_w,
+                           RouterSpec rs, int32_t* topk_idx, float* topk_w,
                            float* logits, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   if (E <= 32 && T >= 4096) {
     // 64 tokens per CTA, K split over 4 groups of 64 threads
     if (E <= 16)
-      return launch_tiled<Tin, 4, 4, 16, 4>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx,
+      return launch_tiled<Tin, 4, 4, 16, 4>(x, Wg, bias, T, d, E, rs, topk_idx,
                                             topk_w, logits, s);   // 64 tokens x 16 experts
-    return launch_tiled<Tin, 4, 4, 16, 2>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx,
+    return launch_tiled<Tin, 4, 4, 16, 2>(x, Wg, bias, T, d, E, rs, topk_idx,
                                           topk_w, logits, s);     // 64 tokens x 32 experts
   }
   if (E <= 32) {
@@ -388,7 +393,7 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
     const dim3 block(128);
 #define MOE_NARROW(NE, TPB, VW)                                                          \
   return launch_pdl(route_narrow_kernel<Tin, NE, TPB, VW>, dim3(ceil_div(T, TPB)), block, 0, s, \
-                    x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits)
+                    x, Wg, bias, T, d, E, rs, topk_idx, topk_w, logits)
 #define MOE_NARROW_E(TPB, VW) \
   do {                        \
     if (E <= 8)               \
@@ -405,13 +410,13 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
 #undef MOE_NARROW_E
 #undef MOE_NARROW
   } else if (E <= 64) {
-    return launch_tiled<Tin, 4, 2, 8>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w,
+    return launch_tiled<Tin, 4, 2, 8>(x, Wg, bias, T, d, E, rs, topk_idx, topk_w,
                                       logits, s);   // 32 tokens x 64 experts
   } else if (E <= 128) {
-    return launch_tiled<Tin, 4, 4, 8>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w,
+    return launch_tiled<Tin, 4, 4, 8>(x, Wg, bias, T, d, E, rs, topk_idx, topk_w,
                                       logits, s);   // 32 tokens x 128 experts
   } else {
-    return launch_tiled<Tin, 4, 8, 8>(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w,
+    return launch_tiled<Tin, 4, 8, 8>(x, Wg, bias, T, d, E, rs, topk_idx, topk_w,
                                       logits, s);   // 32 tokens x 256 experts
   }
   return cudaGetLastError();
@@ -420,20 +425,20 @@ cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T
 }  // namespace
 
 cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* bias, int T,
-                         int d, int E, int k, int pre_k, int router, int32_t* topk_idx,
+                         int d, int E, RouterSpec rs, int32_t* topk_idx,
                          float* topk_w, float* logits, uint32_t* err, cudaStream_t s) {
   // tensor-core gate: always for E a multiple of 64; for narrower gates only
   // with enough 128-token CTAs to fill the GPU (the SIMT kernels win on small
   // batches, e.g. T = 1024)
   if (T > 0 && gate_tc_supported(dtype, E, Wg, x) && (E % 64 == 0 || T >= 4096))
-    return launch_gate_tc(x, Wg, bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits, err,
+    return launch_gate_tc(x, Wg, bias, T, d, E, rs, topk_idx, topk_w, logits, err,
                           s);
   if (dtype == 0)
     return launch_route_t<float>(static_cast<const float*>(x), static_cast<const float*>(Wg),
-                                 bias, T, d, E, k, pre_k, router, topk_idx, topk_w, logits, s);
+                                 bias, T, d, E, rs, topk_idx, topk_w, logits, s);
   return launch_route_t<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
-                                       static_cast<const __nv_bfloat16*>(Wg), bias, T, d, E, k,
-                                       pre_k, router, topk_idx, topk_w, logits, s);
+                                       static_cast<const __nv_bfloat16*>(Wg), bias, T, d, E, rs,
+                                       topk_idx, topk_w, logits, s);
 }
 
 }  // namespace moe

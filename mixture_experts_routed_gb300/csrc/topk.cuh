@@ -1,8 +1,11 @@
-// topk.cuh - the router's selection and weighting step for one token, done
-// by one warp (DeepSeek-V4 EP article, section 3.2): pre_k rounds of a warp
-// argmax under (logit descending, lower expert id first), then the weights
-// from max-subtracted exponentials of the chosen logits. Shared by the SIMT
-// and tensor-core gate kernels.
+// topk.cuh - the router's selection and weighting step for one token
+// (DeepSeek-V4 EP article, section 3.2): the top pre_k (or k) logits under
+// (logit descending, lower expert id first), then the weights from
+// max-subtracted exponentials of the chosen logits. The group-limited mode
+// first drops every expert outside the topk_group groups with the best mean
+// probability (the node limit of the DeepSeek V3/V4 parallel-strategy
+// article, EP section). Two forms: one warp per token (SIMT gate kernels)
+// and one thread per token (tensor-core gate).
 #pragma once
 
 #include <cfloat>
@@ -14,28 +17,80 @@ namespace moe {
 namespace topk {
 
 constexpr int kRouterRenorm = 0;
+constexpr int kRouterPrek = 1;
+constexpr int kRouterGroup = 2;
 
-// Ranking rule: a beats b if a has the larger logit, or equal logits and the
-// lower expert id.
+// Ranking rule: a beats b if a has the larger value, or equal values and the
+// lower id (expert or group).
 __device__ __forceinline__ bool beats(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// Each lane holds NJ (logit, expert id) pairs; padding uses -inf and an id
-// >= E. Selects the top pre_k (or k, for renorm) by repeated warp argmax and
+// Selection rounds: the pre_k softmax router ranks pre_k experts, the others k.
+__device__ __forceinline__ int rounds_of(const RouterSpec& rs) {
+  return rs.mode == kRouterPrek ? rs.pre_k : rs.k;
+}
+
+// Group-limited mode, warp form: the lanes hold NJ (logit, id) pairs each
+// (padding: -inf and an id >= E). Group g (experts g*gs .. g*gs+gs-1, gs =
+// E/n_group) scores sum_e exp(L_e - L_max), which ranks the groups as their
+// mean probability does (common factors dropped). Experts outside the
+// topk_group best groups (ties: lower group id) get -inf, so the following
+// top-k sees only the kept groups.
+template <int NJ>
+__device__ __forceinline__ void warp_group_limit(float (&v)[NJ], const int (&id)[NJ], int E,
+                                                 const RouterSpec& rs) {
+  const int lane = threadIdx.x & 31;
+  const int ng = rs.n_group, gs = E / ng;
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) m = fmaxf(m, v[j]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float ex[NJ];
+  int grp[NJ];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    const bool real = id[j] < E;
+    ex[j] = real ? expf(v[j] - m) : 0.f;
+    grp[j] = real ? id[j] / gs : -1;
+  }
+  float mine = 0.f;  // lane g < ng: group g's score
+  for (int g = 0; g < ng; ++g) {
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) s += (grp[j] == g) ? ex[j] : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == g) mine = s;
+  }
+  int rank = 0;  // groups that beat this lane's group
+  for (int g = 0; g < ng; ++g) {
+    const float o = __shfl_sync(0xffffffffu, mine, g);
+    rank += beats(o, g, mine, lane) ? 1 : 0;
+  }
+  const uint32_t keep = __ballot_sync(0xffffffffu, lane < ng && rank < rs.topk_group);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j)
+    if (grp[j] >= 0 && !((keep >> grp[j]) & 1u)) v[j] = -INFINITY;
+}
+
+// Warp form: each lane holds NJ (logit, expert id) pairs; padding uses -inf
+// and an id >= E. Selects the top rounds_of(rs) by repeated warp argmax and
 // writes slots j < k of token t.
 template <int NJ>
 __device__ __forceinline__ void warp_select_and_weigh(const float (&v)[NJ], const int (&id)[NJ],
-                                                      int k, int pre_k, int router, int t,
+                                                      const RouterSpec& rs, int t,
                                                       int32_t* __restrict__ topk_idx,
                                                       float* __restrict__ topk_w) {
   const int lane = threadIdx.x & 31;
+  const int k = rs.k;
   bool taken[NJ];
 #pragma unroll
   for (int j = 0; j < NJ; ++j) taken[j] = false;
   float sel_v[kMaxTopK];
   int sel_i[kMaxTopK];
-  const int rounds = (router == kRouterRenorm) ? k : pre_k;
+  const int rounds = rounds_of(rs);
 #pragma unroll
   for (int s = 0; s < kMaxTopK; ++s) {
     sel_v[s] = -FLT_MAX;
@@ -83,99 +138,43 @@ __device__ __forceinline__ void warp_select_and_weigh(const float (&v)[NJ], cons
   }
 }
 
-// The same selection and weights for G tokens at once in one warp: token g's
-// logits in v[g] (padding as above), written when valid[g]. The G tokens'
-// butterflies are interleaved (the one-token form is bound by shuffle
-// latency); the arithmetic per token, and so every result, is that of
-// warp_select_and_weigh.
-template <int NJ, int G>
-__device__ __forceinline__ void warp_select_and_weigh_g(const float (&v)[G][NJ],
-                                                        const int (&id)[G][NJ], int k, int pre_k,
-                                                        int router, const int (&t)[G],
-                                                        const bool (&valid)[G],
-                                                        int32_t* __restrict__ topk_idx,
-                                                        float* __restrict__ topk_w) {
-  static_assert(NJ <= 32, "taken bits");
-  const int lane = threadIdx.x & 31;
-  uint32_t taken[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) taken[g] = 0u;
-  float sel_v[G][kMaxTopK];
-  int sel_i[G][kMaxTopK];
-  const int rounds = (router == kRouterRenorm) ? k : pre_k;
-#pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      sel_v[g][s] = -FLT_MAX;
-      sel_i[g][s] = 0x7fffffff;
-    }
-    if (s < rounds) {
-      float bv[G];
-      int bi[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        bv[g] = -INFINITY;
-        bi[g] = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < NJ; ++j)
-          if (!((taken[g] >> j) & 1u) && beats(v[g][j], id[g][j], bv[g], bi[g])) {
-            bv[g] = v[g][j];
-            bi[g] = id[g][j];
-          }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv[g], off);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi[g], off);
-          if (beats(ov, oi, bv[g], bi[g])) {
-            bv[g] = ov;
-            bi[g] = oi;
-          }
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        sel_v[g][s] = bv[g];
-        sel_i[g][s] = bi[g];
-#pragma unroll
-        for (int j = 0; j < NJ; ++j)
-          if (id[g][j] == bi[g]) taken[g] |= 1u << j;
-      }
-    }
+// Group-limited mode, thread form: the bit mask of the kept groups of one
+// logits row (same scores and ranking as warp_group_limit).
+__device__ __forceinline__ uint32_t thread_group_keep(const float* row, int E,
+                                                      const RouterSpec& rs) {
+  const int ng = rs.n_group, gs = E / ng;
+  float m = -INFINITY;
+  for (int e = 0; e < E; ++e) m = fmaxf(m, row[e]);
+  float sg[kMaxGroups];
+  for (int g = 0; g < ng; ++g) {
+    float s = 0.f;
+    for (int e = g * gs; e < (g + 1) * gs; ++e) s += expf(row[e] - m);
+    sg[g] = s;
   }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float m = sel_v[g][0];
-    float den = 0.f;
-    float ex[kMaxTopK];
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      ex[s] = (s < rounds) ? expf(sel_v[g][s] - m) : 0.f;
-      den += ex[s];
-    }
-#pragma unroll
-    for (int s = 0; s < kMaxTopK; ++s) {
-      if (valid[g] && s < k && lane == s) {
-        topk_idx[static_cast<size_t>(t[g]) * k + s] = sel_i[g][s];
-        topk_w[static_cast<size_t>(t[g]) * k + s] = ex[s] / den;
-      }
-    }
+  uint32_t keep = 0u;
+  for (int g = 0; g < ng; ++g) {
+    int rank = 0;
+    for (int h = 0; h < ng; ++h) rank += beats(sg[h], h, sg[g], g) ? 1 : 0;
+    if (rank < rs.topk_group) keep |= 1u << g;
   }
+  return keep;
 }
 
-// One thread per token: scan the token's E logits (row[e], e ascending) and
-// keep the best kMaxTopK in a sorted list; the weights as above. Experts
+// Thread form: one thread per token scans the token's E logits (row[e], e
+// ascending; in the group-limited mode only the kept groups' experts) and
+// keeps the best kMaxTopK in a sorted list; the weights as above. Experts
 // arrive in increasing id, so a logit equal to one already listed ranks
 // after it and the insertion test is a strict `>`. The same ranking and the
-// same weight arithmetic as the warp forms, without a warp-wide argmax per
-// round (the warp forms spend ~1k instructions a token at pre_k = 8).
-__device__ __forceinline__ void thread_select_and_weigh(const float* row, int E, int k, int pre_k,
-                                                        int router, int t,
+// same weight arithmetic as the warp form, without a warp-wide argmax per
+// round (the warp form spends ~1k instructions a token at pre_k = 8).
+__device__ __forceinline__ void thread_select_and_weigh(const float* row, int E,
+                                                        const RouterSpec& rs, int t,
                                                         int32_t* __restrict__ topk_idx,
                                                         float* __restrict__ topk_w) {
+  const int k = rs.k;
+  const bool grouped = rs.mode == kRouterGroup;
+  const int ng = grouped ? rs.n_group : 1, gs = E / ng;
+  const uint32_t keep = grouped ? thread_group_keep(row, E, rs) : 1u;
   float sv[kMaxTopK];
   int si[kMaxTopK];
 #pragma unroll
@@ -183,24 +182,27 @@ __device__ __forceinline__ void thread_select_and_weigh(const float* row, int E,
     sv[j] = -INFINITY;
     si[j] = 0x7fffffff;
   }
-  for (int e = 0; e < E; ++e) {
-    const float v = row[e];
-    if (v > sv[kMaxTopK - 1]) {
-      // shift the entries below the insertion point down by one
+  for (int g = 0; g < ng; ++g) {
+    if (!((keep >> g) & 1u)) continue;
+    for (int e = g * gs; e < (g + 1) * gs; ++e) {
+      const float v = row[e];
+      if (v > sv[kMaxTopK - 1]) {
+        // shift the entries below the insertion point down by one
 #pragma unroll
-      for (int j = kMaxTopK - 1; j > 0; --j) {
-        const bool down = v > sv[j - 1];
-        const bool here = !down && v > sv[j];
-        sv[j] = down ? sv[j - 1] : (here ? v : sv[j]);
-        si[j] = down ? si[j - 1] : (here ? e : si[j]);
-      }
-      if (v > sv[0]) {
-        sv[0] = v;
-        si[0] = e;
+        for (int j = kMaxTopK - 1; j > 0; --j) {
+          const bool down = v > sv[j - 1];
+          const bool here = !down && v > sv[j];
+          sv[j] = down ? sv[j - 1] : (here ? v : sv[j]);
+          si[j] = down ? si[j - 1] : (here ? e : si[j]);
+        }
+        if (v > sv[0]) {
+          sv[0] = v;
+          si[0] = e;
+        }
       }
     }
   }
-  const int rounds = (router == kRouterRenorm) ? k : pre_k;
+  const int rounds = rounds_of(rs);
   const float m = sv[0];
   float den = 0.f;
   float ex[kMaxTopK];

@@ -11,7 +11,8 @@ import numpy as np
 import torch
 
 import oracle
-from workloads import CONFIGS, CONFIG_ORDER, MoEConfig, ROUTER_PREK_SOFTMAX
+from workloads import (CONFIGS, CONFIG_ORDER, VARIANTS, MoEConfig, ROUTER_PREK_SOFTMAX,
+                       ROUTER_GROUP_LIMITED)
 
 # Small shapes that exercise ragged tails, partial tiles and degenerate cases.
 SMALL = {
@@ -86,11 +87,40 @@ SMALL = {
     "gate_E40_T4096_d320_k3_f128": MoEConfig("gate_E40_T4096_d320_k3_f128", T=4096, d=320,
                                              E=40, k=3, f=128, dtype="bf16", bias="normal",
                                              bias_var=1.0, seed=31),
+    # group-limited router on each gate kernel: narrow (E <= 32, bf16 and
+    # fp32), tiled (fp32, E = 64, bias), tensor-core (E = 256 Zipf; E = 128
+    # in 32 groups of 4; E = 16 at T >= 4096 with groups of 2); fp32 E = 16
+    # at T >= 4096 takes the K-split tiled kernel
+    "group_E16_T300_d256_k2_f128_g4top2": MoEConfig(
+        "group_E16_T300_d256_k2_f128_g4top2", T=300, d=256, E=16, k=2, f=128, dtype="bf16",
+        router=ROUTER_GROUP_LIMITED, n_group=4, topk_group=2, seed=40),
+    "group_f32_E8_T256_d128_k2_f256_g4top2": MoEConfig(
+        "group_f32_E8_T256_d128_k2_f256_g4top2", T=256, d=128, E=8, k=2, f=256, dtype="f32",
+        router=ROUTER_GROUP_LIMITED, n_group=4, topk_group=2, seed=41),
+    "group_f32_E64_T500_d256_k4_f128_g8top3": MoEConfig(
+        "group_f32_E64_T500_d256_k4_f128_g8top3", T=500, d=256, E=64, k=4, f=128, dtype="f32",
+        router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=3, bias="normal", bias_var=0.5,
+        seed=42),
+    "group_E256_T1100_d512_k8_f128_g8top4_zipf": MoEConfig(
+        "group_E256_T1100_d512_k8_f128_g8top4_zipf", T=1100, d=512, E=256, k=8, f=128,
+        dtype="bf16", router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=4, bias="zipf",
+        zipf_s=1.1, seed=43),
+    "group_E128_T600_d256_k6_f128_g32top3": MoEConfig(
+        "group_E128_T600_d256_k6_f128_g32top3", T=600, d=256, E=128, k=6, f=128,
+        dtype="bf16", router=ROUTER_GROUP_LIMITED, n_group=32, topk_group=3, seed=44),
+    "group_E16_T4100_d256_k2_f128_g8top1": MoEConfig(
+        "group_E16_T4100_d256_k2_f128_g8top1", T=4100, d=256, E=16, k=2, f=128, dtype="bf16",
+        router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=1, seed=45),
+    "group_f32_E16_T4100_d128_k3_f128_g4top2": MoEConfig(
+        "group_f32_E16_T4100_d128_k3_f128_g4top2", T=4100, d=128, E=16, k=3, f=128,
+        dtype="f32", router=ROUTER_GROUP_LIMITED, n_group=4, topk_group=2, seed=46),
 }
 ALL = dict(SMALL)
 ALL.update(CONFIGS)
+ALL.update(VARIANTS)
 SMALL_NAMES = list(SMALL)
 FULL_NAMES = CONFIG_ORDER
+VARIANT_NAMES = list(VARIANTS)
 # configs whose whole-layer oracle is cheap enough to run on every token
 ORACLE_FULL_OK = set(SMALL_NAMES) | {CONFIG_ORDER[0], CONFIG_ORDER[1]}
 
@@ -113,7 +143,7 @@ def make(cfg):
 def oracle_route(name: str):
     cfg, inp, host = layer(name)
     L = oracle.gate_logits(host["x"], host["Wg"], host["bias"])
-    idx, w = oracle.route(L, cfg.k, cfg.router, cfg.pre_k)
+    idx, w = oracle.route(L, cfg.k, cfg.router, cfg.pre_k, cfg.n_group, cfg.topk_group)
     return L, idx, w
 
 

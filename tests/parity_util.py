@@ -17,6 +17,11 @@ F32_MAX_ABS = 1e-5
 W_MAX_ABS = 1e-6
 LOGIT_MAX_ABS = 1e-5
 TIE_GAP = 1e-5
+# Group-limited router: two group scores (sums of fp32 exponentials of
+# logits that are themselves good to ~1e-5) closer than this relative gap
+# count as tied.
+GROUP_TIE_REL = 5e-5
+ROUTER_GROUP_LIMITED = 2
 
 
 def to_np(t: torch.Tensor) -> np.ndarray:
@@ -67,6 +72,48 @@ def near_tie_tokens(L64: np.ndarray, k: int) -> np.ndarray:
     return gaps.min(axis=1) < TIE_GAP
 
 
+def group_scores(L64: np.ndarray, n_group: int) -> np.ndarray:
+    """sum over each group's experts of exp(L - max L): ranks the groups as
+    their mean softmax probability does."""
+    T, E = L64.shape
+    z = np.exp(L64 - L64.max(axis=1, keepdims=True))
+    return z.reshape(T, n_group, E // n_group).sum(axis=2)
+
+
+def near_tie_tokens_group(L64: np.ndarray, cfg) -> np.ndarray:
+    """Group-limited router: tokens whose topk_group-th and next group scores
+    are within GROUP_TIE_REL, or whose top k+1 logits inside the kept groups
+    hold two within TIE_GAP."""
+    T, E = L64.shape
+    G, M = cfg.n_group, cfg.topk_group
+    gs = E // G
+    sc = group_scores(L64, G)
+    order = np.lexsort((np.broadcast_to(np.arange(G), (T, G)), -sc), axis=1)
+    tie = np.zeros(T, dtype=bool)
+    if M < G:
+        a = sc[np.arange(T), order[:, M - 1]]
+        b = sc[np.arange(T), order[:, M]]
+        tie |= (a - b) <= GROUP_TIE_REL * a
+    allowed = np.zeros((T, E), dtype=bool)
+    for j in range(M):
+        g = order[:, j]
+        for i in range(gs):
+            allowed[np.arange(T), g * gs + i] = True
+    Lk = np.where(allowed, L64, -np.inf)
+    m = min(cfg.k + 1, M * gs)
+    if m >= 2:
+        top = -np.sort(-Lk, axis=1)[:, :m]
+        tie |= (top[:, :-1] - top[:, 1:]).min(axis=1) < TIE_GAP
+    return tie
+
+
+def route_ties(cfg, L64: np.ndarray) -> np.ndarray:
+    """Tokens whose routing fp32 cannot decide reliably, for any router."""
+    if getattr(cfg, "router", 0) == ROUTER_GROUP_LIMITED:
+        return near_tie_tokens_group(L64, cfg)
+    return near_tie_tokens(L64, cfg.k)
+
+
 def topk_of(L: np.ndarray, k: int) -> np.ndarray:
     """Top-k by (value desc, id asc), written independently of the oracle."""
     T, E = L.shape
@@ -80,13 +127,15 @@ def check_route(cfg, L_oracle, idx_oracle, w_oracle, L_gpu, idx_gpu, w_gpu):
     L_gpu = np.asarray(L_gpu, np.float64)
     dl = np.max(np.abs(L_gpu - L_oracle))
     assert dl <= LOGIT_MAX_ABS, f"logits max-abs {dl:.3e}"
-    tie = near_tie_tokens(L_oracle, cfg.k)
+    tie = route_ties(cfg, L_oracle)
     clear = ~tie
     assert np.array_equal(idx_gpu[clear], idx_oracle[clear]), \
         f"{int((idx_gpu[clear] != idx_oracle[clear]).any(1).sum())} clear tokens routed differently"
     dw = np.max(np.abs(w_gpu[clear] - w_oracle[clear])) if clear.any() else 0.0
     assert dw <= W_MAX_ABS, f"weights max-abs {dw:.3e}"
-    if tie.any():
+    if tie.any() and getattr(cfg, "router", 0) == ROUTER_GROUP_LIMITED:
+        _check_group_choice(cfg, L_gpu[tie], idx_gpu[tie], w_gpu[tie])
+    elif tie.any():
         # the GPU's choice must be the exact top-k of its own logits
         own = topk_of(L_gpu[tie], cfg.k)
         assert np.array_equal(idx_gpu[tie], own)
@@ -94,3 +143,27 @@ def check_route(cfg, L_oracle, idx_oracle, w_oracle, L_gpu, idx_gpu, w_gpu):
         dw_t = np.max(np.abs(w_gpu[tie][same] - w_oracle[tie][same])) if same.any() else 0.0
         assert dw_t <= W_MAX_ABS
     return int(tie.sum())
+
+
+def _check_group_choice(cfg, L_own, idx, w):
+    """A group-limited choice is valid for the GPU's own logits when its
+    experts come from at most topk_group groups, each scoring within
+    GROUP_TIE_REL of the topk_group-th best, when they are the top k of the
+    union of their own groups, and when the weights are those logits'
+    renormalised softmax."""
+    L_own = np.asarray(L_own, np.float64)
+    n, E = L_own.shape
+    G, M, k = cfg.n_group, cfg.topk_group, cfg.k
+    gs = E // G
+    sc = group_scores(L_own, G)
+    thr = -np.sort(-sc, axis=1)[:, M - 1]
+    for t in range(n):
+        groups = sorted(set(int(e) // gs for e in idx[t]))
+        assert len(groups) <= M, (t, idx[t])
+        assert all(sc[t, g] >= thr[t] * (1 - GROUP_TIE_REL) for g in groups), (t, idx[t])
+        cand = np.array([e for g in groups for e in range(g * gs, (g + 1) * gs)])
+        sub = L_own[t, cand]
+        best = cand[np.lexsort((cand, -sub))[:k]]
+        assert list(idx[t]) == list(best), (t, idx[t], best)
+        z = np.exp(L_own[t, idx[t]] - L_own[t, idx[t]].max())
+        assert np.max(np.abs(w[t] - z / z.sum())) <= W_MAX_ABS

@@ -53,7 +53,8 @@ def test_only_abi_symbols_are_exported(lib):
 
 
 def cfg(**kw):
-    base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0)
+    base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0,
+                n_group=0, topk_group=0)
     base.update(kw)
     return L.MoeConfig(*[base[n] for n, _ in L.MoeConfig._fields_])
 
@@ -76,7 +77,20 @@ def cfg(**kw):
     (dict(k=3, pre_k=2), L.MOE_ERR_INVALID_ARG),
     (dict(E=4, k=2, pre_k=8), L.MOE_ERR_INVALID_ARG),
     (dict(dtype=2), L.MOE_ERR_INVALID_ARG),
+    (dict(router=3), L.MOE_ERR_INVALID_ARG),
+    # group-limited router: n_group | E, 1 <= topk_group <= n_group <= 32,
+    # k <= topk_group * E / n_group; the other routers ignore both fields
+    (dict(router=2, n_group=4, topk_group=2), L.MOE_OK),
+    (dict(router=2, E=256, k=8, n_group=8, topk_group=4), L.MOE_OK),
+    (dict(router=2, E=256, k=8, n_group=32, topk_group=1), L.MOE_OK),
+    (dict(router=2, n_group=1, topk_group=1), L.MOE_OK),
     (dict(router=2), L.MOE_ERR_INVALID_ARG),
+    (dict(router=2, n_group=3, topk_group=1), L.MOE_ERR_INVALID_ARG),
+    (dict(router=2, E=256, k=8, n_group=64, topk_group=8), L.MOE_ERR_INVALID_ARG),
+    (dict(router=2, n_group=4, topk_group=0), L.MOE_ERR_INVALID_ARG),
+    (dict(router=2, n_group=4, topk_group=5), L.MOE_ERR_INVALID_ARG),
+    (dict(router=2, k=3, n_group=4, topk_group=1), L.MOE_ERR_INVALID_ARG),
+    (dict(router=0, n_group=3, topk_group=7), L.MOE_OK),
     (dict(payload_fp8=2), L.MOE_ERR_INVALID_ARG),
     (dict(payload_fp8=1, dtype=0), L.MOE_ERR_UNSUPPORTED),
     (dict(T=1 << 30, k=8), L.MOE_ERR_UNSUPPORTED),

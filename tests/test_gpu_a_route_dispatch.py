@@ -7,11 +7,11 @@ import torch
 
 import oracle
 import mixture_experts_routed_gb300 as moe
-from gpu_layers import SMALL_NAMES, FULL_NAMES, layer, oracle_route, oracle_dispatch
+from gpu_layers import SMALL_NAMES, FULL_NAMES, VARIANT_NAMES, layer, oracle_route, oracle_dispatch
 from parity_util import check_route, bits, to_np
 
 pytestmark = pytest.mark.gpu
-NAMES = SMALL_NAMES + FULL_NAMES
+NAMES = SMALL_NAMES + FULL_NAMES + VARIANT_NAMES
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -22,7 +22,7 @@ def test_route_parity(cuda_ok, name):
     L, idx_o, w_o = oracle_route(name)
     n_tie = check_route(cfg, L, idx_o, w_o, to_np(logits), to_np(idx), to_np(w))
     print(f"{name}: near-tie tokens {n_tie}")
-    if cfg.router == 0:
+    if cfg.router in (0, 2):      # renormalised weights
         assert np.all(np.abs(to_np(w).sum(1) - 1.0) <= 1e-6)
 
 
