@@ -184,16 +184,25 @@ def dispatch(topk_idx: np.ndarray, E: int):
 # FP8 payload [SYNC-TAX 3.1]: per-token scale so the token's largest magnitude
 # maps to the E4M3 maximum; symmetric (absmax) form, fp32 scale.
 # ----------------------------------------------------------------------------
-def quantize_payload_fp8(x_rows: np.ndarray):
+def quantize_payload_fp8(x_rows: np.ndarray, static_scale: float | None = None):
     """Per row t: a = max |x_t| (fp32), s = fp32(a / 448) with an fp32 IEEE
     division (s = 1 for an all-zero row), q = E4M3(fp32(x / s)) with an fp32
     IEEE division, rounded to nearest even and saturated to +-448.
 
+    With ``static_scale`` (the "static global" variant [SYNC-TAX 3.1]: one
+    scale fixed ahead of time for the whole tensor), s = fp32(static_scale)
+    for every row and no absmax is taken; values beyond 448 s saturate.
+
     Returns (q as fp64 E4M3 values [T, d], s as fp64 holding fp32 values [T])."""
     x32 = np.asarray(x_rows, np.float64).astype(np.float32)
-    a = np.abs(x32).max(axis=1)
-    s = (a / E4M3_MAX_F32).astype(np.float32)
-    s = np.where(a == 0, np.float32(1.0), s).astype(np.float32)
+    if static_scale is not None:
+        s = np.full(x32.shape[0], np.float32(static_scale), dtype=np.float32)
+        if not (np.isfinite(s).all() and (s > 0).all()):
+            raise ValueError("static scale must be finite and positive")
+    else:
+        a = np.abs(x32).max(axis=1)
+        s = (a / E4M3_MAX_F32).astype(np.float32)
+        s = np.where(a == 0, np.float32(1.0), s).astype(np.float32)
     ratio = (x32 / s[:, None]).astype(np.float32)     # fp32 division, RN
     q = e4m3_round_satfinite(ratio.astype(np.float64))
     return q, s.astype(np.float64)
@@ -246,6 +255,15 @@ def _groups(cfg):
     return getattr(cfg, "n_group", 1), getattr(cfg, "topk_group", 1)
 
 
+def _payload(cfg, x):
+    """The rows the experts see and the payload: (x_hat, q, s) or (x, None, None)."""
+    if not cfg.payload_fp8:
+        return x, None, None
+    static = getattr(cfg, "payload_scale", 0.0) if int(cfg.payload_fp8) == 2 else None
+    q, s = quantize_payload_fp8(x, static)
+    return q * s[:, None], q, s
+
+
 def _storage(cfg) -> str:
     return "bf16" if cfg.dtype == "bf16" else "f32"
 
@@ -269,13 +287,10 @@ def forward(cfg, inp: dict, keep_h: bool = True) -> dict:
     counts, offsets, pos, src = dispatch(idx, cfg.E)
     res = {"L": L, "topk_idx": idx, "topk_w": w, "counts": counts,
            "offsets": offsets, "pos": pos, "src": src}
-    if cfg.payload_fp8:
-        q_tok, s_tok = quantize_payload_fp8(x)
+    x_hat_tok, q_tok, s_tok = _payload(cfg, x)
+    if q_tok is not None:
         res["q"] = q_tok[src]
         res["scale"] = s_tok[src]
-        x_hat_tok = q_tok * s_tok[:, None]
-    else:
-        x_hat_tok = x
     R = idx.size
     Y = np.zeros((R, cfg.d), dtype=np.float64)
     H = np.zeros((R, cfg.f), dtype=np.float64) if keep_h else None
@@ -305,11 +320,7 @@ def forward_tokens(cfg, inp: dict, tokens) -> dict:
     x = a["x"][tokens]
     L = gate_logits(x, a["Wg"], a["bias"])
     idx, w = route(L, cfg.k, cfg.router, cfg.pre_k, *_groups(cfg))
-    if cfg.payload_fp8:
-        q, s = quantize_payload_fp8(x)
-        x_hat = q * s[:, None]
-    else:
-        x_hat = x
+    x_hat, _, _ = _payload(cfg, x)
     n, k = idx.shape
     y_slot = np.zeros((n, k, cfg.d), dtype=np.float64)
     for e in np.unique(idx):

@@ -104,3 +104,40 @@ def test_payload_quantisation_uses_fp32_division():
     st = torch.from_numpy(s.astype(np.float32))
     ref = (x / st[:, None]).clamp(-448, 448).to(torch.float8_e4m3fn).double().numpy()
     assert np.array_equal(q, ref)
+
+
+# ---- static global scale (the sync-tax article's "static global" FP8
+# variant: one scale fixed ahead of time for the whole tensor)
+def test_static_scale_equal_to_absmax_scale_reproduces_dynamic():
+    x = torch.randn(1, 512).to(torch.bfloat16).float().numpy().astype(np.float64)
+    qd, sd = quantize_payload_fp8(x)
+    qs, ss = quantize_payload_fp8(x, static_scale=float(sd[0]))
+    assert np.array_equal(qd, qs) and np.array_equal(sd, ss)
+
+
+def test_static_scale_worked_values():
+    # s = 0.5: 1 -> 2; 224 -> 448; 300 -> 600 saturates to 448; -2^-7 -> -2^-6
+    # (exact: E4M3's smallest normal); 8.5 -> 17, halfway between 16 and 18
+    # (spacing 2 at exponent 4) -> 16, the even mantissa; 9.5 -> 19 -> 20
+    x = np.array([[1.0, 224.0, 300.0, -2.0 ** -7, 8.5, 9.5, -1000.0, 0.0]])
+    q, s = quantize_payload_fp8(x, static_scale=0.5)
+    assert s.tolist() == [0.5]
+    assert q[0].tolist() == [2.0, 448.0, 448.0, -2.0 ** -6, 16.0, 20.0, -448.0, 0.0]
+
+
+def test_static_scale_is_one_scale_for_every_row():
+    rng = np.random.default_rng(5)
+    x = torch.randn(16, 128).to(torch.bfloat16).float().numpy().astype(np.float64)
+    x[2] = 0.0
+    scale = float(np.float32(20.0 / 448.0))
+    q, s = quantize_payload_fp8(x, static_scale=scale)
+    assert np.all(s == np.float32(scale))            # the all-zero row too
+    st = torch.full((16, 1), scale, dtype=torch.float32)
+    ref = (torch.from_numpy(x).float() / st).clamp(-448, 448).to(torch.float8_e4m3fn)
+    assert np.array_equal(q, ref.double().numpy())
+
+
+@pytest.mark.parametrize("bad", [0.0, -1.0, float("inf"), float("nan")])
+def test_static_scale_rejects_bad_values(bad):
+    with pytest.raises(ValueError):
+        quantize_payload_fp8(np.ones((2, 8)), static_scale=bad)

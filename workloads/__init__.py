@@ -52,7 +52,8 @@ class MoEConfig:
     pre_k: int = 8
     n_group: int = 1          # expert groups (group-limited router only)
     topk_group: int = 1       # groups kept per token (group-limited router only)
-    payload_fp8: bool = False
+    payload_fp8: int = 0      # 0 none, 1 per-token absmax FP8, 2 FP8 with one static scale
+    payload_scale: float = 0.0  # the static scale (payload_fp8 == 2)
     bias: str = "zero"        # "zero" | "normal" (variance bias_var) | "zipf" (exponent zipf_s)
     bias_var: float = 0.0
     zipf_s: float = 0.0
@@ -101,7 +102,14 @@ CONFIG_ORDER = list(CONFIGS)
 # layer (256 experts, top-8) with its experts in 8 groups of 32 ("nodes") and
 # each token's 8 experts taken from its 4 best groups (DeepSeek V3/V4
 # parallel-strategy article, EP section).
+# Static global FP8 scale (sync-tax article, section 3.1, "static global"):
+# the wide layer with one payload scale fixed ahead of time, 20/448, so the
+# largest magnitude in the data (the +-20 outliers) maps to the E4M3 maximum.
 VARIANTS = {
+    "wide_fp8static_T16384_d5120_E16_k2_f1536": MoEConfig(
+        "wide_fp8static_T16384_d5120_E16_k2_f1536", T=32 * 512, d=5120, E=16, k=2,
+        f=1536, dtype="bf16", payload_fp8=2, payload_scale=20.0 / 448.0, outlier_rate=1e-3,
+        outlier_mag=20.0, seed=3),
     "skewed_T16384_d7168_E256_k8_f2048_zipf_group8top4": MoEConfig(
         "skewed_T16384_d7168_E256_k8_f2048_zipf_group8top4", T=16384, d=7168, E=256, k=8,
         f=2048, dtype="bf16", router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=4,
