@@ -18,6 +18,7 @@ source pages give, with no blocking, fusion or reordering:
   payload   optional per-token absmax FP8 E4M3                  (sync-tax, sec. 3.1)
   FFN       h = SiLU(x W1_e), y = h W2_e     ("L1 + Act + L2", V3/V4 parallel
             strategy article, Waved-EP section)
+  payload   optional FP8 expert outputs, per-row min/max affine (sync-tax, 3.1)
   combine   out_t = sum_j w_tj y_(t,j)       (sync-tax article, sec. 2.3)
 
 Pins (tests/test_oracle_*.py) tie it to brute force, closed forms, special
@@ -25,7 +26,8 @@ cases and library routines; the FFN/combine absolute values are pinned only by
 those special cases (dense FFN when E = 1, identical experts, linearity).
 """
 from .moe_oracle import (  # noqa: F401
-    gate_logits, route, dispatch, quantize_payload_fp8, expert_ffn_rows,
+    gate_logits, route, dispatch, quantize_payload_fp8, quantize_output_fp8,
+    dequantize_output_fp8, expert_ffn_rows,
     combine, forward, forward_tokens, inputs_to_numpy, ROUTER_RENORM,
     ROUTER_PREK_SOFTMAX, ROUTER_GROUP_LIMITED,
 )

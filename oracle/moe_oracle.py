@@ -10,7 +10,8 @@ page references name the article and its section:
              weights laid out contiguously by expert id).
   [SYNC-TAX] "Deepseek-MoE sync tax", sections 2.1 (top-k gating, per-
              destination packed buffers), 2.3 (weighted sum of the k expert
-             outputs per token), 3.1 (per-token FP8 payload quantisation).
+             outputs per token), 3.1 (per-token FP8 payload quantisation of
+             expert inputs and, by min/max affine maps, expert outputs).
   [V3V4-PAR] "DeepSeek V3/V4 parallel strategy", EP and Waved-EP sections
              (dispatch, expert L1 + Act + L2, combine; the V3 limit of a
              token's 8 experts to the 4 nodes that are best on average).
@@ -209,6 +210,40 @@ def quantize_payload_fp8(x_rows: np.ndarray, static_scale: float | None = None):
 
 
 # ----------------------------------------------------------------------------
+# FP8 expert-output payload [SYNC-TAX 3.1]: each expert output vector is
+# quantised on its own, from its min and max, by an affine map.
+# ----------------------------------------------------------------------------
+def quantize_output_fp8(Y_rows: np.ndarray):
+    """Per row r of the fp32 expert outputs y: mn = min y, mx = max y;
+    zero = fp32(mx/2 + mn/2) and half = fp32(mx/2 - mn/2) (each a single fp32
+    rounding; halving is exact); s = fp32(half / 448) with an fp32 IEEE
+    division (s = 1 for a constant row); q = E4M3(fp32(fp32(y - zero) / s)),
+    rounded to nearest even and saturated to +-448. The row decodes as
+    q * s + zero, so [mn, mx] spans the E4M3 range [-448, 448].
+
+    Returns (q as fp64 E4M3 values [R, d], s and zero as fp64 holding fp32
+    values [R])."""
+    y = np.asarray(Y_rows, np.float64).astype(np.float32)
+    half_f = np.float32(0.5)
+    mn = y.min(axis=1)
+    mx = y.max(axis=1)
+    zero = (mx * half_f + mn * half_f).astype(np.float32)
+    half = (mx * half_f - mn * half_f).astype(np.float32)
+    s = (half / E4M3_MAX_F32).astype(np.float32)
+    s = np.where(half == 0, np.float32(1.0), s).astype(np.float32)
+    diff = (y - zero[:, None]).astype(np.float32)
+    ratio = (diff / s[:, None]).astype(np.float32)
+    q = e4m3_round_satfinite(ratio.astype(np.float64))
+    return q, s.astype(np.float64), zero.astype(np.float64)
+
+
+def dequantize_output_fp8(q: np.ndarray, s: np.ndarray, zero: np.ndarray) -> np.ndarray:
+    """The expert outputs the combine sees: q * s + zero per row."""
+    return np.asarray(q, np.float64) * np.asarray(s, np.float64)[:, None] + \
+        np.asarray(zero, np.float64)[:, None]
+
+
+# ----------------------------------------------------------------------------
 # expert FFN [V3V4-PAR Waved-EP: "L1 + Act + L2"; V4-EP 2.3: W1 by columns,
 # W2 by rows]: reading = one up projection, SiLU, one down projection, no
 # biases and no gating branch.
@@ -304,7 +339,12 @@ def forward(cfg, inp: dict, keep_h: bool = True) -> dict:
         Y[lo:hi] = y
         if keep_h:
             H[lo:hi] = h
-    out = combine(Y, pos, w)
+    if getattr(cfg, "output_fp8", 0):
+        yq, ys, yz = quantize_output_fp8(Y)
+        res.update({"y_q": yq, "y_scale": ys, "y_zero": yz})
+        out = combine(dequantize_output_fp8(yq, ys, yz), pos, w)
+    else:
+        out = combine(Y, pos, w)
     res.update({"Y": Y, "out": out, "out_rounded": _round_out(cfg, out)})
     if keep_h:
         res["H"] = H
@@ -328,6 +368,9 @@ def forward_tokens(cfg, inp: dict, tokens) -> dict:
         y, _ = expert_ffn_rows(x_hat[tt], _expert(a["W1"], int(e)),
                                _expert(a["W2"], int(e)), _storage(cfg))
         y_slot[tt, jj] = y
+    if getattr(cfg, "output_fp8", 0):
+        flat = y_slot.reshape(n * k, cfg.d)
+        y_slot = dequantize_output_fp8(*quantize_output_fp8(flat)).reshape(n, k, cfg.d)
     out = np.zeros((n, cfg.d), dtype=np.float64)
     for j in range(k):
         out += w[:, j:j + 1] * y_slot[:, j]

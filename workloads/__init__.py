@@ -54,6 +54,7 @@ class MoEConfig:
     topk_group: int = 1       # groups kept per token (group-limited router only)
     payload_fp8: int = 0      # 0 none, 1 per-token absmax FP8, 2 FP8 with one static scale
     payload_scale: float = 0.0  # the static scale (payload_fp8 == 2)
+    output_fp8: int = 0       # 1: expert outputs reach the combine as FP8 (min/max affine)
     bias: str = "zero"        # "zero" | "normal" (variance bias_var) | "zipf" (exponent zipf_s)
     bias_var: float = 0.0
     zipf_s: float = 0.0
