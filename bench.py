@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 METRIC = "routed tokens/s per MoE layer fwd at 1 GB300"
 UNIT = "tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-STAGES = ["route", "dispatch", "fp8_to_bf16", "gemm_w1_silu", "gemm_w2", "combine"]
+STAGES = ["route", "dispatch", "fp8_to_bf16", "gemm_w1_silu", "gemm_w2", "quantize_out",
+          "combine"]
 
 
 def parse():
@@ -78,7 +79,11 @@ def stage_work(cfg, counts):
     a_bytes = R * d * (2 if cfg.payload_fp8 else b)
     w["gemm_w1_silu"] = (active * d * f * b + a_bytes + R * f * b, 2.0 * R * d * f)
     w["gemm_w2"] = (active * f * d * b + R * f * b + R * d * 4, 2.0 * R * f * d)
-    w["combine"] = (R * d * 4 + R * 8 + T * d * b, 2.0 * R * d)
+    ofp8 = getattr(cfg, "output_fp8", 0)
+    # FP8 expert outputs: read Y once, write the E4M3 rows, scale and zero
+    w["quantize_out"] = ((R * d * 4 + R * d + R * 8) if ofp8 else 0, 0.0)
+    w["combine"] = (R * d * (1 if ofp8 else 4) + R * 8 + (R * 8 if ofp8 else 0) + T * d * b,
+                    2.0 * R * d)
     return w
 
 
@@ -213,9 +218,15 @@ def run_reference(args, cfg):
 
 
 def workload_config(cfg, args):
+    router = {0: "renorm", 1: "prek_softmax",
+              2: f"group_limited(n_group={cfg.n_group}, topk_group={cfg.topk_group})"}
+    payload = {0: cfg.dtype, 1: "fp8_e4m3 (per-token absmax scale)",
+               2: f"fp8_e4m3 (static scale {cfg.payload_scale:.6g})"}
     return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "f": cfg.f,
-            "router": "prek_softmax" if cfg.router else "renorm", "pre_k": cfg.pre_k,
-            "payload": "fp8_e4m3" if cfg.payload_fp8 else cfg.dtype, "seed": cfg.seed,
+            "router": router[cfg.router], "pre_k": cfg.pre_k,
+            "payload": payload[int(cfg.payload_fp8)],
+            "expert_output": ("fp8_e4m3 (per-row min/max affine)" if cfg.output_fp8
+                              else "fp32"), "seed": cfg.seed,
             "parallelism": f"replicas x{args.gpus}",
             "l2": ("flushed between steps" if args.flush_l2 else
                    "not flushed: per-step working set (expert weights) exceeds the 129 MB L2")}
@@ -325,7 +336,9 @@ def run_ours(args, cfg):
     kfile = os.path.join(ROOT, "mixture_experts_routed_gb300", "csrc",
                          "gemm_tc.cu" if dom.startswith("gemm") else
                          {"route": "route.cu", "dispatch": "dispatch.cu",
-                          "combine": "combine.cu", "fp8_to_bf16": "dispatch.cu"}[dom])
+                          "combine": "payload_out.cu" if getattr(cfg, "output_fp8", 0)
+                          else "combine.cu", "quantize_out": "payload_out.cu",
+                          "fp8_to_bf16": "dispatch.cu"}[dom])
     traffic = ncu_traffic(kfile, f"{cfg.name}:{dom}")
     if is_tensor:
         roof = {"bound": "tensor", "achieved": kd["TFLOP_s"], "peak": peaks["bf16_tflops"],

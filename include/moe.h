@@ -94,11 +94,19 @@ typedef struct moe_config {
   int32_t dtype;       /* MOE_DTYPE_F32 or MOE_DTYPE_BF16: x, W_g, W1, W2, H, out */
   int32_t router;      /* MOE_ROUTER_* */
   int32_t pre_k;       /* partial top-k width, k..min(8, E) (8 on the pages) */
-  int32_t payload_fp8; /* 1: dispatch rows as FP8 E4M3 + fp32 scale (bf16 only) */
+  int32_t payload_fp8; /* dispatch rows as FP8 E4M3 + an fp32 scale per row (bf16
+                        * only): 1 = per-token absmax scale; 2 = one static
+                        * scale, payload_scale, for every row (the sync-tax
+                        * article's "static global" variant, section 3.1) */
   int32_t n_group;     /* MOE_ROUTER_GROUP_LIMITED: expert groups, 1..32, dividing E;
                         * ignored by the other routers */
   int32_t topk_group;  /* MOE_ROUTER_GROUP_LIMITED: groups kept per token,
                         * 1..n_group, with k <= topk_group * E / n_group */
+  float payload_scale; /* payload_fp8 == 2: the scale, finite and > 0; values
+                        * beyond 448 * payload_scale saturate to +-448 */
+  int32_t output_fp8;  /* 1: moe_forward hands the expert outputs to the combine
+                        * as an FP8 payload (moe_quantize_output, then
+                        * moe_combine_fp8); 0: fp32 rows (moe_combine) */
 } moe_config_t;
 
 /* Validate a configuration. Returns MOE_OK or MOE_ERR_INVALID_ARG /
@@ -198,9 +206,32 @@ MOE_API int moe_combine(const moe_config_t* cfg, const float* y_perm, const int3
                 const float* topk_w, void* out, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* ---- FP8 expert-output payload -------------------------------------------
+ * The Deepseek-MoE sync-tax article (section 3.1) sends each expert output
+ * vector to the combine as FP8, quantised on its own from its min and max by
+ * an affine map.
+ * moe_quantize_output: for each row r < R = T*k of y_perm [R, d] fp32:
+ *   mn, mx = the row's min and max; zero = fp32(mx/2 + mn/2);
+ *   half = fp32(mx/2 - mn/2); s = fp32(half / 448), IEEE division (1 when
+ *   half = 0); y_q[r][c] = E4M3(fp32(fp32(y - zero) / s)), rounded to
+ *   nearest even, saturating at +-448 (OCP E4M3, no infinities).
+ *   Outputs: y_q [R, d] uint8, y_scale [R] fp32 (s), y_zero [R] fp32 (zero).
+ *   No workspace; no device-side error is possible.
+ * moe_combine_fp8: out[t] = sum_{j=0..k-1} topk_w[t, j] * (q * s + zero) of
+ *   row pos[t*k + j], in fp32 in increasing j (each decoded value one fp32
+ *   fma), stored in dtype; bitwise reproducible. A pos outside [0, R)
+ *   contributes nothing and flags MOE_ERR_BAD_INDEX.
+ *   ws: >= moe_scratch_size bytes (error word). */
+MOE_API int moe_quantize_output(const moe_config_t* cfg, const float* y_perm, uint8_t* y_q,
+                        float* y_scale, float* y_zero, void* stream);
+MOE_API int moe_combine_fp8(const moe_config_t* cfg, const uint8_t* y_q, const float* y_scale,
+                    const float* y_zero, const int32_t* pos, const float* topk_w,
+                    void* out, void* ws, size_t ws_bytes, void* stream);
+
 /* ---- whole layer -----------------------------------------------------------
- * moe_route -> moe_dispatch -> moe_expert_ffn -> moe_combine on one stream,
- * with every intermediate in the workspace (>= moe_workspace_size bytes).
+ * moe_route -> moe_dispatch -> moe_expert_ffn -> moe_combine (or, with
+ * output_fp8, moe_quantize_output -> moe_combine_fp8) on one stream, with
+ * every intermediate in the workspace (>= moe_workspace_size bytes).
  * No host synchronisation, so the call can be captured into a CUDA graph. */
 MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g,
                 const float* bias, const void* W1, const void* W2, void* out,
@@ -211,9 +242,10 @@ MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g,
  *   events[0] before the route kernel      events[1] after route
  *   events[2] after dispatch (3 kernels)   events[3] after the FP8 row
  *   conversion (= events[2] without FP8)   events[4] after the W1 GEMM
- *   events[5] after the W2 GEMM            events[6] after combine
+ *   events[5] after the W2 GEMM            events[6] after the output
+ *   quantisation (= events[5] without)     events[7] after combine
  * n_events must be MOE_NUM_EVENTS; any entry may be NULL (not recorded). */
-#define MOE_NUM_EVENTS 7
+#define MOE_NUM_EVENTS 8
 MOE_API int moe_forward_with_events(const moe_config_t* cfg, const void* x,
                             const void* W_g, const float* bias, const void* W1,
                             const void* W2, void* out, void* ws, size_t ws_bytes,
@@ -227,6 +259,7 @@ typedef struct moe_forward_views {
   int32_t* topk_idx; float* topk_w;
   int32_t* counts; int32_t* offsets; int32_t* pos; int32_t* src;
   void* x_perm; float* x_scale; void* h; float* y_perm;
+  uint8_t* y_q; float* y_scale; float* y_zero;  /* NULL unless output_fp8 */
 } moe_forward_views_t;
 MOE_API int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* views);
 

@@ -8,7 +8,8 @@ build (``build``) and host-side load statistics (``stats``).
 from . import _lib  # noqa: F401
 from .api import (  # noqa: F401
     MoEError, make_config, config_from, workspace_size, scratch_size, alloc_workspace, route,
-    dispatch, expert_ffn, combine, forward, forward_views, get_device_error,
+    dispatch, expert_ffn, combine, quantize_output, combine_fp8, forward, forward_views,
+    get_device_error,
     clear_device_error, kernel_count, check_config,
 )
 from ._lib import (  # noqa: F401

@@ -20,13 +20,14 @@ MOE_DTYPE_BF16 = 1
 MOE_ROUTER_RENORM = 0
 MOE_ROUTER_PREK_SOFTMAX = 1
 MOE_ROUTER_GROUP_LIMITED = 2
-MOE_NUM_EVENTS = 7
+MOE_NUM_EVENTS = 8
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("T", "d", "E", "k", "f", "dtype", "router", "pre_k", "payload_fp8",
-                 "n_group", "topk_group")]
+                 "n_group", "topk_group")] + [("payload_scale", ctypes.c_float),
+                                             ("output_fp8", ctypes.c_int32)]
 
 
 class MoeForwardViews(ctypes.Structure):
@@ -34,7 +35,9 @@ class MoeForwardViews(ctypes.Structure):
                 ("counts", ctypes.c_void_p), ("offsets", ctypes.c_void_p),
                 ("pos", ctypes.c_void_p), ("src", ctypes.c_void_p),
                 ("x_perm", ctypes.c_void_p), ("x_scale", ctypes.c_void_p),
-                ("h", ctypes.c_void_p), ("y_perm", ctypes.c_void_p)]
+                ("h", ctypes.c_void_p), ("y_perm", ctypes.c_void_p),
+                ("y_q", ctypes.c_void_p), ("y_scale", ctypes.c_void_p),
+                ("y_zero", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -51,6 +54,8 @@ PROTOTYPES = {
     "moe_dispatch": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_quantize_output": (_I, [_CFG, _P, _P, _P, _P, _P]),
+    "moe_combine_fp8": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_forward_with_events": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                      ctypes.POINTER(ctypes.c_void_p), _I, _P]),

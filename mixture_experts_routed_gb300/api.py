@@ -28,20 +28,23 @@ class MoEError(RuntimeError):
 
 
 def make_config(T, d, E, k, f, dtype="bf16", router=L.MOE_ROUTER_RENORM, pre_k=8,
-                payload_fp8=False, n_group=1, topk_group=1) -> L.MoeConfig:
+                payload_fp8=0, n_group=1, topk_group=1, payload_scale=0.0,
+                output_fp8=0) -> L.MoeConfig:
     dt = {"f32": L.MOE_DTYPE_F32, "fp32": L.MOE_DTYPE_F32, "bf16": L.MOE_DTYPE_BF16,
           torch.float32: L.MOE_DTYPE_F32, torch.bfloat16: L.MOE_DTYPE_BF16}[dtype]
     return L.MoeConfig(int(T), int(d), int(E), int(k), int(f), dt, int(router), int(pre_k),
-                       int(bool(payload_fp8)), int(n_group), int(topk_group))
+                       int(payload_fp8), int(n_group), int(topk_group), float(payload_scale),
+                       int(output_fp8))
 
 
 def config_from(c) -> L.MoeConfig:
     """From any object with T, d, E, k, f, dtype, router, pre_k, payload_fp8
-    (and, optionally, n_group and topk_group)."""
+    (and, optionally, n_group, topk_group, payload_scale and output_fp8)."""
     if isinstance(c, L.MoeConfig):
         return c
     return make_config(c.T, c.d, c.E, c.k, c.f, c.dtype, c.router, c.pre_k, c.payload_fp8,
-                       getattr(c, "n_group", 1), getattr(c, "topk_group", 1))
+                       getattr(c, "n_group", 1), getattr(c, "topk_group", 1),
+                       getattr(c, "payload_scale", 0.0), getattr(c, "output_fp8", 0))
 
 
 def _cfg(c):
@@ -154,6 +157,33 @@ def combine(c, y_perm, pos, topk_w, *, ws, out=None, stream=None):
     return out
 
 
+def quantize_output(c, y_perm, *, y_q=None, y_scale=None, y_zero=None, stream=None):
+    """FP8 expert-output payload: (y_q uint8 [R, d], y_scale [R], y_zero [R])."""
+    cc = config_from(c)
+    R, dev = cc.T * cc.k, y_perm.device
+    if y_q is None:
+        y_q = torch.empty((R, cc.d), dtype=torch.uint8, device=dev)
+    if y_scale is None:
+        y_scale = torch.empty((R,), dtype=torch.float32, device=dev)
+    if y_zero is None:
+        y_zero = torch.empty((R,), dtype=torch.float32, device=dev)
+    st = L.load().moe_quantize_output(ctypes.byref(cc), _p(y_perm), _p(y_q), _p(y_scale),
+                                      _p(y_zero), _s(stream))
+    _check(st, "moe_quantize_output")
+    return y_q, y_scale, y_zero
+
+
+def combine_fp8(c, y_q, y_scale, y_zero, pos, topk_w, *, ws, out=None, stream=None):
+    cc = config_from(c)
+    if out is None:
+        out = torch.empty((cc.T, cc.d), dtype=_dt(cc), device=y_q.device)
+    st = L.load().moe_combine_fp8(ctypes.byref(cc), _p(y_q), _p(y_scale), _p(y_zero), _p(pos),
+                                  _p(topk_w), _p(out), _p(ws), ws.numel() * ws.element_size(),
+                                  _s(stream))
+    _check(st, "moe_combine_fp8")
+    return out
+
+
 def forward(c, x, Wg, bias, W1, W2, *, ws, out=None, events=None, stream=None):
     """The whole layer. ``events``: optional list of MOE_NUM_EVENTS
     torch.cuda.Event (or None) recorded at the kernel boundaries."""
@@ -207,6 +237,9 @@ def forward_views(c, ws) -> dict:
         "x_scale": view(v.x_scale, R, torch.float32, (R,)) if cc.payload_fp8 else None,
         "h": view(v.h, R * cc.f, _dt(cc), (R, cc.f)),
         "y_perm": view(v.y_perm, R * cc.d, torch.float32, (R, cc.d)),
+        "y_q": view(v.y_q, R * cc.d, torch.uint8, (R, cc.d)) if cc.output_fp8 else None,
+        "y_scale": view(v.y_scale, R, torch.float32, (R,)) if cc.output_fp8 else None,
+        "y_zero": view(v.y_zero, R, torch.float32, (R,)) if cc.output_fp8 else None,
     }
 
 

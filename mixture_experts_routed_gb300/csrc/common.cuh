@@ -98,7 +98,9 @@ cudaError_t launch_dispatch_count(const int32_t* topk_idx, int T, int k, int E, 
 cudaError_t launch_dispatch_scan(const int32_t* hist, int nchunk, int E, int32_t* base,
                                  int32_t* counts, cudaStream_t s);
 // Stable ranks -> pos, src, offsets; row copy (or FP8 quantisation) -> x_perm.
-cudaError_t launch_dispatch_scatter(int dtype, int fp8, const void* x, const int32_t* topk_idx,
+// FP8 scale per row: static_scale when > 0, else the row's absmax / 448.
+cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, const void* x,
+                                    const int32_t* topk_idx,
                                     int T, int d, int k, int E, int nchunk,
                                     const int32_t* counts, const int32_t* base,
                                     int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
@@ -109,6 +111,15 @@ cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaS
 // ---------------------------------------------------------------- combine.cu
 cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const float* w, int T,
                            int d, int k, int R, void* out, uint32_t* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- payload_out.cu
+// Per-row min/max affine FP8 quantisation of the expert outputs, and the
+// combine that decodes it.
+cudaError_t launch_quantize_out(const float* y, int R, int d, uint8_t* yq, float* ys, float* yz,
+                                cudaStream_t s);
+cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, const float* yz,
+                               const int32_t* pos, const float* w, int T, int d, int k, int R,
+                               void* out, uint32_t* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm_tc.cu
 // Grouped GEMM over expert segments on tcgen05: out[r] = epi(A[r] . W[e]).

@@ -15,7 +15,8 @@
 //           below it plus the counts of earlier warps; then each warp copies
 //           one token row, read once with 16-byte loads and written to its k
 //           destinations (or quantised to an FP8 E4M3 payload with a
-//           per-token absmax scale, sync-tax article section 3.1).
+//           per-token absmax scale, or one static scale for every row,
+//           sync-tax article section 3.1).
 //
 // Expert ids outside [0, E) are skipped and flag kErrBadIndex.
 #include <cstdint>
@@ -143,7 +144,8 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
     const void* __restrict__ xv, const int32_t* __restrict__ idx, int T, int d, int k, int E,
     int nchunk, const int32_t* __restrict__ counts, const int32_t* __restrict__ base,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ src,
-    void* __restrict__ x_perm, float* __restrict__ x_scale, uint32_t* __restrict__ err) {
+    void* __restrict__ x_perm, float* __restrict__ x_scale, float static_scale,
+    uint32_t* __restrict__ err) {
   __shared__ int off_s[kMaxExperts + 1];
   __shared__ int cnt_w[2][kMaxExperts];  // per-warp expert counts (<= 64 entries, 2 warps)
   __shared__ int pos_s[kTPC * kMaxTopK];
@@ -243,7 +245,8 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
   for (int j = 0; j < kMaxTopK; ++j) p[j] = (j < k) ? pos_s[w * k + j] : -1;
 
   if constexpr (FP8) {
-    // pass 1: absmax of the token's row (bf16 values are exact in fp32)
+    // pass 1: absmax of the token's row (bf16 values are exact in fp32),
+    // skipped with a static scale
     const int nvec = d / 8;
     const uint4* xr =
         reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xv) +
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
     // four 16-byte loads in flight per lane (one at a time is latency-bound)
     constexpr int UQ = 4;
     float amax = 0.f;
-    for (int v0 = lane; v0 < nvec; v0 += 32 * UQ) {
+    for (int v0 = lane; static_scale <= 0.f && v0 < nvec; v0 += 32 * UQ) {
       uint4 val[UQ];
 #pragma unroll
       for (int u = 0; u < UQ; ++u)
@@ -267,7 +270,8 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float s = (amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f);
+    const float s =
+        static_scale > 0.f ? static_scale : ((amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f));
     // pass 2: q = E4M3(x / s); the k copies share the scale
     uint2* dst = reinterpret_cast<uint2*>(x_perm);
     const size_t row_vecs = static_cast<size_t>(nvec);
@@ -342,16 +346,16 @@ cudaError_t launch_dispatch_scan(const int32_t* hist, int nchunk, int E, int32_t
                     counts);
 }
 
-cudaError_t launch_dispatch_scatter(int dtype, int fp8, const void* x, const int32_t* topk_idx,
-                                    int T, int d, int k, int E, int nchunk,
-                                    const int32_t* counts, const int32_t* base,
+cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, const void* x,
+                                    const int32_t* topk_idx, int T, int d, int k, int E,
+                                    int nchunk, const int32_t* counts, const int32_t* base,
                                     int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
                                     float* x_scale, uint32_t* err, cudaStream_t s) {
   const dim3 grid(nchunk), block(256);
   auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false>
                 : (!fp8 ? dispatch_scatter_kernel<1, false> : dispatch_scatter_kernel<1, true>);
   return launch_pdl(kernel, grid, block, 0, s, x, topk_idx, T, d, k, E, nchunk, counts, base,
-                    offsets, pos, src, x_perm, x_scale, err);
+                    offsets, pos, src, x_perm, x_scale, static_scale, err);
 }
 
 cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s) {

@@ -103,7 +103,9 @@ extern "C" MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void*
                                         nullptr, 0, s);
   if (e == cudaSuccess) e = launch_dispatch_scan(hist, nchunk, cfg->E, tbase, counts, s);
   if (e == cudaSuccess)
-    e = launch_dispatch_scatter(cfg->dtype, cfg->payload_fp8, x, topk_idx, cfg->T, cfg->d,
+    e = launch_dispatch_scatter(cfg->dtype, cfg->payload_fp8 != 0,
+                                cfg->payload_fp8 == 2 ? cfg->payload_scale : 0.f, x, topk_idx,
+                                cfg->T, cfg->d,
                                 cfg->k, cfg->E, nchunk, counts, tbase, offsets, pos, src, x_perm,
                                 x_scale, err, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_LAUNCH;

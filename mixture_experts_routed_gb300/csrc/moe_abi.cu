@@ -1,6 +1,7 @@
 // moe_abi.cu - the exported C ABI (include/moe.h): host-side validation,
 // workspace layout, and the launch sequence of each stage. No entry point
 // allocates, frees or synchronises (except moe_get_device_error).
+#include <cfloat>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -32,7 +33,10 @@ int check_cfg(const moe_config_t* c) {
     if (c->topk_group < 1 || c->topk_group > c->n_group) return MOE_ERR_INVALID_ARG;
     if (c->k > c->topk_group * (c->E / c->n_group)) return MOE_ERR_INVALID_ARG;
   }
-  if (c->payload_fp8 != 0 && c->payload_fp8 != 1) return MOE_ERR_INVALID_ARG;
+  if (c->payload_fp8 < 0 || c->payload_fp8 > 2) return MOE_ERR_INVALID_ARG;
+  if (c->output_fp8 != 0 && c->output_fp8 != 1) return MOE_ERR_INVALID_ARG;
+  if (c->payload_fp8 == 2 && !(c->payload_scale > 0.f && c->payload_scale <= FLT_MAX))
+    return MOE_ERR_INVALID_ARG;
   const int max_pre = c->E < kMaxTopK ? c->E : kMaxTopK;
   if (c->pre_k < 1 || c->pre_k > max_pre) return MOE_ERR_INVALID_ARG;
   if (c->k > c->pre_k) return MOE_ERR_INVALID_ARG;
@@ -46,7 +50,8 @@ size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
 
 struct Layout {
   size_t err, hist, base, stage, scratch_end;
-  size_t topk_idx, topk_w, counts, offsets, pos, src, x_perm, x_scale, h, y, total;
+  size_t topk_idx, topk_w, counts, offsets, pos, src, x_perm, x_scale, h, y, y_q, y_scale,
+      y_zero, total;
   int nchunk;
 };
 
@@ -76,6 +81,9 @@ Layout layout_of(const moe_config_t& c) {
   L.x_scale = take(c.payload_fp8 ? R * 4 : 0);
   L.h = take(R * c.f * es);
   L.y = take(R * c.d * 4);
+  L.y_q = take(c.output_fp8 ? R * c.d : 0);
+  L.y_scale = take(c.output_fp8 ? R * 4 : 0);
+  L.y_zero = take(c.output_fp8 ? R * 4 : 0);
   L.total = o;
   return L;
 }
@@ -125,8 +133,10 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
                                         gemm_counters(ws), kNumGemmCounters, s);
   if (e == cudaSuccess) e = launch_dispatch_scan(hist, L.nchunk, c.E, base, counts, s);
   if (e == cudaSuccess)
-    e = launch_dispatch_scatter(c.dtype, c.payload_fp8, x, idx, c.T, c.d, c.k, c.E, L.nchunk,
-                                counts, base, offsets, pos, src, x_perm, x_scale, err, s);
+    e = launch_dispatch_scatter(c.dtype, c.payload_fp8 != 0,
+                                c.payload_fp8 == 2 ? c.payload_scale : 0.f, x, idx, c.T, c.d,
+                                c.k, c.E, L.nchunk, counts, base, offsets, pos, src, x_perm,
+                                x_scale, err, s);
   return status_of(e);
 }
 
@@ -213,8 +223,21 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
   if ((st = run_gemm(c, L, ws, 2, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
     return st;
   record(events, 5, s);
-  if ((st = run_combine(c, L, ws, y, pos, w, out, s)) != MOE_OK) return st;
-  record(events, 6, s);
+  if (c.output_fp8) {
+    uint8_t* yq = at<uint8_t>(ws, L.y_q);
+    float* ys = at<float>(ws, L.y_scale);
+    float* yz = at<float>(ws, L.y_zero);
+    if ((st = status_of(launch_quantize_out(y, c.T * c.k, c.d, yq, ys, yz, s))) != MOE_OK)
+      return st;
+    record(events, 6, s);
+    st = status_of(launch_combine_fp8(c.dtype, yq, ys, yz, pos, w, c.T, c.d, c.k, c.T * c.k, out,
+                                      at<uint32_t>(ws, L.err), s));
+    if (st != MOE_OK) return st;
+  } else {
+    record(events, 6, s);
+    if ((st = run_combine(c, L, ws, y, pos, w, out, s)) != MOE_OK) return st;
+  }
+  record(events, 7, s);
   return MOE_OK;
 }
 
@@ -297,6 +320,33 @@ int moe_combine(const moe_config_t* cfg, const float* y_perm, const int32_t* pos
   return run_combine(*cfg, L, ws, y_perm, pos, topk_w, out, as_stream(stream));
 }
 
+int moe_quantize_output(const moe_config_t* cfg, const float* y_perm, uint8_t* y_q,
+                        float* y_scale, float* y_zero, void* stream) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T == 0) return MOE_OK;
+  if (!ok_ptr(y_perm) || !ok_ptr(y_q) || y_scale == nullptr || y_zero == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  return status_of(launch_quantize_out(y_perm, cfg->T * cfg->k, cfg->d, y_q, y_scale, y_zero,
+                                       as_stream(stream)));
+}
+
+int moe_combine_fp8(const moe_config_t* cfg, const uint8_t* y_q, const float* y_scale,
+                    const float* y_zero, const int32_t* pos, const float* topk_w, void* out,
+                    void* ws, size_t ws_bytes, void* stream) {
+  const int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  if (ws == nullptr || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!ok_ptr(y_q) || y_scale == nullptr || y_zero == nullptr ||
+                     pos == nullptr || topk_w == nullptr || !ok_ptr(out)))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(*cfg);
+  if (ws_bytes < L.scratch_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return status_of(launch_combine_fp8(cfg->dtype, y_q, y_scale, y_zero, pos, topk_w, cfg->T,
+                                      cfg->d, cfg->k, cfg->T * cfg->k, out,
+                                      at<uint32_t>(ws, L.err), as_stream(stream)));
+}
+
 int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
                 const void* W1, const void* W2, void* out, void* ws, size_t ws_bytes,
                 void* stream) {
@@ -326,6 +376,9 @@ int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* v)
   v->x_scale = cfg->payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
   v->h = at<void>(ws, L.h);
   v->y_perm = at<float>(ws, L.y);
+  v->y_q = cfg->output_fp8 ? at<uint8_t>(ws, L.y_q) : nullptr;
+  v->y_scale = cfg->output_fp8 ? at<float>(ws, L.y_scale) : nullptr;
+  v->y_zero = cfg->output_fp8 ? at<float>(ws, L.y_zero) : nullptr;
   return MOE_OK;
 }
 
@@ -366,7 +419,7 @@ const char* moe_strerror(int status) {
 int moe_forward_kernel_count(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   if (cfg->T == 0) return 1;
-  return 1 + 3 + (cfg->payload_fp8 ? 1 : 0) + 2 + 1;
+  return 1 + 3 + (cfg->payload_fp8 ? 1 : 0) + 2 + (cfg->output_fp8 ? 1 : 0) + 1;
 }
 
 }  // extern "C"

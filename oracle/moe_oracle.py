@@ -354,7 +354,9 @@ def forward(cfg, inp: dict, keep_h: bool = True) -> dict:
 def forward_tokens(cfg, inp: dict, tokens) -> dict:
     """Route, FFN and combine for a subset of tokens only (a token's output
     does not depend on other tokens). Used for sampled checks on the large
-    layers. Returns L, topk_idx, topk_w, out, out_rounded for ``tokens``."""
+    layers. Returns L, topk_idx, topk_w, out, out_rounded for ``tokens``
+    (and, with the FP8 expert-output payload, y_q [n, k, d], y_scale and
+    y_zero [n, k] per token slot)."""
     a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
     tokens = np.asarray(tokens, dtype=np.int64)
     x = a["x"][tokens]
@@ -368,11 +370,15 @@ def forward_tokens(cfg, inp: dict, tokens) -> dict:
         y, _ = expert_ffn_rows(x_hat[tt], _expert(a["W1"], int(e)),
                                _expert(a["W2"], int(e)), _storage(cfg))
         y_slot[tt, jj] = y
+    res = {"tokens": tokens}
     if getattr(cfg, "output_fp8", 0):
-        flat = y_slot.reshape(n * k, cfg.d)
-        y_slot = dequantize_output_fp8(*quantize_output_fp8(flat)).reshape(n, k, cfg.d)
+        yq, ys, yz = quantize_output_fp8(y_slot.reshape(n * k, cfg.d))
+        res.update({"y_q": yq.reshape(n, k, cfg.d), "y_scale": ys.reshape(n, k),
+                    "y_zero": yz.reshape(n, k)})
+        y_slot = dequantize_output_fp8(yq, ys, yz).reshape(n, k, cfg.d)
     out = np.zeros((n, cfg.d), dtype=np.float64)
     for j in range(k):
         out += w[:, j:j + 1] * y_slot[:, j]
-    return {"tokens": tokens, "L": L, "topk_idx": idx, "topk_w": w,
-            "out": out, "out_rounded": _round_out(cfg, out)}
+    res.update({"L": L, "topk_idx": idx, "topk_w": w, "out": out,
+                "out_rounded": _round_out(cfg, out)})
+    return res

@@ -111,6 +111,29 @@ SMALL = {
     "group_E16_T4100_d256_k2_f128_g8top1": MoEConfig(
         "group_E16_T4100_d256_k2_f128_g8top1", T=4100, d=256, E=16, k=2, f=128, dtype="bf16",
         router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=1, seed=45),
+    # static FP8 payload scale: 4/448 saturates the +-20 outliers and the
+    # largest normal values; 20/448 on a ragged 8-expert layer
+    "fp8static_T300_d512_E4_k2_f256": MoEConfig(
+        "fp8static_T300_d512_E4_k2_f256", T=300, d=512, E=4, k=2, f=256, dtype="bf16",
+        pre_k=4, payload_fp8=2, payload_scale=4.0 / 448.0, outlier_rate=0.01, seed=47),
+    "fp8static_T129_d256_E8_k2_f320": MoEConfig(
+        "fp8static_T129_d256_E8_k2_f320", T=129, d=256, E=8, k=2, f=320, dtype="bf16",
+        payload_fp8=2, payload_scale=20.0 / 448.0, outlier_rate=0.001, seed=48),
+    # FP8 expert-output payload (per-row min/max affine) before the combine:
+    # bf16 with a ragged batch, fp32 out with k = 3, k = 8, and together with
+    # the FP8 input payload
+    "outfp8_T300_d512_E4_k2_f256": MoEConfig(
+        "outfp8_T300_d512_E4_k2_f256", T=300, d=512, E=4, k=2, f=256, dtype="bf16", pre_k=4,
+        output_fp8=1, seed=49),
+    "outfp8_f32_T64_d128_E4_k3_f128": MoEConfig(
+        "outfp8_f32_T64_d128_E4_k3_f128", T=64, d=128, E=4, k=3, f=128, dtype="f32", pre_k=4,
+        output_fp8=1, seed=50),
+    "outfp8_T100_d256_E16_k8_f128": MoEConfig(
+        "outfp8_T100_d256_E16_k8_f128", T=100, d=256, E=16, k=8, f=128, dtype="bf16",
+        output_fp8=1, seed=51),
+    "outfp8_fp8in_T200_d256_E8_k2_f256": MoEConfig(
+        "outfp8_fp8in_T200_d256_E8_k2_f256", T=200, d=256, E=8, k=2, f=256, dtype="bf16",
+        payload_fp8=1, output_fp8=1, outlier_rate=0.01, seed=52),
     "group_f32_E16_T4100_d128_k3_f128_g4top2": MoEConfig(
         "group_f32_E16_T4100_d128_k3_f128_g4top2", T=4100, d=128, E=16, k=3, f=128,
         dtype="f32", router=ROUTER_GROUP_LIMITED, n_group=4, topk_group=2, seed=46),
@@ -177,8 +200,13 @@ def sample_rows(offsets: np.ndarray, max_experts: int = 6, per_expert: int = 6, 
     return rows
 
 
+def payload_static(cfg):
+    """The static payload scale of a shape, or None for per-token scales."""
+    return cfg.payload_scale if int(cfg.payload_fp8) == 2 else None
+
+
 @functools.lru_cache(maxsize=1)
 def oracle_payload(name: str):
     """Per-token FP8 payload of the oracle: (q values, scales)."""
-    _, _, host = layer(name)
-    return oracle.quantize_payload_fp8(host["x"])
+    cfg, _, host = layer(name)
+    return oracle.quantize_payload_fp8(host["x"], payload_static(cfg))

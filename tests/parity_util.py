@@ -167,3 +167,44 @@ def _check_group_choice(cfg, L_own, idx, w):
         assert list(idx[t]) == list(best), (t, idx[t], best)
         z = np.exp(L_own[t, idx[t]] - L_own[t, idx[t]].max())
         assert np.max(np.abs(w[t] - z / z.sum())) <= W_MAX_ABS
+
+
+def e4m3_step(q: np.ndarray) -> np.ndarray:
+    """Distance from an E4M3 value to its neighbour away from zero (at most
+    the distance to either neighbour): 2^(e-3) for normals |q| in
+    [2^e, 2^(e+1)), 2^-9 for subnormals and zero."""
+    a = np.abs(np.asarray(q, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    return np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+
+
+def assert_close_output_fp8(cfg, got, ref_out, w, yq_slots, ys_slots, gpu_codes=None, what=""):
+    """Layer output with the FP8 expert-output payload. The GPU quantises its
+    own fp32 expert outputs, which differ from the oracle's in the last bits
+    (fp32 accumulation order, bf16 rounding of H), so a value next to an E4M3
+    rounding midpoint may take the neighbouring code. The bound: each slot
+    may be off by one E4M3 step of its oracle code times its scale; what is
+    left after that slack must meet the layer's max-abs and rel-L2. With
+    ``gpu_codes`` (the GPU's own E4M3 values, decoded by torch, in slot
+    layout) the share of flipped codes is checked too: under 1 %."""
+    rel, mabs = out_tolerance(cfg)
+    got = np.asarray(got, np.float64)
+    ref_out = np.asarray(ref_out, np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    step = e4m3_step(yq_slots)
+    slack = np.einsum("tj,tj,tjc->tc", np.abs(w), ys_slots, step)
+    excess = np.maximum(np.abs(got - ref_out) - slack, 0.0)
+    den = np.linalg.norm(ref_out)
+    r = float(np.linalg.norm(excess) / den) if den > 0 else float(np.linalg.norm(excess))
+    assert r <= rel, f"{what}: rel_l2 beyond one E4M3 step = {r:.3e} (<= {rel})"
+    assert excess.max() <= mabs, f"{what}: max-abs beyond one E4M3 step = {excess.max():.3e}"
+    if gpu_codes is not None:
+        # a systematic error (wrong zero point or scale, truncation) changes
+        # most codes; legitimate flips are rare. A flip may span more than one
+        # step where |q| is small: one bf16 rounding flip of H moves y by
+        # ~|W2| * 2^-8 |H|, several steps of (y - zero)/s near zero.
+        gq = np.asarray(gpu_codes, np.float64)
+        flip = gq != yq_slots
+        print(f"{what}: FP8 output codes differing from the oracle's: {flip.mean():.4%}")
+        assert flip.mean() <= 1e-2, f"{what}: {flip.mean():.2%} of the FP8 codes differ"
+    return r

@@ -54,7 +54,7 @@ def test_only_abi_symbols_are_exported(lib):
 
 def cfg(**kw):
     base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0,
-                n_group=0, topk_group=0)
+                n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0)
     base.update(kw)
     return L.MoeConfig(*[base[n] for n, _ in L.MoeConfig._fields_])
 
@@ -91,7 +91,18 @@ def cfg(**kw):
     (dict(router=2, n_group=4, topk_group=5), L.MOE_ERR_INVALID_ARG),
     (dict(router=2, k=3, n_group=4, topk_group=1), L.MOE_ERR_INVALID_ARG),
     (dict(router=0, n_group=3, topk_group=7), L.MOE_OK),
-    (dict(payload_fp8=2), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=3), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=2, payload_scale=0.04), L.MOE_OK),
+    (dict(payload_fp8=2), L.MOE_ERR_INVALID_ARG),                       # scale 0
+    (dict(payload_fp8=2, payload_scale=-1.0), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=2, payload_scale=float("inf")), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=2, payload_scale=float("nan")), L.MOE_ERR_INVALID_ARG),
+    (dict(payload_fp8=2, payload_scale=0.04, dtype=0), L.MOE_ERR_UNSUPPORTED),
+    (dict(payload_fp8=0, payload_scale=-5.0), L.MOE_OK),
+    (dict(output_fp8=1), L.MOE_OK),
+    (dict(output_fp8=1, dtype=0), L.MOE_OK),
+    (dict(output_fp8=2), L.MOE_ERR_INVALID_ARG),
+    (dict(output_fp8=-1), L.MOE_ERR_INVALID_ARG),
     (dict(payload_fp8=1, dtype=0), L.MOE_ERR_UNSUPPORTED),
     (dict(T=1 << 30, k=8), L.MOE_ERR_UNSUPPORTED),
 ])
@@ -123,6 +134,12 @@ def test_workspace_sizes(lib):
     assert lib.moe_scratch_size(ctypes.byref(c8)) >= sc + R * 4096 * 2
     assert lib.moe_forward_kernel_count(ctypes.byref(c)) == 7
     assert lib.moe_forward_kernel_count(ctypes.byref(c8)) == 8
+    # the FP8 expert-output payload: R*d bytes + scale and zero per row in
+    # the forward workspace, one more kernel, no extra scratch
+    co = cfg(T=1024, d=4096, E=8, k=2, f=11008, output_fp8=1)
+    assert lib.moe_workspace_size(ctypes.byref(co)) >= ws + R * 4096 + R * 8
+    assert lib.moe_scratch_size(ctypes.byref(co)) == sc
+    assert lib.moe_forward_kernel_count(ctypes.byref(co)) == 8
 
 
 FAKE = ctypes.c_void_p(0x100000)       # never dereferenced: validation fails first
@@ -165,6 +182,12 @@ def test_stage_argument_errors(lib):
     assert lib.moe_expert_ffn(ctypes.byref(c), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE_ODD,
                               FAKE, sc, None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_combine(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, None, sc, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_output(ctypes.byref(c), FAKE, FAKE_ODD, FAKE, FAKE, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_output(ctypes.byref(c), FAKE, FAKE, None, FAKE, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_fp8(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, sc - 1,
+                               None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_combine_fp8(ctypes.byref(c), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, sc,
+                               None) == L.MOE_ERR_INVALID_ARG
     # an empty batch needs no device work for routing
     c0 = cfg(T=0)
     assert lib.moe_route(ctypes.byref(c0), None, None, None, None, None, None, None) == L.MOE_OK

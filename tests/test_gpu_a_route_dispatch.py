@@ -7,7 +7,8 @@ import torch
 
 import oracle
 import mixture_experts_routed_gb300 as moe
-from gpu_layers import SMALL_NAMES, FULL_NAMES, VARIANT_NAMES, layer, oracle_route, oracle_dispatch
+from gpu_layers import (SMALL_NAMES, FULL_NAMES, VARIANT_NAMES, layer, oracle_route,
+                        oracle_dispatch, payload_static)
 from parity_util import check_route, bits, to_np
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +59,7 @@ def test_dispatch_parity(cuda_ok, name):
         ref = bits(inp["x"][torch.from_numpy(src[rows]).cuda()])
         assert np.array_equal(got, ref)
     else:
-        q, s = oracle.quantize_payload_fp8(host["x"])
+        q, s = oracle.quantize_payload_fp8(host["x"], payload_static(cfg))
         ref_bytes = oracle.e4m3_encode(q[src[rows]])
         got_bytes = to_np(d["x_perm"])[rows]
         assert np.array_equal(got_bytes, ref_bytes), \

@@ -10,11 +10,12 @@ import oracle
 import mixture_experts_routed_gb300 as moe
 from gpu_layers import (SMALL_NAMES, FULL_NAMES, VARIANT_NAMES, ORACLE_FULL_OK, layer, oracle_route,
                         oracle_dispatch)
-from parity_util import assert_close, out_tolerance, route_ties, to_np
+from parity_util import assert_close, assert_close_output_fp8, out_tolerance, route_ties, to_np
 
 pytestmark = pytest.mark.gpu
 NAMES = SMALL_NAMES + FULL_NAMES + VARIANT_NAMES
-SAMPLED_TOKENS = {FULL_NAMES[2]: 48, FULL_NAMES[3]: 24, FULL_NAMES[4]: 8, VARIANT_NAMES[0]: 8}
+SAMPLED_TOKENS = {FULL_NAMES[2]: 48, FULL_NAMES[3]: 24, FULL_NAMES[4]: 8}
+SAMPLED_TOKENS.update({n: 16 for n in VARIANT_NAMES})
 
 
 def _run(cfg, inp, ws=None):
@@ -22,6 +23,14 @@ def _run(cfg, inp, ws=None):
     out = moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws)
     torch.cuda.synchronize()
     return out, ws
+
+
+def _gpu_codes(views, slots):
+    """The GPU's FP8 expert-output codes of the given slot rows, decoded by
+    torch's own float8_e4m3fn type."""
+    rows = torch.from_numpy(np.asarray(slots, np.int64).reshape(-1)).cuda()
+    q = views["y_q"][rows].view(torch.float8_e4m3fn).double().cpu().numpy()
+    return q.reshape(slots.shape[0], slots.shape[1], -1)
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -36,7 +45,14 @@ def test_forward_parity(cuda_ok, name):
     if name in ORACLE_FULL_OK:
         ref = oracle.forward(cfg, host, keep_h=False)
         keep = ~tie
-        assert_close(to_np(out)[keep], ref["out_rounded"][keep], rel, mabs, name)
+        if cfg.output_fp8:
+            slots = ref["pos"].reshape(cfg.T, cfg.k)
+            codes = _gpu_codes(views, slots)
+            assert_close_output_fp8(cfg, to_np(out)[keep], ref["out_rounded"][keep],
+                                    ref["topk_w"][keep], ref["y_q"][slots][keep],
+                                    ref["y_scale"][slots][keep], codes[keep], name)
+        else:
+            assert_close(to_np(out)[keep], ref["out_rounded"][keep], rel, mabs, name)
         if not tie.any():
             assert np.array_equal(to_np(views["counts"]), ref["counts"])
             assert np.array_equal(to_np(views["pos"]), ref["pos"])
@@ -46,11 +62,18 @@ def test_forward_parity(cuda_ok, name):
         toks = np.sort(rng.choice(cand, size=min(SAMPLED_TOKENS[name], cand.size), replace=False))
         ref = oracle.forward_tokens(cfg, host, toks)
         got = to_np(out[torch.from_numpy(toks).cuda()])
-        assert_close(got, ref["out_rounded"], rel, mabs, name)
+        if cfg.output_fp8:
+            slots = to_np(views["pos"]).reshape(cfg.T, cfg.k)[toks]
+            assert_close_output_fp8(cfg, got, ref["out_rounded"], ref["topk_w"], ref["y_q"],
+                                    ref["y_scale"], _gpu_codes(views, slots), name)
+        else:
+            assert_close(got, ref["out_rounded"], rel, mabs, name)
     print(f"{name}: near-tie tokens excluded {int(tie.sum())}")
 
 
-@pytest.mark.parametrize("name", [SMALL_NAMES[0], SMALL_NAMES[6], FULL_NAMES[0], FULL_NAMES[1]])
+@pytest.mark.parametrize("name", [SMALL_NAMES[0], SMALL_NAMES[6], FULL_NAMES[0], FULL_NAMES[1],
+                                  "outfp8_fp8in_T200_d256_E8_k2_f256",
+                                  "outfp8_f32_T64_d128_E4_k3_f128"])
 def test_stage_calls_compose_to_forward(cuda_ok, name):
     cfg, inp, _ = layer(name)
     out_f, ws = _run(cfg, inp)
@@ -58,10 +81,17 @@ def test_stage_calls_compose_to_forward(cuda_ok, name):
     idx, w, _ = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"])
     d = moe.dispatch(cfg, inp["x"], idx, ws=sc)
     h, y = moe.expert_ffn(cfg, d["x_perm"], d["x_scale"], d["offsets"], inp["W1"], inp["W2"], ws=sc)
-    out_s = moe.combine(cfg, y, d["pos"], w, ws=sc)
+    if cfg.output_fp8:
+        yq, ys, yz = moe.quantize_output(cfg, y)
+        out_s = moe.combine_fp8(cfg, yq, ys, yz, d["pos"], w, ws=sc)
+    else:
+        out_s = moe.combine(cfg, y, d["pos"], w, ws=sc)
     torch.cuda.synchronize()
     assert torch.equal(out_f, out_s)
     v = moe.forward_views(cfg, ws)
+    if cfg.output_fp8:
+        assert torch.equal(v["y_q"], yq) and torch.equal(v["y_scale"], ys)
+        assert torch.equal(v["y_zero"], yz)
     assert torch.equal(v["topk_idx"], idx) and torch.equal(v["pos"], d["pos"])
     assert torch.equal(v["h"], h) and torch.equal(v["y_perm"], y)
 

@@ -106,7 +106,14 @@ CONFIG_ORDER = list(CONFIGS)
 # Static global FP8 scale (sync-tax article, section 3.1, "static global"):
 # the wide layer with one payload scale fixed ahead of time, 20/448, so the
 # largest magnitude in the data (the +-20 outliers) maps to the E4M3 maximum.
+# FP8 expert outputs: the wide layer with both FP8 payloads of the sync-tax
+# article (section 3.1), per-token absmax on the expert inputs and per-row
+# min/max affine on the expert outputs.
 VARIANTS = {
+    "wide_fp8_T16384_d5120_E16_k2_f1536_outfp8": MoEConfig(
+        "wide_fp8_T16384_d5120_E16_k2_f1536_outfp8", T=32 * 512, d=5120, E=16, k=2,
+        f=1536, dtype="bf16", payload_fp8=1, output_fp8=1, outlier_rate=1e-3,
+        outlier_mag=20.0, seed=3),
     "wide_fp8static_T16384_d5120_E16_k2_f1536": MoEConfig(
         "wide_fp8static_T16384_d5120_E16_k2_f1536", T=32 * 512, d=5120, E=16, k=2,
         f=1536, dtype="bf16", payload_fp8=2, payload_scale=20.0 / 448.0, outlier_rate=1e-3,
