@@ -2,7 +2,7 @@
 // section 3.1: each expert output vector is quantised on its own, from its
 // min and max, by an affine map) and the combine that consumes it.
 //
-// quantise, per routed row r of the fp32 expert outputs y (one warp a row):
+// quantise, per routed row r of the fp32 expert outputs y:
 //   zero = mx/2 + mn/2, half = mx/2 - mn/2   (one fp32 rounding each)
 //   s = half / 448 (fp32 IEEE division; 1 for a constant row)
 //   q = E4M3(fp32(y - zero) / s), round to nearest even, saturating
@@ -82,6 +82,72 @@ __global__ void __launch_bounds__(256) quantize_out_kernel(const float* __restri
   }
 }
 
+// One CTA of 256 threads per row, the row held in registers (NV float4 per
+// thread, d <= 1024 NV): one read of y, min/max by warp shuffles and a
+// shared-memory pass over the 8 warps, then the same per-value arithmetic
+// as quantize_out_kernel.
+template <int NV>
+__global__ void __launch_bounds__(256) quantize_out_cta_kernel(const float* __restrict__ y, int R,
+                                                               int d, uint8_t* __restrict__ yq,
+                                                               float* __restrict__ ys,
+                                                               float* __restrict__ yz) {
+  __shared__ float red[2][8];
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int nv = d / 4;
+  const float4* row = reinterpret_cast<const float4*>(y + static_cast<size_t>(r) * d);
+  float4 a[NV];
+  float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int v = tid + 256 * i;
+    if (v < nv) {
+      a[i] = __ldg(row + v);
+      mn = fminf(fminf(mn, a[i].x), fminf(a[i].y, fminf(a[i].z, a[i].w)));
+      mx = fmaxf(fmaxf(mx, a[i].x), fmaxf(a[i].y, fmaxf(a[i].z, a[i].w)));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  if (lane == 0) {
+    red[0][w] = mn;
+    red[1][w] = mx;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    mn = fminf(mn, red[0][i]);
+    mx = fmaxf(mx, red[1][i]);
+  }
+  const float hmx = __fmul_rn(mx, 0.5f), hmn = __fmul_rn(mn, 0.5f);
+  const float zero = __fadd_rn(hmx, hmn);
+  const float half = __fsub_rn(hmx, hmn);
+  const float s = (half == 0.f) ? 1.f : __fdiv_rn(half, 448.f);
+  uint32_t* out = reinterpret_cast<uint32_t*>(yq + static_cast<size_t>(r) * d);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int v = tid + 256 * i;
+    if (v < nv) {
+      const float2 lo = make_float2(__fdiv_rn(__fsub_rn(a[i].x, zero), s),
+                                    __fdiv_rn(__fsub_rn(a[i].y, zero), s));
+      const float2 hi = make_float2(__fdiv_rn(__fsub_rn(a[i].z, zero), s),
+                                    __fdiv_rn(__fsub_rn(a[i].w, zero), s));
+      const uint32_t b0 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t b1 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+      out[v] = b0 | (b1 << 16);
+    }
+  }
+  if (tid == 0) {
+    ys[r] = s;
+    yz[r] = zero;
+  }
+}
+
 // Two E4M3 bytes (element 0 in the low byte) -> two floats, exactly (every
 // E4M3 value is a half value).
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t b) {
@@ -89,8 +155,9 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t b) {
   return __half22float2(*reinterpret_cast<const __half2*>(&hr));
 }
 
-// 128 threads per token, two tokens per CTA; each thread owns 8-byte columns
-// c, c+128, ... of the k payload rows and keeps U of them in flight.
+// 128 threads per token, two tokens per CTA; each thread owns 16-byte
+// columns c, c+128, ... (16 values) of the k payload rows and keeps U of
+// them in flight.
 template <int DT, int KMAX>  // DT 0: fp32 out, 1: bf16 out; k <= KMAX
 __global__ void __launch_bounds__(256) combine_fp8_kernel(
     const uint8_t* __restrict__ yq, const float* __restrict__ ys, const float* __restrict__ yz,
@@ -124,11 +191,11 @@ __global__ void __launch_bounds__(256) combine_fp8_kernel(
   }
   if (bad && tl == 0) atomicOr(err, kErrBadIndex);
 
-  const int nv = d / 8;
-  const uint2* qv = reinterpret_cast<const uint2*>(yq);
-  constexpr int U = 16 / KMAX > 0 ? 16 / KMAX : 1;
+  const int nv = d / 16;
+  const uint4* qv = reinterpret_cast<const uint4*>(yq);
+  constexpr int U = 8 / KMAX > 0 ? 8 / KMAX : 1;
   for (int c0 = tl; c0 < nv; c0 += 128 * U) {
-    uint2 rows[U][KMAX];
+    uint4 rows[U][KMAX];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int c = c0 + u * 128;
@@ -140,33 +207,36 @@ __global__ void __launch_bounds__(256) combine_fp8_kernel(
     for (int u = 0; u < U; ++u) {
       const int c = c0 + u * 128;
       if (c >= nv) break;
-      float acc[8];
+      float acc[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
         if (p[j] < 0) continue;
-        const uint32_t wd[2] = {rows[u][j].x, rows[u][j].y};
+        const uint32_t wd[4] = {rows[u][j].x, rows[u][j].y, rows[u][j].z, rows[u][j].w};
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int h = 0; h < 8; ++h) {
           const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(wd[h >> 1] >> (16 * (h & 1))));
           acc[2 * h] = fmaf(wt[j], fmaf(f.x, sc[j], zr[j]), acc[2 * h]);
           acc[2 * h + 1] = fmaf(wt[j], fmaf(f.y, sc[j], zr[j]), acc[2 * h + 1]);
         }
       }
       if constexpr (DT == 0) {
-        float4* o = reinterpret_cast<float4*>(out) + (static_cast<size_t>(t) * nv + c) * 2;
-        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      } else {
-        uint4 uu;
-        uint32_t* pu = &uu.x;
+        float4* o = reinterpret_cast<float4*>(out) + (static_cast<size_t>(t) * nv + c) * 4;
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
+        for (int q = 0; q < 4; ++q)
+          o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+      } else {
+        uint4 uu[2];
+        uint32_t* pu = &uu[0].x;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
           const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
           pu[h] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        reinterpret_cast<uint4*>(out)[static_cast<size_t>(t) * nv + c] = uu;
+        uint4* o = reinterpret_cast<uint4*>(out) + (static_cast<size_t>(t) * nv + c) * 2;
+        o[0] = uu[0];
+        o[1] = uu[1];
       }
     }
   }
@@ -177,6 +247,15 @@ __global__ void __launch_bounds__(256) combine_fp8_kernel(
 cudaError_t launch_quantize_out(const float* y, int R, int d, uint8_t* yq, float* ys, float* yz,
                                 cudaStream_t s) {
   if (R == 0) return cudaSuccess;
+  // rows of more than 1024 values: a CTA per row, the row in registers (the
+  // warp-per-row kernel's second read misses L2 once many rows are in
+  // flight); short rows: a warp per row, whose re-read hits L2
+  if (d > 1024 && d <= 2048)
+    return launch_pdl(quantize_out_cta_kernel<2>, dim3(R), dim3(256), 0, s, y, R, d, yq, ys, yz);
+  if (d > 2048 && d <= 4096)
+    return launch_pdl(quantize_out_cta_kernel<4>, dim3(R), dim3(256), 0, s, y, R, d, yq, ys, yz);
+  if (d > 4096 && d <= 8192)
+    return launch_pdl(quantize_out_cta_kernel<8>, dim3(R), dim3(256), 0, s, y, R, d, yq, ys, yz);
   return launch_pdl(quantize_out_kernel, dim3(ceil_div(R, kRowsPerCta)), dim3(256), 0, s, y, R, d,
                     yq, ys, yz);
 }

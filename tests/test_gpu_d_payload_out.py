@@ -29,7 +29,12 @@ def _rows(R, d, seed):
     return y
 
 
-@pytest.mark.parametrize("R,d", [(1, 64), (9, 128), (300, 512), (2049, 1024), (32768, 5120)])
+# widths for each quantiser form: a warp per row (d <= 1024 or > 8192), a CTA
+# per row holding 2, 4 or 8 float4 per thread (ragged last pass at 1088,
+# 1536 and 5120)
+@pytest.mark.parametrize("R,d", [(1, 64), (9, 128), (300, 512), (2049, 1024), (37, 1088),
+                                 (300, 1536), (64, 4096), (33, 8192), (5, 8256),
+                                 (32768, 5120)])
 def test_quantize_output_bit_exact(cuda_ok, R, d):
     cfg = moe.make_config(T=R, d=d, E=1, k=1, f=64, pre_k=1, output_fp8=1)
     y = _rows(R, d, seed=R)
