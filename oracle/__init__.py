@@ -12,7 +12,8 @@ source pages give, with no blocking, fusion or reordering:
   gate      L = x W_g + b                   (DeepSeek-V4 EP article, sec. 2.1)
   router    max-subtracted softmax, partial top-8, exact top-k  (same, sec. 3.2);
             optionally limited to the best groups of experts (V3/V4 parallel
-            strategy article, EP section)
+            strategy article, EP section); or soft gating: a Gumbel-softmax
+            over all experts, none dropped (sync-tax article, sec. 3.3)
   dispatch  per-expert histogram, exclusive scan, stable packing (sec. 3.3;
             Deepseek-MoE sync-tax article, sec. 2.1)
   payload   optional per-token absmax FP8 E4M3                  (sync-tax, sec. 3.1)
@@ -29,7 +30,7 @@ from .moe_oracle import (  # noqa: F401
     gate_logits, route, dispatch, quantize_payload_fp8, quantize_output_fp8,
     dequantize_output_fp8, expert_ffn_rows,
     combine, forward, forward_tokens, inputs_to_numpy, ROUTER_RENORM,
-    ROUTER_PREK_SOFTMAX, ROUTER_GROUP_LIMITED,
+    ROUTER_PREK_SOFTMAX, ROUTER_GROUP_LIMITED, ROUTER_SOFT_GUMBEL,
 )
 from .numerics import (  # noqa: F401
     round_to_bf16, round_to_f32, e4m3_round_satfinite, e4m3_encode, e4m3_decode,

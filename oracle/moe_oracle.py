@@ -28,6 +28,7 @@ from .numerics import round_to_bf16, round_to_f32, e4m3_round_satfinite
 ROUTER_RENORM = 0
 ROUTER_PREK_SOFTMAX = 1
 ROUTER_GROUP_LIMITED = 2
+ROUTER_SOFT_GUMBEL = 3
 E4M3_MAX_F32 = np.float32(448.0)
 
 
@@ -45,10 +46,14 @@ def _np64(t) -> np.ndarray:
 
 
 def inputs_to_numpy(inp: dict) -> dict:
-    """x, Wg, bias as fp64 arrays; W1/W2 stay as given and are fetched one
-    expert at a time by ``_expert`` (the largest layer's weights are 15 GB)."""
-    return {"x": _np64(inp["x"]), "Wg": _np64(inp["Wg"]), "bias": _np64(inp["bias"]),
-            "W1": inp["W1"], "W2": inp["W2"]}
+    """x, Wg, bias (and the Gumbel samples of soft gating) as fp64 arrays;
+    W1/W2 stay as given and are fetched one expert at a time by ``_expert``
+    (the largest layer's weights are 15 GB)."""
+    out = {"x": _np64(inp["x"]), "Wg": _np64(inp["Wg"]), "bias": _np64(inp["bias"]),
+           "W1": inp["W1"], "W2": inp["W2"]}
+    if inp.get("gumbel") is not None:
+        out["gumbel"] = _np64(inp["gumbel"])
+    return out
 
 
 def _expert(W, e: int) -> np.ndarray:
@@ -78,7 +83,8 @@ def _softmax_max_subtracted(L: np.ndarray) -> np.ndarray:
 
 
 def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8,
-          n_group: int = 1, topk_group: int = 1):
+          n_group: int = 1, topk_group: int = 1, gumbel: np.ndarray | None = None,
+          tau: float = 1.0):
     """Top-k expert selection and gate weights.
 
     Order: logits descending, equal logits by expert id ascending (the lower
@@ -97,6 +103,10 @@ def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8,
       group id first). The k chosen experts are the top-k logits among the
       kept groups' experts, weighted as in ROUTER_RENORM (their full-softmax
       probabilities divided by their sum). pre_k plays no part.
+    * ROUTER_SOFT_GUMBEL (soft gating, [SYNC-TAX 3.3]): no top-k; the E
+      logits plus the Gumbel samples ``gumbel`` [T, E], divided by the
+      temperature tau, go through a (max-subtracted) softmax and every expert
+      keeps its probability as weight. k must equal E; slot j holds expert j.
 
     Returns (topk_idx int32 [T, k], topk_w fp64 [T, k]).
     """
@@ -104,6 +114,8 @@ def route(L: np.ndarray, k: int, router: int = ROUTER_RENORM, pre_k: int = 8,
     T, E = L.shape
     if router == ROUTER_GROUP_LIMITED:
         return _route_group_limited(L, k, n_group, topk_group)
+    if router == ROUTER_SOFT_GUMBEL:
+        return _route_soft_gumbel(L, k, gumbel, tau)
     pre_k = min(pre_k, E)
     if not (1 <= k <= pre_k):
         raise ValueError("need 1 <= k <= min(pre_k, E)")
@@ -145,6 +157,22 @@ def _route_group_limited(L: np.ndarray, k: int, n_group: int, topk_group: int):
     sel = np.argsort(-Lk, axis=1, kind="stable")[:, :k]
     ps = p[np.arange(T)[:, None], sel]
     return sel.astype(np.int32), ps / ps.sum(axis=1, keepdims=True)
+
+
+def _route_soft_gumbel(L: np.ndarray, k: int, gumbel, tau: float):
+    """Soft gating [SYNC-TAX 3.3]: Gumbel-softmax over all E experts, every
+    expert weighted (none dropped)."""
+    T, E = L.shape
+    if k != E:
+        raise ValueError("soft gating weights every expert: k must equal E")
+    if gumbel is None or np.shape(gumbel) != (T, E):
+        raise ValueError("soft gating needs Gumbel samples of shape [T, E]")
+    if not (np.isfinite(tau) and tau > 0):
+        raise ValueError("tau must be finite and positive")
+    z = (L + np.asarray(gumbel, np.float64)) / float(np.float32(tau))
+    w = _softmax_max_subtracted(z)
+    idx = np.broadcast_to(np.arange(E, dtype=np.int32), (T, E)).copy()
+    return idx, w
 
 
 # ----------------------------------------------------------------------------
@@ -286,8 +314,15 @@ def combine(Y: np.ndarray, pos: np.ndarray, topk_w: np.ndarray) -> np.ndarray:
 # ----------------------------------------------------------------------------
 # whole layer
 # ----------------------------------------------------------------------------
-def _groups(cfg):
-    return getattr(cfg, "n_group", 1), getattr(cfg, "topk_group", 1)
+def _router_args(cfg, a, tokens=None):
+    """Router arguments past (L, k): pre_k, groups, Gumbel samples, tau."""
+    g = a.get("gumbel")
+    if g is not None:
+        g = _np64(g)
+        if tokens is not None:
+            g = g[tokens]
+    return (cfg.pre_k, getattr(cfg, "n_group", 1), getattr(cfg, "topk_group", 1), g,
+            getattr(cfg, "tau", 1.0))
 
 
 def _payload(cfg, x):
@@ -318,7 +353,7 @@ def forward(cfg, inp: dict, keep_h: bool = True) -> dict:
     a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
     x = a["x"]
     L = gate_logits(x, a["Wg"], a["bias"])
-    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k, *_groups(cfg))
+    idx, w = route(L, cfg.k, cfg.router, *_router_args(cfg, a))
     counts, offsets, pos, src = dispatch(idx, cfg.E)
     res = {"L": L, "topk_idx": idx, "topk_w": w, "counts": counts,
            "offsets": offsets, "pos": pos, "src": src}
@@ -361,7 +396,7 @@ def forward_tokens(cfg, inp: dict, tokens) -> dict:
     tokens = np.asarray(tokens, dtype=np.int64)
     x = a["x"][tokens]
     L = gate_logits(x, a["Wg"], a["bias"])
-    idx, w = route(L, cfg.k, cfg.router, cfg.pre_k, *_groups(cfg))
+    idx, w = route(L, cfg.k, cfg.router, *_router_args(cfg, a, tokens))
     x_hat, _, _ = _payload(cfg, x)
     n, k = idx.shape
     y_slot = np.zeros((n, k, cfg.d), dtype=np.float64)

@@ -31,12 +31,14 @@ from dataclasses import dataclass, replace
 import torch
 
 __all__ = ["MoEConfig", "CONFIGS", "VARIANTS", "BENCH_CONFIG", "get_config", "make_inputs",
-           "ROUTER_RENORM", "ROUTER_PREK_SOFTMAX", "ROUTER_GROUP_LIMITED"]
+           "ROUTER_RENORM", "ROUTER_PREK_SOFTMAX", "ROUTER_GROUP_LIMITED",
+           "ROUTER_SOFT_GUMBEL"]
 
 # Router modes (mirrors the values in include/moe.h).
 ROUTER_RENORM = 0        # softmax over all E, keep top-k, divide by their sum
 ROUTER_PREK_SOFTMAX = 1  # softmax over the pre_k largest logits, keep top-k as is
 ROUTER_GROUP_LIMITED = 2  # top-k inside the topk_group best of n_group expert groups
+ROUTER_SOFT_GUMBEL = 3    # Gumbel-softmax over all E experts (k = E), temperature tau
 
 
 @dataclass(frozen=True)
@@ -55,6 +57,7 @@ class MoEConfig:
     payload_fp8: int = 0      # 0 none, 1 per-token absmax FP8, 2 FP8 with one static scale
     payload_scale: float = 0.0  # the static scale (payload_fp8 == 2)
     output_fp8: int = 0       # 1: expert outputs reach the combine as FP8 (min/max affine)
+    tau: float = 1.0          # soft gating temperature
     bias: str = "zero"        # "zero" | "normal" (variance bias_var) | "zipf" (exponent zipf_s)
     bias_var: float = 0.0
     zipf_s: float = 0.0
@@ -157,6 +160,9 @@ def make_inputs(cfg: MoEConfig, device="cpu") -> dict:
       bias [E]        fp32 per-expert gate bias (zeros unless the shape has one)
       W1   [E, d, f]  expert up projections, N(0, 1/d)
       W2   [E, f, d]  expert down projections, N(0, 1/f)
+      gumbel [T, E]   fp32 Gumbel(0, 1) samples, soft gating only: the random
+                      numbers the router draws, passed to both sides as an
+                      input (drawn last, as -ln of Exp(1) draws)
     """
     dev = torch.device(device)
     dt = cfg.torch_dtype
@@ -194,5 +200,9 @@ def make_inputs(cfg: MoEConfig, device="cpu") -> dict:
         bias = torch.empty(E, dtype=torch.float32, device=dev)
         bias[perm] = vals
 
-    return {"x": x.contiguous(), "Wg": Wg.contiguous(), "bias": bias.contiguous(),
-            "W1": W1, "W2": W2}
+    out = {"x": x.contiguous(), "Wg": Wg.contiguous(), "bias": bias.contiguous(),
+           "W1": W1, "W2": W2}
+    if cfg.router == ROUTER_SOFT_GUMBEL:
+        ex = torch.empty((T, E), dtype=torch.float32, device=dev).exponential_(generator=gen)
+        out["gumbel"] = (-torch.log(ex)).contiguous()
+    return out
