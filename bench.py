@@ -73,10 +73,16 @@ def stage_work(cfg, counts):
     pb = 1 if cfg.payload_fp8 else b
     active = sum(1 for c in counts if c > 0)
     w = {}
-    w["route"] = (T * d * b + d * E * b + E * 4 + R * 8, 2.0 * T * d * E)
-    w["dispatch"] = (T * d * b + R * d * pb + R * 12 + (R * 4 if cfg.payload_fp8 else 0), 0.0)
+    soft = getattr(cfg, "router", 0) == 3
+    # soft gating also reads its Gumbel samples; its dispatch writes only the
+    # layout, and its W1 GEMM reads x itself (once per expert from L2: x once
+    # from HBM)
+    w["route"] = (T * d * b + d * E * b + E * 4 + R * 8 + (T * E * 4 if soft else 0),
+                  2.0 * T * d * E)
+    w["dispatch"] = ((R * 8 + E * 8) if soft else
+                     (T * d * b + R * d * pb + R * 12 + (R * 4 if cfg.payload_fp8 else 0)), 0.0)
     w["fp8_to_bf16"] = ((R * d + R * d * 2) if cfg.payload_fp8 else 0, 0.0)
-    a_bytes = R * d * (2 if cfg.payload_fp8 else b)
+    a_bytes = T * d * b if soft else R * d * (2 if cfg.payload_fp8 else b)
     w["gemm_w1_silu"] = (active * d * f * b + a_bytes + R * f * b, 2.0 * R * d * f)
     w["gemm_w2"] = (active * f * d * b + R * f * b + R * d * 4, 2.0 * R * f * d)
     ofp8 = getattr(cfg, "output_fp8", 0)
@@ -219,7 +225,8 @@ def run_reference(args, cfg):
 
 def workload_config(cfg, args):
     router = {0: "renorm", 1: "prek_softmax",
-              2: f"group_limited(n_group={cfg.n_group}, topk_group={cfg.topk_group})"}
+              2: f"group_limited(n_group={cfg.n_group}, topk_group={cfg.topk_group})",
+              3: f"soft_gumbel(tau={cfg.tau:g}), all {cfg.E} experts"}
     payload = {0: cfg.dtype, 1: "fp8_e4m3 (per-token absmax scale)",
                2: f"fp8_e4m3 (static scale {cfg.payload_scale:.6g})"}
     return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "f": cfg.f,
@@ -264,7 +271,7 @@ def run_ours(args, cfg):
         if flush is not None:
             flush.fill_(1)
         moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
-                    out=out, events=events, stream=stream)
+                    out=out, events=events, noise=inp.get("gumbel"), stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -358,11 +365,16 @@ def run_ours(args, cfg):
         x_host = inp["x"].cpu().pin_memory()
         out_host = torch.empty((cfg.T, cfg.d), dtype=cfg.torch_dtype).pin_memory()
         x_dev = torch.empty_like(inp["x"])
+        # soft gating's Gumbel samples are a per-step input too
+        g_host = inp["gumbel"].cpu().pin_memory() if "gumbel" in inp else None
+        g_dev = torch.empty_like(inp["gumbel"]) if g_host is not None else None
 
         def e2e_step():
             x_dev.copy_(x_host, non_blocking=True)
+            if g_host is not None:
+                g_dev.copy_(g_host, non_blocking=True)
             moe.forward(cfg, x_dev, inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
-                        out=out, stream=stream)
+                        out=out, noise=g_dev, stream=stream)
             out_host.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -383,7 +395,8 @@ def run_ours(args, cfg):
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
             e_ms = float(tt.item())
         e2e = {"value": cfg.T * world / (e_ms / K / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+               "h2d_bytes_per_step": x_host.numel() * x_host.element_size() + (
+                   g_host.numel() * g_host.element_size() if g_host is not None else 0),
                "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
 
     if dist:

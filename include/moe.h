@@ -82,7 +82,15 @@ enum {
    * kept (equal scores: lower group id first); the k largest logits among
    * the kept groups' experts are chosen (lower id first on ties) and
    * weighted as in MOE_ROUTER_RENORM. pre_k is validated but not used. */
-  MOE_ROUTER_GROUP_LIMITED = 2
+  MOE_ROUTER_GROUP_LIMITED = 2,
+  /* soft gating (Deepseek-MoE sync-tax article, section 3.3: Gumbel-Softmax
+   * instead of hard top-k, every expert output weighted): with g the
+   * caller's Gumbel samples (the `noise` argument, [T, E] fp32),
+   * w[t, e] = softmax_e((L[t, e] + g[t, e]) / tau), max-subtracted; k must
+   * equal E (at most 16) and slot j holds expert j. Every token goes to
+   * every expert in token order, so dispatch writes only the layout and the
+   * W1 GEMM reads x itself (no packed rows, no FP8 payload). */
+  MOE_ROUTER_SOFT_GUMBEL = 3
 };
 
 typedef struct moe_config {
@@ -107,6 +115,7 @@ typedef struct moe_config {
   int32_t output_fp8;  /* 1: moe_forward hands the expert outputs to the combine
                         * as an FP8 payload (moe_quantize_output, then
                         * moe_combine_fp8); 0: fp32 rows (moe_combine) */
+  float tau;           /* MOE_ROUTER_SOFT_GUMBEL: temperature, finite and > 0 */
 } moe_config_t;
 
 /* Validate a configuration. Returns MOE_OK or MOE_ERR_INVALID_ARG /
@@ -127,18 +136,24 @@ MOE_API size_t moe_scratch_size(const moe_config_t* cfg);
 MOE_API size_t moe_workspace_size(const moe_config_t* cfg);
 
 /* ---- stage 1: gate + router ---------------------------------------------
- * x [T, d] (dtype), W_g [d, E] (dtype), bias [E] fp32 or NULL (= zeros).
+ * x [T, d] (dtype), W_g [d, E] (dtype), bias [E] fp32 or NULL (= zeros),
+ * noise [T, E] fp32: the Gumbel samples of MOE_ROUTER_SOFT_GUMBEL (required
+ * there, ignored by the other routers, may be NULL).
  * Outputs: topk_idx [T, k] int32, topk_w [T, k] fp32, slot j = j-th choice
- * (logit descending, lower id first on ties); logits [T, E] fp32 or NULL:
- * the gate logits including the bias, as the router saw them.
+ * (logit descending, lower id first on ties; soft gating: expert j);
+ * logits [T, E] fp32 or NULL: the gate logits including the bias, as the
+ * router saw them (before the noise).
  * Logits are accumulated in fp32 from exact products, in K-chunks combined
  * with compensated summation. */
 MOE_API int moe_route(const moe_config_t* cfg, const void* x, const void* W_g,
-              const float* bias, int32_t* topk_idx, float* topk_w,
+              const float* bias, const float* noise, int32_t* topk_idx, float* topk_w,
               float* logits, void* stream);
 
 /* ---- stage 2: dispatch ---------------------------------------------------
  * Inputs: x [T, d] (dtype), topk_idx [T, k] int32.
+ * (MOE_ROUTER_SOFT_GUMBEL: only counts, offsets, pos and src are written,
+ * for the routing every token -> every expert in token order; x, topk_idx,
+ * x_perm and x_scale are not used and may be NULL.)
  * Outputs (R = T*k):
  *   counts  [E]    int32  rows routed to each expert
  *   offsets [E+1]  int32  exclusive prefix sum of counts; offsets[E] = R
@@ -190,6 +205,8 @@ MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
  * (dtype, expert-major), h [R, f] (dtype) output, y_perm [R, d] fp32 output.
  * bf16 uses the tcgen05 tensor cores (fp32 accumulate in TMEM); fp32 uses
  * fp32 FMA. Experts with no rows read none of their weights.
+ * MOE_ROUTER_SOFT_GUMBEL: x_perm is x itself, [T, d]; row r of expert e's
+ * segment reads x[r - offsets[e]] (every expert reads all T rows).
  * ws: >= moe_scratch_size bytes. */
 MOE_API int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
                    const float* x_scale, const int32_t* offsets, const void* W1,
@@ -232,24 +249,27 @@ MOE_API int moe_combine_fp8(const moe_config_t* cfg, const uint8_t* y_q, const f
  * moe_route -> moe_dispatch -> moe_expert_ffn -> moe_combine (or, with
  * output_fp8, moe_quantize_output -> moe_combine_fp8) on one stream, with
  * every intermediate in the workspace (>= moe_workspace_size bytes).
+ * noise: as for moe_route (the soft router's Gumbel samples, else NULL).
  * No host synchronisation, so the call can be captured into a CUDA graph. */
 MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g,
-                const float* bias, const void* W1, const void* W2, void* out,
-                void* ws, size_t ws_bytes, void* stream);
+                const float* bias, const float* noise, const void* W1, const void* W2,
+                void* out, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward that also records CUDA events (cudaEvent_t, passed as void*)
  * at the kernel boundaries, for per-kernel timing on the launching stream:
  *   events[0] before the route kernel      events[1] after route
- *   events[2] after dispatch (3 kernels)   events[3] after the FP8 row
+ *   events[2] after dispatch (3 kernels; 1 with soft gating)
+ *                                          events[3] after the FP8 row
  *   conversion (= events[2] without FP8)   events[4] after the W1 GEMM
  *   events[5] after the W2 GEMM            events[6] after the output
  *   quantisation (= events[5] without)     events[7] after combine
  * n_events must be MOE_NUM_EVENTS; any entry may be NULL (not recorded). */
 #define MOE_NUM_EVENTS 8
 MOE_API int moe_forward_with_events(const moe_config_t* cfg, const void* x,
-                            const void* W_g, const float* bias, const void* W1,
-                            const void* W2, void* out, void* ws, size_t ws_bytes,
-                            void* const* events, int n_events, void* stream);
+                            const void* W_g, const float* bias, const float* noise,
+                            const void* W1, const void* W2, void* out, void* ws,
+                            size_t ws_bytes, void* const* events, int n_events,
+                            void* stream);
 
 /* Pointers into a forward workspace, so a caller can inspect the
  * intermediates of the last moe_forward (routing, permutation, H, Y).

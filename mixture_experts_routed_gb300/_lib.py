@@ -20,6 +20,7 @@ MOE_DTYPE_BF16 = 1
 MOE_ROUTER_RENORM = 0
 MOE_ROUTER_PREK_SOFTMAX = 1
 MOE_ROUTER_GROUP_LIMITED = 2
+MOE_ROUTER_SOFT_GUMBEL = 3
 MOE_NUM_EVENTS = 8
 
 
@@ -27,7 +28,8 @@ class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("T", "d", "E", "k", "f", "dtype", "router", "pre_k", "payload_fp8",
                  "n_group", "topk_group")] + [("payload_scale", ctypes.c_float),
-                                             ("output_fp8", ctypes.c_int32)]
+                                             ("output_fp8", ctypes.c_int32),
+                                             ("tau", ctypes.c_float)]
 
 
 class MoeForwardViews(ctypes.Structure):
@@ -50,14 +52,14 @@ PROTOTYPES = {
     "moe_check_config": (_I, [_CFG]),
     "moe_scratch_size": (_SZ, [_CFG]),
     "moe_workspace_size": (_SZ, [_CFG]),
-    "moe_route": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_expert_ffn": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_combine": (_I, [_CFG, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_quantize_output": (_I, [_CFG, _P, _P, _P, _P, _P]),
     "moe_combine_fp8": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_forward": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "moe_forward_with_events": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ,
+    "moe_forward": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "moe_forward_with_events": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
                                      ctypes.POINTER(ctypes.c_void_p), _I, _P]),
     "moe_forward_views": (_I, [_CFG, _P, ctypes.POINTER(MoeForwardViews)]),
     "moe_get_device_error": (_I, [_P, _P]),

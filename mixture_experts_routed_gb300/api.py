@@ -29,22 +29,23 @@ class MoEError(RuntimeError):
 
 def make_config(T, d, E, k, f, dtype="bf16", router=L.MOE_ROUTER_RENORM, pre_k=8,
                 payload_fp8=0, n_group=1, topk_group=1, payload_scale=0.0,
-                output_fp8=0) -> L.MoeConfig:
+                output_fp8=0, tau=1.0) -> L.MoeConfig:
     dt = {"f32": L.MOE_DTYPE_F32, "fp32": L.MOE_DTYPE_F32, "bf16": L.MOE_DTYPE_BF16,
           torch.float32: L.MOE_DTYPE_F32, torch.bfloat16: L.MOE_DTYPE_BF16}[dtype]
     return L.MoeConfig(int(T), int(d), int(E), int(k), int(f), dt, int(router), int(pre_k),
                        int(payload_fp8), int(n_group), int(topk_group), float(payload_scale),
-                       int(output_fp8))
+                       int(output_fp8), float(tau))
 
 
 def config_from(c) -> L.MoeConfig:
     """From any object with T, d, E, k, f, dtype, router, pre_k, payload_fp8
-    (and, optionally, n_group, topk_group, payload_scale and output_fp8)."""
+    (and, optionally, n_group, topk_group, payload_scale, output_fp8, tau)."""
     if isinstance(c, L.MoeConfig):
         return c
     return make_config(c.T, c.d, c.E, c.k, c.f, c.dtype, c.router, c.pre_k, c.payload_fp8,
                        getattr(c, "n_group", 1), getattr(c, "topk_group", 1),
-                       getattr(c, "payload_scale", 0.0), getattr(c, "output_fp8", 0))
+                       getattr(c, "payload_scale", 0.0), getattr(c, "output_fp8", 0),
+                       getattr(c, "tau", 1.0))
 
 
 def _cfg(c):
@@ -93,8 +94,9 @@ def alloc_workspace(c, kind: str = "forward", device=None) -> torch.Tensor:
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
-def route(c, x, Wg, bias=None, *, topk_idx=None, topk_w=None, logits=None,
+def route(c, x, Wg, bias=None, *, noise=None, topk_idx=None, topk_w=None, logits=None,
           want_logits=False, stream=None):
+    """Gate + router. ``noise``: the soft router's Gumbel samples [T, E]."""
     cc = config_from(c)
     dev = x.device
     if topk_idx is None:
@@ -103,8 +105,8 @@ def route(c, x, Wg, bias=None, *, topk_idx=None, topk_w=None, logits=None,
         topk_w = torch.empty((cc.T, cc.k), dtype=torch.float32, device=dev)
     if logits is None and want_logits:
         logits = torch.empty((cc.T, cc.E), dtype=torch.float32, device=dev)
-    st = L.load().moe_route(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(topk_idx),
-                            _p(topk_w), _p(logits), _s(stream))
+    st = L.load().moe_route(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(noise),
+                            _p(topk_idx), _p(topk_w), _p(logits), _s(stream))
     _check(st, "moe_route")
     return topk_idx, topk_w, logits
 
@@ -119,7 +121,8 @@ def dispatch(c, x, topk_idx, *, ws, counts=None, offsets=None, pos=None, src=Non
     offsets = torch.empty(cc.E + 1, **i32) if offsets is None else offsets
     pos = torch.empty(R, **i32) if pos is None else pos
     src = torch.empty(R, **i32) if src is None else src
-    if x_perm is None:
+    soft = cc.router == L.MOE_ROUTER_SOFT_GUMBEL
+    if x_perm is None and not soft:       # soft gating packs no rows
         pdt = torch.uint8 if cc.payload_fp8 else _dt(cc)
         x_perm = torch.empty((R, cc.d), dtype=pdt, device=dev)
     if x_scale is None and cc.payload_fp8:
@@ -133,6 +136,7 @@ def dispatch(c, x, topk_idx, *, ws, counts=None, offsets=None, pos=None, src=Non
 
 
 def expert_ffn(c, x_perm, x_scale, offsets, W1, W2, *, ws, h=None, y_perm=None, stream=None):
+    """Grouped FFN. With the soft router ``x_perm`` is x itself ([T, d])."""
     cc = config_from(c)
     dev = x_perm.device
     R = cc.T * cc.k
@@ -184,17 +188,18 @@ def combine_fp8(c, y_q, y_scale, y_zero, pos, topk_w, *, ws, out=None, stream=No
     return out
 
 
-def forward(c, x, Wg, bias, W1, W2, *, ws, out=None, events=None, stream=None):
+def forward(c, x, Wg, bias, W1, W2, *, ws, out=None, events=None, noise=None, stream=None):
     """The whole layer. ``events``: optional list of MOE_NUM_EVENTS
-    torch.cuda.Event (or None) recorded at the kernel boundaries."""
+    torch.cuda.Event (or None) recorded at the kernel boundaries. ``noise``:
+    the soft router's Gumbel samples [T, E]."""
     cc = config_from(c)
     if out is None:
         out = torch.empty((cc.T, cc.d), dtype=_dt(cc), device=x.device)
     lib = L.load()
     nbytes = ws.numel() * ws.element_size()
     if events is None:
-        st = lib.moe_forward(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(W1), _p(W2),
-                             _p(out), _p(ws), nbytes, _s(stream))
+        st = lib.moe_forward(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(noise), _p(W1),
+                             _p(W2), _p(out), _p(ws), nbytes, _s(stream))
     else:
         strm = stream if stream is not None else torch.cuda.current_stream()
         for e in events:
@@ -202,9 +207,9 @@ def forward(c, x, Wg, bias, W1, W2, *, ws, out=None, events=None, stream=None):
                 e.record(strm)          # torch creates its CUDA event lazily
         arr = (ctypes.c_void_p * L.MOE_NUM_EVENTS)(
             *[None if e is None else e.cuda_event for e in events])
-        st = lib.moe_forward_with_events(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(W1),
-                                         _p(W2), _p(out), _p(ws), nbytes, arr, len(events),
-                                         _s(stream))
+        st = lib.moe_forward_with_events(ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(noise),
+                                         _p(W1), _p(W2), _p(out), _p(ws), nbytes, arr,
+                                         len(events), _s(stream))
     _check(st, "moe_forward")
     return out
 
@@ -233,7 +238,7 @@ def forward_views(c, ws) -> dict:
         "offsets": view(v.offsets, cc.E + 1, torch.int32, (cc.E + 1,)),
         "pos": view(v.pos, R, torch.int32, (R,)),
         "src": view(v.src, R, torch.int32, (R,)),
-        "x_perm": view(v.x_perm, R * cc.d, pdt, (R, cc.d)),
+        "x_perm": view(v.x_perm, R * cc.d, pdt, (R, cc.d)) if v.x_perm else None,
         "x_scale": view(v.x_scale, R, torch.float32, (R,)) if cc.payload_fp8 else None,
         "h": view(v.h, R * cc.f, _dt(cc), (R, cc.f)),
         "y_perm": view(v.y_perm, R * cc.d, torch.float32, (R, cc.d)),

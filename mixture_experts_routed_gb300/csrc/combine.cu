@@ -98,11 +98,13 @@ cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const 
   if (dtype == 0) {
     if (k <= 2) MOE_COMBINE(0, 2);
     if (k <= 4) MOE_COMBINE(0, 4);
-    MOE_COMBINE(0, 8);
+    if (k <= 8) MOE_COMBINE(0, 8);
+    MOE_COMBINE(0, 16);
   }
   if (k <= 2) MOE_COMBINE(1, 2);
   if (k <= 4) MOE_COMBINE(1, 4);
-  MOE_COMBINE(1, 8);
+  if (k <= 8) MOE_COMBINE(1, 8);
+  MOE_COMBINE(1, 16);
 #undef MOE_COMBINE
 }
 

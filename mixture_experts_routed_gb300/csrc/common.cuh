@@ -59,15 +59,21 @@ constexpr int kMaxTopK = 8;
 
 // Router parameters, as in moe_config_t. mode: 0 renormalised top-k, 1
 // softmax over the pre_k largest logits, 2 group-limited top-k (the k best
-// experts inside the topk_group best of n_group groups of consecutive ids).
+// experts inside the topk_group best of n_group groups of consecutive ids),
+// 3 soft gating (softmax((L + noise) / tau) over all E experts, k = E).
 struct RouterSpec {
   int k;
   int pre_k;
   int mode;
   int n_group;
   int topk_group;
+  float tau;
+  const float* noise;  // [T, E] Gumbel samples (soft gating)
 };
 constexpr int kMaxGroups = 32;
+// Rows a token may fan out to (k): kMaxTopK for the top-k routers, up to
+// kMaxFanout (= E) for soft gating.
+constexpr int kMaxFanout = 16;
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -105,6 +111,10 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, cons
                                     const int32_t* counts, const int32_t* base,
                                     int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
                                     float* x_scale, uint32_t* err, cudaStream_t s);
+// Soft gating's layout (every token to every expert, token order): counts,
+// offsets, pos, src; zeroes `nzero` words at `zero` when non-null.
+cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,
+                                int32_t* src, uint32_t* zero, int nzero, cudaStream_t s);
 // E4M3 payload bytes -> bf16 (exact), for the tensor-core A operand.
 cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s);
 
@@ -122,16 +132,20 @@ cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, co
                                void* out, uint32_t* err, cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm_tc.cu
-// Grouped GEMM over expert segments on tcgen05: out[r] = epi(A[r] . W[e]).
-// A [R, K] bf16, W [E, K, N] bf16, offsets [E+1]. epi 0: (row scale) -> SiLU
-// -> bf16 out; epi 1: fp32 out. `tile_ctr` must be zero at launch.
-cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, int K, int N,
-                           const int32_t* offsets, const float* row_scale, void* out,
-                           uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s);
+// Grouped GEMM over expert segments on tcgen05: out[r] = epi(A[a(r)] . W[e])
+// for the rows r of expert e's segment [offsets[e], offsets[e+1]); a(r) = r,
+// or r - offsets[e] when a_shared (every expert reads the same a_rows rows of
+// A). A [a_rows, K] bf16, W [E, K, N] bf16. epi 0: (row scale) -> SiLU ->
+// bf16 out; epi 1: fp32 out. `tile_ctr` must be zero at launch.
+cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int R, const void* W,
+                           int E, int K, int N, const int32_t* offsets, const float* row_scale,
+                           void* out, uint32_t* err, uint32_t* tile_ctr, int num_sms,
+                           cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm_simt.cu
 // The same grouped GEMM in fp32 FMA for fp32 layers.
-cudaError_t launch_gemm_simt(int epi, const float* A, int R, const float* W, int E, int K, int N,
-                             const int32_t* offsets, float* out, uint32_t* err, cudaStream_t s);
+cudaError_t launch_gemm_simt(int epi, const float* A, int a_shared, int R, const float* W, int E,
+                             int K, int N, const int32_t* offsets, float* out, uint32_t* err,
+                             cudaStream_t s);
 
 }  // namespace moe

@@ -327,6 +327,31 @@ __global__ void fp8_to_bf16_kernel(const uint8_t* __restrict__ q, size_t n16,
   }
 }
 
+// Soft gating sends every token to every expert in token order: the layout
+// is known without counting. counts[e] = T, offsets[e] = e T, pos[t E + e] =
+// e T + t, src[e T + t] = t; also zeroes `nzero` words at `zero` (the GEMM
+// tile counters).
+__global__ void __launch_bounds__(256) dense_layout_kernel(int T, int E, int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ pos,
+                                                           int32_t* __restrict__ src,
+                                                           uint32_t* __restrict__ zero, int nzero) {
+  pdl_wait();
+  pdl_trigger();
+  const long long R = static_cast<long long>(T) * E;
+  const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i < R) {
+    const int t = static_cast<int>(i / E), e = static_cast<int>(i % E);
+    pos[i] = e * T + t;
+    src[i] = static_cast<int32_t>(i % T);  // row i = e' T + t' holds token t'
+  }
+  if (blockIdx.x == 0) {
+    if (threadIdx.x <= E) offsets[threadIdx.x] = threadIdx.x * T;
+    if (threadIdx.x < E) counts[threadIdx.x] = T;
+    if (zero != nullptr && threadIdx.x < nzero) zero[threadIdx.x] = 0u;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cudaStream_t s) {
@@ -356,6 +381,14 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, cons
                 : (!fp8 ? dispatch_scatter_kernel<1, false> : dispatch_scatter_kernel<1, true>);
   return launch_pdl(kernel, grid, block, 0, s, x, topk_idx, T, d, k, E, nchunk, counts, base,
                     offsets, pos, src, x_perm, x_scale, static_scale, err);
+}
+
+cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,
+                                int32_t* src, uint32_t* zero, int nzero, cudaStream_t s) {
+  const long long R = static_cast<long long>(T) * E;
+  const int blocks = static_cast<int>((R + 255) / 256) > 0 ? static_cast<int>((R + 255) / 256) : 1;
+  return launch_pdl(dense_layout_kernel, dim3(blocks), dim3(256), 0, s, T, E, counts, offsets,
+                    pos, src, zero, nzero);
 }
 
 cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s) {

@@ -81,14 +81,20 @@ extern "C" MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void*
   const int st = moe_check_config(cfg);
   if (st != MOE_OK) return st;
   if (counts == nullptr || offsets == nullptr) return MOE_ERR_INVALID_ARG;
-  if (cfg->T > 0 && (!aligned16(x) || topk_idx == nullptr || pos == nullptr ||
-                     src == nullptr || !aligned16(x_perm) ||
-                     (cfg->payload_fp8 && x_scale == nullptr)))
+  const bool soft = cfg->router == MOE_ROUTER_SOFT_GUMBEL;
+  if (cfg->T > 0 && (pos == nullptr || src == nullptr ||
+                     (!soft && (!aligned16(x) || topk_idx == nullptr || !aligned16(x_perm) ||
+                                (cfg->payload_fp8 && x_scale == nullptr)))))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cfg->T == 0)
     return launch_dispatch_empty(cfg->E, counts, offsets, s) == cudaSuccess ? MOE_OK
                                                                              : MOE_ERR_LAUNCH;
+  if (soft)  // every token to every expert: no tables needed
+    return launch_dense_layout(cfg->T, cfg->E, counts, offsets, pos, src, nullptr, 0, s) ==
+                   cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_LAUNCH;
   const int nchunk = ceil_div(cfg->T, kDispatchTokensPerChunk);
   if (static_cast<size_t>(cfg->E) * static_cast<size_t>(nchunk) > kNoAllocTableEntries)
     return MOE_ERR_WORKSPACE_TOO_SMALL;

@@ -250,9 +250,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // the logits row from shared memory (stride E + 1: conflict-free)
   if (threadIdx.x < BM) {
     const int r = threadIdx.x;
-    if (t0 + r < T)
-      topk::thread_select_and_weigh(Ls + r * (E + 1), E, rs, t0 + r, topk_idx,
-                                    topk_w);
+    if (t0 + r < T) {
+      if (rs.mode == topk::kRouterSoft)
+        topk::thread_soft_weigh(Ls + r * (E + 1), E, rs, t0 + r, topk_idx, topk_w);
+      else
+        topk::thread_select_and_weigh(Ls + r * (E + 1), E, rs, t0 + r, topk_idx, topk_w);
+    }
   }
   __syncthreads();
   if (warp == 1) {

@@ -60,6 +60,8 @@ struct TcParams {
   uint32_t* tile_ctr;  // next tile to hand out; zero before the launch
   int E, K, N, R, n_tiles;
   int n_tiles_m;       // feature blocks of a merged tile (ceil(N / 224))
+  int a_rows;          // rows of A
+  int a_shared;        // 1: output row r of expert e reads A row r - offsets[e]
 };
 
 // z * sigmoid(z) with the approximate divide: the result is rounded to bf16,
@@ -371,7 +373,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
         // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
         const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
-        const int my_row = min(t.row0 + static_cast<int>(rank) * half_rows, p.R - 1);
+        const int a_base = p.a_shared ? seg[t.e] : 0;
+        const int my_row = min(t.row0 - a_base + static_cast<int>(rank) * half_rows, p.a_rows - 1);
         // MMA j covers features n0 + 256 j + [0, 256); this CTA holds the
         // 128 at n0 + 256 j + half_w rank (half_w = 128, or 112 in a merged
         // tile); a box is issued when it starts below N (one that runs past
@@ -389,7 +392,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         // merged tile: this CTA's half of the remainder rows (8 or 16) in
         // 8-row boxes
         const int tail_half = ((t.tail + 15) & ~15) / 2;
-        const int tail_row = t.row0 + pairk::BM + static_cast<int>(rank) * tail_half;
+        const int tail_row = t.row0 - a_base + pairk::BM + static_cast<int>(rank) * tail_half;
         bytes += static_cast<uint32_t>(2 * tail_half * pairk::BK * 2);
         const int brow = t.e * p.K;
         for (int kb = 0; kb < KB; ++kb) {
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           if constexpr (S::MERGE) {
             for (int r = 0; r < tail_half; r += 8)
               tma_load_2d_pair(sT + s * S::T_BYTES + r * pairk::BK * 2, &tmA8, bar,
-                               kb * pairk::BK, min(tail_row + r, p.R - 1));
+                               kb * pairk::BK, min(tail_row + r, p.a_rows - 1));
           }
           armed |= 1u << s;
           armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
@@ -787,9 +790,10 @@ int pick_nb(int epi, int R, int E, int K, int N, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, int K, int N,
-                           const int32_t* offsets, const float* row_scale, void* out,
-                           uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
+cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int R, const void* W,
+                           int E, int K, int N, const int32_t* offsets, const float* row_scale,
+                           void* out, uint32_t* err, uint32_t* tile_ctr, int num_sms,
+                           cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   if (num_sms < 2) return cudaErrorInvalidValue;
   CUtensorMap mA, mA8, mB;
@@ -799,8 +803,9 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
   // A: token rows, [128 rows][64 k] boxes; B: weights as [E*K rows, N], [64 k][64 n] boxes
   // A: token rows in [128 rows][64 k] boxes, and [8 rows][64 k] boxes for
   // merged tiles' remainders
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128) ||
-      !make_map_2d(&mA8, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 8))
+  if (a_rows <= 0) return cudaErrorInvalidValue;
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64, 128) ||
+      !make_map_2d(&mA8, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64, 8))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64,
                    pairk::BK))
@@ -816,6 +821,8 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int R, const void* W, int E, 
   prm.N = N;
   prm.R = R;
   prm.n_tiles = 0;
+  prm.a_rows = a_rows;
+  prm.a_shared = a_shared;
   int nb = pick_nb(epi, R, E, K, N, num_sms);
   // MOE_GEMM_TILE_FEATURES=256|512 overrides the choice (read on every call)
   if (const char* f = std::getenv("MOE_GEMM_TILE_FEATURES")) {

@@ -24,8 +24,7 @@ int check_cfg(const moe_config_t* c) {
   if (c->d % 64 != 0 || c->f % 64 != 0) return MOE_ERR_INVALID_ARG;
   if (c->E > kMaxExperts) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_DTYPE_F32 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->router != MOE_ROUTER_RENORM && c->router != MOE_ROUTER_PREK_SOFTMAX &&
-      c->router != MOE_ROUTER_GROUP_LIMITED)
+  if (c->router < MOE_ROUTER_RENORM || c->router > MOE_ROUTER_SOFT_GUMBEL)
     return MOE_ERR_INVALID_ARG;
   if (c->router == MOE_ROUTER_GROUP_LIMITED) {
     if (c->n_group < 1 || c->n_group > kMaxGroups || c->E % c->n_group != 0)
@@ -39,7 +38,14 @@ int check_cfg(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   const int max_pre = c->E < kMaxTopK ? c->E : kMaxTopK;
   if (c->pre_k < 1 || c->pre_k > max_pre) return MOE_ERR_INVALID_ARG;
-  if (c->k > c->pre_k) return MOE_ERR_INVALID_ARG;
+  if (c->router == MOE_ROUTER_SOFT_GUMBEL) {
+    // every expert weighted: k = E rows per token, up to kMaxFanout
+    if (c->k != c->E || c->E > kMaxFanout) return MOE_ERR_INVALID_ARG;
+    if (!(c->tau > 0.f && c->tau <= FLT_MAX)) return MOE_ERR_INVALID_ARG;
+    if (c->payload_fp8) return MOE_ERR_UNSUPPORTED;  // the GEMM reads x itself
+  } else if (c->k > c->pre_k) {
+    return MOE_ERR_INVALID_ARG;
+  }
   if (c->payload_fp8 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->d > 65536 || c->f > 65536) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->T) * c->k > INT_MAX) return MOE_ERR_UNSUPPORTED;
@@ -47,6 +53,8 @@ int check_cfg(const moe_config_t* c) {
 }
 
 size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
+
+bool soft(const moe_config_t& c) { return c.router == MOE_ROUTER_SOFT_GUMBEL; }
 
 struct Layout {
   size_t err, hist, base, stage, scratch_end;
@@ -77,7 +85,8 @@ Layout layout_of(const moe_config_t& c) {
   L.offsets = take(static_cast<size_t>(c.E + 1) * 4);
   L.pos = take(R * 4);
   L.src = take(R * 4);
-  L.x_perm = take(R * c.d * (c.payload_fp8 ? 1 : es));
+  // soft gating: every expert reads x itself, nothing is packed
+  L.x_perm = take(soft(c) ? 0 : R * c.d * (c.payload_fp8 ? 1 : es));
   L.x_scale = take(c.payload_fp8 ? R * 4 : 0);
   L.h = take(R * c.f * es);
   L.y = take(R * c.d * 4);
@@ -116,8 +125,9 @@ void record(void* const* ev, int i, cudaStream_t s) {
 
 // ---------------------------------------------------------------- stages
 int run_route(const moe_config_t& c, const void* x, const void* Wg, const float* bias,
-              int32_t* idx, float* w, float* logits, uint32_t* err, cudaStream_t s) {
-  const RouterSpec rs{c.k, c.pre_k, c.router, c.n_group, c.topk_group};
+              const float* noise, int32_t* idx, float* w, float* logits, uint32_t* err,
+              cudaStream_t s) {
+  const RouterSpec rs{c.k, c.pre_k, c.router, c.n_group, c.topk_group, c.tau, noise};
   return status_of(launch_route(c.dtype, x, Wg, bias, c.T, c.d, c.E, rs, idx, w, logits, err, s));
 }
 
@@ -125,6 +135,9 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
                  const int32_t* idx, int32_t* counts, int32_t* offsets, int32_t* pos,
                  int32_t* src, void* x_perm, float* x_scale, cudaStream_t s) {
   if (c.T == 0) return status_of(launch_dispatch_empty(c.E, counts, offsets, s));
+  if (soft(c))  // every token to every expert: the layout needs no counting
+    return status_of(launch_dense_layout(c.T, c.E, counts, offsets, pos, src, gemm_counters(ws),
+                                         kNumGemmCounters, s));
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* hist = at<int32_t>(ws, L.hist);
   int32_t* base = at<int32_t>(ws, L.base);
@@ -157,10 +170,10 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (c.dtype == MOE_DTYPE_F32) {
     if (which == 1)
-      return status_of(launch_gemm_simt(0, static_cast<const float*>(x_perm), R,
+      return status_of(launch_gemm_simt(0, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
                                         static_cast<const float*>(W1), c.E, c.d, c.f, offsets,
                                         static_cast<float*>(h), err, s));
-    return status_of(launch_gemm_simt(1, static_cast<const float*>(h), R,
+    return status_of(launch_gemm_simt(1, static_cast<const float*>(h), 0, R,
                                       static_cast<const float*>(W2), c.E, c.f, c.d, offsets, y,
                                       err, s));
   }
@@ -168,12 +181,14 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
   if (sms <= 0) return MOE_ERR_LAUNCH;
   uint32_t* ctr = gemm_counters(ws) + (which - 1);
   if (which == 1) {
+    // soft gating: x_perm is x itself, [T, d], read by every expert
     const void* A = c.payload_fp8 ? at<void>(ws, L.stage) : x_perm;
-    return status_of(launch_gemm_tc(0, A, R, W1, c.E, c.d, c.f, offsets,
-                                    c.payload_fp8 ? x_scale : nullptr, h, err, ctr, sms, s));
+    return status_of(launch_gemm_tc(0, A, soft(c) ? c.T : R, soft(c) ? 1 : 0, R, W1, c.E, c.d,
+                                    c.f, offsets, c.payload_fp8 ? x_scale : nullptr, h, err, ctr,
+                                    sms, s));
   }
   return status_of(
-      launch_gemm_tc(1, h, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, ctr, sms, s));
+      launch_gemm_tc(1, h, R, 0, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, ctr, sms, s));
 }
 
 int run_combine(const moe_config_t& c, const Layout& L, void* ws, const float* y,
@@ -185,13 +200,13 @@ int run_combine(const moe_config_t& c, const Layout& L, void* ws, const float* y
 bool ok_ptr(const void* p) { return p != nullptr && aligned(p, 16); }
 
 int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const float* bias,
-                 const void* W1, const void* W2, void* out, void* ws, size_t ws_bytes,
-                 void* const* events, void* stream) {
+                 const float* noise, const void* W1, const void* W2, void* out, void* ws,
+                 size_t ws_bytes, void* const* events, void* stream) {
   int st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   const moe_config_t& c = *cfg;
   if (!ok_ptr(x) || Wg == nullptr || !ok_ptr(W1) || !ok_ptr(W2) || !ok_ptr(out) ||
-      ws == nullptr || !aligned(ws, kAlign))
+      ws == nullptr || !aligned(ws, kAlign) || (soft(c) && c.T > 0 && noise == nullptr))
     return MOE_ERR_INVALID_ARG;
   const Layout L = layout_of(c);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -202,13 +217,15 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* pos = at<int32_t>(ws, L.pos);
   int32_t* src = at<int32_t>(ws, L.src);
-  void* x_perm = at<void>(ws, L.x_perm);
+  // soft gating packs nothing: the W1 GEMM reads x for every expert
+  void* x_perm = soft(c) ? const_cast<void*>(x) : at<void>(ws, L.x_perm);
   float* x_scale = c.payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
   void* h = at<void>(ws, L.h);
   float* y = at<float>(ws, L.y);
 
   record(events, 0, s);
-  if ((st = run_route(c, x, Wg, bias, idx, w, nullptr, at<uint32_t>(ws, L.err), s)) != MOE_OK)
+  if ((st = run_route(c, x, Wg, bias, noise, idx, w, nullptr, at<uint32_t>(ws, L.err), s)) !=
+      MOE_OK)
     return st;
   record(events, 1, s);
   if ((st = run_dispatch(c, L, ws, x, idx, counts, offsets, pos, src, x_perm, x_scale, s)) !=
@@ -261,13 +278,16 @@ size_t moe_workspace_size(const moe_config_t* cfg) {
 }
 
 int moe_route(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
-              int32_t* topk_idx, float* topk_w, float* logits, void* stream) {
+              const float* noise, int32_t* topk_idx, float* topk_w, float* logits,
+              void* stream) {
   const int st = check_cfg(cfg);
   if (st != MOE_OK) return st;
   if (cfg->T == 0) return MOE_OK;
-  if (!ok_ptr(x) || W_g == nullptr || topk_idx == nullptr || topk_w == nullptr)
+  if (!ok_ptr(x) || W_g == nullptr || topk_idx == nullptr || topk_w == nullptr ||
+      (soft(*cfg) && noise == nullptr))
     return MOE_ERR_INVALID_ARG;
-  return run_route(*cfg, x, W_g, bias, topk_idx, topk_w, logits, nullptr, as_stream(stream));
+  return run_route(*cfg, x, W_g, bias, noise, topk_idx, topk_w, logits, nullptr,
+                   as_stream(stream));
 }
 
 int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
@@ -277,8 +297,9 @@ int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* topk_idx
   if (st != MOE_OK) return st;
   if (counts == nullptr || offsets == nullptr || ws == nullptr || !aligned(ws, kAlign))
     return MOE_ERR_INVALID_ARG;
-  if (cfg->T > 0 && (!ok_ptr(x) || topk_idx == nullptr || pos == nullptr || src == nullptr ||
-                     !ok_ptr(x_perm) || (cfg->payload_fp8 && x_scale == nullptr)))
+  if (cfg->T > 0 && (pos == nullptr || src == nullptr ||
+                     (!soft(*cfg) && (!ok_ptr(x) || topk_idx == nullptr || !ok_ptr(x_perm) ||
+                                      (cfg->payload_fp8 && x_scale == nullptr)))))
     return MOE_ERR_INVALID_ARG;
   const Layout L = layout_of(*cfg);
   if (ws_bytes < L.scratch_end) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -348,17 +369,17 @@ int moe_combine_fp8(const moe_config_t* cfg, const uint8_t* y_q, const float* y_
 }
 
 int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
-                const void* W1, const void* W2, void* out, void* ws, size_t ws_bytes,
-                void* stream) {
-  return forward_impl(cfg, x, W_g, bias, W1, W2, out, ws, ws_bytes, nullptr, stream);
+                const float* noise, const void* W1, const void* W2, void* out, void* ws,
+                size_t ws_bytes, void* stream) {
+  return forward_impl(cfg, x, W_g, bias, noise, W1, W2, out, ws, ws_bytes, nullptr, stream);
 }
 
 int moe_forward_with_events(const moe_config_t* cfg, const void* x, const void* W_g,
-                            const float* bias, const void* W1, const void* W2, void* out,
-                            void* ws, size_t ws_bytes, void* const* events, int n_events,
-                            void* stream) {
+                            const float* bias, const float* noise, const void* W1, const void* W2,
+                            void* out, void* ws, size_t ws_bytes, void* const* events,
+                            int n_events, void* stream) {
   if (events != nullptr && n_events != MOE_NUM_EVENTS) return MOE_ERR_INVALID_ARG;
-  return forward_impl(cfg, x, W_g, bias, W1, W2, out, ws, ws_bytes, events, stream);
+  return forward_impl(cfg, x, W_g, bias, noise, W1, W2, out, ws, ws_bytes, events, stream);
 }
 
 int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* v) {
@@ -372,7 +393,7 @@ int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* v)
   v->offsets = at<int32_t>(ws, L.offsets);
   v->pos = at<int32_t>(ws, L.pos);
   v->src = at<int32_t>(ws, L.src);
-  v->x_perm = at<void>(ws, L.x_perm);
+  v->x_perm = soft(*cfg) ? nullptr : at<void>(ws, L.x_perm);
   v->x_scale = cfg->payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
   v->h = at<void>(ws, L.h);
   v->y_perm = at<float>(ws, L.y);
@@ -419,7 +440,8 @@ const char* moe_strerror(int status) {
 int moe_forward_kernel_count(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   if (cfg->T == 0) return 1;
-  return 1 + 3 + (cfg->payload_fp8 ? 1 : 0) + 2 + (cfg->output_fp8 ? 1 : 0) + 1;
+  const int dispatch = soft(*cfg) ? 1 : 3;  // dense layout, or count + scan + scatter
+  return 1 + dispatch + (cfg->payload_fp8 ? 1 : 0) + 2 + (cfg->output_fp8 ? 1 : 0) + 1;
 }
 
 }  // extern "C"

@@ -271,11 +271,13 @@ cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, co
   if (dtype == 0) {
     if (k <= 2) MOE_COMBINE8(0, 2);
     if (k <= 4) MOE_COMBINE8(0, 4);
-    MOE_COMBINE8(0, 8);
+    if (k <= 8) MOE_COMBINE8(0, 8);
+    MOE_COMBINE8(0, 16);
   }
   if (k <= 2) MOE_COMBINE8(1, 2);
   if (k <= 4) MOE_COMBINE8(1, 4);
-  MOE_COMBINE8(1, 8);
+  if (k <= 8) MOE_COMBINE8(1, 8);
+  MOE_COMBINE8(1, 16);
 #undef MOE_COMBINE8
 }
 

@@ -9,6 +9,8 @@
 //   group-limited: as renorm, over the experts of the topk_group groups with
 //                  the best mean probability (DeepSeek V3/V4 parallel-
 //                  strategy article, EP section: the node limit)
+//   soft gating:   w_e = softmax_e((L_e + g_e) / tau) over all E experts, g
+//                  the caller's Gumbel samples (sync-tax article, 3.3)
 // The logits never go to HBM unless the caller asks for them.
 //
 // Two gate GEMM shapes:
@@ -129,6 +131,10 @@ __global__ void __launch_bounds__(128) route_narrow_kernel(
     }
     float v[1] = {mine};
     int id[1] = {lane < E ? lane : 0x7fffffff};
+    if (rs.mode == topk::kRouterSoft) {
+      topk::warp_soft_weigh<1>(v, id, E, rs, t, topk_idx, topk_w);
+      continue;
+    }
     if (rs.mode == topk::kRouterGroup) topk::warp_group_limit<1>(v, id, E, rs);
     warp_select_and_weigh<1>(v, id, rs, t, topk_idx, topk_w);
   }
@@ -330,6 +336,10 @@ __global__ void __launch_bounds__(256) route_tiled_kernel(
       const int e = lane + 32 * j;
       v[j] = (e < EP) ? Ls[r * EP + e] : -INFINITY;
       id[j] = (e < E) ? e : 0x7fffffff;
+    }
+    if (rs.mode == topk::kRouterSoft) {
+      topk::warp_soft_weigh<NJ>(v, id, E, rs, t, topk_idx, topk_w);
+      continue;
     }
     if (rs.mode == topk::kRouterGroup) topk::warp_group_limit<NJ>(v, id, E, rs);
     warp_select_and_weigh<NJ>(v, id, rs, t, topk_idx, topk_w);

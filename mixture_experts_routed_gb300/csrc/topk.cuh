@@ -4,8 +4,9 @@
 // max-subtracted exponentials of the chosen logits. The group-limited mode
 // first drops every expert outside the topk_group groups with the best mean
 // probability (the node limit of the DeepSeek V3/V4 parallel-strategy
-// article, EP section). Two forms: one warp per token (SIMT gate kernels)
-// and one thread per token (tensor-core gate).
+// article, EP section). Soft gating weights every expert instead. Two
+// forms: one warp per token (SIMT gate kernels) and one thread per token
+// (tensor-core gate).
 #pragma once
 
 #include <cfloat>
@@ -19,6 +20,7 @@ namespace topk {
 constexpr int kRouterRenorm = 0;
 constexpr int kRouterPrek = 1;
 constexpr int kRouterGroup = 2;
+constexpr int kRouterSoft = 3;
 
 // Ranking rule: a beats b if a has the larger value, or equal values and the
 // lower id (expert or group).
@@ -217,6 +219,59 @@ __device__ __forceinline__ void thread_select_and_weigh(const float* row, int E,
       topk_idx[static_cast<size_t>(t) * k + s] = si[s];
       topk_w[static_cast<size_t>(t) * k + s] = ex[s] / den;
     }
+  }
+}
+
+// Soft gating (Deepseek-MoE sync-tax article, section 3.3), warp form: lane
+// values v[j] for experts id[j] (padding: id >= E); z = (L + g) / tau with
+// the token's Gumbel samples g; w = exp(z - max z) / sum; slot j = expert j
+// of a [T, E] routing.
+template <int NJ>
+__device__ __forceinline__ void warp_soft_weigh(const float (&v)[NJ], const int (&id)[NJ], int E,
+                                                const RouterSpec& rs, int t,
+                                                int32_t* __restrict__ topk_idx,
+                                                float* __restrict__ topk_w) {
+  const float* g = rs.noise + static_cast<size_t>(t) * E;
+  float z[NJ];
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    z[j] = (id[j] < E) ? (v[j] + __ldg(g + id[j])) / rs.tau : -INFINITY;
+    m = fmaxf(m, z[j]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  float ex[NJ];
+  float den = 0.f;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    ex[j] = (id[j] < E) ? expf(z[j] - m) : 0.f;
+    den += ex[j];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) {
+    if (id[j] < E) {
+      topk_idx[static_cast<size_t>(t) * E + id[j]] = id[j];
+      topk_w[static_cast<size_t>(t) * E + id[j]] = ex[j] / den;
+    }
+  }
+}
+
+// Soft gating, thread form (one thread per token, logits row in shared
+// memory): the same arithmetic, with the sum in expert order.
+__device__ __forceinline__ void thread_soft_weigh(const float* row, int E, const RouterSpec& rs,
+                                                  int t, int32_t* __restrict__ topk_idx,
+                                                  float* __restrict__ topk_w) {
+  const float* g = rs.noise + static_cast<size_t>(t) * E;
+  float m = -INFINITY;
+  for (int e = 0; e < E; ++e) m = fmaxf(m, (row[e] + __ldg(g + e)) / rs.tau);
+  float den = 0.f;
+  for (int e = 0; e < E; ++e) den += expf((row[e] + __ldg(g + e)) / rs.tau - m);
+  for (int e = 0; e < E; ++e) {
+    topk_idx[static_cast<size_t>(t) * E + e] = e;
+    topk_w[static_cast<size_t>(t) * E + e] = expf((row[e] + __ldg(g + e)) / rs.tau - m) / den;
   }
 }
 

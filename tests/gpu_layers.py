@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from workloads import (CONFIGS, CONFIG_ORDER, VARIANTS, MoEConfig, ROUTER_PREK_SOFTMAX,
-                       ROUTER_GROUP_LIMITED)
+                       ROUTER_GROUP_LIMITED, ROUTER_SOFT_GUMBEL)
 
 # Small shapes that exercise ragged tails, partial tiles and degenerate cases.
 SMALL = {
@@ -134,6 +134,25 @@ SMALL = {
     "outfp8_fp8in_T200_d256_E8_k2_f256": MoEConfig(
         "outfp8_fp8in_T200_d256_E8_k2_f256", T=200, d=256, E=8, k=2, f=256, dtype="bf16",
         payload_fp8=1, output_fp8=1, outlier_rate=0.01, seed=52),
+    # soft gating (every token to every expert): narrow gate and a merged
+    # remainder-free pair GEMM (bf16, E = 8); fp32 (SIMT GEMM, tau 0.5); the
+    # tensor-core gate with 16 experts at T = 4100 (merged remainders of 4
+    # rows, 16-row combine); fp32 K-split tiled gate; FP8 expert outputs
+    "soft_E8_T300_d256_f256": MoEConfig(
+        "soft_E8_T300_d256_f256", T=300, d=256, E=8, k=8, f=256, dtype="bf16",
+        router=ROUTER_SOFT_GUMBEL, seed=53),
+    "soft_f32_E4_T64_d128_f128_tau05": MoEConfig(
+        "soft_f32_E4_T64_d128_f128_tau05", T=64, d=128, E=4, k=4, f=128, dtype="f32", pre_k=4,
+        router=ROUTER_SOFT_GUMBEL, tau=0.5, seed=54),
+    "soft_E16_T4100_d256_f128": MoEConfig(
+        "soft_E16_T4100_d256_f128", T=4100, d=256, E=16, k=16, f=128, dtype="bf16",
+        router=ROUTER_SOFT_GUMBEL, bias="normal", bias_var=1.0, seed=55),
+    "soft_f32_E16_T4100_d128_f128": MoEConfig(
+        "soft_f32_E16_T4100_d128_f128", T=4100, d=128, E=16, k=16, f=128, dtype="f32",
+        router=ROUTER_SOFT_GUMBEL, tau=2.0, seed=56),
+    "soft_outfp8_E16_T1000_d512_f256": MoEConfig(
+        "soft_outfp8_E16_T1000_d512_f256", T=1000, d=512, E=16, k=16, f=256, dtype="bf16",
+        router=ROUTER_SOFT_GUMBEL, output_fp8=1, seed=57),
     "group_f32_E16_T4100_d128_k3_f128_g4top2": MoEConfig(
         "group_f32_E16_T4100_d128_k3_f128_g4top2", T=4100, d=128, E=16, k=3, f=128,
         dtype="f32", router=ROUTER_GROUP_LIMITED, n_group=4, topk_group=2, seed=46),
@@ -166,7 +185,8 @@ def make(cfg):
 def oracle_route(name: str):
     cfg, inp, host = layer(name)
     L = oracle.gate_logits(host["x"], host["Wg"], host["bias"])
-    idx, w = oracle.route(L, cfg.k, cfg.router, cfg.pre_k, cfg.n_group, cfg.topk_group)
+    idx, w = oracle.route(L, cfg.k, cfg.router, cfg.pre_k, cfg.n_group, cfg.topk_group,
+                          host.get("gumbel"), cfg.tau)
     return L, idx, w
 
 

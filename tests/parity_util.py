@@ -109,6 +109,8 @@ def near_tie_tokens_group(L64: np.ndarray, cfg) -> np.ndarray:
 
 def route_ties(cfg, L64: np.ndarray) -> np.ndarray:
     """Tokens whose routing fp32 cannot decide reliably, for any router."""
+    if getattr(cfg, "router", 0) == 3:     # soft gating selects nothing
+        return np.zeros(L64.shape[0], dtype=bool)
     if getattr(cfg, "router", 0) == ROUTER_GROUP_LIMITED:
         return near_tie_tokens_group(L64, cfg)
     return near_tie_tokens(L64, cfg.k)

@@ -54,7 +54,7 @@ def test_only_abi_symbols_are_exported(lib):
 
 def cfg(**kw):
     base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0,
-                n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0)
+                n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0, tau=0.0)
     base.update(kw)
     return L.MoeConfig(*[base[n] for n, _ in L.MoeConfig._fields_])
 
@@ -77,7 +77,6 @@ def cfg(**kw):
     (dict(k=3, pre_k=2), L.MOE_ERR_INVALID_ARG),
     (dict(E=4, k=2, pre_k=8), L.MOE_ERR_INVALID_ARG),
     (dict(dtype=2), L.MOE_ERR_INVALID_ARG),
-    (dict(router=3), L.MOE_ERR_INVALID_ARG),
     # group-limited router: n_group | E, 1 <= topk_group <= n_group <= 32,
     # k <= topk_group * E / n_group; the other routers ignore both fields
     (dict(router=2, n_group=4, topk_group=2), L.MOE_OK),
@@ -103,6 +102,16 @@ def cfg(**kw):
     (dict(output_fp8=1, dtype=0), L.MOE_OK),
     (dict(output_fp8=2), L.MOE_ERR_INVALID_ARG),
     (dict(output_fp8=-1), L.MOE_ERR_INVALID_ARG),
+    # soft gating: k = E <= 16, tau finite and > 0, no FP8 payload
+    (dict(router=3, E=8, k=8, tau=1.0), L.MOE_OK),
+    (dict(router=3, E=16, k=16, tau=0.5, output_fp8=1), L.MOE_OK),
+    (dict(router=3, E=16, k=16, tau=0.5, dtype=0), L.MOE_OK),
+    (dict(router=3, E=8, k=2, tau=1.0), L.MOE_ERR_INVALID_ARG),
+    (dict(router=3, E=32, k=32, tau=1.0), L.MOE_ERR_INVALID_ARG),
+    (dict(router=3, E=8, k=8, tau=0.0), L.MOE_ERR_INVALID_ARG),
+    (dict(router=3, E=8, k=8, tau=float("nan")), L.MOE_ERR_INVALID_ARG),
+    (dict(router=3, E=8, k=8, tau=1.0, payload_fp8=1), L.MOE_ERR_UNSUPPORTED),
+    (dict(router=4), L.MOE_ERR_INVALID_ARG),
     (dict(payload_fp8=1, dtype=0), L.MOE_ERR_UNSUPPORTED),
     (dict(T=1 << 30, k=8), L.MOE_ERR_UNSUPPORTED),
 ])
@@ -140,6 +149,15 @@ def test_workspace_sizes(lib):
     assert lib.moe_workspace_size(ctypes.byref(co)) >= ws + R * 4096 + R * 8
     assert lib.moe_scratch_size(ctypes.byref(co)) == sc
     assert lib.moe_forward_kernel_count(ctypes.byref(co)) == 8
+    # soft gating packs no rows (the W1 GEMM reads x): the forward workspace
+    # is R*d*2 bytes smaller than a top-k layer with the same fan-out; one
+    # layout kernel instead of the three dispatch kernels
+    cs = cfg(T=1024, d=4096, E=8, k=8, f=11008, router=3, tau=1.0)
+    ck = cfg(T=1024, d=4096, E=8, k=8, f=11008)
+    Rs = 1024 * 8
+    assert lib.moe_workspace_size(ctypes.byref(ck)) - lib.moe_workspace_size(ctypes.byref(cs)) \
+        >= Rs * 4096 * 2
+    assert lib.moe_forward_kernel_count(ctypes.byref(cs)) == 5
 
 
 FAKE = ctypes.c_void_p(0x100000)       # never dereferenced: validation fails first
@@ -150,27 +168,32 @@ def test_forward_argument_errors(lib):
     c = cfg()
     n = lib.moe_workspace_size(ctypes.byref(c))
     f = lib.moe_forward
-    assert f(None, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
-    assert f(ctypes.byref(c), None, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
-    assert f(ctypes.byref(c), FAKE_ODD, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
-    assert f(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE_ODD, n, None) == L.MOE_ERR_INVALID_ARG
-    assert f(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, n - 1, None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert f(None, FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), None, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE_ODD, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE_ODD, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(c), FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, n - 1, None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    soft = cfg(router=3, E=8, k=8, tau=1.0)
+    ns = lib.moe_workspace_size(ctypes.byref(soft))
+    # the soft router needs its Gumbel samples
+    assert f(ctypes.byref(soft), FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, ns, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(ctypes.byref(soft), FAKE, FAKE, None, None, FAKE, FAKE, None, None) == L.MOE_ERR_INVALID_ARG
     bad = cfg(d=96)
-    assert f(ctypes.byref(bad), FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(bad), FAKE, FAKE, None, None, FAKE, FAKE, FAKE, FAKE, n, None) == L.MOE_ERR_INVALID_ARG
 
 
 def test_forward_with_events_wrong_count(lib):
     c = cfg()
     n = lib.moe_workspace_size(ctypes.byref(c))
     ev = (ctypes.c_void_p * 3)()
-    assert lib.moe_forward_with_events(ctypes.byref(c), FAKE, FAKE, None, FAKE, FAKE, FAKE,
+    assert lib.moe_forward_with_events(ctypes.byref(c), FAKE, FAKE, None, None, FAKE, FAKE, FAKE,
                                        FAKE, n, ev, 3, None) == L.MOE_ERR_INVALID_ARG
 
 
 def test_stage_argument_errors(lib):
     c = cfg()
     sc = lib.moe_scratch_size(ctypes.byref(c))
-    assert lib.moe_route(ctypes.byref(c), None, FAKE, None, FAKE, FAKE, None, None) == L.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(ctypes.byref(c), None, FAKE, None, None, FAKE, FAKE, None, None) == L.MOE_ERR_INVALID_ARG
     assert lib.moe_dispatch(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
                             FAKE, sc - 1, None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
     assert lib.moe_dispatch(ctypes.byref(c), FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None,
@@ -190,7 +213,7 @@ def test_stage_argument_errors(lib):
                                None) == L.MOE_ERR_INVALID_ARG
     # an empty batch needs no device work for routing
     c0 = cfg(T=0)
-    assert lib.moe_route(ctypes.byref(c0), None, None, None, None, None, None, None) == L.MOE_OK
+    assert lib.moe_route(ctypes.byref(c0), None, None, None, None, None, None, None, None) == L.MOE_OK
 
 
 def test_strerror(lib):

@@ -18,12 +18,13 @@ NAMES = SMALL_NAMES + FULL_NAMES + VARIANT_NAMES
 @pytest.mark.parametrize("name", NAMES)
 def test_route_parity(cuda_ok, name):
     cfg, inp, host = layer(name)
-    idx, w, logits = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"], want_logits=True)
+    idx, w, logits = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"], noise=inp.get("gumbel"),
+                               want_logits=True)
     torch.cuda.synchronize()
     L, idx_o, w_o = oracle_route(name)
     n_tie = check_route(cfg, L, idx_o, w_o, to_np(logits), to_np(idx), to_np(w))
     print(f"{name}: near-tie tokens {n_tie}")
-    if cfg.router in (0, 2):      # renormalised weights
+    if cfg.router in (0, 2, 3):   # weights that sum to one
         assert np.all(np.abs(to_np(w).sum(1) - 1.0) <= 1e-6)
 
 
@@ -32,8 +33,8 @@ def test_route_without_bias_pointer_equals_zero_bias(cuda_ok, name):
     cfg, inp, _ = layer(name)
     if cfg.bias != "zero":
         pytest.skip("shape has a bias")
-    a = moe.route(cfg, inp["x"], inp["Wg"], None)
-    b = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"])
+    a = moe.route(cfg, inp["x"], inp["Wg"], None, noise=inp.get("gumbel"))
+    b = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"], noise=inp.get("gumbel"))
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
@@ -53,7 +54,9 @@ def test_dispatch_parity(cuda_ok, name):
     assert np.array_equal(to_np(d["src"]), src)
     R = cfg.R
     rows = np.arange(R) if R <= 300000 else np.random.default_rng(0).choice(R, 8192, replace=False)
-    if not cfg.payload_fp8:
+    if cfg.router == 3:
+        assert d["x_perm"] is None      # soft gating packs no rows
+    elif not cfg.payload_fp8:
         # packed row r is the bytes of token src[r]
         got = bits(d["x_perm"][torch.from_numpy(rows).cuda()])
         ref = bits(inp["x"][torch.from_numpy(src[rows]).cuda()])

@@ -18,6 +18,9 @@ NAMES = SMALL_NAMES + FULL_NAMES
 def _ffn_inputs(cfg, inp, host, src, name):
     """Packed rows in the oracle's order, and the fp64 rows the experts see."""
     src_t = torch.from_numpy(src.astype(np.int64)).cuda()
+    if cfg.router == 3:
+        # soft gating: every expert reads x itself
+        return inp["x"], None, host["x"]
     if cfg.payload_fp8:
         q, s = oracle_payload(name)
         payload = torch.from_numpy(oracle.e4m3_encode(q[src])).cuda()

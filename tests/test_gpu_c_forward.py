@@ -20,7 +20,8 @@ SAMPLED_TOKENS.update({n: 16 for n in VARIANT_NAMES})
 
 def _run(cfg, inp, ws=None):
     ws = moe.alloc_workspace(cfg) if ws is None else ws
-    out = moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws)
+    out = moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
+                      noise=inp.get("gumbel"))
     torch.cuda.synchronize()
     return out, ws
 
@@ -73,14 +74,16 @@ def test_forward_parity(cuda_ok, name):
 
 @pytest.mark.parametrize("name", [SMALL_NAMES[0], SMALL_NAMES[6], FULL_NAMES[0], FULL_NAMES[1],
                                   "outfp8_fp8in_T200_d256_E8_k2_f256",
-                                  "outfp8_f32_T64_d128_E4_k3_f128"])
+                                  "outfp8_f32_T64_d128_E4_k3_f128", "soft_E16_T4100_d256_f128",
+                                  "soft_f32_E4_T64_d128_f128_tau05"])
 def test_stage_calls_compose_to_forward(cuda_ok, name):
     cfg, inp, _ = layer(name)
     out_f, ws = _run(cfg, inp)
     sc = moe.alloc_workspace(cfg, kind="scratch")
-    idx, w, _ = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"])
+    idx, w, _ = moe.route(cfg, inp["x"], inp["Wg"], inp["bias"], noise=inp.get("gumbel"))
     d = moe.dispatch(cfg, inp["x"], idx, ws=sc)
-    h, y = moe.expert_ffn(cfg, d["x_perm"], d["x_scale"], d["offsets"], inp["W1"], inp["W2"], ws=sc)
+    a = inp["x"] if cfg.router == 3 else d["x_perm"]      # soft gating reads x itself
+    h, y = moe.expert_ffn(cfg, a, d["x_scale"], d["offsets"], inp["W1"], inp["W2"], ws=sc)
     if cfg.output_fp8:
         yq, ys, yz = moe.quantize_output(cfg, y)
         out_s = moe.combine_fp8(cfg, yq, ys, yz, d["pos"], w, ws=sc)
@@ -106,7 +109,8 @@ def test_forward_is_bitwise_reproducible(cuda_ok, name):
 
 # captured layers: the balanced one (narrow router, merged remainders), the
 # E = 64 one (tensor-core gate, pre-k router) and a small FP8 one
-GRAPH_NAMES = [FULL_NAMES[1], "gate_E16_T4100_d256_k2_f128", "fp8_T64_d256_E4_k2_f256"]
+GRAPH_NAMES = [FULL_NAMES[1], "gate_E16_T4100_d256_k2_f128", "fp8_T64_d256_E4_k2_f256",
+               "soft_E8_T300_d256_f256"]
 
 
 @pytest.mark.parametrize("name", GRAPH_NAMES)
@@ -120,7 +124,7 @@ def test_forward_in_cuda_graph(cuda_ok, name):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         moe.forward(cfg, x, inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws, out=out,
-                    stream=s)
+                    noise=inp.get("gumbel"), stream=s)
     out.zero_()
     g.replay()
     torch.cuda.synchronize()
@@ -133,7 +137,7 @@ def test_forward_in_cuda_graph(cuda_ok, name):
         g.replay()
         torch.cuda.synchronize()
         ref = moe.forward(cfg, x2, inp["Wg"], inp["bias"], inp["W1"], inp["W2"],
-                          ws=moe.alloc_workspace(cfg))
+                          ws=moe.alloc_workspace(cfg), noise=inp.get("gumbel"))
         torch.cuda.synchronize()
         assert torch.equal(out, ref)
     assert moe.get_device_error(ws) == moe.MOE_OK

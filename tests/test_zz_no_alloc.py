@@ -58,8 +58,9 @@ def _routing(lib, c, inp):
     cc = _cfg(c)
     idx = torch.empty((c.T, c.k), dtype=torch.int32, device="cuda")
     w = torch.empty((c.T, c.k), dtype=torch.float32, device="cuda")
-    st = lib.moe_route(ctypes.byref(cc), _p(inp["x"]), _p(inp["Wg"]), _p(inp["bias"]), _p(idx),
-                       _p(w), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    st = lib.moe_route(ctypes.byref(cc), _p(inp["x"]), _p(inp["Wg"]), _p(inp["bias"]), None,
+                       _p(idx), _p(w), None,
+                       ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == L.MOE_OK
     return idx
 

@@ -112,7 +112,12 @@ CONFIG_ORDER = list(CONFIGS)
 # FP8 expert outputs: the wide layer with both FP8 payloads of the sync-tax
 # article (section 3.1), per-token absmax on the expert inputs and per-row
 # min/max affine on the expert outputs.
+# Soft gating (sync-tax article, section 3.3): the wide layer's 16 experts,
+# every token weighted over all of them by a Gumbel-softmax at tau = 1.
 VARIANTS = {
+    "soft_gumbel_T16384_d5120_E16_f1536": MoEConfig(
+        "soft_gumbel_T16384_d5120_E16_f1536", T=32 * 512, d=5120, E=16, k=16, f=1536,
+        dtype="bf16", router=ROUTER_SOFT_GUMBEL, tau=1.0, seed=3),
     "wide_fp8_T16384_d5120_E16_k2_f1536_outfp8": MoEConfig(
         "wide_fp8_T16384_d5120_E16_k2_f1536_outfp8", T=32 * 512, d=5120, E=16, k=2,
         f=1536, dtype="bf16", payload_fp8=1, output_fp8=1, outlier_rate=1e-3,
