@@ -32,9 +32,11 @@
 // (one thread, both CTAs); warp 1 TMEM allocation (both CTAs) and MMA issue
 // (even CTA); warps 2.. epilogue, 8 for the SiLU pass (two per TMEM lane
 // quadrant, each half the columns) and 4 for the fp32 pass (tcgen05.ld 32
-// columns at a time, FP8 row scale and SiLU or fp32 store, rows past the
-// segment masked). Every wait is bounded; a timeout sets kErrTimeout and the
-// kernel drains its copies and MMAs, frees TMEM and exits.
+// columns at a time, FP8 row scale and SiLU, then a 32 x 32 block staged in
+// shared memory and written by one TMA store; rows of a swapped or merged
+// remainder are stored by the threads, rows past the segment masked). Every
+// wait is bounded; a timeout sets kErrTimeout and the kernel drains its
+// copies and MMAs, frees TMEM and exits.
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -147,6 +149,25 @@ struct Shape {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
+// Output staging: each epilogue warp puts a block of its 32 rows x 32
+// columns in shared memory past the ring (fp32: 128-byte rows, 128-byte
+// swizzle; bf16: 64-byte rows, 64-byte swizzle; 1024-byte aligned) and
+// writes it with one TMA store: whole row segments instead of 16-byte pieces
+// of 32 different rows per store instruction.
+template <int EPI>
+__host__ __device__ constexpr int stg_bytes() { return EPI == 1 ? 32 * 32 * 4 : 32 * 32 * 2; }
+template <int NB>
+__host__ __device__ constexpr int off_stg() {
+  return (Shape<NB>::SMEM_USED + 1023) & ~1023;
+}
+template <int EPI, int NB>
+__host__ __device__ constexpr int smem_bytes() {
+  return off_stg<NB>() + num_epi_warps<EPI>() * stg_bytes<EPI>() + 1024;
+}
+static_assert(smem_bytes<0, 1>() <= 227 * 1024 && smem_bytes<0, 2>() <= 227 * 1024 &&
+                  smem_bytes<1, 1>() <= 227 * 1024 && smem_bytes<1, 2>() <= 227 * 1024,
+              "shared memory");
+
 struct PTile {
   int e, row0, ntok, n0;  // token rows [row0, row0 + ntok), features from n0
   bool swap;              // tail tile: weights are the MMA's M side, tokens its N
@@ -221,7 +242,8 @@ template <int EPI, int NB>
 __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmA8,
-                     const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmY, const TcParams p) {
   using S = pairk::Shape<NB>;
   constexpr int NEW = pairk::num_epi_warps<EPI>();
   constexpr int NH = NEW / 4;  // warps per TMEM lane quadrant
@@ -532,6 +554,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     const int q = warp & 3;
     const int hh = (warp - 2) >> 2;
     const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    uint8_t* stg = smem + pairk::off_stg<NB>() + (warp - 2) * pairk::stg_bytes<EPI>();
     int acc = 0;
     uint32_t aph = 0;
     for (;;) {
@@ -552,6 +575,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         const int r = static_cast<int>(rank) * 128 + q * 32 + lane;
         const bool valid = r < t.ntok && t.row0 + r < p.R;
         const size_t grow = static_cast<size_t>(t.row0) + r;
+        // a warp whose 32 rows all belong to the tile (always, in a full or
+        // merged tile) stores through its staging block
+        const bool tma_rows = __all_sync(0xffffffffu, valid);
+        const int wrow0 = t.row0 + static_cast<int>(rank) * 128 + q * 32;
         float scale = 1.f;
         if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
         const int nch = t.width / 32, per = (nch + NH - 1) / NH;
@@ -563,6 +590,23 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, v);
           tmem_ld_wait();
+          if (EPI == 1 && tma_rows) {
+            // the previous store of this block has read it out
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+            uint8_t* row_p = stg + lane * 128;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(row_p + ((i ^ (lane & 7)) << 4)) =
+                  make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmY, smem_u32(stg), col, wrow0);
+              bulk_commit_group();
+            }
+            continue;
+          }
           if (!valid) continue;
           if constexpr (EPI == 0) {
             uint32_t packed[16];
@@ -572,6 +616,23 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
               const float b = silu(__uint_as_float(v[2 * i + 1]) * scale);
               const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
               packed[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            if (tma_rows) {
+              if (lane == 0) bulk_wait_group_read0();
+              __syncwarp();
+              uint8_t* row_p = stg + lane * 64;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(row_p + ((i ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                               packed[4 * i + 3]);
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmY, smem_u32(stg), col, wrow0);
+                bulk_commit_group();
+              }
+              continue;
             }
             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
                                                   grow * p.N + col);
@@ -670,6 +731,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         aph ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's TMA stores are done
   }
 
   if (timed_out) atomicOr(p.err, kErrTimeout);
@@ -714,6 +776,23 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the row-major [rows, cols] output, box [32 rows][32 cols]:
+// fp32 (128-byte rows, 128-byte swizzle) for the fp32 pass, bf16 (64-byte
+// rows, 64-byte swizzle) for the SiLU pass, matching the staging blocks.
+bool make_map_2d_out(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols, bool f32) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * (f32 ? 4 : 2)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int EPI, int NB>
 cudaError_t set_pair_smem_attr() {
   static std::once_flag once;
@@ -721,7 +800,7 @@ cudaError_t set_pair_smem_attr() {
   std::call_once(once, [] {
     st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              pairk::Shape<NB>::SMEM_BYTES);
+                              pairk::smem_bytes<EPI, NB>());
   });
   return st;
 }
@@ -747,7 +826,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
 
 template <int EPI, int NB>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUtensorMap& mB,
-                        TcParams prm, int num_sms,
+                        const CUtensorMap& mY, TcParams prm, int num_sms,
                         cudaStream_t s) {
   using S = pairk::Shape<NB>;
   prm.n_tiles = ceil_div(prm.N, S::BN);
@@ -757,7 +836,7 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
       static_cast<long long>(prm.n_tiles > prm.n_tiles_m ? prm.n_tiles : prm.n_tiles_m);
   cudaLaunchConfig_t lc = {};
   lc.blockDim = dim3(pairk::num_threads<EPI>());
-  lc.dynamicSmemBytes = S::SMEM_BYTES;
+  lc.dynamicSmemBytes = pairk::smem_bytes<EPI, NB>();
   lc.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -775,7 +854,7 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
   const int resident = resident_pairs<EPI, NB>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB>, mA, mA8, mB, prm);
+  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB>, mA, mA8, mB, mY, prm);
 }
 
 // 512-feature tiles (one accumulator, epilogue exposed) pay off only for the
@@ -796,7 +875,8 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int
                            cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   if (num_sms < 2) return cudaErrorInvalidValue;
-  CUtensorMap mA, mA8, mB;
+  CUtensorMap mA, mA8, mB, mY;
+  std::memset(&mY, 0, sizeof(mY));
   std::memset(&mA, 0, sizeof(mA));
   std::memset(&mA8, 0, sizeof(mA8));
   std::memset(&mB, 0, sizeof(mB));
@@ -809,6 +889,9 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int
     return cudaErrorInvalidValue;
   if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64,
                    pairk::BK))
+    return cudaErrorInvalidValue;
+  // both passes write their full tiles' output rows through TMA stores
+  if (!make_map_2d_out(&mY, out, static_cast<uint64_t>(R), static_cast<uint64_t>(N), epi == 1))
     return cudaErrorInvalidValue;
   TcParams prm;
   prm.offsets = offsets;
@@ -830,10 +913,10 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int
     if (std::strcmp(f, "512") == 0) nb = 2;
   }
   if (epi == 0)
-    return nb == 2 ? launch_pair<0, 2>(mA, mA8, mB, prm, num_sms, s)
-                   : launch_pair<0, 1>(mA, mA8, mB, prm, num_sms, s);
-  return nb == 2 ? launch_pair<1, 2>(mA, mA8, mB, prm, num_sms, s)
-                 : launch_pair<1, 1>(mA, mA8, mB, prm, num_sms, s);
+    return nb == 2 ? launch_pair<0, 2>(mA, mA8, mB, mY, prm, num_sms, s)
+                   : launch_pair<0, 1>(mA, mA8, mB, mY, prm, num_sms, s);
+  return nb == 2 ? launch_pair<1, 2>(mA, mA8, mB, mY, prm, num_sms, s)
+                 : launch_pair<1, 1>(mA, mA8, mB, mY, prm, num_sms, s);
 }
 
 }  // namespace moe
