@@ -124,8 +124,8 @@ MOE_API int moe_check_config(const moe_config_t* cfg);
 
 /* ---- workspace ----------------------------------------------------------
  * moe_scratch_size: bytes of workspace that moe_dispatch, moe_expert_ffn and
- *   moe_combine need (an error word, dispatch per-block tables and, with the
- *   FP8 payload, a bf16 staging copy of the rows for the tensor cores).
+ *   moe_combine need (an error word, the GEMM tile counters and the dispatch
+ *   per-block tables).
  * moe_workspace_size: bytes moe_forward needs: the scratch above followed by
  *   every intermediate of the layer (routing, permutation, payload, H, Y).
  *   A forward workspace therefore also serves the stage calls.
@@ -204,7 +204,9 @@ MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
  * rows past offsets[E] are not touched), W1 [E, d, f] and W2 [E, f, d]
  * (dtype, expert-major), h [R, f] (dtype) output, y_perm [R, d] fp32 output.
  * bf16 uses the tcgen05 tensor cores (fp32 accumulate in TMEM); fp32 uses
- * fp32 FMA. Experts with no rows read none of their weights.
+ * fp32 FMA. With the FP8 payload the GEMM reads the E4M3 bytes and expands
+ * them to bf16 in shared memory (exact), applying s_r in its epilogue.
+ * Experts with no rows read none of their weights.
  * MOE_ROUTER_SOFT_GUMBEL: x_perm is x itself, [T, d]; row r of expert e's
  * segment reads x[r - offsets[e]] (every expert reads all T rows).
  * ws: >= moe_scratch_size bytes. */
@@ -259,8 +261,9 @@ MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g,
  * at the kernel boundaries, for per-kernel timing on the launching stream:
  *   events[0] before the route kernel      events[1] after route
  *   events[2] after dispatch (3 kernels; 1 with soft gating)
- *                                          events[3] after the FP8 row
- *   conversion (= events[2] without FP8)   events[4] after the W1 GEMM
+ *                                          events[3] = events[2] (kept for
+ *   the slot; the FP8 payload is expanded  events[4] after the W1 GEMM
+ *   inside the W1 GEMM)
  *   events[5] after the W2 GEMM            events[6] after the output
  *   quantisation (= events[5] without)     events[7] after combine
  * n_events must be MOE_NUM_EVENTS; any entry may be NULL (not recorded). */

@@ -115,8 +115,6 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, cons
 // offsets, pos, src; zeroes `nzero` words at `zero` when non-null.
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,
                                 int32_t* src, uint32_t* zero, int nzero, cudaStream_t s);
-// E4M3 payload bytes -> bf16 (exact), for the tensor-core A operand.
-cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s);
 
 // ---------------------------------------------------------------- combine.cu
 cudaError_t launch_combine(int dtype, const float* y, const int32_t* pos, const float* w, int T,
@@ -135,12 +133,14 @@ cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, co
 // Grouped GEMM over expert segments on tcgen05: out[r] = epi(A[a(r)] . W[e])
 // for the rows r of expert e's segment [offsets[e], offsets[e+1]); a(r) = r,
 // or r - offsets[e] when a_shared (every expert reads the same a_rows rows of
-// A). A [a_rows, K] bf16, W [E, K, N] bf16. epi 0: (row scale) -> SiLU ->
-// bf16 out; epi 1: fp32 out. `tile_ctr` must be zero at launch.
-cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int R, const void* W,
-                           int E, int K, int N, const int32_t* offsets, const float* row_scale,
-                           void* out, uint32_t* err, uint32_t* tile_ctr, int num_sms,
-                           cudaStream_t s);
+// A). A [a_rows, K] bf16, or E4M3 bytes when a_fp8 (epi 0 only: expanded to
+// bf16 in shared memory, the row scale applied in the epilogue); W [E, K, N]
+// bf16. epi 0: (row scale) -> SiLU -> bf16 out; epi 1: fp32 out.
+// `tile_ctr` must be zero at launch.
+cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
+                           const void* W, int E, int K, int N, const int32_t* offsets,
+                           const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
+                           int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm_simt.cu
 // The same grouped GEMM in fp32 FMA for fp32 layers.

@@ -302,31 +302,6 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
   }
 }
 
-__global__ void fp8_to_bf16_kernel(const uint8_t* __restrict__ q, size_t n16,
-                                   __nv_bfloat16* __restrict__ out) {
-  pdl_wait();
-  pdl_trigger();
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(q) + i);
-    const uint8_t* b = reinterpret_cast<const uint8_t*>(&raw);
-    uint32_t o[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      const __nv_fp8x2_storage_t pair =
-          static_cast<__nv_fp8x2_storage_t>(b[2 * p] | (static_cast<uint16_t>(b[2 * p + 1]) << 8));
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-      const __half2 h2 = *reinterpret_cast<const __half2*>(&hr);
-      const float2 f2 = __half22float2(h2);
-      const __nv_bfloat162 bb = __floats2bfloat162_rn(f2.x, f2.y);  // exact: E4M3 fits in bf16
-      o[p] = *reinterpret_cast<const uint32_t*>(&bb);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(out) + 2 * i;
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-  }
-}
-
 // Soft gating sends every token to every expert in token order: the layout
 // is known without counting. counts[e] = T, offsets[e] = e T, pos[t E + e] =
 // e T + t, src[e T + t] = t; also zeroes `nzero` words at `zero` (the GEMM
@@ -389,14 +364,6 @@ cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets,
   const int blocks = static_cast<int>((R + 255) / 256) > 0 ? static_cast<int>((R + 255) / 256) : 1;
   return launch_pdl(dense_layout_kernel, dim3(blocks), dim3(256), 0, s, T, E, counts, offsets,
                     pos, src, zero, nzero);
-}
-
-cudaError_t launch_fp8_to_bf16(const uint8_t* q, size_t n, void* out_bf16, cudaStream_t s) {
-  const size_t n16 = n / 16;
-  if (n16 == 0) return cudaSuccess;
-  int blocks = static_cast<int>(min(n16 / 256 + 1, static_cast<size_t>(152 * 8)));
-  return launch_pdl(fp8_to_bf16_kernel, dim3(blocks), dim3(256), 0, s, q, n16,
-                    static_cast<__nv_bfloat16*>(out_bf16));
 }
 
 }  // namespace moe

@@ -37,6 +37,15 @@
 // remainder are stored by the threads, rows past the segment masked). Every
 // wait is bounded; a timeout sets kErrTimeout and the kernel drains its
 // copies and MMAs, frees TMEM and exits.
+//
+// FP8 token rows (the dispatch's E4M3 payload, W1 pass): the producer loads
+// each CTA's 128 rows x 64 E4M3 bytes into the first half of the stage's
+// token slot; 8 converter warps (two groups of 4 on alternate stages) expand
+// them in place to the bf16 layout the MMA reads (exact) and release the
+// stage: the even CTA's warps by an arrive, the odd CTA's by 16-byte bulk
+// copies whose bytes complete the even CTA's full barrier. The per-row
+// payload scale is applied in the epilogue. This is the GEMM's dequantising
+// prologue; no bf16 copy of the payload is written to memory.
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -45,6 +54,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -100,8 +111,16 @@ constexpr int TMEM_COLS = 512;
 // store bursts against the operand loads, measured slower on GB300).
 template <int EPI>
 __host__ __device__ constexpr int num_epi_warps() { return EPI == 0 ? 8 : 4; }
-template <int EPI>
-__host__ __device__ constexpr int num_threads() { return 64 + 32 * num_epi_warps<EPI>(); }
+// FP8 token rows (A8): 8 more warps expand the staged E4M3 tiles to bf16,
+// two groups of 4 taking alternate stages (one group's chain per stage, ~720
+// cycles measured, is longer than the MMA's k-block).
+constexpr int CONV_GROUP = 4;
+template <bool A8>
+__host__ __device__ constexpr int num_conv_warps() { return A8 ? 2 * CONV_GROUP : 0; }
+template <int EPI, bool A8 = false>
+__host__ __device__ constexpr int num_threads() {
+  return 64 + 32 * (num_epi_warps<EPI>() + num_conv_warps<A8>());
+}
 constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*B MN-major*/ true);
 
 // Merged tiles (256-feature shape only). An expert whose rows end in a short
@@ -138,13 +157,15 @@ struct Shape {
   static constexpr int OFF_T = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
   static constexpr int TQ = 8;  // tile queue slots
-  // full, empty, tfull, tempty, drain, tq_full, tq_empty
-  static constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1 + 2 * TQ;
+  // full, empty, tfull, tempty, drain, tq_full, tq_empty, a8_full
+  static constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1 + 2 * TQ;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_TQ = OFF_MISC + 16;
   static constexpr int OFF_SEG = OFF_TQ + TQ * 4;
   static constexpr int OFF_TSTART = OFF_SEG + (kMaxExperts + 1) * 4;
-  static constexpr int SMEM_USED = OFF_TSTART + (kMaxExperts + 1) * 4;
+  // 16 bytes that the odd CTA's FP8 converters copy to the even CTA (A8)
+  static constexpr int OFF_SINK = (OFF_TSTART + (kMaxExperts + 1) * 4 + 15) & ~15;
+  static constexpr int SMEM_USED = OFF_SINK + 16;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -238,8 +259,8 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
 }
 }  // namespace pairk
 
-template <int EPI, int NB>
-__global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
+template <int EPI, int NB, bool A8>
+__global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmA8,
                      const __grid_constant__ CUtensorMap tmB,
@@ -247,12 +268,16 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
   using S = pairk::Shape<NB>;
   constexpr int NEW = pairk::num_epi_warps<EPI>();
   constexpr int NH = NEW / 4;  // warps per TMEM lane quadrant
+  constexpr int NCV = pairk::num_conv_warps<A8>();
+  // FP8 token rows come without merged remainder tiles (a remainder is a
+  // swapped tile, its rows expanded like any other)
+  constexpr bool MERGE = S::MERGE && !A8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem + S::OFF_A;
   uint8_t* sB = smem + S::OFF_B;
-  uint8_t* sT = smem + S::OFF_T;  // merged tiles' remainder rows (S::MERGE)
+  uint8_t* sT = smem + S::OFF_T;  // merged tiles' remainder rows (MERGE)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
   uint64_t* empty = full + S::STAGES;
   uint64_t* tfull = empty + S::STAGES;
@@ -260,6 +285,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
   uint64_t* drain = tempty + S::NUM_ACC;
   uint64_t* tq_full = drain + 1;
   uint64_t* tq_empty = tq_full + S::TQ;
+  uint64_t* a8_full = tq_empty + S::TQ;  // A8: this CTA's E4M3 tile has landed
   int* tq = reinterpret_cast<int*>(smem + S::OFF_TQ);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::OFF_MISC);
   int* s_total = reinterpret_cast<int*>(smem + S::OFF_MISC + 4);
@@ -284,7 +310,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       if (e < E) {
         const int lo = seg[e], hi = seg[e + 1];
         bad = lo < 0 || hi < lo || hi > p.R;
-        tiles = bad ? 0 : pairk::expert_tiles(hi - lo, p.n_tiles, p.n_tiles_m, S::MERGE);
+        tiles = bad ? 0 : pairk::expert_tiles(hi - lo, p.n_tiles, p.n_tiles_m, MERGE);
       }
       if (__any_sync(0xffffffffu, bad)) ok = false;
       int incl = tiles;
@@ -301,8 +327,12 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       *s_total = ok ? running : 0;
       if (!ok && blockIdx.x == 0) atomicOr(p.err, kErrBadIndex);
       for (int i = 0; i < S::STAGES; ++i) {
-        mbar_init(&full[i], 1);
+        // A8: the producer's arrive and one arrive per warp of the even
+        // CTA's converter group for this stage; the odd CTA's converters
+        // signal through bytes (see the converters)
+        mbar_init(&full[i], A8 ? 1 + pairk::CONV_GROUP : 1);
         mbar_init(&empty[i], 1);
+        mbar_init(&a8_full[i], 1);
       }
       for (int i = 0; i < S::NUM_ACC; ++i) {
         mbar_init(&tfull[i], 1);
@@ -311,7 +341,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       mbar_init(drain, 1);
       for (int i = 0; i < S::TQ; ++i) {
         mbar_init(&tq_full[i], 1);
-        mbar_init(&tq_empty[i], 2 + 2 * NEW);
+        mbar_init(&tq_empty[i], 2 + 2 * NEW + 2 * NCV);
       }
       fence_mbar_init();
     }
@@ -359,7 +389,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       prefetch_tmap(&tmA);
-      prefetch_tmap(&tmA8);
+      if (!A8) prefetch_tmap(&tmA8);
       prefetch_tmap(&tmB);
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
@@ -392,7 +422,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           tile = next_tile(false);
         }
         if (tile >= total || timed_out) break;
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
         // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
         const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
         const int a_base = p.a_shared ? seg[t.e] : 0;
@@ -404,7 +434,9 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         const int half_w = t.tail > 0 ? pairk::MT_HALF : 128;
         auto boxes = [&](int n) { return n < p.N ? min(2, (p.N - n + 63) / 64) : 0; };
         int nbox[NB];
-        uint32_t bytes = 2 * pairk::A_BYTES;
+        // A8: the token rows land on this CTA's a8_full, not on full; the
+        // odd CTA's converter warps each send 16 bytes to full instead
+        uint32_t bytes = A8 ? static_cast<uint32_t>(16 * pairk::CONV_GROUP) : 2u * pairk::A_BYTES;
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
           nbox[j] = boxes(t.n0 + j * 256 + static_cast<int>(rank) * half_w);
@@ -424,14 +456,21 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           }
           if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
           const uint32_t bar = leader_full + static_cast<uint32_t>(s * 8);
-          tma_load_2d_pair(sA + s * pairk::A_BYTES, &tmA, bar, kb * pairk::BK, my_row);
+          if constexpr (A8) {
+            // 128 rows x 64 E4M3 bytes (64-byte swizzle) into the first half
+            // of the stage's token slot; the converters expand them in place
+            mbar_arrive_expect_tx(&a8_full[s], static_cast<uint32_t>(pairk::A_BYTES / 2));
+            tma_load_2d(sA + s * pairk::A_BYTES, &tmA, &a8_full[s], kb * pairk::BK, my_row);
+          } else {
+            tma_load_2d_pair(sA + s * pairk::A_BYTES, &tmA, bar, kb * pairk::BK, my_row);
+          }
 #pragma unroll
           for (int j = 0; j < NB; ++j)
             for (int c = 0; c < nbox[j]; ++c)
               tma_load_2d_pair(sB + s * S::B_BYTES + j * pairk::HALF_B_BYTES + c * pairk::BOX_BYTES,
                                &tmB, bar, t.n0 + j * 256 + static_cast<int>(rank) * half_w + c * 64,
                                brow + kb * pairk::BK);
-          if constexpr (S::MERGE) {
+          if constexpr (MERGE) {
             for (int r = 0; r < tail_half; r += 8)
               tma_load_2d_pair(sT + s * S::T_BYTES + r * pairk::BK * 2, &tmA8, bar,
                                kb * pairk::BK, min(tail_row + r, p.a_rows - 1));
@@ -444,11 +483,16 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           }
         }
       }
-      // drain (even CTA: its full[s] also counts the odd CTA's bytes)
+      // drain (even CTA: its full[s] also counts the odd CTA's bytes; A8:
+      // each CTA's own E4M3 copies)
       if (rank == 0)
         for (int i = 0; i < S::STAGES; ++i)
           if ((armed >> i) & 1u)
             if (!mbar_wait_spin(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
+      if (A8)
+        for (int i = 0; i < S::STAGES; ++i)
+          if ((armed >> i) & 1u)
+            if (!mbar_wait_spin(&a8_full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -465,14 +509,14 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
         // MMAs with any feature below N (the rest of a last tile is skipped)
         const int nmma = min(NB, (p.N - t.n0 + 255) / 256);
         // swapped tile: A = weights (MN-major, the B slot), B = tokens (K-major, the A slot)
         const uint32_t idesc =
             t.swap ? make_idesc_bf16_f32(pairk::BM, (t.ntok + 15) & ~15, true, false) : pairk::IDESC;
         bool merged = false;
-        if constexpr (S::MERGE) merged = t.tail > 0;
+        if constexpr (MERGE) merged = t.tail > 0;
         if (merged) {
           // merged tile: per k-block the four M256 N224 MMAs, then the
           // remainder's four swapped MMAs into columns 224.. (its own loop:
@@ -508,7 +552,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
           }
         } else {
           for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
+            // A8: the odd CTA's converters released their rows with a
+            // cluster-scope arrive; acquire at cluster scope
+            if (!(A8 ? mbar_wait_spin_cluster(&full[s], ph, kWaitLimitNs)
+                     : mbar_wait_spin(&full[s], ph, kWaitLimitNs))) {
               timed_out = true;
               break;
             }
@@ -547,7 +594,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
         mbar_wait_spin(drain, 0, kWaitLimitNs);
       }
     }
-  } else {
+  } else if (!A8 || warp < 2 + NEW) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     // warp w reads TMEM lanes 32 (w % 4) .. +31; with 8 warps, warps 2-5
     // take the first half of the accumulator columns, warps 6-9 the second
@@ -560,7 +607,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
     for (;;) {
       const int tile = next_tile(true);
       if (tile >= total || timed_out) break;
-      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, S::MERGE);
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
       const bool ok = mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) {
         timed_out = true;
@@ -649,7 +696,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
           }
         }
-        if constexpr (S::MERGE) {
+        if constexpr (MERGE) {
           if (t.tail > 0 && hh == NH - 1) {
             // merged tile's remainder: lane = feature (this CTA's M row of
             // the swapped MMA: n0 + 112 rank + 32 q + lane, the first 112 of
@@ -732,6 +779,90 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI>(), 1)
       }
     }
     if (lane == 0) bulk_wait_group0();  // this warp's TMA stores are done
+  } else {
+    // ------------------------------------------------------------ FP8 converters (A8, both CTAs)
+    // Thread ct expands row ct of each staged tile: 64 E4M3 bytes (64-byte
+    // swizzle, first half of the token slot) -> 64 bf16 (128-byte swizzle,
+    // the whole slot, the layout the MMA reads). E4M3 -> f16 -> fp32 -> bf16
+    // is exact. Every row is read before any is overwritten (one barrier of
+    // the group's warps, which also makes a timeout a common decision). Each
+    // warp then releases its rows to the MMA: an arrive on full (even CTA),
+    // or (odd CTA) a 16-byte bulk copy to the even CTA whose completion is
+    // counted on its full barrier, like the odd CTA's weight bytes. Issuing
+    // the copy does not wait; a cluster-scope release arrive from each warp
+    // cost ~0.7 us per stage (measured) and paced the whole GEMM.
+    // group g = 0, 1 takes the stages s with s % 2 == g (STAGES is even, so
+    // fills alternate between the groups); named barrier 1 + g
+    const int cidx = static_cast<int>(threadIdx.x) - 32 * (2 + NEW);
+    const int g = cidx / (32 * pairk::CONV_GROUP);
+    const int ct = cidx - g * 32 * pairk::CONV_GROUP;
+    const uint32_t gbar = 1u + static_cast<uint32_t>(g);
+    const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
+    const uint32_t leader_sink = mapa_shared(smem_u32(smem + S::OFF_SINK), 0);
+    const uint32_t my_sink = smem_u32(smem + S::OFF_SINK);
+    constexpr uint32_t GTHREADS = 32 * pairk::CONV_GROUP;
+    static_assert(S::STAGES % 2 == 0, "converter groups alternate stages");
+    int s = 0;
+    uint32_t ph = 0;
+    for (;;) {
+      const int tile = next_tile(true);
+      if (!bar_and(gbar, GTHREADS, tile < total && !timed_out)) break;
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        if ((s & 1) != g) {
+          if (++s == S::STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+          continue;
+        }
+        ok = mbar_wait_spin(&a8_full[s], ph, kWaitLimitNs);
+        uint8_t* slot = sA + s * pairk::A_BYTES;
+        uint4 raw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          raw[i] = *reinterpret_cast<const uint4*>(slot + ct * 64 + ((i ^ ((ct >> 1) & 3)) << 4));
+        if (!bar_and(gbar, GTHREADS, ok)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint8_t* b = reinterpret_cast<const uint8_t*>(&raw[i]);
+          uint32_t o[8];
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>(
+                b[2 * pp] | (static_cast<uint16_t>(b[2 * pp + 1]) << 8));
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+            const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(f2.x, f2.y);
+            o[pp] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+          *reinterpret_cast<uint4*>(slot + ct * 128 + (((2 * i) ^ (ct & 7)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(slot + ct * 128 + (((2 * i + 1) ^ (ct & 7)) << 4)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&full[s]);
+          else
+            bulk_copy_s2cluster(leader_sink, my_sink, 16u,
+                                leader_full + static_cast<uint32_t>(s * 8));
+        }
+        if (++s == S::STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) {
+        timed_out = true;
+        break;
+      }
+    }
   }
 
   if (timed_out) atomicOr(p.err, kErrTimeout);
@@ -793,12 +924,28 @@ bool make_map_2d_out(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols, b
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, int NB>
+// 2-D map over row-major E4M3 token rows [rows, cols] (bytes), box
+// [128 rows][64 bytes] with the 64-byte swizzle the converters read.
+bool make_map_2d_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int EPI, int NB, bool A8>
 cudaError_t set_pair_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB>,
+    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB, A8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               pairk::smem_bytes<EPI, NB>());
   });
@@ -806,7 +953,7 @@ cudaError_t set_pair_smem_attr() {
 }
 
 // Clusters of two that can be resident at once (cached per device and kernel).
-template <int EPI, int NB>
+template <int EPI, int NB, bool A8>
 int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   static int cache[64] = {};
   int dev = 0;
@@ -815,7 +962,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   cudaLaunchConfig_t lc = lc_in;
   lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB>, &lc) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB, A8>, &lc) != cudaSuccess ||
       n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
@@ -824,7 +971,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   return n;
 }
 
-template <int EPI, int NB>
+template <int EPI, int NB, bool A8>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUtensorMap& mB,
                         const CUtensorMap& mY, TcParams prm, int num_sms,
                         cudaStream_t s) {
@@ -835,7 +982,7 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
       static_cast<long long>(ceil_div(prm.R, pairk::BM) + prm.E) *
       static_cast<long long>(prm.n_tiles > prm.n_tiles_m ? prm.n_tiles : prm.n_tiles_m);
   cudaLaunchConfig_t lc = {};
-  lc.blockDim = dim3(pairk::num_threads<EPI>());
+  lc.blockDim = dim3(pairk::num_threads<EPI, A8>());
   lc.dynamicSmemBytes = pairk::smem_bytes<EPI, NB>();
   lc.stream = s;
   cudaLaunchAttribute attr[2];
@@ -847,14 +994,14 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  cudaError_t st = set_pair_smem_attr<EPI, NB>();
+  cudaError_t st = set_pair_smem_attr<EPI, NB, A8>();
   if (st != cudaSuccess) return st;
   // a persistent grid must fit at once: as many pairs as can be resident
   // together (a pair needs two free SMs of one GPC), not num_sms / 2
-  const int resident = resident_pairs<EPI, NB>(lc, num_sms);
+  const int resident = resident_pairs<EPI, NB, A8>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB>, mA, mA8, mB, mY, prm);
+  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8>, mA, mA8, mB, mY, prm);
 }
 
 // 512-feature tiles (one accumulator, epilogue exposed) pay off only for the
@@ -869,12 +1016,12 @@ int pick_nb(int epi, int R, int E, int K, int N, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int R, const void* W,
-                           int E, int K, int N, const int32_t* offsets, const float* row_scale,
-                           void* out, uint32_t* err, uint32_t* tile_ctr, int num_sms,
-                           cudaStream_t s) {
+cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
+                           const void* W, int E, int K, int N, const int32_t* offsets,
+                           const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
+                           int num_sms, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  if (num_sms < 2) return cudaErrorInvalidValue;
+  if (num_sms < 2 || (a_fp8 && epi != 0)) return cudaErrorInvalidValue;
   CUtensorMap mA, mA8, mB, mY;
   std::memset(&mY, 0, sizeof(mY));
   std::memset(&mA, 0, sizeof(mA));
@@ -884,9 +1031,16 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int
   // A: token rows in [128 rows][64 k] boxes, and [8 rows][64 k] boxes for
   // merged tiles' remainders
   if (a_rows <= 0) return cudaErrorInvalidValue;
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64, 128) ||
-      !make_map_2d(&mA8, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64, 8))
+  if (a_fp8) {
+    // E4M3 token rows, expanded to bf16 in shared memory (no merged tiles)
+    if (!make_map_2d_e4m3(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K)))
+      return cudaErrorInvalidValue;
+  } else if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64,
+                          128) ||
+             !make_map_2d(&mA8, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64,
+                          8)) {
     return cudaErrorInvalidValue;
+  }
   if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64,
                    pairk::BK))
     return cudaErrorInvalidValue;
@@ -912,11 +1066,12 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_rows, int a_shared, int
     if (std::strcmp(f, "256") == 0) nb = 1;
     if (std::strcmp(f, "512") == 0) nb = 2;
   }
+  if (a_fp8) return launch_pair<0, 1, true>(mA, mA8, mB, mY, prm, num_sms, s);
   if (epi == 0)
-    return nb == 2 ? launch_pair<0, 2>(mA, mA8, mB, mY, prm, num_sms, s)
-                   : launch_pair<0, 1>(mA, mA8, mB, mY, prm, num_sms, s);
-  return nb == 2 ? launch_pair<1, 2>(mA, mA8, mB, mY, prm, num_sms, s)
-                 : launch_pair<1, 1>(mA, mA8, mB, mY, prm, num_sms, s);
+    return nb == 2 ? launch_pair<0, 2, false>(mA, mA8, mB, mY, prm, num_sms, s)
+                   : launch_pair<0, 1, false>(mA, mA8, mB, mY, prm, num_sms, s);
+  return nb == 2 ? launch_pair<1, 2, false>(mA, mA8, mB, mY, prm, num_sms, s)
+                 : launch_pair<1, 1, false>(mA, mA8, mB, mY, prm, num_sms, s);
 }
 
 }  // namespace moe

@@ -57,7 +57,7 @@ size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
 bool soft(const moe_config_t& c) { return c.router == MOE_ROUTER_SOFT_GUMBEL; }
 
 struct Layout {
-  size_t err, hist, base, stage, scratch_end;
+  size_t err, hist, base, scratch_end;
   size_t topk_idx, topk_w, counts, offsets, pos, src, x_perm, x_scale, h, y, y_q, y_scale,
       y_zero, total;
   int nchunk;
@@ -77,7 +77,6 @@ Layout layout_of(const moe_config_t& c) {
   L.err = take(kAlign);
   L.hist = take(static_cast<size_t>(c.E) * L.nchunk * 4);
   L.base = take(static_cast<size_t>(c.E) * L.nchunk * 4);
-  L.stage = take(c.payload_fp8 ? R * c.d * 2 : 0);
   L.scratch_end = o;
   L.topk_idx = take(R * 4);
   L.topk_w = take(R * 4);
@@ -153,15 +152,6 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
   return status_of(e);
 }
 
-// FP8 payload -> bf16 staging rows (the GEMM prologue).
-int run_ffn_prologue(const moe_config_t& c, const Layout& L, void* ws, const void* x_perm,
-                     cudaStream_t s) {
-  if (!c.payload_fp8 || c.T == 0) return MOE_OK;
-  const size_t n = static_cast<size_t>(c.T) * c.k * c.d;
-  return status_of(
-      launch_fp8_to_bf16(static_cast<const uint8_t*>(x_perm), n, at<void>(ws, L.stage), s));
-}
-
 int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const void* x_perm,
              const float* x_scale, const int32_t* offsets, const void* W1, const void* W2,
              void* h, float* y, cudaStream_t s) {
@@ -181,14 +171,14 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
   if (sms <= 0) return MOE_ERR_LAUNCH;
   uint32_t* ctr = gemm_counters(ws) + (which - 1);
   if (which == 1) {
-    // soft gating: x_perm is x itself, [T, d], read by every expert
-    const void* A = c.payload_fp8 ? at<void>(ws, L.stage) : x_perm;
-    return status_of(launch_gemm_tc(0, A, soft(c) ? c.T : R, soft(c) ? 1 : 0, R, W1, c.E, c.d,
-                                    c.f, offsets, c.payload_fp8 ? x_scale : nullptr, h, err, ctr,
-                                    sms, s));
+    // soft gating: x_perm is x itself, [T, d], read by every expert; the
+    // FP8 payload is expanded to bf16 inside the GEMM (its prologue)
+    return status_of(launch_gemm_tc(0, x_perm, c.payload_fp8 ? 1 : 0, soft(c) ? c.T : R,
+                                    soft(c) ? 1 : 0, R, W1, c.E, c.d, c.f, offsets,
+                                    c.payload_fp8 ? x_scale : nullptr, h, err, ctr, sms, s));
   }
   return status_of(
-      launch_gemm_tc(1, h, R, 0, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, ctr, sms, s));
+      launch_gemm_tc(1, h, 0, R, 0, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, ctr, sms, s));
 }
 
 int run_combine(const moe_config_t& c, const Layout& L, void* ws, const float* y,
@@ -232,8 +222,7 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
       MOE_OK)
     return st;
   record(events, 2, s);
-  if ((st = run_ffn_prologue(c, L, ws, x_perm, s)) != MOE_OK) return st;
-  record(events, 3, s);
+  record(events, 3, s);  // (no kernel: the FP8 payload is expanded inside the W1 GEMM)
   if ((st = run_gemm(c, L, ws, 1, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
     return st;
   record(events, 4, s);
@@ -323,7 +312,6 @@ int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm, const float* x_s
   if (cfg->T > 0 && cudaMemsetAsync(gemm_counters(ws), 0, kNumGemmCounters * sizeof(uint32_t),
                                     s) != cudaSuccess)
     return MOE_ERR_LAUNCH;
-  if ((st = run_ffn_prologue(*cfg, L, ws, x_perm, s)) != MOE_OK) return st;
   if ((st = run_gemm(*cfg, L, ws, 1, x_perm, x_scale, offsets, W1, W2, h, y_perm, s)) != MOE_OK)
     return st;
   return run_gemm(*cfg, L, ws, 2, x_perm, x_scale, offsets, W1, W2, h, y_perm, s);
@@ -441,7 +429,7 @@ int moe_forward_kernel_count(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   if (cfg->T == 0) return 1;
   const int dispatch = soft(*cfg) ? 1 : 3;  // dense layout, or count + scan + scatter
-  return 1 + dispatch + (cfg->payload_fp8 ? 1 : 0) + 2 + (cfg->output_fp8 ? 1 : 0) + 1;
+  return 1 + dispatch + 2 + (cfg->output_fp8 ? 1 : 0) + 1;
 }
 
 }  // extern "C"

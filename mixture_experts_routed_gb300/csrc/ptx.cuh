@@ -234,6 +234,32 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16, 16-byte aligned) from this CTA's
+// shared memory to another CTA's (shared::cluster addresses from mapa for
+// the destination and its mbarrier); completion is counted in bytes on that
+// mbarrier. Issued asynchronously: the thread does not wait.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst_cluster, uint32_t src_cta,
+                                                    uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (a multiple of 32) that also
+// ANDs a predicate across them: every thread gets the same answer.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -264,6 +290,33 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 // address from mapa); a following release-arrive orders it for the reader.
 __device__ __forceinline__ void st_shared_cluster_s32(uint32_t cluster_addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// Bounded test_wait spin with acquire at cluster scope: for barriers that
+// another CTA's threads arrive on after writing shared memory the waiter
+// then hands to the tensor cores (a suspended try_wait is not woken
+// promptly by a remote arrive).
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_spin_cluster(uint64_t* bar, uint32_t parity,
+                                                       uint64_t limit_ns) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // try_wait with acquire at cluster scope (for barriers other CTAs arrive on).
