@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+        if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t ph = 0, aph = 0;
       bool issued = false;
       for (int c = 0; c < nchunk && !timed_out; ++c) {
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
+        if (!mbar_wait_spin(&tempty[acc], aph ^ 1u, kWaitLimitNs)) {
           timed_out = true;
           break;
         }
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Ep);
         const int kb_end = min(KB, (c + 1) * CHUNK_KB);
         for (int kb = c * CHUNK_KB; kb < kb_end; ++kb) {
-          if (!mbar_wait(&full[s], ph, kWaitLimitNs)) {
+          if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
@@ -246,9 +246,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
-  // selection and weights: one thread per token (row r = thread r), reading
-  // the logits row from shared memory (stride E + 1: conflict-free)
-  if (threadIdx.x < BM) {
+  // selection and weights from the logits rows in shared memory (stride
+  // E + 1): hard top-k with two threads per token (each half the experts,
+  // lists merged: the serial insertion scan over E was ~40 % of the kernel
+  // at E = 64, measured); group-limited and soft routers one thread per
+  // token
+  if (rs.mode == topk::kRouterRenorm || rs.mode == topk::kRouterPrek) {
+    if (threadIdx.x < 2 * BM) {
+      const int r = threadIdx.x >> 1;
+      topk::pair_select_and_weigh(Ls + r * (E + 1), E, rs, t0 + r, threadIdx.x & 1, t0 + r < T,
+                                  topk_idx, topk_w);
+    }
+  } else if (threadIdx.x < BM) {
     const int r = threadIdx.x;
     if (t0 + r < T) {
       if (rs.mode == topk::kRouterSoft)

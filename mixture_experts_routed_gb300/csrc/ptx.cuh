@@ -132,6 +132,17 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// 1-D bulk copy global -> this CTA's shared memory (both addresses 16-byte
+// aligned, `bytes` a multiple of 16), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2-D tiled tensor store shared -> global in the bulk async-group of the
 // issuing thread; c0 is the innermost coordinate (elements), c1 the row.
 // Parts of the box outside the tensor's extent are not written.

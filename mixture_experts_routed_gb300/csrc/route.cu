@@ -25,9 +25,12 @@
 #include <cfloat>
 #include <cstdint>
 #include <cstddef>
+#include <mutex>
+
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -35,8 +38,201 @@ namespace {
 
 using topk::warp_select_and_weigh;
 
+// dynamic shared memory the small-batch kernel may take
+constexpr int kRouteSmemMax = 200 * 1024;
+
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// ---------------------------------------------------------------- small batches
+// E = NE in {8, 16, 32} (bf16) or {4, 8, 16} (fp32): W_g rows of RB = 16, 32
+// or 64 bytes, small enough with TPB tokens' x rows to sit in shared memory.
+// A CTA of 8 warps takes TPB = 64 / NE tokens and pulls W_g and their x rows
+// in with bulk copies on one mbarrier: one round of memory latency for the
+// CTA, where per-thread loads of the hidden dimension took several. Thread c
+// then takes x vectors c, c + 256, ... (VEC elements) of every token and the
+// VEC W_g rows under them, read in a rotated order (row (j + c) % VEC first)
+// so the 8 threads of a quarter-warp hit distinct banks. Partial sums: a
+// reduce-scatter butterfly in each warp (lane l keeps outputs 2l, 2l + 1 of
+// the 64, output q * NE + e), then the 8 warp totals added in warp order: the
+// result does not depend on scheduling.
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N]) {
+  static_assert(N % 32 == 0, "N must be a multiple of 32");
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 16, len = N; m > 0; m >>= 1, len >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < len / 2; ++j) {
+      const float send = upper ? v[j] : v[j + len / 2];
+      const float keep = upper ? v[j + len / 2] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+}
+
+template <typename Tin, int NE>
+__host__ __device__ constexpr int smem_tpb() { return 64 / NE; }
+
+template <typename Tin, int NE>
+size_t route_smem_bytes(int d) {
+  return static_cast<size_t>(d) * NE * sizeof(Tin) +
+         static_cast<size_t>(smem_tpb<Tin, NE>()) * d * sizeof(Tin) + 8 * 64 * 4 + 16;
+}
+
+template <typename Tin, int NE>
+__global__ void __launch_bounds__(256) route_smem_kernel(
+    const Tin* __restrict__ x, const Tin* __restrict__ Wg, const float* __restrict__ bias, int T,
+    int d, int E, RouterSpec rs, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    float* __restrict__ logits, uint32_t* __restrict__ err) {
+  constexpr int TPB = smem_tpb<Tin, NE>();
+  constexpr int N = TPB * NE;  // 64 outputs
+  constexpr int VEC = 16 / sizeof(Tin);
+  constexpr int RB = NE * sizeof(Tin);
+  constexpr int PIECES = RB / 16;
+  static_assert(N == 64 && RB % 16 == 0, "shape");
+  extern __shared__ __align__(16) uint8_t sm[];
+  const size_t xbytes = static_cast<size_t>(d) * sizeof(Tin);
+  uint8_t* sW = sm;
+  uint8_t* sX = sm + static_cast<size_t>(d) * RB;
+  float* part = reinterpret_cast<float*>(sX + TPB * xbytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(part + 8 * N);
+  const int t0 = blockIdx.x * TPB;
+  const int nt = min(TPB, T - t0);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    const uint32_t wbytes = static_cast<uint32_t>(d) * RB;
+    ptx::mbar_arrive_expect_tx(bar, wbytes + static_cast<uint32_t>(nt * xbytes));
+    ptx::bulk_load(sW, Wg, wbytes, bar);
+    for (int q = 0; q < nt; ++q)
+      ptx::bulk_load(sX + q * xbytes, x + static_cast<size_t>(t0 + q) * d,
+                     static_cast<uint32_t>(xbytes), bar);
+  }
+  // a timeout is a common decision of the CTA; the copies must land before
+  // its shared memory is released
+  if (!__syncthreads_and(ptx::mbar_wait(bar, 0, kWaitLimitNs))) {
+    if (threadIdx.x == 0 && err != nullptr) atomicOr(err, kErrTimeout);
+    ptx::mbar_wait(bar, 0, kWaitLimitNs);
+    return;
+  }
+
+  float acc[N];
+#pragma unroll
+  for (int o = 0; o < N; ++o) acc[o] = 0.f;
+  const int nvec = d / VEC;
+  for (int v = threadIdx.x; v < nvec; v += 256) {
+    float xv[TPB][VEC];
+#pragma unroll
+    for (int q = 0; q < TPB; ++q) {
+      const uint4 u = *reinterpret_cast<const uint4*>(sX + q * xbytes + v * 16);
+      const Tin* ue = reinterpret_cast<const Tin*>(&u);
+#pragma unroll
+      for (int jj = 0; jj < VEC; ++jj) xv[q][jj] = to_f32(ue[jj]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < VEC; ++jj) {
+      const int j = (jj + threadIdx.x) & (VEC - 1);
+      const uint8_t* wr = sW + (static_cast<size_t>(v) * VEC + j) * RB;
+      float wv[NE];
+#pragma unroll
+      for (int pc = 0; pc < PIECES; ++pc) {
+        const uint4 u = *reinterpret_cast<const uint4*>(wr + pc * 16);
+        const Tin* ue = reinterpret_cast<const Tin*>(&u);
+#pragma unroll
+        for (int ee = 0; ee < 16 / static_cast<int>(sizeof(Tin)); ++ee)
+          wv[pc * (16 / sizeof(Tin)) + ee] = to_f32(ue[ee]);
+      }
+      // x element j of the vector: a register array indexed by the rotated
+      // j would go to local memory, so select it with a static loop
+      float xj[TPB];
+#pragma unroll
+      for (int q = 0; q < TPB; ++q) {
+        xj[q] = xv[q][0];
+#pragma unroll
+        for (int jj2 = 1; jj2 < VEC; ++jj2) xj[q] = (j == jj2) ? xv[q][jj2] : xj[q];
+      }
+#pragma unroll
+      for (int q = 0; q < TPB; ++q)
+#pragma unroll
+        for (int e = 0; e < NE; ++e) acc[q * NE + e] = fmaf(xj[q], wv[e], acc[q * NE + e]);
+    }
+  }
+  warp_reduce_scatter<N>(acc);
+  part[w * N + 2 * lane] = acc[0];
+  part[w * N + 2 * lane + 1] = acc[1];
+  __syncthreads();
+
+  // warp w selects for tokens t0 + w, t0 + w + 8, ...; lane e owns expert e
+  for (int q = w; q < nt; q += 8) {
+    const int t = t0 + q;
+    float mine = -INFINITY;
+    if (lane < E) {
+      const int o = q * NE + lane;
+      float sum = part[o];
+#pragma unroll
+      for (int ww = 1; ww < 8; ++ww) sum += part[ww * N + o];
+      mine = sum + (bias ? __ldg(bias + lane) : 0.f);
+      if (logits) logits[static_cast<size_t>(t) * E + lane] = mine;
+    }
+    float vv[1] = {mine};
+    int id[1] = {lane < E ? lane : 0x7fffffff};
+    if (rs.mode == topk::kRouterSoft) {
+      topk::warp_soft_weigh<1>(vv, id, E, rs, t, topk_idx, topk_w);
+    } else {
+      if (rs.mode == topk::kRouterGroup) topk::warp_group_limit<1>(vv, id, E, rs);
+      warp_select_and_weigh<1>(vv, id, rs, t, topk_idx, topk_w);
+    }
+  }
+}
+
+template <typename Tin, int NE>
+cudaError_t launch_smem(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
+                        RouterSpec rs, int32_t* topk_idx, float* topk_w, float* logits,
+                        uint32_t* err, cudaStream_t s) {
+  const size_t bytes = route_smem_bytes<Tin, NE>(d);
+  static std::once_flag once;
+  static cudaError_t st = cudaSuccess;
+  std::call_once(once, [] {
+    st = cudaFuncSetAttribute(route_smem_kernel<Tin, NE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteSmemMax);
+  });
+  if (st != cudaSuccess) return st;
+  return launch_pdl(route_smem_kernel<Tin, NE>, dim3(ceil_div(T, smem_tpb<Tin, NE>())),
+                    dim3(256), bytes, s, x, Wg, bias, T, d, E, rs, topk_idx, topk_w, logits,
+                    err);
+}
+
+// The small-batch kernel applies when E is one of its row widths, every x
+// row and W_g start 16-byte aligned, and the tiles fit in shared memory.
+// `err` may be null (the stage call has no workspace): a timeout is then
+// not recorded.
+template <typename Tin>
+bool try_launch_smem(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
+                     RouterSpec rs, int32_t* topk_idx, float* topk_w, float* logits,
+                     uint32_t* err, cudaStream_t s, cudaError_t* out) {
+  if (reinterpret_cast<uintptr_t>(Wg) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(x) % 16 != 0 || (static_cast<size_t>(d) * sizeof(Tin)) % 16 != 0)
+    return false;
+  constexpr int E1 = 16 / sizeof(Tin);  // 16-byte rows
+#define MOE_SMEM(NE)                                                                         \
+  if (E == NE && route_smem_bytes<Tin, NE>(d) <= static_cast<size_t>(kRouteSmemMax)) {      \
+    *out = launch_smem<Tin, NE>(x, Wg, bias, T, d, E, rs, topk_idx, topk_w, logits, err, s); \
+    return true;                                                                             \
+  }
+  MOE_SMEM(E1)
+  MOE_SMEM(2 * E1)
+  MOE_SMEM(4 * E1)
+#undef MOE_SMEM
+  return false;
+}
 
 // ---------------------------------------------------------------- narrow
 // E <= 32. A CTA of 4 warps handles TPB tokens; its 128 threads stride the
@@ -385,8 +581,15 @@ cudaError_t launch_tiled(const Tin* x, const Tin* Wg, const float* bias, int T, 
 template <typename Tin>
 cudaError_t launch_route_t(const Tin* x, const Tin* Wg, const float* bias, int T, int d, int E,
                            RouterSpec rs, int32_t* topk_idx, float* topk_w,
-                           float* logits, cudaStream_t s) {
+                           float* logits, uint32_t* err, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  // d >= 1024: the load rounds of the per-thread kernel dominate (on a
+  // d = 128 layer the bulk-copy kernel measured slower)
+  if (E <= 32 && T < 4096 && d >= 1024) {
+    cudaError_t st = cudaSuccess;
+    if (try_launch_smem<Tin>(x, Wg, bias, T, d, E, rs, topk_idx, topk_w, logits, err, s, &st))
+      return st;
+  }
   if (E <= 32 && T >= 4096) {
     // 64 tokens per CTA, K split over 4 groups of 64 threads
     if (E <= 16)
@@ -445,10 +648,10 @@ cudaError_t launch_route(int dtype, const void* x, const void* Wg, const float* 
                           s);
   if (dtype == 0)
     return launch_route_t<float>(static_cast<const float*>(x), static_cast<const float*>(Wg),
-                                 bias, T, d, E, rs, topk_idx, topk_w, logits, s);
+                                 bias, T, d, E, rs, topk_idx, topk_w, logits, err, s);
   return launch_route_t<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(x),
                                        static_cast<const __nv_bfloat16*>(Wg), bias, T, d, E, rs,
-                                       topk_idx, topk_w, logits, s);
+                                       topk_idx, topk_w, logits, err, s);
 }
 
 }  // namespace moe

@@ -222,6 +222,92 @@ __device__ __forceinline__ void thread_select_and_weigh(const float* row, int E,
   }
 }
 
+// Two threads per token (lanes 2r and 2r+1 of a warp, `half` = lane & 1;
+// every lane of the warp calls this): thread h keeps the best kMaxTopK of
+// experts [h E/2, (h+1) E/2) by insertion (ascending ids, strict >: equal
+// logits keep the lower id first), the two sorted lists are merged by a
+// bitonic step (element s against the partner's 7-s) and an 8-element
+// bitonic sort under `beats`, which gives exactly the list one thread would
+// keep over all E. Weights as thread_select_and_weigh. Not for the
+// group-limited or soft routers.
+__device__ __forceinline__ void pair_select_and_weigh(const float* row, int E,
+                                                      const RouterSpec& rs, int t, int half,
+                                                      bool active,
+                                                      int32_t* __restrict__ topk_idx,
+                                                      float* __restrict__ topk_w) {
+  float sv[kMaxTopK];
+  int si[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    sv[j] = -INFINITY;
+    si[j] = 0x7fffffff;
+  }
+  const int hw = E / 2;
+  for (int e = half * hw; e < (half + 1) * hw; ++e) {
+    const float v = row[e];
+    if (v > sv[kMaxTopK - 1]) {
+#pragma unroll
+      for (int j = kMaxTopK - 1; j > 0; --j) {
+        const bool down = v > sv[j - 1];
+        const bool here = !down && v > sv[j];
+        sv[j] = down ? sv[j - 1] : (here ? v : sv[j]);
+        si[j] = down ? si[j - 1] : (here ? e : si[j]);
+      }
+      if (v > sv[0]) {
+        sv[0] = v;
+        si[0] = e;
+      }
+    }
+  }
+  // bitonic merge with the partner's list: c[s] = better of (mine[s],
+  // partner[7 - s]) holds the best kMaxTopK of both as a bitonic sequence
+  float cv[kMaxTopK];
+  int ci[kMaxTopK];
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    const float pv = __shfl_xor_sync(0xffffffffu, sv[kMaxTopK - 1 - s], 1);
+    const int pi = __shfl_xor_sync(0xffffffffu, si[kMaxTopK - 1 - s], 1);
+    const bool mine = beats(sv[s], si[s], pv, pi);
+    cv[s] = mine ? sv[s] : pv;
+    ci[s] = mine ? si[s] : pi;
+  }
+#pragma unroll
+  for (int stride = kMaxTopK / 2; stride > 0; stride >>= 1) {
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      if ((s & stride) == 0) {
+        const int o = s + stride;
+        if (beats(cv[o], ci[o], cv[s], ci[s])) {
+          const float tv = cv[s];
+          const int ti = ci[s];
+          cv[s] = cv[o];
+          ci[s] = ci[o];
+          cv[o] = tv;
+          ci[o] = ti;
+        }
+      }
+    }
+  }
+  if (!active || half != 0) return;
+  const int k = rs.k;
+  const int rounds = rounds_of(rs);
+  const float m = cv[0];
+  float den = 0.f;
+  float ex[kMaxTopK];
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    ex[s] = (s < rounds) ? expf(cv[s] - m) : 0.f;
+    den += ex[s];
+  }
+#pragma unroll
+  for (int s = 0; s < kMaxTopK; ++s) {
+    if (s < k) {
+      topk_idx[static_cast<size_t>(t) * k + s] = ci[s];
+      topk_w[static_cast<size_t>(t) * k + s] = ex[s] / den;
+    }
+  }
+}
+
 // Soft gating (Deepseek-MoE sync-tax article, section 3.3), warp form: lane
 // values v[j] for experts id[j] (padding: id >= E); z = (L + g) / tau with
 // the token's Gumbel samples g; w = exp(z - max z) / sum; slot j = expert j
