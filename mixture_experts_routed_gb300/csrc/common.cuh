@@ -111,6 +111,14 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, cons
                                     const int32_t* counts, const int32_t* base,
                                     int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
                                     float* x_scale, uint32_t* err, cudaStream_t s);
+// Small batches (R <= kDispatchFusedMaxRows): count, scan and scatter in one
+// kernel (each CTA counts all ids); also zeroes `nzero` words at `zero`.
+constexpr long long kDispatchFusedMaxRows = 4096;
+cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const void* x,
+                                  const int32_t* topk_idx, int T, int d, int k, int E,
+                                  int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                                  void* x_perm, float* x_scale, uint32_t* err, uint32_t* zero,
+                                  int nzero, cudaStream_t s);
 // Soft gating's layout (every token to every expert, token order): counts,
 // offsets, pos, src; zeroes `nzero` words at `zero` when non-null.
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,

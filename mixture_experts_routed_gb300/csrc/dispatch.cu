@@ -18,12 +18,20 @@
 //           per-token absmax scale, or one static scale for every row,
 //           sync-tax article section 3.1).
 //
+// Small batches (R = T*k <= kDispatchFusedMaxRows) run the scatter kernel
+// alone ("fused"): every CTA counts all R expert ids itself (warp-aggregated
+// shared-memory counters: the totals and the entries of earlier chunks), so
+// the count and scan launches and their hist/base tables drop out.
+//
 // Expert ids outside [0, E) are skipped and flag kErrBadIndex.
 #include <cstdint>
+#include <mutex>
+
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -138,25 +146,57 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float s) {
   return make_uint2(w[0], w[1]);
 }
 
-// dtype 0: fp32 rows, 1: bf16 rows. FP8 only with bf16.
-template <int DT, bool FP8>
+// dtype 0: fp32 rows, 1: bf16 rows. FP8 only with bf16. FUSED: counts and
+// the earlier chunks' rows per expert come from this CTA's own pass over all
+// ids (counts is then an output, base unused; `zero` gets nzero zero words).
+template <int DT, bool FP8, bool FUSED>
 __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
     const void* __restrict__ xv, const int32_t* __restrict__ idx, int T, int d, int k, int E,
-    int nchunk, const int32_t* __restrict__ counts, const int32_t* __restrict__ base,
+    int nchunk, int32_t* __restrict__ counts, const int32_t* __restrict__ base,
     int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ src,
     void* __restrict__ x_perm, float* __restrict__ x_scale, float static_scale,
-    uint32_t* __restrict__ err) {
+    uint32_t* __restrict__ err, uint32_t* __restrict__ zero, int nzero, int bulk) {
   __shared__ int off_s[kMaxExperts + 1];
+  __shared__ uint64_t rows_bar;
   __shared__ int cnt_w[2][kMaxExperts];  // per-warp expert counts (<= 64 entries, 2 warps)
   __shared__ int pos_s[kTPC * kMaxTopK];
+  __shared__ int tot_s[FUSED ? kMaxExperts : 1];     // FUSED: rows per expert
+  __shared__ int before_s[FUSED ? kMaxExperts : 1];  // FUSED: rows in earlier chunks
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int c = blockIdx.x;
+  const long long R = static_cast<long long>(T) * k;
+  const long long i0 = static_cast<long long>(c) * kTPC * k;
+
+  if constexpr (FUSED) {
+    if (zero != nullptr && c == 0 && tid < nzero) zero[tid] = 0u;
+    for (int e = tid; e < E; e += 256) {
+      tot_s[e] = 0;
+      before_s[e] = 0;
+    }
+    __syncthreads();
+    // every CTA counts all R ids; a warp's equal ids are added at once
+    for (long long b0 = static_cast<long long>(w) * 32; b0 < R; b0 += 256) {
+      const long long i = b0 + lane;
+      int e = i < R ? __ldg(idx + i) : -1;
+      const bool valid = e >= 0 && e < E;
+      if (i < R && !valid && c == 0) atomicOr(err, kErrBadIndex);
+      if (!valid) e = -1;
+      const unsigned mask = __match_any_sync(0xffffffffu, e);
+      const unsigned early = __ballot_sync(0xffffffffu, i < i0);
+      if (valid && lane == __ffs(mask) - 1) {
+        atomicAdd(&tot_s[e], __popc(mask));
+        const int nb = __popc(mask & early);
+        if (nb) atomicAdd(&before_s[e], nb);
+      }
+    }
+    __syncthreads();
+  }
 
   // offsets = exclusive scan of counts
   {
-    const int v = (tid < E) ? __ldg(counts + tid) : 0;
+    const int v = (tid < E) ? (FUSED ? tot_s[tid] : __ldg(counts + tid)) : 0;
     int total;
     const int ex = block_exclusive_scan_256(v, &total);
     if (tid < E) off_s[tid] = ex;
@@ -164,14 +204,13 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
     if (c == 0) {
       if (tid < E) offsets[tid] = ex;
       if (tid == 0) offsets[E] = total;
+      if (FUSED && tid < E) counts[tid] = v;
     }
   }
   for (int q = tid; q < 2 * kMaxExperts; q += 256) (&cnt_w[0][0])[q] = 0;
   __syncthreads();
 
   // stable ranks of this chunk's entries (at most 64: warps 0 and 1)
-  const long long R = static_cast<long long>(T) * k;
-  const long long i0 = static_cast<long long>(c) * kTPC * k;
   const int n = static_cast<int>(min(static_cast<long long>(kTPC * k), R - i0));
   int e = -2;
   unsigned mask = 0;
@@ -193,7 +232,8 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
       if (e >= 0) {
         const int before = (w == 1) ? cnt_w[0][e] : 0;
         const int rank = before + __popc(mask & ((1u << lane) - 1u));
-        p = off_s[e] + __ldg(base + static_cast<size_t>(e) * nchunk + c) + rank;
+        p = off_s[e] + (FUSED ? before_s[e] : __ldg(base + static_cast<size_t>(e) * nchunk + c)) +
+            rank;
         src[p] = static_cast<int32_t>((i0 + q) / k);
       }
       pos[i0 + q] = p;
@@ -203,10 +243,45 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
   __syncthreads();
 
   if constexpr (!FP8) {
+    constexpr int ES = DT == 0 ? 4 : 2;
+    if (bulk) {
+      // rows of at most kDispatchBulkRowBytes: warp 0 pulls the chunk's rows
+      // into shared memory with bulk copies (one round of latency) and sends
+      // each to its k destinations with bulk stores (asynchronous, no
+      // register traffic); the other warps are done
+      extern __shared__ __align__(16) uint8_t rows_s[];
+      if (w != 0) return;
+      const int t0 = c * kTPC;
+      const int ntok = min(kTPC, T - t0);
+      const uint32_t rb = static_cast<uint32_t>(d) * ES;
+      if (lane == 0) {
+        ptx::mbar_init(&rows_bar, 1);
+        ptx::fence_mbar_init();
+        ptx::mbar_arrive_expect_tx(&rows_bar, rb * static_cast<uint32_t>(ntok));
+        for (int q = 0; q < ntok; ++q)
+          ptx::bulk_load(rows_s + q * rb,
+                         static_cast<const char*>(xv) + static_cast<size_t>(t0 + q) * rb, rb,
+                         &rows_bar);
+      }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, ptx::mbar_wait(&rows_bar, 0, kWaitLimitNs))) {
+        if (lane == 0) atomicOr(err, kErrTimeout);
+        ptx::mbar_wait(&rows_bar, 0, kWaitLimitNs);  // the copies land before exit
+        return;
+      }
+      for (int qj = lane; qj < ntok * k; qj += 32) {
+        const int pj = pos_s[qj];
+        if (pj >= 0)
+          ptx::bulk_store(static_cast<char*>(x_perm) + static_cast<size_t>(pj) * rb,
+                          rows_s + (qj / k) * rb, rb);
+      }
+      ptx::bulk_commit_group();
+      ptx::bulk_wait_group0();  // the rows are written before the CTA exits
+      return;
+    }
     // row copy: the whole CTA strides the chunk's rows (16-byte vectors),
     // four loads in flight per thread; each row is read once and written to
     // its k destinations
-    constexpr int ES = DT == 0 ? 4 : 2;
     const int nvec = d * ES / 16;
     const int t0 = c * kTPC;
     const int ntok = min(kTPC, T - t0);
@@ -327,6 +402,30 @@ __global__ void __launch_bounds__(256) dense_layout_kernel(int T, int E, int32_t
   }
 }
 
+// Rows copied by bulk copies through shared memory: plain (not FP8) rows of
+// at most kDispatchBulkRowBytes (the chunk's rows take kTPC times that).
+constexpr int kDispatchBulkRowBytes = 8192;
+int bulk_rows(int dtype, int fp8, int d) {
+  const long long rb = static_cast<long long>(d) * (dtype == 0 ? 4 : 2);
+  return !fp8 && rb % 16 == 0 && rb <= kDispatchBulkRowBytes ? 1 : 0;
+}
+
+// Opt the plain-row scatter kernels into their shared memory, once.
+template <typename K>
+cudaError_t set_bulk_smem(K) {
+  static std::once_flag once;
+  static cudaError_t st = cudaSuccess;
+  std::call_once(once, [] {
+    const int bytes = kTPC * kDispatchBulkRowBytes;
+    const auto a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    st = cudaFuncSetAttribute(dispatch_scatter_kernel<0, false, false>, a, bytes);
+    if (st == cudaSuccess) st = cudaFuncSetAttribute(dispatch_scatter_kernel<1, false, false>, a, bytes);
+    if (st == cudaSuccess) st = cudaFuncSetAttribute(dispatch_scatter_kernel<0, false, true>, a, bytes);
+    if (st == cudaSuccess) st = cudaFuncSetAttribute(dispatch_scatter_kernel<1, false, true>, a, bytes);
+  });
+  return st;
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_empty(int E, int32_t* counts, int32_t* offsets, cudaStream_t s) {
@@ -352,10 +451,39 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, cons
                                     int32_t* offsets, int32_t* pos, int32_t* src, void* x_perm,
                                     float* x_scale, uint32_t* err, cudaStream_t s) {
   const dim3 grid(nchunk), block(256);
-  auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false>
-                : (!fp8 ? dispatch_scatter_kernel<1, false> : dispatch_scatter_kernel<1, true>);
-  return launch_pdl(kernel, grid, block, 0, s, x, topk_idx, T, d, k, E, nchunk, counts, base,
-                    offsets, pos, src, x_perm, x_scale, static_scale, err);
+  auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false, false>
+                : (!fp8 ? dispatch_scatter_kernel<1, false, false>
+                        : dispatch_scatter_kernel<1, true, false>);
+  const int bulk = bulk_rows(dtype, fp8, d);
+  const size_t smem = bulk ? static_cast<size_t>(kTPC) * d * (dtype == 0 ? 4 : 2) : 0;
+  if (bulk) {
+    const cudaError_t st = set_bulk_smem(kernel);
+    if (st != cudaSuccess) return st;
+  }
+  return launch_pdl(kernel, grid, block, smem, s, x, topk_idx, T, d, k, E, nchunk,
+                    const_cast<int32_t*>(counts), base, offsets, pos, src, x_perm, x_scale,
+                    static_scale, err, static_cast<uint32_t*>(nullptr), 0, bulk);
+}
+
+cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const void* x,
+                                  const int32_t* topk_idx, int T, int d, int k, int E,
+                                  int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                                  void* x_perm, float* x_scale, uint32_t* err, uint32_t* zero,
+                                  int nzero, cudaStream_t s) {
+  const int nchunk = ceil_div(T, kTPC);
+  const dim3 grid(nchunk), block(256);
+  auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false, true>
+                : (!fp8 ? dispatch_scatter_kernel<1, false, true>
+                        : dispatch_scatter_kernel<1, true, true>);
+  const int bulk = bulk_rows(dtype, fp8, d);
+  const size_t smem = bulk ? static_cast<size_t>(kTPC) * d * (dtype == 0 ? 4 : 2) : 0;
+  if (bulk) {
+    const cudaError_t st = set_bulk_smem(kernel);
+    if (st != cudaSuccess) return st;
+  }
+  return launch_pdl(kernel, grid, block, smem, s, x, topk_idx, T, d, k, E, nchunk, counts,
+                    static_cast<const int32_t*>(nullptr), offsets, pos, src, x_perm, x_scale,
+                    static_scale, err, zero, nzero, bulk);
 }
 
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,

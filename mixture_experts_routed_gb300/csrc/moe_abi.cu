@@ -138,6 +138,11 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
     return status_of(launch_dense_layout(c.T, c.E, counts, offsets, pos, src, gemm_counters(ws),
                                          kNumGemmCounters, s));
   uint32_t* err = at<uint32_t>(ws, L.err);
+  if (static_cast<long long>(c.T) * c.k <= kDispatchFusedMaxRows)
+    return status_of(launch_dispatch_fused(
+        c.dtype, c.payload_fp8 != 0, c.payload_fp8 == 2 ? c.payload_scale : 0.f, x, idx, c.T, c.d,
+        c.k, c.E, counts, offsets, pos, src, x_perm, x_scale, err, gemm_counters(ws),
+        kNumGemmCounters, s));
   int32_t* hist = at<int32_t>(ws, L.hist);
   int32_t* base = at<int32_t>(ws, L.base);
   // the count kernel also zeroes the GEMM tile counters for the layer
@@ -428,7 +433,9 @@ const char* moe_strerror(int status) {
 int moe_forward_kernel_count(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   if (cfg->T == 0) return 1;
-  const int dispatch = soft(*cfg) ? 1 : 3;  // dense layout, or count + scan + scatter
+  // dense layout, one fused kernel for small batches, or count + scan + scatter
+  const int dispatch =
+      soft(*cfg) || static_cast<long long>(cfg->T) * cfg->k <= kDispatchFusedMaxRows ? 1 : 3;
   return 1 + dispatch + 2 + (cfg->output_fp8 ? 1 : 0) + 1;
 }
 

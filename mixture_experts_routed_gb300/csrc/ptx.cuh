@@ -154,6 +154,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t sm
       "r"(smem_src), "r"(c0), "r"(c1)
       : "memory");
 }
+// 1-D bulk copy this CTA's shared memory -> global (16-byte aligned
+// addresses, bytes a multiple of 16) in the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
