@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     gate_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                    const float* __restrict__ bias, int T, int d, int E, RouterSpec rs,
                    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-                   float* __restrict__ logits, uint32_t* __restrict__ err) {
+                   float* __restrict__ logits, uint32_t* __restrict__ err, int ksplit) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -79,14 +79,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   float* Ls = reinterpret_cast<float*>(smem);  // [BM][E + 1] after the main loop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * BM;
+  // ksplit = 2: a cluster of two CTAs shares the 128-token tile, CTA `part`
+  // accumulating k-blocks [part * KB/2, ...) of d; the partial logits are
+  // added through distributed shared memory and each CTA routes 64 tokens
+  const int part = ksplit == 2 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t0 = (blockIdx.x / ksplit) * BM;
   // the weight tile is Ep = E rounded up to 64 experts wide: TMA zero-fills
   // the boxes past E, and the padded columns are never read back
   const int Ep = (E + 63) & ~63;
   const int nwbox = Ep / 64;
   const uint32_t stage_bytes = static_cast<uint32_t>(X_BYTES + nwbox * BOX_BYTES);
   const int nst = min(MAX_STAGES, RING_BYTES / static_cast<int>(stage_bytes));
-  const int KB = d / BK;
+  const int KB_all = d / BK;
+  const int kb0 = part == 0 ? 0 : KB_all / 2;
+  const int KB = (ksplit == 2 && part == 0) ? KB_all / 2 : KB_all - kb0;  // this CTA's k-blocks
   const int nchunk = (KB + CHUNK_KB - 1) / CHUNK_KB;
   // TMEM: 512 columns (one CTA per SM) as 512 / E accumulators of E columns,
   // so the MMA runs up to that many 128-K chunks ahead of the epilogue
@@ -134,9 +140,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         uint8_t* st = smem + s * stage_bytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
-        tma_load_2d(st, &tmX, &full[s], kb * BK, t0);
+        tma_load_2d(st, &tmX, &full[s], (kb0 + kb) * BK, t0);
         for (int c = 0; c < nwbox; ++c)
-          tma_load_2d(st + X_BYTES + c * BOX_BYTES, &tmW, &full[s], c * 64, kb * BK);
+          tma_load_2d(st + X_BYTES + c * BOX_BYTES, &tmW, &full[s], c * 64, (kb0 + kb) * BK);
         armed |= 1u << s;
         armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
         if (++s == nst) {
@@ -232,33 +238,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (timed_out && err != nullptr) atomicOr(err, kErrTimeout);
   __syncthreads();  // the ring is idle: reuse it for the logits tile
+  // ksplit = 2: CTA `part` finishes rows [64 part, 64 part + 64); its partial
+  // sums of the other half go straight into the peer's tile at row r ^ 64
+  // (the rows the peer does not finish itself) with remote stores
+  const uint32_t peer_ls =
+      ksplit == 2 ? mapa_shared(smem_u32(Ls), static_cast<uint32_t>(part ^ 1)) : 0u;
   if (warp >= 2) {
     const int q = warp & 3, half = (warp - 2) >> 2, ncol = Ep / 2;
     const int r = q * 32 + lane;
+    const bool own_row = (r / (BM / 2)) == part;
 #pragma unroll
     for (int j = 0; j < HALF; ++j) {
       if (j < ncol && half * ncol + j < E) {
         const int e = half * ncol + j;
-        const float val = tot[j] + (bias ? __ldg(bias + e) : 0.f);
-        Ls[r * (E + 1) + e] = val;
-        if (logits && t0 + r < T) logits[static_cast<size_t>(t0 + r) * E + e] = val;
+        if (ksplit == 2) {
+          if (own_row)
+            Ls[r * (E + 1) + e] = tot[j];  // this CTA's partial sum
+          else
+            st_shared_cluster_s32(peer_ls + static_cast<uint32_t>(((r ^ (BM / 2)) * (E + 1) + e) * 4),
+                                  __float_as_int(tot[j]));
+        } else {
+          const float val = tot[j] + (bias ? __ldg(bias + e) : 0.f);
+          Ls[r * (E + 1) + e] = val;
+          if (logits && t0 + r < T) logits[static_cast<size_t>(t0 + r) * E + e] = val;
+        }
       }
     }
   }
-  __syncthreads();
-  // selection and weights from the logits rows in shared memory (stride
-  // E + 1): hard top-k with two threads per token (each half the experts,
-  // lists merged: the serial insertion scan over E was ~40 % of the kernel
-  // at E = 64, measured); group-limited and soft routers one thread per
-  // token
-  if (rs.mode == topk::kRouterRenorm || rs.mode == topk::kRouterPrek) {
-    if (threadIdx.x < 2 * BM) {
-      const int r = threadIdx.x >> 1;
-      topk::pair_select_and_weigh(Ls + r * (E + 1), E, rs, t0 + r, threadIdx.x & 1, t0 + r < T,
-                                  topk_idx, topk_w);
+  if (ksplit == 2) {
+    // the barrier makes the peer's remote stores visible (and none is in
+    // flight past it); rows [64 part, 64 part + 64) then add the two
+    // partials (P0 + P1 is the same sum either way round) and the bias from
+    // local shared memory
+    cluster_sync();
+    for (int i = threadIdx.x; i < (BM / 2) * E; i += NUM_THREADS) {
+      const int r = (BM / 2) * part + i / E, e = i - (i / E) * E;
+      const int o = r * (E + 1) + e;
+      const float val = (Ls[o] + Ls[(r ^ (BM / 2)) * (E + 1) + e]) + (bias ? __ldg(bias + e) : 0.f);
+      Ls[o] = val;
+      if (logits && t0 + r < T) logits[static_cast<size_t>(t0 + r) * E + e] = val;
     }
-  } else if (threadIdx.x < BM) {
-    const int r = threadIdx.x;
+    __syncthreads();
+  } else {
+    __syncthreads();
+  }
+  // selection and weights from the logits rows in shared memory (stride
+  // E + 1): hard top-k with two threads per token, four with the K split
+  // (each a share of the experts, lists merged: the serial insertion scan
+  // over E was ~40 % of the kernel at E = 64, measured); group-limited and
+  // soft routers one thread per token
+  const int r_lo = ksplit == 2 ? (BM / 2) * part : 0;
+  const int nrows = BM / ksplit;
+  if (rs.mode == topk::kRouterRenorm || rs.mode == topk::kRouterPrek) {
+    // 256 threads: two per token for 128 rows, four for the 64 of a split
+    if (threadIdx.x < 256) {
+      if (ksplit == 2) {
+        const int r = r_lo + (threadIdx.x >> 2);
+        topk::group_select_and_weigh<4>(Ls + r * (E + 1), E, rs, t0 + r, threadIdx.x & 3,
+                                        t0 + r < T, topk_idx, topk_w);
+      } else {
+        const int r = r_lo + (threadIdx.x >> 1);
+        topk::group_select_and_weigh<2>(Ls + r * (E + 1), E, rs, t0 + r, threadIdx.x & 1,
+                                        t0 + r < T, topk_idx, topk_w);
+      }
+    }
+  } else if (threadIdx.x < nrows) {
+    const int r = r_lo + threadIdx.x;
     if (t0 + r < T) {
       if (rs.mode == topk::kRouterSoft)
         topk::thread_soft_weigh(Ls + r * (E + 1), E, rs, t0 + r, topk_idx, topk_w);
@@ -297,6 +342,20 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K is split across a CTA pair when two CTAs per 128-token tile still fit in
+// one wave and each half has at least two k-blocks (GB300, T = 8192, d =
+// 2048, E = 64: 64 CTAs left 88 SMs idle).
+int gate_ksplit(int T, int d) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  return (2 * ceil_div(T, BM) <= sms && d / BK >= 4) ? 2 : 1;
+}
+
 template <int EMAX>
 cudaError_t launch_emax(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int T,
                         int d, int E, RouterSpec rs, int32_t* idx, float* w,
@@ -308,8 +367,23 @@ cudaError_t launch_emax(const CUtensorMap& mx, const CUtensorMap& mw, const floa
                               SMEM_BYTES);
   });
   if (st != cudaSuccess) return st;
-  return launch_pdl(gate_tc_kernel<EMAX>, dim3(ceil_div(T, BM)), dim3(NUM_THREADS), SMEM_BYTES, s,
-                    mx, mw, bias, T, d, E, rs, idx, w, logits, err);
+  const int ksplit = gate_ksplit(T, d);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(ceil_div(T, BM) * ksplit);
+  lc.blockDim = dim3(NUM_THREADS);
+  lc.dynamicSmemBytes = SMEM_BYTES;
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(ksplit);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  return cudaLaunchKernelEx(&lc, gate_tc_kernel<EMAX>, mx, mw, bias, T, d, E, rs, idx, w, logits,
+                            err, ksplit);
 }
 
 }  // namespace

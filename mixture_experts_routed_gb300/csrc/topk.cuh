@@ -222,19 +222,22 @@ __device__ __forceinline__ void thread_select_and_weigh(const float* row, int E,
   }
 }
 
-// Two threads per token (lanes 2r and 2r+1 of a warp, `half` = lane & 1;
-// every lane of the warp calls this): thread h keeps the best kMaxTopK of
-// experts [h E/2, (h+1) E/2) by insertion (ascending ids, strict >: equal
-// logits keep the lower id first), the two sorted lists are merged by a
-// bitonic step (element s against the partner's 7-s) and an 8-element
-// bitonic sort under `beats`, which gives exactly the list one thread would
-// keep over all E. Weights as thread_select_and_weigh. Not for the
+// G threads per token (G = 2 or 4 consecutive lanes of a warp, `h` = lane
+// % G; every lane of the warp calls this; E a multiple of G): thread h keeps
+// the best kMaxTopK of experts [h E/G, (h+1) E/G) by insertion (ascending
+// ids, strict >: equal logits keep the lower id first); the sorted lists are
+// merged pairwise at shuffle distance 1, then 2, each merge a bitonic step
+// (element s against the partner's 7-s) and an 8-element bitonic sort under
+// `beats`, which gives exactly the list one thread would keep over all E.
+// Weights as thread_select_and_weigh (written by h = 0). Not for the
 // group-limited or soft routers.
-__device__ __forceinline__ void pair_select_and_weigh(const float* row, int E,
-                                                      const RouterSpec& rs, int t, int half,
-                                                      bool active,
-                                                      int32_t* __restrict__ topk_idx,
-                                                      float* __restrict__ topk_w) {
+template <int G>
+__device__ __forceinline__ void group_select_and_weigh(const float* row, int E,
+                                                       const RouterSpec& rs, int t, int h,
+                                                       bool active,
+                                                       int32_t* __restrict__ topk_idx,
+                                                       float* __restrict__ topk_w) {
+  static_assert(G == 2 || G == 4, "2 or 4 threads per token");
   float sv[kMaxTopK];
   int si[kMaxTopK];
 #pragma unroll
@@ -242,8 +245,8 @@ __device__ __forceinline__ void pair_select_and_weigh(const float* row, int E,
     sv[j] = -INFINITY;
     si[j] = 0x7fffffff;
   }
-  const int hw = E / 2;
-  for (int e = half * hw; e < (half + 1) * hw; ++e) {
+  const int hw = E / G;
+  for (int e = h * hw; e < (h + 1) * hw; ++e) {
     const float v = row[e];
     if (v > sv[kMaxTopK - 1]) {
 #pragma unroll
@@ -259,50 +262,59 @@ __device__ __forceinline__ void pair_select_and_weigh(const float* row, int E,
       }
     }
   }
-  // bitonic merge with the partner's list: c[s] = better of (mine[s],
-  // partner[7 - s]) holds the best kMaxTopK of both as a bitonic sequence
-  float cv[kMaxTopK];
-  int ci[kMaxTopK];
+  // bitonic merges with the partner's list: c[s] = better of (mine[s],
+  // partner[7 - s]) holds the best kMaxTopK of both as a bitonic sequence,
+  // sorted again by three half-cleaner stages
 #pragma unroll
-  for (int s = 0; s < kMaxTopK; ++s) {
-    const float pv = __shfl_xor_sync(0xffffffffu, sv[kMaxTopK - 1 - s], 1);
-    const int pi = __shfl_xor_sync(0xffffffffu, si[kMaxTopK - 1 - s], 1);
-    const bool mine = beats(sv[s], si[s], pv, pi);
-    cv[s] = mine ? sv[s] : pv;
-    ci[s] = mine ? si[s] : pi;
-  }
-#pragma unroll
-  for (int stride = kMaxTopK / 2; stride > 0; stride >>= 1) {
+  for (int dist = 1; dist < G; dist <<= 1) {
+    float cv[kMaxTopK];
+    int ci[kMaxTopK];
 #pragma unroll
     for (int s = 0; s < kMaxTopK; ++s) {
-      if ((s & stride) == 0) {
-        const int o = s + stride;
-        if (beats(cv[o], ci[o], cv[s], ci[s])) {
-          const float tv = cv[s];
-          const int ti = ci[s];
-          cv[s] = cv[o];
-          ci[s] = ci[o];
-          cv[o] = tv;
-          ci[o] = ti;
+      const float pv = __shfl_xor_sync(0xffffffffu, sv[kMaxTopK - 1 - s], dist);
+      const int pi = __shfl_xor_sync(0xffffffffu, si[kMaxTopK - 1 - s], dist);
+      const bool mine = beats(sv[s], si[s], pv, pi);
+      cv[s] = mine ? sv[s] : pv;
+      ci[s] = mine ? si[s] : pi;
+    }
+#pragma unroll
+    for (int stride = kMaxTopK / 2; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int s = 0; s < kMaxTopK; ++s) {
+        if ((s & stride) == 0) {
+          const int o = s + stride;
+          if (beats(cv[o], ci[o], cv[s], ci[s])) {
+            const float tv = cv[s];
+            const int ti = ci[s];
+            cv[s] = cv[o];
+            ci[s] = ci[o];
+            cv[o] = tv;
+            ci[o] = ti;
+          }
         }
       }
     }
+#pragma unroll
+    for (int s = 0; s < kMaxTopK; ++s) {
+      sv[s] = cv[s];
+      si[s] = ci[s];
+    }
   }
-  if (!active || half != 0) return;
+  if (!active || h != 0) return;
   const int k = rs.k;
   const int rounds = rounds_of(rs);
-  const float m = cv[0];
+  const float m = sv[0];
   float den = 0.f;
   float ex[kMaxTopK];
 #pragma unroll
   for (int s = 0; s < kMaxTopK; ++s) {
-    ex[s] = (s < rounds) ? expf(cv[s] - m) : 0.f;
+    ex[s] = (s < rounds) ? expf(sv[s] - m) : 0.f;
     den += ex[s];
   }
 #pragma unroll
   for (int s = 0; s < kMaxTopK; ++s) {
     if (s < k) {
-      topk_idx[static_cast<size_t>(t) * k + s] = ci[s];
+      topk_idx[static_cast<size_t>(t) * k + s] = si[s];
       topk_w[static_cast<size_t>(t) * k + s] = ex[s] / den;
     }
   }
