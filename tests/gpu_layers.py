@@ -156,6 +156,23 @@ SMALL = {
     "group_f32_E16_T4100_d128_k3_f128_g4top2": MoEConfig(
         "group_f32_E16_T4100_d128_k3_f128_g4top2", T=4100, d=128, E=16, k=3, f=128,
         dtype="f32", router=ROUTER_GROUP_LIMITED, n_group=4, topk_group=2, seed=46),
+    # small-batch gate with W_g and the tokens' rows in shared memory (d >=
+    # 1024, W_g rows of 16/32/64 bytes): bf16 E = 16 (4 tokens per CTA, a
+    # ragged last CTA) and E = 32 (2 per CTA, group-limited); fp32 E = 4 (16
+    # tokens per CTA, more than the 8 warps: each warp selects two) and E = 16
+    # (soft gating)
+    "smemgate_E16_T99_d1024_k2_f128": MoEConfig(
+        "smemgate_E16_T99_d1024_k2_f128", T=99, d=1024, E=16, k=2, f=128, dtype="bf16",
+        bias="normal", bias_var=0.5, seed=60),
+    "smemgate_E32_T70_d2048_k4_f128_g8top2": MoEConfig(
+        "smemgate_E32_T70_d2048_k4_f128_g8top2", T=70, d=2048, E=32, k=4, f=128,
+        dtype="bf16", router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=2, seed=61),
+    "smemgate_f32_E4_T37_d1024_k2_f128": MoEConfig(
+        "smemgate_f32_E4_T37_d1024_k2_f128", T=37, d=1024, E=4, k=2, f=128, dtype="f32",
+        pre_k=4, seed=62),
+    "smemgate_f32_E16_T50_d1024_f128_soft": MoEConfig(
+        "smemgate_f32_E16_T50_d1024_f128_soft", T=50, d=1024, E=16, k=16, f=128, dtype="f32",
+        router=ROUTER_SOFT_GUMBEL, tau=1.0, seed=63),
 }
 ALL = dict(SMALL)
 ALL.update(CONFIGS)
