@@ -47,41 +47,105 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 
   const int nv = d / 4;
   const float4* yv = reinterpret_cast<const float4*>(y);
-  // 8 / KMAX float4 columns of each of the k rows in flight per thread: more
-  // CTAs per SM (fewer registers) beat deeper per-thread batches (measured)
-  constexpr int U = 8 / KMAX > 0 ? 8 / KMAX : 1;
-  for (int c0 = tl; c0 < nv; c0 += 128 * U) {
-    float4 rows[U][KMAX];
+  if constexpr (KMAX <= 8) {
+    // 8 / KMAX float4 columns of each of the k rows in flight per thread:
+    // more CTAs per SM (fewer registers) beat deeper per-thread batches
+    // (measured)
+    constexpr int U = 8 / KMAX > 0 ? 8 / KMAX : 1;
+    for (int c0 = tl; c0 < nv; c0 += 128 * U) {
+      float4 rows[U][KMAX];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * 128;
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 128;
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (p[j] >= 0 && c < nv) rows[u][j] = __ldg(yv + static_cast<size_t>(p[j]) * nv + c);
-    }
+        for (int j = 0; j < KMAX; ++j)
+          if (p[j] >= 0 && c < nv) rows[u][j] = __ldg(yv + static_cast<size_t>(p[j]) * nv + c);
+      }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * 128;
-      if (c >= nv) break;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 128;
+        if (c >= nv) break;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (p[j] >= 0) {
-          acc.x = fmaf(wt[j], rows[u][j].x, acc.x);
-          acc.y = fmaf(wt[j], rows[u][j].y, acc.y);
-          acc.z = fmaf(wt[j], rows[u][j].z, acc.z);
-          acc.w = fmaf(wt[j], rows[u][j].w, acc.w);
+        for (int j = 0; j < KMAX; ++j) {
+          if (p[j] >= 0) {
+            acc.x = fmaf(wt[j], rows[u][j].x, acc.x);
+            acc.y = fmaf(wt[j], rows[u][j].y, acc.y);
+            acc.z = fmaf(wt[j], rows[u][j].z, acc.z);
+            acc.w = fmaf(wt[j], rows[u][j].w, acc.w);
+          }
+        }
+        if constexpr (DT == 0) {
+          reinterpret_cast<float4*>(out)[static_cast<size_t>(t) * nv + c] = acc;
+        } else {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+          uint2 uu;
+          uu.x = *reinterpret_cast<const uint32_t*>(&lo);
+          uu.y = *reinterpret_cast<const uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(out)[static_cast<size_t>(t) * nv + c] = uu;
         }
       }
-      if constexpr (DT == 0) {
-        reinterpret_cast<float4*>(out)[static_cast<size_t>(t) * nv + c] = acc;
-      } else {
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 uu;
-        uu.x = *reinterpret_cast<const uint32_t*>(&lo);
-        uu.y = *reinterpret_cast<const uint32_t*>(&hi);
-        reinterpret_cast<uint2*>(out)[static_cast<size_t>(t) * nv + c] = uu;
+    }
+  } else {
+    // k > 8: the rows in batches of 8 (the fp32 sum still runs j = 0, 1, ...,
+    // k-1 in order); all 16 at once took 176 registers, one CTA per SM
+    constexpr int U = 8 / KMAX > 0 ? 8 / KMAX : 1;
+    constexpr int JB = KMAX < 8 ? KMAX : 8;
+    for (int c0 = tl; c0 < nv; c0 += 128 * U) {
+      float4 acc[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll(KMAX > 8 ? 1 : 2)
+      for (int jb = 0; jb < KMAX; jb += JB) {
+        float4 rows[U][JB];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + u * 128;
+#pragma unroll
+          for (int jj = 0; jj < JB; ++jj) {
+            const int j = jb + jj;
+            int pj = -1;
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) pj = (q == j) ? p[q] : pj;
+            if (pj >= 0 && c < nv) rows[u][jj] = __ldg(yv + static_cast<size_t>(pj) * nv + c);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+          for (int jj = 0; jj < JB; ++jj) {
+            const int j = jb + jj;
+            int pj = -1;
+            float wj = 0.f;
+#pragma unroll
+            for (int q = 0; q < KMAX; ++q) {
+              pj = (q == j) ? p[q] : pj;
+              wj = (q == j) ? wt[q] : wj;
+            }
+            if (pj >= 0) {
+              acc[u].x = fmaf(wj, rows[u][jj].x, acc[u].x);
+              acc[u].y = fmaf(wj, rows[u][jj].y, acc[u].y);
+              acc[u].z = fmaf(wj, rows[u][jj].z, acc[u].z);
+              acc[u].w = fmaf(wj, rows[u][jj].w, acc[u].w);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 128;
+        if (c >= nv) break;
+        if constexpr (DT == 0) {
+          reinterpret_cast<float4*>(out)[static_cast<size_t>(t) * nv + c] = acc[u];
+        } else {
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+          uint2 uu;
+          uu.x = *reinterpret_cast<const uint32_t*>(&lo);
+          uu.y = *reinterpret_cast<const uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(out)[static_cast<size_t>(t) * nv + c] = uu;
+        }
       }
     }
   }
