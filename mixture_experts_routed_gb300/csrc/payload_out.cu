@@ -168,57 +168,127 @@ __global__ void __launch_bounds__(256) combine_fp8_kernel(
   const int tl = threadIdx.x & 127;
   const int t = blockIdx.x * 2 + (threadIdx.x >> 7);
   if (t >= T) return;
-  int p[KMAX];
-  float wt[KMAX], sc[KMAX], zr[KMAX];
-  bool bad = false;
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    p[j] = -1;
-    wt[j] = 0.f;
-    sc[j] = 0.f;
-    zr[j] = 0.f;
-    if (j < k) {
-      const int q = __ldg(pos + static_cast<size_t>(t) * k + j);
-      if (q >= 0 && q < R) {
-        p[j] = q;
-        wt[j] = __ldg(w + static_cast<size_t>(t) * k + j);
-        sc[j] = __ldg(ys + q);
-        zr[j] = __ldg(yz + q);
-      } else {
-        bad = true;
-      }
-    }
-  }
-  if (bad && tl == 0) atomicOr(err, kErrBadIndex);
-
   const int nv = d / 16;
   const uint4* qv = reinterpret_cast<const uint4*>(yq);
-  constexpr int U = 8 / KMAX > 0 ? 8 / KMAX : 1;
-  for (int c0 = tl; c0 < nv; c0 += 128 * U) {
-    uint4 rows[U][KMAX];
+  if constexpr (KMAX <= 4) {
+    int p[KMAX];
+    float wt[KMAX], sc[KMAX], zr[KMAX];
+    bool bad = false;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * 128;
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (p[j] >= 0 && c < nv) rows[u][j] = __ldg(qv + static_cast<size_t>(p[j]) * nv + c);
+    for (int j = 0; j < KMAX; ++j) {
+      p[j] = -1;
+      wt[j] = 0.f;
+      sc[j] = 0.f;
+      zr[j] = 0.f;
+      if (j < k) {
+        const int q = __ldg(pos + static_cast<size_t>(t) * k + j);
+        if (q >= 0 && q < R) {
+          p[j] = q;
+          wt[j] = __ldg(w + static_cast<size_t>(t) * k + j);
+          sc[j] = __ldg(ys + q);
+          zr[j] = __ldg(yz + q);
+        } else {
+          bad = true;
+        }
+      }
     }
+    if (bad && tl == 0) atomicOr(err, kErrBadIndex);
+
+    constexpr int U = 8 / KMAX > 0 ? 8 / KMAX : 1;
+    for (int c0 = tl; c0 < nv; c0 += 128 * U) {
+      uint4 rows[U][KMAX];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int c = c0 + u * 128;
-      if (c >= nv) break;
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 128;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (p[j] >= 0 && c < nv) rows[u][j] = __ldg(qv + static_cast<size_t>(p[j]) * nv + c);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int c = c0 + u * 128;
+        if (c >= nv) break;
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (p[j] < 0) continue;
+          const uint32_t wd[4] = {rows[u][j].x, rows[u][j].y, rows[u][j].z, rows[u][j].w};
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(wd[h >> 1] >> (16 * (h & 1))));
+            acc[2 * h] = fmaf(wt[j], fmaf(f.x, sc[j], zr[j]), acc[2 * h]);
+            acc[2 * h + 1] = fmaf(wt[j], fmaf(f.y, sc[j], zr[j]), acc[2 * h + 1]);
+          }
+        }
+        if constexpr (DT == 0) {
+          float4* o = reinterpret_cast<float4*>(out) + (static_cast<size_t>(t) * nv + c) * 4;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        } else {
+          uint4 uu[2];
+          uint32_t* pu = &uu[0].x;
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * h], acc[2 * h + 1]);
+            pu[h] = *reinterpret_cast<const uint32_t*>(&b);
+          }
+          uint4* o = reinterpret_cast<uint4*>(out) + (static_cast<size_t>(t) * nv + c) * 2;
+          o[0] = uu[0];
+          o[1] = uu[1];
+        }
+      }
+    }
+  } else {
+    // k > 4: rows in batches of 4, each batch's position, weight, scale and
+    // zero read per column block (all k of each in registers took ~190
+    // registers at k = 16); the fp32 sum still runs j = 0..k-1 in order
+    bool bad = false;
+    for (int j = 0; j < k; ++j) {
+      const int q = __ldg(pos + static_cast<size_t>(t) * k + j);
+      bad |= !(q >= 0 && q < R);
+    }
+    if (bad && tl == 0) atomicOr(err, kErrBadIndex);
+    constexpr int JB = 4;
+    for (int c = tl; c < nv; c += 128) {
       float acc[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 1
+      for (int jb = 0; jb < k; jb += JB) {
+        int pj[JB];
+        float wj[JB], sj[JB], zj[JB];
+        uint4 rows[JB];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (p[j] < 0) continue;
-        const uint32_t wd[4] = {rows[u][j].x, rows[u][j].y, rows[u][j].z, rows[u][j].w};
+        for (int jj = 0; jj < JB; ++jj) {
+          const int j = jb + jj;
+          pj[jj] = -1;
+          wj[jj] = sj[jj] = zj[jj] = 0.f;
+          if (j < k) {
+            const int q = __ldg(pos + static_cast<size_t>(t) * k + j);
+            if (q >= 0 && q < R) {
+              pj[jj] = q;
+              wj[jj] = __ldg(w + static_cast<size_t>(t) * k + j);
+              sj[jj] = __ldg(ys + q);
+              zj[jj] = __ldg(yz + q);
+            }
+          }
+        }
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(wd[h >> 1] >> (16 * (h & 1))));
-          acc[2 * h] = fmaf(wt[j], fmaf(f.x, sc[j], zr[j]), acc[2 * h]);
-          acc[2 * h + 1] = fmaf(wt[j], fmaf(f.y, sc[j], zr[j]), acc[2 * h + 1]);
+        for (int jj = 0; jj < JB; ++jj)
+          if (pj[jj] >= 0) rows[jj] = __ldg(qv + static_cast<size_t>(pj[jj]) * nv + c);
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj) {
+          if (pj[jj] < 0) continue;
+          const uint32_t wd[4] = {rows[jj].x, rows[jj].y, rows[jj].z, rows[jj].w};
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(wd[h >> 1] >> (16 * (h & 1))));
+            acc[2 * h] = fmaf(wj[jj], fmaf(f.x, sj[jj], zj[jj]), acc[2 * h]);
+            acc[2 * h + 1] = fmaf(wj[jj], fmaf(f.y, sj[jj], zj[jj]), acc[2 * h + 1]);
+          }
         }
       }
       if constexpr (DT == 0) {
