@@ -21,6 +21,8 @@ source pages give, with no blocking, fusion or reordering:
             strategy article, Waved-EP section)
   payload   optional FP8 expert outputs, per-row min/max affine (sync-tax, 3.1)
   combine   out_t = sum_j w_tj y_(t,j)       (sync-tax article, sec. 2.3)
+  backward  gradients of the above for a given dl/dout, flowing only to the
+            chosen experts (DeepSeek-V4 EP article, sec. 2.1; sync-tax, 2.4)
 
 Pins (tests/test_oracle_*.py) tie it to brute force, closed forms, special
 cases and library routines; the FFN/combine absolute values are pinned only by
@@ -29,7 +31,8 @@ those special cases (dense FFN when E = 1, identical experts, linearity).
 from .moe_oracle import (  # noqa: F401
     gate_logits, route, dispatch, quantize_payload_fp8, quantize_output_fp8,
     dequantize_output_fp8, expert_ffn_rows,
-    combine, forward, forward_tokens, inputs_to_numpy, ROUTER_RENORM,
+    combine, forward, forward_tokens, inputs_to_numpy, backward, router_backward,
+    silu_grad, ROUTER_RENORM,
     ROUTER_PREK_SOFTMAX, ROUTER_GROUP_LIMITED, ROUTER_SOFT_GUMBEL,
 )
 from .numerics import (  # noqa: F401

@@ -417,3 +417,120 @@ def forward_tokens(cfg, inp: dict, tokens) -> dict:
     res.update({"L": L, "topk_idx": idx, "topk_w": w, "out": out,
                 "out_rounded": _round_out(cfg, out)})
     return res
+
+
+# ----------------------------------------------------------------------------
+# backward [V4-EP 2.1: in backpropagation the gradient goes back only to the
+# activated experts; SYNC-TAX 2.4: the backward exchange mirrors the
+# dispatch]: gradients of a loss l whose gradient with respect to the layer
+# output is dout = dl/dout. Readings: the expert choice itself is piecewise
+# constant (no gradient through the top-k selection, only through the
+# chosen experts' weights); the Gumbel samples are constants; storage
+# roundings (H in the layer dtype, the output) pass the gradient unchanged,
+# and dW2 uses the stored H, the value the forward multiplied by W2; the FP8
+# payloads have no backward here.
+# ----------------------------------------------------------------------------
+def silu_grad(z: np.ndarray) -> np.ndarray:
+    """d SiLU / dz = s (1 + z (1 - s)) with s = 1 / (1 + e^-z)."""
+    with np.errstate(over="ignore"):
+        s = 1.0 / (1.0 + np.exp(-z))
+    return s * (1.0 + z * (1.0 - s))
+
+
+def router_backward(L: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, dw: np.ndarray,
+                    router: int = ROUTER_RENORM, pre_k: int = 8, tau: float = 1.0) -> np.ndarray:
+    """dl/dL [T, E] from dl/dw [T, k] (dw[t, j] for the weight in slot j).
+
+    * ROUTER_RENORM and ROUTER_GROUP_LIMITED: the weights are a softmax over
+      the chosen set S (w_j = e^L_j / sum_S e^L_i), so dL_j = w_j (dw_j -
+      sum_i w_i dw_i) for j in S and 0 elsewhere.
+    * ROUTER_PREK_SOFTMAX: q = softmax over the pre_k largest logits P and
+      w_j = q_j for the first k of P, so for i in P dL_i = q_i (g_i -
+      sum_{j<k} dw_j q_j) with g_i = dw_i for the k chosen and 0 for the rest
+      of P; 0 outside P.
+    * ROUTER_SOFT_GUMBEL: w = softmax((L + g) / tau) over all E, slot j =
+      expert j, so dL = (w / tau) (dw - sum_i w_i dw_i)."""
+    L = np.asarray(L, np.float64)
+    T, E = L.shape
+    w = np.asarray(topk_w, np.float64)
+    dw = np.asarray(dw, np.float64)
+    idx = np.asarray(topk_idx, np.int64)
+    dL = np.zeros((T, E), dtype=np.float64)
+    rows = np.arange(T)[:, None]
+    if router == ROUTER_SOFT_GUMBEL:
+        s = (w * dw).sum(axis=1, keepdims=True)
+        dL[rows, idx] = w * (dw - s) / float(np.float32(tau))
+        return dL
+    if router == ROUTER_PREK_SOFTMAX:
+        pk = min(pre_k, E)
+        P = np.argsort(-L, axis=1, kind="stable")[:, :pk]
+        q = _softmax_max_subtracted(L[rows, P])
+        k = idx.shape[1]
+        g = np.zeros_like(q)
+        g[:, :k] = dw
+        s = (dw * q[:, :k]).sum(axis=1, keepdims=True)
+        dL[rows, P] = q * (g - s)
+        return dL
+    s = (w * dw).sum(axis=1, keepdims=True)
+    dL[rows, idx] = w * (dw - s)
+    return dL
+
+
+def backward(cfg, inp: dict, fwd: dict, dout, h_storage: str | None = None) -> dict:
+    """Gradients of the layer for dout = dl/dout [T, d]: dx [T, d], dWg [d, E],
+    dbias [E], dW1 [E, d, f], dW2 [E, f, d], and the intermediates dY (per
+    routed row), dw [T, k], dL [T, E]. ``fwd`` is forward(cfg, inp) (its
+    routing, permutation, H and Y); ``h_storage`` (default: the layer's)
+    must match the forward's."""
+    if cfg.payload_fp8 or getattr(cfg, "output_fp8", 0):
+        raise ValueError("the FP8 payloads have no backward")
+    a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
+    x = a["x"]
+    T, k = np.asarray(fwd["topk_idx"]).shape
+    R = T * k
+    pos = np.asarray(fwd["pos"]).reshape(T, k)
+    src = np.asarray(fwd["src"])
+    offsets = np.asarray(fwd["offsets"])
+    w = np.asarray(fwd["topk_w"], np.float64)
+    Y = np.asarray(fwd["Y"], np.float64)
+    g = np.asarray(dout, np.float64) if not hasattr(dout, "detach") else _np64(dout)
+    hs = h_storage or _storage(cfg)
+    # combine: out[t] = sum_j w[t, j] Y[pos[t, j]]
+    dY = np.zeros((R, cfg.d), dtype=np.float64)
+    dw = np.zeros((T, k), dtype=np.float64)
+    for j in range(k):
+        dY[pos[:, j]] = w[:, j:j + 1] * g
+        dw[:, j] = (g * Y[pos[:, j]]).sum(axis=1)
+    # router and gate: L = x W_g + b
+    dL = router_backward(fwd["L"], fwd["topk_idx"], w, dw, cfg.router, cfg.pre_k,
+                         getattr(cfg, "tau", 1.0))
+    Wg = np.asarray(a["Wg"], np.float64)
+    dx = dL @ Wg.T
+    dWg = x.T @ dL
+    dbias = dL.sum(axis=0)
+    # experts: z = x_e W1_e, h = SiLU(z) (stored rounded), y = h W2_e
+    dW1 = np.zeros((cfg.E, cfg.d, cfg.f), dtype=np.float64)
+    dW2 = np.zeros((cfg.E, cfg.f, cfg.d), dtype=np.float64)
+    dXp = np.zeros((R, cfg.d), dtype=np.float64)
+    for e in range(cfg.E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue                  # no rows: the expert's gradients are 0
+        xe = x[src[lo:hi]]
+        W1e, W2e = _expert(a["W1"], e), _expert(a["W2"], e)
+        z = xe @ W1e
+        h = silu(z)
+        if hs == "bf16":
+            h = round_to_bf16(h)
+        elif hs == "f32":
+            h = round_to_f32(h)
+        dYe = dY[lo:hi]
+        dW2[e] = h.T @ dYe
+        dZ = (dYe @ W2e.T) * silu_grad(z)
+        dW1[e] = xe.T @ dZ
+        dXp[lo:hi] = dZ @ W1e.T
+    # mirror of the dispatch: each routed row's gradient back to its token
+    for j in range(k):
+        dx += dXp[pos[:, j]]
+    return {"dx": dx, "dWg": dWg, "dbias": dbias, "dW1": dW1, "dW2": dW2, "dY": dY, "dw": dw,
+            "dL": dL}
