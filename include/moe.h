@@ -286,6 +286,35 @@ typedef struct moe_forward_views {
 } moe_forward_views_t;
 MOE_API int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* views);
 
+/* ---- backward ------------------------------------------------------------
+ * Gradients of a loss l through one moe_forward call, given dout = dl/dout
+ * [T, d] (the output dtype): in backpropagation the gradient goes back only
+ * to the activated experts (DeepSeek-V4 EP article, section 2.1), along the
+ * mirror of the dispatch (Deepseek-MoE sync-tax article, section 2.4):
+ *   dY[pos(t,j)] = w[t,j] dout[t]           dw[t,j] = <dout[t], Y[pos(t,j)]>
+ *   dL = router Jacobian of dw (softmax over the chosen set; over the pre_k
+ *        set for MOE_ROUTER_PREK_SOFTMAX; over all experts, / tau, for
+ *        soft gating); no gradient flows through the choice itself
+ *   dW_g = x^T dL   db = sum_t dL   dx = dL W_g^T + sum_j dX_perm[pos(t,j)]
+ *   per expert e: Z = X_e W1_e (recomputed), dW2_e = H_e^T dY_e,
+ *   dZ = (dY_e W2_e^T) * SiLU'(Z), dW1_e = X_e^T dZ, dX_perm = dZ W1_e^T
+ * x, W_g, bias, noise, W1, W2: the forward's inputs, unchanged. fwd_ws: the
+ * workspace of that moe_forward call (>= moe_workspace_size bytes; its
+ * routing, permutation, x_perm, H and Y are read, not changed). Outputs,
+ * fp32, overwritten: dx [T, d], dW_g [d, E], dbias [E] (nullable), dW1 [E,
+ * d, f], dW2 [E, f, d]; an expert with no rows gets zero gradients. ws: >=
+ * moe_backward_workspace_size bytes, 256-byte aligned; its first word is
+ * the backward's device error word (moe_get_device_error(ws, ...)). The
+ * FP8 payloads (payload_fp8, output_fp8) have no backward:
+ * MOE_ERR_UNSUPPORTED. Every sum runs in a fixed order (no atomics): the
+ * result is bitwise reproducible. Asynchronous on `stream`. */
+MOE_API size_t moe_backward_workspace_size(const moe_config_t* cfg);
+MOE_API int moe_backward(const moe_config_t* cfg, const void* x, const void* W_g,
+                 const float* bias, const float* noise, const void* W1, const void* W2,
+                 const void* fwd_ws, size_t fwd_ws_bytes, const void* dout, float* dx,
+                 float* dW_g, float* dbias, float* dW1, float* dW2, void* ws,
+                 size_t ws_bytes, void* stream);
+
 /* ---- errors --------------------------------------------------------------
  * moe_get_device_error synchronises `stream`, reads the workspace error
  * word, clears it, and returns MOE_OK, MOE_ERR_BAD_INDEX or MOE_ERR_TIMEOUT

@@ -1,4 +1,4 @@
-"""GB300-native routed mixture-of-experts layer forward.
+"""GB300-native routed mixture-of-experts layer (forward and backward).
 
 The layer (gate -> softmax/top-k router -> dispatch -> grouped expert FFN ->
 combine) runs as hand-written sm_103a CUDA kernels behind the C ABI in
@@ -10,7 +10,7 @@ from .api import (  # noqa: F401
     MoEError, make_config, config_from, workspace_size, scratch_size, alloc_workspace, route,
     dispatch, expert_ffn, combine, quantize_output, combine_fp8, forward, forward_views,
     get_device_error,
-    clear_device_error, kernel_count, check_config,
+    clear_device_error, kernel_count, check_config, backward, backward_workspace_size,
 )
 from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE_TOO_SMALL,

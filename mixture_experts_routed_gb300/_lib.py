@@ -67,6 +67,9 @@ PROTOTYPES = {
     "moe_strerror": (ctypes.c_char_p, [_I]),
     "moe_forward_kernel_count": (_I, [_CFG]),
     "moe_dispatch_noalloc": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_backward_workspace_size": (_SZ, [_CFG]),
+    "moe_backward": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P,
+                          _SZ, _P]),
 }
 
 _lib = None

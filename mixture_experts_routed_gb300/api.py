@@ -17,7 +17,7 @@ from . import _lib as L
 __all__ = ["MoEError", "make_config", "config_from", "workspace_size", "scratch_size",
            "alloc_workspace", "route", "dispatch", "expert_ffn", "combine", "forward",
            "forward_views", "get_device_error", "clear_device_error", "kernel_count",
-           "check_config"]
+           "check_config", "backward", "backward_workspace_size"]
 
 
 class MoEError(RuntimeError):
@@ -86,9 +86,15 @@ def kernel_count(c) -> int:
     return L.load().moe_forward_kernel_count(_cfg(c))
 
 
+def backward_workspace_size(c) -> int:
+    return int(L.load().moe_backward_workspace_size(_cfg(c)))
+
+
 def alloc_workspace(c, kind: str = "forward", device=None) -> torch.Tensor:
-    """Zeroed workspace (so the device error word starts clear)."""
-    n = workspace_size(c) if kind == "forward" else scratch_size(c)
+    """Zeroed workspace (so the device error word starts clear); kind is
+    "forward", "scratch" or "backward"."""
+    n = {"forward": workspace_size, "scratch": scratch_size,
+         "backward": backward_workspace_size}[kind](c)
     if n == 0:
         raise MoEError(L.MOE_ERR_INVALID_ARG, "workspace size")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
@@ -212,6 +218,26 @@ def forward(c, x, Wg, bias, W1, W2, *, ws, out=None, events=None, noise=None, st
                                          len(events), _s(stream))
     _check(st, "moe_forward")
     return out
+
+
+def backward(c, x, Wg, bias, W1, W2, dout, *, fwd_ws, ws, noise=None, stream=None) -> dict:
+    """Gradients of the layer for dout = dl/dout [T, d] after a forward in
+    ``fwd_ws`` on the same inputs: dx [T, d], dWg [d, E], dbias [E], dW1 [E,
+    d, f], dW2 [E, f, d], all fp32. ``ws``: a backward workspace."""
+    cc = config_from(c)
+    dev = x.device
+    g = {"dx": torch.empty((cc.T, cc.d), dtype=torch.float32, device=dev),
+         "dWg": torch.empty((cc.d, cc.E), dtype=torch.float32, device=dev),
+         "dbias": torch.empty((cc.E,), dtype=torch.float32, device=dev),
+         "dW1": torch.empty((cc.E, cc.d, cc.f), dtype=torch.float32, device=dev),
+         "dW2": torch.empty((cc.E, cc.f, cc.d), dtype=torch.float32, device=dev)}
+    st = L.load().moe_backward(
+        ctypes.byref(cc), _p(x), _p(Wg), _p(bias), _p(noise), _p(W1), _p(W2), _p(fwd_ws),
+        fwd_ws.numel() * fwd_ws.element_size(), _p(dout), _p(g["dx"]), _p(g["dWg"]),
+        _p(g["dbias"]), _p(g["dW1"]), _p(g["dW2"]), _p(ws), ws.numel() * ws.element_size(),
+        _s(stream))
+    _check(st, "moe_backward")
+    return g
 
 
 def forward_views(c, ws) -> dict:

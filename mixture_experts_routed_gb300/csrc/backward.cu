@@ -1,0 +1,437 @@
+// backward.cu - kernels of the layer's backward pass (DeepSeek-V4 EP article,
+// section 2.1: in backpropagation the gradient goes back only to the
+// activated experts; Deepseek-MoE sync-tax article, section 2.4: the backward
+// exchange mirrors the dispatch). Given dout = dl/dout:
+//
+//   combine_bwd    dY[pos(t,j)] = w[t,j] dout[t],  dw[t,j] = <dout[t], Y[pos(t,j)]>
+//   router_bwd     dL[t] from dw[t] through the router's softmax Jacobian
+//   gemm_nt        out[r] = A[r] . W[e]^T (row r of expert e's segment; W[e]
+//                  is [N][K] row-major), optionally times SiLU'(Z) in place
+//   gemm_tn        out[e] = A_e^T . B_e over the segment's rows (ragged K)
+//   bias_bwd       db[e] = sum_t dL[t, e]
+//   undispatch     dx[t] = dx_gate[t] + sum_j dX_perm[pos(t,j)]
+//
+// Every sum runs in a fixed order (no atomics on data): the results are
+// bitwise reproducible. The GEMMs are SIMT fp32 FMA (64 x 64 tiles, 4 x 4 per
+// thread): a first correct form; the weight-gradient GEMMs over ragged token
+// segments are the ones to move to the tensor cores next.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+// router modes, as RouterSpec::mode
+constexpr int kRouterModePrek = 1;
+constexpr int kRouterModeSoft = 3;
+
+__device__ __forceinline__ float ld_f32(const float* p, size_t i) { return __ldg(p + i); }
+__device__ __forceinline__ float ld_f32(const __nv_bfloat16* p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+
+// ---------------------------------------------------------------- combine
+// One CTA of 128 threads per token: the k rows of dY and the k dot products
+// (warp butterflies, then the 4 warp partials in warp order).
+template <typename Tout>
+__global__ void __launch_bounds__(128) combine_bwd_kernel(
+    const Tout* __restrict__ dout, const float* __restrict__ y, const int32_t* __restrict__ pos,
+    const float* __restrict__ w, int T, int d, int k, int R, float* __restrict__ dY,
+    float* __restrict__ dw, uint32_t* __restrict__ err, uint32_t* __restrict__ zero, int nzero,
+    int32_t* __restrict__ seg01) {
+  __shared__ float red[4][kMaxFanout];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  if (t == 0) {
+    if (tid < nzero && zero != nullptr) zero[tid] = 0u;
+    if (tid == 0) {
+      seg01[0] = 0;
+      seg01[1] = T;
+    }
+  }
+  for (int j = 0; j < k; ++j) {
+    const int p = __ldg(pos + static_cast<size_t>(t) * k + j);
+    const bool ok = p >= 0 && p < R;
+    if (!ok && tid == 0) atomicOr(err, kErrBadIndex);
+    const float wt = ok ? __ldg(w + static_cast<size_t>(t) * k + j) : 0.f;
+    float part = 0.f;
+    if (ok) {
+      for (int c = tid; c < d; c += 128) {
+        const float g = ld_f32(dout, static_cast<size_t>(t) * d + c);
+        dY[static_cast<size_t>(p) * d + c] = wt * g;
+        part = fmaf(g, __ldg(y + static_cast<size_t>(p) * d + c), part);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) red[wp][j] = part;
+  }
+  __syncthreads();
+  if (tid < k) dw[static_cast<size_t>(t) * k + tid] = ((red[0][tid] + red[1][tid]) + red[2][tid]) +
+                                                       red[3][tid];
+}
+
+// ---------------------------------------------------------------- router
+// One warp per token; lane l owns experts l, l + 32, ... (up to 8 of them).
+constexpr int kRB_NJ = kMaxExperts / 32;
+
+__device__ __forceinline__ bool beats_b(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void __launch_bounds__(256) router_bwd_kernel(
+    const float* __restrict__ L, const int32_t* __restrict__ idx, const float* __restrict__ w,
+    const float* __restrict__ dw, int T, int E, int k, int mode, int pre_k, float tau,
+    float* __restrict__ dL) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* Lt = L + static_cast<size_t>(t) * E;
+  float g[kRB_NJ];
+#pragma unroll
+  for (int jj = 0; jj < kRB_NJ; ++jj) g[jj] = 0.f;
+  if (mode == kRouterModePrek) {
+    // the pre_k largest logits (logit desc, id asc), as the forward chose them
+    float v[kRB_NJ];
+    bool taken[kRB_NJ];
+#pragma unroll
+    for (int jj = 0; jj < kRB_NJ; ++jj) {
+      const int e = lane + 32 * jj;
+      v[jj] = e < E ? Lt[e] : -INFINITY;
+      taken[jj] = e >= E;
+    }
+    const int pk = min(pre_k, E);
+    float pv[kMaxTopK];
+    int pi[kMaxTopK];
+    for (int r = 0; r < pk; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int jj = 0; jj < kRB_NJ; ++jj)
+        if (!taken[jj] && beats_b(v[jj], lane + 32 * jj, bv, bi)) {
+          bv = v[jj];
+          bi = lane + 32 * jj;
+        }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (beats_b(ov, oi, bv, bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < kRB_NJ; ++jj)
+        if (lane + 32 * jj == bi) taken[jj] = true;
+      pv[r] = bv;
+      pi[r] = bi;
+    }
+    // q = softmax over the pre_k; w_j = q_j for the first k
+    const float m = pv[0];
+    float q[kMaxTopK], den = 0.f;
+    for (int r = 0; r < pk; ++r) {
+      q[r] = expf(pv[r] - m);
+      den += q[r];
+    }
+    float s = 0.f;
+    for (int r = 0; r < pk; ++r) {
+      q[r] = q[r] / den;
+      if (r < k) s = fmaf(__ldg(dw + static_cast<size_t>(t) * k + r), q[r], s);
+    }
+    for (int r = 0; r < pk; ++r) {
+      const float gr = r < k ? __ldg(dw + static_cast<size_t>(t) * k + r) : 0.f;
+      const float val = q[r] * (gr - s);
+#pragma unroll
+      for (int jj = 0; jj < kRB_NJ; ++jj)
+        if (lane + 32 * jj == pi[r]) g[jj] = val;
+    }
+  } else {
+    // renormalised / group-limited: softmax over the chosen set; soft
+    // gating: over all experts (slot j = expert j), divided by tau
+    float s = 0.f;
+    for (int j = 0; j < k; ++j)
+      s = fmaf(__ldg(w + static_cast<size_t>(t) * k + j), __ldg(dw + static_cast<size_t>(t) * k + j),
+               s);
+    const float inv_tau = mode == kRouterModeSoft ? 1.f / tau : 1.f;
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + static_cast<size_t>(t) * k + j);
+      const float val = __ldg(w + static_cast<size_t>(t) * k + j) *
+                        (__ldg(dw + static_cast<size_t>(t) * k + j) - s) * inv_tau;
+#pragma unroll
+      for (int jj = 0; jj < kRB_NJ; ++jj)
+        if (lane + 32 * jj == e) g[jj] = val;
+    }
+  }
+#pragma unroll
+  for (int jj = 0; jj < kRB_NJ; ++jj) {
+    const int e = lane + 32 * jj;
+    if (e < E) dL[static_cast<size_t>(t) * E + e] = g[jj];
+  }
+}
+
+// ---------------------------------------------------------------- GEMMs
+constexpr int BM = 64, BN = 64, BK = 16;
+
+// m-tile index -> (expert, rows) over the segments (as the forward's SIMT
+// GEMM); returns -1 for no tile, -2 for bad offsets
+__device__ __forceinline__ int find_tile(const int32_t* offsets, int E, int R, int mt, int* r0,
+                                         int* r1, int* lo_out) {
+  if (offsets[0] != 0) return -2;
+  for (int e = 0; e < E; ++e) {
+    const int lo = offsets[e], hi = offsets[e + 1];
+    if (hi < lo || hi > R) return -2;
+    const int tiles = (hi - lo + BM - 1) / BM;
+    if (mt < tiles) {
+      *r0 = lo + mt * BM;
+      *r1 = min(*r0 + BM, hi);
+      *lo_out = lo;
+      return e;
+    }
+    mt -= tiles;
+  }
+  return -1;
+}
+
+// out[r, n] = sum_k A[r, k] W[e][n][k] for the rows r of expert e's segment;
+// A fp32 [R, K]; W [E][N][K] (TW). SILU: out holds Z on entry and gets
+// acc * SiLU'(Z) (each element read and written by the same thread).
+template <typename TW, bool SILU>
+__global__ void __launch_bounds__(256) gemm_nt_kernel(const float* __restrict__ A,
+                                                      const TW* __restrict__ W, int E, int R,
+                                                      int K, int N,
+                                                      const int32_t* __restrict__ offsets,
+                                                      float* __restrict__ out,
+                                                      uint32_t* __restrict__ err) {
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Ws[BK][BN + 4];
+  __shared__ int s_e, s_r0, s_r1;
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    int r0 = 0, r1 = 0, lo = 0;
+    const int e = find_tile(offsets, E, R, blockIdx.x, &r0, &r1, &lo);
+    if (e == -2 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(err, kErrBadIndex);
+    s_e = e;
+    s_r0 = r0;
+    s_r1 = r1;
+  }
+  __syncthreads();
+  const int e = s_e;
+  if (e < 0) return;
+  const int row0 = s_r0, nrows = s_r1 - s_r0, n0 = blockIdx.y * BN;
+  const float* Ae = A + static_cast<size_t>(row0) * K;
+  const TW* We = W + static_cast<size_t>(e) * N * K;
+  const int tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += BK) {
+    for (int q = tid; q < BM * BK; q += 256) {
+      const int r = q / BK, kk = q % BK;
+      As[kk][r] = (r < nrows && k0 + kk < K) ? __ldg(Ae + static_cast<size_t>(r) * K + k0 + kk)
+                                               : 0.f;
+    }
+    for (int q = tid; q < BN * BK; q += 256) {
+      const int n = q / BK, kk = q % BK;
+      Ws[kk][n] = (n0 + n < N && k0 + kk < K)
+                      ? ld_f32(We, static_cast<size_t>(n0 + n) * K + k0 + kk)
+                      : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Ws[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = ty * 4 + i;
+    if (r >= nrows) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= N) continue;
+      float* o = out + static_cast<size_t>(row0 + r) * N + n;
+      float v = acc[i][j];
+      if (SILU) {
+        const float z = *o;
+        const float sg = 1.f / (1.f + expf(-z));
+        v *= sg * (1.f + z * (1.f - sg));
+      }
+      *o = v;
+    }
+  }
+}
+
+// out[e][m][n] = sum over the rows r of expert e's segment of A[a(r)][m] B[r][n]
+// (a(r) = r, or r - offsets[e] when A is shared by every expert); A [*, M]
+// (TA), B fp32 [R, N]; out [E][M][N] fp32. An expert with no rows gets zeros.
+template <typename TA>
+__global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, int a_shared,
+                                                      const float* __restrict__ B, int R, int M,
+                                                      int N, const int32_t* __restrict__ offsets,
+                                                      float* __restrict__ out,
+                                                      uint32_t* __restrict__ err) {
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs[BK][BN + 4];
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, e = blockIdx.z;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  int lo = __ldg(offsets + e), hi = __ldg(offsets + e + 1);
+  if (lo < 0 || hi < lo || hi > R) {
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(err, kErrBadIndex);
+    lo = hi = 0;
+  }
+  const int abase = a_shared ? lo : 0;
+  const int tx = tid & 15, ty = tid >> 4;
+  float acc[4][4] = {};
+  for (int r0 = lo; r0 < hi; r0 += BK) {
+    for (int q = tid; q < BK * BM; q += 256) {
+      const int kk = q / BM, m = q % BM;
+      As[kk][m] = (r0 + kk < hi && m0 + m < M)
+                      ? ld_f32(A, static_cast<size_t>(r0 + kk - abase) * M + m0 + m)
+                      : 0.f;
+    }
+    for (int q = tid; q < BK * BN; q += 256) {
+      const int kk = q / BN, n = q % BN;
+      Bs[kk][n] = (r0 + kk < hi && n0 + n < N) ? __ldg(B + static_cast<size_t>(r0 + kk) * N + n0 + n)
+                                              : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* oe = out + static_cast<size_t>(e) * M * N;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < N) oe[static_cast<size_t>(m) * N + n] = acc[i][j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- bias, dx
+// db[e] = sum_t dL[t, e]: one thread per expert, t ascending.
+__global__ void __launch_bounds__(256) bias_bwd_kernel(const float* __restrict__ dL, int T, int E,
+                                                       float* __restrict__ db) {
+  pdl_wait();
+  pdl_trigger();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float s = 0.f;
+    for (int t = 0; t < T; ++t) s += __ldg(dL + static_cast<size_t>(t) * E + e);
+    db[e] = s;
+  }
+}
+
+// dx[t] = dx_gate[t] + sum_j dX_perm[pos(t, j)], j ascending; 128 threads per token.
+__global__ void __launch_bounds__(128) undispatch_kernel(const float* __restrict__ dxg,
+                                                         const float* __restrict__ dxp,
+                                                         const int32_t* __restrict__ pos, int T,
+                                                         int d, int k, int R,
+                                                         float* __restrict__ dx) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  for (int c = threadIdx.x; c < d; c += 128) {
+    float v = __ldg(dxg + static_cast<size_t>(t) * d + c);
+    for (int j = 0; j < k; ++j) {
+      const int p = __ldg(pos + static_cast<size_t>(t) * k + j);
+      if (p >= 0 && p < R) v += __ldg(dxp + static_cast<size_t>(p) * d + c);
+    }
+    dx[static_cast<size_t>(t) * d + c] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
+                               const float* w, int T, int d, int k, int R, float* dY, float* dw,
+                               uint32_t* err, uint32_t* zero, int nzero, int32_t* seg01,
+                               cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (dtype == 0)
+    return launch_pdl(combine_bwd_kernel<float>, dim3(T), dim3(128), 0, s,
+                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, dw, err, zero,
+                      nzero, seg01);
+  return launch_pdl(combine_bwd_kernel<__nv_bfloat16>, dim3(T), dim3(128), 0, s,
+                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, dw, err,
+                    zero, nzero, seg01);
+}
+
+cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
+                              int T, int E, int k, int mode, int pre_k, float tau, float* dL,
+                              cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  return launch_pdl(router_bwd_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, L, idx, w, dw, T, E,
+                    k, mode, pre_k, tau, dL);
+}
+
+cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W, int E, int R,
+                           int K, int N, const int32_t* offsets, float* out, uint32_t* err,
+                           cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  const dim3 grid(ceil_div(R, BM) + E, ceil_div(N, BN)), block(256);
+  if (wdtype == 0)
+    return silu ? launch_pdl(gemm_nt_kernel<float, true>, grid, block, 0, s, A,
+                             static_cast<const float*>(W), E, R, K, N, offsets, out, err)
+                : launch_pdl(gemm_nt_kernel<float, false>, grid, block, 0, s, A,
+                             static_cast<const float*>(W), E, R, K, N, offsets, out, err);
+  return silu ? launch_pdl(gemm_nt_kernel<__nv_bfloat16, true>, grid, block, 0, s, A,
+                           static_cast<const __nv_bfloat16*>(W), E, R, K, N, offsets, out, err)
+              : launch_pdl(gemm_nt_kernel<__nv_bfloat16, false>, grid, block, 0, s, A,
+                           static_cast<const __nv_bfloat16*>(W), E, R, K, N, offsets, out, err);
+}
+
+cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float* B, int E, int R,
+                           int M, int N, const int32_t* offsets, float* out, uint32_t* err,
+                           cudaStream_t s) {
+  if (E == 0) return cudaSuccess;
+  const dim3 grid(ceil_div(M, BM), ceil_div(N, BN), E), block(256);
+  if (adtype == 0)
+    return launch_pdl(gemm_tn_kernel<float>, grid, block, 0, s, static_cast<const float*>(A),
+                      a_shared, B, R, M, N, offsets, out, err);
+  return launch_pdl(gemm_tn_kernel<__nv_bfloat16>, grid, block, 0, s,
+                    static_cast<const __nv_bfloat16*>(A), a_shared, B, R, M, N, offsets, out, err);
+}
+
+cudaError_t launch_bias_bwd(const float* dL, int T, int E, float* db, cudaStream_t s) {
+  return launch_pdl(bias_bwd_kernel, dim3(1), dim3(256), 0, s, dL, T, E, db);
+}
+
+cudaError_t launch_undispatch(const float* dxg, const float* dxp, const int32_t* pos, int T, int d,
+                              int k, int R, float* dx, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  return launch_pdl(undispatch_kernel, dim3(T), dim3(128), 0, s, dxg, dxp, pos, T, d, k, R, dx);
+}
+
+}  // namespace moe

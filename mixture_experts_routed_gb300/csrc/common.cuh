@@ -150,6 +150,33 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
                            int num_sms, cudaStream_t s);
 
+// ---------------------------------------------------------------- backward.cu
+// The backward pass's kernels (dtype 0 = fp32, 1 = bf16 for the tensors the
+// forward takes; every gradient and intermediate is fp32).
+// dY[pos(t,j)] = w[t,j] dout[t]; dw[t,j] = <dout[t], Y[pos(t,j)]>; also
+// zeroes `nzero` words at `zero` and writes seg01 = {0, T}.
+cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
+                               const float* w, int T, int d, int k, int R, float* dY, float* dw,
+                               uint32_t* err, uint32_t* zero, int nzero, int32_t* seg01,
+                               cudaStream_t s);
+// dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec).
+cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
+                              int T, int E, int k, int mode, int pre_k, float tau, float* dL,
+                              cudaStream_t s);
+// out[r] = A[r] . W[e]^T over the segments (W [E][N][K], dtype wdtype);
+// silu: out holds Z and gets acc * SiLU'(Z).
+cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W, int E, int R,
+                           int K, int N, const int32_t* offsets, float* out, uint32_t* err,
+                           cudaStream_t s);
+// out[e] = A_e^T . B_e over each segment's rows (A [*, M] dtype adtype,
+// shared rows when a_shared; B fp32 [R, N]); out [E][M][N].
+cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float* B, int E, int R,
+                           int M, int N, const int32_t* offsets, float* out, uint32_t* err,
+                           cudaStream_t s);
+cudaError_t launch_bias_bwd(const float* dL, int T, int E, float* db, cudaStream_t s);
+cudaError_t launch_undispatch(const float* dxg, const float* dxp, const int32_t* pos, int T, int d,
+                              int k, int R, float* dx, cudaStream_t s);
+
 // ---------------------------------------------------------------- gemm_simt.cu
 // The same grouped GEMM in fp32 FMA for fp32 layers.
 cudaError_t launch_gemm_simt(int epi, const float* A, int a_shared, int R, const float* W, int E,

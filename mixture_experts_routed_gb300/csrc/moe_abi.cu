@@ -252,6 +252,117 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------- backward
+// The backward workspace: an error word and the GEMM tile counters, then the
+// recomputed logits (and the route call's unused top-k), dw, dL, the single
+// segment {0, T} of the gate GEMMs, dY, Z (overwritten by dZ), dX_perm and
+// the gate part of dx; all fp32 but the ints.
+struct BwdLayout {
+  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, total;
+};
+
+BwdLayout bwd_layout_of(const moe_config_t& c) {
+  BwdLayout B;
+  const size_t R = static_cast<size_t>(c.T) * c.k, T = c.T, E = c.E;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    return at;
+  };
+  B.err = take(kAlign);
+  B.L = take(T * E * 4);
+  B.ridx = take(R * 4);
+  B.rw = take(R * 4);
+  B.dw = take(R * 4);
+  B.dL = take(T * E * 4);
+  B.seg01 = take(8);
+  B.dY = take(R * c.d * 4);
+  B.Z = take(R * c.f * 4);
+  B.dXp = take(R * c.d * 4);
+  B.dxg = take(T * c.d * 4);
+  B.total = o;
+  return B;
+}
+
+int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const float* bias,
+                  const float* noise, const void* W1, const void* W2, const void* fwd_ws,
+                  size_t fwd_ws_bytes, const void* dout, float* dx, float* dWg, float* dbias,
+                  float* dW1, float* dW2, void* bws, size_t bws_bytes, void* stream) {
+  int st = check_cfg(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config_t& c = *cfg;
+  if (c.payload_fp8 || c.output_fp8) return MOE_ERR_UNSUPPORTED;
+  if (!ok_ptr(x) || Wg == nullptr || !ok_ptr(W1) || !ok_ptr(W2) || fwd_ws == nullptr ||
+      !aligned(fwd_ws, kAlign) || dout == nullptr || dx == nullptr || dWg == nullptr ||
+      dW1 == nullptr || dW2 == nullptr || bws == nullptr || !aligned(bws, kAlign) ||
+      (soft(c) && c.T > 0 && noise == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_of(c);
+  const BwdLayout B = bwd_layout_of(c);
+  if (fwd_ws_bytes < L.total || bws_bytes < B.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = as_stream(stream);
+  const int T = c.T, d = c.d, E = c.E, k = c.k, f = c.f, R = c.T * c.k;
+  void* fws = const_cast<void*>(fwd_ws);
+  const int32_t* idx = at<int32_t>(fws, L.topk_idx);
+  const float* w = at<float>(fws, L.topk_w);
+  const int32_t* offsets = at<int32_t>(fws, L.offsets);
+  const int32_t* pos = at<int32_t>(fws, L.pos);
+  const void* x_perm = soft(c) ? x : at<void>(fws, L.x_perm);
+  const void* h = at<void>(fws, L.h);
+  const float* y = at<float>(fws, L.y);
+  uint32_t* err = at<uint32_t>(bws, B.err);
+  float* Lr = at<float>(bws, B.L);
+  float* dw = at<float>(bws, B.dw);
+  float* dL = at<float>(bws, B.dL);
+  int32_t* seg01 = at<int32_t>(bws, B.seg01);
+  float* dY = at<float>(bws, B.dY);
+  float* Z = at<float>(bws, B.Z);
+  float* dXp = at<float>(bws, B.dXp);
+  float* dxg = at<float>(bws, B.dxg);
+  const int dt = c.dtype;
+  if (T == 0) {
+    // no tokens: every gradient is zero
+    cudaError_t e = cudaMemsetAsync(dWg, 0, static_cast<size_t>(d) * E * 4, s);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, static_cast<size_t>(E) * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW1, 0, static_cast<size_t>(E) * d * f * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW2, 0, static_cast<size_t>(E) * f * d * 4, s);
+    return status_of(e);
+  }
+  // the logits, recomputed by the forward's own gate kernel (bit for bit)
+  if ((st = run_route(c, x, Wg, bias, noise, at<int32_t>(bws, B.ridx), at<float>(bws, B.rw), Lr,
+                      err, s)) != MOE_OK)
+    return st;
+  cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, dY, dw, err,
+                                     at<uint32_t>(bws, kGemmCounterOffset), kNumGemmCounters,
+                                     seg01, s);
+  if (e == cudaSuccess) e = launch_router_bwd(Lr, idx, w, dw, T, E, k, c.router, c.pre_k, c.tau, dL, s);
+  // gate: dx_gate = dL W_g^T ([T, E] x [E, d]), dW_g = x^T dL, db = sum_t dL
+  if (e == cudaSuccess) e = launch_gemm_nt(dt, false, dL, Wg, 1, T, E, d, seg01, dxg, err, s);
+  if (e == cudaSuccess) e = launch_gemm_tn(dt, x, 0, dL, 1, T, d, E, seg01, dWg, err, s);
+  if (e == cudaSuccess && dbias != nullptr) e = launch_bias_bwd(dL, T, E, dbias, s);
+  // experts: Z = X_e W1_e again (fp32), dZ = (dY W2_e^T) * SiLU'(Z) in place,
+  // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T
+  if (e == cudaSuccess) {
+    if (dt == MOE_DTYPE_F32) {
+      e = launch_gemm_simt(1, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
+                           static_cast<const float*>(W1), E, d, f, offsets, Z, err, s);
+    } else {
+      const int sms = num_sms();
+      if (sms <= 0) return MOE_ERR_LAUNCH;
+      e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
+                         nullptr, Z, err, at<uint32_t>(bws, kGemmCounterOffset), sms, s);
+    }
+  }
+  if (e == cudaSuccess) e = launch_gemm_nt(dt, true, dY, W2, E, R, d, f, offsets, Z, err, s);
+  if (e == cudaSuccess) e = launch_gemm_tn(dt, h, 0, dY, E, R, f, d, offsets, dW2, err, s);
+  if (e == cudaSuccess)
+    e = launch_gemm_tn(dt, x_perm, soft(c) ? 1 : 0, Z, E, R, d, f, offsets, dW1, err, s);
+  if (e == cudaSuccess) e = launch_gemm_nt(dt, false, Z, W1, E, R, f, d, offsets, dXp, err, s);
+  if (e == cudaSuccess) e = launch_undispatch(dxg, dXp, pos, T, d, k, R, dx, s);
+  return status_of(e);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -428,6 +539,19 @@ const char* moe_strerror(int status) {
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     default: return "unknown status";
   }
+}
+
+size_t moe_backward_workspace_size(const moe_config_t* cfg) {
+  if (check_cfg(cfg) != MOE_OK) return 0;
+  return bwd_layout_of(*cfg).total;
+}
+
+int moe_backward(const moe_config_t* cfg, const void* x, const void* W_g, const float* bias,
+                 const float* noise, const void* W1, const void* W2, const void* fwd_ws,
+                 size_t fwd_ws_bytes, const void* dout, float* dx, float* dW_g, float* dbias,
+                 float* dW1, float* dW2, void* ws, size_t ws_bytes, void* stream) {
+  return backward_impl(cfg, x, W_g, bias, noise, W1, W2, fwd_ws, fwd_ws_bytes, dout, dx, dW_g,
+                       dbias, dW1, dW2, ws, ws_bytes, stream);
 }
 
 int moe_forward_kernel_count(const moe_config_t* cfg) {

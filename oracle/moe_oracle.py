@@ -534,3 +534,40 @@ def backward(cfg, inp: dict, fwd: dict, dout, h_storage: str | None = None) -> d
         dx += dXp[pos[:, j]]
     return {"dx": dx, "dWg": dWg, "dbias": dbias, "dW1": dW1, "dW2": dW2, "dY": dY, "dw": dw,
             "dL": dL}
+
+
+def backward_tokens(cfg, inp: dict, dout, tokens, h_storage: str | None = None) -> dict:
+    """dx and dL for a subset of tokens only (a token's input gradient depends
+    only on its own routing, expert rows and dout row). Used for sampled
+    checks on the large layers. ``dout``: [T, d] (all tokens) or [n, d]."""
+    if cfg.payload_fp8 or getattr(cfg, "output_fp8", 0):
+        raise ValueError("the FP8 payloads have no backward")
+    a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
+    tokens = np.asarray(tokens, dtype=np.int64)
+    x = a["x"][tokens]
+    g = np.asarray(dout, np.float64) if not hasattr(dout, "detach") else _np64(dout)
+    if g.shape[0] != len(tokens):
+        g = g[tokens]
+    L = gate_logits(x, a["Wg"], a["bias"])
+    idx, w = route(L, cfg.k, cfg.router, *_router_args(cfg, a, tokens))
+    hs = h_storage or _storage(cfg)
+    n, k = idx.shape
+    dw = np.zeros((n, k))
+    dXp_slot = np.zeros((n, k, cfg.d))
+    for e in np.unique(idx):
+        tt, jj = np.nonzero(idx == e)
+        W1e, W2e = _expert(a["W1"], int(e)), _expert(a["W2"], int(e))
+        z = x[tt] @ W1e
+        h = silu(z)
+        if hs == "bf16":
+            h = round_to_bf16(h)
+        elif hs == "f32":
+            h = round_to_f32(h)
+        y = h @ W2e
+        dw[tt, jj] = (g[tt] * y).sum(axis=1)
+        dY = w[tt, jj][:, None] * g[tt]
+        dZ = (dY @ W2e.T) * silu_grad(z)
+        dXp_slot[tt, jj] = dZ @ W1e.T
+    dL = router_backward(L, idx, w, dw, cfg.router, cfg.pre_k, getattr(cfg, "tau", 1.0))
+    dx = dL @ np.asarray(a["Wg"], np.float64).T + dXp_slot.sum(axis=1)
+    return {"tokens": tokens, "topk_idx": idx, "dL": dL, "dx": dx}

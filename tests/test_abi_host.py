@@ -223,6 +223,32 @@ def test_stage_argument_errors(lib):
     assert lib.moe_route(ctypes.byref(c0), None, None, None, None, None, None, None, None) == L.MOE_OK
 
 
+def test_backward_argument_errors(lib):
+    c = cfg(T=1024, d=4096, E=8, k=2, f=11008)
+    ws = lib.moe_workspace_size(ctypes.byref(c))
+    bws = lib.moe_backward_workspace_size(ctypes.byref(c))
+    R = 1024 * 2
+    # dY, Z/dZ, dX_perm (fp32 per routed row) and the gate part of dx
+    assert bws >= R * 4096 * 4 * 2 + R * 11008 * 4 + 1024 * 4096 * 4
+    args = lambda cc, fws, b: (ctypes.byref(cc), FAKE, FAKE, None, None, FAKE, FAKE, FAKE, fws,
+                               FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, b, None)
+    assert lib.moe_backward(*args(c, ws - 1, bws)) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert lib.moe_backward(*args(c, ws, bws - 1)) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    bad = list(args(c, ws, bws))
+    bad[9] = None                                     # no dout
+    assert lib.moe_backward(*bad) == L.MOE_ERR_INVALID_ARG
+    bad = list(args(c, ws, bws))
+    bad[7] = FAKE_ODD                                 # forward workspace misaligned
+    assert lib.moe_backward(*bad) == L.MOE_ERR_INVALID_ARG
+    # the FP8 payloads have no backward
+    for c8 in (cfg(T=1024, d=4096, E=8, k=2, f=11008, payload_fp8=1),
+               cfg(T=1024, d=4096, E=8, k=2, f=11008, output_fp8=1)):
+        assert lib.moe_backward(*args(c8, 1 << 40, 1 << 40)) == L.MOE_ERR_UNSUPPORTED
+    # soft gating needs the Gumbel samples
+    cs = cfg(T=16, E=8, k=8, router=3, tau=1.0)
+    assert lib.moe_backward(*args(cs, 1 << 40, 1 << 40)) == L.MOE_ERR_INVALID_ARG
+
+
 def test_strerror(lib):
     for code in range(-6, 1):
         s = lib.moe_strerror(code).decode()

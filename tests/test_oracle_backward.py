@@ -174,3 +174,14 @@ def test_fp8_payloads_have_no_backward():
     cfg = _cfg(ROUTER_RENORM, payload_fp8=1)
     with pytest.raises(ValueError):
         oracle.backward(cfg, _inputs(cfg, 0), {}, np.zeros((cfg.T, cfg.d)))
+
+
+@pytest.mark.parametrize("router", [ROUTER_RENORM, ROUTER_PREK_SOFTMAX, ROUTER_SOFT_GUMBEL])
+def test_token_subset_equals_the_whole_layer(router):
+    cfg = _cfg(router, T=10, E=6, k=6 if router == ROUTER_SOFT_GUMBEL else 2, pre_k=4)
+    a = _inputs(cfg, 12)
+    dout = np.random.default_rng(13).standard_normal((cfg.T, cfg.d))
+    full = oracle.backward(cfg, a, oracle.forward(cfg, a), dout)
+    sub = oracle.backward_tokens(cfg, a, dout, [7, 2, 5])
+    np.testing.assert_allclose(sub["dx"], full["dx"][[7, 2, 5]], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(sub["dL"], full["dL"][[7, 2, 5]], rtol=1e-12, atol=1e-12)
