@@ -53,6 +53,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=256)
+    p.add_argument("--backward", action="store_true",
+                   help="also time moe_backward (adds a 'backward' object to the line)")
     return p.parse_args()
 
 
@@ -400,6 +402,48 @@ def run_ours(args, cfg):
                    g_host.numel() * g_host.element_size() if g_host is not None else 0),
                "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
 
+    # ---- backward (optional): K steps of moe_backward after the forward above
+    bwd = None
+    if args.backward and not (cfg.payload_fp8 or getattr(cfg, "output_fp8", 0)):
+        bws = moe.alloc_workspace(cfg, "backward")
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(5)
+        dout = torch.randn((cfg.T, cfg.d), generator=gen, device=dev).to(cfg.torch_dtype)
+
+        def bwd_step():
+            moe.backward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], dout,
+                         fwd_ws=ws, ws=bws, noise=inp.get("gumbel"), stream=stream)
+
+        for _ in range(max(1, args.warmup)):
+            bwd_step()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(K):
+            bwd_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        if moe.get_device_error(bws) != moe.MOE_OK:
+            raise RuntimeError("device error in the backward steps")
+        b_ms = a.elapsed_time(b) / K
+        R = cfg.T * cfg.k
+        # fp32 FMA work: dgrad (2 GEMMs) + wgrad (2 GEMMs) of the experts and
+        # the gate's two GEMMs; Z is recomputed on the tensor cores (bf16)
+        simt = 8.0 * R * cfg.d * cfg.f + 4.0 * cfg.T * cfg.d * cfg.E
+        if cfg.dtype == "f32":
+            simt += 2.0 * R * cfg.d * cfg.f
+        # fp32 FMA peak from unit counts: SMs x 128 fp32 lanes x 2 flop x clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        fp32_peak = sms * 128 * 2 * (clk or {}).get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        bwd = {"ms_per_step": b_ms, "tokens_per_s": cfg.T * world / (b_ms / 1e3),
+               "roofline": {"bound": "alu", "achieved": simt / (b_ms / 1e3) / 1e12,
+                            "peak": fp32_peak, "unit": "TFLOP/s",
+                            "frac": simt / (b_ms / 1e3) / 1e12 / fp32_peak,
+                            "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 x max SM clock",
+                            "flops": simt},
+               "note": "fp32 SIMT grouped GEMMs for dgrad and wgrad (first correct form)"}
+
     if dist:
         dist.barrier()
     if rank != 0:
@@ -430,6 +474,8 @@ def run_ours(args, cfg):
                 (work["gemm_w1_silu"][1] + work["gemm_w2"][1]) /
                 ((stage_ms["gemm_w1_silu"] + stage_ms["gemm_w2"]) / 1e3) / 1e12,
             "load": load_stats(counts), "peaks": peaks}
+    if bwd is not None:
+        line["backward"] = bwd
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
