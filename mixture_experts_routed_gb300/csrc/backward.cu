@@ -12,9 +12,8 @@
 //   undispatch     dx[t] = dx_gate[t] + sum_j dX_perm[pos(t,j)]
 //
 // Every sum runs in a fixed order (no atomics on data): the results are
-// bitwise reproducible. The GEMMs are SIMT fp32 FMA (64 x 64 tiles, 4 x 4 per
-// thread): a first correct form; the weight-gradient GEMMs over ragged token
-// segments are the ones to move to the tensor cores next.
+// bitwise reproducible. The GEMMs are SIMT fp32 FMA (128 x 128 tiles, 8 x 8
+// per thread); moving them to the tensor cores (bf16 operands) is next.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -176,10 +175,16 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
 }
 
 // ---------------------------------------------------------------- GEMMs
-constexpr int BM = 64, BN = 64, BK = 16;
+// 128 x 128 CTA tiles, 256 threads with 8 x 8 outputs each: thread (ty, tx)
+// owns rows {4 ty .. 4 ty + 3, 64 + 4 ty .. 64 + 4 ty + 3} and the same
+// columns from tx, so its shared-memory reads are float4s at distinct banks.
+// K steps of 8, the next step's tiles loaded into registers while the
+// current one is multiplied (two shared-memory buffers). 64 x 64 tiles with
+// 4 x 4 per thread reached ~0.28 of the fp32 FMA peak (GB300).
+constexpr int BM = 128, BN = 128, BK = 8;
 
-// m-tile index -> (expert, rows) over the segments (as the forward's SIMT
-// GEMM); returns -1 for no tile, -2 for bad offsets
+// m-tile index -> (expert, rows) over the segments; returns -1 for no tile,
+// -2 for bad offsets
 __device__ __forceinline__ int find_tile(const int32_t* offsets, int E, int R, int mt, int* r0,
                                          int* r1, int* lo_out) {
   if (offsets[0] != 0) return -2;
@@ -198,9 +203,31 @@ __device__ __forceinline__ int find_tile(const int32_t* offsets, int E, int R, i
   return -1;
 }
 
+// acc += As[buf] (BK x 128) ^T . Bs[buf] (BK x 128) for this thread's 8 x 8
+__device__ __forceinline__ void mma_tile(const float (*As)[BM + 4], const float (*Bs)[BN + 4],
+                                         int tx, int ty, float (&acc)[8][8]) {
+#pragma unroll
+  for (int kk = 0; kk < BK; ++kk) {
+    const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][64 + ty * 4]);
+    const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+    const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
+    const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+  }
+}
+
+// the tile row / column of this thread's output i (0..7)
+__device__ __forceinline__ int sub_idx(int t, int i) { return (i < 4 ? 0 : 64) + t * 4 + (i & 3); }
+
 // out[r, n] = sum_k A[r, k] W[e][n][k] for the rows r of expert e's segment;
 // A fp32 [R, K]; W [E][N][K] (TW). SILU: out holds Z on entry and gets
 // acc * SiLU'(Z) (each element read and written by the same thread).
+// Loads: thread q takes row q / 2 of the A and W tiles, k half (q & 1) * 4.
 template <typename TW, bool SILU>
 __global__ void __launch_bounds__(256) gemm_nt_kernel(const float* __restrict__ A,
                                                       const TW* __restrict__ W, int E, int R,
@@ -208,8 +235,8 @@ __global__ void __launch_bounds__(256) gemm_nt_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ offsets,
                                                       float* __restrict__ out,
                                                       uint32_t* __restrict__ err) {
-  __shared__ float As[BK][BM + 4];
-  __shared__ float Ws[BK][BN + 4];
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Ws[2][BK][BN + 4];
   __shared__ int s_e, s_r0, s_r1;
   pdl_wait();
   pdl_trigger();
@@ -229,41 +256,43 @@ __global__ void __launch_bounds__(256) gemm_nt_kernel(const float* __restrict__ 
   const float* Ae = A + static_cast<size_t>(row0) * K;
   const TW* We = W + static_cast<size_t>(e) * N * K;
   const int tx = tid & 15, ty = tid >> 4;
-  float acc[4][4] = {};
+  const int lr = tid >> 1, lk = (tid & 1) * 4;
+  float ra[4], rw[4];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int kk = k0 + lk + u;
+      ra[u] = (lr < nrows && kk < K) ? __ldg(Ae + static_cast<size_t>(lr) * K + kk) : 0.f;
+      rw[u] = (n0 + lr < N && kk < K) ? ld_f32(We, static_cast<size_t>(n0 + lr) * K + kk) : 0.f;
+    }
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      As[buf][lk + u][lr] = ra[u];
+      Ws[buf][lk + u][lr] = rw[u];
+    }
+  };
+  float acc[8][8] = {};
+  load(0);
+  store(0);
+  __syncthreads();
+  int buf = 0;
   for (int k0 = 0; k0 < K; k0 += BK) {
-    for (int q = tid; q < BM * BK; q += 256) {
-      const int r = q / BK, kk = q % BK;
-      As[kk][r] = (r < nrows && k0 + kk < K) ? __ldg(Ae + static_cast<size_t>(r) * K + k0 + kk)
-                                               : 0.f;
-    }
-    for (int q = tid; q < BN * BK; q += 256) {
-      const int n = q / BK, kk = q % BK;
-      Ws[kk][n] = (n0 + n < N && k0 + kk < K)
-                      ? ld_f32(We, static_cast<size_t>(n0 + n) * K + k0 + kk)
-                      : 0.f;
-    }
+    const bool more = k0 + BK < K;
+    if (more) load(k0 + BK);
+    mma_tile(As[buf], Ws[buf], tx, ty, acc);
+    if (more) store(buf ^ 1);
     __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < BK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Ws[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
+    buf ^= 1;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int r = sub_idx(ty, i);
     if (r >= nrows) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + sub_idx(tx, j);
       if (n >= N) continue;
       float* o = out + static_cast<size_t>(row0 + r) * N + n;
       float v = acc[i][j];
@@ -280,14 +309,15 @@ __global__ void __launch_bounds__(256) gemm_nt_kernel(const float* __restrict__ 
 // out[e][m][n] = sum over the rows r of expert e's segment of A[a(r)][m] B[r][n]
 // (a(r) = r, or r - offsets[e] when A is shared by every expert); A [*, M]
 // (TA), B fp32 [R, N]; out [E][M][N] fp32. An expert with no rows gets zeros.
+// Loads: thread q takes k row q / 32 of the tiles, columns (q & 31) * 4 ..+3.
 template <typename TA>
 __global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, int a_shared,
                                                       const float* __restrict__ B, int R, int M,
                                                       int N, const int32_t* __restrict__ offsets,
                                                       float* __restrict__ out,
                                                       uint32_t* __restrict__ err) {
-  __shared__ float As[BK][BM + 4];
-  __shared__ float Bs[BK][BN + 4];
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, e = blockIdx.z;
@@ -299,42 +329,45 @@ __global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, 
   }
   const int abase = a_shared ? lo : 0;
   const int tx = tid & 15, ty = tid >> 4;
-  float acc[4][4] = {};
-  for (int r0 = lo; r0 < hi; r0 += BK) {
-    for (int q = tid; q < BK * BM; q += 256) {
-      const int kk = q / BM, m = q % BM;
-      As[kk][m] = (r0 + kk < hi && m0 + m < M)
-                      ? ld_f32(A, static_cast<size_t>(r0 + kk - abase) * M + m0 + m)
-                      : 0.f;
+  const int lkr = tid >> 5, lc = (tid & 31) * 4;
+  float ra[4], rb[4];
+  auto load = [&](int r0) {
+    const int r = r0 + lkr;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      ra[u] = (r < hi && m0 + lc + u < M) ? ld_f32(A, static_cast<size_t>(r - abase) * M + m0 + lc + u)
+                                          : 0.f;
+      rb[u] = (r < hi && n0 + lc + u < N) ? __ldg(B + static_cast<size_t>(r) * N + n0 + lc + u)
+                                          : 0.f;
     }
-    for (int q = tid; q < BK * BN; q += 256) {
-      const int kk = q / BN, n = q % BN;
-      Bs[kk][n] = (r0 + kk < hi && n0 + n < N) ? __ldg(B + static_cast<size_t>(r0 + kk) * N + n0 + n)
-                                              : 0.f;
-    }
+  };
+  auto store = [&](int buf) {
+    *reinterpret_cast<float4*>(&As[buf][lkr][lc]) = make_float4(ra[0], ra[1], ra[2], ra[3]);
+    *reinterpret_cast<float4*>(&Bs[buf][lkr][lc]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
+  };
+  float acc[8][8] = {};
+  if (lo < hi) {
+    load(lo);
+    store(0);
     __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < BK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    int buf = 0;
+    for (int r0 = lo; r0 < hi; r0 += BK) {
+      const bool more = r0 + BK < hi;
+      if (more) load(r0 + BK);
+      mma_tile(As[buf], Bs[buf], tx, ty, acc);
+      if (more) store(buf ^ 1);
+      __syncthreads();
+      buf ^= 1;
     }
-    __syncthreads();
   }
   float* oe = out + static_cast<size_t>(e) * M * N;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + sub_idx(ty, i);
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + sub_idx(tx, j);
       if (n < N) oe[static_cast<size_t>(m) * N + n] = acc[i][j];
     }
   }
