@@ -428,11 +428,16 @@ def run_ours(args, cfg):
             raise RuntimeError("device error in the backward steps")
         b_ms = a.elapsed_time(b) / K
         R = cfg.T * cfg.k
-        # fp32 FMA work: dgrad (2 GEMMs) + wgrad (2 GEMMs) of the experts and
-        # the gate's two GEMMs; Z is recomputed on the tensor cores (bf16)
-        simt = 8.0 * R * cfg.d * cfg.f + 4.0 * cfg.T * cfg.d * cfg.E
+        # fp32 FMA work: the experts' weight gradients (2 GEMMs) and the
+        # gate's two GEMMs; bf16 layers run Z and the two dgrad GEMMs (K
+        # doubled by the hi/lo operand split) on the tensor cores, fp32
+        # layers in fp32 FMA as well
+        simt = 4.0 * R * cfg.d * cfg.f + 4.0 * cfg.T * cfg.d * cfg.E
+        tensor = 0.0
         if cfg.dtype == "f32":
-            simt += 2.0 * R * cfg.d * cfg.f
+            simt += 6.0 * R * cfg.d * cfg.f
+        else:
+            tensor = 2.0 * R * cfg.d * cfg.f + 8.0 * R * cfg.d * cfg.f
         # fp32 FMA peak from unit counts: SMs x 128 fp32 lanes x 2 flop x clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         fp32_peak = sms * 128 * 2 * (clk or {}).get("sm_max_mhz", 2070.0) * 1e6 / 1e12
@@ -442,7 +447,10 @@ def run_ours(args, cfg):
                             "frac": simt / (b_ms / 1e3) / 1e12 / fp32_peak,
                             "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 x max SM clock",
                             "flops": simt},
-               "note": "fp32 SIMT grouped GEMMs for dgrad and wgrad (first correct form)"}
+               "tensor_flops": tensor,
+               "note": "achieved = the fp32 FMA work (weight gradients, gate) over the whole "
+                       "backward time (an upper bound on its own time); the tensor-core work "
+                       "(recomputed Z, split-operand dgrad) is tensor_flops"}
 
     if dist:
         dist.barrier()

@@ -14,6 +14,7 @@
 // Every sum runs in a fixed order (no atomics on data): the results are
 // bitwise reproducible. The GEMMs are SIMT fp32 FMA (128 x 128 tiles, 8 x 8
 // per thread); moving them to the tensor cores (bf16 operands) is next.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -38,8 +39,8 @@ template <typename Tout>
 __global__ void __launch_bounds__(128) combine_bwd_kernel(
     const Tout* __restrict__ dout, const float* __restrict__ y, const int32_t* __restrict__ pos,
     const float* __restrict__ w, int T, int d, int k, int R, float* __restrict__ dY,
-    float* __restrict__ dw, uint32_t* __restrict__ err, uint32_t* __restrict__ zero, int nzero,
-    int32_t* __restrict__ seg01) {
+    __nv_bfloat16* __restrict__ dYs, float* __restrict__ dw, uint32_t* __restrict__ err,
+    uint32_t* __restrict__ zero, int nzero, int32_t* __restrict__ seg01) {
   __shared__ float red[4][kMaxFanout];
   pdl_wait();
   pdl_trigger();
@@ -60,7 +61,14 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     if (ok) {
       for (int c = tid; c < d; c += 128) {
         const float g = ld_f32(dout, static_cast<size_t>(t) * d + c);
-        dY[static_cast<size_t>(p) * d + c] = wt * g;
+        const float v = wt * g;
+        dY[static_cast<size_t>(p) * d + c] = v;
+        if (dYs != nullptr) {
+          // bf16 split for the tensor-core dgrad: v = hi + lo to ~2^-17
+          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+          dYs[static_cast<size_t>(p) * 2 * d + c] = hi;
+          dYs[static_cast<size_t>(p) * 2 * d + d + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        }
         part = fmaf(g, __ldg(y + static_cast<size_t>(p) * d + c), part);
       }
     }
@@ -373,6 +381,60 @@ __global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, 
   }
 }
 
+// ---------------------------------------------------------------- tensor-core dgrad
+// The dgrad GEMMs run on the forward's tcgen05 pair GEMM in bf16 with every
+// fp32 operand split in two: v = hi + lo with hi = bf16(v), lo = bf16(v - hi)
+// (a 16-bit significand, error ~2^-17 |v|), A = [hi | lo] along K and B =
+// the transposed weights stacked twice along K, so A . B = hi . W + lo . W
+// with exact products and fp32 accumulation.
+
+// dst[e][c][r] = dst[e][C + c][r] = src[e][r][c]: src [E][Rw][C] -> dst [E][2C][Rw]
+// (32 x 32 tiles through shared memory, both sides coalesced)
+__global__ void __launch_bounds__(256) transpose_stack_kernel(const __nv_bfloat16* __restrict__ src,
+                                                              int Rw, int C,
+                                                              __nv_bfloat16* __restrict__ dst) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  pdl_wait();
+  pdl_trigger();
+  const int e = blockIdx.z, r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const __nv_bfloat16* se = src + static_cast<size_t>(e) * Rw * C;
+  __nv_bfloat16* de = dst + static_cast<size_t>(e) * 2 * C * Rw;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + tx;
+    if (r < Rw && c < C) tile[i][tx] = se[static_cast<size_t>(r) * C + c];
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + tx;
+    if (r < Rw && c < C) {
+      const __nv_bfloat16 v = tile[tx][i];
+      de[static_cast<size_t>(c) * Rw + r] = v;
+      de[static_cast<size_t>(C + c) * Rw + r] = v;
+    }
+  }
+}
+
+// dZ = dH * SiLU'(Z), written over Z (fp32, for the weight gradients) and
+// as the bf16 split [R][2N] (for the dgrad GEMM)
+__global__ void __launch_bounds__(256) silu_bwd_kernel(const float* __restrict__ dH,
+                                                       float* __restrict__ Z, size_t n, int N,
+                                                       __nv_bfloat16* __restrict__ dZs) {
+  pdl_wait();
+  pdl_trigger();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float z = Z[i];
+    const float sg = 1.f / (1.f + expf(-z));
+    const float v = __ldg(dH + i) * (sg * (1.f + z * (1.f - sg)));
+    Z[i] = v;
+    const size_t r = i / N, c = i - r * N;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    dZs[r * 2 * N + c] = hi;
+    dZs[r * 2 * N + N + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
+  }
+}
+
 // ---------------------------------------------------------------- bias, dx
 // db[e] = sum_t dL[t, e]: one thread per expert, t ascending.
 __global__ void __launch_bounds__(256) bias_bwd_kernel(const float* __restrict__ dL, int T, int E,
@@ -408,17 +470,35 @@ __global__ void __launch_bounds__(128) undispatch_kernel(const float* __restrict
 }  // namespace
 
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
-                               const float* w, int T, int d, int k, int R, float* dY, float* dw,
-                               uint32_t* err, uint32_t* zero, int nzero, int32_t* seg01,
-                               cudaStream_t s) {
+                               const float* w, int T, int d, int k, int R, float* dY, void* dYs,
+                               float* dw, uint32_t* err, uint32_t* zero, int nzero,
+                               int32_t* seg01, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(dYs);
   if (dtype == 0)
     return launch_pdl(combine_bwd_kernel<float>, dim3(T), dim3(128), 0, s,
-                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, dw, err, zero,
-                      nzero, seg01);
+                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, ys, dw, err,
+                      zero, nzero, seg01);
   return launch_pdl(combine_bwd_kernel<__nv_bfloat16>, dim3(T), dim3(128), 0, s,
-                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, dw, err,
-                    zero, nzero, seg01);
+                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys, dw,
+                    err, zero, nzero, seg01);
+}
+
+cudaError_t launch_transpose_stack(const void* src, int E, int Rw, int C, void* dst,
+                                   cudaStream_t s) {
+  if (E == 0) return cudaSuccess;
+  const dim3 grid(ceil_div(C, 32), ceil_div(Rw, 32), E), block(256);
+  return launch_pdl(transpose_stack_kernel, grid, block, 0, s,
+                    static_cast<const __nv_bfloat16*>(src), Rw, C,
+                    static_cast<__nv_bfloat16*>(dst));
+}
+
+cudaError_t launch_silu_bwd(const float* dH, float* Z, int R, int N, void* dZs, cudaStream_t s) {
+  const size_t n = static_cast<size_t>(R) * N;
+  if (n == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 152 * 16));
+  return launch_pdl(silu_bwd_kernel, dim3(blocks), dim3(256), 0, s, dH, Z, n, N,
+                    static_cast<__nv_bfloat16*>(dZs));
 }
 
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,

@@ -153,12 +153,19 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 // ---------------------------------------------------------------- backward.cu
 // The backward pass's kernels (dtype 0 = fp32, 1 = bf16 for the tensors the
 // forward takes; every gradient and intermediate is fp32).
-// dY[pos(t,j)] = w[t,j] dout[t]; dw[t,j] = <dout[t], Y[pos(t,j)]>; also
-// zeroes `nzero` words at `zero` and writes seg01 = {0, T}.
+// dY[pos(t,j)] = w[t,j] dout[t] (and, when dYs is non-null, its bf16 split
+// [R][2d] = [hi | lo]); dw[t,j] = <dout[t], Y[pos(t,j)]>; also zeroes `nzero`
+// words at `zero` and writes seg01 = {0, T}.
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
-                               const float* w, int T, int d, int k, int R, float* dY, float* dw,
-                               uint32_t* err, uint32_t* zero, int nzero, int32_t* seg01,
-                               cudaStream_t s);
+                               const float* w, int T, int d, int k, int R, float* dY, void* dYs,
+                               float* dw, uint32_t* err, uint32_t* zero, int nzero,
+                               int32_t* seg01, cudaStream_t s);
+// bf16 src [E][Rw][C] -> dst [E][2C][Rw], the transpose written twice along
+// its first axis (the B operand of a split-operand dgrad GEMM).
+cudaError_t launch_transpose_stack(const void* src, int E, int Rw, int C, void* dst,
+                                   cudaStream_t s);
+// dZ = dH * SiLU'(Z) over Z [R, N] (fp32) and as the bf16 split [R][2N].
+cudaError_t launch_silu_bwd(const float* dH, float* Z, int R, int N, void* dZs, cudaStream_t s);
 // dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec).
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
                               int T, int E, int k, int mode, int pre_k, float tau, float* dL,

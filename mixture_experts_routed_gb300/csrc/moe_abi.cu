@@ -256,9 +256,11 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // The backward workspace: an error word and the GEMM tile counters, then the
 // recomputed logits (and the route call's unused top-k), dw, dL, the single
 // segment {0, T} of the gate GEMMs, dY, Z (overwritten by dZ), dX_perm and
-// the gate part of dx; all fp32 but the ints.
+// the gate part of dx, all fp32 but the ints; bf16 layers add the operands
+// of the tensor-core dgrad: the bf16 splits of dY and dZ, dH, and W2 and W1
+// transposed and stacked twice along K.
 struct BwdLayout {
-  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, total;
+  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, dYs, dH, dZs, W2ts, W1ts, total;
 };
 
 BwdLayout bwd_layout_of(const moe_config_t& c) {
@@ -281,6 +283,12 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.Z = take(R * c.f * 4);
   B.dXp = take(R * c.d * 4);
   B.dxg = take(T * c.d * 4);
+  const bool tc = c.dtype == MOE_DTYPE_BF16;
+  B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
+  B.dH = take(tc ? R * c.f * 4 : 0);
+  B.dZs = take(tc ? R * 2 * c.f * 2 : 0);
+  B.W2ts = take(tc ? E * 2 * static_cast<size_t>(c.d) * c.f * 2 : 0);
+  B.W1ts = take(tc ? E * 2 * static_cast<size_t>(c.f) * c.d * 2 : 0);
   B.total = o;
   return B;
 }
@@ -333,32 +341,50 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   if ((st = run_route(c, x, Wg, bias, noise, at<int32_t>(bws, B.ridx), at<float>(bws, B.rw), Lr,
                       err, s)) != MOE_OK)
     return st;
-  cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, dY, dw, err,
-                                     at<uint32_t>(bws, kGemmCounterOffset), kNumGemmCounters,
-                                     seg01, s);
+  const bool tc = dt == MOE_DTYPE_BF16;
+  uint32_t* ctr = at<uint32_t>(bws, kGemmCounterOffset);  // three tile counters
+  cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, dY,
+                                     tc ? at<void>(bws, B.dYs) : nullptr, dw, err, ctr, 3, seg01,
+                                     s);
   if (e == cudaSuccess) e = launch_router_bwd(Lr, idx, w, dw, T, E, k, c.router, c.pre_k, c.tau, dL, s);
   // gate: dx_gate = dL W_g^T ([T, E] x [E, d]), dW_g = x^T dL, db = sum_t dL
   if (e == cudaSuccess) e = launch_gemm_nt(dt, false, dL, Wg, 1, T, E, d, seg01, dxg, err, s);
   if (e == cudaSuccess) e = launch_gemm_tn(dt, x, 0, dL, 1, T, d, E, seg01, dWg, err, s);
   if (e == cudaSuccess && dbias != nullptr) e = launch_bias_bwd(dL, T, E, dbias, s);
-  // experts: Z = X_e W1_e again (fp32), dZ = (dY W2_e^T) * SiLU'(Z) in place,
-  // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T
+  // experts: Z = X_e W1_e again (fp32), dZ = (dY W2_e^T) * SiLU'(Z) over Z,
+  // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T. bf16 layers run Z and
+  // the two dgrad GEMMs on the tensor cores (the dgrad operands split into
+  // bf16 hi + lo, the weights transposed and stacked twice along K); the
+  // weight gradients, and every GEMM of fp32 layers, in fp32 FMA.
   if (e == cudaSuccess) {
-    if (dt == MOE_DTYPE_F32) {
+    if (!tc) {
       e = launch_gemm_simt(1, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
                            static_cast<const float*>(W1), E, d, f, offsets, Z, err, s);
     } else {
       const int sms = num_sms();
       if (sms <= 0) return MOE_ERR_LAUNCH;
       e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
-                         nullptr, Z, err, at<uint32_t>(bws, kGemmCounterOffset), sms, s);
+                         nullptr, Z, err, ctr, sms, s);
+      void* W2ts = at<void>(bws, B.W2ts);
+      void* W1ts = at<void>(bws, B.W1ts);
+      if (e == cudaSuccess) e = launch_transpose_stack(W2, E, f, d, W2ts, s);  // [E][2d][f]
+      if (e == cudaSuccess) e = launch_transpose_stack(W1, E, d, f, W1ts, s);  // [E][2f][d]
+      float* dH = at<float>(bws, B.dH);
+      if (e == cudaSuccess)
+        e = launch_gemm_tc(1, at<void>(bws, B.dYs), 0, R, 0, R, W2ts, E, 2 * d, f, offsets,
+                           nullptr, dH, err, ctr + 1, sms, s);
+      if (e == cudaSuccess) e = launch_silu_bwd(dH, Z, R, f, at<void>(bws, B.dZs), s);
+      if (e == cudaSuccess)
+        e = launch_gemm_tc(1, at<void>(bws, B.dZs), 0, R, 0, R, W1ts, E, 2 * f, d, offsets,
+                           nullptr, dXp, err, ctr + 2, sms, s);
     }
   }
-  if (e == cudaSuccess) e = launch_gemm_nt(dt, true, dY, W2, E, R, d, f, offsets, Z, err, s);
+  if (e == cudaSuccess && !tc) e = launch_gemm_nt(dt, true, dY, W2, E, R, d, f, offsets, Z, err, s);
   if (e == cudaSuccess) e = launch_gemm_tn(dt, h, 0, dY, E, R, f, d, offsets, dW2, err, s);
   if (e == cudaSuccess)
     e = launch_gemm_tn(dt, x_perm, soft(c) ? 1 : 0, Z, E, R, d, f, offsets, dW1, err, s);
-  if (e == cudaSuccess) e = launch_gemm_nt(dt, false, Z, W1, E, R, f, d, offsets, dXp, err, s);
+  if (e == cudaSuccess && !tc)
+    e = launch_gemm_nt(dt, false, Z, W1, E, R, f, d, offsets, dXp, err, s);
   if (e == cudaSuccess) e = launch_undispatch(dxg, dXp, pos, T, d, k, R, dx, s);
   return status_of(e);
 }
