@@ -428,29 +428,33 @@ def run_ours(args, cfg):
             raise RuntimeError("device error in the backward steps")
         b_ms = a.elapsed_time(b) / K
         R = cfg.T * cfg.k
-        # fp32 FMA work: the experts' weight gradients (2 GEMMs) and the
-        # gate's two GEMMs; bf16 layers run Z and the two dgrad GEMMs (K
-        # doubled by the hi/lo operand split) on the tensor cores, fp32
-        # layers in fp32 FMA as well
-        simt = 4.0 * R * cfg.d * cfg.f + 4.0 * cfg.T * cfg.d * cfg.E
-        tensor = 0.0
-        if cfg.dtype == "f32":
-            simt += 6.0 * R * cfg.d * cfg.f
-        else:
-            tensor = 2.0 * R * cfg.d * cfg.f + 8.0 * R * cfg.d * cfg.f
-        # fp32 FMA peak from unit counts: SMs x 128 fp32 lanes x 2 flop x clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        fp32_peak = sms * 128 * 2 * (clk or {}).get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        gate = 4.0 * cfg.T * cfg.d * cfg.E  # dx_gate and dW_g (fp32 FMA)
+        if cfg.dtype == "f32":
+            # every GEMM in fp32 FMA: Z, dH, dX_perm, dW2, dW1 and the gate's
+            simt = 10.0 * R * cfg.d * cfg.f + gate
+            # fp32 FMA peak from unit counts: SMs x 128 fp32 lanes x 2 flop x clock
+            fp32_peak = sms * 128 * 2 * (clk or {}).get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+            roof = {"bound": "alu", "achieved": simt / (b_ms / 1e3) / 1e12, "peak": fp32_peak,
+                    "unit": "TFLOP/s", "frac": simt / (b_ms / 1e3) / 1e12 / fp32_peak,
+                    "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 x max SM clock",
+                    "flops": simt}
+            note = "achieved = every GEMM's fp32 FMA work over the whole backward time"
+        else:
+            # tensor cores: Z recomputed (2Rdf) and four GEMMs whose fp32
+            # operand (dY or dZ) is split into bf16 hi + lo (2 x 2Rdf each)
+            tensor = 18.0 * R * cfg.d * cfg.f
+            roof = {"bound": "tensor", "achieved": tensor / (b_ms / 1e3) / 1e12,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": tensor / (b_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                    "peak_source": "measured bf16 (burst)", "flops": tensor,
+                    "algorithmic_flops": 10.0 * R * cfg.d * cfg.f}
+            note = ("achieved = the tensor-core flops executed (the hi/lo split doubles four "
+                    "GEMMs) over the whole backward time; the gate's fp32 FMA work is "
+                    "simt_flops")
         bwd = {"ms_per_step": b_ms, "tokens_per_s": cfg.T * world / (b_ms / 1e3),
-               "roofline": {"bound": "alu", "achieved": simt / (b_ms / 1e3) / 1e12,
-                            "peak": fp32_peak, "unit": "TFLOP/s",
-                            "frac": simt / (b_ms / 1e3) / 1e12 / fp32_peak,
-                            "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 x max SM clock",
-                            "flops": simt},
-               "tensor_flops": tensor,
-               "note": "achieved = the fp32 FMA work (weight gradients, gate) over the whole "
-                       "backward time (an upper bound on its own time); the tensor-core work "
-                       "(recomputed Z, split-operand dgrad) is tensor_flops"}
+               "roofline": roof, "simt_flops": gate if cfg.dtype != "f32" else None,
+               "note": note}
 
     if dist:
         dist.barrier()

@@ -12,8 +12,10 @@
 //   undispatch     dx[t] = dx_gate[t] + sum_j dX_perm[pos(t,j)]
 //
 // Every sum runs in a fixed order (no atomics on data): the results are
-// bitwise reproducible. The GEMMs are SIMT fp32 FMA (128 x 128 tiles, 8 x 8
-// per thread); moving them to the tensor cores (bf16 operands) is next.
+// bitwise reproducible. The gate's GEMMs, and every GEMM of fp32 layers, are
+// SIMT fp32 FMA here (128 x 128 tiles, 8 x 8 per thread); bf16 layers run
+// the experts' GEMMs on the tensor cores (gemm_tc.cu, wgrad_tc.cu) with the
+// operand split below.
 #include <algorithm>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -30,6 +32,24 @@ constexpr int kRouterModeSoft = 3;
 __device__ __forceinline__ float ld_f32(const float* p, size_t i) { return __ldg(p + i); }
 __device__ __forceinline__ float ld_f32(const __nv_bfloat16* p, size_t i) {
   return __bfloat162float(p[i]);
+}
+// four consecutive values from a 4-aligned index
+__device__ __forceinline__ float4 ld_f32x4(const float* p, size_t i) {
+  return __ldg(reinterpret_cast<const float4*>(p + i));
+}
+__device__ __forceinline__ float4 ld_f32x4(const __nv_bfloat16* p, size_t i) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p + i));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+// v = hi + lo, hi = bf16(v), lo = bf16(v - hi), for two values packed
+__device__ __forceinline__ void split2(float a, float b, uint32_t* hi, uint32_t* lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  *hi = *reinterpret_cast<const uint32_t*>(&h);
+  *lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // ---------------------------------------------------------------- combine
@@ -59,17 +79,24 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     const float wt = ok ? __ldg(w + static_cast<size_t>(t) * k + j) : 0.f;
     float part = 0.f;
     if (ok) {
-      for (int c = tid; c < d; c += 128) {
-        const float g = ld_f32(dout, static_cast<size_t>(t) * d + c);
-        const float v = wt * g;
-        dY[static_cast<size_t>(p) * d + c] = v;
+      // four columns per thread (d is a multiple of 64)
+      for (int c = tid * 4; c < d; c += 512) {
+        const float4 g = ld_f32x4(dout, static_cast<size_t>(t) * d + c);
+        const float4 v = make_float4(wt * g.x, wt * g.y, wt * g.z, wt * g.w);
+        if (dY != nullptr) *reinterpret_cast<float4*>(dY + static_cast<size_t>(p) * d + c) = v;
         if (dYs != nullptr) {
-          // bf16 split for the tensor-core dgrad: v = hi + lo to ~2^-17
-          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-          dYs[static_cast<size_t>(p) * 2 * d + c] = hi;
-          dYs[static_cast<size_t>(p) * 2 * d + d + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
+          // bf16 split for the tensor-core GEMMs: v = hi + lo to ~2^-17
+          uint2 hi, lo;
+          split2(v.x, v.y, &hi.x, &lo.x);
+          split2(v.z, v.w, &hi.y, &lo.y);
+          *reinterpret_cast<uint2*>(dYs + static_cast<size_t>(p) * 2 * d + c) = hi;
+          *reinterpret_cast<uint2*>(dYs + static_cast<size_t>(p) * 2 * d + d + c) = lo;
         }
-        part = fmaf(g, __ldg(y + static_cast<size_t>(p) * d + c), part);
+        const float4 yv = ld_f32x4(y, static_cast<size_t>(p) * d + c);
+        part = fmaf(g.x, yv.x, part);
+        part = fmaf(g.y, yv.y, part);
+        part = fmaf(g.z, yv.z, part);
+        part = fmaf(g.w, yv.w, part);
       }
     }
 #pragma unroll
@@ -92,7 +119,7 @@ __device__ __forceinline__ bool beats_b(float va, int ia, float vb, int ib) {
 __global__ void __launch_bounds__(256) router_bwd_kernel(
     const float* __restrict__ L, const int32_t* __restrict__ idx, const float* __restrict__ w,
     const float* __restrict__ dw, int T, int E, int k, int mode, int pre_k, float tau,
-    float* __restrict__ dL) {
+    float* __restrict__ dL, __nv_bfloat16* __restrict__ dLs) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -178,7 +205,16 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
 #pragma unroll
   for (int jj = 0; jj < kRB_NJ; ++jj) {
     const int e = lane + 32 * jj;
-    if (e < E) dL[static_cast<size_t>(t) * E + e] = g[jj];
+    if (e < E) {
+      dL[static_cast<size_t>(t) * E + e] = g[jj];
+      if (dLs != nullptr) {
+        // [T][2E] = [hi | lo] for the tensor-core gate GEMMs
+        const __nv_bfloat16 hi = __float2bfloat16_rn(g[jj]);
+        dLs[static_cast<size_t>(t) * 2 * E + e] = hi;
+        dLs[static_cast<size_t>(t) * 2 * E + E + e] =
+            __float2bfloat16_rn(g[jj] - __bfloat162float(hi));
+      }
+    }
   }
 }
 
@@ -381,53 +417,25 @@ __global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, 
   }
 }
 
-// ---------------------------------------------------------------- tensor-core dgrad
-// The dgrad GEMMs run on the forward's tcgen05 pair GEMM in bf16 with every
-// fp32 operand split in two: v = hi + lo with hi = bf16(v), lo = bf16(v - hi)
-// (a 16-bit significand, error ~2^-17 |v|), A = [hi | lo] along K and B =
-// the transposed weights stacked twice along K, so A . B = hi . W + lo . W
-// with exact products and fp32 accumulation.
+// ---------------------------------------------------------------- tensor-core GEMM operands
+// bf16 layers run the experts' backward GEMMs on the tensor cores in bf16
+// with every fp32 operand split in two: v = hi + lo with hi = bf16(v), lo =
+// bf16(v - hi) (a 16-bit significand, error ~2^-17 |v|); the GEMMs take both
+// parts against the same bf16 weight or activation, so the products are
+// exact and the sums fp32.
 
-// dst[e][c][r] = dst[e][C + c][r] = src[e][r][c]: src [E][Rw][C] -> dst [E][2C][Rw]
-// (32 x 32 tiles through shared memory, both sides coalesced)
-__global__ void __launch_bounds__(256) transpose_stack_kernel(const __nv_bfloat16* __restrict__ src,
-                                                              int Rw, int C,
-                                                              __nv_bfloat16* __restrict__ dst) {
-  __shared__ __nv_bfloat16 tile[32][33];
-  pdl_wait();
-  pdl_trigger();
-  const int e = blockIdx.z, r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  const __nv_bfloat16* se = src + static_cast<size_t>(e) * Rw * C;
-  __nv_bfloat16* de = dst + static_cast<size_t>(e) * 2 * C * Rw;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int i = ty; i < 32; i += 8) {
-    const int r = r0 + i, c = c0 + tx;
-    if (r < Rw && c < C) tile[i][tx] = se[static_cast<size_t>(r) * C + c];
-  }
-  __syncthreads();
-  for (int i = ty; i < 32; i += 8) {
-    const int c = c0 + i, r = r0 + tx;
-    if (r < Rw && c < C) {
-      const __nv_bfloat16 v = tile[tx][i];
-      de[static_cast<size_t>(c) * Rw + r] = v;
-      de[static_cast<size_t>(C + c) * Rw + r] = v;
-    }
-  }
-}
-
-// dZ = dH * SiLU'(Z), written over Z (fp32, for the weight gradients) and
-// as the bf16 split [R][2N] (for the dgrad GEMM)
+// dZ = dH * SiLU'(Z) as the bf16 split [R][2N] = [hi | lo] (the operand of
+// the tensor-core dgrad and weight-gradient GEMMs)
 __global__ void __launch_bounds__(256) silu_bwd_kernel(const float* __restrict__ dH,
-                                                       float* __restrict__ Z, size_t n, int N,
-                                                       __nv_bfloat16* __restrict__ dZs) {
+                                                       const float* __restrict__ Z, size_t n,
+                                                       int N, __nv_bfloat16* __restrict__ dZs) {
   pdl_wait();
   pdl_trigger();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float z = Z[i];
+    const float z = __ldg(Z + i);
     const float sg = 1.f / (1.f + expf(-z));
     const float v = __ldg(dH + i) * (sg * (1.f + z * (1.f - sg)));
-    Z[i] = v;
     const size_t r = i / N, c = i - r * N;
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
     dZs[r * 2 * N + c] = hi;
@@ -436,15 +444,26 @@ __global__ void __launch_bounds__(256) silu_bwd_kernel(const float* __restrict__
 }
 
 // ---------------------------------------------------------------- bias, dx
-// db[e] = sum_t dL[t, e]: one thread per expert, t ascending.
-__global__ void __launch_bounds__(256) bias_bwd_kernel(const float* __restrict__ dL, int T, int E,
-                                                       float* __restrict__ db) {
+// db[e] = sum_t dL[t, e]. A CTA of 32 warps takes 32 experts (lane = expert,
+// so each warp reads 128 contiguous bytes of a row of dL); warp w sums the
+// tokens t = w mod 32 in ascending order, then warp 0 adds the 32 partials
+// in warp order: a fixed order, bitwise reproducible.
+__global__ void __launch_bounds__(1024) bias_bwd_kernel(const float* __restrict__ dL, int T, int E,
+                                                        float* __restrict__ db) {
+  __shared__ float red[32][33];
   pdl_wait();
   pdl_trigger();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float s = 0.f;
-    for (int t = 0; t < T; ++t) s += __ldg(dL + static_cast<size_t>(t) * E + e);
-    db[e] = s;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (e < E)
+    for (int t = w; t < T; t += 32) s += __ldg(dL + static_cast<size_t>(t) * E + e);
+  red[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && e < E) {
+    float tot = 0.f;
+    for (int i = 0; i < 32; ++i) tot += red[i][lane];
+    db[e] = tot;
   }
 }
 
@@ -457,13 +476,20 @@ __global__ void __launch_bounds__(128) undispatch_kernel(const float* __restrict
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x;
-  for (int c = threadIdx.x; c < d; c += 128) {
-    float v = __ldg(dxg + static_cast<size_t>(t) * d + c);
+  // four columns per thread (d is a multiple of 64): 16-byte loads and stores
+  for (int c = threadIdx.x * 4; c < d; c += 512) {
+    float4 v = __ldg(reinterpret_cast<const float4*>(dxg + static_cast<size_t>(t) * d + c));
     for (int j = 0; j < k; ++j) {
       const int p = __ldg(pos + static_cast<size_t>(t) * k + j);
-      if (p >= 0 && p < R) v += __ldg(dxp + static_cast<size_t>(p) * d + c);
+      if (p >= 0 && p < R) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(dxp + static_cast<size_t>(p) * d + c));
+        v.x += a.x;
+        v.y += a.y;
+        v.z += a.z;
+        v.w += a.w;
+      }
     }
-    dx[static_cast<size_t>(t) * d + c] = v;
+    *reinterpret_cast<float4*>(dx + static_cast<size_t>(t) * d + c) = v;
   }
 }
 
@@ -484,16 +510,8 @@ cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, cons
                     err, zero, nzero, seg01);
 }
 
-cudaError_t launch_transpose_stack(const void* src, int E, int Rw, int C, void* dst,
-                                   cudaStream_t s) {
-  if (E == 0) return cudaSuccess;
-  const dim3 grid(ceil_div(C, 32), ceil_div(Rw, 32), E), block(256);
-  return launch_pdl(transpose_stack_kernel, grid, block, 0, s,
-                    static_cast<const __nv_bfloat16*>(src), Rw, C,
-                    static_cast<__nv_bfloat16*>(dst));
-}
-
-cudaError_t launch_silu_bwd(const float* dH, float* Z, int R, int N, void* dZs, cudaStream_t s) {
+cudaError_t launch_silu_bwd(const float* dH, const float* Z, int R, int N, void* dZs,
+                            cudaStream_t s) {
   const size_t n = static_cast<size_t>(R) * N;
   if (n == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 152 * 16));
@@ -503,10 +521,10 @@ cudaError_t launch_silu_bwd(const float* dH, float* Z, int R, int N, void* dZs, 
 
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
                               int T, int E, int k, int mode, int pre_k, float tau, float* dL,
-                              cudaStream_t s) {
+                              void* dLs, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   return launch_pdl(router_bwd_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, L, idx, w, dw, T, E,
-                    k, mode, pre_k, tau, dL);
+                    k, mode, pre_k, tau, dL, static_cast<__nv_bfloat16*>(dLs));
 }
 
 cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W, int E, int R,
@@ -538,7 +556,7 @@ cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float*
 }
 
 cudaError_t launch_bias_bwd(const float* dL, int T, int E, float* db, cudaStream_t s) {
-  return launch_pdl(bias_bwd_kernel, dim3(1), dim3(256), 0, s, dL, T, E, db);
+  return launch_pdl(bias_bwd_kernel, dim3(ceil_div(E, 32)), dim3(1024), 0, s, dL, T, E, db);
 }
 
 cudaError_t launch_undispatch(const float* dxg, const float* dxp, const int32_t* pos, int T, int d,

@@ -153,23 +153,21 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 // ---------------------------------------------------------------- backward.cu
 // The backward pass's kernels (dtype 0 = fp32, 1 = bf16 for the tensors the
 // forward takes; every gradient and intermediate is fp32).
-// dY[pos(t,j)] = w[t,j] dout[t] (and, when dYs is non-null, its bf16 split
+// dY[pos(t,j)] = w[t,j] dout[t] (when dY is non-null; when dYs is, its bf16 split
 // [R][2d] = [hi | lo]); dw[t,j] = <dout[t], Y[pos(t,j)]>; also zeroes `nzero`
 // words at `zero` and writes seg01 = {0, T}.
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
                                float* dw, uint32_t* err, uint32_t* zero, int nzero,
                                int32_t* seg01, cudaStream_t s);
-// bf16 src [E][Rw][C] -> dst [E][2C][Rw], the transpose written twice along
-// its first axis (the B operand of a split-operand dgrad GEMM).
-cudaError_t launch_transpose_stack(const void* src, int E, int Rw, int C, void* dst,
-                                   cudaStream_t s);
-// dZ = dH * SiLU'(Z) over Z [R, N] (fp32) and as the bf16 split [R][2N].
-cudaError_t launch_silu_bwd(const float* dH, float* Z, int R, int N, void* dZs, cudaStream_t s);
-// dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec).
+// dZ = dH * SiLU'(Z) ([R, N] fp32 in) as the bf16 split [R][2N] = [hi | lo].
+cudaError_t launch_silu_bwd(const float* dH, const float* Z, int R, int N, void* dZs,
+                            cudaStream_t s);
+// dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec),
+// and, when dLs is non-null, its bf16 split [T][2E] = [hi | lo].
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
                               int T, int E, int k, int mode, int pre_k, float tau, float* dL,
-                              cudaStream_t s);
+                              void* dLs, cudaStream_t s);
 // out[r] = A[r] . W[e]^T over the segments (W [E][N][K], dtype wdtype);
 // silu: out holds Z and gets acc * SiLU'(Z).
 cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W, int E, int R,
@@ -177,6 +175,22 @@ cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W,
                            cudaStream_t s);
 // out[e] = A_e^T . B_e over each segment's rows (A [*, M] dtype adtype,
 // shared rows when a_shared; B fp32 [R, N]); out [E][M][N].
+// The same GEMM (fp32 output, no activation) with the weights stored
+// transposed: out[r] = A[r] . W_e^T, W bf16 [E][N][k_wrap]
+// row-major, A bf16 [R, K] with K = k_wrap or 2 k_wrap (k >= k_wrap reads
+// weight column k - k_wrap: the hi | lo operand split against one weight).
+cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K, int k_wrap,
+                              int N, const int32_t* offsets, float* out, uint32_t* err,
+                              uint32_t* tile_ctr, int num_sms, cudaStream_t s);
+
+// The experts' weight gradients on the tensor cores (wgrad_tc.cu):
+// out[e] = A_e^T . (Bs_e[:, :N] + Bs_e[:, N:]) over the rows of expert e's
+// segment (A row r, or r - offsets[e] with a_shared), A bf16 [a_rows, M],
+// Bs bf16 [R, 2N] (the hi | lo split), out fp32 [E][M][N]; M a multiple of
+// 64, N of 8.
+cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void* Bs, int R, int E,
+                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
+                            int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float* B, int E, int R,
                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
                            cudaStream_t s);

@@ -59,6 +59,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace moe {
 namespace {
@@ -75,6 +76,8 @@ struct TcParams {
   int n_tiles_m;       // feature blocks of a merged tile (ceil(N / 224))
   int a_rows;          // rows of A
   int a_shared;        // 1: output row r of expert e reads A row r - offsets[e]
+  int k_wrap;          // BT: columns of the stored weight; k-block kb reads
+                       // columns (64 kb) mod k_wrap (K = 2 k_wrap stacks it twice)
 };
 
 // z * sigmoid(z) with the approximate divide: the result is rounded to bf16,
@@ -189,6 +192,16 @@ static_assert(smem_bytes<0, 1>() <= 227 * 1024 && smem_bytes<0, 2>() <= 227 * 10
                   smem_bytes<1, 1>() <= 227 * 1024 && smem_bytes<1, 2>() <= 227 * 1024,
               "shared memory");
 
+// Descriptor of this CTA's staged weights at k-step kk: MN-major (two
+// [64 k][64 n] boxes, 8 KB apart; a k-step is 16 rows of 128 bytes) or, for
+// transposed weights, K-major ([128 n][64 k], a k-step is 32 bytes along the
+// swizzled row).
+template <bool BT>
+__device__ __forceinline__ uint64_t wdesc(uint32_t base, int kk) {
+  return BT ? make_sdesc_sw128(base + kk * 32, 16, 1024)
+            : make_sdesc_sw128(base + kk * 2048, BOX_BYTES, 1024);
+}
+
 struct PTile {
   int e, row0, ntok, n0;  // token rows [row0, row0 + ntok), features from n0
   bool swap;              // tail tile: weights are the MMA's M side, tokens its N
@@ -259,7 +272,11 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
 }
 }  // namespace pairk
 
-template <int EPI, int NB, bool A8>
+// BT: the weights are stored transposed, [E][N][k_wrap] row-major (the
+// layer's own W2 for dH = dY W2^T, W1 for dX = dZ W1^T), and are read
+// K-major: one [128 features][64 k] box per CTA and k-block, with no
+// transposed copy in memory.
+template <int EPI, int NB, bool A8, bool BT = false>
 __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmA8,
@@ -272,6 +289,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
   // FP8 token rows come without merged remainder tiles (a remainder is a
   // swapped tile, its rows expanded like any other)
   constexpr bool MERGE = S::MERGE && !A8;
+  static_assert(!BT || (NB == 1 && !A8), "transposed weights: 256-feature tiles, bf16 rows");
+  // instruction descriptors (A or B K-major / MN-major per the weight layout)
+  constexpr uint32_t IDESC_N = make_idesc_bf16_f32(pairk::BM, 256, false, !BT);
+  constexpr uint32_t IDESC_M = make_idesc_bf16_f32(pairk::BM, pairk::MT_W, false, !BT);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -432,7 +453,11 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
         // tile); a box is issued when it starts below N (one that runs past
         // N is zero-filled, its bytes still counted)
         const int half_w = t.tail > 0 ? pairk::MT_HALF : 128;
-        auto boxes = [&](int n) { return n < p.N ? min(2, (p.N - n + 63) / 64) : 0; };
+        // (BT: one [128][64] box, counted as two 8 KB boxes)
+        auto boxes = [&](int n) {
+          if (BT) return n < p.N ? 2 : 0;
+          return n < p.N ? min(2, (p.N - n + 63) / 64) : 0;
+        };
         int nbox[NB];
         // A8: the token rows land on this CTA's a8_full, not on full; the
         // odd CTA's converter warps each send 16 bytes to full instead
@@ -464,12 +489,20 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
           } else {
             tma_load_2d_pair(sA + s * pairk::A_BYTES, &tmA, bar, kb * pairk::BK, my_row);
           }
+          if constexpr (BT) {
+            // rows e N + n0 + half_w rank .. +127 of the stored [E N][k_wrap]
+            if (nbox[0] > 0)
+              tma_load_2d_pair(sB + s * S::B_BYTES, &tmB, bar, (kb * pairk::BK) % p.k_wrap,
+                               t.e * p.N + t.n0 + static_cast<int>(rank) * half_w);
+          } else {
 #pragma unroll
-          for (int j = 0; j < NB; ++j)
-            for (int c = 0; c < nbox[j]; ++c)
-              tma_load_2d_pair(sB + s * S::B_BYTES + j * pairk::HALF_B_BYTES + c * pairk::BOX_BYTES,
-                               &tmB, bar, t.n0 + j * 256 + static_cast<int>(rank) * half_w + c * 64,
-                               brow + kb * pairk::BK);
+            for (int j = 0; j < NB; ++j)
+              for (int c = 0; c < nbox[j]; ++c)
+                tma_load_2d_pair(
+                    sB + s * S::B_BYTES + j * pairk::HALF_B_BYTES + c * pairk::BOX_BYTES, &tmB,
+                    bar, t.n0 + j * 256 + static_cast<int>(rank) * half_w + c * 64,
+                    brow + kb * pairk::BK);
+          }
           if constexpr (MERGE) {
             for (int r = 0; r < tail_half; r += 8)
               tma_load_2d_pair(sT + s * S::T_BYTES + r * pairk::BK * 2, &tmA8, bar,
@@ -512,9 +545,9 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
         const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
         // MMAs with any feature below N (the rest of a last tile is skipped)
         const int nmma = min(NB, (p.N - t.n0 + 255) / 256);
-        // swapped tile: A = weights (MN-major, the B slot), B = tokens (K-major, the A slot)
+        // swapped tile: A = weights (the B slot), B = tokens (K-major, the A slot)
         const uint32_t idesc =
-            t.swap ? make_idesc_bf16_f32(pairk::BM, (t.ntok + 15) & ~15, true, false) : pairk::IDESC;
+            t.swap ? make_idesc_bf16_f32(pairk::BM, (t.ntok + 15) & ~15, !BT, false) : IDESC_N;
         bool merged = false;
         if constexpr (MERGE) merged = t.tail > 0;
         if (merged) {
@@ -522,7 +555,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
           // remainder's four swapped MMAs into columns 224.. (its own loop:
           // the extra MMA inside the plain loop slowed every tile's issue)
           const uint32_t idesc_tail =
-              make_idesc_bf16_f32(pairk::BM, (t.tail + 15) & ~15, true, false);
+              make_idesc_bf16_f32(pairk::BM, (t.tail + 15) & ~15, !BT, false);
           for (int kb = 0; kb < KB; ++kb) {
             if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
               timed_out = true;
@@ -535,12 +568,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
 #pragma unroll
             for (int kk = 0; kk < pairk::BK / 16; ++kk)
               tc_mma_f16_pair(d_tmem, make_sdesc_sw128(a_base + kk * 32, 16, 1024),
-                              make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024),
-                              pairk::IDESC_MT, (kb | kk) != 0 ? 1u : 0u);
+                              pairk::wdesc<BT>(b_base, kk), IDESC_M, (kb | kk) != 0 ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < pairk::BK / 16; ++kk)
-              tc_mma_f16_pair(d_tmem + pairk::MT_W,
-                              make_sdesc_sw128(b_base + kk * 2048, pairk::BOX_BYTES, 1024),
+              tc_mma_f16_pair(d_tmem + pairk::MT_W, pairk::wdesc<BT>(b_base, kk),
                               make_sdesc_sw128(t_base + kk * 32, 16, 1024), idesc_tail,
                               (kb | kk) != 0 ? 1u : 0u);
             issued = true;
@@ -568,8 +599,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
 #pragma unroll
               for (int j = 0; j < NB; ++j) {
                 if (j >= nmma) break;
-                const uint64_t wt = make_sdesc_sw128(b_base + j * pairk::HALF_B_BYTES + kk * 2048,
-                                                     pairk::BOX_BYTES, 1024);
+                const uint64_t wt = pairk::wdesc<BT>(b_base + j * pairk::HALF_B_BYTES, kk);
                 tc_mma_f16_pair(d_tmem + j * 256, t.swap ? wt : tok, t.swap ? tok : wt, idesc,
                                 (kb | kk) != 0 ? 1u : 0u);
               }
@@ -874,7 +904,11 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
   }
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------- host side
+// Tensor maps (declared in tmap.cuh; the weight-gradient GEMM uses them too).
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -889,6 +923,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   });
   return g_encode;
 }
+}  // namespace
 
 // 2-D bf16 map over a row-major [rows, cols] matrix, box [box_rows][box_cols]
 // (box_cols * 2 bytes = 128, the swizzle span).
@@ -940,12 +975,14 @@ bool make_map_2d_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int EPI, int NB, bool A8>
+namespace {
+
+template <int EPI, int NB, bool A8, bool BT>
 cudaError_t set_pair_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB, A8>,
+    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB, A8, BT>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               pairk::smem_bytes<EPI, NB>());
   });
@@ -953,7 +990,7 @@ cudaError_t set_pair_smem_attr() {
 }
 
 // Clusters of two that can be resident at once (cached per device and kernel).
-template <int EPI, int NB, bool A8>
+template <int EPI, int NB, bool A8, bool BT>
 int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   static int cache[64] = {};
   int dev = 0;
@@ -962,7 +999,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   cudaLaunchConfig_t lc = lc_in;
   lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB, A8>, &lc) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB, A8, BT>, &lc) != cudaSuccess ||
       n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
@@ -971,7 +1008,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   return n;
 }
 
-template <int EPI, int NB, bool A8>
+template <int EPI, int NB, bool A8, bool BT = false>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUtensorMap& mB,
                         const CUtensorMap& mY, TcParams prm, int num_sms,
                         cudaStream_t s) {
@@ -994,14 +1031,14 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  cudaError_t st = set_pair_smem_attr<EPI, NB, A8>();
+  cudaError_t st = set_pair_smem_attr<EPI, NB, A8, BT>();
   if (st != cudaSuccess) return st;
   // a persistent grid must fit at once: as many pairs as can be resident
   // together (a pair needs two free SMs of one GPC), not num_sms / 2
-  const int resident = resident_pairs<EPI, NB, A8>(lc, num_sms);
+  const int resident = resident_pairs<EPI, NB, A8, BT>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8>, mA, mA8, mB, mY, prm);
+  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8, BT>, mA, mA8, mB, mY, prm);
 }
 
 // 512-feature tiles (one accumulator, epilogue exposed) pay off only for the
@@ -1060,6 +1097,7 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
   prm.n_tiles = 0;
   prm.a_rows = a_rows;
   prm.a_shared = a_shared;
+  prm.k_wrap = K;
   int nb = pick_nb(epi, R, E, K, N, num_sms);
   // MOE_GEMM_TILE_FEATURES=256|512 overrides the choice (read on every call)
   if (const char* f = std::getenv("MOE_GEMM_TILE_FEATURES")) {
@@ -1072,6 +1110,41 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
                    : launch_pair<0, 1, false>(mA, mA8, mB, mY, prm, num_sms, s);
   return nb == 2 ? launch_pair<1, 2, false>(mA, mA8, mB, mY, prm, num_sms, s)
                  : launch_pair<1, 1, false>(mA, mA8, mB, mY, prm, num_sms, s);
+}
+
+cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K, int k_wrap,
+                              int N, const int32_t* offsets, float* out, uint32_t* err,
+                              uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  if (num_sms < 2 || k_wrap <= 0 || k_wrap % 64 != 0 || K % k_wrap != 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap mA, mA8, mB, mY;
+  std::memset(&mA, 0, sizeof(mA));
+  std::memset(&mA8, 0, sizeof(mA8));
+  std::memset(&mB, 0, sizeof(mB));
+  std::memset(&mY, 0, sizeof(mY));
+  // A: [R, K] rows in [128][64] boxes (and [8][64] for merged remainders);
+  // weights: the stored [E N, k_wrap] matrix in [128 features][64 k] boxes
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128) ||
+      !make_map_2d(&mA8, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 8) ||
+      !make_map_2d(&mB, Wt, static_cast<uint64_t>(E) * N, static_cast<uint64_t>(k_wrap), 64, 128) ||
+      !make_map_2d_out(&mY, out, static_cast<uint64_t>(R), static_cast<uint64_t>(N), true))
+    return cudaErrorInvalidValue;
+  TcParams prm;
+  prm.offsets = offsets;
+  prm.row_scale = nullptr;
+  prm.out = out;
+  prm.err = err;
+  prm.tile_ctr = tile_ctr;
+  prm.E = E;
+  prm.K = K;
+  prm.N = N;
+  prm.R = R;
+  prm.n_tiles = 0;
+  prm.a_rows = R;
+  prm.a_shared = 0;
+  prm.k_wrap = k_wrap;
+  return launch_pair<1, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s);
 }
 
 }  // namespace moe

@@ -255,12 +255,12 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // ---------------------------------------------------------------- backward
 // The backward workspace: an error word and the GEMM tile counters, then the
 // recomputed logits (and the route call's unused top-k), dw, dL, the single
-// segment {0, T} of the gate GEMMs, dY, Z (overwritten by dZ), dX_perm and
-// the gate part of dx, all fp32 but the ints; bf16 layers add the operands
-// of the tensor-core dgrad: the bf16 splits of dY and dZ, dH, and W2 and W1
-// transposed and stacked twice along K.
+// segment {0, T} of the gate GEMMs, dY (fp32 layers), the recomputed
+// pre-activation Z (fp32 layers overwrite it with dZ), dX_perm and the gate
+// part of dx, all fp32 but the ints; bf16 layers add the tensor-core GEMMs'
+// operands: the bf16 splits of dY, dZ and dL, and dH.
 struct BwdLayout {
-  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, dYs, dH, dZs, W2ts, W1ts, total;
+  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, dYs, dH, dZs, dLs, total;
 };
 
 BwdLayout bwd_layout_of(const moe_config_t& c) {
@@ -279,16 +279,15 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.dw = take(R * 4);
   B.dL = take(T * E * 4);
   B.seg01 = take(8);
-  B.dY = take(R * c.d * 4);
+  const bool tc = c.dtype == MOE_DTYPE_BF16;
+  B.dY = take(tc ? 0 : R * c.d * 4);  // fp32 layers (bf16 ones keep only the split)
   B.Z = take(R * c.f * 4);
   B.dXp = take(R * c.d * 4);
   B.dxg = take(T * c.d * 4);
-  const bool tc = c.dtype == MOE_DTYPE_BF16;
   B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
   B.dH = take(tc ? R * c.f * 4 : 0);
   B.dZs = take(tc ? R * 2 * c.f * 2 : 0);
-  B.W2ts = take(tc ? E * 2 * static_cast<size_t>(c.d) * c.f * 2 : 0);
-  B.W1ts = take(tc ? E * 2 * static_cast<size_t>(c.f) * c.d * 2 : 0);
+  B.dLs = take(tc ? T * 2 * E * 2 : 0);
   B.total = o;
   return B;
 }
@@ -301,9 +300,10 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   if (st != MOE_OK) return st;
   const moe_config_t& c = *cfg;
   if (c.payload_fp8 || c.output_fp8) return MOE_ERR_UNSUPPORTED;
-  if (!ok_ptr(x) || Wg == nullptr || !ok_ptr(W1) || !ok_ptr(W2) || fwd_ws == nullptr ||
-      !aligned(fwd_ws, kAlign) || dout == nullptr || dx == nullptr || dWg == nullptr ||
-      dW1 == nullptr || dW2 == nullptr || bws == nullptr || !aligned(bws, kAlign) ||
+  // tensors read or written in 16-byte pieces or by TMA: 16-byte aligned
+  if (!ok_ptr(x) || !ok_ptr(Wg) || !ok_ptr(W1) || !ok_ptr(W2) || fwd_ws == nullptr ||
+      !aligned(fwd_ws, kAlign) || !ok_ptr(dout) || !ok_ptr(dx) || !ok_ptr(dWg) ||
+      !ok_ptr(dW1) || !ok_ptr(dW2) || bws == nullptr || !aligned(bws, kAlign) ||
       (soft(c) && c.T > 0 && noise == nullptr))
     return MOE_ERR_INVALID_ARG;
   const Layout L = layout_of(c);
@@ -342,49 +342,66 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
                       err, s)) != MOE_OK)
     return st;
   const bool tc = dt == MOE_DTYPE_BF16;
-  uint32_t* ctr = at<uint32_t>(bws, kGemmCounterOffset);  // three tile counters
-  cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, dY,
-                                     tc ? at<void>(bws, B.dYs) : nullptr, dw, err, ctr, 3, seg01,
+  uint32_t* ctr = at<uint32_t>(bws, kGemmCounterOffset);  // four tile counters
+  cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
+                                     tc ? at<void>(bws, B.dYs) : nullptr, dw, err, ctr, 4, seg01,
                                      s);
-  if (e == cudaSuccess) e = launch_router_bwd(Lr, idx, w, dw, T, E, k, c.router, c.pre_k, c.tau, dL, s);
-  // gate: dx_gate = dL W_g^T ([T, E] x [E, d]), dW_g = x^T dL, db = sum_t dL
-  if (e == cudaSuccess) e = launch_gemm_nt(dt, false, dL, Wg, 1, T, E, d, seg01, dxg, err, s);
-  if (e == cudaSuccess) e = launch_gemm_tn(dt, x, 0, dL, 1, T, d, E, seg01, dWg, err, s);
+  void* dLs = tc ? at<void>(bws, B.dLs) : nullptr;
+  if (e == cudaSuccess)
+    e = launch_router_bwd(Lr, idx, w, dw, T, E, k, c.router, c.pre_k, c.tau, dL, dLs, s);
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_LAUNCH;
+  // gate: dx_gate = dL W_g^T ([T, E] x [E, d]), dW_g = x^T dL, db = sum_t dL.
+  // bf16 layers put them on the tensor cores with dL split into hi + lo
+  // (dx_gate: W_g read K-major, K = E a multiple of 64; dW_g: E a multiple
+  // of 8), else fp32 FMA.
+  if (e == cudaSuccess)
+    e = tc && E % 64 == 0 ? launch_gemm_tc_wt(dLs, T, Wg, 1, 2 * E, E, d, seg01, dxg, err, ctr + 3,
+                                              sms, s)
+                          : launch_gemm_nt(dt, false, dL, Wg, 1, T, E, d, seg01, dxg, err, s);
+  if (e == cudaSuccess)
+    e = tc && E % 8 == 0 ? launch_wgrad_tc(x, T, 0, dLs, T, 1, d, E, seg01, dWg, err, sms, s)
+                         : launch_gemm_tn(dt, x, 0, dL, 1, T, d, E, seg01, dWg, err, s);
   if (e == cudaSuccess && dbias != nullptr) e = launch_bias_bwd(dL, T, E, dbias, s);
   // experts: Z = X_e W1_e again (fp32), dZ = (dY W2_e^T) * SiLU'(Z) over Z,
-  // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T. bf16 layers run Z and
-  // the two dgrad GEMMs on the tensor cores (the dgrad operands split into
-  // bf16 hi + lo, the weights transposed and stacked twice along K); the
-  // weight gradients, and every GEMM of fp32 layers, in fp32 FMA.
+  // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T. bf16 layers run every
+  // expert GEMM on the tensor cores (dY and dZ split into bf16 hi + lo; for
+  // the dgrad GEMMs the weights transposed and stacked twice along K); fp32
+  // layers run them in fp32 FMA.
   if (e == cudaSuccess) {
     if (!tc) {
       e = launch_gemm_simt(1, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
                            static_cast<const float*>(W1), E, d, f, offsets, Z, err, s);
     } else {
-      const int sms = num_sms();
-      if (sms <= 0) return MOE_ERR_LAUNCH;
       e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
                          nullptr, Z, err, ctr, sms, s);
-      void* W2ts = at<void>(bws, B.W2ts);
-      void* W1ts = at<void>(bws, B.W1ts);
-      if (e == cudaSuccess) e = launch_transpose_stack(W2, E, f, d, W2ts, s);  // [E][2d][f]
-      if (e == cudaSuccess) e = launch_transpose_stack(W1, E, d, f, W1ts, s);  // [E][2f][d]
+      // dH = [dY hi | dY lo] . [W2_e^T ; W2_e^T] and dX_perm likewise with
+      // W1_e: the stored weights read K-major, K = 2d (2f) wrapping at d (f)
       float* dH = at<float>(bws, B.dH);
       if (e == cudaSuccess)
-        e = launch_gemm_tc(1, at<void>(bws, B.dYs), 0, R, 0, R, W2ts, E, 2 * d, f, offsets,
-                           nullptr, dH, err, ctr + 1, sms, s);
+        e = launch_gemm_tc_wt(at<void>(bws, B.dYs), R, W2, E, 2 * d, d, f, offsets, dH, err,
+                              ctr + 1, sms, s);
       if (e == cudaSuccess) e = launch_silu_bwd(dH, Z, R, f, at<void>(bws, B.dZs), s);
       if (e == cudaSuccess)
-        e = launch_gemm_tc(1, at<void>(bws, B.dZs), 0, R, 0, R, W1ts, E, 2 * f, d, offsets,
-                           nullptr, dXp, err, ctr + 2, sms, s);
+        e = launch_gemm_tc_wt(at<void>(bws, B.dZs), R, W1, E, 2 * f, f, d, offsets, dXp, err,
+                              ctr + 2, sms, s);
     }
   }
-  if (e == cudaSuccess && !tc) e = launch_gemm_nt(dt, true, dY, W2, E, R, d, f, offsets, Z, err, s);
-  if (e == cudaSuccess) e = launch_gemm_tn(dt, h, 0, dY, E, R, f, d, offsets, dW2, err, s);
-  if (e == cudaSuccess)
-    e = launch_gemm_tn(dt, x_perm, soft(c) ? 1 : 0, Z, E, R, d, f, offsets, dW1, err, s);
-  if (e == cudaSuccess && !tc)
-    e = launch_gemm_nt(dt, false, Z, W1, E, R, f, d, offsets, dXp, err, s);
+  if (e == cudaSuccess && tc) {
+    // weight gradients on the tensor cores: dW2 = H^T (dY hi + lo),
+    // dW1 = X^T (dZ hi + lo), contracted over each expert's rows
+    e = launch_wgrad_tc(h, R, 0, at<void>(bws, B.dYs), R, E, f, d, offsets, dW2, err, sms, s);
+    if (e == cudaSuccess)
+      e = launch_wgrad_tc(x_perm, soft(c) ? T : R, soft(c) ? 1 : 0, at<void>(bws, B.dZs), R, E, d,
+                          f, offsets, dW1, err, sms, s);
+  }
+  if (e == cudaSuccess && !tc) {
+    e = launch_gemm_nt(dt, true, dY, W2, E, R, d, f, offsets, Z, err, s);
+    if (e == cudaSuccess) e = launch_gemm_tn(dt, h, 0, dY, E, R, f, d, offsets, dW2, err, s);
+    if (e == cudaSuccess)
+      e = launch_gemm_tn(dt, x_perm, soft(c) ? 1 : 0, Z, E, R, d, f, offsets, dW1, err, s);
+    if (e == cudaSuccess) e = launch_gemm_nt(dt, false, Z, W1, E, R, f, d, offsets, dXp, err, s);
+  }
   if (e == cudaSuccess) e = launch_undispatch(dxg, dXp, pos, T, d, k, R, dx, s);
   return status_of(e);
 }

@@ -1,0 +1,420 @@
+// wgrad_tc.cu - the experts' weight gradients on the sm_103a tensor cores
+// (tcgen05 + TMEM, fed by TMA). In backpropagation the gradient reaches only
+// the activated experts (DeepSeek-V4 EP article, section 2.1), so each
+// expert's weight gradient is a sum over the rows routed to it:
+//
+//   dW[e][m][n] = sum over r in [offsets[e], offsets[e+1]) of A[a(r)][m] * dB[r][n]
+//
+// with A the rows' bf16 activations (the dispatched tokens for dW1, the
+// stored SiLU output H for dW2; a(r) = r, or r - offsets[e] when every
+// expert reads the same rows) and dB their fp32 output gradient, held as two
+// bf16 parts dB = hi + lo ([R][2N]: columns [0, N) hi, [N, 2N) lo, the
+// split the dgrad GEMMs read; hi + lo carries dB to ~2^-17 relative). Both
+// parts go through the tensor cores into one fp32 accumulator, so the result
+// has the accuracy of an fp32 operand. Output fp32 [E][M][N]; an expert with
+// no rows gets zeros.
+//
+// Tiles: 128 output rows (m) x 128 output columns (n) of one expert; the
+// contraction runs over the expert's rows in blocks of 64 (ragged: the last
+// block holds n_e mod 64 rows). Both operands are read MN-major straight
+// from their row-major storage: a TMA box [64 rows][64 columns] (128-byte
+// swizzle) is 64 contraction rows of 64 consecutive m (or n), so the
+// transposes cost nothing. Per block: A 16 KB, hi 16 KB, lo 16 KB; eight
+// M128 N128 K16 MMAs (four k-steps, hi then lo). Rows of the last block past
+// the expert's end are whatever follows in memory (the next expert's rows,
+// or the TMA's zero fill past the matrix): the MMA thread's warp overwrites
+// them with zeros in all three staged tiles before the MMAs read them, and
+// k-steps wholly past the end are skipped.
+//
+// Schedule: a persistent grid of one CTA per SM walks the tiles (expert,
+// m block, n block) with a stride of the grid size; every expert has the
+// same tile count and the tiles of one expert are adjacent, so the CTAs
+// running side by side share its operand rows through L2. Warp roles:
+// warp 0 TMA producer (4-stage ring of 48 KB), warp 1 TMEM allocation and
+// MMA issue, warps 2-5 epilogue (tcgen05.ld of their TMEM lane quadrant,
+// 32 x 32 fp32 blocks staged in shared memory, two buffers a warp, and
+// written by TMA stores clipped at the matrix edge; a block is written while
+// the previous one's store still reads the other buffer). Two 128-column accumulators let a tile's
+// epilogue overlap the next tile's main loop. Every wait is bounded; a
+// timeout sets kErrTimeout, drains the copies and MMAs in flight, frees
+// TMEM and exits.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace moe {
+namespace {
+
+using namespace ptx;
+
+namespace wg {
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int BOX_BYTES = BK * 64 * 2;     // [64 rows][64 columns] bf16
+constexpr int TILE_BYTES = 2 * BOX_BYTES;  // 128 m (or n) x 64 rows
+constexpr int STAGES = 4;
+constexpr int STAGE_BYTES = 3 * TILE_BYTES;  // A, hi, lo
+constexpr int NUM_ACC = 2;
+constexpr int TMEM_COLS = NUM_ACC * BN;
+constexpr int NUM_EPI = 4;
+constexpr int THREADS = 64 + 32 * NUM_EPI;
+constexpr int STG_BYTES = 32 * 32 * 4;  // one 32 x 32 fp32 block; two per epilogue warp
+constexpr int OFF_STG = STAGES * STAGE_BYTES;
+constexpr int OFF_BAR = OFF_STG + NUM_EPI * 2 * STG_BYTES;
+// full, empty, tfull, tempty, drain
+constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_SEG = OFF_MISC + 16;
+constexpr int SMEM_BYTES = OFF_SEG + (kMaxExperts + 1) * 4 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+// M128 N128, A and B both MN-major
+constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, true, true);
+
+struct Params {
+  const int32_t* offsets;
+  uint32_t* err;
+  int E, M, N, R;
+  int a_shared;
+  int tiles_m, tiles_n, total;
+};
+
+struct Tile {
+  int e, m0, n0;
+};
+
+__device__ __forceinline__ Tile decode(int t, const Params& p) {
+  const int per = p.tiles_m * p.tiles_n;
+  Tile r;
+  r.e = t / per;
+  const int l = t - r.e * per;
+  const int mb = l / p.tiles_n;
+  r.m0 = mb * BM;
+  r.n0 = (l - mb * p.tiles_n) * BN;
+  return r;
+}
+}  // namespace wg
+
+__global__ void __launch_bounds__(wg::THREADS, 1)
+    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmY, const wg::Params p) {
+  using namespace wg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + NUM_ACC;
+  uint64_t* drain = tempty + NUM_ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  int* s_ok = reinterpret_cast<int*>(smem + OFF_MISC + 4);
+  int* seg = reinterpret_cast<int*>(smem + OFF_SEG);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    for (int e = lane; e <= E; e += 32) seg[e] = __ldg(p.offsets + e);
+    __syncwarp();
+    bool bad = false;
+    for (int e = lane; e < E; e += 32) {
+      const int lo = seg[e], hi = seg[e + 1];
+      bad |= lo < 0 || hi < lo || hi > p.R;
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      // segments out of range: every expert is taken as empty (zeros out)
+      *s_ok = bad ? 0 : 1;
+      if (bad && blockIdx.x == 0) atomicOr(p.err, kErrBadIndex);
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(&full[i], 1);
+        mbar_init(&empty[i], 1);
+      }
+      for (int i = 0; i < NUM_ACC; ++i) {
+        mbar_init(&tfull[i], 1);
+        mbar_init(&tempty[i], NUM_EPI);
+      }
+      mbar_init(drain, 1);
+      fence_mbar_init();
+    }
+  } else if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const bool seg_ok = *s_ok != 0;
+  auto rows_of = [&](int e) { return seg_ok ? seg[e + 1] - seg[e] : 0; };
+  bool timed_out = false;
+
+  if (warp == 0) {
+    // -------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      int s = 0;
+      uint32_t ph = 0, armed = 0, armed_ph = 0;
+      for (int t = blockIdx.x; t < p.total && !timed_out; t += gridDim.x) {
+        const Tile tl = decode(t, p);
+        const int n = rows_of(tl.e);
+        if (n == 0) continue;
+        const int lo = seg[tl.e];
+        const int a0 = p.a_shared ? 0 : lo;
+        // 64-wide boxes that start inside the matrix (M a multiple of 64); the
+        // MMA's rows / columns from a skipped box, or from a box's part past
+        // N (the lo half's first columns, or zero fill), are never stored
+        const int na = min(2, (p.M - tl.m0) / 64), nb = min(2, (p.N - tl.n0 + 63) / 64);
+        const uint32_t bytes = static_cast<uint32_t>((na + 2 * nb) * BOX_BYTES);
+        const int nkb = (n + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+            timed_out = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          uint8_t* st = smem + s * STAGE_BYTES;
+          for (int c = 0; c < na; ++c)
+            tma_load_2d(st + c * BOX_BYTES, &tmA, &full[s], tl.m0 + c * 64, a0 + kb * BK);
+          for (int c = 0; c < nb; ++c) {
+            tma_load_2d(st + TILE_BYTES + c * BOX_BYTES, &tmB, &full[s], tl.n0 + c * 64,
+                        lo + kb * BK);
+            tma_load_2d(st + 2 * TILE_BYTES + c * BOX_BYTES, &tmB, &full[s], p.N + tl.n0 + c * 64,
+                        lo + kb * BK);
+          }
+          armed |= 1u << s;
+          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // no copy may still be landing when the CTA exits
+      for (int i = 0; i < STAGES; ++i)
+        if ((armed >> i) & 1u)
+          if (!mbar_wait_spin(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issue (whole warp waits)
+    int s = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
+    bool issued = false;
+    for (int t = blockIdx.x; t < p.total; t += gridDim.x) {
+      const Tile tl = decode(t, p);
+      const int n = rows_of(tl.e);
+      if (n == 0) continue;
+      if (!__all_sync(0xffffffffu, mbar_wait_spin(&tempty[acc], aph ^ 1u, kWaitLimitNs))) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const int nkb = (n + BK - 1) / BK;
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&full[s], ph, kWaitLimitNs))) {
+          timed_out = true;
+          break;
+        }
+        const int valid = min(BK, n - kb * BK);
+        const int ksteps = (valid + 15) / 16;
+        uint8_t* st = smem + s * STAGE_BYTES;
+        if (valid & 15) {
+          // rows [valid, 16 ksteps) of the last k-step belong to no row of
+          // this expert: zero them in the six boxes (row j of a box is its
+          // 128-byte line j; the swizzle permutes within the line)
+          const int z0 = valid * 128, per_box = (ksteps * 16 - valid) * 8;
+          for (int i = lane; i < 6 * per_box; i += 32) {
+            const int b = i / per_box, j = i - b * per_box;
+            *reinterpret_cast<uint4*>(st + b * BOX_BYTES + z0 + j * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_shared();
+        }
+        __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(st);
+          const uint32_t h_base = a_base + TILE_BYTES, l_base = a_base + 2 * TILE_BYTES;
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t ad = make_sdesc_sw128(a_base + kk * 2048, BOX_BYTES, 1024);
+            tc_mma_f16(d_tmem, ad, make_sdesc_sw128(h_base + kk * 2048, BOX_BYTES, 1024), IDESC,
+                       (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_f16(d_tmem, ad, make_sdesc_sw128(l_base + kk * 2048, BOX_BYTES, 1024), IDESC,
+                       1u);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+        issued = true;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (timed_out) break;
+      if (lane == 0) tc_commit(&tfull[acc]);
+      __syncwarp();
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+    if (timed_out && issued) {
+      // the MMAs in flight finish before TMEM is freed
+      if (lane == 0) tc_commit(drain);
+      __syncwarp();
+      mbar_wait_spin(drain, 0, kWaitLimitNs);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 = the tile's output rows
+    const int q = warp & 3;
+    uint8_t* stg0 = smem + OFF_STG + (warp - 2) * 2 * STG_BYTES;
+    int acc = 0;
+    uint32_t aph = 0;
+    bool stg_zero = false;  // buffer 0 holds zeros
+    int last = -1;          // buffer of the most recent store group
+    // before buffer b is rewritten, its last store has read it out
+    auto claim = [&](int b) {
+      if (lane == 0) {
+        if (last == b)
+          bulk_wait_group_read0();
+        else
+          bulk_wait_group_read1();
+      }
+      __syncwarp();
+    };
+    for (int t = blockIdx.x; t < p.total; t += gridDim.x) {
+      const Tile tl = decode(t, p);
+      const int n = rows_of(tl.e);
+      const int mrow = tl.m0 + q * 32;
+      const bool rows_in = mrow < p.M;
+      const int out_row = tl.e * p.M + mrow;
+      if (n == 0) {
+        // an expert with no rows: store zeros from a zeroed staging block
+        if (rows_in) {
+          if (!stg_zero) {
+            claim(0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              *reinterpret_cast<uint4*>(stg0 + lane * 128 + i * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_shared();
+            __syncwarp();
+            stg_zero = true;
+          }
+          if (lane == 0) {
+            for (int c = 0; c < BN / 32; ++c)
+              if (tl.n0 + c * 32 < p.N) tma_store_2d(&tmY, smem_u32(stg0), tl.n0 + c * 32, out_row);
+            bulk_commit_group();
+          }
+          last = 0;
+        }
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs))) {
+        timed_out = true;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      if (rows_in) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col = tl.n0 + c * 32;
+          if (col >= p.N) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tb + c * 32, v);
+          tmem_ld_wait();
+          const int b = c & 1;
+          claim(b);
+          uint8_t* stg = stg0 + b * STG_BYTES;
+          uint8_t* row_p = stg + lane * 128;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<uint4*>(row_p + ((i ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmY, smem_u32(stg), col, out_row);
+            bulk_commit_group();
+          }
+          last = b;
+          if (b == 0) stg_zero = false;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == NUM_ACC) {
+        acc = 0;
+        aph ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_group0();  // this warp's stores are done
+  }
+
+  if (timed_out) atomicOr(p.err, kErrTimeout);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+cudaError_t set_wgrad_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t st = cudaSuccess;
+  std::call_once(once, [] {
+    st = cudaFuncSetAttribute(wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              wg::SMEM_BYTES);
+  });
+  return st;
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void* Bs, int R, int E,
+                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
+                            int num_sms, cudaStream_t s) {
+  if (E <= 0) return cudaSuccess;
+  if (M <= 0 || N <= 0 || M % 64 != 0 || N % 8 != 0 || num_sms < 1 || E > kMaxExperts)
+    return cudaErrorInvalidValue;
+  if (R <= 0 || a_rows <= 0)  // no rows anywhere: every gradient is zero
+    return cudaMemsetAsync(out, 0, static_cast<size_t>(E) * M * N * 4, s);
+  CUtensorMap mA, mB, mY;
+  std::memset(&mA, 0, sizeof(mA));
+  std::memset(&mB, 0, sizeof(mB));
+  std::memset(&mY, 0, sizeof(mY));
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(M), 64, wg::BK) ||
+      !make_map_2d(&mB, Bs, static_cast<uint64_t>(R), 2 * static_cast<uint64_t>(N), 64, wg::BK) ||
+      !make_map_2d_out(&mY, out, static_cast<uint64_t>(E) * M, static_cast<uint64_t>(N), true))
+    return cudaErrorInvalidValue;
+  wg::Params prm;
+  prm.offsets = offsets;
+  prm.err = err;
+  prm.E = E;
+  prm.M = M;
+  prm.N = N;
+  prm.R = R;
+  prm.a_shared = a_shared;
+  prm.tiles_m = ceil_div(M, wg::BM);
+  prm.tiles_n = ceil_div(N, wg::BN);
+  prm.total = E * prm.tiles_m * prm.tiles_n;
+  cudaError_t st = set_wgrad_smem_attr();
+  if (st != cudaSuccess) return st;
+  const int grid = prm.total < num_sms ? prm.total : num_sms;
+  return launch_pdl(wgrad_tc_kernel, dim3(grid), dim3(wg::THREADS), wg::SMEM_BYTES, s, mA, mB, mY,
+                    prm);
+}
+
+}  // namespace moe

@@ -240,6 +240,10 @@ def test_backward_argument_errors(lib):
     bad = list(args(c, ws, bws))
     bad[7] = FAKE_ODD                                 # forward workspace misaligned
     assert lib.moe_backward(*bad) == L.MOE_ERR_INVALID_ARG
+    for i in (9, 10, 13):                             # dout, dx, dW1 misaligned
+        bad = list(args(c, ws, bws))
+        bad[i] = FAKE_ODD
+        assert lib.moe_backward(*bad) == L.MOE_ERR_INVALID_ARG
     # the FP8 payloads have no backward
     for c8 in (cfg(T=1024, d=4096, E=8, k=2, f=11008, payload_fp8=1),
                cfg(T=1024, d=4096, E=8, k=2, f=11008, output_fp8=1)):
