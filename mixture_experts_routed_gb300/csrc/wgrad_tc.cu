@@ -1,43 +1,55 @@
 // wgrad_tc.cu - the experts' weight gradients on the sm_103a tensor cores
-// (tcgen05 + TMEM, fed by TMA). In backpropagation the gradient reaches only
-// the activated experts (DeepSeek-V4 EP article, section 2.1), so each
-// expert's weight gradient is a sum over the rows routed to it:
+// (tcgen05 + TMEM, 2-SM pair mode, fed by TMA). In backpropagation the
+// gradient reaches only the activated experts (DeepSeek-V4 EP article,
+// section 2.1), so each expert's weight gradient is a sum over the rows
+// routed to it:
 //
 //   dW[e][m][n] = sum over r in [offsets[e], offsets[e+1]) of A[a(r)][m] * dB[r][n]
 //
 // with A the rows' bf16 activations (the dispatched tokens for dW1, the
-// stored SiLU output H for dW2; a(r) = r, or r - offsets[e] when every
-// expert reads the same rows) and dB their fp32 output gradient, held as two
-// bf16 parts dB = hi + lo ([R][2N]: columns [0, N) hi, [N, 2N) lo, the
-// split the dgrad GEMMs read; hi + lo carries dB to ~2^-17 relative). Both
-// parts go through the tensor cores into one fp32 accumulator, so the result
-// has the accuracy of an fp32 operand. Output fp32 [E][M][N]; an expert with
-// no rows gets zeros.
+// stored SiLU output H for dW2, the layer input for the gate's dW_g; a(r) =
+// r, or r - offsets[e] when every expert reads the same rows) and dB their
+// fp32 output gradient, held as two bf16 parts dB = hi + lo ([R][2N]:
+// columns [0, N) hi, [N, 2N) lo; hi + lo carries dB to ~2^-17 relative).
+// Both parts go through the tensor cores into one fp32 accumulator, so the
+// result has the accuracy of an fp32 operand. Output fp32 [E][M][N]; an
+// expert with no rows gets zeros.
 //
-// Tiles: 128 output rows (m) x 128 output columns (n) of one expert; the
+// Tiles: 256 output rows (m) x 256 output columns (n) of one expert, computed
+// by a cluster of two CTAs (one per SM of an SM pair) with one
+// tcgen05.mma.cta_group::2 M256 N256 K16 per k-step and operand part, issued
+// by the even CTA. CTA r stages only rows m0 + 128 r .. +127 of A and
+// columns n0 + 128 r .. +127 of hi and of lo, and its tensor memory receives
+// its 128 output rows; per SM this is half the shared-memory traffic per flop
+// of a one-CTA 128 x 128 tile (measured bound by that traffic). The
 // contraction runs over the expert's rows in blocks of 64 (ragged: the last
 // block holds n_e mod 64 rows). Both operands are read MN-major straight
 // from their row-major storage: a TMA box [64 rows][64 columns] (128-byte
 // swizzle) is 64 contraction rows of 64 consecutive m (or n), so the
-// transposes cost nothing. Per block: A 16 KB, hi 16 KB, lo 16 KB; eight
-// M128 N128 K16 MMAs (four k-steps, hi then lo). Rows of the last block past
-// the expert's end are whatever follows in memory (the next expert's rows,
-// or the TMA's zero fill past the matrix): the MMA thread's warp overwrites
-// them with zeros in all three staged tiles before the MMAs read them, and
+// transposes cost nothing. Per block and CTA: A 16 KB, hi 16 KB, lo 16 KB.
+//
+// Rows of the last block past the expert's end are whatever follows in
+// memory (the next expert's rows, or the TMA's zero fill past the matrix).
+// Each CTA's loads land on its own barrier; a forwarder warp waits for
+// them, overwrites those rows with zeros in the staged tiles (row j of a box
+// is its 128-byte line j; the swizzle permutes within the line), and
+// releases the stage to the MMA: the even CTA's by an arrive on the full
+// barrier, the odd CTA's by a 16-byte bulk copy into the even CTA whose
+// completion is counted on that barrier (a cluster-scope release arrive per
+// stage measured far slower in the FP8 prologue of the forward GEMM).
 // k-steps wholly past the end are skipped.
 //
-// Schedule: a persistent grid of one CTA per SM walks the tiles (expert,
-// m block, n block) with a stride of the grid size; every expert has the
-// same tile count and the tiles of one expert are adjacent, so the CTAs
-// running side by side share its operand rows through L2. Warp roles:
-// warp 0 TMA producer (4-stage ring of 48 KB), warp 1 TMEM allocation and
-// MMA issue, warps 2-5 epilogue (tcgen05.ld of their TMEM lane quadrant,
-// 32 x 32 fp32 blocks staged in shared memory, two buffers a warp, and
-// written by TMA stores clipped at the matrix edge; a block is written while
-// the previous one's store still reads the other buffer). Two 128-column accumulators let a tile's
-// epilogue overlap the next tile's main loop. Every wait is bounded; a
-// timeout sets kErrTimeout, drains the copies and MMAs in flight, frees
-// TMEM and exits.
+// Schedule: a persistent grid of as many clusters as fit at once walks the
+// tiles (expert, m block, n block) with a stride of the cluster count; every
+// expert has the same tile count and the tiles of one expert are adjacent,
+// so the clusters running side by side share its operand rows through L2.
+// Warp roles: warp 0 TMA producer (4-stage ring of 48 KB), warp 1 TMEM
+// allocation (both CTAs) and MMA issue (even CTA), warp 2 forwarder, warps
+// 3-6 epilogue (tcgen05.ld of their TMEM lane quadrant, 32 x 32 fp32 blocks
+// staged in shared memory, two buffers a warp, written by TMA stores clipped
+// at the matrix edge). Two 256-column accumulators let a tile's epilogue
+// overlap the next tile's main loop. Every wait is bounded; a timeout sets
+// kErrTimeout, drains the copies and MMAs in flight, frees TMEM and exits.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -55,25 +67,28 @@ namespace {
 using namespace ptx;
 
 namespace wg {
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int BOX_BYTES = BK * 64 * 2;     // [64 rows][64 columns] bf16
-constexpr int TILE_BYTES = 2 * BOX_BYTES;  // 128 m (or n) x 64 rows
+constexpr int BM = 256, BN = 256, BK = 64;  // pair tile; a CTA holds half of M and of N
+constexpr int BOX_BYTES = BK * 64 * 2;      // [64 rows][64 columns] bf16
+constexpr int HALF_BYTES = 2 * BOX_BYTES;   // this CTA's 128 m (or n) x 64 rows
 constexpr int STAGES = 4;
-constexpr int STAGE_BYTES = 3 * TILE_BYTES;  // A, hi, lo
+constexpr int STAGE_BYTES = 3 * HALF_BYTES;  // A, hi, lo
 constexpr int NUM_ACC = 2;
-constexpr int TMEM_COLS = NUM_ACC * BN;
+constexpr int ACC_COLS = BN;
+constexpr int TMEM_COLS = NUM_ACC * ACC_COLS;
 constexpr int NUM_EPI = 4;
-constexpr int THREADS = 64 + 32 * NUM_EPI;
+constexpr int EPI_WARP0 = 3;
+constexpr int THREADS = 32 * (EPI_WARP0 + NUM_EPI);
 constexpr int STG_BYTES = 32 * 32 * 4;  // one 32 x 32 fp32 block; two per epilogue warp
 constexpr int OFF_STG = STAGES * STAGE_BYTES;
 constexpr int OFF_BAR = OFF_STG + NUM_EPI * 2 * STG_BYTES;
-// full, empty, tfull, tempty, drain
-constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
+// lfull, full, empty, tfull, tempty, drain
+constexpr int NUM_BARS = 3 * STAGES + 2 * NUM_ACC + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_SEG = OFF_MISC + 16;
+constexpr int OFF_SINK = (OFF_MISC + 16 + 15) & ~15;  // 16 bytes the odd CTA's releases copy
+constexpr int OFF_SEG = OFF_SINK + 16;
 constexpr int SMEM_BYTES = OFF_SEG + (kMaxExperts + 1) * 4 + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-// M128 N128, A and B both MN-major
+// M256 N256 (pair), A and B both MN-major
 constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, BN, true, true);
 
 struct Params {
@@ -98,25 +113,41 @@ __device__ __forceinline__ Tile decode(int t, const Params& p) {
   r.n0 = (l - mb * p.tiles_n) * BN;
   return r;
 }
+
+// Ring position over the k-blocks of a CTA's tiles (every role walks the
+// same sequence).
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next() {
+    if (++s == STAGES) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
 }  // namespace wg
 
 __global__ void __launch_bounds__(wg::THREADS, 1)
-    wgrad_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmY, const wg::Params p) {
+    wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmY, const wg::Params p) {
   using namespace wg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + NUM_ACC;
+  uint64_t* lfull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // this CTA's loads landed
+  uint64_t* full = lfull + STAGES;     // even CTA: both CTAs' stages released
+  uint64_t* empty = full + STAGES;     // both CTAs, from one multicast commit
+  uint64_t* tfull = empty + STAGES;    // both CTAs, multicast commit
+  uint64_t* tempty = tfull + NUM_ACC;  // even CTA: every epilogue warp of both CTAs
   uint64_t* drain = tempty + NUM_ACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* s_ok = reinterpret_cast<int*>(smem + OFF_MISC + 4);
   int* seg = reinterpret_cast<int*>(smem + OFF_SEG);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cl = static_cast<int>(blockIdx.x >> 1), ncl = static_cast<int>(gridDim.x >> 1);
   const int E = p.E;
   pdl_wait();
   pdl_trigger();
@@ -135,21 +166,23 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
       *s_ok = bad ? 0 : 1;
       if (bad && blockIdx.x == 0) atomicOr(p.err, kErrBadIndex);
       for (int i = 0; i < STAGES; ++i) {
+        mbar_init(&lfull[i], 1);
         mbar_init(&full[i], 1);
         mbar_init(&empty[i], 1);
       }
       for (int i = 0; i < NUM_ACC; ++i) {
         mbar_init(&tfull[i], 1);
-        mbar_init(&tempty[i], NUM_EPI);
+        mbar_init(&tempty[i], 2 * NUM_EPI);
       }
       mbar_init(drain, 1);
       fence_mbar_init();
     }
   } else if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const bool seg_ok = *s_ok != 0;
@@ -157,127 +190,166 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
   bool timed_out = false;
 
   if (warp == 0) {
-    // -------------------------------------------------------------- TMA producer
+    // -------------------------------------------------------------- TMA producer (both CTAs)
     if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      int s = 0;
-      uint32_t ph = 0, armed = 0, armed_ph = 0;
-      for (int t = blockIdx.x; t < p.total && !timed_out; t += gridDim.x) {
+      Ring rg;
+      uint32_t armed = 0, armed_ph = 0;
+      for (int t = cl; t < p.total && !timed_out; t += ncl) {
         const Tile tl = decode(t, p);
         const int n = rows_of(tl.e);
         if (n == 0) continue;
         const int lo = seg[tl.e];
         const int a0 = p.a_shared ? 0 : lo;
-        // 64-wide boxes that start inside the matrix (M a multiple of 64); the
-        // MMA's rows / columns from a skipped box, or from a box's part past
-        // N (the lo half's first columns, or zero fill), are never stored
-        const int na = min(2, (p.M - tl.m0) / 64), nb = min(2, (p.N - tl.n0 + 63) / 64);
+        // this CTA's halves: 64-wide boxes that start inside the matrix (M a
+        // multiple of 64); the MMA's rows / columns from a skipped box, or
+        // from a box's part past N, are never stored
+        const int mh = tl.m0 + static_cast<int>(rank) * 128;
+        const int nh = tl.n0 + static_cast<int>(rank) * 128;
+        const int na = mh < p.M ? min(2, (p.M - mh) / 64) : 0;
+        const int nb = nh < p.N ? min(2, (p.N - nh + 63) / 64) : 0;
         const uint32_t bytes = static_cast<uint32_t>((na + 2 * nb) * BOX_BYTES);
         const int nkb = (n + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
+          if (!mbar_wait_spin(&empty[rg.s], rg.ph ^ 1u, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], bytes);
-          uint8_t* st = smem + s * STAGE_BYTES;
+          uint64_t* bar = &lfull[rg.s];
+          mbar_arrive_expect_tx(bar, bytes);
+          uint8_t* st = smem + rg.s * STAGE_BYTES;
           for (int c = 0; c < na; ++c)
-            tma_load_2d(st + c * BOX_BYTES, &tmA, &full[s], tl.m0 + c * 64, a0 + kb * BK);
+            tma_load_2d(st + c * BOX_BYTES, &tmA, bar, mh + c * 64, a0 + kb * BK);
           for (int c = 0; c < nb; ++c) {
-            tma_load_2d(st + TILE_BYTES + c * BOX_BYTES, &tmB, &full[s], tl.n0 + c * 64,
-                        lo + kb * BK);
-            tma_load_2d(st + 2 * TILE_BYTES + c * BOX_BYTES, &tmB, &full[s], p.N + tl.n0 + c * 64,
+            tma_load_2d(st + HALF_BYTES + c * BOX_BYTES, &tmB, bar, nh + c * 64, lo + kb * BK);
+            tma_load_2d(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, bar, p.N + nh + c * 64,
                         lo + kb * BK);
           }
-          armed |= 1u << s;
-          armed_ph = (armed_ph & ~(1u << s)) | (ph << s);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
+          armed |= 1u << rg.s;
+          armed_ph = (armed_ph & ~(1u << rg.s)) | (rg.ph << rg.s);
+          rg.next();
         }
       }
       // no copy may still be landing when the CTA exits
       for (int i = 0; i < STAGES; ++i)
         if ((armed >> i) & 1u)
-          if (!mbar_wait_spin(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
+          if (!mbar_wait_spin(&lfull[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
     }
   } else if (warp == 1) {
-    // -------------------------------------------------------------- MMA issue (whole warp waits)
-    int s = 0, acc = 0;
-    uint32_t ph = 0, aph = 0;
-    bool issued = false;
-    for (int t = blockIdx.x; t < p.total; t += gridDim.x) {
+    if (rank == 0) {
+      // ------------------------------------------------------------ MMA issue (even CTA, whole warp waits)
+      Ring rg;
+      int acc = 0;
+      uint32_t aph = 0;
+      bool issued = false;
+      for (int t = cl; t < p.total; t += ncl) {
+        const Tile tl = decode(t, p);
+        const int n = rows_of(tl.e);
+        if (n == 0) continue;
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&tempty[acc], aph ^ 1u, kWaitLimitNs))) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+        const int nkb = (n + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          // released by both CTAs' forwarders (the odd one's bytes at cluster scope)
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_spin_cluster(&full[rg.s], rg.ph, kWaitLimitNs))) {
+            timed_out = true;
+            break;
+          }
+          if (lane == 0) {
+            tc_fence_after();
+            const int ksteps = (min(BK, n - kb * BK) + 15) / 16;
+            const uint32_t a_base = smem_u32(smem + rg.s * STAGE_BYTES);
+            const uint32_t h_base = a_base + HALF_BYTES, l_base = a_base + 2 * HALF_BYTES;
+            for (int kk = 0; kk < ksteps; ++kk) {
+              const uint64_t ad = make_sdesc_sw128(a_base + kk * 2048, BOX_BYTES, 1024);
+              tc_mma_f16_pair(d_tmem, ad, make_sdesc_sw128(h_base + kk * 2048, BOX_BYTES, 1024),
+                              IDESC, (kb | kk) != 0 ? 1u : 0u);
+              tc_mma_f16_pair(d_tmem, ad, make_sdesc_sw128(l_base + kk * 2048, BOX_BYTES, 1024),
+                              IDESC, 1u);
+            }
+            tc_commit_pair_mc(&empty[rg.s], 0x3);
+          }
+          __syncwarp();
+          issued = true;
+          rg.next();
+        }
+        if (timed_out) break;
+        if (lane == 0) tc_commit_pair_mc(&tfull[acc], 0x3);
+        __syncwarp();
+        if (++acc == NUM_ACC) {
+          acc = 0;
+          aph ^= 1u;
+        }
+      }
+      if (timed_out && issued) {
+        // the MMAs in flight finish before TMEM is freed
+        if (lane == 0) tc_commit_pair_mc(drain, 0x1);
+        __syncwarp();
+        mbar_wait_spin(drain, 0, kWaitLimitNs);
+      }
+    }
+  } else if (warp == 2) {
+    // -------------------------------------------------------------- forwarder (both CTAs)
+    const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
+    const uint32_t leader_sink = mapa_shared(smem_u32(smem + OFF_SINK), 0);
+    const uint32_t my_sink = smem_u32(smem + OFF_SINK);
+    Ring rg;
+    uint32_t armed = 0, armed_ph = 0;
+    for (int t = cl; t < p.total && !timed_out; t += ncl) {
       const Tile tl = decode(t, p);
       const int n = rows_of(tl.e);
       if (n == 0) continue;
-      if (!__all_sync(0xffffffffu, mbar_wait_spin(&tempty[acc], aph ^ 1u, kWaitLimitNs))) {
-        timed_out = true;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       const int nkb = (n + BK - 1) / BK;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait_spin(&full[s], ph, kWaitLimitNs))) {
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&lfull[rg.s], rg.ph, kWaitLimitNs))) {
           timed_out = true;
           break;
         }
         const int valid = min(BK, n - kb * BK);
         const int ksteps = (valid + 15) / 16;
-        uint8_t* st = smem + s * STAGE_BYTES;
         if (valid & 15) {
           // rows [valid, 16 ksteps) of the last k-step belong to no row of
-          // this expert: zero them in the six boxes (row j of a box is its
-          // 128-byte line j; the swizzle permutes within the line)
+          // this expert: zeros in this CTA's six boxes
+          uint8_t* st = smem + rg.s * STAGE_BYTES;
           const int z0 = valid * 128, per_box = (ksteps * 16 - valid) * 8;
           for (int i = lane; i < 6 * per_box; i += 32) {
             const int b = i / per_box, j = i - b * per_box;
             *reinterpret_cast<uint4*>(st + b * BOX_BYTES + z0 + j * 16) = make_uint4(0, 0, 0, 0);
           }
-          fence_proxy_async_shared();
         }
+        fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0) {
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(st);
-          const uint32_t h_base = a_base + TILE_BYTES, l_base = a_base + 2 * TILE_BYTES;
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t ad = make_sdesc_sw128(a_base + kk * 2048, BOX_BYTES, 1024);
-            tc_mma_f16(d_tmem, ad, make_sdesc_sw128(h_base + kk * 2048, BOX_BYTES, 1024), IDESC,
-                       (kb | kk) != 0 ? 1u : 0u);
-            tc_mma_f16(d_tmem, ad, make_sdesc_sw128(l_base + kk * 2048, BOX_BYTES, 1024), IDESC,
-                       1u);
-          }
-          tc_commit(&empty[s]);
+          if (rank == 0)
+            mbar_arrive_expect_tx(&full[rg.s], 16u);  // + the odd CTA's 16 bytes
+          else
+            bulk_copy_s2cluster(leader_sink, my_sink, 16u,
+                                leader_full + static_cast<uint32_t>(rg.s * 8));
         }
-        __syncwarp();
-        issued = true;
-        if (++s == STAGES) {
-          s = 0;
-          ph ^= 1u;
-        }
-      }
-      if (timed_out) break;
-      if (lane == 0) tc_commit(&tfull[acc]);
-      __syncwarp();
-      if (++acc == NUM_ACC) {
-        acc = 0;
-        aph ^= 1u;
+        armed |= 1u << rg.s;
+        armed_ph = (armed_ph & ~(1u << rg.s)) | (rg.ph << rg.s);
+        rg.next();
       }
     }
-    if (timed_out && issued) {
-      // the MMAs in flight finish before TMEM is freed
-      if (lane == 0) tc_commit(drain);
-      __syncwarp();
-      mbar_wait_spin(drain, 0, kWaitLimitNs);
-    }
+    // even CTA: the odd CTA's release copies have landed before either exits
+    if (rank == 0)
+      for (int i = 0; i < STAGES; ++i)
+        if ((armed >> i) & 1u)
+          if (!mbar_wait_spin_cluster(&full[i], (armed_ph >> i) & 1u, kWaitLimitNs))
+            timed_out = true;
   } else {
-    // -------------------------------------------------------------- epilogue
-    // warp w reads TMEM lanes 32 (w % 4) .. +31 = the tile's output rows
+    // -------------------------------------------------------------- epilogue (both CTAs)
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 = this CTA's output rows
+    // m0 + 128 rank + 32 (w % 4) + lane; columns = the tile's 256 n
     const int q = warp & 3;
-    uint8_t* stg0 = smem + OFF_STG + (warp - 2) * 2 * STG_BYTES;
+    const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    uint8_t* stg0 = smem + OFF_STG + (warp - EPI_WARP0) * 2 * STG_BYTES;
     int acc = 0;
     uint32_t aph = 0;
     bool stg_zero = false;  // buffer 0 holds zeros
@@ -292,10 +364,10 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
       }
       __syncwarp();
     };
-    for (int t = blockIdx.x; t < p.total; t += gridDim.x) {
+    for (int t = cl; t < p.total; t += ncl) {
       const Tile tl = decode(t, p);
       const int n = rows_of(tl.e);
-      const int mrow = tl.m0 + q * 32;
+      const int mrow = tl.m0 + static_cast<int>(rank) * 128 + q * 32;
       const bool rows_in = mrow < p.M;
       const int out_row = tl.e * p.M + mrow;
       if (n == 0) {
@@ -325,7 +397,7 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
       }
       tc_fence_after();
       const uint32_t tb =
-          tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(q * 32) << 16);
+          tmem_base + static_cast<uint32_t>(acc * ACC_COLS) + (static_cast<uint32_t>(q * 32) << 16);
       if (rows_in) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -354,7 +426,12 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&tempty[acc]);
+        else
+          mbar_arrive_remote(leader_tempty + static_cast<uint32_t>(acc * 8));
+      }
       if (++acc == NUM_ACC) {
         acc = 0;
         aph ^= 1u;
@@ -365,9 +442,10 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
 
   if (timed_out) atomicOr(p.err, kErrTimeout);
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal or read it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -375,10 +453,28 @@ cudaError_t set_wgrad_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(wgrad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    st = cudaFuncSetAttribute(wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               wg::SMEM_BYTES);
   });
   return st;
+}
+
+// Clusters of two that can be resident at once (cached per device): a
+// persistent grid must fit at once (a pair needs two free SMs of one GPC).
+int resident_clusters(const cudaLaunchConfig_t& lc_in, int num_sms) {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+  if (cache[dev] > 0) return cache[dev];
+  cudaLaunchConfig_t lc = lc_in;
+  lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, wgrad_pair_kernel, &lc) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = num_sms / 2;
+  }
+  cache[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -387,7 +483,7 @@ cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void*
                             int M, int N, const int32_t* offsets, float* out, uint32_t* err,
                             int num_sms, cudaStream_t s) {
   if (E <= 0) return cudaSuccess;
-  if (M <= 0 || N <= 0 || M % 64 != 0 || N % 8 != 0 || num_sms < 1 || E > kMaxExperts)
+  if (M <= 0 || N <= 0 || M % 64 != 0 || N % 8 != 0 || num_sms < 2 || E > kMaxExperts)
     return cudaErrorInvalidValue;
   if (R <= 0 || a_rows <= 0)  // no rows anywhere: every gradient is zero
     return cudaMemsetAsync(out, 0, static_cast<size_t>(E) * M * N * 4, s);
@@ -412,9 +508,23 @@ cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void*
   prm.total = E * prm.tiles_m * prm.tiles_n;
   cudaError_t st = set_wgrad_smem_attr();
   if (st != cudaSuccess) return st;
-  const int grid = prm.total < num_sms ? prm.total : num_sms;
-  return launch_pdl(wgrad_tc_kernel, dim3(grid), dim3(wg::THREADS), wg::SMEM_BYTES, s, mA, mB, mY,
-                    prm);
+  cudaLaunchConfig_t lc = {};
+  lc.blockDim = dim3(wg::THREADS);
+  lc.dynamicSmemBytes = wg::SMEM_BYTES;
+  lc.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  const int resident = resident_clusters(lc, num_sms);
+  const int clusters = prm.total < resident ? prm.total : resident;
+  lc.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+  return cudaLaunchKernelEx(&lc, wgrad_pair_kernel, mA, mB, mY, prm);
 }
 
 }  // namespace moe
