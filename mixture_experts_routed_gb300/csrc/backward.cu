@@ -424,25 +424,6 @@ __global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, 
 // parts against the same bf16 weight or activation, so the products are
 // exact and the sums fp32.
 
-// dZ = dH * SiLU'(Z) as the bf16 split [R][2N] = [hi | lo] (the operand of
-// the tensor-core dgrad and weight-gradient GEMMs)
-__global__ void __launch_bounds__(256) silu_bwd_kernel(const float* __restrict__ dH,
-                                                       const float* __restrict__ Z, size_t n,
-                                                       int N, __nv_bfloat16* __restrict__ dZs) {
-  pdl_wait();
-  pdl_trigger();
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const float z = __ldg(Z + i);
-    const float sg = 1.f / (1.f + expf(-z));
-    const float v = __ldg(dH + i) * (sg * (1.f + z * (1.f - sg)));
-    const size_t r = i / N, c = i - r * N;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    dZs[r * 2 * N + c] = hi;
-    dZs[r * 2 * N + N + c] = __float2bfloat16_rn(v - __bfloat162float(hi));
-  }
-}
-
 // ---------------------------------------------------------------- bias, dx
 // db[e] = sum_t dL[t, e]. A CTA of 32 warps takes 32 experts (lane = expert,
 // so each warp reads 128 contiguous bytes of a row of dL); warp w sums the
@@ -508,15 +489,6 @@ cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, cons
   return launch_pdl(combine_bwd_kernel<__nv_bfloat16>, dim3(T), dim3(128), 0, s,
                     static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys, dw,
                     err, zero, nzero, seg01);
-}
-
-cudaError_t launch_silu_bwd(const float* dH, const float* Z, int R, int N, void* dZs,
-                            cudaStream_t s) {
-  const size_t n = static_cast<size_t>(R) * N;
-  if (n == 0) return cudaSuccess;
-  const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 152 * 16));
-  return launch_pdl(silu_bwd_kernel, dim3(blocks), dim3(256), 0, s, dH, Z, n, N,
-                    static_cast<__nv_bfloat16*>(dZs));
 }
 
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,

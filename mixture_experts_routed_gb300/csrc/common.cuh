@@ -160,9 +160,6 @@ cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, cons
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
                                float* dw, uint32_t* err, uint32_t* zero, int nzero,
                                int32_t* seg01, cudaStream_t s);
-// dZ = dH * SiLU'(Z) ([R, N] fp32 in) as the bf16 split [R][2N] = [hi | lo].
-cudaError_t launch_silu_bwd(const float* dH, const float* Z, int R, int N, void* dZs,
-                            cudaStream_t s);
 // dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec),
 // and, when dLs is non-null, its bf16 split [T][2E] = [hi | lo].
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
@@ -175,13 +172,14 @@ cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W,
                            cudaStream_t s);
 // out[e] = A_e^T . B_e over each segment's rows (A [*, M] dtype adtype,
 // shared rows when a_shared; B fp32 [R, N]); out [E][M][N].
-// The same GEMM (fp32 output, no activation) with the weights stored
-// transposed: out[r] = A[r] . W_e^T, W bf16 [E][N][k_wrap]
-// row-major, A bf16 [R, K] with K = k_wrap or 2 k_wrap (k >= k_wrap reads
-// weight column k - k_wrap: the hi | lo operand split against one weight).
+// The same GEMM with the weights stored transposed: y[r] = A[r] . W_e^T,
+// W bf16 [E][N][k_wrap] row-major, A bf16 [R, K] with K = k_wrap or
+// 2 k_wrap (k >= k_wrap reads weight column k - k_wrap: the hi | lo operand
+// split against one weight). zin null: out = y, fp32 [R, N]; else out =
+// the bf16 split [R][2N] = [hi | lo] of y * SiLU'(zin) (zin fp32 [R, N]).
 cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K, int k_wrap,
-                              int N, const int32_t* offsets, float* out, uint32_t* err,
-                              uint32_t* tile_ctr, int num_sms, cudaStream_t s);
+                              int N, const int32_t* offsets, const float* zin, void* out,
+                              uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s);
 
 // The experts' weight gradients on the tensor cores (wgrad_tc.cu):
 // out[e] = A_e^T . (Bs_e[:, :N] + Bs_e[:, N:]) over the rows of expert e's

@@ -5,7 +5,10 @@
 // section):
 //   W1 pass: H[r] = SiLU(s_r * A[r] . W1[e])  -> bf16   (epi 0)
 //   W2 pass: Y[r] = H[r] . W2[e]              -> fp32   (epi 1)
-// for the rows r of each expert's segment [offsets[e], offsets[e+1]).
+// for the rows r of each expert's segment [offsets[e], offsets[e+1]); the
+// backward's dgrad uses it too (fp32 out, or epi 2: dZ[r] = (A[r] . W[e]) *
+// SiLU'(Z[r]) written as its bf16 split [hi | lo], the operand of the next
+// GEMMs).
 //
 // Work split. A cluster of two CTAs (one per SM of an SM pair) computes a
 // pair tile of 256 token rows x 256 output features with one
@@ -69,6 +72,7 @@ using namespace ptx;
 struct TcParams {
   const int32_t* offsets;
   const float* row_scale;
+  const float* zin;    // epi 2: the pre-activation Z [R, N] (fp32)
   void* out;
   uint32_t* err;
   uint32_t* tile_ctr;  // next tile to hand out; zero before the launch
@@ -79,6 +83,25 @@ struct TcParams {
   int k_wrap;          // BT: columns of the stored weight; k-block kb reads
                        // columns (64 kb) mod k_wrap (K = 2 k_wrap stacks it twice)
 };
+
+// SiLU'(z) = s (1 + z (1 - s)), s = sigmoid(z), in the same fp32 steps as
+// the backward's element-wise kernel
+__device__ __forceinline__ float silu_grad(float z) {
+  const float sg = 1.f / (1.f + expf(-z));
+  return sg * (1.f + z * (1.f - sg));
+}
+// v = hi + lo, hi = bf16(v), lo = bf16(v - hi), two values packed per word
+__device__ __forceinline__ void split2(float a, float b, uint32_t* hi, uint32_t* lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  *hi = *reinterpret_cast<const uint32_t*>(&h);
+  *lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__device__ __forceinline__ void split1(float v, __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  *hi = __float2bfloat16_rn(v);
+  *lo = __float2bfloat16_rn(v - __bfloat162float(*hi));
+}
 
 // z * sigmoid(z) with the approximate divide: the result is rounded to bf16,
 // far coarser than the few-ulp error of __expf / __fdividef. For z < -87 the
@@ -179,7 +202,7 @@ struct Shape {
 // writes it with one TMA store: whole row segments instead of 16-byte pieces
 // of 32 different rows per store instruction.
 template <int EPI>
-__host__ __device__ constexpr int stg_bytes() { return EPI == 1 ? 32 * 32 * 4 : 32 * 32 * 2; }
+__host__ __device__ constexpr int stg_bytes() { return EPI == 0 ? 32 * 32 * 2 : 32 * 32 * 4; }
 template <int NB>
 __host__ __device__ constexpr int off_stg() {
   return (Shape<NB>::SMEM_USED + 1023) & ~1023;
@@ -189,7 +212,8 @@ __host__ __device__ constexpr int smem_bytes() {
   return off_stg<NB>() + num_epi_warps<EPI>() * stg_bytes<EPI>() + 1024;
 }
 static_assert(smem_bytes<0, 1>() <= 227 * 1024 && smem_bytes<0, 2>() <= 227 * 1024 &&
-                  smem_bytes<1, 1>() <= 227 * 1024 && smem_bytes<1, 2>() <= 227 * 1024,
+                  smem_bytes<1, 1>() <= 227 * 1024 && smem_bytes<1, 2>() <= 227 * 1024 &&
+                  smem_bytes<2, 1>() <= 227 * 1024,
               "shared memory");
 
 // Descriptor of this CTA's staged weights at k-step kk: MN-major (two
@@ -667,6 +691,51 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
           uint32_t v[32];
           tmem_ld_32x32b_x32(tbase + c * 32, v);
           tmem_ld_wait();
+          if constexpr (EPI == 2) {
+            // dZ = dH * SiLU'(Z) for this row's 32 columns, split hi | lo
+            if (!valid) continue;  // (tma_rows: every lane valid)
+            uint32_t hi[16], lo[16];
+            const float4* zr = reinterpret_cast<const float4*>(p.zin + grow * p.N + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 z = __ldg(zr + i);
+              split2(__uint_as_float(v[4 * i]) * silu_grad(z.x),
+                     __uint_as_float(v[4 * i + 1]) * silu_grad(z.y), &hi[2 * i], &lo[2 * i]);
+              split2(__uint_as_float(v[4 * i + 2]) * silu_grad(z.z),
+                     __uint_as_float(v[4 * i + 3]) * silu_grad(z.w), &hi[2 * i + 1],
+                     &lo[2 * i + 1]);
+            }
+            if (tma_rows) {
+              // two bf16 32 x 32 blocks (64-byte rows, 64-byte swizzle):
+              // hi at column col, lo at N + col of the [R, 2N] output
+              if (lane == 0) bulk_wait_group_read0();
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int o = lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
+                *reinterpret_cast<uint4*>(stg + o) =
+                    make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+                *reinterpret_cast<uint4*>(stg + 2048 + o) =
+                    make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+              }
+              fence_proxy_async_shared();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmY, smem_u32(stg), col, wrow0);
+                tma_store_2d(&tmY, smem_u32(stg + 2048), p.N + col, wrow0);
+                bulk_commit_group();
+              }
+              continue;
+            }
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                  grow * 2 * p.N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              dst[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+              dst[i + p.N / 8] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+            }
+            continue;
+          }
           if (EPI == 1 && tma_rows) {
             // the previous store of this block has read it out
             if (lane == 0) bulk_wait_group_read0();
@@ -751,6 +820,22 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
                   out[static_cast<size_t>(jj) * p.N] =
                       __float2bfloat16_rn(silu(__uint_as_float(v[jj]) * sj));
               }
+            } else if constexpr (EPI == 2) {
+              __nv_bfloat16* out =
+                  static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(trow) * 2 * p.N + f;
+              // every Z load issued before the first store
+              float z[32];
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                z[jj] = jj < t.tail && f_ok
+                            ? __ldg(p.zin + static_cast<size_t>(trow + jj) * p.N + f)
+                            : 0.f;
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj)
+                if (jj < t.tail && f_ok) {
+                  __nv_bfloat16* o = out + static_cast<size_t>(jj) * 2 * p.N;
+                  split1(__uint_as_float(v[jj]) * silu_grad(z[jj]), o, o + p.N);
+                }
             } else {
               float* out = static_cast<float*>(p.out) + base;
 #pragma unroll
@@ -787,6 +872,20 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
                 out[static_cast<size_t>(jj) * p.N] =
                     __float2bfloat16_rn(silu(__uint_as_float(v[jj]) * sj));
             }
+          } else if constexpr (EPI == 2) {
+            const size_t r0 = static_cast<size_t>(t.row0) + tok0;
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + r0 * 2 * p.N + f;
+            // every Z load issued before the first store
+            float z[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              z[jj] = jj < nt && f_ok ? __ldg(p.zin + (r0 + jj) * p.N + f) : 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              if (jj < nt && f_ok) {
+                __nv_bfloat16* o = out + static_cast<size_t>(jj) * 2 * p.N;
+                split1(__uint_as_float(v[jj]) * silu_grad(z[jj]), o, o + p.N);
+              }
           } else {
             float* out = static_cast<float*>(p.out) + base;
 #pragma unroll
@@ -1087,6 +1186,7 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
   TcParams prm;
   prm.offsets = offsets;
   prm.row_scale = row_scale;
+  prm.zin = nullptr;
   prm.out = out;
   prm.err = err;
   prm.tile_ctr = tile_ctr;
@@ -1113,10 +1213,10 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 }
 
 cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K, int k_wrap,
-                              int N, const int32_t* offsets, float* out, uint32_t* err,
-                              uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
+                              int N, const int32_t* offsets, const float* zin, void* out,
+                              uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
-  if (num_sms < 2 || k_wrap <= 0 || k_wrap % 64 != 0 || K % k_wrap != 0)
+  if (num_sms < 2 || k_wrap <= 0 || k_wrap % 64 != 0 || K % k_wrap != 0 || N % 8 != 0)
     return cudaErrorInvalidValue;
   CUtensorMap mA, mA8, mB, mY;
   std::memset(&mA, 0, sizeof(mA));
@@ -1128,11 +1228,13 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128) ||
       !make_map_2d(&mA8, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 8) ||
       !make_map_2d(&mB, Wt, static_cast<uint64_t>(E) * N, static_cast<uint64_t>(k_wrap), 64, 128) ||
-      !make_map_2d_out(&mY, out, static_cast<uint64_t>(R), static_cast<uint64_t>(N), true))
+      !make_map_2d_out(&mY, out, static_cast<uint64_t>(R),
+                       static_cast<uint64_t>(zin ? 2 * N : N), zin == nullptr))
     return cudaErrorInvalidValue;
   TcParams prm;
   prm.offsets = offsets;
   prm.row_scale = nullptr;
+  prm.zin = zin;
   prm.out = out;
   prm.err = err;
   prm.tile_ctr = tile_ctr;
@@ -1144,7 +1246,8 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   prm.a_rows = R;
   prm.a_shared = 0;
   prm.k_wrap = k_wrap;
-  return launch_pair<1, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s);
+  return zin ? launch_pair<2, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s)
+             : launch_pair<1, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s);
 }
 
 }  // namespace moe

@@ -258,9 +258,9 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // segment {0, T} of the gate GEMMs, dY (fp32 layers), the recomputed
 // pre-activation Z (fp32 layers overwrite it with dZ), dX_perm and the gate
 // part of dx, all fp32 but the ints; bf16 layers add the tensor-core GEMMs'
-// operands: the bf16 splits of dY, dZ and dL, and dH.
+// operands: the bf16 splits of dY, dZ and dL.
 struct BwdLayout {
-  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, dYs, dH, dZs, dLs, total;
+  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, dYs, dZs, dLs, total;
 };
 
 BwdLayout bwd_layout_of(const moe_config_t& c) {
@@ -285,7 +285,6 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.dXp = take(R * c.d * 4);
   B.dxg = take(T * c.d * 4);
   B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
-  B.dH = take(tc ? R * c.f * 4 : 0);
   B.dZs = take(tc ? R * 2 * c.f * 2 : 0);
   B.dLs = take(tc ? T * 2 * E * 2 : 0);
   B.total = o;
@@ -356,8 +355,8 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   // (dx_gate: W_g read K-major, K = E a multiple of 64; dW_g: E a multiple
   // of 8), else fp32 FMA.
   if (e == cudaSuccess)
-    e = tc && E % 64 == 0 ? launch_gemm_tc_wt(dLs, T, Wg, 1, 2 * E, E, d, seg01, dxg, err, ctr + 3,
-                                              sms, s)
+    e = tc && E % 64 == 0 ? launch_gemm_tc_wt(dLs, T, Wg, 1, 2 * E, E, d, seg01, nullptr, dxg,
+                                              err, ctr + 3, sms, s)
                           : launch_gemm_nt(dt, false, dL, Wg, 1, T, E, d, seg01, dxg, err, s);
   if (e == cudaSuccess)
     e = tc && E % 8 == 0 ? launch_wgrad_tc(x, T, 0, dLs, T, 1, d, E, seg01, dWg, err, sms, s)
@@ -375,16 +374,15 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
     } else {
       e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
                          nullptr, Z, err, ctr, sms, s);
-      // dH = [dY hi | dY lo] . [W2_e^T ; W2_e^T] and dX_perm likewise with
-      // W1_e: the stored weights read K-major, K = 2d (2f) wrapping at d (f)
-      float* dH = at<float>(bws, B.dH);
+      // dH = [dY hi | dY lo] . [W2_e^T ; W2_e^T], its epilogue writing the
+      // split of dZ = dH * SiLU'(Z); dX_perm = [dZ hi | dZ lo] . [W1_e^T ;
+      // W1_e^T]: the stored weights read K-major, K = 2d (2f) wrapping at d (f)
       if (e == cudaSuccess)
-        e = launch_gemm_tc_wt(at<void>(bws, B.dYs), R, W2, E, 2 * d, d, f, offsets, dH, err,
-                              ctr + 1, sms, s);
-      if (e == cudaSuccess) e = launch_silu_bwd(dH, Z, R, f, at<void>(bws, B.dZs), s);
+        e = launch_gemm_tc_wt(at<void>(bws, B.dYs), R, W2, E, 2 * d, d, f, offsets, Z,
+                              at<void>(bws, B.dZs), err, ctr + 1, sms, s);
       if (e == cudaSuccess)
-        e = launch_gemm_tc_wt(at<void>(bws, B.dZs), R, W1, E, 2 * f, f, d, offsets, dXp, err,
-                              ctr + 2, sms, s);
+        e = launch_gemm_tc_wt(at<void>(bws, B.dZs), R, W1, E, 2 * f, f, d, offsets, nullptr, dXp,
+                              err, ctr + 2, sms, s);
     }
   }
   if (e == cudaSuccess && tc) {

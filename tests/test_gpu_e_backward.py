@@ -52,6 +52,22 @@ SHAPES = {
         "bwd_skew_T256_d128_E64_k8_f128_zipf", T=256, d=128, E=64, k=8, f=128, dtype="bf16",
         bias="zipf", zipf_s=3.0, seed=77),
     "bwd_tiny_fp32_layer": get_config("tiny_T256_d128_E8_k2_f256_fp32"),
+    # one token: most experts have no rows
+    "bwd_one_token_T1_d64_E4_k2_f64": MoEConfig(
+        "bwd_one_token_T1_d64_E4_k2_f64", T=1, d=64, E=4, k=2, f=64, dtype="bf16", pre_k=4,
+        seed=78),
+    # d = 192, f = 448: pair tiles whose odd half is partly or wholly past M / N
+    "bwd_ragged_T96_d192_E3_k2_f448": MoEConfig(
+        "bwd_ragged_T96_d192_E3_k2_f448", T=96, d=192, E=3, k=2, f=448, dtype="bf16",
+        pre_k=3, seed=79),
+    # E = 128: both gate GEMMs on the tensor cores; experts of a few rows
+    "bwd_gate_tc_T160_d128_E128_k4_f64": MoEConfig(
+        "bwd_gate_tc_T160_d128_E128_k4_f64", T=160, d=128, E=128, k=4, f=64, dtype="bf16",
+        bias="normal", bias_var=0.5, seed=80),
+    # a single expert of exactly 128 rows (whole 64-row blocks, no tail)
+    "bwd_whole_blocks_T128_d128_E1_k1_f128": MoEConfig(
+        "bwd_whole_blocks_T128_d128_E1_k1_f128", T=128, d=128, E=1, k=1, f=128,
+        dtype="bf16", pre_k=1, seed=81),
 }
 
 
