@@ -435,7 +435,7 @@ def run_ours(args, cfg):
             simt = 10.0 * R * cfg.d * cfg.f + gate
             # fp32 FMA peak from unit counts: SMs x 128 fp32 lanes x 2 flop x clock
             fp32_peak = sms * 128 * 2 * (clk or {}).get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-            roof = {"bound": "alu", "achieved": simt / (b_ms / 1e3) / 1e12, "peak": fp32_peak,
+            broof = {"bound": "alu", "achieved": simt / (b_ms / 1e3) / 1e12, "peak": fp32_peak,
                     "unit": "TFLOP/s", "frac": simt / (b_ms / 1e3) / 1e12 / fp32_peak,
                     "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 x max SM clock",
                     "flops": simt}
@@ -444,7 +444,7 @@ def run_ours(args, cfg):
             # tensor cores: Z recomputed (2Rdf) and four GEMMs whose fp32
             # operand (dY or dZ) is split into bf16 hi + lo (2 x 2Rdf each)
             tensor = 18.0 * R * cfg.d * cfg.f
-            roof = {"bound": "tensor", "achieved": tensor / (b_ms / 1e3) / 1e12,
+            broof = {"bound": "tensor", "achieved": tensor / (b_ms / 1e3) / 1e12,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                     "frac": tensor / (b_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
                     "peak_source": "measured bf16 (burst)", "flops": tensor,
@@ -453,7 +453,7 @@ def run_ours(args, cfg):
                     "GEMMs) over the whole backward time; the gate's fp32 FMA work is "
                     "simt_flops")
         bwd = {"ms_per_step": b_ms, "tokens_per_s": cfg.T * world / (b_ms / 1e3),
-               "roofline": roof, "simt_flops": gate if cfg.dtype != "f32" else None,
+               "roofline": broof, "simt_flops": gate if cfg.dtype != "f32" else None,
                "note": note}
 
     if dist:
