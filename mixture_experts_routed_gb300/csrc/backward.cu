@@ -60,7 +60,8 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     const Tout* __restrict__ dout, const float* __restrict__ y, const int32_t* __restrict__ pos,
     const float* __restrict__ w, int T, int d, int k, int R, float* __restrict__ dY,
     __nv_bfloat16* __restrict__ dYs, float* __restrict__ dw, uint32_t* __restrict__ err,
-    uint32_t* __restrict__ zero, int nzero, int32_t* __restrict__ seg01) {
+    uint32_t* __restrict__ zero, int nzero, int32_t* __restrict__ seg01,
+    int32_t* __restrict__ segk, int nsegk, int chunk) {
   __shared__ float red[4][kMaxFanout];
   pdl_wait();
   pdl_trigger();
@@ -71,6 +72,8 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
       seg01[0] = 0;
       seg01[1] = T;
     }
+    // token chunks of the gate's split weight gradient: [i chunk, (i+1) chunk)
+    if (segk != nullptr && tid <= nsegk) segk[tid] = min(tid * chunk, T);
   }
   for (int j = 0; j < k; ++j) {
     const int p = __ldg(pos + static_cast<size_t>(t) * k + j);
@@ -425,26 +428,49 @@ __global__ void __launch_bounds__(256) gemm_tn_kernel(const TA* __restrict__ A, 
 // exact and the sums fp32.
 
 // ---------------------------------------------------------------- bias, dx
-// db[e] = sum_t dL[t, e]. A CTA of 32 warps takes 32 experts (lane = expert,
-// so each warp reads 128 contiguous bytes of a row of dL); warp w sums the
-// tokens t = w mod 32 in ascending order, then warp 0 adds the 32 partials
-// in warp order: a fixed order, bitwise reproducible.
+// Partial sums of db[e] = sum_t dL[t, e] over token chunk c = blockIdx.y
+// ([c chunk, (c+1) chunk)). A CTA of 32 warps takes 32 experts (lane =
+// expert, so each warp reads 128 contiguous bytes of a row of dL); warp w
+// sums the chunk's tokens t = w mod 32 in ascending order, then warp 0 adds
+// the 32 partials in warp order: a fixed order, bitwise reproducible.
 __global__ void __launch_bounds__(1024) bias_bwd_kernel(const float* __restrict__ dL, int T, int E,
-                                                        float* __restrict__ db) {
+                                                        int chunk, float* __restrict__ part) {
   __shared__ float red[32][33];
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int e = blockIdx.x * 32 + lane;
+  const int t0 = blockIdx.y * chunk, t1 = min(t0 + chunk, T);
   float s = 0.f;
   if (e < E)
-    for (int t = w; t < T; t += 32) s += __ldg(dL + static_cast<size_t>(t) * E + e);
+    for (int t = t0 + w; t < t1; t += 32) s += __ldg(dL + static_cast<size_t>(t) * E + e);
   red[w][lane] = s;
   __syncthreads();
   if (w == 0 && e < E) {
     float tot = 0.f;
     for (int i = 0; i < 32; ++i) tot += red[i][lane];
-    db[e] = tot;
+    part[static_cast<size_t>(blockIdx.y) * E + e] = tot;
+  }
+}
+
+// out[i] = sum over s < S of part[s][i], s ascending; two independent jobs
+// (blockIdx.y), each skipped when its S is 0.
+struct ReduceJob {
+  const float* part;
+  int S;
+  size_t n;
+  float* out;
+};
+__global__ void __launch_bounds__(256) reduce_partials_kernel(ReduceJob a, ReduceJob b) {
+  pdl_wait();
+  pdl_trigger();
+  const ReduceJob j = blockIdx.y == 0 ? a : b;
+  if (j.S == 0) return;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < j.n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < j.S; ++s) v += __ldg(j.part + static_cast<size_t>(s) * j.n + i);
+    j.out[i] = v;
   }
 }
 
@@ -479,16 +505,17 @@ __global__ void __launch_bounds__(128) undispatch_kernel(const float* __restrict
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
                                float* dw, uint32_t* err, uint32_t* zero, int nzero,
-                               int32_t* seg01, cudaStream_t s) {
+                               int32_t* seg01, int32_t* segk, int nsegk, int chunk,
+                               cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(dYs);
   if (dtype == 0)
     return launch_pdl(combine_bwd_kernel<float>, dim3(T), dim3(128), 0, s,
                       static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, ys, dw, err,
-                      zero, nzero, seg01);
+                      zero, nzero, seg01, segk, nsegk, chunk);
   return launch_pdl(combine_bwd_kernel<__nv_bfloat16>, dim3(T), dim3(128), 0, s,
                     static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys, dw,
-                    err, zero, nzero, seg01);
+                    err, zero, nzero, seg01, segk, nsegk, chunk);
 }
 
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
@@ -527,8 +554,20 @@ cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float*
                     static_cast<const __nv_bfloat16*>(A), a_shared, B, R, M, N, offsets, out, err);
 }
 
-cudaError_t launch_bias_bwd(const float* dL, int T, int E, float* db, cudaStream_t s) {
-  return launch_pdl(bias_bwd_kernel, dim3(ceil_div(E, 32)), dim3(1024), 0, s, dL, T, E, db);
+cudaError_t launch_bias_bwd(const float* dL, int T, int E, int chunk, int nchunk, float* part,
+                            cudaStream_t s) {
+  if (T == 0 || E == 0) return cudaSuccess;
+  return launch_pdl(bias_bwd_kernel, dim3(ceil_div(E, 32), nchunk), dim3(1024), 0, s, dL, T, E,
+                    chunk, part);
+}
+
+cudaError_t launch_reduce_partials(const float* pa, int Sa, size_t na, float* oa, const float* pb,
+                                   int Sb, size_t nb, float* ob, cudaStream_t s) {
+  if (Sa == 0 && Sb == 0) return cudaSuccess;
+  const size_t n = na > nb ? na : nb;
+  const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 152 * 8));
+  return launch_pdl(reduce_partials_kernel, dim3(blocks > 0 ? blocks : 1, 2), dim3(256), 0, s,
+                    ReduceJob{pa, Sa, na, oa}, ReduceJob{pb, Sb, nb, ob});
 }
 
 cudaError_t launch_undispatch(const float* dxg, const float* dxp, const int32_t* pos, int T, int d,

@@ -155,11 +155,13 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 // forward takes; every gradient and intermediate is fp32).
 // dY[pos(t,j)] = w[t,j] dout[t] (when dY is non-null; when dYs is, its bf16 split
 // [R][2d] = [hi | lo]); dw[t,j] = <dout[t], Y[pos(t,j)]>; also zeroes `nzero`
-// words at `zero` and writes seg01 = {0, T}.
+// words at `zero`, writes seg01 = {0, T} and, when segk is non-null, the
+// token chunks segk[i] = min(i chunk, T), i = 0 .. nsegk (nsegk < 128).
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
                                float* dw, uint32_t* err, uint32_t* zero, int nzero,
-                               int32_t* seg01, cudaStream_t s);
+                               int32_t* seg01, int32_t* segk, int nsegk, int chunk,
+                               cudaStream_t s);
 // dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec),
 // and, when dLs is non-null, its bf16 split [T][2E] = [hi | lo].
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
@@ -192,7 +194,14 @@ cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void*
 cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float* B, int E, int R,
                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
                            cudaStream_t s);
-cudaError_t launch_bias_bwd(const float* dL, int T, int E, float* db, cudaStream_t s);
+// part[c][e] = sum of dL[t, e] over the tokens of chunk c ([c chunk, (c+1)
+// chunk), c < nchunk), in a fixed order.
+cudaError_t launch_bias_bwd(const float* dL, int T, int E, int chunk, int nchunk, float* part,
+                            cudaStream_t s);
+// oa[i] = sum_{s < Sa} pa[s][i] (i < na) and ob likewise, s ascending; a job
+// with S = 0 is skipped.
+cudaError_t launch_reduce_partials(const float* pa, int Sa, size_t na, float* oa, const float* pb,
+                                   int Sb, size_t nb, float* ob, cudaStream_t s);
 cudaError_t launch_undispatch(const float* dxg, const float* dxp, const int32_t* pos, int T, int d,
                               int k, int R, float* dx, cudaStream_t s);
 

@@ -260,8 +260,24 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // part of dx, all fp32 but the ints; bf16 layers add the tensor-core GEMMs'
 // operands: the bf16 splits of dY, dZ and dL.
 struct BwdLayout {
-  size_t err, L, ridx, rw, dw, dL, seg01, dY, Z, dXp, dxg, dYs, dZs, dLs, total;
+  size_t err, L, ridx, rw, dw, dL, seg01, segk, bpart, gpart, dY, Z, dXp, dxg, dYs, dZs, dLs,
+      total;
 };
+
+// Token chunks of the gate's weight gradient (split along T so that its few
+// output tiles fill the GPU; the chunks' partial sums are added in chunk
+// order) and of the bias gradient's partial sums.
+constexpr int kTokChunks = 32;
+struct TokChunks {
+  int n, len;
+};
+TokChunks tok_chunks(const moe_config_t& c, int sms) {
+  const int tiles = ceil_div(c.d, 256) * ceil_div(c.E, 256);
+  int n = ceil_div(sms / 2 > 0 ? sms / 2 : 1, tiles);
+  n = n < 1 ? 1 : (n > kTokChunks ? kTokChunks : n);
+  const int len = (ceil_div(c.T > 0 ? c.T : 1, n) + 63) / 64 * 64;
+  return {ceil_div(c.T > 0 ? c.T : 1, len), len};
+}
 
 BwdLayout bwd_layout_of(const moe_config_t& c) {
   BwdLayout B;
@@ -280,6 +296,9 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.dL = take(T * E * 4);
   B.seg01 = take(8);
   const bool tc = c.dtype == MOE_DTYPE_BF16;
+  B.segk = take((kTokChunks + 1) * 4);
+  B.bpart = take(kTokChunks * E * 4);
+  B.gpart = take(tc ? kTokChunks * E * static_cast<size_t>(c.d) * 4 : 0);
   B.dY = take(tc ? 0 : R * c.d * 4);  // fp32 layers (bf16 ones keep only the split)
   B.Z = take(R * c.f * 4);
   B.dXp = take(R * c.d * 4);
@@ -341,15 +360,17 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
                       err, s)) != MOE_OK)
     return st;
   const bool tc = dt == MOE_DTYPE_BF16;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_LAUNCH;
+  const TokChunks ch = tok_chunks(c, sms);
+  int32_t* segk = at<int32_t>(bws, B.segk);
   uint32_t* ctr = at<uint32_t>(bws, kGemmCounterOffset);  // four tile counters
   cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
                                      tc ? at<void>(bws, B.dYs) : nullptr, dw, err, ctr, 4, seg01,
-                                     s);
+                                     segk, ch.n, ch.len, s);
   void* dLs = tc ? at<void>(bws, B.dLs) : nullptr;
   if (e == cudaSuccess)
     e = launch_router_bwd(Lr, idx, w, dw, T, E, k, c.router, c.pre_k, c.tau, dL, dLs, s);
-  const int sms = num_sms();
-  if (sms <= 0) return MOE_ERR_LAUNCH;
   // gate: dx_gate = dL W_g^T ([T, E] x [E, d]), dW_g = x^T dL, db = sum_t dL.
   // bf16 layers put them on the tensor cores with dL split into hi + lo
   // (dx_gate: W_g read K-major, K = E a multiple of 64; dW_g: E a multiple
@@ -358,10 +379,23 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
     e = tc && E % 64 == 0 ? launch_gemm_tc_wt(dLs, T, Wg, 1, 2 * E, E, d, seg01, nullptr, dxg,
                                               err, ctr + 3, sms, s)
                           : launch_gemm_nt(dt, false, dL, Wg, 1, T, E, d, seg01, dxg, err, s);
+  // dW_g on the tensor cores: one partial per token chunk (the chunks are
+  // the "experts" of the weight-gradient GEMM), then summed in chunk order
+  const bool wg_tc = tc && E % 8 == 0;
+  const int wg_parts = wg_tc && ch.n > 1 ? ch.n : 0;
+  float* gpart = at<float>(bws, B.gpart);
   if (e == cudaSuccess)
-    e = tc && E % 8 == 0 ? launch_wgrad_tc(x, T, 0, dLs, T, 1, d, E, seg01, dWg, err, sms, s)
-                         : launch_gemm_tn(dt, x, 0, dL, 1, T, d, E, seg01, dWg, err, s);
-  if (e == cudaSuccess && dbias != nullptr) e = launch_bias_bwd(dL, T, E, dbias, s);
+    e = wg_tc ? launch_wgrad_tc(x, T, 0, dLs, T, ch.n, d, E, segk, wg_parts ? gpart : dWg, err,
+                                sms, s)
+              : launch_gemm_tn(dt, x, 0, dL, 1, T, d, E, seg01, dWg, err, s);
+  // db: partial sums per token chunk, then the same ordered sum
+  const int b_parts = dbias != nullptr && ch.n > 1 ? ch.n : 0;
+  float* bpart = at<float>(bws, B.bpart);
+  if (e == cudaSuccess && dbias != nullptr)
+    e = launch_bias_bwd(dL, T, E, ch.len, ch.n, b_parts ? bpart : dbias, s);
+  if (e == cudaSuccess)
+    e = launch_reduce_partials(gpart, wg_parts, static_cast<size_t>(d) * E, dWg, bpart, b_parts,
+                               static_cast<size_t>(E), dbias, s);
   // experts: Z = X_e W1_e again (fp32), dZ = (dY W2_e^T) * SiLU'(Z) over Z,
   // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T. bf16 layers run every
   // expert GEMM on the tensor cores (dY and dZ split into bf16 hi + lo; for
