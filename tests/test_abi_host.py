@@ -228,7 +228,8 @@ def test_backward_argument_errors(lib):
     ws = lib.moe_workspace_size(ctypes.byref(c))
     bws = lib.moe_backward_workspace_size(ctypes.byref(c))
     R = 1024 * 2
-    # dY, Z/dZ, dX_perm (fp32 per routed row) and the gate part of dx
+    # per routed row: dY (fp32, or for bf16 layers its bf16 hi/lo split: the
+    # same bytes), Z and dX_perm (fp32); and the gate part of dx
     assert bws >= R * 4096 * 4 * 2 + R * 11008 * 4 + 1024 * 4096 * 4
     args = lambda cc, fws, b: (ctypes.byref(cc), FAKE, FAKE, None, None, FAKE, FAKE, FAKE, fws,
                                FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, b, None)
