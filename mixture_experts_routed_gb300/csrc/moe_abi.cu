@@ -267,16 +267,27 @@ struct BwdLayout {
 // Token chunks of the gate's weight gradient (split along T so that its few
 // output tiles fill the GPU; the chunks' partial sums are added in chunk
 // order) and of the bias gradient's partial sums.
+// At most kTokChunks chunks, one per 64 tokens, and as many as 128 clusters
+// of two CTAs need (the cap the workspace is sized for; GB300 has 76).
 constexpr int kTokChunks = 32;
+constexpr int kMaxClusters = 128;
+int max_tok_chunks(const moe_config_t& c) {
+  const int tiles = ceil_div(c.d, 256) * ceil_div(c.E, 256);
+  int n = ceil_div(kMaxClusters, tiles);
+  const int by_rows = ceil_div(c.T > 0 ? c.T : 1, 64);
+  n = n < by_rows ? n : by_rows;
+  return n < 1 ? 1 : (n > kTokChunks ? kTokChunks : n);
+}
 struct TokChunks {
   int n, len;
 };
 TokChunks tok_chunks(const moe_config_t& c, int sms) {
   const int tiles = ceil_div(c.d, 256) * ceil_div(c.E, 256);
+  const int cap = max_tok_chunks(c);
   int n = ceil_div(sms / 2 > 0 ? sms / 2 : 1, tiles);
-  n = n < 1 ? 1 : (n > kTokChunks ? kTokChunks : n);
+  n = n < 1 ? 1 : (n > cap ? cap : n);
   const int len = (ceil_div(c.T > 0 ? c.T : 1, n) + 63) / 64 * 64;
-  return {ceil_div(c.T > 0 ? c.T : 1, len), len};
+  return {ceil_div(c.T > 0 ? c.T : 1, len), len};  // <= n chunks
 }
 
 BwdLayout bwd_layout_of(const moe_config_t& c) {
@@ -296,9 +307,10 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.dL = take(T * E * 4);
   B.seg01 = take(8);
   const bool tc = c.dtype == MOE_DTYPE_BF16;
+  const size_t nch = static_cast<size_t>(max_tok_chunks(c));
   B.segk = take((kTokChunks + 1) * 4);
-  B.bpart = take(kTokChunks * E * 4);
-  B.gpart = take(tc ? kTokChunks * E * static_cast<size_t>(c.d) * 4 : 0);
+  B.bpart = take(nch * E * 4);
+  B.gpart = take(tc ? nch * E * static_cast<size_t>(c.d) * 4 : 0);
   B.dY = take(tc ? 0 : R * c.d * 4);  // fp32 layers (bf16 ones keep only the split)
   B.Z = take(R * c.f * 4);
   B.dXp = take(R * c.d * 4);
