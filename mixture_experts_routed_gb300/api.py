@@ -53,7 +53,16 @@ def _cfg(c):
 
 
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    """Device address of a dense CUDA tensor: the C ABI takes row-major
+    buffers in GPU memory, so a strided view (read with the wrong layout) or
+    a host tensor (an address no kernel may touch) is refused here."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise MoEError(L.MOE_ERR_INVALID_ARG, "tensor is not contiguous")
+    if not t.is_cuda:
+        raise MoEError(L.MOE_ERR_INVALID_ARG, "tensor is not in GPU memory")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _s(stream):

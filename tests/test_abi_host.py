@@ -273,3 +273,17 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load(str(tmp_path / "missing.so"))
     finally:
         mod._lib = saved
+
+
+def test_binding_refuses_strided_and_host_tensors():
+    # the Python binding hands the C ABI raw addresses: a transposed view or
+    # a host tensor is refused before any call is made (no GPU needed)
+    import torch
+    import mixture_experts_routed_gb300 as moe
+    from workloads import get_config
+    c = get_config("tiny_T256_d128_E8_k2_f256_fp32")
+    Wg = torch.zeros((c.d, c.E))
+    with pytest.raises(moe.MoEError, match="not contiguous"):
+        moe.route(c, torch.zeros((c.d, c.T)).t(), Wg)
+    with pytest.raises(moe.MoEError, match="not in GPU memory"):
+        moe.route(c, torch.zeros((c.T, c.d)), Wg)
