@@ -194,6 +194,18 @@ def cores():
         return os.cpu_count() or 1
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (a replicated job is as slow as its
+    slowest rank); on one process (dist None) the value itself."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, cfg):
     import numpy as np
@@ -308,11 +320,7 @@ def run_ours(args, cfg):
         step(evs[i])
     torch.cuda.synchronize(dev)
     clk = clocks.stop() if rank == 0 else None
-    total_ms = t_start.elapsed_time(t_end)
-    if dist:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     if moe.get_device_error(ws) != moe.MOE_OK:
         raise RuntimeError("device error in the timed steps")
     ms_per_step = total_ms / K
@@ -392,11 +400,7 @@ def run_ours(args, cfg):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e_ms = a.elapsed_time(b)
-        if dist:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(a.elapsed_time(b), dist, dev)
         e2e = {"value": cfg.T * world / (e_ms / K / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": x_host.numel() * x_host.element_size() + (
                    g_host.numel() * g_host.element_size() if g_host is not None else 0),
@@ -417,6 +421,8 @@ def run_ours(args, cfg):
         for _ in range(max(1, args.warmup)):
             bwd_step()
         torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -426,7 +432,7 @@ def run_ours(args, cfg):
         torch.cuda.synchronize(dev)
         if moe.get_device_error(bws) != moe.MOE_OK:
             raise RuntimeError("device error in the backward steps")
-        b_ms = a.elapsed_time(b) / K
+        b_ms = max_over_ranks(a.elapsed_time(b), dist, dev) / K
         R = cfg.T * cfg.k
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         gate = 4.0 * cfg.T * cfg.d * cfg.E  # dx_gate and dW_g (fp32 FMA)
