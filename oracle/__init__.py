@@ -32,7 +32,7 @@ from .moe_oracle import (  # noqa: F401
     gate_logits, route, dispatch, quantize_payload_fp8, quantize_output_fp8,
     dequantize_output_fp8, expert_ffn_rows,
     combine, forward, forward_tokens, inputs_to_numpy, backward, backward_tokens,
-    router_backward,
+    backward_router, backward_expert, router_backward,
     silu_grad, ROUTER_RENORM,
     ROUTER_PREK_SOFTMAX, ROUTER_GROUP_LIMITED, ROUTER_SOFT_GUMBEL,
 )

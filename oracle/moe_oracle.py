@@ -476,31 +476,59 @@ def router_backward(L: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, dw:
     return dL
 
 
+def _combine_backward(pos: np.ndarray, w: np.ndarray, Y: np.ndarray, g: np.ndarray):
+    """Combine step backward: out[t] = sum_j w[t, j] Y[pos[t, j]] gives
+    dY[pos[t, j]] = w[t, j] dout[t] and dw[t, j] = <dout[t], Y[pos[t, j]]>."""
+    T, k = w.shape
+    dY = np.zeros((T * k, Y.shape[1]), dtype=np.float64)
+    dw = np.zeros((T, k), dtype=np.float64)
+    for j in range(k):
+        dY[pos[:, j]] = w[:, j:j + 1] * g
+        dw[:, j] = (g * Y[pos[:, j]]).sum(axis=1)
+    return dY, dw
+
+
+def _expert_backward(xe: np.ndarray, W1e: np.ndarray, W2e: np.ndarray, dYe: np.ndarray,
+                     hs: str):
+    """One expert's rows: z = x_e W1_e, h = SiLU(z) (stored rounded), y = h W2_e.
+    Returns dW1_e = x_e^T dZ, dW2_e = h^T dY_e and dX_e = dZ W1_e^T, with
+    dZ = (dY_e W2_e^T) * SiLU'(z)."""
+    z = xe @ W1e
+    h = silu(z)
+    if hs == "bf16":
+        h = round_to_bf16(h)
+    elif hs == "f32":
+        h = round_to_f32(h)
+    dW2e = h.T @ dYe
+    dZ = (dYe @ W2e.T) * silu_grad(z)
+    return xe.T @ dZ, dW2e, dZ @ W1e.T
+
+
+def _backward_setup(cfg, inp, fwd, dout):
+    if cfg.payload_fp8 or getattr(cfg, "output_fp8", 0):
+        raise ValueError("the FP8 payloads have no backward")
+    a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
+    T, k = np.asarray(fwd["topk_idx"]).shape
+    pos = np.asarray(fwd["pos"]).reshape(T, k)
+    w = np.asarray(fwd["topk_w"], np.float64)
+    g = np.asarray(dout, np.float64) if not hasattr(dout, "detach") else _np64(dout)
+    return a, pos, w, g
+
+
 def backward(cfg, inp: dict, fwd: dict, dout, h_storage: str | None = None) -> dict:
     """Gradients of the layer for dout = dl/dout [T, d]: dx [T, d], dWg [d, E],
     dbias [E], dW1 [E, d, f], dW2 [E, f, d], and the intermediates dY (per
     routed row), dw [T, k], dL [T, E]. ``fwd`` is forward(cfg, inp) (its
     routing, permutation, H and Y); ``h_storage`` (default: the layer's)
     must match the forward's."""
-    if cfg.payload_fp8 or getattr(cfg, "output_fp8", 0):
-        raise ValueError("the FP8 payloads have no backward")
-    a = inputs_to_numpy(inp) if not isinstance(inp.get("x"), np.ndarray) else inp
+    a, pos, w, g = _backward_setup(cfg, inp, fwd, dout)
     x = a["x"]
-    T, k = np.asarray(fwd["topk_idx"]).shape
-    R = T * k
-    pos = np.asarray(fwd["pos"]).reshape(T, k)
+    R = pos.size
     src = np.asarray(fwd["src"])
     offsets = np.asarray(fwd["offsets"])
-    w = np.asarray(fwd["topk_w"], np.float64)
-    Y = np.asarray(fwd["Y"], np.float64)
-    g = np.asarray(dout, np.float64) if not hasattr(dout, "detach") else _np64(dout)
     hs = h_storage or _storage(cfg)
     # combine: out[t] = sum_j w[t, j] Y[pos[t, j]]
-    dY = np.zeros((R, cfg.d), dtype=np.float64)
-    dw = np.zeros((T, k), dtype=np.float64)
-    for j in range(k):
-        dY[pos[:, j]] = w[:, j:j + 1] * g
-        dw[:, j] = (g * Y[pos[:, j]]).sum(axis=1)
+    dY, dw = _combine_backward(pos, w, np.asarray(fwd["Y"], np.float64), g)
     # router and gate: L = x W_g + b
     dL = router_backward(fwd["L"], fwd["topk_idx"], w, dw, cfg.router, cfg.pre_k,
                          getattr(cfg, "tau", 1.0))
@@ -516,24 +544,45 @@ def backward(cfg, inp: dict, fwd: dict, dout, h_storage: str | None = None) -> d
         lo, hi = int(offsets[e]), int(offsets[e + 1])
         if hi == lo:
             continue                  # no rows: the expert's gradients are 0
-        xe = x[src[lo:hi]]
-        W1e, W2e = _expert(a["W1"], e), _expert(a["W2"], e)
-        z = xe @ W1e
-        h = silu(z)
-        if hs == "bf16":
-            h = round_to_bf16(h)
-        elif hs == "f32":
-            h = round_to_f32(h)
-        dYe = dY[lo:hi]
-        dW2[e] = h.T @ dYe
-        dZ = (dYe @ W2e.T) * silu_grad(z)
-        dW1[e] = xe.T @ dZ
-        dXp[lo:hi] = dZ @ W1e.T
+        dW1[e], dW2[e], dXp[lo:hi] = _expert_backward(
+            x[src[lo:hi]], _expert(a["W1"], e), _expert(a["W2"], e), dY[lo:hi], hs)
     # mirror of the dispatch: each routed row's gradient back to its token
-    for j in range(k):
+    for j in range(pos.shape[1]):
         dx += dXp[pos[:, j]]
     return {"dx": dx, "dWg": dWg, "dbias": dbias, "dW1": dW1, "dW2": dW2, "dY": dY, "dw": dw,
             "dL": dL}
+
+
+def backward_router(cfg, inp: dict, fwd: dict, dout) -> dict:
+    """The gate's part of ``backward`` alone (no expert GEMMs): dw [T, k],
+    dL [T, E], dWg [d, E], dbias [E]. Used for full checks of the gate's
+    gradients on layers too large for the whole backward."""
+    a, pos, w, g = _backward_setup(cfg, inp, fwd, dout)
+    _, dw = _combine_backward(pos, w, np.asarray(fwd["Y"], np.float64), g)
+    dL = router_backward(fwd["L"], fwd["topk_idx"], w, dw, cfg.router, cfg.pre_k,
+                         getattr(cfg, "tau", 1.0))
+    return {"dw": dw, "dL": dL, "dWg": a["x"].T @ dL, "dbias": dL.sum(axis=0)}
+
+
+def backward_expert(cfg, inp: dict, fwd: dict, dout, e: int,
+                    h_storage: str | None = None) -> dict:
+    """Expert e's part of ``backward`` alone: dW1[e] [d, f] and dW2[e] [f, d]
+    (zeros for an expert with no rows), from the rows routed to it."""
+    a, pos, w, g = _backward_setup(cfg, inp, fwd, dout)
+    offsets = np.asarray(fwd["offsets"])
+    lo, hi = int(offsets[e]), int(offsets[e + 1])
+    if hi == lo:
+        return {"dW1": np.zeros((cfg.d, cfg.f)), "dW2": np.zeros((cfg.f, cfg.d))}
+    k = pos.shape[1]
+    # the flat entry t*k + j of each routed row r: dY[r] = w[t, j] dout[t]
+    flat = np.empty(pos.size, dtype=np.int64)
+    flat[pos.reshape(-1)] = np.arange(pos.size)
+    i = flat[lo:hi]
+    dYe = w.reshape(-1)[i][:, None] * g[i // k]
+    src = np.asarray(fwd["src"])
+    dW1e, dW2e, _ = _expert_backward(a["x"][src[lo:hi]], _expert(a["W1"], e),
+                                     _expert(a["W2"], e), dYe, h_storage or _storage(cfg))
+    return {"dW1": dW1e, "dW2": dW2e}
 
 
 def backward_tokens(cfg, inp: dict, dout, tokens, h_storage: str | None = None) -> dict:

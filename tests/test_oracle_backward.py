@@ -185,3 +185,23 @@ def test_token_subset_equals_the_whole_layer(router):
     sub = oracle.backward_tokens(cfg, a, dout, [7, 2, 5])
     np.testing.assert_allclose(sub["dx"], full["dx"][[7, 2, 5]], rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(sub["dL"], full["dL"][[7, 2, 5]], rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("router", [ROUTER_RENORM, ROUTER_PREK_SOFTMAX, ROUTER_SOFT_GUMBEL])
+def test_router_and_expert_parts_equal_the_whole_backward(router):
+    # the gate's part and each expert's part on their own (the pieces the
+    # full-size GPU checks use) are the whole backward's, value for value;
+    # k = 3 of 5 experts over 9 tokens leaves uneven (and maybe empty) experts
+    kw = dict(E=5, k=5, pre_k=5, tau=0.8) if router == ROUTER_SOFT_GUMBEL else dict(E=5, k=3)
+    cfg = _cfg(router, T=9, **kw)
+    a = _inputs(cfg, 11)
+    fwd = _exact_forward(cfg, a)
+    dout = np.random.default_rng(12).standard_normal((cfg.T, cfg.d))
+    whole = oracle.backward(cfg, a, fwd, dout, h_storage="exact")
+    part = oracle.backward_router(cfg, a, fwd, dout)
+    for n in ("dw", "dL", "dWg", "dbias"):
+        np.testing.assert_allclose(part[n], whole[n], rtol=1e-12, atol=1e-14, err_msg=n)
+    for e in range(cfg.E):
+        pe = oracle.backward_expert(cfg, a, fwd, dout, e, h_storage="exact")
+        np.testing.assert_allclose(pe["dW1"], whole["dW1"][e], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(pe["dW2"], whole["dW2"][e], rtol=1e-12, atol=1e-14)
