@@ -3,8 +3,9 @@
 
 A step is one moe_forward (route -> dispatch -> grouped expert FFN ->
 combine) over one batch of synthetic tokens already resident in HBM. The
-default workload is the balanced 8-expert layer (T=1024, d=4096, E=8, top-2,
-f=11008, bf16). Prints ONE JSON line (rank 0).
+default workload is the largest layer that fits one GPU: the fine-grained
+skewed layer (T=16384, d=7168, E=256, top-8, f=2048, bf16, Zipf(1.1) expert
+popularity). Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -16,7 +17,7 @@ being scheduled early. Per-kernel times (the `kernels` table and the roofline
 `achieved`) come from a second pass of K steps right after it, with events
 at every kernel boundary (moe_forward_with_events) on the launching stream.
 The per-step working set
-(expert weights, 1.44 GB for the default layer) is larger than the 129 MB L2,
+(expert weights, 15 GB for the default layer) is larger than the 129 MB L2,
 so no L2 flush is needed between steps; --flush-l2 adds one anyway.
 """
 from __future__ import annotations
@@ -52,7 +53,8 @@ def parse():
     p.add_argument("--flush-l2", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--cpu-sample-tokens", type=int, default=256)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU oracle baseline: run 16-token chunks until this much time has passed")
     p.add_argument("--backward", action="store_true",
                    help="also time moe_backward (adds a 'backward' object to the line)")
     return p.parse_args()
@@ -67,10 +69,11 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- algorithmic work
-def stage_work(cfg, counts):
+def stage_work(cfg, counts, gathered=False):
     """Algorithmic bytes and flops per launch of each stage: only what the
     method must move (weights of experts that received rows, each operand
-    read once, each result written once)."""
+    read once, each result written once). `gathered`: the W1 GEMM reads each
+    routed row from x itself and the dispatch writes only the layout."""
     T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
     R = T * k
     b = 4 if cfg.dtype == "f32" else 2
@@ -83,7 +86,8 @@ def stage_work(cfg, counts):
     # from HBM)
     w["route"] = (T * d * b + d * E * b + E * 4 + R * 8 + (T * E * 4 if soft else 0),
                   2.0 * T * d * E)
-    w["dispatch"] = ((R * 8 + E * 8) if soft else
+    # soft gating: the layout only; gathered rows: ids read, the layout written
+    w["dispatch"] = ((R * 8 + E * 8) if soft else (R * 12 + E * 8) if gathered else
                      (T * d * b + R * d * pb + R * 12 + (R * 4 if cfg.payload_fp8 else 0)), 0.0)
     w["w1_prologue"] = (0, 0.0)
     a_bytes = T * d * b if soft else R * d * pb
@@ -183,8 +187,22 @@ def cpu_oracle_run(cfg, host, tokens):
 
 
 def host_inputs(inp):
-    """CPU copies of the inputs (outside any timed region)."""
-    return {k: v.detach().cpu() for k, v in inp.items()}
+    """The oracle's host inputs (outside any timed region): fp64 arrays of x,
+    W_g, bias (and the Gumbel samples), CPU copies of the expert weights,
+    which the oracle upcasts one expert at a time."""
+    import oracle
+    return oracle.inputs_to_numpy({k: v.detach().cpu() for k, v in inp.items()})
+
+
+def cpu_oracle_sample(cfg, host, seconds, chunk=16):
+    """The oracle over consecutive chunks of `chunk` tokens from token 0 until
+    `seconds` have passed (or the batch is done): (tokens, wall seconds)."""
+    done, t = 0, 0.0
+    while done < cfg.T and (done == 0 or t < seconds):
+        n = min(chunk, cfg.T - done)
+        t += cpu_oracle_run(cfg, host, list(range(done, done + n)))
+        done += n
+    return done, t
 
 
 def cores():
@@ -207,15 +225,30 @@ def max_over_ranks(value, dist, device):
 
 
 # ---------------------------------------------------------------- reference arm
+def reference_sample_tokens(cfg):
+    """Tokens the reference arm runs per step: about 128 routed rows, so that
+    one step stays around a second or two of host work even on the layers
+    whose oracle upcasts many experts' weights."""
+    return max(1, min(cfg.T, 128 // cfg.k))
+
+
 def run_reference(args, cfg):
     import numpy as np
+    import torch
     from workloads import make_inputs
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    inp = make_inputs(cfg, device="cpu")
+    # the draws are made on the GPU when there is one (the CPU generator takes
+    # minutes for the 15 GB of expert weights) and copied to host memory; the
+    # oracle itself runs on the host cores only
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(cfg, device=gen_dev)
     host = host_inputs(inp)
-    S = min(cfg.T, 64)
+    del inp
+    if gen_dev == "cuda":
+        torch.cuda.empty_cache()
+    S = reference_sample_tokens(cfg)
     rng = np.random.default_rng(0)
     for _ in range(args.warmup):
         cpu_oracle_run(cfg, host, np.sort(rng.choice(cfg.T, S, replace=False)))
@@ -224,8 +257,9 @@ def run_reference(args, cfg):
         t += cpu_oracle_run(cfg, host, np.sort(rng.choice(cfg.T, S, replace=False)))
     per_step = t / args.steps
     value = S / per_step
-    sample = (f"{S} random tokens of the {cfg.T}-token batch per step (all {cfg.E} experts' "
-              f"weights upcast to fp64 as the oracle does), numpy fp64")
+    sample = (f"{S} random tokens of the {cfg.T}-token batch per step: gate, router, the FFN "
+              f"of every chosen expert (its weights upcast to fp64 as the oracle does) and the "
+              f"combine, numpy fp64; inputs drawn on {gen_dev}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -248,6 +282,7 @@ def workload_config(cfg, args):
     return {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "f": cfg.f,
             "router": router[cfg.router], "pre_k": cfg.pre_k,
             "payload": payload[int(cfg.payload_fp8)],
+            "x_perm_mode": {0: "library's choice", 1: "packed", 2: "gathered"}[cfg.x_perm_mode],
             "expert_output": ("fp8_e4m3 (per-row min/max affine)" if cfg.output_fp8
                               else "fp32"), "seed": cfg.seed,
             "parallelism": f"replicas x{args.gpus}",
@@ -333,7 +368,8 @@ def run_ours(args, cfg):
 
     views = moe.forward_views(cfg, ws)
     counts = views["counts"].cpu().tolist()
-    work = stage_work(cfg, counts)
+    gathered = views["x_perm"] is None and cfg.router != 3
+    work = stage_work(cfg, counts, gathered)
     peaks, peak_src = load_peaks()
     kernels = {}
     for name in STAGES:
@@ -430,9 +466,10 @@ def run_ours(args, cfg):
             bwd_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
+        # every rank joins the collective before any of them can raise
+        b_ms = max_over_ranks(a.elapsed_time(b), dist, dev) / K
         if moe.get_device_error(bws) != moe.MOE_OK:
             raise RuntimeError("device error in the backward steps")
-        b_ms = max_over_ranks(a.elapsed_time(b), dist, dev) / K
         R = cfg.T * cfg.k
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         gate = 4.0 * cfg.T * cfg.d * cfg.E  # dx_gate and dW_g (fp32 FMA)
@@ -447,17 +484,24 @@ def run_ours(args, cfg):
                     "flops": simt}
             note = "achieved = every GEMM's fp32 FMA work over the whole backward time"
         else:
-            # tensor cores: Z recomputed (2Rdf) and four GEMMs whose fp32
-            # operand (dY or dZ) is split into bf16 hi + lo (2 x 2Rdf each)
-            tensor = 18.0 * R * cfg.d * cfg.f
-            broof = {"bound": "tensor", "achieved": tensor / (b_ms / 1e3) / 1e12,
+            # the method's own work: Z recomputed and four expert GEMMs, 2Rdf
+            # each. The tensor cores execute more: each of the four GEMMs with
+            # an fp32 operand (dY or dZ) runs on its bf16 split hi + lo, which
+            # doubles it (18Rdf executed)
+            algo = 10.0 * R * cfg.d * cfg.f
+            executed = 18.0 * R * cfg.d * cfg.f
+            t_s = b_ms / 1e3
+            broof = {"bound": "tensor", "achieved": algo / t_s / 1e12,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": tensor / (b_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-                    "peak_source": "measured bf16 (burst)", "flops": tensor,
-                    "algorithmic_flops": 10.0 * R * cfg.d * cfg.f}
-            note = ("achieved = the tensor-core flops executed (the hi/lo split doubles four "
-                    "GEMMs) over the whole backward time; the gate's fp32 FMA work is "
-                    "simt_flops")
+                    "frac": algo / t_s / 1e12 / peaks["bf16_tflops"],
+                    "peak_source": "measured bf16 (burst)", "flops": algo,
+                    "executed_flops": executed,
+                    "executed_tflops": executed / t_s / 1e12,
+                    "executed_frac": executed / t_s / 1e12 / peaks["bf16_tflops"]}
+            note = ("achieved = the method's expert-GEMM flops (10 R d f: Z recomputed, dH, "
+                    "dX_perm, dW1, dW2) over the whole backward time; executed_* count the "
+                    "tensor-core flops actually run (the hi/lo operand split doubles four "
+                    "GEMMs: 18 R d f); the gate's fp32 FMA work is simt_flops")
         bwd = {"ms_per_step": b_ms, "tokens_per_s": cfg.T * world / (b_ms / 1e3),
                "roofline": broof, "simt_flops": gate if cfg.dtype != "f32" else None,
                "note": note}
@@ -472,11 +516,10 @@ def run_ours(args, cfg):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         host = host_inputs(inp)
-        S = min(cfg.T, args.cpu_sample_tokens)
-        toks = np.arange(S)
-        t = cpu_oracle_run(cfg, host, toks)
+        S, t = cpu_oracle_sample(cfg, host, args.cpu_seconds)
         cpu = {"value": S / t, "unit": UNIT, "cores": cores(), "kind": "oracle",
-               "sample": f"first {S} tokens of the {cfg.T}-token batch, whole layer (gate, "
+               "sample": f"the first {S} tokens of the {cfg.T}-token batch in chunks of 16 "
+                         f"(run until {args.cpu_seconds:g} s had passed), whole layer (gate, "
                          f"router, FFN of every chosen expert incl. its fp64 weight upcast, "
                          f"combine) in numpy fp64; {t:.1f} s"}
 

@@ -116,7 +116,28 @@ typedef struct moe_config {
                         * as an FP8 payload (moe_quantize_output, then
                         * moe_combine_fp8); 0: fp32 rows (moe_combine) */
   float tau;           /* MOE_ROUTER_SOFT_GUMBEL: temperature, finite and > 0 */
+  int32_t gemm_tile_n; /* bf16 expert GEMMs: output features per 2-SM pair tile.
+                        * 0 = the library's choice (512 for long-K SiLU passes
+                        * with many tiles, else 256); 256 or 512 force it (the
+                        * FP8 payload's W1 pass always takes 256). A tuning
+                        * knob with no effect on the result beyond fp32
+                        * summation order; other values: MOE_ERR_INVALID_ARG */
+  int32_t x_perm_mode; /* moe_forward's packed rows (MOE_XPERM_*): packed by the
+                        * dispatch into x_perm and read by the W1 GEMM, or
+                        * gathered by the W1 GEMM from x through src, x_perm
+                        * never written (the dispatch and the first expert
+                        * GEMM in one pass: the single-GPU form of the
+                        * Waved-EP fusion, DeepSeek V3/V4 parallel-strategy
+                        * article). Gathering takes bf16 layers without an FP8
+                        * payload or soft gating; asking for it elsewhere is
+                        * MOE_ERR_UNSUPPORTED. The stage calls always pack. */
 } moe_config_t;
+
+enum {
+  MOE_XPERM_AUTO = 0,     /* the library's choice */
+  MOE_XPERM_PACKED = 1,   /* the dispatch writes x_perm */
+  MOE_XPERM_GATHERED = 2  /* the W1 GEMM reads x[src[r]]; no x_perm */
+};
 
 /* Validate a configuration. Returns MOE_OK or MOE_ERR_INVALID_ARG /
  * MOE_ERR_UNSUPPORTED without touching the device. */
@@ -189,7 +210,11 @@ MOE_API int moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* 
  * call rewrites the tables and clears its error word first). Calls whose
  * kernels overlap on the GPU race on the array: order them on one stream.
  * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture. */
+ * that device current) and keeps it for the life of the process; make that
+ * first call before any stream capture. The kept address belongs to the
+ * device's primary context: after cudaDeviceReset (or anything else that
+ * destroys that context) it is stale, so do not call this entry point again
+ * in a process that has reset the device. */
 MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
                          const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
                          int32_t* pos, int32_t* src, void* x_perm, float* x_scale,
@@ -276,7 +301,8 @@ MOE_API int moe_forward_with_events(const moe_config_t* cfg, const void* x,
 
 /* Pointers into a forward workspace, so a caller can inspect the
  * intermediates of the last moe_forward (routing, permutation, H, Y).
- * Any output pointer may be NULL. Returns MOE_ERR_INVALID_ARG for a bad
+ * Any output pointer may be NULL. x_perm is NULL when that forward packs no
+ * rows (gathered rows, soft gating). Returns MOE_ERR_INVALID_ARG for a bad
  * configuration. No device access. */
 typedef struct moe_forward_views {
   int32_t* topk_idx; float* topk_w;

@@ -16,5 +16,5 @@ from ._lib import (  # noqa: F401
     MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE_TOO_SMALL,
     MOE_ERR_LAUNCH, MOE_ERR_BAD_INDEX, MOE_ERR_TIMEOUT, MOE_DTYPE_F32, MOE_DTYPE_BF16,
     MOE_ROUTER_RENORM, MOE_ROUTER_PREK_SOFTMAX, MOE_ROUTER_GROUP_LIMITED,
-    MOE_ROUTER_SOFT_GUMBEL, MOE_NUM_EVENTS,
+    MOE_ROUTER_SOFT_GUMBEL, MOE_NUM_EVENTS, MOE_XPERM_AUTO, MOE_XPERM_PACKED, MOE_XPERM_GATHERED,
 )

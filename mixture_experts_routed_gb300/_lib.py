@@ -22,6 +22,9 @@ MOE_ROUTER_PREK_SOFTMAX = 1
 MOE_ROUTER_GROUP_LIMITED = 2
 MOE_ROUTER_SOFT_GUMBEL = 3
 MOE_NUM_EVENTS = 8
+MOE_XPERM_AUTO = 0
+MOE_XPERM_PACKED = 1
+MOE_XPERM_GATHERED = 2
 
 
 class MoeConfig(ctypes.Structure):
@@ -29,7 +32,9 @@ class MoeConfig(ctypes.Structure):
                 ("T", "d", "E", "k", "f", "dtype", "router", "pre_k", "payload_fp8",
                  "n_group", "topk_group")] + [("payload_scale", ctypes.c_float),
                                              ("output_fp8", ctypes.c_int32),
-                                             ("tau", ctypes.c_float)]
+                                             ("tau", ctypes.c_float),
+                                             ("gemm_tile_n", ctypes.c_int32),
+                                             ("x_perm_mode", ctypes.c_int32)]
 
 
 class MoeForwardViews(ctypes.Structure):

@@ -119,6 +119,9 @@ cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const 
                                   int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
                                   void* x_perm, float* x_scale, uint32_t* err, uint32_t* zero,
                                   int nzero, cudaStream_t s);
+// x_perm[r] = x[src[r]] for the R routed rows (d elements of dtype each).
+cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* src, int T, int R, int d,
+                               void* x_perm, uint32_t* err, cudaStream_t s);
 // Soft gating's layout (every token to every expert, token order): counts,
 // offsets, pos, src; zeroes `nzero` words at `zero` when non-null.
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,
@@ -144,11 +147,14 @@ cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, co
 // A). A [a_rows, K] bf16, or E4M3 bytes when a_fp8 (epi 0 only: expanded to
 // bf16 in shared memory, the row scale applied in the epilogue); W [E, K, N]
 // bf16. epi 0: (row scale) -> SiLU -> bf16 out; epi 1: fp32 out.
-// `tile_ctr` must be zero at launch.
+// `tile_ctr` must be zero at launch. tile_n: 0 (the built-in choice of pair
+// tile width), 256 or 512 (forced; the fp8 token rows always take 256).
+// gather_src non-null (epi 0, bf16, not a_shared): A is x [a_rows, K] and
+// routed row r reads x row gather_src[r] (no packed copy of the rows).
 cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
                            const void* W, int E, int K, int N, const int32_t* offsets,
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
-                           int num_sms, cudaStream_t s);
+                           const int32_t* gather_src, int tile_n, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- backward.cu
 // The backward pass's kernels (dtype 0 = fp32, 1 = bf16 for the tensors the

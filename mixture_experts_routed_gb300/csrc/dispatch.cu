@@ -23,6 +23,10 @@
 // shared-memory counters: the totals and the entries of earlier chunks), so
 // the count and scan launches and their hist/base tables drop out.
 //
+// With no x_perm (the grouped GEMM then gathers each routed row from x
+// through src itself) the scatter kernels write only the layout: counts,
+// offsets, pos and src.
+//
 // Expert ids outside [0, E) are skipped and flag kErrBadIndex.
 #include <cstdint>
 #include <mutex>
@@ -240,6 +244,7 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
       pos_s[q] = p;
     }
   }
+  if (x_perm == nullptr) return;  // layout only: no rows are packed
   __syncthreads();
 
   if constexpr (!FP8) {
@@ -402,6 +407,28 @@ __global__ void __launch_bounds__(256) dense_layout_kernel(int T, int E, int32_t
   }
 }
 
+// x_perm[r] = x[src[r]] for r < R (rows of `row_bytes`, a multiple of 16):
+// one warp per row, 16-byte vectors. A src outside [0, T) flags
+// kErrBadIndex and leaves the row unwritten.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
+                                                          const int32_t* __restrict__ src, int T,
+                                                          long long R, int vecs,
+                                                          uint4* __restrict__ x_perm,
+                                                          uint32_t* __restrict__ err) {
+  pdl_wait();
+  pdl_trigger();
+  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const int t = __ldg(src + r);
+  if (t < 0 || t >= T) {
+    if ((threadIdx.x & 31) == 0) atomicOr(err, kErrBadIndex);
+    return;
+  }
+  const uint4* a = x + static_cast<size_t>(t) * vecs;
+  uint4* b = x_perm + static_cast<size_t>(r) * vecs;
+  for (int v = threadIdx.x & 31; v < vecs; v += 32) b[v] = __ldg(a + v);
+}
+
 // Rows copied by bulk copies through shared memory: plain (not FP8) rows of
 // at most kDispatchBulkRowBytes (the chunk's rows take kTPC times that).
 constexpr int kDispatchBulkRowBytes = 8192;
@@ -454,7 +481,7 @@ cudaError_t launch_dispatch_scatter(int dtype, int fp8, float static_scale, cons
   auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false, false>
                 : (!fp8 ? dispatch_scatter_kernel<1, false, false>
                         : dispatch_scatter_kernel<1, true, false>);
-  const int bulk = bulk_rows(dtype, fp8, d);
+  const int bulk = x_perm != nullptr ? bulk_rows(dtype, fp8, d) : 0;
   const size_t smem = bulk ? static_cast<size_t>(kTPC) * d * (dtype == 0 ? 4 : 2) : 0;
   if (bulk) {
     const cudaError_t st = set_bulk_smem(kernel);
@@ -475,7 +502,7 @@ cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const 
   auto kernel = dtype == 0 ? dispatch_scatter_kernel<0, false, true>
                 : (!fp8 ? dispatch_scatter_kernel<1, false, true>
                         : dispatch_scatter_kernel<1, true, true>);
-  const int bulk = bulk_rows(dtype, fp8, d);
+  const int bulk = x_perm != nullptr ? bulk_rows(dtype, fp8, d) : 0;
   const size_t smem = bulk ? static_cast<size_t>(kTPC) * d * (dtype == 0 ? 4 : 2) : 0;
   if (bulk) {
     const cudaError_t st = set_bulk_smem(kernel);
@@ -484,6 +511,15 @@ cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const 
   return launch_pdl(kernel, grid, block, smem, s, x, topk_idx, T, d, k, E, nchunk, counts,
                     static_cast<const int32_t*>(nullptr), offsets, pos, src, x_perm, x_scale,
                     static_scale, err, zero, nzero, bulk);
+}
+
+cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* src, int T, int R, int d,
+                               void* x_perm, uint32_t* err, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const int vecs = d * (dtype == 0 ? 4 : 2) / 16;
+  return launch_pdl(gather_rows_kernel, dim3(ceil_div(R, 8)), dim3(256), 0, s,
+                    static_cast<const uint4*>(x), src, T, static_cast<long long>(R), vecs,
+                    static_cast<uint4*>(x_perm), err);
 }
 
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,

@@ -28,7 +28,10 @@
 // Host code cannot use the array's name as a device address (it refers to a
 // host-side stand-in). The first call on each device, with that device
 // current, looks up the real device address with cudaGetSymbolAddress and
-// caches it; make that first call before any stream capture begins.
+// caches it; make that first call before any stream capture begins. The
+// cached address belongs to the device's primary context and is never looked
+// up again, so it is stale once that context is destroyed (cudaDeviceReset):
+// a process that resets the device must not call this entry point again.
 #include <cstdint>
 #include <mutex>
 

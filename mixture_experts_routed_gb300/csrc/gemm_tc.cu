@@ -49,8 +49,16 @@
 // copies whose bytes complete the even CTA's full barrier. The per-row
 // payload scale is applied in the epilogue. This is the GEMM's dequantising
 // prologue; no bf16 copy of the payload is written to memory.
+//
+// Gathered token rows (GA, the W1 pass of the single-GPU form of the
+// Waved-EP fusion, DeepSeek V3/V4 parallel-strategy article: the dispatch
+// and the first expert GEMM in one pass): the packed rows are never written.
+// Row r of expert e's segment is row src[r] of x; 4 gather warps copy each
+// stage's rows from x into the swizzled token slot with 16-byte cp.async
+// copies (whole 128-byte row pieces per 8 lanes), wait for their own copies,
+// and release the stage like the FP8 converters do. TMA keeps the weight
+// boxes.
 #include <cstdint>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -70,6 +78,9 @@ namespace {
 using namespace ptx;
 
 struct TcParams {
+  const int32_t* gsrc;  // GA: token of each routed row (the dispatch's src)
+  const void* gx;       // GA: x [gx_rows, K] bf16, the rows gathered
+  int gx_rows;
   const int32_t* offsets;
   const float* row_scale;
   const float* zin;    // epi 2: the pre-activation Z [R, N] (fp32)
@@ -135,9 +146,9 @@ constexpr int HALF_B_BYTES = 2 * BOX_BYTES; // 16 KB: this CTA's 128 features of
 constexpr int TMEM_COLS = 512;
 // Epilogue warps: 8 for the SiLU pass (two per TMEM lane quadrant, each half
 // the columns: the exp/divide work is issue-bound at one warp per SM
-// sub-partition), 4 for the fp32 pass (plain stores; more warps only add
+// sub-partition), 4 for the fp32 passes (plain stores; more warps only add
 // store bursts against the operand loads, measured slower on GB300).
-template <int EPI>
+template <int EPI, int NB>
 __host__ __device__ constexpr int num_epi_warps() { return EPI == 0 ? 8 : 4; }
 // FP8 token rows (A8): 8 more warps expand the staged E4M3 tiles to bf16,
 // two groups of 4 taking alternate stages (one group's chain per stage, ~720
@@ -145,11 +156,14 @@ __host__ __device__ constexpr int num_epi_warps() { return EPI == 0 ? 8 : 4; }
 constexpr int CONV_GROUP = 4;
 template <bool A8>
 __host__ __device__ constexpr int num_conv_warps() { return A8 ? 2 * CONV_GROUP : 0; }
-template <int EPI, bool A8 = false>
+// Gathered token rows (GA): 4 more warps copy each stage's rows from x.
+constexpr int GATHER_WARPS = 4;
+template <bool GA>
+__host__ __device__ constexpr int num_gather_warps() { return GA ? GATHER_WARPS : 0; }
+template <int EPI, int NB, bool A8 = false, bool GA = false>
 __host__ __device__ constexpr int num_threads() {
-  return 64 + 32 * (num_epi_warps<EPI>() + num_conv_warps<A8>());
+  return 64 + 32 * (num_epi_warps<EPI, NB>() + num_conv_warps<A8>() + num_gather_warps<GA>());
 }
-constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*B MN-major*/ true);
 
 // Merged tiles (256-feature shape only). An expert whose rows end in a short
 // remainder (1..TAIL_MAX rows after at least one full 256-row tile) covers
@@ -162,7 +176,6 @@ constexpr uint32_t IDESC = make_idesc_bf16_f32(BM, 256, /*A MN-major*/ false, /*
 // second read of the weight tile nor a tile of its own.
 constexpr int MT_W = 224, MT_HALF = 112, TAIL_MAX = 32;
 constexpr int TAIL_SLOT = (TAIL_MAX / 2) * BK * 2;  // 2 KB: this CTA's half of the remainder
-constexpr uint32_t IDESC_MT = make_idesc_bf16_f32(BM, MT_W, false, true);
 
 // NB = 1: 256-feature pair tiles, two TMEM accumulators (the epilogue of one
 // tile overlaps the next tile's main loop), 6 stages of 32 KB.
@@ -202,7 +215,10 @@ struct Shape {
 // columns in shared memory past the ring (fp32: 128-byte rows, 128-byte
 // swizzle; bf16: 64-byte rows, 64-byte swizzle; 1024-byte aligned) and
 // writes it with one TMA store: whole row segments instead of 16-byte pieces
-// of 32 different rows per store instruction.
+// of 32 different rows per store instruction. (A build whose fp32 warps
+// exchanged 16-byte pieces by shuffles so that each plain store wrote four
+// whole 128-byte row segments, with no staging, measured 1 % slower on the
+// 256-expert layer's W2 pass.)
 template <int EPI>
 __host__ __device__ constexpr int stg_bytes() { return EPI == 0 ? 32 * 32 * 2 : 32 * 32 * 4; }
 template <int NB>
@@ -211,7 +227,7 @@ __host__ __device__ constexpr int off_stg() {
 }
 template <int EPI, int NB>
 __host__ __device__ constexpr int smem_bytes() {
-  return off_stg<NB>() + num_epi_warps<EPI>() * stg_bytes<EPI>() + 1024;
+  return off_stg<NB>() + num_epi_warps<EPI, NB>() * stg_bytes<EPI>() + 1024;
 }
 static_assert(smem_bytes<0, 1>() <= 227 * 1024 && smem_bytes<0, 2>() <= 227 * 1024 &&
                   smem_bytes<1, 1>() <= 227 * 1024 && smem_bytes<1, 2>() <= 227 * 1024 &&
@@ -302,16 +318,18 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
 // layer's own W2 for dH = dY W2^T, W1 for dX = dZ W1^T), and are read
 // K-major: one [128 features][64 k] box per CTA and k-block, with no
 // transposed copy in memory.
-template <int EPI, int NB, bool A8, bool BT = false>
-__global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
+template <int EPI, int NB, bool A8, bool BT = false, bool GA = false>
+__global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmA8,
                      const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmY, const TcParams p) {
   using S = pairk::Shape<NB>;
-  constexpr int NEW = pairk::num_epi_warps<EPI>();
+  constexpr int NEW = pairk::num_epi_warps<EPI, NB>();
   constexpr int NH = NEW / 4;  // warps per TMEM lane quadrant
   constexpr int NCV = pairk::num_conv_warps<A8>();
+  constexpr int NGW = pairk::num_gather_warps<GA>();
+  static_assert(!GA || (!A8 && !BT), "gathered rows: bf16 rows, weights read MN-major");
   // FP8 token rows come without merged remainder tiles (a remainder is a
   // swapped tile, its rows expanded like any other)
   constexpr bool MERGE = S::MERGE && !A8;
@@ -377,7 +395,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
         // A8: the producer's arrive and one arrive per warp of the even
         // CTA's converter group for this stage; the odd CTA's converters
         // signal through bytes (see the converters)
-        mbar_init(&full[i], A8 ? 1 + pairk::CONV_GROUP : 1);
+        mbar_init(&full[i], A8 ? 1 + pairk::CONV_GROUP : (GA ? 1 + NGW : 1));
         mbar_init(&empty[i], 1);
         mbar_init(&a8_full[i], 1);
       }
@@ -388,7 +406,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
       mbar_init(drain, 1);
       for (int i = 0; i < S::TQ; ++i) {
         mbar_init(&tq_full[i], 1);
-        mbar_init(&tq_empty[i], 2 + 2 * NEW + 2 * NCV);
+        mbar_init(&tq_empty[i], 2 + 2 * NEW + 2 * NCV + 2 * NGW);
       }
       fence_mbar_init();
     }
@@ -435,8 +453,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
-      prefetch_tmap(&tmA);
-      if (!A8) prefetch_tmap(&tmA8);
+      if (!GA) prefetch_tmap(&tmA);
+      if (!A8 && !GA) prefetch_tmap(&tmA8);
       prefetch_tmap(&tmB);
       int s = 0;
       uint32_t ph = 0, armed = 0, armed_ph = 0;
@@ -486,8 +504,11 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
         };
         int nbox[NB];
         // A8: the token rows land on this CTA's a8_full, not on full; the
-        // odd CTA's converter warps each send 16 bytes to full instead
-        uint32_t bytes = A8 ? static_cast<uint32_t>(16 * pairk::CONV_GROUP) : 2u * pairk::A_BYTES;
+        // odd CTA's converter warps each send 16 bytes to full instead. GA:
+        // the gather warps copy the rows; the odd CTA's send 16 bytes each
+        uint32_t bytes = A8   ? static_cast<uint32_t>(16 * pairk::CONV_GROUP)
+                         : GA ? static_cast<uint32_t>(16 * NGW)
+                              : 2u * pairk::A_BYTES;
 #pragma unroll
         for (int j = 0; j < NB; ++j) {
           nbox[j] = boxes(t.n0 + j * 256 + static_cast<int>(rank) * half_w);
@@ -498,7 +519,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
         // 8-row boxes
         const int tail_half = ((t.tail + 15) & ~15) / 2;
         const int tail_row = t.row0 - a_base + pairk::BM + static_cast<int>(rank) * tail_half;
-        bytes += static_cast<uint32_t>(2 * tail_half * pairk::BK * 2);
+        if (!GA) bytes += static_cast<uint32_t>(2 * tail_half * pairk::BK * 2);
         const int brow = t.e * p.K;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs)) {
@@ -512,6 +533,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
             // of the stage's token slot; the converters expand them in place
             mbar_arrive_expect_tx(&a8_full[s], static_cast<uint32_t>(pairk::A_BYTES / 2));
             tma_load_2d(sA + s * pairk::A_BYTES, &tmA, &a8_full[s], kb * pairk::BK, my_row);
+          } else if constexpr (GA) {
+            // (the gather warps fill the token slot)
           } else {
             tma_load_2d_pair(sA + s * pairk::A_BYTES, &tmA, bar, kb * pairk::BK, my_row);
           }
@@ -529,7 +552,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
                     bar, t.n0 + j * 256 + static_cast<int>(rank) * half_w + c * 64,
                     brow + kb * pairk::BK);
           }
-          if constexpr (MERGE) {
+          if constexpr (MERGE && !GA) {
             for (int r = 0; r < tail_half; r += 8)
               tma_load_2d_pair(sT + s * S::T_BYTES + r * pairk::BK * 2, &tmA8, bar,
                                kb * pairk::BK, min(tail_row + r, p.a_rows - 1));
@@ -583,7 +606,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
           const uint32_t idesc_tail =
               make_idesc_bf16_f32(pairk::BM, (t.tail + 15) & ~15, !BT, false);
           for (int kb = 0; kb < KB; ++kb) {
-            if (!mbar_wait_spin(&full[s], ph, kWaitLimitNs)) {
+            if (!(GA ? mbar_wait_spin_cluster(&full[s], ph, kWaitLimitNs)
+                     : mbar_wait_spin(&full[s], ph, kWaitLimitNs))) {
               timed_out = true;
               break;
             }
@@ -611,8 +635,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
           for (int kb = 0; kb < KB; ++kb) {
             // A8: the odd CTA's converters released their rows with a
             // cluster-scope arrive; acquire at cluster scope
-            if (!(A8 ? mbar_wait_spin_cluster(&full[s], ph, kWaitLimitNs)
-                     : mbar_wait_spin(&full[s], ph, kWaitLimitNs))) {
+            if (!((A8 || GA) ? mbar_wait_spin_cluster(&full[s], ph, kWaitLimitNs)
+                             : mbar_wait_spin(&full[s], ph, kWaitLimitNs))) {
               timed_out = true;
               break;
             }
@@ -650,7 +674,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
         mbar_wait_spin(drain, 0, kWaitLimitNs);
       }
     }
-  } else if (!A8 || warp < 2 + NEW) {
+  } else if (warp < 2 + NEW) {
     // ------------------------------------------------------------ epilogue (both CTAs)
     // warp w reads TMEM lanes 32 (w % 4) .. +31; with 8 warps, warps 2-5
     // take the first half of the accumulator columns, warps 6-9 the second
@@ -910,6 +934,101 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, A8>(), 1)
       }
     }
     if (lane == 0) bulk_wait_group0();  // this warp's TMA stores are done
+  } else if constexpr (GA) {
+    // ------------------------------------------------------------ row gather (GA, both CTAs)
+    // Thread g copies chunk g % 8 (16 bytes) of rows g / 8 + 16 j, j = 0..7,
+    // of each stage's k-block: 8 lanes read one row's 128 contiguous bytes.
+    // Up to STAGES stages are in flight per thread; when the oldest has
+    // landed (the thread's own copies: cp.async.wait_group) its writes are
+    // made visible to the tensor cores (proxy fence) and the stage is
+    // released to the MMA: an arrive on full (even CTA), or a 16-byte bulk
+    // copy whose bytes complete the even CTA's full barrier (odd CTA).
+    const int gidx = static_cast<int>(threadIdx.x) - 32 * (2 + NEW);
+    const int ch = gidx & 7;
+    const int rg = gidx >> 3;
+    const uint32_t swz = static_cast<uint32_t>((ch ^ (rg & 7)) << 4);
+    const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
+    const uint32_t leader_sink = mapa_shared(smem_u32(smem + S::OFF_SINK), 0);
+    const uint32_t my_sink = smem_u32(smem + S::OFF_SINK);
+    const __nv_bfloat16* gx = static_cast<const __nv_bfloat16*>(p.gx);
+    // a routed row's token; a bad one is flagged and read as token 0
+    auto token_row = [&](int r) -> const __nv_bfloat16* {
+      int tok = __ldg(p.gsrc + min(r, p.R - 1));
+      if (tok < 0 || tok >= p.gx_rows) {
+        atomicOr(p.err, kErrBadIndex);
+        tok = 0;
+      }
+      return gx + static_cast<size_t>(tok) * p.K + ch * 8;
+    };
+    int s = 0, so = 0, inflight = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    auto release_oldest = [&]() {
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&full[so]);
+        else
+          bulk_copy_s2cluster(leader_sink, my_sink, 16u,
+                              leader_full + static_cast<uint32_t>(so * 8));
+      }
+      if (++so == S::STAGES) so = 0;
+      --inflight;
+    };
+    for (;;) {
+      const int tile = next_tile(true);
+      if (tile >= total || timed_out) break;
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
+      // this CTA's rows: 128 of a full tile, its half of a swapped tile's
+      // tokens (rounded to 16); rows past the segment read a valid row and
+      // feed only outputs the epilogue does not store
+      const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
+      const int r0 = t.row0 + static_cast<int>(rank) * half_rows;
+      const __nv_bfloat16* rowp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) rowp[j] = rg + 16 * j < half_rows ? token_row(r0 + rg + 16 * j) : nullptr;
+      // merged tile: this CTA's half of the remainder rows (8 or 16)
+      const __nv_bfloat16* tailp = nullptr;
+      if constexpr (MERGE) {
+        const int tail_half = ((t.tail + 15) & ~15) / 2;
+        if (rg < tail_half)
+          tailp = token_row(t.row0 + pairk::BM + static_cast<int>(rank) * tail_half + rg);
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs);
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = smem_u32(sA + s * pairk::A_BYTES) + swz;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (rowp[j] != nullptr)
+            cp_async16(dst + static_cast<uint32_t>((rg + 16 * j) * 128), rowp[j] + kb * pairk::BK);
+        if constexpr (MERGE) {
+          if (tailp != nullptr)
+            cp_async16(smem_u32(sT + s * S::T_BYTES) + static_cast<uint32_t>(rg * 128) + swz,
+                       tailp + kb * pairk::BK);
+        }
+        cp_async_commit();
+        ++inflight;
+        if (++s == S::STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+        if (inflight == S::STAGES) {
+          cp_async_wait<S::STAGES - 1>();
+          release_oldest();
+        }
+      }
+      if (!ok) break;
+    }
+    // every copy lands before the CTA can leave; stages still held go to the MMA
+    cp_async_wait<0>();
+    while (inflight > 0) release_oldest();
+    if (!ok) timed_out = true;
   } else {
     // ------------------------------------------------------------ FP8 converters (A8, both CTAs)
     // Thread ct expands row ct of each staged tile: 64 E4M3 bytes (64-byte
@@ -1078,12 +1197,12 @@ bool make_map_2d_e4m3(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
 
 namespace {
 
-template <int EPI, int NB, bool A8, bool BT>
+template <int EPI, int NB, bool A8, bool BT, bool GA>
 cudaError_t set_pair_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB, A8, BT>,
+    st = cudaFuncSetAttribute(gemm_pair_kernel<EPI, NB, A8, BT, GA>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               pairk::smem_bytes<EPI, NB>());
   });
@@ -1091,7 +1210,7 @@ cudaError_t set_pair_smem_attr() {
 }
 
 // Clusters of two that can be resident at once (cached per device and kernel).
-template <int EPI, int NB, bool A8, bool BT>
+template <int EPI, int NB, bool A8, bool BT, bool GA>
 int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   static int cache[64] = {};
   int dev = 0;
@@ -1100,7 +1219,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   cudaLaunchConfig_t lc = lc_in;
   lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB, A8, BT>, &lc) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<EPI, NB, A8, BT, GA>, &lc) != cudaSuccess ||
       n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
@@ -1109,7 +1228,7 @@ int resident_pairs(const cudaLaunchConfig_t& lc_in, int num_sms) {
   return n;
 }
 
-template <int EPI, int NB, bool A8, bool BT = false>
+template <int EPI, int NB, bool A8, bool BT = false, bool GA = false>
 cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUtensorMap& mB,
                         const CUtensorMap& mY, TcParams prm, int num_sms,
                         cudaStream_t s) {
@@ -1120,7 +1239,7 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
       static_cast<long long>(ceil_div(prm.R, pairk::BM) + prm.E) *
       static_cast<long long>(prm.n_tiles > prm.n_tiles_m ? prm.n_tiles : prm.n_tiles_m);
   cudaLaunchConfig_t lc = {};
-  lc.blockDim = dim3(pairk::num_threads<EPI, A8>());
+  lc.blockDim = dim3(pairk::num_threads<EPI, NB, A8, GA>());
   lc.dynamicSmemBytes = pairk::smem_bytes<EPI, NB>();
   lc.stream = s;
   cudaLaunchAttribute attr[2];
@@ -1132,14 +1251,14 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
-  cudaError_t st = set_pair_smem_attr<EPI, NB, A8, BT>();
+  cudaError_t st = set_pair_smem_attr<EPI, NB, A8, BT, GA>();
   if (st != cudaSuccess) return st;
   // a persistent grid must fit at once: as many pairs as can be resident
   // together (a pair needs two free SMs of one GPC), not num_sms / 2
-  const int resident = resident_pairs<EPI, NB, A8, BT>(lc, num_sms);
+  const int resident = resident_pairs<EPI, NB, A8, BT, GA>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
   lc.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8, BT>, mA, mA8, mB, mY, prm);
+  return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8, BT, GA>, mA, mA8, mB, mY, prm);
 }
 
 // 512-feature tiles (one accumulator, epilogue exposed) pay off only for the
@@ -1157,28 +1276,32 @@ int pick_nb(int epi, int R, int E, int K, int N, int num_sms) {
 cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
                            const void* W, int E, int K, int N, const int32_t* offsets,
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
-                           int num_sms, cudaStream_t s) {
+                           const int32_t* gather_src, int tile_n, int num_sms, cudaStream_t s) {
   if (R == 0) return cudaSuccess;
   if (num_sms < 2 || (a_fp8 && epi != 0)) return cudaErrorInvalidValue;
+  if (tile_n != 0 && tile_n != 256 && tile_n != 512) return cudaErrorInvalidValue;
+  // gathered rows: bf16 token rows of x read through src, W1 pass only
+  if (gather_src != nullptr && (a_fp8 || a_shared || epi != 0)) return cudaErrorInvalidValue;
   CUtensorMap mA, mA8, mB, mY;
   std::memset(&mY, 0, sizeof(mY));
   std::memset(&mA, 0, sizeof(mA));
   std::memset(&mA8, 0, sizeof(mA8));
   std::memset(&mB, 0, sizeof(mB));
-  // A: token rows, [128 rows][64 k] boxes; B: weights as [E*K rows, N], [64 k][64 n] boxes
   // A: token rows in [128 rows][64 k] boxes, and [8 rows][64 k] boxes for
-  // merged tiles' remainders
+  // merged tiles' remainders (none when the rows are gathered)
   if (a_rows <= 0) return cudaErrorInvalidValue;
   if (a_fp8) {
     // E4M3 token rows, expanded to bf16 in shared memory (no merged tiles)
     if (!make_map_2d_e4m3(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K)))
       return cudaErrorInvalidValue;
-  } else if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64,
-                          128) ||
-             !make_map_2d(&mA8, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64,
-                          8)) {
+  } else if (gather_src == nullptr &&
+             (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64,
+                           128) ||
+              !make_map_2d(&mA8, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64,
+                           8))) {
     return cudaErrorInvalidValue;
   }
+  // B: the weights as [E*K rows, N], [64 k][64 n] boxes
   if (!make_map_2d(&mB, W, static_cast<uint64_t>(E) * K, static_cast<uint64_t>(N), 64,
                    pairk::BK))
     return cudaErrorInvalidValue;
@@ -1186,6 +1309,9 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
   if (!make_map_2d_out(&mY, out, static_cast<uint64_t>(R), static_cast<uint64_t>(N), epi == 1))
     return cudaErrorInvalidValue;
   TcParams prm;
+  prm.gsrc = gather_src;
+  prm.gx = gather_src != nullptr ? A : nullptr;
+  prm.gx_rows = a_rows;
   prm.offsets = offsets;
   prm.row_scale = row_scale;
   prm.zin = nullptr;
@@ -1200,13 +1326,12 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
   prm.a_rows = a_rows;
   prm.a_shared = a_shared;
   prm.k_wrap = K;
-  int nb = pick_nb(epi, R, E, K, N, num_sms);
-  // MOE_GEMM_TILE_FEATURES=256|512 overrides the choice (read on every call)
-  if (const char* f = std::getenv("MOE_GEMM_TILE_FEATURES")) {
-    if (std::strcmp(f, "256") == 0) nb = 1;
-    if (std::strcmp(f, "512") == 0) nb = 2;
-  }
+  // tile_n 256 or 512 forces the pair-tile width; 0 takes the built-in choice
+  const int nb = tile_n == 0 ? pick_nb(epi, R, E, K, N, num_sms) : tile_n / 256;
   if (a_fp8) return launch_pair<0, 1, true>(mA, mA8, mB, mY, prm, num_sms, s);
+  if (gather_src != nullptr)
+    return nb == 2 ? launch_pair<0, 2, false, false, true>(mA, mA8, mB, mY, prm, num_sms, s)
+                   : launch_pair<0, 1, false, false, true>(mA, mA8, mB, mY, prm, num_sms, s);
   if (epi == 0)
     return nb == 2 ? launch_pair<0, 2, false>(mA, mA8, mB, mY, prm, num_sms, s)
                    : launch_pair<0, 1, false>(mA, mA8, mB, mY, prm, num_sms, s);
@@ -1234,6 +1359,9 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
                        static_cast<uint64_t>(zin ? 2 * N : N), zin == nullptr))
     return cudaErrorInvalidValue;
   TcParams prm;
+  prm.gsrc = nullptr;
+  prm.gx = nullptr;
+  prm.gx_rows = 0;
   prm.offsets = offsets;
   prm.row_scale = nullptr;
   prm.zin = zin;

@@ -49,12 +49,31 @@ int check_cfg(const moe_config_t* c) {
   if (c->payload_fp8 && c->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->d > 65536 || c->f > 65536) return MOE_ERR_UNSUPPORTED;
   if (static_cast<long long>(c->T) * c->k > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  if (c->gemm_tile_n != 0 && c->gemm_tile_n != 256 && c->gemm_tile_n != 512)
+    return MOE_ERR_INVALID_ARG;
+  if (c->x_perm_mode < MOE_XPERM_AUTO || c->x_perm_mode > MOE_XPERM_GATHERED)
+    return MOE_ERR_INVALID_ARG;
+  // gathered rows: bf16 rows of x, no FP8 payload, not soft gating (which
+  // reads x itself already)
+  if (c->x_perm_mode == MOE_XPERM_GATHERED &&
+      (c->dtype != MOE_DTYPE_BF16 || c->payload_fp8 || c->router == MOE_ROUTER_SOFT_GUMBEL))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
 size_t elem_size(int dtype) { return dtype == MOE_DTYPE_F32 ? 4 : 2; }
 
 bool soft(const moe_config_t& c) { return c.router == MOE_ROUTER_SOFT_GUMBEL; }
+
+// moe_forward's W1 GEMM gathers the routed rows from x through src (the
+// packed rows x_perm are not written): asked for, or the library's choice
+// for bf16 layers without an FP8 payload or soft gating.
+constexpr bool kGatherByDefault = false;
+bool gathers(const moe_config_t& c) {
+  if (c.dtype != MOE_DTYPE_BF16 || c.payload_fp8 || soft(c)) return false;
+  return c.x_perm_mode == MOE_XPERM_GATHERED ||
+         (c.x_perm_mode == MOE_XPERM_AUTO && kGatherByDefault);
+}
 
 struct Layout {
   size_t err, hist, base, scratch_end;
@@ -84,8 +103,9 @@ Layout layout_of(const moe_config_t& c) {
   L.offsets = take(static_cast<size_t>(c.E + 1) * 4);
   L.pos = take(R * 4);
   L.src = take(R * 4);
-  // soft gating: every expert reads x itself, nothing is packed
-  L.x_perm = take(soft(c) ? 0 : R * c.d * (c.payload_fp8 ? 1 : es));
+  // soft gating: every expert reads x itself, nothing is packed; gathered
+  // rows: the W1 GEMM reads x through src
+  L.x_perm = take(soft(c) || gathers(c) ? 0 : R * c.d * (c.payload_fp8 ? 1 : es));
   L.x_scale = take(c.payload_fp8 ? R * 4 : 0);
   L.h = take(R * c.f * es);
   L.y = take(R * c.d * 4);
@@ -157,9 +177,11 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
   return status_of(e);
 }
 
+// which 1: the W1 pass, reading x_perm, or (gather_src non-null) x itself
+// through the routed rows' tokens; which 2: the W2 pass.
 int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const void* x_perm,
              const float* x_scale, const int32_t* offsets, const void* W1, const void* W2,
-             void* h, float* y, cudaStream_t s) {
+             void* h, float* y, cudaStream_t s, const int32_t* gather_src = nullptr) {
   const int R = c.T * c.k;
   if (R == 0) return MOE_OK;
   uint32_t* err = at<uint32_t>(ws, L.err);
@@ -177,13 +199,15 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
   uint32_t* ctr = gemm_counters(ws) + (which - 1);
   if (which == 1) {
     // soft gating: x_perm is x itself, [T, d], read by every expert; the
-    // FP8 payload is expanded to bf16 inside the GEMM (its prologue)
-    return status_of(launch_gemm_tc(0, x_perm, c.payload_fp8 ? 1 : 0, soft(c) ? c.T : R,
-                                    soft(c) ? 1 : 0, R, W1, c.E, c.d, c.f, offsets,
-                                    c.payload_fp8 ? x_scale : nullptr, h, err, ctr, sms, s));
+    // FP8 payload is expanded to bf16 inside the GEMM (its prologue);
+    // gathered rows: x_perm is x, [T, d], row r of the layout reads x[src[r]]
+    return status_of(launch_gemm_tc(0, x_perm, c.payload_fp8 ? 1 : 0,
+                                    soft(c) || gather_src ? c.T : R, soft(c) ? 1 : 0, R, W1, c.E,
+                                    c.d, c.f, offsets, c.payload_fp8 ? x_scale : nullptr, h, err,
+                                    ctr, gather_src, c.gemm_tile_n, sms, s));
   }
-  return status_of(
-      launch_gemm_tc(1, h, 0, R, 0, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err, ctr, sms, s));
+  return status_of(launch_gemm_tc(1, h, 0, R, 0, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err,
+                                  ctr, nullptr, c.gemm_tile_n, sms, s));
 }
 
 int run_combine(const moe_config_t& c, const Layout& L, void* ws, const float* y,
@@ -212,8 +236,11 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
   int32_t* offsets = at<int32_t>(ws, L.offsets);
   int32_t* pos = at<int32_t>(ws, L.pos);
   int32_t* src = at<int32_t>(ws, L.src);
-  // soft gating packs nothing: the W1 GEMM reads x for every expert
-  void* x_perm = soft(c) ? const_cast<void*>(x) : at<void>(ws, L.x_perm);
+  // soft gating packs nothing: the W1 GEMM reads x for every expert; with
+  // gathered rows the dispatch writes only the layout and the W1 GEMM reads
+  // each routed row from x through src
+  const bool ga = gathers(c);
+  void* x_perm = soft(c) ? const_cast<void*>(x) : (ga ? nullptr : at<void>(ws, L.x_perm));
   float* x_scale = c.payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
   void* h = at<void>(ws, L.h);
   float* y = at<float>(ws, L.y);
@@ -228,7 +255,8 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
     return st;
   record(events, 2, s);
   record(events, 3, s);  // (no kernel: the FP8 payload is expanded inside the W1 GEMM)
-  if ((st = run_gemm(c, L, ws, 1, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
+  if ((st = run_gemm(c, L, ws, 1, ga ? x : x_perm, x_scale, offsets, W1, W2, h, y, s,
+                     ga ? src : nullptr)) != MOE_OK)
     return st;
   record(events, 4, s);
   if ((st = run_gemm(c, L, ws, 2, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
@@ -261,7 +289,7 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // operands: the bf16 splits of dY, dZ and dL.
 struct BwdLayout {
   size_t err, L, ridx, rw, dw, dL, seg01, segk, bpart, gpart, dY, Z, dXp, dxg, dYs, dZs, dLs,
-      total;
+      xp, total;
 };
 
 // Token chunks of the gate's weight gradient (split along T so that its few
@@ -318,6 +346,8 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
   B.dZs = take(tc ? R * 2 * c.f * 2 : 0);
   B.dLs = take(tc ? T * 2 * E * 2 : 0);
+  // the packed rows, when the forward gathered them instead of writing them
+  B.xp = take(gathers(c) ? R * c.d * 2 : 0);
   B.total = o;
   return B;
 }
@@ -346,7 +376,9 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   const float* w = at<float>(fws, L.topk_w);
   const int32_t* offsets = at<int32_t>(fws, L.offsets);
   const int32_t* pos = at<int32_t>(fws, L.pos);
-  const void* x_perm = soft(c) ? x : at<void>(fws, L.x_perm);
+  // the packed rows: the forward's, or (gathered forward) packed here from x
+  // through the forward's src
+  const void* x_perm = soft(c) ? x : (gathers(c) ? at<void>(bws, B.xp) : at<void>(fws, L.x_perm));
   const void* h = at<void>(fws, L.h);
   const float* y = at<float>(fws, L.y);
   uint32_t* err = at<uint32_t>(bws, B.err);
@@ -377,7 +409,11 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   const TokChunks ch = tok_chunks(c, sms);
   int32_t* segk = at<int32_t>(bws, B.segk);
   uint32_t* ctr = at<uint32_t>(bws, kGemmCounterOffset);  // four tile counters
-  cudaError_t e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
+  cudaError_t e = gathers(c) ? launch_gather_rows(dt, x, at<int32_t>(fws, L.src), T, R, d,
+                                                  at<void>(bws, B.xp), err, s)
+                             : cudaSuccess;
+  if (e == cudaSuccess)
+    e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
                                      tc ? at<void>(bws, B.dYs) : nullptr, dw, err, ctr, 4, seg01,
                                      segk, ch.n, ch.len, s);
   void* dLs = tc ? at<void>(bws, B.dLs) : nullptr;
@@ -419,7 +455,7 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
                            static_cast<const float*>(W1), E, d, f, offsets, Z, err, s);
     } else {
       e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
-                         nullptr, Z, err, ctr, sms, s);
+                         nullptr, Z, err, ctr, nullptr, c.gemm_tile_n, sms, s);
       // dH = [dY hi | dY lo] . [W2_e^T ; W2_e^T], its epilogue writing the
       // split of dZ = dH * SiLU'(Z); dX_perm = [dZ hi | dZ lo] . [W1_e^T ;
       // W1_e^T]: the stored weights read K-major, K = 2d (2f) wrapping at d (f)
@@ -584,7 +620,7 @@ int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* v)
   v->offsets = at<int32_t>(ws, L.offsets);
   v->pos = at<int32_t>(ws, L.pos);
   v->src = at<int32_t>(ws, L.src);
-  v->x_perm = soft(*cfg) ? nullptr : at<void>(ws, L.x_perm);
+  v->x_perm = soft(*cfg) || gathers(*cfg) ? nullptr : at<void>(ws, L.x_perm);
   v->x_scale = cfg->payload_fp8 ? at<float>(ws, L.x_scale) : nullptr;
   v->h = at<void>(ws, L.h);
   v->y_perm = at<float>(ws, L.y);

@@ -257,6 +257,22 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16-byte copy global -> this CTA's shared memory through L2 only (no L1
+// allocation), asynchronous; completion is tracked per thread by
+// commit/wait groups. Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Bulk copy of `bytes` (a multiple of 16, 16-byte aligned) from this CTA's
 // shared memory to another CTA's (shared::cluster addresses from mapa for
 // the destination and its mbarrier); completion is counted in bytes on that

@@ -54,7 +54,8 @@ def test_only_abi_symbols_are_exported(lib):
 
 def cfg(**kw):
     base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0,
-                n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0, tau=0.0)
+                n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0, tau=0.0,
+                gemm_tile_n=0, x_perm_mode=0)
     base.update(kw)
     return L.MoeConfig(*[base[n] for n, _ in L.MoeConfig._fields_])
 
@@ -98,6 +99,21 @@ def cfg(**kw):
     (dict(payload_fp8=2, payload_scale=float("nan")), L.MOE_ERR_INVALID_ARG),
     (dict(payload_fp8=2, payload_scale=0.04, dtype=0), L.MOE_ERR_UNSUPPORTED),
     (dict(payload_fp8=0, payload_scale=-5.0), L.MOE_OK),
+    # the GEMM pair-tile width: the built-in choice (0) or forced to 256 / 512
+    (dict(gemm_tile_n=256), L.MOE_OK),
+    (dict(gemm_tile_n=512), L.MOE_OK),
+    (dict(gemm_tile_n=128), L.MOE_ERR_INVALID_ARG),
+    (dict(gemm_tile_n=-1), L.MOE_ERR_INVALID_ARG),
+    # packed or gathered rows: gathering takes bf16 without FP8 payload or soft gating
+    (dict(x_perm_mode=1), L.MOE_OK),
+    (dict(x_perm_mode=2), L.MOE_OK),
+    (dict(x_perm_mode=2, E=256, k=8), L.MOE_OK),
+    (dict(x_perm_mode=3), L.MOE_ERR_INVALID_ARG),
+    (dict(x_perm_mode=-1), L.MOE_ERR_INVALID_ARG),
+    (dict(x_perm_mode=2, dtype=0), L.MOE_ERR_UNSUPPORTED),
+    (dict(x_perm_mode=2, payload_fp8=1), L.MOE_ERR_UNSUPPORTED),
+    (dict(x_perm_mode=2, router=3, E=8, k=8, tau=1.0), L.MOE_ERR_UNSUPPORTED),
+    (dict(x_perm_mode=1, dtype=0), L.MOE_OK),
     (dict(output_fp8=1), L.MOE_OK),
     (dict(output_fp8=1, dtype=0), L.MOE_OK),
     (dict(output_fp8=2), L.MOE_ERR_INVALID_ARG),

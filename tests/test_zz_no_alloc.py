@@ -20,6 +20,9 @@ SHAPES = [
     MoEConfig("na_bf16_T129_d256_E8_k2", T=129, d=256, E=8, k=2, f=128, dtype="bf16", seed=31),
     MoEConfig("na_fp8_T300_d512_E16_k2", T=300, d=512, E=16, k=2, f=128, dtype="bf16",
               payload_fp8=True, outlier_rate=0.01, seed=32),
+    # one static FP8 scale for every row (small enough that the outliers saturate)
+    MoEConfig("na_fp8static_T300_d512_E16_k2", T=300, d=512, E=16, k=2, f=128, dtype="bf16",
+              payload_fp8=2, payload_scale=0.02, outlier_rate=0.01, seed=35),
     MoEConfig("na_f32_T64_d128_E5_k2", T=64, d=128, E=5, k=2, f=128, dtype="f32", pre_k=5,
               seed=33),
     MoEConfig("na_zipf_T2048_d256_E256_k8", T=2048, d=256, E=256, k=8, f=128, dtype="bf16",
@@ -37,7 +40,7 @@ def lib():
 
 def _cfg(c):
     return L.MoeConfig(c.T, c.d, c.E, c.k, c.f, 0 if c.dtype == "f32" else 1, c.router,
-                       c.pre_k, int(c.payload_fp8))
+                       c.pre_k, int(c.payload_fp8), payload_scale=c.payload_scale)
 
 
 def _p(t):

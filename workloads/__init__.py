@@ -58,6 +58,8 @@ class MoEConfig:
     payload_scale: float = 0.0  # the static scale (payload_fp8 == 2)
     output_fp8: int = 0       # 1: expert outputs reach the combine as FP8 (min/max affine)
     tau: float = 1.0          # soft gating temperature
+    gemm_tile_n: int = 0      # expert GEMM pair-tile width: 0 = the library's choice, 256, 512
+    x_perm_mode: int = 0      # 0 = the library's choice, 1 = packed rows, 2 = gathered by the W1 GEMM
     bias: str = "zero"        # "zero" | "normal" (variance bias_var) | "zipf" (exponent zipf_s)
     bias_var: float = 0.0
     zipf_s: float = 0.0
@@ -131,8 +133,16 @@ VARIANTS = {
         f=2048, dtype="bf16", router=ROUTER_GROUP_LIMITED, n_group=8, topk_group=4,
         bias="zipf", zipf_s=1.1, seed=4),
 }
-# The layer the headline throughput is quoted on (balanced, 8 experts).
-BENCH_CONFIG = CONFIG_ORDER[1]
+# A scaled-down copy of the fine-grained skewed layer (same d, f, k, router
+# and Zipf bias; 32 experts over 2048 tokens keep its mean of 512 rows per
+# expert): small enough for detailed profiler captures of its kernels.
+VARIANTS["skewed_small_T2048_d7168_E32_k8_f2048_zipf"] = MoEConfig(
+    "skewed_small_T2048_d7168_E32_k8_f2048_zipf", T=2048, d=7168, E=32, k=8, f=2048,
+    dtype="bf16", bias="zipf", zipf_s=1.1, seed=4)
+
+# The layer the headline throughput is quoted on: the largest that fits one
+# GPU, the fine-grained skewed layer (256 experts, top-8).
+BENCH_CONFIG = CONFIG_ORDER[4]
 
 
 def get_config(name: str) -> MoEConfig:
