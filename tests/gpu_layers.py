@@ -247,3 +247,42 @@ def oracle_payload(name: str):
     """Per-token FP8 payload of the oracle: (q values, scales)."""
     cfg, _, host = layer(name)
     return oracle.quantize_payload_fp8(host["x"], payload_static(cfg))
+
+
+def tile_class_experts(offsets: np.ndarray, bm: int = 256, tail_max: int = 32) -> dict:
+    """One expert of each GEMM tile form, from a dispatch's offsets: the
+    heaviest; the smallest whose rows end in a merged remainder (at least one
+    full 256-row tile, then 1..32 rows); the smallest with a swapped remainder
+    (33..255 rows after its full tiles, or fewer than 256 rows in all); the
+    smallest with a single row. A form no expert has is left out."""
+    counts = np.diff(np.asarray(offsets, np.int64))
+    order = np.argsort(counts, kind="stable")
+    out = {"heaviest": int(np.argmax(counts))}
+    for e in order:
+        c, e = int(counts[e]), int(e)
+        rem = c % bm
+        if c == 0:
+            continue
+        if "merged_tail" not in out and c > bm and 1 <= rem <= tail_max:
+            out["merged_tail"] = e
+        if "swapped_tail" not in out and rem > tail_max:
+            out["swapped_tail"] = e
+        if "one_row" not in out and c == 1:
+            out["one_row"] = e
+    return out
+
+
+def tile_rows(offsets: np.ndarray, e: int, bm: int = 256) -> np.ndarray:
+    """Routed rows of expert e in its first tile and in its last full tile
+    plus remainder (all its rows when it has at most two tiles' worth)."""
+    lo, hi = int(offsets[e]), int(offsets[e + 1])
+    full = (hi - lo) // bm
+    last = lo + max(full - 1, 0) * bm
+    return np.unique(np.concatenate([np.arange(lo, min(hi, lo + bm)), np.arange(last, hi)]))
+
+
+def targeted_tokens(offsets: np.ndarray, src: np.ndarray) -> np.ndarray:
+    """Tokens routed to the first and last tiles of each expert that
+    tile_class_experts picks (every such token, not a sample)."""
+    rows = [tile_rows(offsets, e) for e in tile_class_experts(offsets).values()]
+    return np.unique(np.asarray(src)[np.concatenate(rows)])

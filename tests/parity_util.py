@@ -54,6 +54,33 @@ def assert_close(got, ref, rel, max_abs, what=""):
     return r, m
 
 
+def bf16_ulp(v) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits): 2^(e - 7) for
+    |v| in [2^e, 2^(e+1)); the subnormal spacing below 2^-126."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def assert_close_bf16_stored(got, ref, rel, max_abs, what=""):
+    """assert_close for values stored in bf16 (the expert FFN's H): both
+    sides round an fp32 (GPU) or fp64 (oracle) sum to bf16, and a sum that
+    lies next to a rounding midpoint may round to the neighbouring bf16
+    value on one side. Each element may therefore also differ by one bf16
+    ulp of its value; rel-L2 stays bounded as usual."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    r = rel_l2(got, ref)
+    d = np.abs(got - ref)
+    bad = d > np.maximum(max_abs, bf16_ulp(ref))
+    assert r <= rel and not bad.any(), (
+        f"{what}: rel_l2={r:.3e} (<= {rel}), {int(bad.sum())} elements beyond max(max_abs "
+        f"{max_abs}, one bf16 ulp), largest difference {float(d.max()) if d.size else 0.0:.3e}")
+    return r, float(d.max()) if d.size else 0.0
+
+
 def out_tolerance(cfg):
     if cfg.dtype == "f32":
         return F32_REL_L2, F32_MAX_ABS

@@ -8,8 +8,9 @@ import torch
 import oracle
 import mixture_experts_routed_gb300 as moe
 from gpu_layers import (SMALL_NAMES, FULL_NAMES, layer, oracle_route, oracle_dispatch,
-                        oracle_payload, sample_rows)
-from parity_util import assert_close, out_tolerance, to_np, BF16_REL_L2, BF16_MAX_ABS
+                        oracle_payload, sample_rows, tile_class_experts)
+from parity_util import (assert_close, assert_close_bf16_stored, out_tolerance, to_np,
+                         BF16_REL_L2, BF16_MAX_ABS)
 
 pytestmark = pytest.mark.gpu
 NAMES = SMALL_NAMES + FULL_NAMES
@@ -30,13 +31,14 @@ def _ffn_inputs(cfg, inp, host, src, name):
 
 
 @pytest.mark.parametrize("name", NAMES)
-def test_expert_ffn_parity(cuda_ok, name):
+def test_expert_ffn_parity(cuda_ok, name, gemm_tile_n=0):
     cfg, inp, host = layer(name)
     counts, offsets, pos, src = oracle_dispatch(name)
     x_perm, x_scale, x_hat = _ffn_inputs(cfg, inp, host, src, name)
     off_t = torch.from_numpy(offsets.astype(np.int32)).cuda()
     ws = moe.alloc_workspace(cfg, kind="scratch")
-    h, y = moe.expert_ffn(cfg, x_perm, x_scale, off_t, inp["W1"], inp["W2"], ws=ws)
+    h, y = moe.expert_ffn(cfg.with_(gemm_tile_n=gemm_tile_n), x_perm, x_scale, off_t, inp["W1"],
+                          inp["W2"], ws=ws)
     torch.cuda.synchronize()
     assert moe.get_device_error(ws) == moe.MOE_OK
     storage = "bf16" if cfg.dtype == "bf16" else "f32"
@@ -44,13 +46,21 @@ def test_expert_ffn_parity(cuda_ok, name):
     full = cfg.R <= 4096
     rows = {e: list(range(int(offsets[e]), int(offsets[e + 1]))) for e in range(cfg.E)
             if offsets[e + 1] > offsets[e]} if full else sample_rows(offsets)
+    if not full:
+        # every row of one expert of each tile form (the heaviest; a merged,
+        # a swapped and a one-row remainder), besides the sampled rows
+        for e in tile_class_experts(offsets).values():
+            rows[e] = list(range(int(offsets[e]), int(offsets[e + 1])))
     for e, rs in rows.items():
         rs = np.asarray(rs)
         W1e = oracle.moe_oracle._expert(inp["W1"], e)
         W2e = oracle.moe_oracle._expert(inp["W2"], e)
         y_ref, h_ref = oracle.expert_ffn_rows(x_hat[src[rs]], W1e, W2e, storage)
         rs_t = torch.from_numpy(rs).cuda()
-        assert_close(to_np(h[rs_t]), h_ref, rel, mabs, f"{name} H expert {e}")
+        if storage == "bf16":
+            assert_close_bf16_stored(to_np(h[rs_t]), h_ref, rel, mabs, f"{name} H expert {e}")
+        else:
+            assert_close(to_np(h[rs_t]), h_ref, rel, mabs, f"{name} H expert {e}")
         assert_close(to_np(y[rs_t]), y_ref, rel, mabs, f"{name} Y expert {e}")
 
 
@@ -141,6 +151,5 @@ WIDTH_CASES.append((FULL_NAMES[4], "256"))
 
 
 @pytest.mark.parametrize("name,width", WIDTH_CASES)
-def test_expert_ffn_tile_width(cuda_ok, monkeypatch, name, width):
-    monkeypatch.setenv("MOE_GEMM_TILE_FEATURES", width)
-    test_expert_ffn_parity(cuda_ok, name)
+def test_expert_ffn_tile_width(cuda_ok, name, width):
+    test_expert_ffn_parity(cuda_ok, name, gemm_tile_n=int(width))

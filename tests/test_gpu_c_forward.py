@@ -8,14 +8,18 @@ import torch
 
 import oracle
 import mixture_experts_routed_gb300 as moe
-from gpu_layers import (SMALL_NAMES, FULL_NAMES, VARIANT_NAMES, ORACLE_FULL_OK, layer, oracle_route,
-                        oracle_dispatch)
+from gpu_layers import (ALL, SMALL_NAMES, FULL_NAMES, VARIANT_NAMES, ORACLE_FULL_OK, layer,
+                        oracle_route, oracle_dispatch, targeted_tokens)
 from parity_util import assert_close, assert_close_output_fp8, out_tolerance, route_ties, to_np
 
 pytestmark = pytest.mark.gpu
 NAMES = SMALL_NAMES + FULL_NAMES + VARIANT_NAMES
-SAMPLED_TOKENS = {FULL_NAMES[2]: 48, FULL_NAMES[3]: 24, FULL_NAMES[4]: 8}
+# random tokens compared on the layers too large for the whole-layer oracle;
+# the three large layers add every token of the first and last tiles of
+# their heaviest, merged-remainder, swapped-remainder and one-row experts
+SAMPLED_TOKENS = {FULL_NAMES[2]: 256, FULL_NAMES[3]: 256, FULL_NAMES[4]: 256}
 SAMPLED_TOKENS.update({n: 16 for n in VARIANT_NAMES})
+TARGETED = set(FULL_NAMES[2:5])
 
 
 def _run(cfg, inp, ws=None):
@@ -60,7 +64,13 @@ def test_forward_parity(cuda_ok, name):
     else:
         rng = np.random.default_rng(3)
         cand = np.nonzero(~tie)[0]
-        toks = np.sort(rng.choice(cand, size=min(SAMPLED_TOKENS[name], cand.size), replace=False))
+        toks = rng.choice(cand, size=min(SAMPLED_TOKENS[name], cand.size), replace=False)
+        if name in TARGETED:
+            # tiles picked from the oracle's own dispatch of the layer
+            _, offsets, _, src = oracle_dispatch(name)
+            tt = targeted_tokens(offsets, src)
+            toks = np.concatenate([toks, tt[~tie[tt]]])
+        toks = np.unique(toks)
         ref = oracle.forward_tokens(cfg, host, toks)
         got = to_np(out[torch.from_numpy(toks).cuda()])
         if cfg.output_fp8:
@@ -69,7 +79,8 @@ def test_forward_parity(cuda_ok, name):
                                     ref["y_scale"], _gpu_codes(views, slots), name)
         else:
             assert_close(got, ref["out_rounded"], rel, mabs, name)
-    print(f"{name}: near-tie tokens excluded {int(tie.sum())}")
+    print(f"{name}: near-tie tokens excluded {int(tie.sum())}"
+          + ("" if name in ORACLE_FULL_OK else f", tokens compared {toks.size}"))
 
 
 @pytest.mark.parametrize("name", [SMALL_NAMES[0], SMALL_NAMES[6], FULL_NAMES[0], FULL_NAMES[1],
@@ -169,3 +180,32 @@ def test_forward_empty_batch(cuda_ok):
     torch.cuda.synchronize()
     v = moe.forward_views(cfg, ws)
     assert v["offsets"].tolist() == [0] * 5
+
+
+def _gatherable(cfg):
+    return cfg.dtype == "bf16" and not cfg.payload_fp8 and cfg.router != 3
+
+
+# every shape whose W1 GEMM can gather its rows from x (bf16, no FP8
+# payload, no soft gating), and both pair-tile widths on the shapes that
+# have swapped and merged remainders
+GATHER_CASES = [(n, 0) for n in SMALL_NAMES + FULL_NAMES + VARIANT_NAMES if _gatherable(ALL[n])]
+GATHER_CASES += [(n, w) for n in ("wide_tile_T300_d1024_E2_k2_f1600", "merged_tail_T270_d256_E2_k2_f320",
+                                  "merged_tail_T257_d128_E1_k1_f256", "ragged_T129_d256_E8_k2_f320",
+                                  "gate_E192_T300_d320_k4_f128") for w in (256, 512)]
+
+
+@pytest.mark.parametrize("name,width", GATHER_CASES)
+def test_gathered_rows_equal_packed_rows(cuda_ok, name, width):
+    # the W1 GEMM reading x through src sees the same bits the packed rows
+    # hold, in the same order: H, Y and the output are equal bit for bit
+    cfg, inp, _ = layer(name)
+    packed, ws_p = _run(cfg.with_(x_perm_mode=moe.MOE_XPERM_PACKED, gemm_tile_n=width), inp)
+    gathered, ws_g = _run(cfg.with_(x_perm_mode=moe.MOE_XPERM_GATHERED, gemm_tile_n=width), inp)
+    assert moe.get_device_error(ws_g) == moe.MOE_OK
+    assert torch.equal(packed, gathered)
+    vp = moe.forward_views(cfg.with_(x_perm_mode=moe.MOE_XPERM_PACKED), ws_p)
+    vg = moe.forward_views(cfg.with_(x_perm_mode=moe.MOE_XPERM_GATHERED), ws_g)
+    assert vg["x_perm"] is None and vp["x_perm"] is not None
+    for key in ("topk_idx", "counts", "offsets", "pos", "src", "h", "y_perm"):
+        assert torch.equal(vp[key], vg[key]), key

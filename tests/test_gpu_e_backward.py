@@ -3,8 +3,12 @@ the fp64 oracle's backward.
 
 Small layers (every router mode, fp32 and bf16, a single expert, experts
 with no rows, ragged batches) are compared element by element on every
-gradient; the 1024-token d=4096 E=8 layer on dx of sampled tokens. Both sides
-start from the same inputs and dout; the routing is checked equal first.
+gradient. Two full-size layers, the 1024-token d=4096 E=8 one and a
+2048-token copy of the 256-expert layer's shape (d=7168, f=2048, top-8 of 32
+Zipf-skewed experts), are compared in full on the gate's gradients (dW_g,
+db), on dW1 and dW2 of one expert of each GEMM tile form, and on dx of 256+
+tokens. Both sides start from the same inputs and dout; the routing is
+checked equal first.
 
 Tolerances, from the arithmetic: the GPU sums in fp32 (fp32 FMA on fp32
 layers; on bf16 layers fp32 accumulation on the tensor cores, with every
@@ -23,10 +27,10 @@ import torch
 import mixture_experts_routed_gb300 as moe
 import oracle
 from backward_shapes import SHAPES
+from gpu_layers import tile_class_experts
 from workloads import get_config, make_inputs
 
 pytestmark = pytest.mark.gpu
-
 
 
 def _dout(cfg, seed=5):
@@ -36,7 +40,8 @@ def _dout(cfg, seed=5):
     return t.to(torch.bfloat16 if cfg.dtype == "bf16" else torch.float32)
 
 
-def _run(cfg):
+def _run_dev(cfg):
+    """Forward then backward on the GPU; the gradients stay in device memory."""
     inp = make_inputs(cfg, device="cuda")
     ws = moe.alloc_workspace(cfg)
     moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
@@ -48,7 +53,16 @@ def _run(cfg):
     torch.cuda.synchronize()
     assert moe.get_device_error(bws) == moe.MOE_OK
     assert moe.get_device_error(ws) == moe.MOE_OK
-    return inp, ws, dout, {k: v.cpu().numpy().astype(np.float64) for k, v in g.items()}
+    return inp, ws, dout, g
+
+
+def _host(t):
+    return t.cpu().numpy().astype(np.float64)
+
+
+def _run(cfg):
+    inp, ws, dout, g = _run_dev(cfg)
+    return inp, ws, dout, {k: _host(v) for k, v in g.items()}
 
 
 def _close(got, ref, rel, name):
@@ -87,6 +101,37 @@ def test_backward_sampled_tokens_full_layer(cuda_ok):
         assert (counts[e] == 0) == (not np.any(g["dW1"][e]))
 
 
+FULL_BWD = ["balanced_T1024_d4096_E8_k2_f11008", "skewed_small_T2048_d7168_E32_k8_f2048_zipf"]
+
+
+@pytest.mark.parametrize("name", FULL_BWD)
+def test_backward_full_layer(cuda_ok, name):
+    cfg = get_config(name)
+    inp, ws, dout, g = _run_dev(cfg)
+    host = oracle.inputs_to_numpy(inp)
+    fwd = oracle.forward(cfg, host, keep_h=False)
+    views = moe.forward_views(cfg, ws)
+    assert np.array_equal(views["topk_idx"].cpu().numpy(), fwd["topk_idx"])
+    dout_h = dout.float().cpu().numpy()
+    # the gate's gradients over every token
+    r = oracle.backward_router(cfg, host, fwd, dout_h)
+    _close(_host(g["dWg"]), r["dWg"], 2e-3, f"{name} dWg")
+    _close(_host(g["dbias"]), r["dbias"], 2e-3, f"{name} dbias")
+    # whole weight gradients of one expert of each tile form, and the lightest
+    counts = np.diff(fwd["offsets"])
+    pick = set(tile_class_experts(fwd["offsets"]).values())
+    pick.add(int(np.argmin(np.where(counts > 0, counts, np.iinfo(np.int64).max))))
+    for e in sorted(pick):
+        pe = oracle.backward_expert(cfg, host, fwd, dout_h, e)
+        _close(_host(g["dW1"][e]), pe["dW1"], 2e-3, f"{name} dW1[{e}] ({counts[e]} rows)")
+        _close(_host(g["dW2"][e]), pe["dW2"], 2e-3, f"{name} dW2[{e}] ({counts[e]} rows)")
+    # dx of 256 random tokens
+    tokens = np.sort(np.random.default_rng(9).choice(cfg.T, 256, replace=False))
+    ref = oracle.backward_tokens(cfg, host, dout_h, tokens)
+    _close(_host(g["dx"][torch.from_numpy(tokens).cuda()]), ref["dx"], 2e-3, f"{name} dx")
+    print(f"{name}: experts compared {sorted(pick)}")
+
+
 def test_backward_is_bitwise_reproducible(cuda_ok):
     cfg = SHAPES["bwd_prek_T200_d256_E64_k2_f128"]
     _, _, _, g1 = _run(cfg)
@@ -103,3 +148,17 @@ def test_backward_rejects_fp8_payloads(cuda_ok):
     with pytest.raises(moe.MoEError):
         moe.backward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], _dout(cfg),
                      fwd_ws=ws, ws=bws)
+
+
+@pytest.mark.parametrize("name", ["bwd_bf16_T129_d256_E8_k2_f320", "bwd_skew_T256_d128_E64_k8_f128_zipf",
+                                  "bwd_ragged_T96_d192_E3_k2_f448"])
+def test_backward_after_gathered_forward(cuda_ok, name):
+    # a forward that gathers its rows leaves no packed rows behind: the
+    # backward packs them itself and gives the same gradients, bit for bit
+    base = SHAPES[name]
+    grads = []
+    for mode in (moe.MOE_XPERM_PACKED, moe.MOE_XPERM_GATHERED):
+        _, _, _, g = _run(base.with_(x_perm_mode=mode))
+        grads.append(g)
+    for n in grads[0]:
+        assert np.array_equal(grads[0][n], grads[1][n]), n
