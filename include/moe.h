@@ -358,6 +358,21 @@ MOE_API const char* moe_strerror(int status);
 /* Number of kernels one moe_forward call launches for cfg (0 if invalid). */
 MOE_API int moe_forward_kernel_count(const moe_config_t* cfg);
 
+/* ---- test hook: the bounded-wait path ---------------------------------------
+ * Every wait inside the library's kernels gives up after a bound (2 s by
+ * default: a wait that long means the GPU is not making progress), flags
+ * MOE_ERR_TIMEOUT in the workspace's error word and lets the kernel finish
+ * cleanly (copies and tensor-core work in flight are awaited, tensor memory
+ * is freed), so the context stays usable. This call sets, for launches made
+ * after it in this process, the bound of one of those waits in the grouped
+ * expert GEMM: its epilogue's wait for a finished accumulator, the one a
+ * test can make run out without a copy being left in flight (a tiny bound
+ * such as 1 ns does it). The GEMM then reports MOE_ERR_TIMEOUT, having taken
+ * up to the default bound to wind down. 0 restores the default. Not for use
+ * outside tests: the library itself never shortens a bound. Returns
+ * MOE_OK. */
+MOE_API int moe_set_gemm_epilogue_wait_ns(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

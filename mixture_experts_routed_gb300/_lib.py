@@ -71,6 +71,7 @@ PROTOTYPES = {
     "moe_clear_device_error": (_I, [_P, _P]),
     "moe_strerror": (ctypes.c_char_p, [_I]),
     "moe_forward_kernel_count": (_I, [_CFG]),
+    "moe_set_gemm_epilogue_wait_ns": (_I, [ctypes.c_uint64]),
     "moe_dispatch_noalloc": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_backward_workspace_size": (_SZ, [_CFG]),
     "moe_backward": (_I, [_CFG, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P, _P, _P, _P, _P, _P,

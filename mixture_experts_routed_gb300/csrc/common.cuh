@@ -151,6 +151,9 @@ cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, co
 // tile width), 256 or 512 (forced; the fp8 token rows always take 256).
 // gather_src non-null (epi 0, bf16, not a_shared): A is x [a_rows, K] and
 // routed row r reads x row gather_src[r] (no packed copy of the rows).
+// Bound of the grouped GEMM epilogue's wait for a finished accumulator in
+// later launches (0: the default kWaitLimitNs); a test hook.
+void set_gemm_epilogue_wait_ns(uint64_t ns);
 cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
                            const void* W, int E, int K, int N, const int32_t* offsets,
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,

@@ -58,6 +58,7 @@
 // copies (whole 128-byte row pieces per 8 lanes), wait for their own copies,
 // and release the stage like the FP8 converters do. TMA keeps the weight
 // boxes.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -93,6 +94,7 @@ struct TcParams {
   int a_shared;        // 1: output row r of expert e reads A row r - offsets[e]
   int k_wrap;          // BT: columns of the stored weight; k-block kb reads
                        // columns (64 kb) mod k_wrap (K = 2 k_wrap stacks it twice)
+  uint64_t epi_wait_ns;  // bound of the epilogue's wait for a finished accumulator
 };
 
 // SiLU'(z) = s (1 + z (1 - s)), s = sigmoid(z), with the approximate exp
@@ -688,7 +690,10 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
       const int tile = next_tile(true);
       if (tile >= total || timed_out) break;
       const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
-      const bool ok = mbar_wait_spin(&tfull[acc], aph, kWaitLimitNs);
+      // (a bound a test may shorten: once the epilogue gives up, the MMA and
+      // the producers stop within their own bounds with no copy armed on one
+      // CTA of the pair alone, and every drain below keeps the full bound)
+      const bool ok = mbar_wait_spin(&tfull[acc], aph, p.epi_wait_ns);
       if (!__all_sync(0xffffffffu, ok)) {
         timed_out = true;
         break;
@@ -938,11 +943,14 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
     // ------------------------------------------------------------ row gather (GA, both CTAs)
     // Thread g copies chunk g % 8 (16 bytes) of rows g / 8 + 16 j, j = 0..7,
     // of each stage's k-block: 8 lanes read one row's 128 contiguous bytes.
-    // Up to STAGES stages are in flight per thread; when the oldest has
-    // landed (the thread's own copies: cp.async.wait_group) its writes are
-    // made visible to the tensor cores (proxy fence) and the stage is
-    // released to the MMA: an arrive on full (even CTA), or a 16-byte bulk
-    // copy whose bytes complete the even CTA's full barrier (odd CTA).
+    // After issuing a stage, a thread with STAGES - 1 stages in flight waits
+    // for the oldest (its own copies: cp.async.wait_group), makes its writes
+    // visible to the tensor cores (proxy fence) and releases it to the MMA:
+    // an arrive on full (even CTA), or a 16-byte bulk copy whose bytes
+    // complete the even CTA's full barrier (odd CTA). The oldest stage is
+    // then released one k-block before the MMA needs it; releasing only
+    // with all STAGES in flight put the release behind the MMA's freeing of
+    // the next slot, a stall at every k-block (measured 1.7-2.1x slower).
     const int gidx = static_cast<int>(threadIdx.x) - 32 * (2 + NEW);
     const int ch = gidx & 7;
     const int rg = gidx >> 3;
@@ -951,9 +959,9 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
     const uint32_t leader_sink = mapa_shared(smem_u32(smem + S::OFF_SINK), 0);
     const uint32_t my_sink = smem_u32(smem + S::OFF_SINK);
     const __nv_bfloat16* gx = static_cast<const __nv_bfloat16*>(p.gx);
-    // a routed row's token; a bad one is flagged and read as token 0
-    auto token_row = [&](int r) -> const __nv_bfloat16* {
-      int tok = __ldg(p.gsrc + min(r, p.R - 1));
+    // a routed row's token (loaded with the others first); a bad one is
+    // flagged and read as token 0
+    auto token_row = [&](int tok) -> const __nv_bfloat16* {
       if (tok < 0 || tok >= p.gx_rows) {
         atomicOr(p.err, kErrBadIndex);
         tok = 0;
@@ -985,16 +993,20 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
       // feed only outputs the epilogue does not store
       const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
       const int r0 = t.row0 + static_cast<int>(rank) * half_rows;
+      // merged tile: this CTA's half of the remainder rows (8 or 16)
+      const int tail_half = MERGE ? ((t.tail + 15) & ~15) / 2 : 0;
+      int tok[9];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        tok[j] = rg + 16 * j < half_rows ? __ldg(p.gsrc + min(r0 + rg + 16 * j, p.R - 1)) : 0;
+      tok[8] = rg < tail_half
+                   ? __ldg(p.gsrc + min(t.row0 + pairk::BM + static_cast<int>(rank) * tail_half + rg,
+                                        p.R - 1))
+                   : 0;
       const __nv_bfloat16* rowp[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) rowp[j] = rg + 16 * j < half_rows ? token_row(r0 + rg + 16 * j) : nullptr;
-      // merged tile: this CTA's half of the remainder rows (8 or 16)
-      const __nv_bfloat16* tailp = nullptr;
-      if constexpr (MERGE) {
-        const int tail_half = ((t.tail + 15) & ~15) / 2;
-        if (rg < tail_half)
-          tailp = token_row(t.row0 + pairk::BM + static_cast<int>(rank) * tail_half + rg);
-      }
+      for (int j = 0; j < 8; ++j) rowp[j] = rg + 16 * j < half_rows ? token_row(tok[j]) : nullptr;
+      const __nv_bfloat16* tailp = rg < tail_half ? token_row(tok[8]) : nullptr;
       for (int kb = 0; kb < KB; ++kb) {
         bool got = true;
         if (lane == 0) got = mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs);
@@ -1018,8 +1030,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
           s = 0;
           ph ^= 1u;
         }
-        if (inflight == S::STAGES) {
-          cp_async_wait<S::STAGES - 1>();
+        if (inflight == S::STAGES - 1) {
+          cp_async_wait<S::STAGES - 2>();
           release_oldest();
         }
       }
@@ -1129,6 +1141,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
 // ---------------------------------------------------------------- host side
 // Tensor maps (declared in tmap.cuh; the weight-gradient GEMM uses them too).
 namespace {
+std::atomic<uint64_t> g_epi_wait_ns{kWaitLimitNs};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -1273,6 +1286,8 @@ int pick_nb(int epi, int R, int E, int K, int N, int num_sms) {
 
 }  // namespace
 
+void set_gemm_epilogue_wait_ns(uint64_t ns) { g_epi_wait_ns.store(ns == 0 ? kWaitLimitNs : ns); }
+
 cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
                            const void* W, int E, int K, int N, const int32_t* offsets,
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
@@ -1326,6 +1341,7 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
   prm.a_rows = a_rows;
   prm.a_shared = a_shared;
   prm.k_wrap = K;
+  prm.epi_wait_ns = g_epi_wait_ns.load();
   // tile_n 256 or 512 forces the pair-tile width; 0 takes the built-in choice
   const int nb = tile_n == 0 ? pick_nb(epi, R, E, K, N, num_sms) : tile_n / 256;
   if (a_fp8) return launch_pair<0, 1, true>(mA, mA8, mB, mY, prm, num_sms, s);
@@ -1376,6 +1392,7 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   prm.a_rows = R;
   prm.a_shared = 0;
   prm.k_wrap = k_wrap;
+  prm.epi_wait_ns = g_epi_wait_ns.load();
   return zin ? launch_pair<2, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s)
              : launch_pair<1, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s);
 }

@@ -495,6 +495,11 @@ extern "C" {
 
 int moe_check_config(const moe_config_t* cfg) { return check_cfg(cfg); }
 
+int moe_set_gemm_epilogue_wait_ns(uint64_t ns) {
+  set_gemm_epilogue_wait_ns(ns);
+  return MOE_OK;
+}
+
 size_t moe_scratch_size(const moe_config_t* cfg) {
   if (check_cfg(cfg) != MOE_OK) return 0;
   return layout_of(*cfg).scratch_end;
