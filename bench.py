@@ -57,6 +57,10 @@ def parse():
                    help="CPU oracle baseline: run 16-token chunks until this much time has passed")
     p.add_argument("--backward", action="store_true",
                    help="also time moe_backward (adds a 'backward' object to the line)")
+    p.add_argument("--x-perm-mode", type=int, default=None, choices=[0, 1, 2],
+                   help="0 the library's choice, 1 packed rows, 2 rows gathered by the W1 GEMM")
+    p.add_argument("--gemm-tile-n", type=int, default=None, choices=[0, 256, 512],
+                   help="expert GEMM pair-tile width (0: the library's choice)")
     return p.parse_args()
 
 
@@ -283,6 +287,7 @@ def workload_config(cfg, args):
             "router": router[cfg.router], "pre_k": cfg.pre_k,
             "payload": payload[int(cfg.payload_fp8)],
             "x_perm_mode": {0: "library's choice", 1: "packed", 2: "gathered"}[cfg.x_perm_mode],
+            "gemm_tile_n": cfg.gemm_tile_n or "library's choice",
             "expert_output": ("fp8_e4m3 (per-row min/max affine)" if cfg.output_fp8
                               else "fp32"), "seed": cfg.seed,
             "parallelism": f"replicas x{args.gpus}",
@@ -547,6 +552,10 @@ def main():
     args = parse()
     from workloads import get_config, BENCH_CONFIG
     cfg = get_config(args.config or BENCH_CONFIG)
+    if args.x_perm_mode is not None:
+        cfg = cfg.with_(x_perm_mode=args.x_perm_mode)
+    if args.gemm_tile_n is not None:
+        cfg = cfg.with_(gemm_tile_n=args.gemm_tile_n)
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_ours(args, cfg)

@@ -134,7 +134,9 @@ typedef struct moe_config {
 } moe_config_t;
 
 enum {
-  MOE_XPERM_AUTO = 0,     /* the library's choice */
+  MOE_XPERM_AUTO = 0,     /* the library's choice: gathered where it can be and
+                           * the packed rows (T k d bf16 values) would take
+                           * 256 MiB or more, else packed */
   MOE_XPERM_PACKED = 1,   /* the dispatch writes x_perm */
   MOE_XPERM_GATHERED = 2  /* the W1 GEMM reads x[src[r]]; no x_perm */
 };

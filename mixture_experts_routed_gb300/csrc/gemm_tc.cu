@@ -468,9 +468,38 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
       const uint32_t peer_tq_full = mapa_shared(smem_u32(tq_full), 1);
       // unsigned: any counter value maps to a valid tile or to the end
       uint32_t claimed = rank == 0 ? atomicAdd(p.tile_ctr, 1u) : 0u;
+      // GA: the even CTA posts each tile one ahead of the one it loads, so
+      // the gather warps can fetch the next tile's row tokens while they
+      // copy the current one (the post: both CTAs' queue copies, then the
+      // end marker once the tiles run out; a timeout posts the end)
+      auto post = [&](int tile) -> int {
+        if (!mbar_wait_cluster(&tq_empty[q_slot], q_ph ^ 1u, kWaitLimitNs)) {
+          timed_out = true;
+          tile = total;
+        }
+        tq[q_slot] = tile;
+        st_shared_cluster_s32(peer_tq + static_cast<uint32_t>(q_slot * 4), tile);
+        mbar_arrive(&tq_full[q_slot]);
+        mbar_arrive_remote(peer_tq_full + static_cast<uint32_t>(q_slot * 8));
+        if (++q_slot == S::TQ) {
+          q_slot = 0;
+          q_ph ^= 1u;
+        }
+        return tile;
+      };
+      auto claim = [&]() -> int {
+        const uint32_t c = atomicAdd(p.tile_ctr, 1u);
+        return c < static_cast<uint32_t>(total) ? static_cast<int>(c) : total;
+      };
+      int ahead = -1;  // GA: the tile posted but not yet loaded
       for (;;) {
         int tile;
-        if (rank == 0) {
+        if (GA && rank == 0) {
+          if (ahead < 0)
+            ahead = post(claimed < static_cast<uint32_t>(total) ? static_cast<int>(claimed) : total);
+          tile = ahead;
+          if (tile < total && !timed_out) ahead = post(claim());
+        } else if (rank == 0) {
           tile = claimed < static_cast<uint32_t>(total) ? static_cast<int>(claimed) : total;
           if (!mbar_wait_cluster(&tq_empty[q_slot], q_ph ^ 1u, kWaitLimitNs)) {
             timed_out = true;
@@ -958,15 +987,16 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
     const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
     const uint32_t leader_sink = mapa_shared(smem_u32(smem + S::OFF_SINK), 0);
     const uint32_t my_sink = smem_u32(smem + S::OFF_SINK);
-    const __nv_bfloat16* gx = static_cast<const __nv_bfloat16*>(p.gx);
-    // a routed row's token (loaded with the others first); a bad one is
+    const uint4* xv = static_cast<const uint4*>(p.gx);
+    // offset (in 16-byte units) of this thread's piece of a routed row's
+    // token row (the tokens are loaded together first); a bad token is
     // flagged and read as token 0
-    auto token_row = [&](int tok) -> const __nv_bfloat16* {
+    auto token_piece = [&](int tok) -> uint32_t {
       if (tok < 0 || tok >= p.gx_rows) {
         atomicOr(p.err, kErrBadIndex);
         tok = 0;
       }
-      return gx + static_cast<size_t>(tok) * p.K + ch * 8;
+      return static_cast<uint32_t>(tok) * static_cast<uint32_t>(p.K / 8) + static_cast<uint32_t>(ch);
     };
     int s = 0, so = 0, inflight = 0;
     uint32_t ph = 0;
@@ -984,29 +1014,52 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
       if (++so == S::STAGES) so = 0;
       --inflight;
     };
+    // this CTA's rows of a tile: 128 of a full tile, its half of a swapped
+    // tile's tokens (rounded to 16); rows past the segment read a valid row
+    // and feed only outputs the epilogue does not store; a merged tile adds
+    // this CTA's half of the remainder rows (8 or 16)
+    auto tile_rows = [&](const pairk::PTile& t, int& half_rows, int& tail_half) {
+      half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
+      tail_half = MERGE ? ((t.tail + 15) & ~15) / 2 : 0;
+    };
+    // the tokens of this thread's rows (rows rg + 16 j, and remainder row rg)
+    auto load_tokens = [&](const pairk::PTile& t, int (&tk)[9]) {
+      int half_rows, tail_half;
+      tile_rows(t, half_rows, tail_half);
+      const int r0 = t.row0 + static_cast<int>(rank) * half_rows;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        tk[j] = rg + 16 * j < half_rows ? __ldg(p.gsrc + min(r0 + rg + 16 * j, p.R - 1)) : 0;
+      tk[8] = rg < tail_half
+                  ? __ldg(p.gsrc + min(t.row0 + pairk::BM + static_cast<int>(rank) * tail_half + rg,
+                                       p.R - 1))
+                  : 0;
+    };
+    int next_known = -1;  // the next tile, read ahead from the queue
+    int next_tok[9];
     for (;;) {
       const int tile = next_tile(true);
       if (tile >= total || timed_out) break;
       const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
-      // this CTA's rows: 128 of a full tile, its half of a swapped tile's
-      // tokens (rounded to 16); rows past the segment read a valid row and
-      // feed only outputs the epilogue does not store
-      const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
-      const int r0 = t.row0 + static_cast<int>(rank) * half_rows;
-      // merged tile: this CTA's half of the remainder rows (8 or 16)
-      const int tail_half = MERGE ? ((t.tail + 15) & ~15) / 2 : 0;
+      int half_rows, tail_half;
+      tile_rows(t, half_rows, tail_half);
       int tok[9];
+      if (tile == next_known) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        tok[j] = rg + 16 * j < half_rows ? __ldg(p.gsrc + min(r0 + rg + 16 * j, p.R - 1)) : 0;
-      tok[8] = rg < tail_half
-                   ? __ldg(p.gsrc + min(t.row0 + pairk::BM + static_cast<int>(rank) * tail_half + rg,
-                                        p.R - 1))
-                   : 0;
-      const __nv_bfloat16* rowp[8];
+        for (int j = 0; j < 9; ++j) tok[j] = next_tok[j];
+      } else {
+        load_tokens(t, tok);
+      }
+      next_known = -1;
+      // row pieces: rows rg + 16 j (j < nj: the rows this CTA stages) and,
+      // in a merged tile, remainder row rg
+      uint32_t off[8];
+      const int nj = min(8, max(0, (half_rows - rg + 15) / 16));
 #pragma unroll
-      for (int j = 0; j < 8; ++j) rowp[j] = rg + 16 * j < half_rows ? token_row(tok[j]) : nullptr;
-      const __nv_bfloat16* tailp = rg < tail_half ? token_row(tok[8]) : nullptr;
+      for (int j = 0; j < 8; ++j) off[j] = j < nj ? token_piece(tok[j]) : 0u;
+      const bool has_tail = rg < tail_half;
+      const uint32_t toff = has_tail ? token_piece(tok[8]) : 0u;
+      constexpr uint32_t KSTEP = pairk::BK / 8;  // a k-block in 16-byte units
       for (int kb = 0; kb < KB; ++kb) {
         bool got = true;
         if (lane == 0) got = mbar_wait_spin(&empty[s], ph ^ 1u, kWaitLimitNs);
@@ -1017,12 +1070,12 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
         const uint32_t dst = smem_u32(sA + s * pairk::A_BYTES) + swz;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (rowp[j] != nullptr)
-            cp_async16(dst + static_cast<uint32_t>((rg + 16 * j) * 128), rowp[j] + kb * pairk::BK);
+          if (j < nj)
+            cp_async16(dst + static_cast<uint32_t>((rg + 16 * j) * 128), xv + off[j] + kb * KSTEP);
         if constexpr (MERGE) {
-          if (tailp != nullptr)
+          if (has_tail)
             cp_async16(smem_u32(sT + s * S::T_BYTES) + static_cast<uint32_t>(rg * 128) + swz,
-                       tailp + kb * pairk::BK);
+                       xv + toff + kb * KSTEP);
         }
         cp_async_commit();
         ++inflight;
@@ -1033,6 +1086,20 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
         if (inflight == S::STAGES - 1) {
           cp_async_wait<S::STAGES - 2>();
           release_oldest();
+        }
+        if (kb == 0) {
+          // the next tile is already in the queue (posted one ahead): fetch
+          // its row tokens now, while this tile's rows are copied
+          // (every lane acquires the slot, as next_tile does)
+          const bool got_next = mbar_wait_cluster(&tq_full[q_slot], q_ph, kWaitLimitNs);
+          if (__all_sync(0xffffffffu, got_next)) {
+            const int nt = tq[q_slot];
+            if (nt < total) {
+              load_tokens(pairk::decode(nt, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE),
+                          next_tok);
+              next_known = nt;
+            }
+          }
         }
       }
       if (!ok) break;
