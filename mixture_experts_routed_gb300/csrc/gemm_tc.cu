@@ -90,6 +90,8 @@ struct TcParams {
   uint32_t* tile_ctr;  // next tile to hand out; zero before the launch
   int E, K, N, R, n_tiles;
   int n_tiles_m;       // feature blocks of a merged tile (ceil(N / 224))
+  int group;           // token tiles of one expert that run over all its
+                       // feature blocks before the next ones (>= 1)
   int a_rows;          // rows of A
   int a_shared;        // 1: output row r of expert e reads A row r - offsets[e]
   int k_wrap;          // BT: columns of the stored weight; k-block kb reads
@@ -269,10 +271,27 @@ __device__ __forceinline__ int expert_tiles(int rows, int n_tiles, int n_tiles_m
 // remainder (1..255 rows), one swapped tile whose MMA N is the remainder
 // rounded up to 16, so a short tail costs a fraction of a full tile; or, for
 // a remainder of at most TAIL_MAX rows, merged tiles (see MT_W) in place of
-// the last full tile and the swapped one. Token tiles of one weight tile are
-// adjacent in the order.
+// the last full tile and the swapped one.
+// Order: the expert's token tiles go in groups of `group`; a group runs over
+// every weight tile (feature block), weight tile by weight tile, before the
+// next group starts, and the group's token tiles of one weight tile are
+// adjacent. Pairs running side by side then share each weight tile, and a
+// group's token rows and weight tiles stay in L2 while it runs: with one
+// group per expert (the plain weight-tile-major order) a heavy expert's
+// token rows left L2 between its weight tiles and were read again from
+// DRAM for each of them.
+__device__ __forceinline__ void order(int local, int mt, int n_tiles, int group, int& nt, int& m) {
+  const int g = local / (group * n_tiles);
+  const int base = g * group;
+  const int gm = min(group, mt - base);  // token tiles in this group
+  const int idx = local - base * n_tiles;
+  nt = idx / gm;
+  m = base + (idx - nt * gm);
+}
+
 __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* seg, int E,
-                                        int n_tiles, int bn, int n_tiles_m, bool merge) {
+                                        int n_tiles, int bn, int n_tiles_m, bool merge,
+                                        int group) {
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -299,7 +318,8 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
       t.tail = rem;
       return t;
     }
-    const int nt = local / (full - 1), m = local - nt * (full - 1);
+    int nt, m;
+    order(local, full - 1, n_tiles, group, nt, m);
     t.row0 = seg[lo] + m * BM;
     t.swap = false;
     t.ntok = BM;
@@ -307,7 +327,8 @@ __device__ __forceinline__ PTile decode(int tile, const int* tstart, const int* 
     return t;
   }
   const int mt = full + (rem > 0 ? 1 : 0);
-  const int nt = local / mt, m = local - nt * mt;
+  int nt, m;
+  order(local, mt, n_tiles, group, nt, m);
   t.row0 = seg[lo] + m * BM;
   t.swap = m == full;
   t.ntok = t.swap ? rem : BM;
@@ -518,7 +539,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
           tile = next_tile(false);
         }
         if (tile >= total || timed_out) break;
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE, p.group);
         // normal tile: this CTA's 128 rows; swapped tile: its half of the N tokens
         const int half_rows = t.swap ? ((t.ntok + 15) & ~15) / 2 : 128;
         const int a_base = p.a_shared ? seg[t.e] : 0;
@@ -622,7 +643,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
-        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
+        const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE, p.group);
         // MMAs with any feature below N (the rest of a last tile is skipped)
         const int nmma = min(NB, (p.N - t.n0 + 255) / 256);
         // swapped tile: A = weights (the B slot), B = tokens (K-major, the A slot)
@@ -718,7 +739,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
     for (;;) {
       const int tile = next_tile(true);
       if (tile >= total || timed_out) break;
-      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE, p.group);
       // (a bound a test may shorten: once the epilogue gives up, the MMA and
       // the producers stop within their own bounds with no copy armed on one
       // CTA of the pair alone, and every drain below keeps the full bound)
@@ -1040,7 +1061,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
     for (;;) {
       const int tile = next_tile(true);
       if (tile >= total || timed_out) break;
-      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE);
+      const pairk::PTile t = pairk::decode(tile, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE, p.group);
       int half_rows, tail_half;
       tile_rows(t, half_rows, tail_half);
       int tok[9];
@@ -1095,7 +1116,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
           if (__all_sync(0xffffffffu, got_next)) {
             const int nt = tq[q_slot];
             if (nt < total) {
-              load_tokens(pairk::decode(nt, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE),
+              load_tokens(pairk::decode(nt, tstart, seg, E, p.n_tiles, S::BN, p.n_tiles_m, MERGE, p.group),
                           next_tok);
               next_known = nt;
             }
@@ -1337,6 +1358,9 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
   // together (a pair needs two free SMs of one GPC), not num_sms / 2
   const int resident = resident_pairs<EPI, NB, A8, BT, GA>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
+  // token tiles per group: about one wave of pairs over the expert's weight
+  // tiles
+  prm.group = resident / prm.n_tiles > 1 ? resident / prm.n_tiles : 1;
   lc.gridDim = dim3(2 * pairs);
   return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8, BT, GA>, mA, mA8, mB, mY, prm);
 }
