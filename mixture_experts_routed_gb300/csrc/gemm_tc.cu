@@ -276,10 +276,10 @@ __device__ __forceinline__ int expert_tiles(int rows, int n_tiles, int n_tiles_m
 // every weight tile (feature block), weight tile by weight tile, before the
 // next group starts, and the group's token tiles of one weight tile are
 // adjacent. Pairs running side by side then share each weight tile, and a
-// group's token rows and weight tiles stay in L2 while it runs: with one
-// group per expert (the plain weight-tile-major order) a heavy expert's
-// token rows left L2 between its weight tiles and were read again from
-// DRAM for each of them.
+// group's token rows stay in L2 while its weight tiles stream past: with
+// one group per expert (the plain weight-tile-major order) a heavy
+// expert's token rows left L2 between its weight tiles and were read again
+// from DRAM for each of them.
 __device__ __forceinline__ void order(int local, int mt, int n_tiles, int group, int& nt, int& m) {
   const int g = local / (group * n_tiles);
   const int base = g * group;
@@ -1358,9 +1358,13 @@ cudaError_t launch_pair(const CUtensorMap& mA, const CUtensorMap& mA8, const CUt
   // together (a pair needs two free SMs of one GPC), not num_sms / 2
   const int resident = resident_pairs<EPI, NB, A8, BT, GA>(lc, num_sms);
   const int pairs = static_cast<int>(max_pt < resident ? max_pt : resident);
-  // token tiles per group: about one wave of pairs over the expert's weight
-  // tiles
-  prm.group = resident / prm.n_tiles > 1 ? resident / prm.n_tiles : 1;
+  // token tiles per group: as many as keep the group's token rows (256 rows
+  // of K bf16 each) within ~48 MB of the 126 MB L2 while its weight tiles
+  // stream past (an expert with fewer token tiles runs in one group, the
+  // plain weight-tile-major order)
+  const long long tile_bytes = static_cast<long long>(pairk::BM) * prm.K * 2;
+  const long long g = (48LL << 20) / (tile_bytes > 0 ? tile_bytes : 1);
+  prm.group = g < 1 ? 1 : (g > (1 << 20) ? (1 << 20) : static_cast<int>(g));
   lc.gridDim = dim3(2 * pairs);
   return cudaLaunchKernelEx(&lc, gemm_pair_kernel<EPI, NB, A8, BT, GA>, mA, mA8, mB, mY, prm);
 }
