@@ -109,16 +109,19 @@ def source_sha(path):
     return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel_file, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of the kernel; else None."""
+def ncu_traffic(workload_stage):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current source of the kernel (the entry names its file and hash);
+    else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        d = json.load(open(path))
-        ent = d.get(workload, {}).get(os.path.basename(kernel_file))
-        if ent and ent.get("source_sha") == source_sha(kernel_file):
+        ent = json.load(open(path)).get(workload_stage)
+        if not ent:
+            return None
+        src = os.path.join(ROOT, "mixture_experts_routed_gb300", "csrc", ent["file"])
+        if os.path.exists(src) and ent.get("source_sha") == source_sha(src):
             return ent.get("dram_bytes_per_launch")
     except Exception:
         return None
@@ -393,12 +396,7 @@ def run_ours(args, cfg):
     by, fl = work[dom]
     is_tensor = dom.startswith("gemm") and cfg.dtype == "bf16" and \
         fl / (peaks["bf16_tflops"] * 1e12) > by / (peaks["hbm_gbs"] * 1e9)
-    kfile = os.path.join(ROOT, "mixture_experts_routed_gb300", "csrc",
-                         "gemm_tc.cu" if dom.startswith("gemm") else
-                         {"route": "route.cu", "dispatch": "dispatch.cu",
-                          "combine": "payload_out.cu" if getattr(cfg, "output_fp8", 0)
-                          else "combine.cu", "quantize_out": "payload_out.cu"}[dom])
-    traffic = ncu_traffic(kfile, f"{cfg.name}:{dom}")
+    traffic = ncu_traffic(f"{cfg.name}:{dom}")
     if is_tensor:
         roof = {"bound": "tensor", "achieved": kd["TFLOP_s"], "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": kd["TFLOP_s"] / peaks["bf16_tflops"],
