@@ -562,7 +562,12 @@ def run_ours(args, cfg):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-            "config": workload_config(cfg, args), "roofline": roof, "cpu_baseline": cpu,
+            "config": dict(workload_config(cfg, args),
+                           rows=("x itself, read by every expert (soft gating)"
+                                 if cfg.router == 3 else
+                                 "gathered by the W1 GEMM from x (no packed copy)" if gathered
+                                 else "packed by the dispatch")),
+            "roofline": roof, "cpu_baseline": cpu,
             "e2e": e2e, "gpu_launches": moe.kernel_count(cfg) * K, "clocks": clk,
             "kernel_times": "CUDA events at every kernel boundary, in a second pass of K steps "
                             "after the timed one (events between kernels would stop their "
