@@ -165,9 +165,11 @@ def test_forward_events_bracket_kernels(cuda_ok):
     assert ms[3] > 0 and ms[4] > 0      # the two GEMMs
 
 
-def test_forward_empty_batch(cuda_ok):
+@pytest.mark.parametrize("mode", [moe.MOE_XPERM_PACKED, moe.MOE_XPERM_GATHERED])
+def test_forward_empty_batch(cuda_ok, mode):
     from workloads import MoEConfig
-    cfg = MoEConfig("empty", T=0, d=128, E=4, k=2, f=128, dtype="bf16", pre_k=4)
+    cfg = MoEConfig("empty", T=0, d=128, E=4, k=2, f=128, dtype="bf16", pre_k=4,
+                    x_perm_mode=mode)
     ws = moe.alloc_workspace(cfg)
     x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
     Wg = torch.zeros((128, 4), dtype=torch.bfloat16, device="cuda")
@@ -178,6 +180,7 @@ def test_forward_empty_batch(cuda_ok):
     dummy = torch.empty(16, dtype=torch.bfloat16, device="cuda")
     moe.forward(cfg, dummy, Wg, None, W1, W2, ws=ws, out=dummy)
     torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == moe.MOE_OK
     v = moe.forward_views(cfg, ws)
     assert v["offsets"].tolist() == [0] * 5
 
