@@ -98,3 +98,88 @@ def test_dispatch_empty_batch(cuda_ok):
     d = moe.dispatch(cfg, x, idx, ws=ws, counts=counts, offsets=offsets)
     assert to_np(d["counts"]).tolist() == [0] * 4
     assert to_np(d["offsets"]).tolist() == [0] * 5
+
+
+def _fp8_edge_rows(T, d, static_scale, seed):
+    """bf16 rows whose quotients x / s sit where E4M3 rounding is delicate.
+    Candidates are every positive bf16 value below the row's absmax (or
+    below 1000 s with a static scale, so that some saturate); each row holds
+    every candidate where x times the rounded reciprocal of s gives another
+    E4M3 code than the IEEE quotient, up to 160 within 8 fp32 steps of a
+    rounding midpoint, 40 in E4M3's subnormal range, two zeros and ordinary
+    values, with random signs. A per-token row starts with its absmax, which
+    fixes s = fp32(amax / 448); its absmax is the best of 8 draws for the
+    number of such disagreements."""
+    from oracle.numerics import e4m3_round_satfinite
+    rng = np.random.default_rng(seed)
+    pos_bf16 = (np.arange(1, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    pool = pos_bf16[(pos_bf16 > 1e-3) & (pos_bf16 < 1e3)]
+
+    def classify(cand, s):
+        y = (cand * np.float32(np.float32(1.0) / s)).astype(np.float32)
+        q = (cand / s).astype(np.float32)
+        wrong = e4m3_round_satfinite(y.astype(np.float64)) != e4m3_round_satfinite(q.astype(np.float64))
+        low = (y.view(np.uint32) & 0xFFFFF).astype(np.int64)
+        tiny = np.abs(q) < 2.0 ** -6
+        near = (np.abs(low - 0x80000) <= 8) & ~tiny
+        return wrong, near, tiny
+
+    rows = np.zeros((T, d), np.float32)
+    for t in range(T):
+        if static_scale is None:
+            best = None
+            for amax in rng.choice(pool, 8):
+                amax = np.float32(amax)
+                s = np.float32(amax / np.float32(448.0))
+                cand = pos_bf16[pos_bf16 <= amax]
+                cls = classify(cand, s)
+                if best is None or cls[0].sum() > best[3][0].sum():
+                    best = (amax, s, cand, cls)
+            amax, s, cand, (wrong, near, tiny) = best
+        else:
+            amax, s = None, np.float32(static_scale)
+            cand = pos_bf16[pos_bf16 < np.float32(1000.0) * s]
+            wrong, near, tiny = classify(cand, s)
+        parts = [cand[wrong][:120]]
+        for mask, n in ((near & ~wrong, 160), (tiny & ~wrong, 40)):
+            c = cand[mask]
+            parts.append(rng.choice(c, size=min(n, c.size), replace=False) if c.size else c)
+        chosen = np.concatenate(parts)[: d - 3]
+        row = rng.choice(cand[~tiny], size=d).astype(np.float32)
+        row[3:3 + chosen.size] = chosen
+        row[1:3] = 0.0
+        row *= np.where(rng.random(d) < 0.5, -1.0, 1.0).astype(np.float32)
+        if amax is not None:
+            row[0] = amax
+        rows[t] = row
+    return rows
+
+
+# static scales 7 * 2^-9 and 13 * 2^-10: bf16 values exist whose product with
+# 1/s takes another code than the quotient (30 and 1 of them)
+@pytest.mark.parametrize("static_scale", [None, 0.013671875, 0.0126953125])
+def test_dispatch_fp8_payload_rounding_edges(cuda_ok, static_scale):
+    # the payload bytes are those of the IEEE fp32 quotient on rows built
+    # around the cases a shortcut (x times 1/s) would get wrong: E4M3
+    # rounding midpoints, E4M3 subnormals, saturation
+    from workloads import MoEConfig
+    T, d, E, k = 96, 512, 4, 2
+    mode = True if static_scale is None else 2
+    cfg = MoEConfig("fp8_edges", T=T, d=d, E=E, k=k, f=128, dtype="bf16", pre_k=4,
+                    payload_fp8=mode, payload_scale=static_scale or 0.0)
+    rows = _fp8_edge_rows(T, d, static_scale, seed=11 if static_scale is None else 12)
+    x = torch.from_numpy(rows).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.from_numpy(rows))      # the rows are bf16 values
+    idx = np.stack([np.arange(T) % E, (np.arange(T) + 1 + np.arange(T) // E) % E], 1)
+    idx[idx[:, 0] == idx[:, 1], 1] = (idx[idx[:, 0] == idx[:, 1], 1] + 1) % E
+    ws = moe.alloc_workspace(cfg, kind="scratch")
+    dd = moe.dispatch(cfg, x.cuda(), torch.from_numpy(idx.astype(np.int32)).cuda(), ws=ws)
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == moe.MOE_OK
+    _, _, _, src = oracle.dispatch(idx, E)
+    q, s = oracle.quantize_payload_fp8(rows.astype(np.float64), static_scale)
+    ref = oracle.e4m3_encode(q[src])
+    got = to_np(dd["x_perm"])
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} payload bytes differ"
+    got_s = to_np(dd["x_scale"]).astype(np.float32)
+    assert np.array_equal(got_s.view(np.uint32), s[src].astype(np.float32).view(np.uint32))
