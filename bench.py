@@ -130,20 +130,24 @@ def ncu_traffic(workload_stage):
 
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi every 100 ms, each sample time-stamped; the summary keeps
+    the samples inside the window the caller marks (the GPU-busy steps)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -153,6 +157,29 @@ class ClockSampler:
     def _read(self):
         for ln in self.proc.stdout:
             self.lines.append(ln.strip())
+
+    def mark(self, t0, t1):
+        """The busy window, host wall-clock datetimes."""
+        self.window = (t0, t1)
+
+    @staticmethod
+    def _summary(rows):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for parts in rows:
+            try:
+                sm.append(float(parts[2]))
+                mx = float(parts[3])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
 
     def stop(self):
         if self.proc is None:
@@ -164,25 +191,30 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.t.join(timeout=2)
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        rows, inside = [], []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return None
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            rows.append(parts)
+            if self.window is not None:
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                except ValueError:
+                    continue
+                if self.window[0] <= ts <= self.window[1]:
+                    inside.append(parts)
+        out = self._summary(inside)
+        if out is not None:
+            out["window"] = "samples taken while the timed steps and the per-kernel pass ran"
+            out["window_ms"] = round((self.window[1] - self.window[0]).total_seconds() * 1e3, 1)
+            return out
+        out = self._summary(rows)
+        if out is not None:
+            out["window"] = ("no sample fell inside the busy window; every sample of the run "
+                             "(before, during and after the timed steps)")
+        return out
 
 
 # ---------------------------------------------------------------- CPU oracle timing
@@ -351,6 +383,8 @@ def run_ours(args, cfg):
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    import datetime
+    busy_from = datetime.datetime.now()
     t_start.record(stream)
     for i in range(K):
         step()
@@ -362,6 +396,7 @@ def run_ours(args, cfg):
     for i in range(K):
         step(evs[i])
     torch.cuda.synchronize(dev)
+    clocks.mark(busy_from, datetime.datetime.now())
     clk = clocks.stop() if rank == 0 else None
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     if moe.get_device_error(ws) != moe.MOE_OK:
@@ -390,7 +425,9 @@ def run_ours(args, cfg):
         kernels[name] = {"us": stage_ms[name] * 1e3, "bytes": by, "flops": fl, "GB_s": gbs,
                          "TFLOP_s": tfl, "hbm_frac": gbs / peaks["hbm_gbs"],
                          "tensor_frac": (tfl / peaks["bf16_tflops"]) if name.startswith("gemm")
-                         else None}
+                         else None,
+                         "tensor_frac_sustained": (tfl / peaks["bf16_tflops_sustained"])
+                         if name.startswith("gemm") else None}
     dom = max(kernels, key=lambda n: kernels[n]["us"])
     kd = kernels[dom]
     by, fl = work[dom]
