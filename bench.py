@@ -567,11 +567,12 @@ def run_ours(args, cfg):
             note = "achieved = every GEMM's fp32 FMA work over the whole backward time"
         else:
             # the method's own work: Z recomputed and four expert GEMMs, 2Rdf
-            # each. The tensor cores execute more: each of the four GEMMs with
-            # an fp32 operand (dY or dZ) runs on its bf16 split hi + lo, which
-            # doubles it (18Rdf executed)
+            # each. The tensor cores execute more: each of the three GEMMs with
+            # an fp32 operand (dY for dW2, dZ for dX_perm and dW1) runs on its
+            # bf16 split hi + lo, which doubles it; dH reads the bf16 dout rows
+            # with the routing weight applied after the sum (16Rdf executed)
             algo = 10.0 * R * cfg.d * cfg.f
-            executed = 18.0 * R * cfg.d * cfg.f
+            executed = 16.0 * R * cfg.d * cfg.f
             t_s = b_ms / 1e3
             broof = {"bound": "tensor", "achieved": algo / t_s / 1e12,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -582,8 +583,8 @@ def run_ours(args, cfg):
                     "executed_frac": executed / t_s / 1e12 / peaks["bf16_tflops"]}
             note = ("achieved = the method's expert-GEMM flops (10 R d f: Z recomputed, dH, "
                     "dX_perm, dW1, dW2) over the whole backward time; executed_* count the "
-                    "tensor-core flops actually run (the hi/lo operand split doubles four "
-                    "GEMMs: 18 R d f); the gate's fp32 FMA work is simt_flops")
+                    "tensor-core flops actually run (the hi/lo operand split doubles three "
+                    "GEMMs: 16 R d f); the gate's fp32 FMA work is simt_flops")
         bwd = {"ms_per_step": b_ms, "tokens_per_s": cfg.T * world / (b_ms / 1e3),
                "roofline": broof, "simt_flops": gate if cfg.dtype != "f32" else None,
                "note": note}

@@ -3,7 +3,9 @@
 // activated experts; Deepseek-MoE sync-tax article, section 2.4: the backward
 // exchange mirrors the dispatch). Given dout = dl/dout:
 //
-//   combine_bwd    dY[pos(t,j)] = w[t,j] dout[t],  dw[t,j] = <dout[t], Y[pos(t,j)]>
+//   combine_bwd    dY[pos(t,j)] = w[t,j] dout[t],  dw[t,j] = <dout[t], Y[pos(t,j)]>;
+//                  bf16 layers also keep, per routed row p, dout[t] itself and
+//                  w[t,j] (the dH GEMM takes the weight out of its sum)
 //   router_bwd     dL[t] from dw[t] through the router's softmax Jacobian
 //   gemm_nt        out[r] = A[r] . W[e]^T (row r of expert e's segment; W[e]
 //                  is [N][K] row-major), optionally times SiLU'(Z) in place
@@ -43,6 +45,13 @@ __device__ __forceinline__ float4 ld_f32x4(const __nv_bfloat16* p, size_t i) {
   const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
   return make_float4(a.x, a.y, b.x, b.y);
 }
+// four consecutive elements copied bit for bit
+__device__ __forceinline__ void copy4(float* dst, const float* src) {
+  *reinterpret_cast<float4*>(dst) = __ldg(reinterpret_cast<const float4*>(src));
+}
+__device__ __forceinline__ void copy4(__nv_bfloat16* dst, const __nv_bfloat16* src) {
+  *reinterpret_cast<uint2*>(dst) = __ldg(reinterpret_cast<const uint2*>(src));
+}
 // v = hi + lo, hi = bf16(v), lo = bf16(v - hi), for two values packed
 __device__ __forceinline__ void split2(float a, float b, uint32_t* hi, uint32_t* lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -59,7 +68,8 @@ template <typename Tout>
 __global__ void __launch_bounds__(128) combine_bwd_kernel(
     const Tout* __restrict__ dout, const float* __restrict__ y, const int32_t* __restrict__ pos,
     const float* __restrict__ w, int T, int d, int k, int R, float* __restrict__ dY,
-    __nv_bfloat16* __restrict__ dYs, float* __restrict__ dw, uint32_t* __restrict__ err,
+    __nv_bfloat16* __restrict__ dYs, Tout* __restrict__ doutp, float* __restrict__ wr,
+    float* __restrict__ dw, uint32_t* __restrict__ err,
     uint32_t* __restrict__ zero, int nzero, int32_t* __restrict__ seg01,
     int32_t* __restrict__ segk, int nsegk, int chunk) {
   __shared__ float red[4][kMaxFanout];
@@ -80,11 +90,13 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     const bool ok = p >= 0 && p < R;
     if (!ok && tid == 0) atomicOr(err, kErrBadIndex);
     const float wt = ok ? __ldg(w + static_cast<size_t>(t) * k + j) : 0.f;
+    if (ok && wr != nullptr && tid == 0) wr[p] = wt;
     float part = 0.f;
     if (ok) {
       // four columns per thread (d is a multiple of 64)
       for (int c = tid * 4; c < d; c += 512) {
         const float4 g = ld_f32x4(dout, static_cast<size_t>(t) * d + c);
+        if (doutp != nullptr) copy4(doutp + static_cast<size_t>(p) * d + c, dout + static_cast<size_t>(t) * d + c);
         const float4 v = make_float4(wt * g.x, wt * g.y, wt * g.z, wt * g.w);
         if (dY != nullptr) *reinterpret_cast<float4*>(dY + static_cast<size_t>(p) * d + c) = v;
         if (dYs != nullptr) {
@@ -504,18 +516,20 @@ __global__ void __launch_bounds__(128) undispatch_kernel(const float* __restrict
 
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
-                               float* dw, uint32_t* err, uint32_t* zero, int nzero,
-                               int32_t* seg01, int32_t* segk, int nsegk, int chunk,
+                               void* doutp, float* wr, float* dw, uint32_t* err, uint32_t* zero,
+                               int nzero, int32_t* seg01, int32_t* segk, int nsegk, int chunk,
                                cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(dYs);
   if (dtype == 0)
     return launch_pdl(combine_bwd_kernel<float>, dim3(T), dim3(128), 0, s,
-                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, ys, dw, err,
-                      zero, nzero, seg01, segk, nsegk, chunk);
+                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, ys,
+                      static_cast<float*>(doutp), wr, dw, err, zero, nzero, seg01, segk, nsegk,
+                      chunk);
   return launch_pdl(combine_bwd_kernel<__nv_bfloat16>, dim3(T), dim3(128), 0, s,
-                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys, dw,
-                    err, zero, nzero, seg01, segk, nsegk, chunk);
+                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys,
+                    static_cast<__nv_bfloat16*>(doutp), wr, dw, err, zero, nzero, seg01, segk,
+                    nsegk, chunk);
 }
 
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,

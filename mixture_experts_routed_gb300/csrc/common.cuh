@@ -166,10 +166,12 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 // [R][2d] = [hi | lo]); dw[t,j] = <dout[t], Y[pos(t,j)]>; also zeroes `nzero`
 // words at `zero`, writes seg01 = {0, T} and, when segk is non-null, the
 // token chunks segk[i] = min(i chunk, T), i = 0 .. nsegk (nsegk < 128).
+// doutp, wr (nullable): per routed row p = pos(t, j), dout[t] (the layer's dtype,
+// bit for bit) and w[t, j].
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
-                               float* dw, uint32_t* err, uint32_t* zero, int nzero,
-                               int32_t* seg01, int32_t* segk, int nsegk, int chunk,
+                               void* doutp, float* wr, float* dw, uint32_t* err, uint32_t* zero,
+                               int nzero, int32_t* seg01, int32_t* segk, int nsegk, int chunk,
                                cudaStream_t s);
 // dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec),
 // and, when dLs is non-null, its bf16 split [T][2E] = [hi | lo].
@@ -187,10 +189,14 @@ cudaError_t launch_gemm_nt(int wdtype, bool silu, const float* A, const void* W,
 // W bf16 [E][N][k_wrap] row-major, A bf16 [R, K] with K = k_wrap or
 // 2 k_wrap (k >= k_wrap reads weight column k - k_wrap: the hi | lo operand
 // split against one weight). zin null: out = y, fp32 [R, N]; else out =
-// the bf16 split [R][2N] = [hi | lo] of y * SiLU'(zin) (zin fp32 [R, N]).
+// the bf16 split [R][2N] = [hi | lo] of (row_scale[r] y) * SiLU'(zin) (zin
+// fp32 [R, N]; row_scale nullable: 1). a_shared: A holds a_rows rows and
+// row r of expert e reads row r - offsets[e] (else a_rows = R).
 cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K, int k_wrap,
                               int N, const int32_t* offsets, const float* zin, void* out,
-                              uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s);
+                              uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s,
+                              const float* row_scale = nullptr, int a_rows = -1,
+                              int a_shared = 0);
 
 // The experts' weight gradients on the tensor cores (wgrad_tc.cu):
 // out[e] = A_e^T . (Bs_e[:, :N] + Bs_e[:, N:]) over the rows of expert e's

@@ -762,7 +762,8 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
         const bool tma_rows = __all_sync(0xffffffffu, valid);
         const int wrow0 = t.row0 + static_cast<int>(rank) * 128 + q * 32;
         float scale = 1.f;
-        if (EPI == 0 && p.row_scale != nullptr && valid) scale = __ldg(p.row_scale + grow);
+        if ((EPI == 0 || EPI == 2) && p.row_scale != nullptr && valid)
+          scale = __ldg(p.row_scale + grow);
         const int nch = t.width / 32, per = (nch + NH - 1) / NH;
         const int c_end = min(nch, (hh + 1) * per);
 #pragma unroll 1
@@ -780,10 +781,11 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 z = __ldg(zr + i);
-              split2(__uint_as_float(v[4 * i]) * silu_grad(z.x),
-                     __uint_as_float(v[4 * i + 1]) * silu_grad(z.y), &hi[2 * i], &lo[2 * i]);
-              split2(__uint_as_float(v[4 * i + 2]) * silu_grad(z.z),
-                     __uint_as_float(v[4 * i + 3]) * silu_grad(z.w), &hi[2 * i + 1],
+              split2(__uint_as_float(v[4 * i]) * scale * silu_grad(z.x),
+                     __uint_as_float(v[4 * i + 1]) * scale * silu_grad(z.y), &hi[2 * i],
+                     &lo[2 * i]);
+              split2(__uint_as_float(v[4 * i + 2]) * scale * silu_grad(z.z),
+                     __uint_as_float(v[4 * i + 3]) * scale * silu_grad(z.w), &hi[2 * i + 1],
                      &lo[2 * i + 1]);
             }
             if (tma_rows) {
@@ -889,7 +891,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
             tmem_ld_wait();
             const int trow = t.row0 + pairk::BM;
             float my_scale = 1.f;
-            if (EPI == 0 && p.row_scale != nullptr && lane < t.tail)
+            if ((EPI == 0 || EPI == 2) && p.row_scale != nullptr && lane < t.tail)
               my_scale = __ldg(p.row_scale + trow + lane);
             const size_t base = static_cast<size_t>(trow) * p.N + f;
             if constexpr (EPI == 0) {
@@ -912,11 +914,13 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
                             ? __ldg(p.zin + static_cast<size_t>(trow + jj) * p.N + f)
                             : 0.f;
 #pragma unroll
-              for (int jj = 0; jj < 32; ++jj)
+              for (int jj = 0; jj < 32; ++jj) {
+                const float sj = __shfl_sync(0xffffffffu, my_scale, jj);
                 if (jj < t.tail && f_ok) {
                   __nv_bfloat16* o = out + static_cast<size_t>(jj) * 2 * p.N;
-                  split1(__uint_as_float(v[jj]) * silu_grad(z[jj]), o, o + p.N);
+                  split1(__uint_as_float(v[jj]) * sj * silu_grad(z[jj]), o, o + p.N);
                 }
+              }
             } else {
               float* out = static_cast<float*>(p.out) + base;
 #pragma unroll
@@ -941,7 +945,7 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
           const int tok0 = c * 32;
           const int nt = min(32, t.ntok - tok0);
           float my_scale = 1.f;
-          if (EPI == 0 && p.row_scale != nullptr && lane < nt)
+          if ((EPI == 0 || EPI == 2) && p.row_scale != nullptr && lane < nt)
             my_scale = __ldg(p.row_scale + t.row0 + tok0 + lane);
           const size_t base = (static_cast<size_t>(t.row0) + tok0) * p.N + f;
           if constexpr (EPI == 0) {
@@ -962,11 +966,13 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
             for (int jj = 0; jj < 32; ++jj)
               z[jj] = jj < nt && f_ok ? __ldg(p.zin + (r0 + jj) * p.N + f) : 0.f;
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
+            for (int jj = 0; jj < 32; ++jj) {
+              const float sj = __shfl_sync(0xffffffffu, my_scale, jj);
               if (jj < nt && f_ok) {
                 __nv_bfloat16* o = out + static_cast<size_t>(jj) * 2 * p.N;
-                split1(__uint_as_float(v[jj]) * silu_grad(z[jj]), o, o + p.N);
+                split1(__uint_as_float(v[jj]) * sj * silu_grad(z[jj]), o, o + p.N);
               }
+            }
           } else {
             float* out = static_cast<float*>(p.out) + base;
 #pragma unroll
@@ -1452,8 +1458,11 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 
 cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K, int k_wrap,
                               int N, const int32_t* offsets, const float* zin, void* out,
-                              uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s) {
+                              uint32_t* err, uint32_t* tile_ctr, int num_sms, cudaStream_t s,
+                              const float* row_scale, int a_rows, int a_shared) {
   if (R == 0) return cudaSuccess;
+  if (a_rows < 0) a_rows = R;
+  if (a_rows == 0) return cudaErrorInvalidValue;
   if (num_sms < 2 || k_wrap <= 0 || k_wrap % 64 != 0 || K % k_wrap != 0 || N % 8 != 0)
     return cudaErrorInvalidValue;
   CUtensorMap mA, mA8, mB, mY;
@@ -1463,8 +1472,8 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   std::memset(&mY, 0, sizeof(mY));
   // A: [R, K] rows in [128][64] boxes (and [8][64] for merged remainders);
   // weights: the stored [E N, k_wrap] matrix in [128 features][64 k] boxes
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 128) ||
-      !make_map_2d(&mA8, A, static_cast<uint64_t>(R), static_cast<uint64_t>(K), 64, 8) ||
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64, 128) ||
+      !make_map_2d(&mA8, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(K), 64, 8) ||
       !make_map_2d(&mB, Wt, static_cast<uint64_t>(E) * N, static_cast<uint64_t>(k_wrap), 64, 128) ||
       !make_map_2d_out(&mY, out, static_cast<uint64_t>(R),
                        static_cast<uint64_t>(zin ? 2 * N : N), zin == nullptr))
@@ -1474,7 +1483,7 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   prm.gx = nullptr;
   prm.gx_rows = 0;
   prm.offsets = offsets;
-  prm.row_scale = nullptr;
+  prm.row_scale = zin ? row_scale : nullptr;
   prm.zin = zin;
   prm.out = out;
   prm.err = err;
@@ -1484,8 +1493,8 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   prm.N = N;
   prm.R = R;
   prm.n_tiles = 0;
-  prm.a_rows = R;
-  prm.a_shared = 0;
+  prm.a_rows = a_rows;
+  prm.a_shared = a_shared;
   prm.k_wrap = k_wrap;
   prm.epi_wait_ns = g_epi_wait_ns.load();
   return zin ? launch_pair<2, 1, false, true>(mA, mA8, mB, mY, prm, num_sms, s)

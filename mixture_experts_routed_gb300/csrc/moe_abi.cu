@@ -293,10 +293,11 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // segment {0, T} of the gate GEMMs, dY (fp32 layers), the recomputed
 // pre-activation Z (fp32 layers overwrite it with dZ), dX_perm and the gate
 // part of dx, all fp32 but the ints; bf16 layers add the tensor-core GEMMs'
-// operands: the bf16 splits of dY, dZ and dL.
+// operands: the bf16 splits of dY, dZ and dL, and per routed row its token's
+// dout row (hard routers) and its routing weight.
 struct BwdLayout {
   size_t err, L, ridx, rw, dw, dL, seg01, segk, bpart, gpart, dY, Z, dXp, dxg, dYs, dZs, dLs,
-      xp, total;
+      doutp, wr, xp, total;
 };
 
 // Token chunks of the gate's weight gradient (split along T so that its few
@@ -353,6 +354,8 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
   B.dZs = take(tc ? R * 2 * c.f * 2 : 0);
   B.dLs = take(tc ? T * 2 * E * 2 : 0);
+  B.doutp = take(tc && !soft(c) ? R * c.d * 2 : 0);
+  B.wr = take(tc ? R * 4 : 0);
   // the packed rows, when the forward gathered them instead of writing them
   B.xp = take(gathers(c) ? R * c.d * 2 : 0);
   B.total = o;
@@ -421,8 +424,10 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
                              : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
-                                     tc ? at<void>(bws, B.dYs) : nullptr, dw, err, ctr, 4, seg01,
-                                     segk, ch.n, ch.len, s);
+                           tc ? at<void>(bws, B.dYs) : nullptr,
+                           tc && !soft(c) ? at<void>(bws, B.doutp) : nullptr,
+                           tc ? at<float>(bws, B.wr) : nullptr, dw, err, ctr, 4, seg01, segk,
+                           ch.n, ch.len, s);
   void* dLs = tc ? at<void>(bws, B.dLs) : nullptr;
   if (e == cudaSuccess)
     e = launch_router_bwd(Lr, idx, w, dw, T, E, k, c.router, c.pre_k, c.tau, dL, dLs, s);
@@ -463,12 +468,16 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
     } else {
       e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
                          nullptr, Z, err, ctr, nullptr, c.gemm_tile_n, sms, s);
-      // dH = [dY hi | dY lo] . [W2_e^T ; W2_e^T], its epilogue writing the
-      // split of dZ = dH * SiLU'(Z); dX_perm = [dZ hi | dZ lo] . [W1_e^T ;
-      // W1_e^T]: the stored weights read K-major, K = 2d (2f) wrapping at d (f)
+      // dH[r] = w_r (dout[t(r)] . W2_e^T): row r's routing weight comes out of
+      // the sum, so the GEMM reads the exact bf16 dout rows (K = d; soft
+      // gating: dout itself, every expert reading all T rows) and its
+      // epilogue scales by w_r and writes the split of dZ = dH * SiLU'(Z);
+      // dX_perm = [dZ hi | dZ lo] . [W1_e^T ; W1_e^T]: the stored weights
+      // read K-major, K = 2f wrapping at f
       if (e == cudaSuccess)
-        e = launch_gemm_tc_wt(at<void>(bws, B.dYs), R, W2, E, 2 * d, d, f, offsets, Z,
-                              at<void>(bws, B.dZs), err, ctr + 1, sms, s);
+        e = launch_gemm_tc_wt(soft(c) ? dout : at<void>(bws, B.doutp), R, W2, E, d, d, f,
+                              offsets, Z, at<void>(bws, B.dZs), err, ctr + 1, sms, s,
+                              at<float>(bws, B.wr), soft(c) ? T : R, soft(c) ? 1 : 0);
       if (e == cudaSuccess)
         e = launch_gemm_tc_wt(at<void>(bws, B.dZs), R, W1, E, 2 * f, f, d, offsets, nullptr, dXp,
                               err, ctr + 2, sms, s);
