@@ -127,3 +127,63 @@ def test_empty_expert_does_not_contribute():
     inp["W1"][3] = float("nan")                 # never read
     r2 = oracle.forward(cfg, inp)
     assert np.array_equal(r["out"], r2["out"])
+
+
+@pytest.mark.parametrize("f_extra", [0, 64])
+def test_permutation_weights_give_scaled_silu(f_extra):
+    # W1_e = [P_e | 0] (d x f), W2_e = c_e [P_e^T ; R] (f x d): row-vector
+    # convention x W1 permutes x, SiLU acts elementwise (SiLU(0) = 0 on the
+    # padding columns, so R never matters), W2 undoes the permutation. So
+    # expert e returns c_e SiLU(x) exactly and the layer returns
+    # (sum_j w_tj c_e(t,j)) SiLU(x_t), checked with math.exp. A transposed or
+    # mis-indexed W1 or W2, or a combine using the wrong expert's output,
+    # fails this.
+    import math
+    d, E, k = 64, 6, 3
+    cfg = _cfg(d=d, E=E, k=k, f=d + f_extra, pre_k=4, bias="normal", bias_var=1.0)
+    inp = make_inputs(cfg)
+    a = oracle.inputs_to_numpy(inp)
+    rng = np.random.default_rng(11)
+    c = rng.uniform(0.5, 2.0, size=E)
+    W1 = np.zeros((E, d, cfg.f))
+    W2 = rng.standard_normal((E, cfg.f, d))       # rows past d are multiplied by SiLU(0) = 0
+    for e in range(E):
+        P = np.eye(d)[rng.permutation(d)]
+        W1[e, :, :d] = P
+        W2[e, :d, :] = c[e] * P.T
+    a["W1"], a["W2"] = W1, W2
+    r = oracle.forward(cfg, a)
+    x = a["x"]
+    # H is stored in the layer's dtype (fp32 here), so SiLU(x) is rounded to fp32
+    silu = np.vectorize(lambda v: v / (1.0 + math.exp(-v)))(x).astype(np.float32).astype(np.float64)
+    scale = np.array([sum(r["topk_w"][t, j] * c[r["topk_idx"][t, j]] for j in range(k))
+                      for t in range(cfg.T)])
+    assert np.max(np.abs(r["out"] - scale[:, None] * silu)) <= 1e-12
+
+
+@pytest.mark.parametrize("mistake", ["w1_transposed", "w2_transposed", "no_silu", "wrong_expert"])
+def test_permutation_pin_catches_planted_mistakes(monkeypatch, mistake):
+    # the pin above must fail when the oracle's FFN is wrong in a plausible
+    # way: a mistake planted in the oracle (on the CPU) is caught
+    mo = oracle.moe_oracle
+    real_rows, real_expert = mo.expert_ffn_rows, mo._expert
+
+    def bad_rows(x_rows, W1e, W2e, h_storage="bf16"):
+        # (the pin runs with f = d here, so the weights are square)
+        if mistake == "w1_transposed":
+            return real_rows(x_rows, np.asarray(W1e).T, W2e, h_storage)
+        if mistake == "w2_transposed":
+            return real_rows(x_rows, W1e, np.asarray(W2e).T, h_storage)
+        if mistake == "no_silu":
+            z = np.asarray(x_rows, np.float64) @ np.asarray(W1e, np.float64)
+            h = mo.round_to_f32(z) if h_storage == "f32" else z
+            return h @ np.asarray(W2e, np.float64), h
+        return real_rows(x_rows, W1e, W2e, h_storage)
+
+    def bad_expert(W, e):
+        return real_expert(W, (e + 1) % W.shape[0]) if mistake == "wrong_expert" else real_expert(W, e)
+
+    monkeypatch.setattr(mo, "expert_ffn_rows", bad_rows)
+    monkeypatch.setattr(mo, "_expert", bad_expert)
+    with pytest.raises(AssertionError):
+        test_permutation_weights_give_scaled_silu(0)
