@@ -110,3 +110,33 @@ def test_random_layer_backward_matches_oracle(cuda_ok, i):
     rel = 1e-4 if cfg.dtype == "f32" else 2e-3
     for n in ("dx", "dWg", "dbias", "dW1", "dW2"):
         _close(grads[n].cpu().numpy().astype(np.float64), ref[n], rel, f"{cfg} {n}")
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_layer_fp8_expert_outputs_match_oracle(cuda_ok, i):
+    # the same sweep with the expert outputs handed to the combine as the FP8
+    # min/max-affine payload (hard routers), with its own comparator
+    from parity_util import assert_close_output_fp8
+    cfg = _random_layer(200 + i)
+    if cfg.router == 3:
+        cfg = cfg.with_(router=0, k=min(2, cfg.E), pre_k=min(8, cfg.E))
+    cfg = cfg.with_(output_fp8=1)
+    assert moe.check_config(cfg) == moe.MOE_OK, cfg
+    inp = make_inputs(cfg, device="cuda")
+    ws = moe.alloc_workspace(cfg)
+    out = moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
+                      noise=inp.get("gumbel"))
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == moe.MOE_OK, cfg
+    host = oracle.inputs_to_numpy(inp)
+    ref = oracle.forward(cfg, host, keep_h=False)
+    L = oracle.gate_logits(host["x"], host["Wg"], host["bias"])
+    keep = ~route_ties(cfg, L)
+    slots = ref["pos"].reshape(cfg.T, cfg.k)
+    v = moe.forward_views(cfg, ws)
+    rows = torch.from_numpy(slots.reshape(-1).astype(np.int64)).cuda()
+    codes = v["y_q"][rows].view(torch.float8_e4m3fn).double().cpu().numpy()
+    codes = codes.reshape(cfg.T, cfg.k, -1)
+    assert_close_output_fp8(cfg, to_np(out)[keep], ref["out_rounded"][keep], ref["topk_w"][keep],
+                            ref["y_q"][slots][keep], ref["y_scale"][slots][keep], codes[keep],
+                            str(cfg))
