@@ -44,15 +44,23 @@ STAGES = ["route", "dispatch", "w1_prologue", "gemm_w1_silu", "gemm_w2", "quanti
 
 
 def parse():
-    p = argparse.ArgumentParser()
-    p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--config", default=None)
-    p.add_argument("--flush-l2", action="store_true")
-    p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--no-e2e", action="store_true")
+    from workloads import CONFIG_ORDER, VARIANTS
+    p = argparse.ArgumentParser(
+        description="Routed tokens/s of one MoE layer forward: one JSON line on rank 0.")
+    p.add_argument("--gpus", type=int, default=1,
+                   help="replicas, one process per GPU (launched by torch.distributed.run)")
+    p.add_argument("--steps", type=int, default=20, help="timed forwards")
+    p.add_argument("--warmup", type=int, default=5, help="untimed forwards first (at least 3)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"],
+                   help="ours: the CUDA library; reference: the fp64 CPU oracle")
+    p.add_argument("--config", default=None,
+                   help="layer name (default: the 256-expert layer); one of "
+                   + ", ".join(list(CONFIG_ORDER) + list(VARIANTS)))
+    p.add_argument("--flush-l2", action="store_true",
+                   help="write a buffer twice the L2 before every timed forward")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
+    p.add_argument("--no-e2e", action="store_true",
+                   help="skip the end-to-end timing with host buffers")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle baseline: run 16-token chunks until this much time has passed")
     p.add_argument("--backward", action="store_true",
