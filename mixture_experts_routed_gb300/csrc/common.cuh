@@ -23,6 +23,37 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------------------------ quotient
+// x / s rounded to nearest even (the IEEE quotient) without a division per
+// element. With y = RN(1/s) (one correctly rounded reciprocal per row),
+// q = RN(x y) is within two ulps of x / s; a correction
+// q <- RN(q + RN(x - s q) y), the residual from one FMA, brings it within
+// one ulp, and by Markstein's theorem (P. Markstein, IBM J. Res. Dev. 34(1),
+// 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. 4) a second
+// one then gives the correctly rounded quotient: once q is within one ulp,
+// the residual is exact. The callers take this path only for s in
+// [2^-64, 2^64] (y normal). The theorem wants a normal residual; where it is
+// subnormal the quotient is below 2^-100, far under the first E4M3 rounding
+// boundary (2^-10), and the sign of x is kept, so the E4M3 code is the same.
+// CLAMP: quotients of magnitude above 1024 (the first product says so to
+// within 2^-22) saturate to +-448 in E4M3 either way and are returned as
+// +-1024, which keeps the corrections away from overflow; without it the
+// caller guarantees |x| <= 448 s (x within the row's absmax, s = amax / 448
+// rounded). For finite x.
+__device__ __forceinline__ bool quotient_scale_ok(float s) {
+  return s >= 0x1p-64f && s <= 0x1p64f;
+}
+template <bool CLAMP = true>
+__device__ __forceinline__ float quotient_rn(float x, float s, float y) {
+  float q = __fmul_rn(x, y);
+  const bool big = CLAMP && fabsf(q) > 1024.f;
+  float r = __fmaf_rn(-s, q, x);
+  q = __fmaf_rn(r, y, q);
+  r = __fmaf_rn(-s, q, x);
+  q = __fmaf_rn(r, y, q);
+  return copysignf(big ? 1024.f : q, x);
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t s, Args&&... args) {

@@ -29,6 +29,7 @@
 //
 // Expert ids outside [0, E) are skipped and flag kErrBadIndex.
 #include <cstdint>
+#include <type_traits>
 #include <mutex>
 
 #include <cuda_bf16.h>
@@ -130,17 +131,50 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t u) {
   return __uint_as_float(static_cast<uint32_t>(u) << 16);
 }
 
-// 8 floats -> 8 E4M3 bytes of x / s (round to nearest even, saturating),
-// element 0 in the lowest byte.
-__device__ __forceinline__ uint2 quant8(const float (&v)[8], float s) {
+// Running largest magnitudes of bf16 pairs (max is exact in bf16), and the
+// largest of a pair as fp32.
+__device__ __forceinline__ __nv_bfloat162 absmax8(__nv_bfloat162 m, const uint4& v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = __hmax2(m, __habs2(h[i]));
+  return m;
+}
+__device__ __forceinline__ float pair_max(__nv_bfloat162 m) {
+  return fmaxf(__bfloat162float(m.x), __bfloat162float(m.y));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// The token's payload scale: the static one if given, else fp32(amax / 448)
+// (1 for an all-zero row).
+__device__ __forceinline__ float payload_scale(float amax, float static_scale) {
+  return static_scale > 0.f ? static_scale : ((amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f));
+}
+
+// Rows of up to 32 * kRowRegVecs 16-byte vectors (d <= 5120 bf16) are held
+// in registers by the FP8 quantiser.
+constexpr int kRowRegVecs = 20;
+
+// 8 floats -> 8 E4M3 bytes of x / s (the IEEE quotient, then round to
+// nearest even, saturating), element 0 in the lowest byte. FAST: the
+// quotient from y = RN(1/s) and two residual corrections (quotient_rn, the
+// same bits); otherwise one IEEE division per element. CLAMP = false: the
+// caller knows |x| <= 448 s.
+template <bool FAST, bool CLAMP = true>
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], float s, float y) {
   uint32_t w[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t acc = 0;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-      const float a = __fdiv_rn(v[h * 4 + p * 2], s);
-      const float b = __fdiv_rn(v[h * 4 + p * 2 + 1], s);
+      const float x0 = v[h * 4 + p * 2], x1 = v[h * 4 + p * 2 + 1];
+      const float a = FAST ? quotient_rn<CLAMP>(x0, s, y) : __fdiv_rn(x0, s);
+      const float b = FAST ? quotient_rn<CLAMP>(x1, s, y) : __fdiv_rn(x1, s);
       const __nv_fp8x2_storage_t q =
           __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
       acc |= static_cast<uint32_t>(q) << (16 * p);
@@ -148,6 +182,38 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8], float s) {
     w[h] = acc;
   }
   return make_uint2(w[0], w[1]);
+}
+
+// Pass 2 of the FP8 payload for one token (one warp): q = E4M3(x / s) for
+// the row's 16-byte vectors, written to each of its routed rows p[j] >= 0.
+// The division form (scales outside [2^-64, 2^64] only) keeps one load in
+// flight per lane, so that it does not raise the kernel's register count.
+template <bool FAST>
+__device__ __forceinline__ void quant_row(const uint4* __restrict__ xr, int nvec, int lane,
+                                          float s, const int (&p)[kMaxTopK],
+                                          uint2* __restrict__ dst) {
+  const float y = FAST ? __frcp_rn(s) : 0.f;
+  const size_t row_vecs = static_cast<size_t>(nvec);
+  constexpr int UQ = FAST ? 4 : 1;
+  for (int v0 = lane; v0 < nvec; v0 += 32 * UQ) {
+    uint4 val[UQ];
+#pragma unroll
+    for (int u = 0; u < UQ; ++u)
+      if (v0 + 32 * u < nvec) val[u] = __ldg(xr + v0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < UQ; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nvec) break;
+      const uint16_t* h = reinterpret_cast<const uint16_t*>(&val[u]);
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = bf16_to_f32(h[i]);
+      const uint2 q = quant8<FAST>(f, s, y);
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = q;
+    }
+  }
 }
 
 // dtype 0: fp32 rows, 1: bf16 rows. FP8 only with bf16. FUSED: counts and
@@ -325,54 +391,77 @@ __global__ void __launch_bounds__(256) dispatch_scatter_kernel(
   for (int j = 0; j < kMaxTopK; ++j) p[j] = (j < k) ? pos_s[w * k + j] : -1;
 
   if constexpr (FP8) {
-    // pass 1: absmax of the token's row (bf16 values are exact in fp32),
-    // skipped with a static scale
     const int nvec = d / 8;
     const uint4* xr =
         reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(xv) +
                                        static_cast<size_t>(t) * d);
-    // four 16-byte loads in flight per lane (one at a time is latency-bound)
-    constexpr int UQ = 4;
-    float amax = 0.f;
-    for (int v0 = lane; static_scale <= 0.f && v0 < nvec; v0 += 32 * UQ) {
-      uint4 val[UQ];
-#pragma unroll
-      for (int u = 0; u < UQ; ++u)
-        if (v0 + 32 * u < nvec) val[u] = __ldg(xr + v0 + 32 * u);
-#pragma unroll
-      for (int u = 0; u < UQ; ++u) {
-        if (v0 + 32 * u >= nvec) break;
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&val[u]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(bf16_to_f32(h[i])));
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float s =
-        static_scale > 0.f ? static_scale : ((amax == 0.f) ? 1.f : __fdiv_rn(amax, 448.f));
-    // pass 2: q = E4M3(x / s); the k copies share the scale
     uint2* dst = reinterpret_cast<uint2*>(x_perm);
-    const size_t row_vecs = static_cast<size_t>(nvec);
-    for (int v0 = lane; v0 < nvec; v0 += 32 * UQ) {
-      uint4 val[UQ];
+    float s;
+    if (nvec <= 32 * kRowRegVecs) {
+      // one read of the row: it stays in registers (kRowRegVecs 16-byte
+      // vectors per lane, all loads in flight at once) between the absmax
+      // and the cast
+      uint4 val[kRowRegVecs];
 #pragma unroll
-      for (int u = 0; u < UQ; ++u)
-        if (v0 + 32 * u < nvec) val[u] = __ldg(xr + v0 + 32 * u);
+      for (int u = 0; u < kRowRegVecs; ++u)
+        if (lane + 32 * u < nvec) val[u] = __ldg(xr + lane + 32 * u);
+      float amax = 0.f;
+      if (static_scale <= 0.f) {
+        __nv_bfloat162 m2 = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < UQ; ++u) {
-        const int v = v0 + 32 * u;
-        if (v >= nvec) break;
-        const uint16_t* h = reinterpret_cast<const uint16_t*>(&val[u]);
-        float f[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = bf16_to_f32(h[i]);
-        const uint2 q = quant8(f, s);
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j)
-          if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = q;
+        for (int u = 0; u < kRowRegVecs; ++u)
+          if (lane + 32 * u < nvec) m2 = absmax8(m2, val[u]);
+        amax = warp_max(pair_max(m2));
       }
+      s = payload_scale(amax, static_scale);
+      if (quotient_scale_ok(s)) {  // s is uniform across the warp
+        const float y = __frcp_rn(s);
+        const size_t row_vecs = static_cast<size_t>(nvec);
+        // a per-token scale bounds every |x / s| by 448: no clamp
+        auto quant_reg = [&](auto clamp) {
+#pragma unroll
+          for (int u = 0; u < kRowRegVecs; ++u) {
+            const int v = lane + 32 * u;
+            if (v >= nvec) break;
+            const uint16_t* h = reinterpret_cast<const uint16_t*>(&val[u]);
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = bf16_to_f32(h[i]);
+            const uint2 q = quant8<true, decltype(clamp)::value>(f, s, y);
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j)
+              if (p[j] >= 0) dst[static_cast<size_t>(p[j]) * row_vecs + v] = q;
+          }
+        };
+        if (static_scale > 0.f)
+          quant_reg(std::true_type{});
+        else
+          quant_reg(std::false_type{});
+      } else {
+        quant_row<false>(xr, nvec, lane, s, p, dst);
+      }
+    } else {
+      // wider rows: pass 1 reads the row for its absmax (skipped with a
+      // static scale), pass 2 reads it again, from L2
+      constexpr int UQ = 4;  // 16-byte loads in flight per lane
+      float amax = 0.f;
+      for (int v0 = lane; static_scale <= 0.f && v0 < nvec; v0 += 32 * UQ) {
+        uint4 val[UQ];
+#pragma unroll
+        for (int u = 0; u < UQ; ++u)
+          if (v0 + 32 * u < nvec) val[u] = __ldg(xr + v0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < UQ; ++u) {
+          if (v0 + 32 * u >= nvec) break;
+          amax = fmaxf(amax, pair_max(absmax8(__floats2bfloat162_rn(0.f, 0.f), val[u])));
+        }
+      }
+      amax = warp_max(amax);
+      s = payload_scale(amax, static_scale);
+      if (quotient_scale_ok(s))
+        quant_row<true>(xr, nvec, lane, s, p, dst);
+      else
+        quant_row<false>(xr, nvec, lane, s, p, dst);
     }
     if (lane == 0) {
 #pragma unroll

@@ -21,8 +21,47 @@ namespace {
 
 constexpr int kRowsPerCta = 8;  // one warp per row
 
+// Four values of a row -> four E4M3 bytes of fp32(v - zero) / s (the IEEE
+// quotient; FAST: from y = RN(1/s) and two residual corrections, the same
+// bits), element 0 in the lowest byte.
+template <bool FAST>
+__device__ __forceinline__ uint32_t quant4(float4 a, float zero, float s, float y) {
+  const float x0 = __fsub_rn(a.x, zero), x1 = __fsub_rn(a.y, zero);
+  const float x2 = __fsub_rn(a.z, zero), x3 = __fsub_rn(a.w, zero);
+  const float2 lo = FAST ? make_float2(quotient_rn(x0, s, y), quotient_rn(x1, s, y))
+                         : make_float2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+  const float2 hi = FAST ? make_float2(quotient_rn(x2, s, y), quotient_rn(x3, s, y))
+                         : make_float2(__fdiv_rn(x2, s), __fdiv_rn(x3, s));
+  const uint32_t b0 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+  const uint32_t b1 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+  return b0 | (b1 << 16);
+}
+
+// Pass 2 of quantize_out_kernel for one row (one warp); the division form
+// (scales outside [2^-64, 2^64] only) keeps one load in flight per lane.
+template <bool FAST>
+__device__ __forceinline__ void quant_row_out(const float4* __restrict__ row, int nv, int lane,
+                                              float zero, float s, uint32_t* __restrict__ out) {
+  const float y = FAST ? __frcp_rn(s) : 0.f;
+  constexpr int U = FAST ? 4 : 1;
+  for (int v0 = lane; v0 < nv; v0 += 32 * U) {
+    float4 a[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + 32 * u < nv) a[u] = __ldg(row + v0 + 32 * u);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= nv) break;
+      out[v] = quant4<FAST>(a[u], zero, s, y);
+    }
+  }
+}
+
 // Pass 1 reads the row for its min and max, pass 2 reads it again (from L2:
 // the row was read a moment before) and writes 4 E4M3 bytes per float4.
+// The quotients come from one reciprocal per row and two residual
+// corrections (quotient_rn), bit for bit the IEEE division.
 __global__ void __launch_bounds__(256) quantize_out_kernel(const float* __restrict__ y, int R,
                                                            int d, uint8_t* __restrict__ yq,
                                                            float* __restrict__ ys,
@@ -58,24 +97,10 @@ __global__ void __launch_bounds__(256) quantize_out_kernel(const float* __restri
   const float half = __fsub_rn(hmx, hmn);
   const float s = (half == 0.f) ? 1.f : __fdiv_rn(half, 448.f);
   uint32_t* out = reinterpret_cast<uint32_t*>(yq + static_cast<size_t>(r) * d);
-  for (int v0 = lane; v0 < nv; v0 += 32 * U) {
-    float4 a[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (v0 + 32 * u < nv) a[u] = __ldg(row + v0 + 32 * u);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int v = v0 + 32 * u;
-      if (v >= nv) break;
-      const float2 lo = make_float2(__fdiv_rn(__fsub_rn(a[u].x, zero), s),
-                                    __fdiv_rn(__fsub_rn(a[u].y, zero), s));
-      const float2 hi = make_float2(__fdiv_rn(__fsub_rn(a[u].z, zero), s),
-                                    __fdiv_rn(__fsub_rn(a[u].w, zero), s));
-      const uint32_t b0 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t b1 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-      out[v] = b0 | (b1 << 16);
-    }
-  }
+  if (quotient_scale_ok(s))  // s is uniform across the warp
+    quant_row_out<true>(row, nv, lane, zero, s, out);
+  else
+    quant_row_out<false>(row, nv, lane, zero, s, out);
   if (lane == 0) {
     ys[r] = s;
     yz[r] = zero;
@@ -129,18 +154,12 @@ __global__ void __launch_bounds__(256) quantize_out_cta_kernel(const float* __re
   const float half = __fsub_rn(hmx, hmn);
   const float s = (half == 0.f) ? 1.f : __fdiv_rn(half, 448.f);
   uint32_t* out = reinterpret_cast<uint32_t*>(yq + static_cast<size_t>(r) * d);
+  const bool fast = quotient_scale_ok(s);  // uniform across the CTA
+  const float yr = fast ? __frcp_rn(s) : 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int v = tid + 256 * i;
-    if (v < nv) {
-      const float2 lo = make_float2(__fdiv_rn(__fsub_rn(a[i].x, zero), s),
-                                    __fdiv_rn(__fsub_rn(a[i].y, zero), s));
-      const float2 hi = make_float2(__fdiv_rn(__fsub_rn(a[i].z, zero), s),
-                                    __fdiv_rn(__fsub_rn(a[i].w, zero), s));
-      const uint32_t b0 = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t b1 = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-      out[v] = b0 | (b1 << 16);
-    }
+    if (v < nv) out[v] = fast ? quant4<true>(a[i], zero, s, yr) : quant4<false>(a[i], zero, s, yr);
   }
   if (tid == 0) {
     ys[r] = s;

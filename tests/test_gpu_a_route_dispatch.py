@@ -157,6 +157,60 @@ def _fp8_edge_rows(T, d, static_scale, seed):
 
 # static scales 7 * 2^-9 and 13 * 2^-10: bf16 values exist whose product with
 # 1/s takes another code than the quotient (30 and 1 of them)
+def _every_bf16_rows(d, amax, rng):
+    """Rows of width d that together hold every finite bf16 value of
+    magnitude <= amax (all of them if amax is None), each with a random
+    sign, zero-padded; with an amax each row starts with +amax, so a
+    per-token scale is fp32(amax / 448) on every row."""
+    mags = (np.arange(0, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    if amax is not None:
+        mags = mags[mags <= np.float32(amax)]
+    vals = mags * np.where(rng.random(mags.size) < 0.5, -1.0, 1.0).astype(np.float32)
+    width = d if amax is None else d - 1
+    n = -(-vals.size // width)
+    body = np.zeros(n * width, np.float32)
+    body[:vals.size] = vals
+    body = body.reshape(n, width)
+    if amax is None:
+        return body
+    return np.concatenate([np.full((n, 1), np.float32(amax), np.float32), body], 1)
+
+
+# every bf16 value through the quantiser: static scales on both sides of the
+# range where the quotient comes from a reciprocal and two corrections
+# ([2^-64, 2^64]) and per-token scales from a few absmax values; rows held in
+# registers (d <= 5120) and rows read twice (wider)
+@pytest.mark.parametrize("d", [4096, 6144])
+@pytest.mark.parametrize("static_scale", [None, 0.013671875, 0.02, 3.0, 2.0 ** -70, 2.0 ** 70])
+def test_dispatch_fp8_every_bf16_value(cuda_ok, static_scale, d):
+    from workloads import MoEConfig
+    rng = np.random.default_rng(21)
+    E, k = 4, 2
+    if static_scale is None:
+        rows = np.concatenate([_every_bf16_rows(d, a, rng)
+                               for a in (20.0, 0.75, 448.0, 0.0029296875, 2.0 ** -100)])
+    else:
+        rows = _every_bf16_rows(d, None, rng)
+    T = rows.shape[0]
+    mode = True if static_scale is None else 2
+    cfg = MoEConfig("fp8_every_bf16", T=T, d=d, E=E, k=k, f=128, dtype="bf16", pre_k=4,
+                    payload_fp8=mode, payload_scale=static_scale or 0.0)
+    x = torch.from_numpy(rows).to(torch.bfloat16)
+    assert torch.equal(x.float(), torch.from_numpy(rows))
+    idx = np.stack([np.arange(T) % E, (np.arange(T) + 1) % E], 1).astype(np.int32)
+    ws = moe.alloc_workspace(cfg, kind="scratch")
+    dd = moe.dispatch(cfg, x.cuda(), torch.from_numpy(idx).cuda(), ws=ws)
+    torch.cuda.synchronize()
+    assert moe.get_device_error(ws) == moe.MOE_OK
+    _, _, _, src = oracle.dispatch(idx, E)
+    q, s = oracle.quantize_payload_fp8(rows.astype(np.float64), static_scale)
+    ref = oracle.e4m3_encode(q[src])
+    got = to_np(dd["x_perm"])
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} payload bytes differ"
+    got_s = to_np(dd["x_scale"]).astype(np.float32)
+    assert np.array_equal(got_s.view(np.uint32), s[src].astype(np.float32).view(np.uint32))
+
+
 @pytest.mark.parametrize("static_scale", [None, 0.013671875, 0.0126953125])
 def test_dispatch_fp8_payload_rounding_edges(cuda_ok, static_scale):
     # the payload bytes are those of the IEEE fp32 quotient on rows built
