@@ -64,7 +64,11 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU oracle baseline: run 16-token chunks until this much time has passed")
     p.add_argument("--backward", action="store_true",
-                   help="also time moe_backward (adds a 'backward' object to the line)")
+                   help="also time moe_backward (adds a 'backward' object to the line): after "
+                        "a forward that keeps the pre-activation Z (keep_z, timed too), or, "
+                        "with --recompute-z, after the plain forward, recomputing Z")
+    p.add_argument("--recompute-z", action="store_true",
+                   help="with --backward: the backward recomputes Z instead of reading it")
     p.add_argument("--x-perm-mode", type=int, default=None, choices=[0, 1, 2],
                    help="0 the library's choice, 1 packed rows, 2 rows gathered by the W1 GEMM")
     p.add_argument("--gemm-tile-n", type=int, default=None, choices=[0, 256, 512],
@@ -535,14 +539,42 @@ def run_ours(args, cfg):
     # ---- backward (optional): K steps of moe_backward after the forward above
     bwd = None
     if args.backward and not (cfg.payload_fp8 or getattr(cfg, "output_fp8", 0)):
-        bws = moe.alloc_workspace(cfg, "backward")
+        # training form: the forward keeps Z (keep_z) and the backward reads
+        # it; --recompute-z: the plain forward, the backward recomputes Z
+        kept = not args.recompute_z
+        bcfg = cfg.with_(keep_z=1) if kept else cfg
+        fws = moe.alloc_workspace(bcfg) if kept else ws
+        bws = moe.alloc_workspace(bcfg, "backward")
         gen = torch.Generator(device=dev)
         gen.manual_seed(5)
         dout = torch.randn((cfg.T, cfg.d), generator=gen, device=dev).to(cfg.torch_dtype)
+        fwd_z_ms = None
+        if kept:
+            fout = torch.empty((cfg.T, cfg.d), dtype=cfg.torch_dtype, device=dev)
+
+            def fwd_z_step():
+                moe.forward(bcfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"],
+                            ws=fws, out=fout, noise=inp.get("gumbel"), stream=stream)
+
+            for _ in range(max(1, args.warmup)):
+                fwd_z_step()
+            torch.cuda.synchronize(dev)
+            if dist:
+                dist.barrier()
+            fa = torch.cuda.Event(enable_timing=True)
+            fb = torch.cuda.Event(enable_timing=True)
+            fa.record(stream)
+            for _ in range(K):
+                fwd_z_step()
+            fb.record(stream)
+            torch.cuda.synchronize(dev)
+            fwd_z_ms = max_over_ranks(fa.elapsed_time(fb), dist, dev) / K
+            if moe.get_device_error(fws) != moe.MOE_OK:
+                raise RuntimeError("device error in the forward steps keeping Z")
 
         def bwd_step():
-            moe.backward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], dout,
-                         fwd_ws=ws, ws=bws, noise=inp.get("gumbel"), stream=stream)
+            moe.backward(bcfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], dout,
+                         fwd_ws=fws, ws=bws, noise=inp.get("gumbel"), stream=stream)
 
         for _ in range(max(1, args.warmup)):
             bwd_step()
@@ -563,9 +595,11 @@ def run_ours(args, cfg):
         R = cfg.T * cfg.k
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         gate = 4.0 * cfg.T * cfg.d * cfg.E  # dx_gate and dW_g (fp32 FMA)
+        # Z = X W1 is one 2Rdf GEMM of the backward unless the forward kept it
+        nz = 0.0 if kept else 2.0
         if cfg.dtype == "f32":
-            # every GEMM in fp32 FMA: Z, dH, dX_perm, dW2, dW1 and the gate's
-            simt = 10.0 * R * cfg.d * cfg.f + gate
+            # every GEMM in fp32 FMA: (Z,) dH, dX_perm, dW2, dW1 and the gate's
+            simt = (8.0 + nz) * R * cfg.d * cfg.f + gate
             # fp32 FMA peak from unit counts: SMs x 128 fp32 lanes x 2 flop x clock
             fp32_peak = sms * 128 * 2 * (clk or {}).get("sm_max_mhz", 2070.0) * 1e6 / 1e12
             broof = {"bound": "alu", "achieved": simt / (b_ms / 1e3) / 1e12, "peak": fp32_peak,
@@ -574,13 +608,14 @@ def run_ours(args, cfg):
                     "flops": simt}
             note = "achieved = every GEMM's fp32 FMA work over the whole backward time"
         else:
-            # the method's own work: Z recomputed and four expert GEMMs, 2Rdf
-            # each. The tensor cores execute more: each of the three GEMMs with
-            # an fp32 operand (dY for dW2, dZ for dX_perm and dW1) runs on its
-            # bf16 split hi + lo, which doubles it; dH reads the bf16 dout rows
-            # with the routing weight applied after the sum (16Rdf executed)
-            algo = 10.0 * R * cfg.d * cfg.f
-            executed = 16.0 * R * cfg.d * cfg.f
+            # the method's own work: four expert GEMMs (and Z, when it is
+            # recomputed), 2Rdf each. The tensor cores execute more: each of
+            # the three GEMMs with an fp32 operand (dY for dW2, dZ for dX_perm
+            # and dW1) runs on its bf16 split hi + lo, which doubles it; dH
+            # reads the bf16 dout rows with the routing weight applied after
+            # the sum (14Rdf executed, 16Rdf with Z recomputed)
+            algo = (8.0 + nz) * R * cfg.d * cfg.f
+            executed = (14.0 + nz) * R * cfg.d * cfg.f
             t_s = b_ms / 1e3
             broof = {"bound": "tensor", "achieved": algo / t_s / 1e12,
                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -589,11 +624,16 @@ def run_ours(args, cfg):
                     "executed_flops": executed,
                     "executed_tflops": executed / t_s / 1e12,
                     "executed_frac": executed / t_s / 1e12 / peaks["bf16_tflops"]}
-            note = ("achieved = the method's expert-GEMM flops (10 R d f: Z recomputed, dH, "
-                    "dX_perm, dW1, dW2) over the whole backward time; executed_* count the "
-                    "tensor-core flops actually run (the hi/lo operand split doubles three "
-                    "GEMMs: 16 R d f); the gate's fp32 FMA work is simt_flops")
+            note = ("achieved = the method's expert-GEMM flops (" +
+                    ("8 R d f: dH, dX_perm, dW1, dW2; Z kept by the forward" if kept else
+                     "10 R d f: Z recomputed, dH, dX_perm, dW1, dW2") +
+                    ") over the whole backward time; executed_* count the tensor-core flops "
+                    "actually run (the hi/lo operand split doubles three GEMMs: " +
+                    ("14" if kept else "16") + " R d f); the gate's fp32 FMA work is simt_flops")
         bwd = {"ms_per_step": b_ms, "tokens_per_s": cfg.T * world / (b_ms / 1e3),
+               "z": "kept by the forward (keep_z)" if kept else "recomputed",
+               "forward_keep_z_ms_per_step": fwd_z_ms,
+               "training_step_ms": (fwd_z_ms + b_ms) if kept else (ms_per_step + b_ms),
                "roofline": broof, "simt_flops": gate if cfg.dtype != "f32" else None,
                "note": note}
 

@@ -131,6 +131,15 @@ typedef struct moe_config {
                         * article). Gathering takes bf16 layers without an FP8
                         * payload or soft gating; asking for it elsewhere is
                         * MOE_ERR_UNSUPPORTED. The stage calls always pack. */
+  int32_t keep_z;      /* 1: moe_forward also keeps the W1 GEMM's pre-activation
+                        * Z = X_e W1_e [T k, f] (fp32, the value SiLU takes) in
+                        * its workspace (moe_workspace_size grows by T k f 4
+                        * bytes), and moe_backward, given the same config,
+                        * reads it there instead of recomputing it. For a
+                        * forward followed by a backward (training); not
+                        * with an FP8 payload (those have no backward):
+                        * MOE_ERR_UNSUPPORTED. Other values than 0 and 1:
+                        * MOE_ERR_INVALID_ARG */
 } moe_config_t;
 
 enum {
@@ -311,6 +320,7 @@ typedef struct moe_forward_views {
   int32_t* counts; int32_t* offsets; int32_t* pos; int32_t* src;
   void* x_perm; float* x_scale; void* h; float* y_perm;
   uint8_t* y_q; float* y_scale; float* y_zero;  /* NULL unless output_fp8 */
+  float* z;                                     /* NULL unless keep_z */
 } moe_forward_views_t;
 MOE_API int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* views);
 
@@ -324,11 +334,13 @@ MOE_API int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_vie
  *        set for MOE_ROUTER_PREK_SOFTMAX; over all experts, / tau, for
  *        soft gating); no gradient flows through the choice itself
  *   dW_g = x^T dL   db = sum_t dL   dx = dL W_g^T + sum_j dX_perm[pos(t,j)]
- *   per expert e: Z = X_e W1_e (recomputed), dW2_e = H_e^T dY_e,
+ *   per expert e: Z = X_e W1_e (recomputed, or kept by the forward with
+ *   keep_z), dW2_e = H_e^T dY_e,
  *   dZ = (dY_e W2_e^T) * SiLU'(Z), dW1_e = X_e^T dZ, dX_perm = dZ W1_e^T
  * x, W_g, bias, noise, W1, W2: the forward's inputs, unchanged. fwd_ws: the
  * workspace of that moe_forward call (>= moe_workspace_size bytes; its
- * routing, permutation, x_perm, H and Y are read, not changed). Outputs,
+ * routing, permutation, x_perm, H, Y and, with keep_z, Z are read, not
+ * changed; keep_z must be the same on both calls). Outputs,
  * fp32, overwritten: dx [T, d], dW_g [d, E], dbias [E] (nullable), dW1 [E,
  * d, f], dW2 [E, f, d]; an expert with no rows gets zero gradients. ws: >=
  * moe_backward_workspace_size bytes, 256-byte aligned; its first word is

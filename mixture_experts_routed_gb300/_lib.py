@@ -34,7 +34,8 @@ class MoeConfig(ctypes.Structure):
                                              ("output_fp8", ctypes.c_int32),
                                              ("tau", ctypes.c_float),
                                              ("gemm_tile_n", ctypes.c_int32),
-                                             ("x_perm_mode", ctypes.c_int32)]
+                                             ("x_perm_mode", ctypes.c_int32),
+                                             ("keep_z", ctypes.c_int32)]
 
 
 class MoeForwardViews(ctypes.Structure):
@@ -44,7 +45,7 @@ class MoeForwardViews(ctypes.Structure):
                 ("x_perm", ctypes.c_void_p), ("x_scale", ctypes.c_void_p),
                 ("h", ctypes.c_void_p), ("y_perm", ctypes.c_void_p),
                 ("y_q", ctypes.c_void_p), ("y_scale", ctypes.c_void_p),
-                ("y_zero", ctypes.c_void_p)]
+                ("y_zero", ctypes.c_void_p), ("z", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p

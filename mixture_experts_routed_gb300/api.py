@@ -29,25 +29,26 @@ class MoEError(RuntimeError):
 
 def make_config(T, d, E, k, f, dtype="bf16", router=L.MOE_ROUTER_RENORM, pre_k=8,
                 payload_fp8=0, n_group=1, topk_group=1, payload_scale=0.0,
-                output_fp8=0, tau=1.0, gemm_tile_n=0, x_perm_mode=0) -> L.MoeConfig:
+                output_fp8=0, tau=1.0, gemm_tile_n=0, x_perm_mode=0, keep_z=0) -> L.MoeConfig:
     dt = {"f32": L.MOE_DTYPE_F32, "fp32": L.MOE_DTYPE_F32, "bf16": L.MOE_DTYPE_BF16,
           torch.float32: L.MOE_DTYPE_F32, torch.bfloat16: L.MOE_DTYPE_BF16}[dtype]
     return L.MoeConfig(int(T), int(d), int(E), int(k), int(f), dt, int(router), int(pre_k),
                        int(payload_fp8), int(n_group), int(topk_group), float(payload_scale),
-                       int(output_fp8), float(tau), int(gemm_tile_n), int(x_perm_mode))
+                       int(output_fp8), float(tau), int(gemm_tile_n), int(x_perm_mode),
+                       int(keep_z))
 
 
 def config_from(c) -> L.MoeConfig:
     """From any object with T, d, E, k, f, dtype, router, pre_k, payload_fp8
     (and, optionally, n_group, topk_group, payload_scale, output_fp8, tau,
-    gemm_tile_n, x_perm_mode)."""
+    gemm_tile_n, x_perm_mode, keep_z)."""
     if isinstance(c, L.MoeConfig):
         return c
     return make_config(c.T, c.d, c.E, c.k, c.f, c.dtype, c.router, c.pre_k, c.payload_fp8,
                        getattr(c, "n_group", 1), getattr(c, "topk_group", 1),
                        getattr(c, "payload_scale", 0.0), getattr(c, "output_fp8", 0),
                        getattr(c, "tau", 1.0), getattr(c, "gemm_tile_n", 0),
-                       getattr(c, "x_perm_mode", 0))
+                       getattr(c, "x_perm_mode", 0), getattr(c, "keep_z", 0))
 
 
 def _cfg(c):
@@ -282,6 +283,7 @@ def forward_views(c, ws) -> dict:
         "y_q": view(v.y_q, R * cc.d, torch.uint8, (R, cc.d)) if cc.output_fp8 else None,
         "y_scale": view(v.y_scale, R, torch.float32, (R,)) if cc.output_fp8 else None,
         "y_zero": view(v.y_zero, R, torch.float32, (R,)) if cc.output_fp8 else None,
+        "z": view(v.z, R * cc.f, torch.float32, (R, cc.f)) if cc.keep_z else None,
     }
 
 

@@ -182,13 +182,16 @@ cudaError_t launch_combine_fp8(int dtype, const uint8_t* yq, const float* ys, co
 // tile width), 256 or 512 (forced; the fp8 token rows always take 256).
 // gather_src non-null (epi 0, bf16, not a_shared): A is x [a_rows, K] and
 // routed row r reads x row gather_src[r] (no packed copy of the rows).
+// zout non-null (epi 0): the pre-activation Z [R, N] (fp32, after the row
+// scale: the value SiLU takes) is written too.
 // Bound of the grouped GEMM epilogue's wait for a finished accumulator in
 // later launches (0: the default kWaitLimitNs); a test hook.
 void set_gemm_epilogue_wait_ns(uint64_t ns);
 cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
                            const void* W, int E, int K, int N, const int32_t* offsets,
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
-                           const int32_t* gather_src, int tile_n, int num_sms, cudaStream_t s);
+                           const int32_t* gather_src, int tile_n, int num_sms, cudaStream_t s,
+                           float* zout = nullptr);
 
 // ---------------------------------------------------------------- backward.cu
 // The backward pass's kernels (dtype 0 = fp32, 1 = bf16 for the tensors the
@@ -253,8 +256,9 @@ cudaError_t launch_undispatch(const float* dxg, const float* dxp, const int32_t*
 
 // ---------------------------------------------------------------- gemm_simt.cu
 // The same grouped GEMM in fp32 FMA for fp32 layers.
+// zout (epi 0, nullable): the pre-activation Z [R, N] is written too.
 cudaError_t launch_gemm_simt(int epi, const float* A, int a_shared, int R, const float* W, int E,
                              int K, int N, const int32_t* offsets, float* out, uint32_t* err,
-                             cudaStream_t s);
+                             cudaStream_t s, float* zout = nullptr);
 
 }  // namespace moe

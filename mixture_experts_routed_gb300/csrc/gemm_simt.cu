@@ -3,7 +3,8 @@
 // Same contract as the tensor-core kernel: for every expert e, rows
 // [offsets[e], offsets[e+1]) of A (or, shared, rows 0.. of A for every
 // expert) times W[e] (K x N, row-major), with
-//   epi 0: out = SiLU(acc)   epi 1: out = acc
+//   epi 0: out = SiLU(acc) (and zout = acc when zout is non-null)
+//   epi 1: out = acc
 // CTA tile 64 x 64, K step 16, 256 threads with 4 x 4 outputs each. The grid
 // covers an upper bound of the m-tiles; each CTA finds its (expert, m-tile)
 // from the offsets and exits if it has none.
@@ -23,7 +24,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
                                                         int K, int N,
                                                         const int32_t* __restrict__ offsets,
                                                         float* __restrict__ out,
-                                                        uint32_t* __restrict__ err) {
+                                                        uint32_t* __restrict__ err,
+                                                        float* __restrict__ zout) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN];
   __shared__ int s_e, s_row0, s_row1, s_lo;
@@ -101,7 +103,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
       const int n = n0 + tx * 4 + j;
       if (n >= N) continue;
       float v = acc[i][j];
-      if (EPI == 0) v = v / (1.f + expf(-v));
+      if (EPI == 0) {
+        if (zout != nullptr) zout[static_cast<size_t>(row0 + r) * N + n] = v;
+        v = v / (1.f + expf(-v));
+      }
       out[static_cast<size_t>(row0 + r) * N + n] = v;
     }
   }
@@ -111,11 +116,11 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const float* __restrict_
 
 cudaError_t launch_gemm_simt(int epi, const float* A, int a_shared, int R, const float* W, int E,
                              int K, int N, const int32_t* offsets, float* out, uint32_t* err,
-                             cudaStream_t s) {
+                             cudaStream_t s, float* zout) {
   if (R == 0) return cudaSuccess;
   const dim3 grid(ceil_div(R, BM) + E, ceil_div(N, BN)), block(256);
   return launch_pdl(epi == 0 ? gemm_simt_kernel<0> : gemm_simt_kernel<1>, grid, block, 0, s, A,
-                    a_shared, R, W, E, K, N, offsets, out, err);
+                    a_shared, R, W, E, K, N, offsets, out, err, epi == 0 ? zout : nullptr);
 }
 
 }  // namespace moe

@@ -85,6 +85,8 @@ struct TcParams {
   const int32_t* offsets;
   const float* row_scale;
   const float* zin;    // epi 2: the pre-activation Z [R, N] (fp32)
+  float* zout;         // epi 0, nullable: also write the pre-activation Z [R, N]
+                       // (fp32, the value SiLU takes), for a backward pass
   void* out;
   uint32_t* err;
   uint32_t* tile_ctr;  // next tile to hand out; zero before the launch
@@ -838,6 +840,15 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
           }
           if (!valid) continue;
           if constexpr (EPI == 0) {
+            if (!A8 && p.zout != nullptr) {  // (no backward for FP8 rows)
+              float4* zd = reinterpret_cast<float4*>(p.zout + grow * p.N + col);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                zd[i] = make_float4(__uint_as_float(v[4 * i]) * scale,
+                                    __uint_as_float(v[4 * i + 1]) * scale,
+                                    __uint_as_float(v[4 * i + 2]) * scale,
+                                    __uint_as_float(v[4 * i + 3]) * scale);
+            }
             uint32_t packed[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -899,9 +910,11 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
 #pragma unroll
               for (int jj = 0; jj < 32; ++jj) {
                 const float sj = __shfl_sync(0xffffffffu, my_scale, jj);
-                if (jj < t.tail && f_ok)
-                  out[static_cast<size_t>(jj) * p.N] =
-                      __float2bfloat16_rn(silu(__uint_as_float(v[jj]) * sj));
+                if (jj < t.tail && f_ok) {
+                  const float z = __uint_as_float(v[jj]) * sj;
+                  if (!A8 && p.zout != nullptr) p.zout[base + static_cast<size_t>(jj) * p.N] = z;
+                  out[static_cast<size_t>(jj) * p.N] = __float2bfloat16_rn(silu(z));
+                }
               }
             } else if constexpr (EPI == 2) {
               __nv_bfloat16* out =
@@ -953,9 +966,11 @@ __global__ void __launch_bounds__(pairk::num_threads<EPI, NB, A8, GA>(), 1)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               const float sj = __shfl_sync(0xffffffffu, my_scale, jj);
-              if (jj < nt && f_ok)
-                out[static_cast<size_t>(jj) * p.N] =
-                    __float2bfloat16_rn(silu(__uint_as_float(v[jj]) * sj));
+              if (jj < nt && f_ok) {
+                const float z = __uint_as_float(v[jj]) * sj;
+                if (!A8 && p.zout != nullptr) p.zout[base + static_cast<size_t>(jj) * p.N] = z;
+                out[static_cast<size_t>(jj) * p.N] = __float2bfloat16_rn(silu(z));
+              }
             }
           } else if constexpr (EPI == 2) {
             const size_t r0 = static_cast<size_t>(t.row0) + tok0;
@@ -1392,7 +1407,8 @@ void set_gemm_epilogue_wait_ns(uint64_t ns) { g_epi_wait_ns.store(ns == 0 ? kWai
 cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_shared, int R,
                            const void* W, int E, int K, int N, const int32_t* offsets,
                            const float* row_scale, void* out, uint32_t* err, uint32_t* tile_ctr,
-                           const int32_t* gather_src, int tile_n, int num_sms, cudaStream_t s) {
+                           const int32_t* gather_src, int tile_n, int num_sms, cudaStream_t s,
+                           float* zout) {
   if (R == 0) return cudaSuccess;
   if (num_sms < 2 || (a_fp8 && epi != 0)) return cudaErrorInvalidValue;
   if (tile_n != 0 && tile_n != 256 && tile_n != 512) return cudaErrorInvalidValue;
@@ -1431,6 +1447,7 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
   prm.offsets = offsets;
   prm.row_scale = row_scale;
   prm.zin = nullptr;
+  prm.zout = epi == 0 ? zout : nullptr;
   prm.out = out;
   prm.err = err;
   prm.tile_ctr = tile_ctr;
@@ -1485,6 +1502,7 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
   prm.offsets = offsets;
   prm.row_scale = zin ? row_scale : nullptr;
   prm.zin = zin;
+  prm.zout = nullptr;
   prm.out = out;
   prm.err = err;
   prm.tile_ctr = tile_ctr;

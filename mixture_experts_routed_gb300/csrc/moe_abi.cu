@@ -53,6 +53,9 @@ int check_cfg(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   if (c->x_perm_mode < MOE_XPERM_AUTO || c->x_perm_mode > MOE_XPERM_GATHERED)
     return MOE_ERR_INVALID_ARG;
+  if (c->keep_z != 0 && c->keep_z != 1) return MOE_ERR_INVALID_ARG;
+  // Z is kept for the backward, which the FP8 payloads do not have
+  if (c->keep_z && (c->payload_fp8 || c->output_fp8)) return MOE_ERR_UNSUPPORTED;
   // gathered rows: bf16 rows of x, no FP8 payload, not soft gating (which
   // reads x itself already)
   if (c->x_perm_mode == MOE_XPERM_GATHERED &&
@@ -85,7 +88,7 @@ bool gathers(const moe_config_t& c) {
 struct Layout {
   size_t err, hist, base, scratch_end;
   size_t topk_idx, topk_w, counts, offsets, pos, src, x_perm, x_scale, h, y, y_q, y_scale,
-      y_zero, total;
+      y_zero, z, total;
   int nchunk;
 };
 
@@ -119,6 +122,7 @@ Layout layout_of(const moe_config_t& c) {
   L.y_q = take(c.output_fp8 ? R * c.d : 0);
   L.y_scale = take(c.output_fp8 ? R * 4 : 0);
   L.y_zero = take(c.output_fp8 ? R * 4 : 0);
+  L.z = take(c.keep_z ? R * c.f * 4 : 0);  // the pre-activation, for a backward
   L.total = o;
   return L;
 }
@@ -185,10 +189,12 @@ int run_dispatch(const moe_config_t& c, const Layout& L, void* ws, const void* x
 }
 
 // which 1: the W1 pass, reading x_perm, or (gather_src non-null) x itself
-// through the routed rows' tokens; which 2: the W2 pass.
+// through the routed rows' tokens, and writing the pre-activation to zout
+// too when it is non-null; which 2: the W2 pass.
 int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const void* x_perm,
              const float* x_scale, const int32_t* offsets, const void* W1, const void* W2,
-             void* h, float* y, cudaStream_t s, const int32_t* gather_src = nullptr) {
+             void* h, float* y, cudaStream_t s, const int32_t* gather_src = nullptr,
+             float* zout = nullptr) {
   const int R = c.T * c.k;
   if (R == 0) return MOE_OK;
   uint32_t* err = at<uint32_t>(ws, L.err);
@@ -196,7 +202,7 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
     if (which == 1)
       return status_of(launch_gemm_simt(0, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
                                         static_cast<const float*>(W1), c.E, c.d, c.f, offsets,
-                                        static_cast<float*>(h), err, s));
+                                        static_cast<float*>(h), err, s, zout));
     return status_of(launch_gemm_simt(1, static_cast<const float*>(h), 0, R,
                                       static_cast<const float*>(W2), c.E, c.f, c.d, offsets, y,
                                       err, s));
@@ -211,7 +217,7 @@ int run_gemm(const moe_config_t& c, const Layout& L, void* ws, int which, const 
     return status_of(launch_gemm_tc(0, x_perm, c.payload_fp8 ? 1 : 0,
                                     soft(c) || gather_src ? c.T : R, soft(c) ? 1 : 0, R, W1, c.E,
                                     c.d, c.f, offsets, c.payload_fp8 ? x_scale : nullptr, h, err,
-                                    ctr, gather_src, c.gemm_tile_n, sms, s));
+                                    ctr, gather_src, c.gemm_tile_n, sms, s, zout));
   }
   return status_of(launch_gemm_tc(1, h, 0, R, 0, R, W2, c.E, c.f, c.d, offsets, nullptr, y, err,
                                   ctr, nullptr, c.gemm_tile_n, sms, s));
@@ -262,8 +268,9 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
     return st;
   record(events, 2, s);
   record(events, 3, s);  // (no kernel: the FP8 payload is expanded inside the W1 GEMM)
+  // keep_z: the W1 pass also leaves the pre-activation Z in the workspace
   if ((st = run_gemm(c, L, ws, 1, ga ? x : x_perm, x_scale, offsets, W1, W2, h, y, s,
-                     ga ? src : nullptr)) != MOE_OK)
+                     ga ? src : nullptr, c.keep_z ? at<float>(ws, L.z) : nullptr)) != MOE_OK)
     return st;
   record(events, 4, s);
   if ((st = run_gemm(c, L, ws, 2, x_perm, x_scale, offsets, W1, W2, h, y, s)) != MOE_OK)
@@ -291,7 +298,8 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // The backward workspace: an error word and the GEMM tile counters, then the
 // recomputed logits (and the route call's unused top-k), dw, dL, the single
 // segment {0, T} of the gate GEMMs, dY (fp32 layers), the recomputed
-// pre-activation Z (fp32 layers overwrite it with dZ), dX_perm and the gate
+// pre-activation Z (fp32 layers overwrite it with dZ; with keep_z, bf16
+// layers read the forward's and fp32 layers copy it), dX_perm and the gate
 // part of dx, all fp32 but the ints; bf16 layers add the tensor-core GEMMs'
 // operands: the bf16 splits of dY, dZ and dL, and per routed row its token's
 // dout row (hard routers) and its routing weight.
@@ -348,7 +356,9 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.bpart = take(nch * E * 4);
   B.gpart = take(tc ? nch * E * static_cast<size_t>(c.d) * 4 : 0);
   B.dY = take(tc ? 0 : R * c.d * 4);  // fp32 layers (bf16 ones keep only the split)
-  B.Z = take(R * c.f * 4);
+  // Z: recomputed here, or kept by the forward (keep_z) and read there;
+  // fp32 layers turn it into dZ in place, so they always hold a copy
+  B.Z = take(c.keep_z && tc ? 0 : R * c.f * 4);
   B.dXp = take(R * c.d * 4);
   B.dxg = take(T * c.d * 4);
   B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
@@ -397,7 +407,9 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   float* dL = at<float>(bws, B.dL);
   int32_t* seg01 = at<int32_t>(bws, B.seg01);
   float* dY = at<float>(bws, B.dY);
-  float* Z = at<float>(bws, B.Z);
+  // keep_z: the forward left Z in its workspace (read-only here)
+  const bool kept = c.keep_z != 0;
+  float* Z = kept && c.dtype == MOE_DTYPE_BF16 ? at<float>(fws, L.z) : at<float>(bws, B.Z);
   float* dXp = at<float>(bws, B.dXp);
   float* dxg = at<float>(bws, B.dxg);
   const int dt = c.dtype;
@@ -456,18 +468,22 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   if (e == cudaSuccess)
     e = launch_reduce_partials(gpart, wg_parts, static_cast<size_t>(d) * E, dWg, bpart, b_parts,
                                static_cast<size_t>(E), dbias, s);
-  // experts: Z = X_e W1_e again (fp32), dZ = (dY W2_e^T) * SiLU'(Z) over Z,
+  // experts: Z = X_e W1_e again (fp32; with keep_z the forward's), dZ =
+  // (dY W2_e^T) * SiLU'(Z) over Z,
   // dW2 = H^T dY, dW1 = X^T dZ, dX_perm = dZ W1_e^T. bf16 layers run every
   // expert GEMM on the tensor cores (dY and dZ split into bf16 hi + lo; for
   // the dgrad GEMMs the weights transposed and stacked twice along K); fp32
   // layers run them in fp32 FMA.
   if (e == cudaSuccess) {
     if (!tc) {
-      e = launch_gemm_simt(1, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
-                           static_cast<const float*>(W1), E, d, f, offsets, Z, err, s);
+      e = kept ? cudaMemcpyAsync(Z, at<float>(fws, L.z), static_cast<size_t>(R) * f * 4,
+                                 cudaMemcpyDeviceToDevice, s)
+               : launch_gemm_simt(1, static_cast<const float*>(x_perm), soft(c) ? 1 : 0, R,
+                                  static_cast<const float*>(W1), E, d, f, offsets, Z, err, s);
     } else {
-      e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f, offsets,
-                         nullptr, Z, err, ctr, nullptr, c.gemm_tile_n, sms, s);
+      if (!kept)
+        e = launch_gemm_tc(1, x_perm, 0, soft(c) ? T : R, soft(c) ? 1 : 0, R, W1, E, d, f,
+                           offsets, nullptr, Z, err, ctr, nullptr, c.gemm_tile_n, sms, s);
       // dH[r] = w_r (dout[t(r)] . W2_e^T): row r's routing weight comes out of
       // the sum, so the GEMM reads the exact bf16 dout rows (K = d; soft
       // gating: dout itself, every expert reading all T rows) and its
@@ -648,6 +664,7 @@ int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_views_t* v)
   v->y_q = cfg->output_fp8 ? at<uint8_t>(ws, L.y_q) : nullptr;
   v->y_scale = cfg->output_fp8 ? at<float>(ws, L.y_scale) : nullptr;
   v->y_zero = cfg->output_fp8 ? at<float>(ws, L.y_zero) : nullptr;
+  v->z = cfg->keep_z ? at<float>(ws, L.z) : nullptr;
   return MOE_OK;
 }
 

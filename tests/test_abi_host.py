@@ -55,7 +55,7 @@ def test_only_abi_symbols_are_exported(lib):
 def cfg(**kw):
     base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0,
                 n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0, tau=0.0,
-                gemm_tile_n=0, x_perm_mode=0)
+                gemm_tile_n=0, x_perm_mode=0, keep_z=0)
     base.update(kw)
     return L.MoeConfig(*[base[n] for n, _ in L.MoeConfig._fields_])
 
@@ -130,6 +130,15 @@ def cfg(**kw):
     (dict(router=4), L.MOE_ERR_INVALID_ARG),
     (dict(payload_fp8=1, dtype=0), L.MOE_ERR_UNSUPPORTED),
     (dict(T=1 << 30, k=8), L.MOE_ERR_UNSUPPORTED),
+    # the forward keeps Z for the backward: not with an FP8 payload
+    (dict(keep_z=1), L.MOE_OK),
+    (dict(keep_z=1, dtype=0), L.MOE_OK),
+    (dict(keep_z=1, router=3, E=8, k=8, tau=1.0), L.MOE_OK),
+    (dict(keep_z=1, x_perm_mode=2), L.MOE_OK),
+    (dict(keep_z=2), L.MOE_ERR_INVALID_ARG),
+    (dict(keep_z=-1), L.MOE_ERR_INVALID_ARG),
+    (dict(keep_z=1, payload_fp8=1), L.MOE_ERR_UNSUPPORTED),
+    (dict(keep_z=1, output_fp8=1), L.MOE_ERR_UNSUPPORTED),
 ])
 def test_check_config(lib, kw, status):
     c = cfg(**kw)
@@ -181,6 +190,28 @@ def test_workspace_sizes(lib):
     assert lib.moe_workspace_size(ctypes.byref(ck)) - lib.moe_workspace_size(ctypes.byref(cs)) \
         >= Rs * 4096 * 2
     assert lib.moe_forward_kernel_count(ctypes.byref(cs)) == 5
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_keep_z_workspaces(lib, dtype):
+    # keep_z: the forward workspace holds Z (R*f fp32 more, aligned); a bf16
+    # backward then reads it there and its own workspace drops the R*f fp32
+    # of the recomputed Z, while an fp32 backward keeps it (dZ is formed in
+    # place over a copy); the kernel count of the forward is unchanged
+    c = cfg(T=1024, d=4096, E=8, k=2, f=11008, dtype=dtype)
+    cz = cfg(T=1024, d=4096, E=8, k=2, f=11008, dtype=dtype, keep_z=1)
+    R, f = 1024 * 2, 11008
+    dws = lib.moe_workspace_size(ctypes.byref(cz)) - lib.moe_workspace_size(ctypes.byref(c))
+    assert R * f * 4 <= dws <= R * f * 4 + 256
+    assert lib.moe_scratch_size(ctypes.byref(cz)) == lib.moe_scratch_size(ctypes.byref(c))
+    assert lib.moe_forward_kernel_count(ctypes.byref(cz)) == \
+        lib.moe_forward_kernel_count(ctypes.byref(c))
+    dbw = lib.moe_backward_workspace_size(ctypes.byref(c)) - \
+        lib.moe_backward_workspace_size(ctypes.byref(cz))
+    if dtype == 1:
+        assert R * f * 4 <= dbw <= R * f * 4 + 256
+    else:
+        assert dbw == 0
 
 
 FAKE = ctypes.c_void_p(0x100000)       # never dereferenced: validation fails first

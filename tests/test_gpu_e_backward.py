@@ -132,6 +132,58 @@ def test_backward_full_layer(cuda_ok, name):
     print(f"{name}: experts compared {sorted(pick)}")
 
 
+def _fwd_bwd(cfg, inp, dout):
+    ws = moe.alloc_workspace(cfg)
+    out = moe.forward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws,
+                      noise=inp.get("gumbel"))
+    bws = moe.alloc_workspace(cfg, "backward")
+    g = moe.backward(cfg, inp["x"], inp["Wg"], inp["bias"], inp["W1"], inp["W2"], dout,
+                     fwd_ws=ws, ws=bws, noise=inp.get("gumbel"))
+    torch.cuda.synchronize()
+    assert moe.get_device_error(bws) == moe.MOE_OK
+    assert moe.get_device_error(ws) == moe.MOE_OK
+    return out, moe.forward_views(cfg, ws), g
+
+
+def _check_keep_z(cfg, rows_mode=0):
+    """keep_z: the forward's output and H are the same bits, its Z is X_e W1_e
+    (fp32 summation against the oracle's fp64), and the backward that reads
+    it gives the same bits as the one that recomputes Z."""
+    base = cfg.with_(x_perm_mode=rows_mode)
+    inp = make_inputs(base, device="cuda")
+    dout = _dout(base)
+    out0, v0, g0 = _fwd_bwd(base, inp, dout)
+    out1, v1, g1 = _fwd_bwd(base.with_(keep_z=1), inp, dout)
+    assert v0["z"] is None and v1["z"] is not None
+    assert torch.equal(out0, out1)
+    assert torch.equal(v0["h"], v1["h"])
+    for n in g0:
+        assert torch.equal(g0[n], g1[n]), n
+    host = oracle.inputs_to_numpy(inp)
+    off = v1["offsets"].cpu().numpy()
+    src = v1["src"].cpu().numpy()
+    z = _host(v1["z"])
+    ref = np.zeros_like(z)
+    for e in range(cfg.E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            ref[lo:hi] = host["x"][src[lo:hi]] @ oracle.moe_oracle._expert(host["W1"], e)
+    _close(z, ref, 1e-5, "Z")
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_keep_z_matches_recompute(cuda_ok, name):
+    _check_keep_z(SHAPES[name])
+
+
+# the 256-expert layer's shape at 2048 tokens: 512-feature W1 tiles, merged
+# and swapped remainders; packed and gathered rows (the gathered W1 pass
+# writes Z from the same epilogue)
+@pytest.mark.parametrize("rows_mode", [1, 2])
+def test_keep_z_matches_recompute_full_layer(cuda_ok, rows_mode):
+    _check_keep_z(get_config("skewed_small_T2048_d7168_E32_k8_f2048_zipf"), rows_mode)
+
+
 def test_backward_is_bitwise_reproducible(cuda_ok):
     cfg = SHAPES["bwd_prek_T200_d256_E64_k2_f128"]
     _, _, _, g1 = _run(cfg)

@@ -60,6 +60,7 @@ class MoEConfig:
     tau: float = 1.0          # soft gating temperature
     gemm_tile_n: int = 0      # expert GEMM pair-tile width: 0 = the library's choice, 256, 512
     x_perm_mode: int = 0      # 0 = the library's choice, 1 = packed rows, 2 = gathered by the W1 GEMM
+    keep_z: int = 0           # 1: the forward keeps the pre-activation Z for the backward
     bias: str = "zero"        # "zero" | "normal" (variance bias_var) | "zipf" (exponent zipf_s)
     bias_var: float = 0.0
     zipf_s: float = 0.0
