@@ -184,6 +184,46 @@ def test_keep_z_matches_recompute_full_layer(cuda_ok, rows_mode):
     _check_keep_z(get_config("skewed_small_T2048_d7168_E32_k8_f2048_zipf"), rows_mode)
 
 
+# a training step (the forward keeping Z, then the backward) captured in one
+# CUDA graph: no host synchronisation inside either call; replays give the
+# eager results bit for bit, also after a new batch is copied into the
+# captured input buffer
+@pytest.mark.parametrize("name", ["bwd_bf16_T129_d256_E8_k2_f320", "bwd_f32_T50_d64_E5_k2_f128",
+                                  "bwd_soft_T100_d256_E8_f128"])
+def test_training_step_in_cuda_graph(cuda_ok, name):
+    cfg = SHAPES[name].with_(keep_z=1)
+    inp = make_inputs(cfg, device="cuda")
+    dout = _dout(cfg)
+    out0, _, g0 = _fwd_bwd(cfg, inp, dout)
+    x = inp["x"].clone()
+    ws = moe.alloc_workspace(cfg)
+    bws = moe.alloc_workspace(cfg, "backward")
+    out = torch.empty_like(out0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        moe.forward(cfg, x, inp["Wg"], inp["bias"], inp["W1"], inp["W2"], ws=ws, out=out,
+                    noise=inp.get("gumbel"), stream=s)
+        grads = moe.backward(cfg, x, inp["Wg"], inp["bias"], inp["W1"], inp["W2"], dout,
+                             fwd_ws=ws, ws=bws, noise=inp.get("gumbel"), stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out0)
+    for n in g0:
+        assert torch.equal(grads[n], g0[n]), n
+    x2 = torch.flip(inp["x"], dims=[0]).contiguous()
+    x.copy_(x2)
+    graph.replay()
+    torch.cuda.synchronize()
+    out1, _, g1 = _fwd_bwd(cfg, dict(inp, x=x2), dout)
+    assert torch.equal(out, out1)
+    for n in g1:
+        assert torch.equal(grads[n], g1[n]), n
+    assert moe.get_device_error(bws) == moe.MOE_OK
+    assert moe.get_device_error(ws) == moe.MOE_OK
+
+
 def test_backward_is_bitwise_reproducible(cuda_ok):
     cfg = SHAPES["bwd_prek_T200_d256_E64_k2_f128"]
     _, _, _, g1 = _run(cfg)
