@@ -176,6 +176,17 @@ def test_keep_z_matches_recompute(cuda_ok, name):
     _check_keep_z(SHAPES[name])
 
 
+# merged remainder tiles (256-feature tiles: 270 rows per expert, a 14-row
+# remainder; 257 rows, a 1-row remainder), packed and gathered rows: the
+# epilogue's remainder path writes Z too
+@pytest.mark.parametrize("rows_mode", [1, 2])
+@pytest.mark.parametrize("name", ["merged_tail_T270_d256_E2_k2_f320",
+                                  "merged_tail_T257_d128_E1_k1_f256"])
+def test_keep_z_merged_tail_tiles(cuda_ok, name, rows_mode):
+    from gpu_layers import SMALL
+    _check_keep_z(SMALL[name].with_(gemm_tile_n=256), rows_mode)
+
+
 # the 256-expert layer's shape at 2048 tokens: 512-feature W1 tiles, merged
 # and swapped remainders; packed and gathered rows (the gathered W1 pass
 # writes Z from the same epilogue)
