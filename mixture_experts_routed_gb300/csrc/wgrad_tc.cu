@@ -28,11 +28,16 @@
 // swizzle) is 64 contraction rows of 64 consecutive m (or n), so the
 // transposes cost nothing. Per block and CTA: A 16 KB, hi 16 KB, lo 16 KB.
 //
-// Rows of the last block past the expert's end are whatever follows in
-// memory (the next expert's rows, or the TMA's zero fill past the matrix).
-// Each CTA's loads land on its own barrier; a forwarder warp waits for
-// them, overwrites those rows with zeros in the staged tiles (row j of a box
-// is its 128-byte line j; the swizzle permutes within the line), and
+// A block whose valid rows are a whole number of 16-row k-steps (every block
+// but an expert's last, and that one when its row count is a multiple of
+// 16) needs nothing done to it: both CTAs' loads complete directly on the
+// even CTA's full barrier (the pair form of the TMA load), which the even
+// CTA's producer arms for both CTAs' bytes. In an expert's last block
+// otherwise, rows of its last k-step past the expert's end are whatever
+// follows in memory (the next expert's rows, or the TMA's zero fill past
+// the matrix): each CTA's loads then land on its own barrier, a forwarder
+// warp overwrites those rows with zeros in the staged tiles (row j of a box
+// is its 128-byte line j; the swizzle permutes within the line) and
 // releases the stage to the MMA: the even CTA's by an arrive on the full
 // barrier, the odd CTA's by a 16-byte bulk copy into the even CTA whose
 // completion is counted on that barrier (a cluster-scope release arrive per
@@ -112,6 +117,12 @@ __device__ __forceinline__ Tile decode(int t, const Params& p) {
   r.m0 = mb * BM;
   r.n0 = (l - mb * p.tiles_n) * BN;
   return r;
+}
+
+// A block that goes through the forwarder: its last k-step holds rows past
+// the expert's end.
+__device__ __forceinline__ bool needs_zeroing(int n, int kb) {
+  return (min(BK, n - kb * BK) & 15) != 0;
 }
 
 // Ring position over the k-blocks of a CTA's tiles (every role walks the
@@ -195,46 +206,76 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       Ring rg;
-      uint32_t armed = 0, armed_ph = 0;
+      const uint32_t leader_full = mapa_shared(smem_u32(full), 0);
+      // lfull[s] completes once per forwarded block in stage s: its phase
+      // parity per stage, and the parity of the last such use to drain
+      uint32_t lph = 0, larmed = 0, larmed_ph = 0;
+      // 64-wide boxes of CTA r's halves that start inside the matrix (M a
+      // multiple of 64); the MMA's rows / columns from a skipped box, or
+      // from a box's part past N, are never stored
+      auto boxes_a = [&](const Tile& tl, int r) {
+        const int mh = tl.m0 + r * 128;
+        return mh < p.M ? min(2, (p.M - mh) / 64) : 0;
+      };
+      auto boxes_b = [&](const Tile& tl, int r) {
+        const int nh = tl.n0 + r * 128;
+        return nh < p.N ? min(2, (p.N - nh + 63) / 64) : 0;
+      };
       for (int t = cl; t < p.total && !timed_out; t += ncl) {
         const Tile tl = decode(t, p);
         const int n = rows_of(tl.e);
         if (n == 0) continue;
         const int lo = seg[tl.e];
         const int a0 = p.a_shared ? 0 : lo;
-        // this CTA's halves: 64-wide boxes that start inside the matrix (M a
-        // multiple of 64); the MMA's rows / columns from a skipped box, or
-        // from a box's part past N, are never stored
         const int mh = tl.m0 + static_cast<int>(rank) * 128;
         const int nh = tl.n0 + static_cast<int>(rank) * 128;
-        const int na = mh < p.M ? min(2, (p.M - mh) / 64) : 0;
-        const int nb = nh < p.N ? min(2, (p.N - nh + 63) / 64) : 0;
+        const int na = boxes_a(tl, static_cast<int>(rank));
+        const int nb = boxes_b(tl, static_cast<int>(rank));
         const uint32_t bytes = static_cast<uint32_t>((na + 2 * nb) * BOX_BYTES);
+        // both CTAs' bytes, counted on the even CTA's full barrier
+        const uint32_t pair_bytes = static_cast<uint32_t>(
+            (boxes_a(tl, 0) + 2 * boxes_b(tl, 0) + boxes_a(tl, 1) + 2 * boxes_b(tl, 1)) *
+            BOX_BYTES);
         const int nkb = (n + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_spin(&empty[rg.s], rg.ph ^ 1u, kWaitLimitNs)) {
             timed_out = true;
             break;
           }
-          uint64_t* bar = &lfull[rg.s];
-          mbar_arrive_expect_tx(bar, bytes);
           uint8_t* st = smem + rg.s * STAGE_BYTES;
-          for (int c = 0; c < na; ++c)
-            tma_load_2d(st + c * BOX_BYTES, &tmA, bar, mh + c * 64, a0 + kb * BK);
-          for (int c = 0; c < nb; ++c) {
-            tma_load_2d(st + HALF_BYTES + c * BOX_BYTES, &tmB, bar, nh + c * 64, lo + kb * BK);
-            tma_load_2d(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, bar, p.N + nh + c * 64,
-                        lo + kb * BK);
+          if (needs_zeroing(n, kb)) {
+            uint64_t* bar = &lfull[rg.s];
+            mbar_arrive_expect_tx(bar, bytes);
+            for (int c = 0; c < na; ++c)
+              tma_load_2d(st + c * BOX_BYTES, &tmA, bar, mh + c * 64, a0 + kb * BK);
+            for (int c = 0; c < nb; ++c) {
+              tma_load_2d(st + HALF_BYTES + c * BOX_BYTES, &tmB, bar, nh + c * 64, lo + kb * BK);
+              tma_load_2d(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, bar, p.N + nh + c * 64,
+                          lo + kb * BK);
+            }
+            larmed |= 1u << rg.s;
+            larmed_ph = (larmed_ph & ~(1u << rg.s)) | (lph & (1u << rg.s));
+            lph ^= 1u << rg.s;
+          } else {
+            if (rank == 0) mbar_arrive_expect_tx(&full[rg.s], pair_bytes);
+            const uint32_t bar = leader_full + static_cast<uint32_t>(rg.s * 8);
+            for (int c = 0; c < na; ++c)
+              tma_load_2d_pair(st + c * BOX_BYTES, &tmA, bar, mh + c * 64, a0 + kb * BK);
+            for (int c = 0; c < nb; ++c) {
+              tma_load_2d_pair(st + HALF_BYTES + c * BOX_BYTES, &tmB, bar, nh + c * 64,
+                               lo + kb * BK);
+              tma_load_2d_pair(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, bar, p.N + nh + c * 64,
+                               lo + kb * BK);
+            }
           }
-          armed |= 1u << rg.s;
-          armed_ph = (armed_ph & ~(1u << rg.s)) | (rg.ph << rg.s);
           rg.next();
         }
       }
-      // no copy may still be landing when the CTA exits
+      // no copy may still be landing when the CTA exits (the direct ones are
+      // counted on the even CTA's full barriers, which its forwarder drains)
       for (int i = 0; i < STAGES; ++i)
-        if ((armed >> i) & 1u)
-          if (!mbar_wait_spin(&lfull[i], (armed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
+        if ((larmed >> i) & 1u)
+          if (!mbar_wait_spin(&lfull[i], (larmed_ph >> i) & 1u, kWaitLimitNs)) timed_out = true;
     }
   } else if (warp == 1) {
     if (rank == 0) {
@@ -255,7 +296,8 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
         const int nkb = (n + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
-          // released by both CTAs' forwarders (the odd one's bytes at cluster scope)
+          // both CTAs' bytes landed (direct), or released by both CTAs'
+          // forwarders (the odd one's bytes at cluster scope)
           if (!__all_sync(0xffffffffu,
                           mbar_wait_spin_cluster(&full[rg.s], rg.ph, kWaitLimitNs))) {
             timed_out = true;
@@ -301,13 +343,22 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
     const uint32_t my_sink = smem_u32(smem + OFF_SINK);
     Ring rg;
     uint32_t armed = 0, armed_ph = 0;
+    uint32_t lph = 0;  // lfull's phase parity per stage (forwarded blocks only)
     for (int t = cl; t < p.total && !timed_out; t += ncl) {
       const Tile tl = decode(t, p);
       const int n = rows_of(tl.e);
       if (n == 0) continue;
       const int nkb = (n + BK - 1) / BK;
       for (int kb = 0; kb < nkb; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait_spin(&lfull[rg.s], rg.ph, kWaitLimitNs))) {
+        armed |= 1u << rg.s;
+        armed_ph = (armed_ph & ~(1u << rg.s)) | (rg.ph << rg.s);
+        if (!needs_zeroing(n, kb)) {  // loaded straight onto the even CTA's full barrier
+          rg.next();
+          continue;
+        }
+        const uint32_t want = (lph >> rg.s) & 1u;
+        lph ^= 1u << rg.s;
+        if (!__all_sync(0xffffffffu, mbar_wait_spin(&lfull[rg.s], want, kWaitLimitNs))) {
           timed_out = true;
           break;
         }
@@ -332,12 +383,11 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
             bulk_copy_s2cluster(leader_sink, my_sink, 16u,
                                 leader_full + static_cast<uint32_t>(rg.s * 8));
         }
-        armed |= 1u << rg.s;
-        armed_ph = (armed_ph & ~(1u << rg.s)) | (rg.ph << rg.s);
         rg.next();
       }
     }
-    // even CTA: the odd CTA's release copies have landed before either exits
+    // even CTA: every stage's bytes (both CTAs' direct loads, the odd CTA's
+    // release copies) have landed before either CTA exits
     if (rank == 0)
       for (int i = 0; i < STAGES; ++i)
         if ((armed >> i) & 1u)
