@@ -150,9 +150,11 @@ cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const 
                                   int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
                                   void* x_perm, float* x_scale, uint32_t* err, uint32_t* zero,
                                   int nzero, cudaStream_t s);
-// x_perm[r] = x[src[r]] for the R routed rows (d elements of dtype each).
-cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* src, int T, int R, int d,
-                               void* x_perm, uint32_t* err, cudaStream_t s);
+// x_perm[pos[t k + j]] = x[t] for every token and slot (rows of d elements
+// of dtype; the dispatch's layout, k <= kMaxTopK); entries with pos outside
+// [0, T k) are skipped.
+cudaError_t launch_scatter_rows(int dtype, const void* x, const int32_t* pos, int T, int k,
+                                int d, void* x_perm, cudaStream_t s);
 // Soft gating's layout (every token to every expert, token order): counts,
 // offsets, pos, src; zeroes `nzero` words at `zero` when non-null.
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,

@@ -496,26 +496,43 @@ __global__ void __launch_bounds__(256) dense_layout_kernel(int T, int E, int32_t
   }
 }
 
-// x_perm[r] = x[src[r]] for r < R (rows of `row_bytes`, a multiple of 16):
-// one warp per row, 16-byte vectors. A src outside [0, T) flags
-// kErrBadIndex and leaves the row unwritten.
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x,
-                                                          const int32_t* __restrict__ src, int T,
-                                                          long long R, int vecs,
-                                                          uint4* __restrict__ x_perm,
-                                                          uint32_t* __restrict__ err) {
+// x_perm[pos[t k + j]] = x[t] for every token t and slot j < k (rows of
+// `vecs` 16-byte vectors): one warp per token reads its row once, four
+// vectors per lane in flight, and writes them to each of the token's k
+// routed rows (reading x once per routed row instead moved k times the
+// bytes). A pos outside [0, R) (the dispatch's mark of an entry it
+// dropped) is skipped.
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restrict__ x,
+                                                           const int32_t* __restrict__ pos, int T,
+                                                           int k, long long R, int vecs,
+                                                           uint4* __restrict__ x_perm) {
   pdl_wait();
   pdl_trigger();
-  const long long r = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (r >= R) return;
-  const int t = __ldg(src + r);
-  if (t < 0 || t >= T) {
-    if ((threadIdx.x & 31) == 0) atomicOr(err, kErrBadIndex);
-    return;
+  const long long t = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  int p[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    p[j] = j < k ? __ldg(pos + t * k + j) : -1;
+    if (p[j] >= R) p[j] = -1;
   }
   const uint4* a = x + static_cast<size_t>(t) * vecs;
-  uint4* b = x_perm + static_cast<size_t>(r) * vecs;
-  for (int v = threadIdx.x & 31; v < vecs; v += 32) b[v] = __ldg(a + v);
+  constexpr int U = 4;
+  for (int v0 = lane; v0 < vecs; v0 += 32 * U) {
+    uint4 val[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (v0 + 32 * u < vecs) val[u] = __ldg(a + v0 + 32 * u);
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (p[j] < 0) continue;
+      uint4* b = x_perm + static_cast<size_t>(p[j]) * vecs;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + 32 * u < vecs) b[v0 + 32 * u] = val[u];
+    }
+  }
 }
 
 // Rows copied by bulk copies through shared memory: plain (not FP8) rows of
@@ -602,13 +619,14 @@ cudaError_t launch_dispatch_fused(int dtype, int fp8, float static_scale, const 
                     static_scale, err, zero, nzero, bulk);
 }
 
-cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* src, int T, int R, int d,
-                               void* x_perm, uint32_t* err, cudaStream_t s) {
-  if (R <= 0) return cudaSuccess;
+cudaError_t launch_scatter_rows(int dtype, const void* x, const int32_t* pos, int T, int k,
+                                int d, void* x_perm, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (k < 1 || k > kMaxTopK) return cudaErrorInvalidValue;
   const int vecs = d * (dtype == 0 ? 4 : 2) / 16;
-  return launch_pdl(gather_rows_kernel, dim3(ceil_div(R, 8)), dim3(256), 0, s,
-                    static_cast<const uint4*>(x), src, T, static_cast<long long>(R), vecs,
-                    static_cast<uint4*>(x_perm), err);
+  return launch_pdl(scatter_rows_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s,
+                    static_cast<const uint4*>(x), pos, T, k,
+                    static_cast<long long>(T) * k, vecs, static_cast<uint4*>(x_perm));
 }
 
 cudaError_t launch_dense_layout(int T, int E, int32_t* counts, int32_t* offsets, int32_t* pos,

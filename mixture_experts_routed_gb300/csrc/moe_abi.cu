@@ -431,8 +431,9 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
   const TokChunks ch = tok_chunks(c, sms);
   int32_t* segk = at<int32_t>(bws, B.segk);
   uint32_t* ctr = at<uint32_t>(bws, kGemmCounterOffset);  // four tile counters
-  cudaError_t e = gathers(c) ? launch_gather_rows(dt, x, at<int32_t>(fws, L.src), T, R, d,
-                                                  at<void>(bws, B.xp), err, s)
+  // (gathered forward) the packed rows dW1 reads, written token by token
+  // through the forward's layout: each x row read once, written k times
+  cudaError_t e = gathers(c) ? launch_scatter_rows(dt, x, pos, T, k, d, at<void>(bws, B.xp), s)
                              : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
