@@ -32,9 +32,11 @@ __device__ __forceinline__ void pdl_trigger() {
 // 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. 4) a second
 // one then gives the correctly rounded quotient: once q is within one ulp,
 // the residual is exact. The callers take this path only for s in
-// [2^-64, 2^64] (y normal). The theorem wants a normal residual; where it is
-// subnormal the quotient is below 2^-100, far under the first E4M3 rounding
-// boundary (2^-10), and the sign of x is kept, so the E4M3 code is the same.
+// [2^-64, 2^64] (y normal). The theorem wants no underflow: for quotients
+// of magnitude 2^-11 or more the exact residual x - s q is a multiple of
+// ulp(s) ulp(q) >= 2^-121, so normal or zero; smaller quotients lie below
+// the first E4M3 rounding boundary (2^-10), where the code is +-0 whatever
+// their last bits, and the sign of x is kept.
 // CLAMP: quotients of magnitude above 1024 (the first product says so to
 // within 2^-22) saturate to +-448 in E4M3 either way and are returned as
 // +-1024, which keeps the corrections away from overflow; without it the
