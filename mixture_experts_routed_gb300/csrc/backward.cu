@@ -62,13 +62,15 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t* hi, uint32_t*
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA of 128 threads per token: the k rows of dY and the k dot products
+// One CTA of 128 threads per token: the k rows of dY (or, bf16 layers, the
+// split of dY or of w H), the dout rows, and the k dot products
 // (warp butterflies, then the 4 warp partials in warp order).
 template <typename Tout>
 __global__ void __launch_bounds__(128) combine_bwd_kernel(
     const Tout* __restrict__ dout, const float* __restrict__ y, const int32_t* __restrict__ pos,
     const float* __restrict__ w, int T, int d, int k, int R, float* __restrict__ dY,
-    __nv_bfloat16* __restrict__ dYs, Tout* __restrict__ doutp, float* __restrict__ wr,
+    __nv_bfloat16* __restrict__ dYs, const __nv_bfloat16* __restrict__ h, int f,
+    __nv_bfloat16* __restrict__ hs, Tout* __restrict__ doutp, float* __restrict__ wr,
     float* __restrict__ dw, uint32_t* __restrict__ err,
     uint32_t* __restrict__ zero, int nzero, int32_t* __restrict__ seg01,
     int32_t* __restrict__ segk, int nsegk, int chunk) {
@@ -112,6 +114,18 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
         part = fmaf(g.y, yv.y, part);
         part = fmaf(g.z, yv.z, part);
         part = fmaf(g.w, yv.w, part);
+      }
+    }
+    if (ok && hs != nullptr) {
+      // H'[p] = w H[p] split for the tensor-core weight gradient dW2 =
+      // sum_r H'_r^T dout_r (bf16 parts v = hi + lo to ~2^-17, [R][2f])
+      for (int c = tid * 4; c < f; c += 512) {
+        const float4 hv = ld_f32x4(h, static_cast<size_t>(p) * f + c);
+        uint2 hi, lo;
+        split2(wt * hv.x, wt * hv.y, &hi.x, &lo.x);
+        split2(wt * hv.z, wt * hv.w, &hi.y, &lo.y);
+        *reinterpret_cast<uint2*>(hs + static_cast<size_t>(p) * 2 * f + c) = hi;
+        *reinterpret_cast<uint2*>(hs + static_cast<size_t>(p) * 2 * f + f + c) = lo;
       }
     }
 #pragma unroll
@@ -516,20 +530,23 @@ __global__ void __launch_bounds__(128) undispatch_kernel(const float* __restrict
 
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
-                               void* doutp, float* wr, float* dw, uint32_t* err, uint32_t* zero,
-                               int nzero, int32_t* seg01, int32_t* segk, int nsegk, int chunk,
-                               cudaStream_t s) {
+                               const void* h, int f, void* hs, void* doutp, float* wr, float* dw,
+                               uint32_t* err, uint32_t* zero, int nzero, int32_t* seg01,
+                               int32_t* segk, int nsegk, int chunk, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  if (hs != nullptr && (dtype != 1 || h == nullptr || f % 4 != 0)) return cudaErrorInvalidValue;
   __nv_bfloat16* ys = static_cast<__nv_bfloat16*>(dYs);
+  const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
+  __nv_bfloat16* hsb = static_cast<__nv_bfloat16*>(hs);
   if (dtype == 0)
     return launch_pdl(combine_bwd_kernel<float>, dim3(T), dim3(128), 0, s,
-                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, ys,
+                      static_cast<const float*>(dout), y, pos, w, T, d, k, R, dY, ys, hb, f, hsb,
                       static_cast<float*>(doutp), wr, dw, err, zero, nzero, seg01, segk, nsegk,
                       chunk);
   return launch_pdl(combine_bwd_kernel<__nv_bfloat16>, dim3(T), dim3(128), 0, s,
-                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys,
-                    static_cast<__nv_bfloat16*>(doutp), wr, dw, err, zero, nzero, seg01, segk,
-                    nsegk, chunk);
+                    static_cast<const __nv_bfloat16*>(dout), y, pos, w, T, d, k, R, dY, ys, hb,
+                    f, hsb, static_cast<__nv_bfloat16*>(doutp), wr, dw, err, zero, nzero, seg01,
+                    segk, nsegk, chunk);
 }
 
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,

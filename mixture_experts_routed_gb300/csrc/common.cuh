@@ -200,17 +200,19 @@ cudaError_t launch_gemm_tc(int epi, const void* A, int a_fp8, int a_rows, int a_
 // ---------------------------------------------------------------- backward.cu
 // The backward pass's kernels (dtype 0 = fp32, 1 = bf16 for the tensors the
 // forward takes; every gradient and intermediate is fp32).
-// dY[pos(t,j)] = w[t,j] dout[t] (when dY is non-null; when dYs is, its bf16 split
-// [R][2d] = [hi | lo]); dw[t,j] = <dout[t], Y[pos(t,j)]>; also zeroes `nzero`
+// dY[pos(t,j)] = w[t,j] dout[t] (when dY is non-null; when dYs is, its bf16
+// split [R][2d] = [hi | lo]); hs (bf16 layers, nullable): for p = pos(t,j),
+// the bf16 split [R][2f] of w[t,j] h[p] (h the forward's H [R][f]);
+// dw[t,j] = <dout[t], Y[pos(t,j)]>; also zeroes `nzero`
 // words at `zero`, writes seg01 = {0, T} and, when segk is non-null, the
 // token chunks segk[i] = min(i chunk, T), i = 0 .. nsegk (nsegk < 128).
 // doutp, wr (nullable): per routed row p = pos(t, j), dout[t] (the layer's dtype,
 // bit for bit) and w[t, j].
 cudaError_t launch_combine_bwd(int dtype, const void* dout, const float* y, const int32_t* pos,
                                const float* w, int T, int d, int k, int R, float* dY, void* dYs,
-                               void* doutp, float* wr, float* dw, uint32_t* err, uint32_t* zero,
-                               int nzero, int32_t* seg01, int32_t* segk, int nsegk, int chunk,
-                               cudaStream_t s);
+                               const void* h, int f, void* hs, void* doutp, float* wr, float* dw,
+                               uint32_t* err, uint32_t* zero, int nzero, int32_t* seg01,
+                               int32_t* segk, int nsegk, int chunk, cudaStream_t s);
 // dL [T, E] from dw through the router's softmax Jacobian (mode as RouterSpec),
 // and, when dLs is non-null, its bf16 split [T][2E] = [hi | lo].
 cudaError_t launch_router_bwd(const float* L, const int32_t* idx, const float* w, const float* dw,
@@ -244,6 +246,12 @@ cudaError_t launch_gemm_tc_wt(const void* A, int R, const void* Wt, int E, int K
 cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void* Bs, int R, int E,
                             int M, int N, const int32_t* offsets, float* out, uint32_t* err,
                             int num_sms, cudaStream_t s);
+// The same with the split on A: out[e] = (As_e[:, :M] + As_e[:, M:])^T . B_e,
+// As bf16 [R, 2M] (hi | lo), B bf16 [b_rows, N], B row r of expert e's
+// segment (or r - offsets[e] with b_shared).
+cudaError_t launch_wgrad_tc_split_a(const void* As, int R, const void* B, int b_rows,
+                                    int b_shared, int E, int M, int N, const int32_t* offsets,
+                                    float* out, uint32_t* err, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_tn(int adtype, const void* A, int a_shared, const float* B, int E, int R,
                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
                            cudaStream_t s);

@@ -301,10 +301,18 @@ int forward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const f
 // pre-activation Z (fp32 layers overwrite it with dZ; with keep_z, bf16
 // layers read the forward's and fp32 layers copy it), dX_perm and the gate
 // part of dx, all fp32 but the ints; bf16 layers add the tensor-core GEMMs'
-// operands: the bf16 splits of dY, dZ and dL, and per routed row its token's
-// dout row (hard routers) and its routing weight.
+// operands: the bf16 splits of dY (or, when 2f <= d, of w H: per routed row
+// its routing weight times its H row), dZ and dL, and per routed row its
+// token's dout row (hard routers) and its routing weight.
+// bf16 layers: dW2 takes the routing weight on its H side, splitting w H
+// ([R][2f]) instead of dY ([R][2d]), where that operand is at most half as
+// wide (measured on GB300, same box: 256-expert layer, d = 3.5 f, backward
+// 25.36 -> 24.67 ms; the balanced and 64-expert layers, f > d / 2, were
+// 1.32 -> 1.36 and 1.02 -> 1.04 ms the other way)
+bool split_h(const moe_config_t& c) { return 2 * static_cast<long long>(c.f) <= c.d; }
+
 struct BwdLayout {
-  size_t err, L, ridx, rw, dw, dL, seg01, segk, bpart, gpart, dY, Z, dXp, dxg, dYs, dZs, dLs,
+  size_t err, L, ridx, rw, dw, dL, seg01, segk, bpart, gpart, dY, Z, dXp, dxg, dYs, hs, dZs, dLs,
       doutp, wr, xp, total;
 };
 
@@ -361,7 +369,8 @@ BwdLayout bwd_layout_of(const moe_config_t& c) {
   B.Z = take(c.keep_z && tc ? 0 : R * c.f * 4);
   B.dXp = take(R * c.d * 4);
   B.dxg = take(T * c.d * 4);
-  B.dYs = take(tc ? R * 2 * c.d * 2 : 0);
+  B.dYs = take(tc && !split_h(c) ? R * 2 * c.d * 2 : 0);
+  B.hs = take(tc && split_h(c) ? R * 2 * c.f * 2 : 0);
   B.dZs = take(tc ? R * 2 * c.f * 2 : 0);
   B.dLs = take(tc ? T * 2 * E * 2 : 0);
   B.doutp = take(tc && !soft(c) ? R * c.d * 2 : 0);
@@ -437,7 +446,9 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
                              : cudaSuccess;
   if (e == cudaSuccess)
     e = launch_combine_bwd(dt, dout, y, pos, w, T, d, k, R, tc ? nullptr : dY,
-                           tc ? at<void>(bws, B.dYs) : nullptr,
+                           tc && !split_h(c) ? at<void>(bws, B.dYs) : nullptr,
+                           tc && split_h(c) ? h : nullptr, f,
+                           tc && split_h(c) ? at<void>(bws, B.hs) : nullptr,
                            tc && !soft(c) ? at<void>(bws, B.doutp) : nullptr,
                            tc ? at<float>(bws, B.wr) : nullptr, dw, err, ctr, 4, seg01, segk,
                            ch.n, ch.len, s);
@@ -501,9 +512,17 @@ int backward_impl(const moe_config_t* cfg, const void* x, const void* Wg, const 
     }
   }
   if (e == cudaSuccess && tc) {
-    // weight gradients on the tensor cores: dW2 = H^T (dY hi + lo),
-    // dW1 = X^T (dZ hi + lo), contracted over each expert's rows
-    e = launch_wgrad_tc(h, R, 0, at<void>(bws, B.dYs), R, E, f, d, offsets, dW2, err, sms, s);
+    // weight gradients on the tensor cores, contracted over each expert's
+    // rows: dW2 = sum_r H_r^T dY_r with dY_r = w_r dout[t(r)]: H^T (dY hi +
+    // lo), or, when 2f <= d, (w H hi + lo)^T . the bf16 dout rows (the split
+    // on the narrower operand; soft gating: dout itself, every expert
+    // reading all T rows); dW1 = X^T (dZ hi + lo)
+    e = split_h(c) ? launch_wgrad_tc_split_a(at<void>(bws, B.hs), R,
+                                             soft(c) ? dout : at<void>(bws, B.doutp),
+                                             soft(c) ? T : R, soft(c) ? 1 : 0, E, f, d, offsets,
+                                             dW2, err, sms, s)
+                   : launch_wgrad_tc(h, R, 0, at<void>(bws, B.dYs), R, E, f, d, offsets, dW2, err,
+                                     sms, s);
     if (e == cudaSuccess)
       e = launch_wgrad_tc(x_perm, soft(c) ? T : R, soft(c) ? 1 : 0, at<void>(bws, B.dZs), R, E, d,
                           f, offsets, dW1, err, sms, s);

@@ -7,19 +7,23 @@
 //   dW[e][m][n] = sum over r in [offsets[e], offsets[e+1]) of A[a(r)][m] * dB[r][n]
 //
 // with A the rows' bf16 activations (the dispatched tokens for dW1, the
-// stored SiLU output H for dW2, the layer input for the gate's dW_g; a(r) =
-// r, or r - offsets[e] when every expert reads the same rows) and dB their
-// fp32 output gradient, held as two bf16 parts dB = hi + lo ([R][2N]:
-// columns [0, N) hi, [N, 2N) lo; hi + lo carries dB to ~2^-17 relative).
-// Both parts go through the tensor cores into one fp32 accumulator, so the
-// result has the accuracy of an fp32 operand. Output fp32 [E][M][N]; an
-// expert with no rows gets zeros.
+// layer input for the gate's dW_g; a(r) = r, or r - offsets[e] when every
+// expert reads the same rows) and dB their fp32 output gradient, held as
+// two bf16 parts dB = hi + lo ([R][2N]: columns [0, N) hi, [N, 2N) lo; hi +
+// lo carries dB to ~2^-17 relative). Or the other way round (split A): for
+// dW2 = sum_r (w_r H_r)^T dout_r the fp32 operand is A' = w H, split into
+// [R][2M], and B the bf16 dout rows (per routed row; or dout itself, b(r) =
+// r - offsets[e], when every expert reads the same rows). Both parts go
+// through the tensor cores into one fp32 accumulator, so the result has the
+// accuracy of an fp32 operand. Output fp32 [E][M][N]; an expert with no rows
+// gets zeros.
 //
 // Tiles: 256 output rows (m) x 256 output columns (n) of one expert, computed
 // by a cluster of two CTAs (one per SM of an SM pair) with one
 // tcgen05.mma.cta_group::2 M256 N256 K16 per k-step and operand part, issued
 // by the even CTA. CTA r stages only rows m0 + 128 r .. +127 of A and
-// columns n0 + 128 r .. +127 of hi and of lo, and its tensor memory receives
+// columns n0 + 128 r .. +127 of B, each operand's split one twice (hi and
+// lo), and its tensor memory receives
 // its 128 output rows; per SM this is half the shared-memory traffic per flop
 // of a one-CTA 128 x 128 tile (measured bound by that traffic). The
 // contraction runs over the expert's rows in blocks of 64 (ragged: the last
@@ -101,6 +105,7 @@ struct Params {
   uint32_t* err;
   int E, M, N, R;
   int a_shared;
+  int b_shared;  // B row of routed row r: r - offsets[e] (split A only)
   int tiles_m, tiles_n, total;
 };
 
@@ -139,6 +144,9 @@ struct Ring {
 };
 }  // namespace wg
 
+// SPLIT_A: A is the split operand ([R][2M]) and B single ([rows][N]);
+// otherwise A single ([rows][M]) and B split ([R][2N])
+template <bool SPLIT_A>
 __global__ void __launch_bounds__(wg::THREADS, 1)
     wgrad_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
@@ -227,15 +235,32 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
         if (n == 0) continue;
         const int lo = seg[tl.e];
         const int a0 = p.a_shared ? 0 : lo;
+        const int b0 = p.b_shared ? 0 : lo;
         const int mh = tl.m0 + static_cast<int>(rank) * 128;
         const int nh = tl.n0 + static_cast<int>(rank) * 128;
         const int na = boxes_a(tl, static_cast<int>(rank));
         const int nb = boxes_b(tl, static_cast<int>(rank));
-        const uint32_t bytes = static_cast<uint32_t>((na + 2 * nb) * BOX_BYTES);
+        // the split operand's boxes count twice
+        auto cta_bytes = [&](int a, int b) {
+          return static_cast<uint32_t>((SPLIT_A ? 2 * a + b : a + 2 * b) * BOX_BYTES);
+        };
+        const uint32_t bytes = cta_bytes(na, nb);
         // both CTAs' bytes, counted on the even CTA's full barrier
-        const uint32_t pair_bytes = static_cast<uint32_t>(
-            (boxes_a(tl, 0) + 2 * boxes_b(tl, 0) + boxes_a(tl, 1) + 2 * boxes_b(tl, 1)) *
-            BOX_BYTES);
+        const uint32_t pair_bytes =
+            cta_bytes(boxes_a(tl, 0), boxes_b(tl, 0)) + cta_bytes(boxes_a(tl, 1), boxes_b(tl, 1));
+        // stage slots: A (or A hi) | B (or B hi) | the split operand's lo
+        auto load_stage = [&](uint8_t* st, int kb, auto load) {
+          for (int c = 0; c < na; ++c) load(st + c * BOX_BYTES, &tmA, mh + c * 64, a0 + kb * BK);
+          for (int c = 0; c < nb; ++c)
+            load(st + HALF_BYTES + c * BOX_BYTES, &tmB, nh + c * 64, b0 + kb * BK);
+          if constexpr (SPLIT_A) {
+            for (int c = 0; c < na; ++c)
+              load(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmA, p.M + mh + c * 64, a0 + kb * BK);
+          } else {
+            for (int c = 0; c < nb; ++c)
+              load(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, p.N + nh + c * 64, b0 + kb * BK);
+          }
+        };
         const int nkb = (n + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_spin(&empty[rg.s], rg.ph ^ 1u, kWaitLimitNs)) {
@@ -246,27 +271,18 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
           if (needs_zeroing(n, kb)) {
             uint64_t* bar = &lfull[rg.s];
             mbar_arrive_expect_tx(bar, bytes);
-            for (int c = 0; c < na; ++c)
-              tma_load_2d(st + c * BOX_BYTES, &tmA, bar, mh + c * 64, a0 + kb * BK);
-            for (int c = 0; c < nb; ++c) {
-              tma_load_2d(st + HALF_BYTES + c * BOX_BYTES, &tmB, bar, nh + c * 64, lo + kb * BK);
-              tma_load_2d(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, bar, p.N + nh + c * 64,
-                          lo + kb * BK);
-            }
+            load_stage(st, kb, [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1) {
+              tma_load_2d(dst, m, bar, c0, c1);
+            });
             larmed |= 1u << rg.s;
             larmed_ph = (larmed_ph & ~(1u << rg.s)) | (lph & (1u << rg.s));
             lph ^= 1u << rg.s;
           } else {
             if (rank == 0) mbar_arrive_expect_tx(&full[rg.s], pair_bytes);
             const uint32_t bar = leader_full + static_cast<uint32_t>(rg.s * 8);
-            for (int c = 0; c < na; ++c)
-              tma_load_2d_pair(st + c * BOX_BYTES, &tmA, bar, mh + c * 64, a0 + kb * BK);
-            for (int c = 0; c < nb; ++c) {
-              tma_load_2d_pair(st + HALF_BYTES + c * BOX_BYTES, &tmB, bar, nh + c * 64,
-                               lo + kb * BK);
-              tma_load_2d_pair(st + 2 * HALF_BYTES + c * BOX_BYTES, &tmB, bar, p.N + nh + c * 64,
-                               lo + kb * BK);
-            }
+            load_stage(st, kb, [&](uint8_t* dst, const CUtensorMap* m, int c0, int c1) {
+              tma_load_2d_pair(dst, m, bar, c0, c1);
+            });
           }
           rg.next();
         }
@@ -307,13 +323,17 @@ __global__ void __launch_bounds__(wg::THREADS, 1)
             tc_fence_after();
             const int ksteps = (min(BK, n - kb * BK) + 15) / 16;
             const uint32_t a_base = smem_u32(smem + rg.s * STAGE_BYTES);
-            const uint32_t h_base = a_base + HALF_BYTES, l_base = a_base + 2 * HALF_BYTES;
+            const uint32_t b_base = a_base + HALF_BYTES, l_base = a_base + 2 * HALF_BYTES;
             for (int kk = 0; kk < ksteps; ++kk) {
               const uint64_t ad = make_sdesc_sw128(a_base + kk * 2048, BOX_BYTES, 1024);
-              tc_mma_f16_pair(d_tmem, ad, make_sdesc_sw128(h_base + kk * 2048, BOX_BYTES, 1024),
-                              IDESC, (kb | kk) != 0 ? 1u : 0u);
-              tc_mma_f16_pair(d_tmem, ad, make_sdesc_sw128(l_base + kk * 2048, BOX_BYTES, 1024),
-                              IDESC, 1u);
+              const uint64_t bd = make_sdesc_sw128(b_base + kk * 2048, BOX_BYTES, 1024);
+              const uint64_t ld = make_sdesc_sw128(l_base + kk * 2048, BOX_BYTES, 1024);
+              // (A hi or A) x (B or B hi), then the lo part against the other
+              tc_mma_f16_pair(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+              if constexpr (SPLIT_A)
+                tc_mma_f16_pair(d_tmem, ld, bd, IDESC, 1u);
+              else
+                tc_mma_f16_pair(d_tmem, ad, ld, IDESC, 1u);
             }
             tc_commit_pair_mc(&empty[rg.s], 0x3);
           }
@@ -503,8 +523,11 @@ cudaError_t set_wgrad_smem_attr() {
   static std::once_flag once;
   static cudaError_t st = cudaSuccess;
   std::call_once(once, [] {
-    st = cudaFuncSetAttribute(wgrad_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              wg::SMEM_BYTES);
+    st = cudaFuncSetAttribute(wgrad_pair_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, wg::SMEM_BYTES);
+    if (st == cudaSuccess)
+      st = cudaFuncSetAttribute(wgrad_pair_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, wg::SMEM_BYTES);
   });
   return st;
 }
@@ -519,7 +542,8 @@ int resident_clusters(const cudaLaunchConfig_t& lc_in, int num_sms) {
   cudaLaunchConfig_t lc = lc_in;
   lc.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, wgrad_pair_kernel, &lc) != cudaSuccess || n <= 0) {
+  // (both forms: the same threads, registers within the launch bound and shared memory)
+  if (cudaOccupancyMaxActiveClusters(&n, wgrad_pair_kernel<false>, &lc) != cudaSuccess || n <= 0) {
     cudaGetLastError();
     n = num_sms / 2;
   }
@@ -529,20 +553,26 @@ int resident_clusters(const cudaLaunchConfig_t& lc_in, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void* Bs, int R, int E,
-                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
-                            int num_sms, cudaStream_t s) {
+namespace {
+// Either form: A [a_rows][M] single and B [R][2N] split, or (split_a) A
+// [R][2M] split and B [b_rows][N] single.
+cudaError_t launch_wgrad(const void* A, int a_rows, int a_shared, const void* B, int b_rows,
+                         int b_shared, int split_a, int R, int E, int M, int N,
+                         const int32_t* offsets, float* out, uint32_t* err, int num_sms,
+                         cudaStream_t s) {
   if (E <= 0) return cudaSuccess;
   if (M <= 0 || N <= 0 || M % 64 != 0 || N % 8 != 0 || num_sms < 2 || E > kMaxExperts)
     return cudaErrorInvalidValue;
-  if (R <= 0 || a_rows <= 0)  // no rows anywhere: every gradient is zero
+  if (R <= 0 || a_rows <= 0 || b_rows <= 0)  // no rows anywhere: every gradient is zero
     return cudaMemsetAsync(out, 0, static_cast<size_t>(E) * M * N * 4, s);
   CUtensorMap mA, mB, mY;
   std::memset(&mA, 0, sizeof(mA));
   std::memset(&mB, 0, sizeof(mB));
   std::memset(&mY, 0, sizeof(mY));
-  if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(M), 64, wg::BK) ||
-      !make_map_2d(&mB, Bs, static_cast<uint64_t>(R), 2 * static_cast<uint64_t>(N), 64, wg::BK) ||
+  const uint64_t a_cols = static_cast<uint64_t>(M) * (split_a ? 2 : 1);
+  const uint64_t b_cols = static_cast<uint64_t>(N) * (split_a ? 1 : 2);
+  if (!make_map_2d(&mA, A, static_cast<uint64_t>(a_rows), a_cols, 64, wg::BK) ||
+      !make_map_2d(&mB, B, static_cast<uint64_t>(b_rows), b_cols, 64, wg::BK) ||
       !make_map_2d_out(&mY, out, static_cast<uint64_t>(E) * M, static_cast<uint64_t>(N), true))
     return cudaErrorInvalidValue;
   wg::Params prm;
@@ -553,6 +583,7 @@ cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void*
   prm.N = N;
   prm.R = R;
   prm.a_shared = a_shared;
+  prm.b_shared = b_shared;
   prm.tiles_m = ceil_div(M, wg::BM);
   prm.tiles_n = ceil_div(N, wg::BN);
   prm.total = E * prm.tiles_m * prm.tiles_n;
@@ -574,7 +605,22 @@ cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void*
   const int resident = resident_clusters(lc, num_sms);
   const int clusters = prm.total < resident ? prm.total : resident;
   lc.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-  return cudaLaunchKernelEx(&lc, wgrad_pair_kernel, mA, mB, mY, prm);
+  return split_a ? cudaLaunchKernelEx(&lc, wgrad_pair_kernel<true>, mA, mB, mY, prm)
+                 : cudaLaunchKernelEx(&lc, wgrad_pair_kernel<false>, mA, mB, mY, prm);
+}
+}  // namespace
+
+cudaError_t launch_wgrad_tc(const void* A, int a_rows, int a_shared, const void* Bs, int R, int E,
+                            int M, int N, const int32_t* offsets, float* out, uint32_t* err,
+                            int num_sms, cudaStream_t s) {
+  return launch_wgrad(A, a_rows, a_shared, Bs, R, 0, 0, R, E, M, N, offsets, out, err, num_sms, s);
+}
+
+cudaError_t launch_wgrad_tc_split_a(const void* As, int R, const void* B, int b_rows,
+                                    int b_shared, int E, int M, int N, const int32_t* offsets,
+                                    float* out, uint32_t* err, int num_sms, cudaStream_t s) {
+  return launch_wgrad(As, R, 0, B, b_rows, b_shared, 1, R, E, M, N, offsets, out, err, num_sms,
+                      s);
 }
 
 }  // namespace moe
