@@ -610,10 +610,10 @@ def run_ours(args, cfg):
         else:
             # the method's own work: four expert GEMMs (and Z, when it is
             # recomputed), 2Rdf each. The tensor cores execute more: each of
-            # the three GEMMs with an fp32 operand (dY for dW2, dZ for dX_perm
-            # and dW1) runs on its bf16 split hi + lo, which doubles it; dH
-            # reads the bf16 dout rows with the routing weight applied after
-            # the sum (14Rdf executed, 16Rdf with Z recomputed)
+            # the three GEMMs with an fp32 operand (dY or w H for dW2, dZ for
+            # dX_perm and dW1) runs on its bf16 split hi + lo, which doubles
+            # it; dH reads the bf16 dout rows with the routing weight applied
+            # after the sum (14Rdf executed, 16Rdf with Z recomputed)
             algo = (8.0 + nz) * R * cfg.d * cfg.f
             executed = (14.0 + nz) * R * cfg.d * cfg.f
             t_s = b_ms / 1e3

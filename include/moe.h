@@ -349,11 +349,13 @@ MOE_API int moe_forward_views(const moe_config_t* cfg, void* ws, moe_forward_vie
  * MOE_ERR_UNSUPPORTED. Every tensor pointer (x, W_g, W1, W2, dout, dx,
  * dW_g, dW1, dW2) must be 16-byte aligned, else MOE_ERR_INVALID_ARG.
  * Precision: bf16 layers run the GEMMs on the tensor cores with each fp32
- * gradient operand (dY for dW2, dZ, dL) carried as two bf16 parts hi + lo
- * (~2^-17 relative) against the bf16 weights or activations, fp32
- * accumulation; dH takes the bf16 dout rows themselves, the routing weight
- * applied to the fp32 sum; fp32 layers use fp32 FMA. Every sum runs in a fixed order (no atomics):
- * the result is bitwise reproducible. Asynchronous on `stream`. */
+ * operand carried as two bf16 parts hi + lo (~2^-17 relative) against a
+ * bf16 one, fp32 accumulation: dZ and dL against the weights or inputs,
+ * and for dW2 either dY against H or, where 2f <= d, w H (each routed row's
+ * weight times its H row) against the dout rows; dH takes the bf16 dout
+ * rows themselves, the routing weight applied to the fp32 sum; fp32 layers
+ * use fp32 FMA. Every sum runs in a fixed order (no atomics): the result is
+ * bitwise reproducible. Asynchronous on `stream`. */
 MOE_API size_t moe_backward_workspace_size(const moe_config_t* cfg);
 MOE_API int moe_backward(const moe_config_t* cfg, const void* x, const void* W_g,
                  const float* bias, const float* noise, const void* W1, const void* W2,
