@@ -493,15 +493,19 @@ def run_ours(args, cfg):
         ev_fwd = [torch.cuda.Event() for _ in range(nb)]
         ev_down = [torch.cuda.Event() for _ in range(nb)]
 
-        def e2e_step(i):
+        def e2e_step(i, m=None):
             b = i % nb
             # upload into buffer b once the forward two steps back has read it
             if i >= nb:
                 up.wait_event(ev_fwd[b])
             with torch.cuda.stream(up):
+                if m is not None:
+                    m[0].record(up)
                 x_dev[b].copy_(x_host, non_blocking=True)
                 if g_host is not None:
                     g_dev[b].copy_(g_host, non_blocking=True)
+                if m is not None:
+                    m[1].record(up)
                 ev_up[b].record(up)
             stream.wait_event(ev_up[b])
             if i >= nb:
@@ -511,7 +515,11 @@ def run_ours(args, cfg):
             ev_fwd[b].record(stream)
             down.wait_event(ev_fwd[b])
             with torch.cuda.stream(down):
+                if m is not None:
+                    m[2].record(down)
                 o_host[b].copy_(o_dev[b], non_blocking=True)
+                if m is not None:
+                    m[3].record(down)
                 ev_down[b].record(down)
 
         for i in range(3):
@@ -521,18 +529,24 @@ def run_ours(args, cfg):
             dist.barrier()
         a = torch.cuda.Event(enable_timing=True)
         b_ev = torch.cuda.Event(enable_timing=True)
+        # copy start / end events of every timed step (the copy streams'
+        # own time, so a slow host link shows in the line)
+        cp = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
         a.record(stream)
         up.wait_event(a)
         for i in range(K):
-            e2e_step(i)
+            e2e_step(i, cp[i])
         stream.wait_event(ev_down[(K - 1) % nb])
         b_ev.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = max_over_ranks(a.elapsed_time(b_ev), dist, dev)
+        h2d_ms = sum(m[0].elapsed_time(m[1]) for m in cp) / K
+        d2h_ms = sum(m[2].elapsed_time(m[3]) for m in cp) / K
         e2e = {"value": cfg.T * world / (e_ms / K / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": x_host.numel() * x_host.element_size() + (
                    g_host.numel() * g_host.element_size() if g_host is not None else 0),
                "d2h_bytes_per_step": o_host[0].numel() * o_host[0].element_size(),
+               "h2d_ms_per_step": h2d_ms, "d2h_ms_per_step": d2h_ms,
                "pipelining": "uploads and downloads on two copy streams, double-buffered, "
                              "overlapping the neighbouring steps' forwards"}
 
