@@ -214,6 +214,28 @@ def test_keep_z_workspaces(lib, dtype):
         assert dbw == 0
 
 
+def test_backward_workspace_follows_the_dw2_split_side(lib):
+    # bf16 layers split dW2's fp32 operand on its narrower side: w H ([R][2f]
+    # bf16) where 2f <= d, else dY ([R][2d]); growing d by 64 then changes the
+    # backward workspace by the d-wide buffers only (dY's split when it is
+    # the one kept, dX_perm, the dout rows, dx_gate), not by the split of w H
+    T, E, k, f = 256, 8, 2, 128
+    R = T * k
+    def bws(d, dtype=1):
+        c = cfg(T=T, d=d, E=E, k=k, f=f, dtype=dtype)
+        return lib.moe_backward_workspace_size(ctypes.byref(c))
+    # d-wide bytes per unit of d: dX_perm R*4, dout rows R*2, dx_gate T*4,
+    # gate partials (token chunks * E * 4), and dY's split R*4 when kept
+    d0, d1 = 256, 320                       # 2f = 256 <= d: w H split
+    grow_h = bws(d1) - bws(d0)
+    d2, d3 = 128, 192                       # 2f = 256 > d: dY split
+    grow_y = bws(d3) - bws(d2)
+    # the dY split adds R * 2 * 2 bytes per unit of d on the second pair only
+    assert abs((grow_y - grow_h) - 64 * R * 4) <= 4 * 256
+    # fp32 layers keep fp32 dY whichever is narrower
+    assert bws(d1, 0) - bws(d0, 0) == bws(d3, 0) - bws(d2, 0)
+
+
 FAKE = ctypes.c_void_p(0x100000)       # never dereferenced: validation fails first
 FAKE_ODD = ctypes.c_void_p(0x100008)   # 8-byte aligned only
 
