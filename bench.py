@@ -275,6 +275,12 @@ def max_over_ranks(value, dist, device):
     return float(t.item())
 
 
+def error_on_any_rank(bad, dist, device):
+    """True on every rank when any rank saw a device error (a collective, so
+    that all ranks raise together and none is left waiting in the next one)."""
+    return max_over_ranks(1.0 if bad else 0.0, dist, device) > 0.0
+
+
 # ---------------------------------------------------------------- reference arm
 def reference_sample_tokens(cfg):
     """Tokens the reference arm runs per step: about 128 routed rows, so that
@@ -379,7 +385,7 @@ def run_ours(args, cfg):
     for _ in range(max(args.warmup, 3)):
         step()
     torch.cuda.synchronize(dev)
-    if moe.get_device_error(ws) != moe.MOE_OK:
+    if error_on_any_rank(moe.get_device_error(ws) != moe.MOE_OK, dist, dev):
         raise RuntimeError("device error during warm-up")
 
     # ---- timed region: K steps, no event between kernels
@@ -411,7 +417,7 @@ def run_ours(args, cfg):
     clocks.mark(busy_from, datetime.datetime.now())
     clk = clocks.stop() if rank == 0 else None
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
-    if moe.get_device_error(ws) != moe.MOE_OK:
+    if error_on_any_rank(moe.get_device_error(ws) != moe.MOE_OK, dist, dev):
         raise RuntimeError("device error in the timed steps")
     ms_per_step = total_ms / K
     value = cfg.T * world / (ms_per_step / 1e3)
@@ -583,7 +589,7 @@ def run_ours(args, cfg):
             fb.record(stream)
             torch.cuda.synchronize(dev)
             fwd_z_ms = max_over_ranks(fa.elapsed_time(fb), dist, dev) / K
-            if moe.get_device_error(fws) != moe.MOE_OK:
+            if error_on_any_rank(moe.get_device_error(fws) != moe.MOE_OK, dist, dev):
                 raise RuntimeError("device error in the forward steps keeping Z")
 
         def bwd_step():
@@ -602,9 +608,8 @@ def run_ours(args, cfg):
             bwd_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        # every rank joins the collective before any of them can raise
         b_ms = max_over_ranks(a.elapsed_time(b), dist, dev) / K
-        if moe.get_device_error(bws) != moe.MOE_OK:
+        if error_on_any_rank(moe.get_device_error(bws) != moe.MOE_OK, dist, dev):
             raise RuntimeError("device error in the backward steps")
         R = cfg.T * cfg.k
         sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -45,6 +45,34 @@ def test_max_over_ranks_two_gloo_ranks(tmp_path):
         assert json.loads((tmp_path / f"rank{r}.json").read_text()) == 3.5
 
 
+def _error_rank_main(rank, world, port, bad, outdir):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.error_on_any_rank(bad[rank], dist, torch.device("cpu"))
+        with open(os.path.join(outdir, f"err{rank}.json"), "w") as fh:
+            json.dump(got, fh)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("bad", [(False, True), (False, False)])
+def test_device_error_seen_by_every_rank(tmp_path, bad):
+    # one rank's error makes every rank raise, so none waits in a later
+    # collective for a rank that has left
+    mp.spawn(_error_rank_main, args=(2, _free_port(), list(bad), str(tmp_path)), nprocs=2,
+             join=True)
+    for r in range(2):
+        assert json.loads((tmp_path / f"err{r}.json").read_text()) is any(bad)
+
+
+def test_device_error_one_process():
+    assert bench.error_on_any_rank(True, None, None) is True
+    assert bench.error_on_any_rank(False, None, None) is False
+
+
 def test_max_over_ranks_one_process():
     assert bench.max_over_ranks(2.75, None, None) == 2.75
 
