@@ -106,6 +106,25 @@ def test_payload_quantisation_uses_fp32_division():
     assert np.array_equal(q, ref)
 
 
+def test_payload_quotient_is_rounded_to_fp32_before_e4m3():
+    """Rows whose second value lands, after the fp32 division, exactly on an
+    E4M3 rounding midpoint, while the exact quotient lies just above it:
+    s = fp32(1.875 / 448), 1.40625 / s = 336.0000107 exactly, fp32 336 (the
+    midpoint of 320 and 352), which ties to the even code 320, where the
+    exact quotient would round up to 352; likewise 168 between 160 and 176.
+    (Rows found by searching bf16 pairs; the torch column repeats the fp32
+    division and torch's own E4M3 cast.)"""
+    x = np.array([[1.875, 1.40625], [4.3125, 1.6171875], [4.75, 1.78125]])
+    q, s = quantize_payload_fp8(x)
+    assert q.tolist() == [[448.0, 320.0], [448.0, 160.0], [448.0, 160.0]]
+    exact = x[:, 1] / s                       # fp64: not on the midpoint
+    assert np.all(exact > [336.0, 168.0, 168.0])
+    xt = torch.from_numpy(x.astype(np.float32))
+    st = torch.from_numpy(s.astype(np.float32))
+    ref = (xt / st[:, None]).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(q, ref)
+
+
 # ---- static global scale (the sync-tax article's "static global" FP8
 # variant: one scale fixed ahead of time for the whole tensor)
 def test_static_scale_equal_to_absmax_scale_reproduces_dynamic():
