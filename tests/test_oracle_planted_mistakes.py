@@ -10,8 +10,11 @@ maximum or by mean logit, the temperature or the noise of soft gating
 ignored, an unstable packing, a source index that forgets k, a combine
 without its weights or with its slots crossed, E4M3 ties away from zero, no
 subnormal range or no saturation, an fp64 payload scale or quotient, an
-output payload mapped onto [0, 448], and backward passes that forget a term.
-(The FFN's own planted mistakes sit beside its permutation pin.)"""
+output payload mapped onto [0, 448] or decoded without its zero point, 240
+for the E4M3 maximum, H not rounded to its storage type, ReLU for SiLU,
+bf16 rounding to seven bits or by truncation, and backward passes that
+forget a term. (The FFN's planted mistakes against its permutation pin sit
+beside that pin.)"""
 import numpy as np
 import pytest
 
@@ -33,8 +36,10 @@ HOLDERS = [oracle, mo, nu, backward_pins, dispatch_pins, ffn_pins, numerics_pins
 REAL = {n: getattr(mo, n) for n in (
     "gate_logits", "route", "_softmax_max_subtracted", "_route_group_limited",
     "_route_soft_gumbel", "dispatch", "combine", "quantize_payload_fp8",
-    "quantize_output_fp8", "router_backward", "silu_grad", "_combine_backward", "backward")}
+    "quantize_output_fp8", "dequantize_output_fp8", "router_backward", "silu_grad",
+    "_combine_backward", "backward", "expert_ffn_rows", "silu")}
 REAL["e4m3_round_satfinite"] = nu.e4m3_round_satfinite
+REAL["round_to_bf16"] = nu.round_to_bf16
 
 
 def plant(monkeypatch, name, bad):
@@ -191,7 +196,49 @@ def test_combine_slots_crossed(monkeypatch):
     must_fail(ffn_pins.test_combine_matches_loops)
 
 
+# ---------------------------------------------------------------- FFN, storage roundings
+def test_hidden_activation_not_rounded_to_its_storage(monkeypatch):
+    plant(monkeypatch, "expert_ffn_rows",
+          lambda x, W1e, W2e, h_storage="bf16": REAL["expert_ffn_rows"](x, W1e, W2e, "exact"))
+    must_fail(ffn_pins.test_one_expert_bf16_storage_of_h)
+
+
+def test_relu_for_silu(monkeypatch):
+    plant(monkeypatch, "silu", lambda z: np.maximum(z, 0.0))
+    must_fail(ffn_pins.test_one_expert_is_a_dense_ffn)
+
+
+def test_bf16_rounding_keeps_seven_bits(monkeypatch):
+    def bad(v):
+        v = np.asarray(v, dtype=np.float64)
+        m, ex = np.frexp(v)
+        return np.where(v == 0.0, v, np.ldexp(np.rint(np.ldexp(m, 7)), ex - 7))
+    plant(monkeypatch, "round_to_bf16", bad)
+    must_fail(numerics_pins.test_bf16_rounding_matches_torch)
+
+
+def test_bf16_rounding_truncates(monkeypatch):
+    def bad(v):
+        v = np.asarray(v, dtype=np.float64)
+        m, ex = np.frexp(v)
+        return np.where(v == 0.0, v, np.ldexp(np.trunc(np.ldexp(m, 8)), ex - 8))
+    plant(monkeypatch, "round_to_bf16", bad)
+    must_fail(numerics_pins.test_bf16_rounding_matches_torch)
+
+
 # ---------------------------------------------------------------- E4M3, FP8 payloads
+def test_payload_e4m3_maximum_taken_as_240(monkeypatch):
+    monkeypatch.setattr(mo, "E4M3_MAX_F32", np.float32(240.0))
+    must_fail(numerics_pins.test_payload_scale_and_saturation)
+
+
+def test_output_payload_decoded_without_its_zero(monkeypatch):
+    plant(monkeypatch, "dequantize_output_fp8",
+          lambda q, s, zero: REAL["dequantize_output_fp8"](q, s, np.zeros_like(zero)))
+    must_fail(outpay_pins.test_worked_row)
+    must_fail(outpay_pins.test_constant_rows_decode_exactly)
+
+
 def _e4m3_variant(rnd=np.rint, subnormals=True, saturate=True):
     def bad(v):
         v = np.asarray(v, dtype=np.float64)
