@@ -52,6 +52,74 @@ def test_only_abi_symbols_are_exported(lib):
     assert not stray, stray
 
 
+def header_source():
+    """The headers' text with the comments taken out."""
+    text = "".join(open(os.path.join(ROOT, "include", fn)).read()
+                   for fn in sorted(os.listdir(os.path.join(ROOT, "include"))) if fn.endswith(".h"))
+    return re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+
+
+def struct_fields(tag):
+    body = re.search(r"typedef struct %s \{(.*?)\}" % tag, header_source(), re.S).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = " ".join(decl.split())
+        if decl:
+            ctype, ptr, name = re.fullmatch(r"([\w ]+?)\s*(\**)\s*(\w+)", decl).groups()
+            fields.append((name, ctype + ptr))
+    return fields
+
+
+def test_config_struct_matches_the_header():
+    # the ctypes mirror must have the header's fields, in its order and types
+    # (a drift would shift every later field of every call)
+    fields = struct_fields("moe_config")
+    assert [n for n, _ in fields] == [n for n, _ in L.MoeConfig._fields_]
+    ctypes_of = {"int32_t": ctypes.c_int32, "float": ctypes.c_float}
+    for (name, ctype), (_, mirror) in zip(fields, L.MoeConfig._fields_):
+        assert ctypes_of[ctype] is mirror, name
+    assert ctypes.sizeof(L.MoeConfig) == 4 * len(fields)
+
+
+def test_views_struct_matches_the_header():
+    fields = struct_fields("moe_forward_views")
+    assert [n for n, _ in fields] == [n for n, _ in L.MoeForwardViews._fields_]
+    assert all(ctype.endswith("*") for _, ctype in fields)
+    assert all(t is ctypes.c_void_p for _, t in L.MoeForwardViews._fields_)
+
+
+def _param_ctype(param):
+    if "moe_config_t*" in param:
+        return ctypes.POINTER(L.MoeConfig)
+    if "moe_forward_views_t*" in param:
+        return ctypes.POINTER(L.MoeForwardViews)
+    if param.startswith("void* const*"):
+        return ctypes.POINTER(ctypes.c_void_p)
+    if "*" in param:
+        return ctypes.c_void_p
+    kind = param.split()[0]
+    return {"size_t": ctypes.c_size_t, "int": ctypes.c_int, "int32_t": ctypes.c_int,
+            "uint64_t": ctypes.c_uint64}[kind]
+
+
+def test_every_prototype_matches_the_header():
+    # each function's return type, parameter count and parameter kinds
+    # (pointer, size_t, int, uint64_t) against its ctypes prototype
+    rets = {"int": ctypes.c_int, "size_t": ctypes.c_size_t, "const char*": ctypes.c_char_p}
+    seen = set()
+    for m in re.finditer(r"MOE_API\s+([\w\s\*]+?)\b(moe_\w+)\s*\((.*?)\)\s*;",
+                         header_source(), re.S):
+        ret, name, params = " ".join(m.group(1).split()), m.group(2), " ".join(m.group(3).split())
+        res, args = L.PROTOTYPES[name]
+        assert rets[ret] is res, name
+        plist = [] if params in ("", "void") else [q.strip() for q in params.split(",")]
+        assert len(plist) == len(args), name
+        for q, a in zip(plist, args):
+            assert _param_ctype(q) is a, (name, q)
+        seen.add(name)
+    assert seen == set(L.PROTOTYPES)
+
+
 def cfg(**kw):
     base = dict(T=64, d=128, E=8, k=2, f=256, dtype=1, router=0, pre_k=8, payload_fp8=0,
                 n_group=0, topk_group=0, payload_scale=0.0, output_fp8=0, tau=0.0,
