@@ -11,10 +11,10 @@ ignored, an unstable packing, a source index that forgets k, a combine
 without its weights or with its slots crossed, E4M3 ties away from zero, no
 subnormal range or no saturation, an fp64 payload scale or quotient, an
 output payload mapped onto [0, 448] or decoded without its zero point, 240
-for the E4M3 maximum, H not rounded to its storage type, ReLU for SiLU,
-bf16 rounding to seven bits or by truncation, and backward passes that
-forget a term. (The FFN's planted mistakes against its permutation pin sit
-beside that pin.)"""
+for the E4M3 maximum, experts fed the rows before quantisation, H not
+rounded to its storage type, ReLU for SiLU, bf16 rounding to seven bits or
+by truncation, and backward passes that forget a term. (The FFN's planted
+mistakes against its permutation pin sit beside that pin.)"""
 import numpy as np
 import pytest
 
@@ -37,7 +37,7 @@ REAL = {n: getattr(mo, n) for n in (
     "gate_logits", "route", "_softmax_max_subtracted", "_route_group_limited",
     "_route_soft_gumbel", "dispatch", "combine", "quantize_payload_fp8",
     "quantize_output_fp8", "dequantize_output_fp8", "router_backward", "silu_grad",
-    "_combine_backward", "backward", "expert_ffn_rows", "silu")}
+    "_combine_backward", "backward", "expert_ffn_rows", "silu", "_payload")}
 REAL["e4m3_round_satfinite"] = nu.e4m3_round_satfinite
 REAL["round_to_bf16"] = nu.round_to_bf16
 
@@ -227,6 +227,14 @@ def test_bf16_rounding_truncates(monkeypatch):
 
 
 # ---------------------------------------------------------------- E4M3, FP8 payloads
+def test_experts_see_the_rows_before_quantisation(monkeypatch):
+    def bad(cfg, x):
+        x_hat, q, s = REAL["_payload"](cfg, x)
+        return x, q, s                             # the payload computed, then not used
+    plant(monkeypatch, "_payload", bad)
+    must_fail(ffn_pins.test_fp8_payload_forward)
+
+
 def test_payload_e4m3_maximum_taken_as_240(monkeypatch):
     monkeypatch.setattr(mo, "E4M3_MAX_F32", np.float32(240.0))
     must_fail(numerics_pins.test_payload_scale_and_saturation)
