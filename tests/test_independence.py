@@ -4,7 +4,8 @@ oracle never imports the product; the seeded input generator in
 `workloads`, the one module both sides use, imports neither; outside
 `tests/`, only the CPU-baseline and reference-arm functions of bench.py and
 `smoke()` import the oracle, inside their own bodies; no CUDA or C source
-includes anything from `oracle/`."""
+includes anything from `oracle/`. And the library reads no environment
+variable, so what runs follows the config alone."""
 import ast
 import os
 import re
@@ -72,3 +73,16 @@ def test_no_native_source_includes_the_oracle():
                 text = open(os.path.join(ROOT, sub, fn)).read()
                 for inc in re.findall(r'#include\s*[<"]([^>"]+)[>"]', text):
                     assert "oracle" not in inc, (fn, inc)
+
+
+def test_library_reads_no_environment_variable():
+    # the kernel shapes the product runs follow the config alone: no source
+    # of the library or its binding reads the environment (the build script
+    # may look for nvcc there)
+    for sub in (os.path.join(PKG, "csrc"), "include"):
+        for fn in os.listdir(os.path.join(ROOT, sub)):
+            text = open(os.path.join(ROOT, sub, fn)).read()
+            assert "getenv" not in text and "environ" not in text, fn
+    for path in _py_files(PKG):
+        if os.path.basename(path) != "build.py":
+            assert "environ" not in open(path).read(), path
