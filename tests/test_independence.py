@@ -5,7 +5,8 @@ oracle never imports the product; the seeded input generator in
 `tests/`, only the CPU-baseline and reference-arm functions of bench.py and
 `smoke()` import the oracle, inside their own bodies; no CUDA or C source
 includes anything from `oracle/`. And the library reads no environment
-variable, so what runs follows the config alone."""
+variable, so what runs follows the config alone; `profiles/` holds short
+text summaries whose ncu commands leave the clocks alone."""
 import ast
 import os
 import re
@@ -86,3 +87,16 @@ def test_library_reads_no_environment_variable():
     for path in _py_files(PKG):
         if os.path.basename(path) != "build.py":
             assert "environ" not in open(path).read(), path
+
+
+def test_profiles_are_short_text_summaries():
+    # ncu summaries only: text, a few KB each, every capture command with
+    # --clock-control none and running committed files (bench.py)
+    for fn in os.listdir(os.path.join(ROOT, "profiles")):
+        path = os.path.join(ROOT, "profiles", fn)
+        assert fn.endswith((".md", ".txt", ".json")), fn
+        assert os.path.getsize(path) < 16 * 1024, fn
+        if fn.endswith(".md") and fn != "INDEX.md":
+            text = open(path).read()
+            assert "ncu " in text and "--clock-control none" in text, fn
+            assert "bench.py" in text, fn
