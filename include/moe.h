@@ -168,6 +168,9 @@ MOE_API size_t moe_scratch_size(const moe_config_t* cfg);
 MOE_API size_t moe_workspace_size(const moe_config_t* cfg);
 
 /* ---- stage 1: gate + router ---------------------------------------------
+ * The gate's per-expert logit (DeepSeek-V4 EP article, section 2.1) and the
+ * router's max-subtracted softmax, partial top-8 and exact top-k (section
+ * 3.2); the variants as cited at moe_config.router.
  * x [T, d] (dtype), W_g [d, E] (dtype), bias [E] fp32 or NULL (= zeros),
  * noise [T, E] fp32: the Gumbel samples of MOE_ROUTER_SOFT_GUMBEL (required
  * there, ignored by the other routers, may be NULL).
@@ -182,6 +185,9 @@ MOE_API int moe_route(const moe_config_t* cfg, const void* x, const void* W_g,
               float* logits, void* stream);
 
 /* ---- stage 2: dispatch ---------------------------------------------------
+ * Packing by expert id (DeepSeek-V4 EP article, section 3.3; Deepseek-MoE
+ * sync-tax article, section 2.1), with the optional FP8 payload (sync-tax
+ * article, section 3.1).
  * Inputs: x [T, d] (dtype), topk_idx [T, k] int32.
  * (MOE_ROUTER_SOFT_GUMBEL: only counts, offsets, pos and src are written,
  * for the routing every token -> every expert in token order; x, topk_idx,
@@ -232,6 +238,8 @@ MOE_API int moe_dispatch_noalloc(const moe_config_t* cfg, const void* x,
                          void* stream);
 
 /* ---- stage 3: grouped expert FFN -----------------------------------------
+ * "L1 + Act + L2" per expert (DeepSeek V3/V4 parallel-strategy article,
+ * Waved-EP section), read as one up projection, SiLU and one down projection:
  * For every expert e with rows [offsets[e], offsets[e+1]) of x_perm:
  *   h[r] = SiLU(s_r * x_perm[r] . W1[e])   (s_r = x_scale[r] with FP8, else 1)
  *   y_perm[r] = h[r] . W2[e]
@@ -252,6 +260,8 @@ MOE_API int moe_expert_ffn(const moe_config_t* cfg, const void* x_perm,
                    size_t ws_bytes, void* stream);
 
 /* ---- stage 4: combine ------------------------------------------------------
+ * The weighted sum of a token's k expert outputs (Deepseek-MoE sync-tax
+ * article, section 2.3):
  * out[t] = sum_{j=0..k-1} topk_w[t, j] * y_perm[pos[t*k + j]], accumulated in
  * fp32 in increasing j, then stored in dtype. No atomics: the result is
  * bitwise reproducible. y_perm [R, d] fp32, pos [R] int32, topk_w [T, k]
@@ -284,6 +294,8 @@ MOE_API int moe_combine_fp8(const moe_config_t* cfg, const uint8_t* y_q, const f
                     void* out, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- whole layer -----------------------------------------------------------
+ * Dispatch, L1 + Act + L2 and combine in sequence (DeepSeek V3/V4
+ * parallel-strategy article, EP and Waved-EP sections), on one GPU:
  * moe_route -> moe_dispatch -> moe_expert_ffn -> moe_combine (or, with
  * output_fp8, moe_quantize_output -> moe_combine_fp8) on one stream, with
  * every intermediate in the workspace (>= moe_workspace_size bytes).
@@ -293,7 +305,8 @@ MOE_API int moe_forward(const moe_config_t* cfg, const void* x, const void* W_g,
                 const float* bias, const float* noise, const void* W1, const void* W2,
                 void* out, void* ws, size_t ws_bytes, void* stream);
 
-/* moe_forward that also records CUDA events (cudaEvent_t, passed as void*)
+/* (No counterpart on the source pages: timing instrumentation.)
+ * moe_forward that also records CUDA events (cudaEvent_t, passed as void*)
  * at the kernel boundaries, for per-kernel timing on the launching stream:
  *   events[0] before the route kernel      events[1] after route
  *   events[2] after dispatch (3 kernels; 1 with soft gating)
@@ -310,7 +323,8 @@ MOE_API int moe_forward_with_events(const moe_config_t* cfg, const void* x,
                             size_t ws_bytes, void* const* events, int n_events,
                             void* stream);
 
-/* Pointers into a forward workspace, so a caller can inspect the
+/* (No counterpart on the source pages: inspection of intermediates.)
+ * Pointers into a forward workspace, so a caller can inspect the
  * intermediates of the last moe_forward (routing, permutation, H, Y).
  * Any output pointer may be NULL. x_perm is NULL when that forward packs no
  * rows (gathered rows, soft gating). Returns MOE_ERR_INVALID_ARG for a bad
