@@ -351,3 +351,18 @@ def test_dx_without_the_gate_path(monkeypatch):
         return r
     plant(monkeypatch, "backward", bad)
     must_fail(backward_pins.test_finite_differences_renorm, 0)
+
+
+def test_soft_gating_gradient_without_the_temperature(monkeypatch):
+    def bad(L, idx, w, dw, router=0, pre_k=8, tau=1.0):
+        return REAL["router_backward"](L, idx, w, dw, router, pre_k, 1.0)
+    plant(monkeypatch, "router_backward", bad)
+    must_fail(backward_pins.test_finite_differences_soft_gating)
+
+
+def test_routing_weight_gradient_with_slots_crossed(monkeypatch):
+    def bad(pos, w, Y, g):
+        dY, dw = REAL["_combine_backward"](pos, w, Y, g)
+        return dY, dw[:, ::-1]
+    plant(monkeypatch, "_combine_backward", bad)
+    must_fail(backward_pins.test_finite_differences_renorm, 0)
