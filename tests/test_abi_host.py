@@ -424,3 +424,18 @@ def test_binding_refuses_strided_and_host_tensors():
         moe.route(c, torch.zeros((c.d, c.T)).t(), Wg)
     with pytest.raises(moe.MoEError, match="not in GPU memory"):
         moe.route(c, torch.zeros((c.T, c.d)), Wg)
+
+
+@pytest.mark.parametrize("compiler,std", [("gcc", "-std=c11"), ("g++", "-std=c++17")])
+def test_header_compiles_as_plain_c_and_cpp(tmp_path, compiler, std):
+    # a C ABI: the header alone, warnings as errors, in C and in C++
+    if subprocess.run(["which", compiler], capture_output=True).returncode != 0:
+        pytest.skip(f"{compiler} not installed")
+    src = tmp_path / "use_moe.c"
+    src.write_text('#include "moe.h"\n'
+                   "int use(const moe_config_t* c) { return moe_check_config(c); }\n")
+    lang = ["-x", "c++"] if compiler == "g++" else []
+    r = subprocess.run([compiler, std, "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-fsyntax-only", *lang, "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
